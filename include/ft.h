@@ -1,0 +1,254 @@
+/*
+ * ft.h -- C ABI of libft, a single-GPU (sm_103a) implementation of the
+ * FreeToken MoE layer's data-parallel hot path: the per-layer routing-control
+ * pass over an all-layer, slot-indexed GPU expert cache, the cache fills, the
+ * expert SwiGLU computation over resident slots merged with a supplied
+ * CPU-set partial sum, the full-layer double-buffered prefill, and cache
+ * resize.
+ *
+ * Conventions (all entry points):
+ *   - Every call returns an ft_status; nothing throws across the ABI.
+ *   - Pointers are plain host or device addresses as stated per argument;
+ *     sizes are element counts unless stated.  No ownership is transferred
+ *     unless stated: the library owns the slot pool, residency maps, LRU
+ *     stamps, worklists and scratch; the caller owns the host expert pool and
+ *     every input/output buffer.
+ *   - Calls marked "async" enqueue work on the context's compute stream (and,
+ *     for prefill, its transfer stream) and return without a host
+ *     synchronisation.  Calls marked "syncs" block until the context's
+ *     streams are idle.
+ *   - Problems detected on the device (an out-of-range or duplicated expert id,
+ *     a non-finite logit, a bounded wait that ran out) latch a sticky error
+ *     word; ft_get_status() returns and clears it.
+ *   - A context must be used from one host thread at a time.
+ */
+#ifndef FT_H
+#define FT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ft_status;
+#define FT_OK             0
+#define FT_ERR_ARG       -1   /* invalid argument (checked on the host)              */
+#define FT_ERR_CUDA      -2   /* a CUDA runtime / driver call failed                  */
+#define FT_ERR_OOM       -3   /* device or pinned memory could not be allocated       */
+#define FT_ERR_CAPACITY  -4   /* the cache is too small for the request (prefill <2E) */
+#define FT_ERR_TIMEOUT   -5   /* a bounded device wait gave up                        */
+#define FT_ERR_STATE     -6   /* call not allowed in the current state                */
+#define FT_ERR_DEVICE    -7   /* invalid input detected on the device (ids, logits)   */
+
+#define FT_FMT_BF16   0       /* bf16 banks                                           */
+#define FT_FMT_NVFP4  1       /* e2m1 values + e4m3 block-16 scales + fp32 global     */
+
+typedef struct ft_ctx ft_ctx; /* opaque; created by ft_layer_init, freed by ft_destroy */
+
+/* Result summary of the last control pass (ft_get_last_ctl). */
+typedef struct {
+    int32_t layer;     /* MoE layer of the pass                                      */
+    int32_t T;         /* tokens                                                     */
+    int32_t u;         /* unique experts routed (|U|)                                */
+    int32_t h;         /* hits                                                       */
+    int32_t m;         /* misses                                                     */
+    int32_t q0;        /* round(m*B_P/B_H), halves away from zero                    */
+    int32_t q1;        /* q0 clamped to [1, m] (0 when m = 0)                        */
+    int32_t q;         /* fills after the capacity clamp min(q1, S-h)                */
+    int32_t nC;        /* experts left to the CPU set C (m - q)                      */
+    int32_t u_gpu;     /* experts computed on the GPU (h + q)                        */
+    int32_t n_assign;  /* routed (token, expert) pairs computed on the GPU           */
+    uint32_t clock;    /* LRU clock value of the pass                                */
+} ft_ctl_info;
+
+/* Cumulative counters since init (ft_get_counters). */
+typedef struct {
+    uint64_t calls, unique, hits, misses, fills, cpu;
+} ft_counters;
+
+/* ABI version of this header; ft_abi_version() returns the library's. */
+#define FT_ABI_VERSION 1
+int32_t ft_abi_version(void);
+const char* ft_status_str(ft_status s);
+
+/*
+ * ft_layer_init -- create a context: the slot cache and control state for L
+ * MoE layers of E experts each (top-k routing, hidden size H, expert ffn size
+ * F), with S slots.  FreeToken deepmox chapter "The Expert Cache That Follows
+ * the Router", section "One logical expert, two physical levels of memory":
+ * the host pool is the source of truth and holds one complete record per flat
+ * id layer*E+expert; a GPU slot holds one complete record; one cache is shared
+ * by all layers.
+ *
+ *   L, E, k, H, F  sizes; need E <= 1024, k <= 16, k <= E, H % 256 == 0,
+ *                  F % 32 == 0.
+ *   S              number of slots (>= 1).  Prefill needs S >= 2E.
+ *   fmt            FT_FMT_BF16 or FT_FMT_NVFP4 (record layout in ft_record_bytes).
+ *   T_max          largest T of a decode call (ft_route_ctl), 1..256, and
+ *                  T_max*k <= 4096.
+ *   T_prefill_max  largest T of a prefill layer call; 0 disables prefill (no
+ *                  prefill scratch is allocated).
+ *   host_pool      HOST address of the caller's expert pool: L*E records of
+ *                  ft_record_bytes(H,F,fmt) bytes, record l*E+e at offset
+ *                  (l*E+e)*record_bytes.  Must be page-locked (cudaHostAlloc /
+ *                  cudaHostRegister) or otherwise device-accessible, and stay
+ *                  valid and unchanged until ft_destroy.  Not copied.
+ *   nvfp4_global   HOST array of L*E fp32 per-record global scales (NVFP4), or
+ *                  NULL for BF16.  Copied to device memory at init (the pages:
+ *                  small per-expert values stay GPU-resident).
+ *   compute_stream, transfer_stream
+ *                  cudaStream_t handles owned by the caller (NULL = legacy
+ *                  default stream for compute; transfer must then differ only
+ *                  if prefill is used).  They must outlive the context.
+ *   out            receives the context.
+ * Errors: FT_ERR_ARG (sizes, NULL pool), FT_ERR_OOM, FT_ERR_CUDA.  Syncs.
+ */
+ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H, int32_t F,
+                        int32_t S, int32_t fmt, int32_t T_max, int32_t T_prefill_max,
+                        const void* host_pool, const float* nvfp4_global,
+                        void* compute_stream, void* transfer_stream);
+
+/* Bytes of one complete layer-expert record.
+ * BF16 : [W_gu 2F x H bf16, row-major, gate/up rows interleaved in groups of 16
+ *         (16 gate rows, the 16 matching up rows, ...)] [W_d H x F bf16 row-major].
+ * NVFP4: [W_gu values 2F x H e2m1, 2 per byte, low nibble first, same row order]
+ *        [W_d values H x F] [W_gu e4m3 scales 2F x H/16] [W_d scales H x F/16]. */
+size_t ft_record_bytes(int32_t H, int32_t F, int32_t fmt);
+
+/*
+ * ft_route_ctl -- the per-layer control pass and the cache fills, async.
+ * FreeToken explainer sections 4-10 and deepmox section "How residency
+ * follows demand without leaving the device": dedup the routed experts, look
+ * each flat id up in slot_for_id (resident = hit), q = clamp(round(m*B_P/B_H),
+ * 1, m) for m >= 1 (explainer section 5; txtmix: at least one fill), the fill
+ * set F = the first q misses by routed-token count (descending, lower id
+ * first), the rest is the CPU set C; victims = the q least recently used slots
+ * not holding a hit of this call (smallest (stamp, slot)); hits and fills get
+ * the pass's clock as stamp; route ids are rewritten to slot ids; then the q
+ * complete records are copied from the host pool into their victim slots.
+ * All of it runs on the device: no host synchronisation.
+ *
+ *   layer     0..L-1.
+ *   T         tokens, 1..T_max.
+ *   logits    DEVICE fp32 [T, E] router logits, or NULL when top-k is given.
+ *             Top-k is taken by value (descending), lower id first on ties;
+ *             gates are the softmax over the k selected logits (fp32).
+ *   topk_ids  DEVICE int32 [T, k] expert ids (distinct within a token), or NULL.
+ *   topk_w    DEVICE fp32 [T, k] gate weights matching topk_ids, or NULL.
+ *             Exactly one of logits / (topk_ids and topk_w) must be given.
+ *   B_P, B_H  host-to-device expert-transfer and host-side expert bandwidths
+ *             (any common unit, B_P > 0, B_H > 0).  q uses (m*B_P)/B_H in fp64.
+ * Errors: FT_ERR_ARG (host checks), FT_ERR_STATE (a prefill chunk is open).
+ * Invalid ids or non-finite logits latch FT_ERR_DEVICE; the pass then routes
+ * nothing to the GPU and changes no residency.
+ */
+ft_status ft_route_ctl(ft_ctx* ctx, int32_t layer, int32_t T, const float* logits,
+                       const int32_t* topk_ids, const float* topk_w, double B_P, double B_H);
+
+/*
+ * ft_moe_forward -- expert computation for the layer of the last
+ * ft_route_ctl, async.  For every routed pair (t, j) whose expert is a hit or
+ * a fill: FFN(x_t) = W_d (SiLU(W_g x_t) * (W_u x_t)) over the slot's record;
+ * y_t = sum_j g_tj FFN_{e_tj}(x_t) (j ascending) + partial_C_t.  The METAL
+ * MEDIA page, Figure 2 caption, and explainer section 14: GPU and CPU partial
+ * outputs merge exactly.
+ *
+ *   x          DEVICE bf16 [T, H] (T of the last ft_route_ctl).
+ *   partial_C  DEVICE fp32 [T, H] partial sum of the CPU set C, or NULL (zeros).
+ *   y          DEVICE fp32 [T, H] output; must not alias x or partial_C.
+ * Errors: FT_ERR_STATE if no control pass preceded it.
+ */
+ft_status ft_moe_forward(ft_ctx* ctx, const void* x, const float* partial_C, float* y);
+
+/*
+ * ft_prefill_begin -- open a prefill chunk, async.  FreeToken explainer
+ * section 2 and deepmox section "How residency follows demand...": prefill
+ * streams whole layers through two full-layer buffers carved from the first
+ * two expert-layer regions of the slot pool (buffer b = slots [b*E, (b+1)*E)).
+ * A begin fence orders the transfer after earlier decode work; the owners of
+ * buffer (layer & 1) are invalidated (slot_for_id cleared, stamp 0) and the
+ * E records of `layer` are copied host-to-device on the transfer stream.
+ *   layer  first layer of the chunk.
+ * Errors: FT_ERR_CAPACITY (S < 2E), FT_ERR_STATE (chunk already open or
+ * prefill disabled).
+ */
+ft_status ft_prefill_begin(ft_ctx* ctx, int32_t layer);
+
+/*
+ * ft_prefill_layer -- one prefill layer, async.  Waits for buffer `buffer` to
+ * hold `layer`; if next_layer >= 0, invalidates the other buffer and streams
+ * next_layer into it on the transfer stream once the previous layer's GEMMs
+ * released it (release event); routes T tokens (top-k of logits, softmax
+ * gates), runs the grouped SwiGLU FFN over the buffer with tensor cores and
+ * writes y_t = sum_j g_tj FFN_{e_tj}(x_t) (j ascending).  next_layer = -1
+ * closes the chunk; the buffer slots are left empty afterwards.
+ *
+ *   buffer      0 or 1; must equal the buffer the layer was streamed into
+ *               (layer & 1 counted from the chunk's first layer parity).
+ *   layer       layer held by `buffer`.
+ *   next_layer  layer to stream next, or -1.
+ *   T           tokens, 1..T_prefill_max.
+ *   x           DEVICE bf16 [T, H];  logits DEVICE fp32 [T, E];
+ *   y           DEVICE fp32 [T, H].
+ * Errors: FT_ERR_STATE (no open chunk / wrong buffer), FT_ERR_ARG.
+ */
+ft_status ft_prefill_layer(ft_ctx* ctx, int32_t buffer, int32_t layer, int32_t next_layer,
+                           int32_t T, const void* x, const float* logits, float* y);
+
+/*
+ * ft_cache_resize -- rebuild the slot cache with S_new slots, syncs.
+ * FreeToken explainer section 11 and txtmix section on "ft ctl cache": the
+ * cache is rebuilt for a new VRAM budget at a safe point without restarting;
+ * the host pool keeps results correct.  Shrinking evicts in LRU order
+ * (smallest (stamp, slot) first) until min(S_new, occupied) entries remain and
+ * packs the survivors, in ascending old slot order, into slots 0..n-1;
+ * growing keeps every slot and adds empty ones.  Stamps and clock are kept.
+ * On any failure the old cache is left unchanged.
+ * Errors: FT_ERR_ARG (S_new < 1), FT_ERR_STATE (prefill chunk open), FT_ERR_OOM.
+ */
+ft_status ft_cache_resize(ft_ctx* ctx, int32_t S_new);
+
+/* ---- observability and test surface (all sync) ------------------------- */
+
+/* Copy the control state to HOST buffers: slot_for_id [L*E], id_for_slot [S],
+ * stamps [S], clock [1].  Any pointer may be NULL to skip it. */
+ft_status ft_get_ctl_state(ft_ctx* ctx, int32_t* slot_for_id, int32_t* id_for_slot,
+                           uint32_t* stamps, uint32_t* clock);
+
+/* Replace the control state from HOST buffers (same shapes).  Checked: maps
+ * form a bijection on occupied slots, ids and slots in range, stamps <= clock.
+ * Slot CONTENTS are not touched: use only with a state whose occupied slots
+ * already hold the named records, or right after init with an all-empty map. */
+ft_status ft_set_ctl_state(ft_ctx* ctx, const int32_t* slot_for_id, const int32_t* id_for_slot,
+                           const uint32_t* stamps, uint32_t clock);
+
+/* Details of the last control pass, into HOST buffers (any may be NULL):
+ * F [q] fill experts (fill order), C [nC] CPU-set experts (same order),
+ * victims [q] slots (ascending (stamp, slot); victims[i] received F[i]),
+ * topk_ids [T*k], gates [T*k] (routing used), slots_topk [T*k] (slot or -1). */
+ft_status ft_get_last_ctl(ft_ctx* ctx, ft_ctl_info* info, int32_t* F, int32_t* C,
+                          int32_t* victims, int32_t* topk_ids, float* gates, int32_t* slots_topk);
+
+/* Copy slot `slot`'s record (ft_record_bytes bytes) to a HOST buffer. */
+ft_status ft_read_slot(ft_ctx* ctx, int32_t slot, void* host_dst);
+
+/* Cumulative counters into a HOST struct. */
+ft_status ft_get_counters(ft_ctx* ctx, ft_counters* out);
+
+/* Current number of slots. */
+int32_t ft_num_slots(const ft_ctx* ctx);
+
+/* Synchronise the context's streams and return (and clear) the sticky device
+ * error word: FT_OK, FT_ERR_DEVICE or FT_ERR_TIMEOUT; FT_ERR_CUDA if a CUDA
+ * error is pending. */
+ft_status ft_get_status(ft_ctx* ctx);
+
+/* Free every library-owned resource.  Syncs.  ctx may be NULL. */
+void ft_destroy(ft_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FT_H */

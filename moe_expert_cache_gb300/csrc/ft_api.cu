@@ -1,0 +1,433 @@
+// libft host side: the C ABI declared in include/ft.h.
+//
+// Owns the context (slot pool, residency maps, LRU stamps, worklists,
+// scratch), validates arguments on the host, and enqueues the kernels on the
+// caller's streams.  The decode path (ft_route_ctl, ft_moe_forward) performs
+// no host synchronisation and no allocation, so a whole decode step can be
+// captured into a CUDA graph by the caller.
+#include "ft_common.cuh"
+#include "ft_prefill.cuh"
+#include "../../include/ft.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+struct ft_ctx {
+    int L, E, k, H, F, S, fmt, T_max, T_prefill_max;
+    size_t rb;
+    int device, num_sms;
+    cudaStream_t cs, ts;
+    const void* host_pool;
+    const uint8_t* host_pool_dev;
+    uint8_t* slot_pool;
+    int* slot_for_id;
+    int* id_for_slot;
+    unsigned* stamps;
+    float* nvfp4_global;
+    // fixed-size control outputs and worklists (one arena)
+    void* arena;
+    unsigned* clock;
+    int *ids, *slots_topk, *pos, *as_tok, *wl_slot, *wl_off, *fill_slot, *fill_fid, *Fl, *Cl, *victims, *info;
+    float *gates, *as_gate;
+    unsigned long long* counters;
+    unsigned* err;
+    float* hbuf;
+    int last_T;
+    bool have_ctl;
+    PrefillState pf;
+};
+
+namespace {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+#define FT_CUDA(call)                                                                          \
+    do {                                                                                       \
+        cudaError_t e_ = (call);                                                               \
+        if (e_ != cudaSuccess) {                                                               \
+            if (getenv("FT_DEBUG")) fprintf(stderr, "libft: %s -> %s\n", #call, cudaGetErrorString(e_)); \
+            return e_ == cudaErrorMemoryAllocation ? FT_ERR_OOM : FT_ERR_CUDA;                 \
+        }                                                                                      \
+    } while (0)
+
+void free_ctx(ft_ctx* c) {
+    if (!c) return;
+    prefill_free(c->pf);
+    cudaFree(c->slot_pool);
+    cudaFree(c->slot_for_id);
+    cudaFree(c->id_for_slot);
+    cudaFree(c->stamps);
+    cudaFree(c->nvfp4_global);
+    cudaFree(c->arena);
+    cudaFree(c->hbuf);
+    delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t ft_abi_version(void) { return FT_ABI_VERSION; }
+
+const char* ft_status_str(ft_status s) {
+    switch (s) {
+        case FT_OK: return "ok";
+        case FT_ERR_ARG: return "invalid argument";
+        case FT_ERR_CUDA: return "CUDA call failed";
+        case FT_ERR_OOM: return "out of memory";
+        case FT_ERR_CAPACITY: return "cache too small for the request";
+        case FT_ERR_TIMEOUT: return "bounded device wait gave up";
+        case FT_ERR_STATE: return "call not allowed in the current state";
+        case FT_ERR_DEVICE: return "invalid input detected on the device";
+        default: return "unknown status";
+    }
+}
+
+size_t ft_record_bytes(int32_t H, int32_t F, int32_t fmt) {
+    const size_t n = (size_t)3 * H * F;
+    if (fmt == FT_FMT_BF16) return 2 * n;
+    if (fmt == FT_FMT_NVFP4) return n / 2 + n / 16;
+    return 0;
+}
+
+ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H, int32_t F, int32_t S,
+                        int32_t fmt, int32_t T_max, int32_t T_prefill_max, const void* host_pool,
+                        const float* nvfp4_global, void* compute_stream, void* transfer_stream) {
+    if (!out) return FT_ERR_ARG;
+    *out = nullptr;
+    if (L < 1 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E || H < 64 || H % 64 || F < 64 || F % 64 || S < 1 ||
+        T_max < 1 || T_max > 256 || T_max * k > 4096 || T_prefill_max < 0 || !host_pool)
+        return FT_ERR_ARG;
+    if (fmt != FT_FMT_BF16) return FT_ERR_ARG;  // NVFP4 banks are accepted by a later version
+    ft_ctx* c = new (std::nothrow) ft_ctx();
+    if (!c) return FT_ERR_OOM;
+    c->L = L; c->E = E; c->k = k; c->H = H; c->F = F; c->S = S; c->fmt = fmt;
+    c->T_max = T_max; c->T_prefill_max = T_prefill_max;
+    c->rb = ft_record_bytes(H, F, fmt);
+    c->cs = (cudaStream_t)compute_stream;
+    c->ts = (cudaStream_t)transfer_stream;
+    c->host_pool = host_pool;
+    ft_status st = FT_OK;
+    auto fail = [&](ft_status s) { free_ctx(c); return s; };
+#define INIT_CUDA(call)                                                                        \
+    do {                                                                                       \
+        cudaError_t e_ = (call);                                                               \
+        if (e_ != cudaSuccess) {                                                               \
+            if (getenv("FT_DEBUG")) fprintf(stderr, "libft: %s -> %s\n", #call, cudaGetErrorString(e_)); \
+            return fail(e_ == cudaErrorMemoryAllocation ? FT_ERR_OOM : FT_ERR_CUDA);           \
+        }                                                                                      \
+    } while (0)
+    INIT_CUDA(cudaGetDevice(&c->device));
+    INIT_CUDA(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
+    // Device address of the host pool: the mapping of page-locked memory, or
+    // the host address itself where the GPU reads pageable memory directly.
+    void* dptr = nullptr;
+    if (cudaHostGetDevicePointer(&dptr, const_cast<void*>(host_pool), 0) != cudaSuccess) {
+        cudaGetLastError();
+        int pageable = 0;
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccessUsesHostPageTables, c->device);
+        if (!pageable) return fail(FT_ERR_ARG);
+        dptr = const_cast<void*>(host_pool);
+    }
+    c->host_pool_dev = (const uint8_t*)dptr;
+    if ((uintptr_t)dptr % 16) return fail(FT_ERR_ARG);
+
+    INIT_CUDA(cudaMalloc(&c->slot_pool, (size_t)S * c->rb));
+    INIT_CUDA(cudaMalloc(&c->slot_for_id, (size_t)L * E * 4));
+    INIT_CUDA(cudaMalloc(&c->id_for_slot, (size_t)S * 4));
+    INIT_CUDA(cudaMalloc(&c->stamps, (size_t)S * 4));
+    INIT_CUDA(cudaMemset(c->slot_for_id, 0xff, (size_t)L * E * 4));
+    INIT_CUDA(cudaMemset(c->id_for_slot, 0xff, (size_t)S * 4));
+    INIT_CUDA(cudaMemset(c->stamps, 0, (size_t)S * 4));
+
+    const size_t TK = (size_t)T_max * k;
+    size_t off = 0;
+    auto carve = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t o_clock = carve(4), o_ids = carve(TK * 4), o_gates = carve(TK * 4), o_slots = carve(TK * 4),
+                 o_pos = carve(TK * 4), o_astok = carve(TK * 4), o_asg = carve(TK * 4),
+                 o_wls = carve((size_t)E * 4), o_wlo = carve((size_t)(E + 1) * 4), o_fs = carve((size_t)E * 4),
+                 o_ff = carve((size_t)E * 4), o_F = carve((size_t)E * 4), o_C = carve((size_t)E * 4),
+                 o_v = carve((size_t)E * 4), o_info = carve(INFO_WORDS * 4), o_cnt = carve(CNT_WORDS * 8),
+                 o_err = carve(4);
+    INIT_CUDA(cudaMalloc(&c->arena, off));
+    INIT_CUDA(cudaMemset(c->arena, 0, off));
+    uint8_t* a = (uint8_t*)c->arena;
+    c->clock = (unsigned*)(a + o_clock);
+    c->ids = (int*)(a + o_ids);
+    c->gates = (float*)(a + o_gates);
+    c->slots_topk = (int*)(a + o_slots);
+    c->pos = (int*)(a + o_pos);
+    c->as_tok = (int*)(a + o_astok);
+    c->as_gate = (float*)(a + o_asg);
+    c->wl_slot = (int*)(a + o_wls);
+    c->wl_off = (int*)(a + o_wlo);
+    c->fill_slot = (int*)(a + o_fs);
+    c->fill_fid = (int*)(a + o_ff);
+    c->Fl = (int*)(a + o_F);
+    c->Cl = (int*)(a + o_C);
+    c->victims = (int*)(a + o_v);
+    c->info = (int*)(a + o_info);
+    c->counters = (unsigned long long*)(a + o_cnt);
+    c->err = (unsigned*)(a + o_err);
+    INIT_CUDA(cudaMalloc(&c->hbuf, TK * F * 4));
+    if (nvfp4_global) {
+        INIT_CUDA(cudaMalloc(&c->nvfp4_global, (size_t)L * E * 4));
+        INIT_CUDA(cudaMemcpy(c->nvfp4_global, nvfp4_global, (size_t)L * E * 4, cudaMemcpyHostToDevice));
+    }
+    if (T_prefill_max > 0) {
+        st = prefill_alloc(c->pf, T_prefill_max, k, H, F, E);
+        if (st != FT_OK) return fail(st);
+    }
+    INIT_CUDA(cudaDeviceSynchronize());
+#undef INIT_CUDA
+    *out = c;
+    return FT_OK;
+}
+
+ft_status ft_route_ctl(ft_ctx* c, int32_t layer, int32_t T, const float* logits, const int32_t* topk_ids,
+                       const float* topk_w, double B_P, double B_H) {
+    if (!c || layer < 0 || layer >= c->L || T < 1 || T > c->T_max) return FT_ERR_ARG;
+    if (!(B_P > 0.0) || !(B_H > 0.0)) return FT_ERR_ARG;
+    if ((logits != nullptr) == (topk_ids != nullptr || topk_w != nullptr)) return FT_ERR_ARG;
+    if (!logits && (!topk_ids || !topk_w)) return FT_ERR_ARG;
+    if (c->pf.open) return FT_ERR_STATE;
+    CtlParams p{};
+    p.layer = layer; p.T = T; p.E = c->E; p.k = c->k; p.L = c->L; p.S = c->S;
+    p.logits = logits; p.topk_ids = topk_ids; p.topk_w = topk_w;
+    p.B_P = B_P; p.B_H = B_H;
+    p.slot_for_id = c->slot_for_id; p.id_for_slot = c->id_for_slot; p.stamps = c->stamps; p.clock = c->clock;
+    p.out_ids = c->ids; p.out_gates = c->gates; p.out_slots = c->slots_topk; p.out_pos = c->pos;
+    p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok; p.as_gate = c->as_gate;
+    p.fill_slot = c->fill_slot; p.fill_fid = c->fill_fid;
+    p.out_F = c->Fl; p.out_C = c->Cl; p.out_victims = c->victims;
+    p.info = c->info; p.counters = c->counters; p.err = c->err;
+    FT_CUDA(launch_route_ctl(p, c->cs));
+    FillParams fp{};
+    fp.host_pool = (const uint4*)c->host_pool_dev;
+    fp.slot_pool = (uint4*)c->slot_pool;
+    fp.rec16 = c->rb / 16;
+    fp.info = c->info; fp.fill_slot = c->fill_slot; fp.fill_fid = c->fill_fid;
+    FT_CUDA(launch_fill(fp, 2 * c->num_sms, c->cs));
+    c->last_T = T;
+    c->have_ctl = true;
+    return FT_OK;
+}
+
+ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float* y) {
+    if (!c || !x || !y) return FT_ERR_ARG;
+    if (!c->have_ctl) return FT_ERR_STATE;
+    if ((const void*)y == x || (const void*)y == (const void*)partial_C) return FT_ERR_ARG;
+    ExpertParams p{};
+    p.slot_pool = c->slot_pool; p.rb = c->rb; p.H = c->H; p.F = c->F; p.T = c->last_T; p.k = c->k;
+    p.x = (const __nv_bfloat16*)x; p.partial_C = partial_C; p.y = y;
+    p.info = c->info; p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok;
+    p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err;
+    FT_CUDA(launch_gateup(p, c->num_sms, c->cs));
+    FT_CUDA(launch_down(p, c->num_sms, c->cs));
+    return FT_OK;
+}
+
+// -------------------------------------------------------------------- resize
+
+ft_status ft_cache_resize(ft_ctx* c, int32_t S_new) {
+    if (!c || S_new < 1) return FT_ERR_ARG;
+    if (c->pf.open) return FT_ERR_STATE;
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    if (c->ts) FT_CUDA(cudaStreamSynchronize(c->ts));
+    const int S = c->S, LE = c->L * c->E;
+    std::vector<int> sfi(LE), ifs(S);
+    std::vector<unsigned> stamp(S);
+    FT_CUDA(cudaMemcpy(sfi.data(), c->slot_for_id, (size_t)LE * 4, cudaMemcpyDeviceToHost));
+    FT_CUDA(cudaMemcpy(ifs.data(), c->id_for_slot, (size_t)S * 4, cudaMemcpyDeviceToHost));
+    FT_CUDA(cudaMemcpy(stamp.data(), c->stamps, (size_t)S * 4, cudaMemcpyDeviceToHost));
+
+    // plan: (old slot -> new slot) moves of the kept records
+    std::vector<std::pair<int, int>> moves;
+    std::vector<int> nifs(S_new, -1);
+    std::vector<unsigned> nstamp(S_new, 0u);
+    std::vector<int> nsfi = sfi;
+    if (S_new >= S) {
+        for (int s = 0; s < S; ++s) {
+            nifs[s] = ifs[s];
+            nstamp[s] = stamp[s];
+            if (ifs[s] >= 0) moves.emplace_back(s, s);
+        }
+    } else {
+        std::vector<int> occ;
+        for (int s = 0; s < S; ++s)
+            if (ifs[s] >= 0) occ.push_back(s);
+        std::sort(occ.begin(), occ.end(), [&](int a, int b) {
+            return stamp[a] != stamp[b] ? stamp[a] < stamp[b] : a < b;
+        });
+        const size_t drop = occ.size() > (size_t)S_new ? occ.size() - S_new : 0;
+        for (size_t i = 0; i < drop; ++i) nsfi[ifs[occ[i]]] = -1;
+        std::vector<int> keep(occ.begin() + drop, occ.end());
+        std::sort(keep.begin(), keep.end());
+        for (size_t i = 0; i < keep.size(); ++i) {
+            const int s = keep[i];
+            nifs[i] = ifs[s];
+            nstamp[i] = stamp[s];
+            nsfi[ifs[s]] = (int)i;
+            moves.emplace_back(s, (int)i);
+        }
+    }
+    uint8_t* npool = nullptr;
+    int* nifs_d = nullptr;
+    unsigned* nstamp_d = nullptr;
+    auto undo = [&](ft_status s) {
+        cudaFree(npool);
+        cudaFree(nifs_d);
+        cudaFree(nstamp_d);
+        cudaGetLastError();
+        return s;
+    };
+    if (cudaMalloc(&npool, (size_t)S_new * c->rb) != cudaSuccess) return undo(FT_ERR_OOM);
+    if (cudaMalloc(&nifs_d, (size_t)S_new * 4) != cudaSuccess) return undo(FT_ERR_OOM);
+    if (cudaMalloc(&nstamp_d, (size_t)S_new * 4) != cudaSuccess) return undo(FT_ERR_OOM);
+    for (auto& mv : moves) {
+        if (cudaMemcpyAsync(npool + (size_t)mv.second * c->rb, c->slot_pool + (size_t)mv.first * c->rb, c->rb,
+                            cudaMemcpyDeviceToDevice, c->cs) != cudaSuccess)
+            return undo(FT_ERR_CUDA);
+    }
+    if (cudaMemcpyAsync(nifs_d, nifs.data(), (size_t)S_new * 4, cudaMemcpyHostToDevice, c->cs) != cudaSuccess ||
+        cudaMemcpyAsync(nstamp_d, nstamp.data(), (size_t)S_new * 4, cudaMemcpyHostToDevice, c->cs) != cudaSuccess ||
+        cudaStreamSynchronize(c->cs) != cudaSuccess)
+        return undo(FT_ERR_CUDA);
+    // commit: from here on the new cache replaces the old one
+    if (cudaMemcpy(c->slot_for_id, nsfi.data(), (size_t)LE * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+        return undo(FT_ERR_CUDA);
+    cudaFree(c->slot_pool);
+    cudaFree(c->id_for_slot);
+    cudaFree(c->stamps);
+    c->slot_pool = npool;
+    c->id_for_slot = nifs_d;
+    c->stamps = nstamp_d;
+    c->S = S_new;
+    c->have_ctl = false;
+    return FT_OK;
+}
+
+// ------------------------------------------------------------ observability
+
+ft_status ft_get_ctl_state(ft_ctx* c, int32_t* slot_for_id, int32_t* id_for_slot, uint32_t* stamps,
+                           uint32_t* clock) {
+    if (!c) return FT_ERR_ARG;
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    if (slot_for_id) FT_CUDA(cudaMemcpy(slot_for_id, c->slot_for_id, (size_t)c->L * c->E * 4, cudaMemcpyDeviceToHost));
+    if (id_for_slot) FT_CUDA(cudaMemcpy(id_for_slot, c->id_for_slot, (size_t)c->S * 4, cudaMemcpyDeviceToHost));
+    if (stamps) FT_CUDA(cudaMemcpy(stamps, c->stamps, (size_t)c->S * 4, cudaMemcpyDeviceToHost));
+    if (clock) FT_CUDA(cudaMemcpy(clock, c->clock, 4, cudaMemcpyDeviceToHost));
+    return FT_OK;
+}
+
+ft_status ft_set_ctl_state(ft_ctx* c, const int32_t* slot_for_id, const int32_t* id_for_slot,
+                           const uint32_t* stamps, uint32_t clock) {
+    if (!c || !slot_for_id || !id_for_slot || !stamps) return FT_ERR_ARG;
+    if (c->pf.open) return FT_ERR_STATE;
+    const int LE = c->L * c->E, S = c->S;
+    for (int s = 0; s < S; ++s) {
+        const int o = id_for_slot[s];
+        if (o < -1 || o >= LE) return FT_ERR_ARG;
+        if (o >= 0 && slot_for_id[o] != s) return FT_ERR_ARG;
+        if (stamps[s] > clock) return FT_ERR_ARG;
+    }
+    for (int f = 0; f < LE; ++f) {
+        const int s = slot_for_id[f];
+        if (s < -1 || s >= S) return FT_ERR_ARG;
+        if (s >= 0 && id_for_slot[s] != f) return FT_ERR_ARG;
+    }
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    FT_CUDA(cudaMemcpy(c->slot_for_id, slot_for_id, (size_t)LE * 4, cudaMemcpyHostToDevice));
+    FT_CUDA(cudaMemcpy(c->id_for_slot, id_for_slot, (size_t)S * 4, cudaMemcpyHostToDevice));
+    FT_CUDA(cudaMemcpy(c->stamps, stamps, (size_t)S * 4, cudaMemcpyHostToDevice));
+    FT_CUDA(cudaMemcpy(c->clock, &clock, 4, cudaMemcpyHostToDevice));
+    c->have_ctl = false;
+    return FT_OK;
+}
+
+ft_status ft_get_last_ctl(ft_ctx* c, ft_ctl_info* info, int32_t* F, int32_t* C, int32_t* victims,
+                          int32_t* topk_ids, float* gates, int32_t* slots_topk) {
+    if (!c) return FT_ERR_ARG;
+    if (!c->have_ctl) return FT_ERR_STATE;
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    int I[INFO_WORDS];
+    FT_CUDA(cudaMemcpy(I, c->info, sizeof(I), cudaMemcpyDeviceToHost));
+    if (info) {
+        info->layer = I[INFO_LAYER]; info->T = I[INFO_T]; info->u = I[INFO_U]; info->h = I[INFO_H];
+        info->m = I[INFO_M]; info->q0 = I[INFO_Q0]; info->q1 = I[INFO_Q1]; info->q = I[INFO_Q];
+        info->nC = I[INFO_NC]; info->u_gpu = I[INFO_UGPU]; info->n_assign = I[INFO_NASSIGN];
+        info->clock = (uint32_t)I[INFO_CLOCK];
+    }
+    const size_t TK = (size_t)c->last_T * c->k;
+    if (F && I[INFO_Q] > 0) FT_CUDA(cudaMemcpy(F, c->Fl, (size_t)I[INFO_Q] * 4, cudaMemcpyDeviceToHost));
+    if (C && I[INFO_NC] > 0) FT_CUDA(cudaMemcpy(C, c->Cl, (size_t)I[INFO_NC] * 4, cudaMemcpyDeviceToHost));
+    if (victims && I[INFO_Q] > 0) FT_CUDA(cudaMemcpy(victims, c->victims, (size_t)I[INFO_Q] * 4, cudaMemcpyDeviceToHost));
+    if (topk_ids) FT_CUDA(cudaMemcpy(topk_ids, c->ids, TK * 4, cudaMemcpyDeviceToHost));
+    if (gates) FT_CUDA(cudaMemcpy(gates, c->gates, TK * 4, cudaMemcpyDeviceToHost));
+    if (slots_topk) FT_CUDA(cudaMemcpy(slots_topk, c->slots_topk, TK * 4, cudaMemcpyDeviceToHost));
+    return FT_OK;
+}
+
+ft_status ft_read_slot(ft_ctx* c, int32_t slot, void* host_dst) {
+    if (!c || !host_dst || slot < 0 || slot >= c->S) return FT_ERR_ARG;
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    if (c->ts) FT_CUDA(cudaStreamSynchronize(c->ts));
+    FT_CUDA(cudaMemcpy(host_dst, c->slot_pool + (size_t)slot * c->rb, c->rb, cudaMemcpyDeviceToHost));
+    return FT_OK;
+}
+
+ft_status ft_get_counters(ft_ctx* c, ft_counters* out) {
+    if (!c || !out) return FT_ERR_ARG;
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    unsigned long long v[CNT_WORDS];
+    FT_CUDA(cudaMemcpy(v, c->counters, sizeof(v), cudaMemcpyDeviceToHost));
+    out->calls = v[CNT_CALLS]; out->unique = v[CNT_UNIQUE]; out->hits = v[CNT_HITS];
+    out->misses = v[CNT_MISSES]; out->fills = v[CNT_FILLS]; out->cpu = v[CNT_CPU];
+    return FT_OK;
+}
+
+int32_t ft_num_slots(const ft_ctx* c) { return c ? c->S : 0; }
+
+ft_status ft_get_status(ft_ctx* c) {
+    if (!c) return FT_ERR_ARG;
+    cudaError_t e1 = cudaStreamSynchronize(c->cs);
+    cudaError_t e2 = c->ts ? cudaStreamSynchronize(c->ts) : cudaSuccess;
+    if (e1 != cudaSuccess || e2 != cudaSuccess) return FT_ERR_CUDA;
+    unsigned e = 0;
+    if (cudaMemcpy(&e, c->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return FT_ERR_CUDA;
+    if (e) {
+        const unsigned z = 0;
+        if (cudaMemcpy(c->err, &z, 4, cudaMemcpyHostToDevice) != cudaSuccess) return FT_ERR_CUDA;
+    }
+    if (e & FT_DEVERR_TIMEOUT) return FT_ERR_TIMEOUT;
+    if (e & FT_DEVERR_ARG) return FT_ERR_DEVICE;
+    return FT_OK;
+}
+
+void ft_destroy(ft_ctx* c) {
+    if (!c) return;
+    cudaStreamSynchronize(c->cs);
+    if (c->ts) cudaStreamSynchronize(c->ts);
+    free_ctx(c);
+}
+
+// ------------------------------------------------------------------ prefill
+
+ft_status ft_prefill_begin(ft_ctx* c, int32_t layer) {
+    if (!c || layer < 0 || layer >= c->L) return FT_ERR_ARG;
+    if (c->T_prefill_max <= 0 || c->pf.open) return FT_ERR_STATE;
+    if (c->S < 2 * c->E) return FT_ERR_CAPACITY;
+    return FT_ERR_STATE;  // prefill kernels are added by the prefill translation unit
+}
+
+ft_status ft_prefill_layer(ft_ctx* c, int32_t buffer, int32_t layer, int32_t next_layer, int32_t T,
+                           const void* x, const float* logits, float* y) {
+    (void)buffer; (void)layer; (void)next_layer; (void)T; (void)x; (void)logits; (void)y;
+    if (!c) return FT_ERR_ARG;
+    return FT_ERR_STATE;
+}
+
+}  // extern "C"

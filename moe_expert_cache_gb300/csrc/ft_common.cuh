@@ -1,0 +1,195 @@
+// Internal helpers shared by the libft kernels: PTX wrappers for mbarriers,
+// bulk (TMA) copies and the global timer, the sticky device error word, and
+// the parameter blocks passed to the kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+// Device error bits (latched in ctx->err, read by ft_get_status).
+#define FT_DEVERR_ARG      1u   // invalid ids / non-finite logits
+#define FT_DEVERR_TIMEOUT  2u   // a bounded wait gave up
+
+// Every spin wait in this library gives up after this many nanoseconds of
+// global time, latches FT_DEVERR_TIMEOUT and lets the kernel wind down.
+#define FT_WAIT_LIMIT_NS 2000000000ull
+
+// Slots of the int32 info block written by the control kernel.
+enum {
+    INFO_LAYER = 0, INFO_T, INFO_U, INFO_H, INFO_M, INFO_Q0, INFO_Q1, INFO_Q, INFO_NC,
+    INFO_UGPU, INFO_NASSIGN, INFO_CLOCK, INFO_VALID, INFO_WORDS
+};
+// Cumulative counters (uint64): calls, unique, hits, misses, fills, cpu.
+enum { CNT_CALLS = 0, CNT_UNIQUE, CNT_HITS, CNT_MISSES, CNT_FILLS, CNT_CPU, CNT_WORDS };
+
+namespace ft {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy and the CTA.
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; bounded by
+// FT_WAIT_LIMIT_NS.  Returns false (and latches the timeout bit) on give-up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((it & 63u) == 0 && globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+            atomicOr(err, FT_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes` of
+// transaction count on `bar`.  dst, src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Same, with an L2 evict-first hint for data read once (streamed weights).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 8 bf16 packed in a uint4 -> 8 floats.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace ft
+
+// ------------------------------------------------------------------ params
+
+struct CtlParams {
+    int layer, T, E, k, L, S;
+    const float* logits;      // [T,E] or null
+    const int* topk_ids;      // [T,k] or null
+    const float* topk_w;      // [T,k] or null
+    double B_P, B_H;
+    int* slot_for_id;         // [L*E]
+    int* id_for_slot;         // [S]
+    unsigned* stamps;         // [S]
+    unsigned* clock;          // [1]
+    int* out_ids;             // [T*k]
+    float* out_gates;         // [T*k]
+    int* out_slots;           // [T*k]  slot or -1
+    int* out_pos;             // [T*k]  row of (t,j) in the assignment arrays or -1
+    int* wl_slot;             // [E]    slot of GPU entry i (entries ascending expert id)
+    int* wl_off;              // [E+1]  first assignment of entry i
+    int* as_tok;              // [T*k]  token of each assignment (entry-major, token ascending)
+    float* as_gate;           // [T*k]
+    int* fill_slot;           // [E]
+    int* fill_fid;            // [E]
+    int* out_F;               // [E]
+    int* out_C;               // [E]
+    int* out_victims;         // [E]
+    int* info;                // [INFO_WORDS]
+    unsigned long long* counters;  // [CNT_WORDS]
+    unsigned* err;
+};
+
+struct FillParams {
+    const uint4* host_pool;   // device-accessible address of the host pool
+    uint4* slot_pool;
+    unsigned long long rec16; // record bytes / 16
+    const int* info;
+    const int* fill_slot;
+    const int* fill_fid;
+};
+
+struct ExpertParams {
+    const uint8_t* slot_pool;
+    unsigned long long rb;    // record bytes
+    int H, F, T, k;
+    const __nv_bfloat16* x;   // [T,H]
+    const float* partial_C;   // [T,H] or null
+    float* y;                 // [T,H]
+    const int* info;
+    const int* wl_slot;
+    const int* wl_off;
+    const int* as_tok;
+    const float* as_gate;
+    const int* out_pos;
+    float* hbuf;              // [T*k, F] fp32
+    unsigned* err;
+    int nstage;               // pipeline depth (stages in shared memory)
+    unsigned stage_bytes;     // bytes of one stage
+};
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s);
+cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gateup(ExpertParams p, int num_sms, cudaStream_t s);
+cudaError_t launch_down(ExpertParams p, int num_sms, cudaStream_t s);
+size_t route_ctl_smem_bytes(int T, int k, int E);

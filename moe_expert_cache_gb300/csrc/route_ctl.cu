@@ -1,0 +1,452 @@
+// Per-layer routing-control pass of the expert cache: one CTA per call.
+//
+// FreeToken explainer, section 10 "Dynamic Scheduling Without Giving Up CUDA
+// Graphs", and deepmox chapter "The Expert Cache That Follows the Router",
+// section "How residency follows demand without leaving the device": the
+// pass deduplicates the routed experts, classifies each flat id layer*E+e as
+// hit or miss through slot_for_id, derives the fill count q (explainer
+// section 5, q* = m*B_P/B_H; txtmix: at least one fill), picks the fill set
+// F and the LRU victims, updates the maps and recency, rewrites the route ids
+// to slot ids and leaves fixed-size worklists with a valid count for the
+// expert kernels -- all on the device, without a host round trip.
+//
+// Conventions of this implementation (the pages leave them open):
+//   top-k by logit descending, lower id first on ties; gates = softmax over
+//   the k selected logits (fp32); q0 = round((m*B_P)/B_H) in fp64, halves away
+//   from zero; q = min(clamp(q0,1,m), S-h); fill order = routed-token count
+//   descending, lower id first; a clock incremented per pass stamps hits and
+//   fills; victims = the q smallest (stamp, slot) among slots not holding a
+//   hit; the i-th fill expert takes the i-th victim.
+//
+// Victim discovery is one radix select over the slot stamps (4 passes of 8
+// bits) -- the txtmix write-up's "one scan yields K LRU candidates" -- done
+// after the hits' stamps were refreshed to the current clock: every non-hit
+// slot then has a smaller stamp than every hit slot, so the q smallest keys
+// over all slots are exactly the q smallest non-hit keys (q <= S - h).
+#include "ft_common.cuh"
+
+#include <math.h>
+
+namespace {
+
+constexpr int CTL_THREADS = 1024;
+constexpr int CTL_WARPS = CTL_THREADS / 32;
+
+struct CtlShared {
+    int bad;
+    int u, h, m;
+    int q0, q1, q;
+    unsigned clk;
+    int sel_bin, sel_before;
+    int ugpu, nassign;
+    int warp_tot[CTL_WARPS];
+    int hist[256];
+};
+
+// Block-wide exclusive scan of one int per thread (blockDim == CTL_THREADS).
+__device__ int block_excl_scan(int v, int* warp_tot, int* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int w = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_tot[lane] = w;
+    }
+    __syncthreads();
+    const int base = wid ? warp_tot[wid - 1] : 0;
+    const int tot = warp_tot[CTL_WARPS - 1];
+    __syncthreads();
+    *total = tot;
+    return base + x - v;
+}
+
+__global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ CtlShared sh;
+    const int T = p.T, k = p.k, E = p.E, S = p.S, TK = T * k;
+    const int TW = (T + 63) >> 6;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+    unsigned long long* s_tmask = reinterpret_cast<unsigned long long*>(smem_raw);  // [E*TW]
+    int* s_ids = reinterpret_cast<int*>(s_tmask + (size_t)E * TW);               // [TK]
+    float* s_g = reinterpret_cast<float*>(s_ids + TK);                            // [TK]
+    int* s_cnt = reinterpret_cast<int*>(s_g + TK);                                // [E]
+    int* s_cls = s_cnt + E;     // [E] 0 not routed, 1 hit, 2 fill, 3 CPU (miss)
+    int* s_slot = s_cls + E;    // [E] slot of a GPU expert
+    int* s_order = s_slot + E;  // [E] misses by fill rank
+    int* s_eoff = s_order + E;  // [E] first assignment of GPU expert e
+    int* s_vict = s_eoff + E;   // [E] victims by rank
+    int* s_cslot = s_vict + E;  // [E] candidate victims with stamp < tau
+    unsigned* s_cst = reinterpret_cast<unsigned*>(s_cslot + E);  // [E]
+
+    if (tid == 0) {
+        sh.bad = 0;
+        sh.u = sh.h = sh.m = 0;
+    }
+    for (int e = tid; e < E; e += CTL_THREADS) {
+        s_cnt[e] = 0;
+        s_cls[e] = 0;
+        s_slot[e] = -1;
+    }
+    for (int i = tid; i < E * TW; i += CTL_THREADS) s_tmask[i] = 0ull;
+    __syncthreads();
+
+    // ---- a1: routing (top-k + softmax gates), or validate the given top-k
+    if (p.logits) {
+        for (int t = wid; t < T; t += CTL_WARPS) {
+            const float* row = p.logits + (size_t)t * E;
+            unsigned used = 0;
+            float sel_v = 0.f;
+            int sel_e = 0;
+            bool bad = false;
+            for (int i = 0; lane + 32 * i < E; ++i)
+                if (!isfinite(row[lane + 32 * i])) bad = true;
+            for (int j = 0; j < k; ++j) {
+                float bv = -INFINITY;
+                int be = 0x7fffffff;
+                for (int i = 0; lane + 32 * i < E; ++i) {
+                    if ((used >> i) & 1u) continue;
+                    const int e = lane + 32 * i;
+                    const float v = row[e];
+                    if (v > bv || (v == bv && e < be)) {
+                        bv = v;
+                        be = e;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    if (ov > bv || (ov == bv && oe < be)) {
+                        bv = ov;
+                        be = oe;
+                    }
+                }
+                if (be >= E) {
+                    bad = true;
+                    break;
+                }
+                if ((be & 31) == lane) used |= 1u << (be >> 5);
+                if (lane == j) {
+                    sel_v = bv;
+                    sel_e = be;
+                }
+            }
+            if (__any_sync(0xffffffffu, bad)) {
+                if (lane == 0) sh.bad = 1;
+                continue;
+            }
+            const float v0 = __shfl_sync(0xffffffffu, sel_v, 0);
+            const float ex = lane < k ? expf(sel_v - v0) : 0.f;
+            const float den = ft::warp_sum(ex);
+            if (lane < k) {
+                const float g = ex / den;
+                s_ids[t * k + lane] = sel_e;
+                s_g[t * k + lane] = g;
+                p.out_ids[t * k + lane] = sel_e;
+                p.out_gates[t * k + lane] = g;
+            }
+        }
+        __syncthreads();
+    } else {
+        for (int a = tid; a < TK; a += CTL_THREADS) {
+            const int e = p.topk_ids[a];
+            const float g = p.topk_w[a];
+            if (e < 0 || e >= E || !isfinite(g)) sh.bad = 1;
+            s_ids[a] = e;
+            s_g[a] = g;
+            p.out_ids[a] = e;
+            p.out_gates[a] = g;
+        }
+        __syncthreads();
+        for (int a = tid; a < TK; a += CTL_THREADS) {
+            const int t = a / k, j = a - t * k;
+            for (int j2 = 0; j2 < j; ++j2)
+                if (s_ids[t * k + j2] == s_ids[a]) sh.bad = 1;
+        }
+        __syncthreads();
+    }
+    if (sh.bad) {
+        for (int a = tid; a < TK; a += CTL_THREADS) {
+            p.out_pos[a] = -1;
+            p.out_slots[a] = -1;
+        }
+        if (tid == 0) {
+            atomicOr(p.err, FT_DEVERR_ARG);
+            for (int i = 0; i < INFO_WORDS; ++i) p.info[i] = 0;
+            p.info[INFO_LAYER] = p.layer;
+            p.info[INFO_T] = T;
+            p.info[INFO_CLOCK] = (int)*p.clock;
+            p.wl_off[0] = 0;
+        }
+        return;
+    }
+
+    // ---- a2: dedup -- routed-token count n_e and token membership masks
+    for (int a = tid; a < TK; a += CTL_THREADS) {
+        const int e = s_ids[a];
+        const int t = a / k;
+        atomicAdd(&s_cnt[e], 1);
+        atomicOr(&s_tmask[(size_t)e * TW + (t >> 6)], 1ull << (t & 63));
+    }
+    __syncthreads();
+
+    // ---- a3: classify against the residency row of this layer
+    const int fbase = p.layer * E;
+    for (int e = tid; e < E; e += CTL_THREADS) {
+        if (s_cnt[e] > 0) {
+            const int sl = p.slot_for_id[fbase + e];
+            atomicAdd(&sh.u, 1);
+            if (sl >= 0) {
+                s_cls[e] = 1;
+                s_slot[e] = sl;
+                atomicAdd(&sh.h, 1);
+            } else {
+                s_cls[e] = 3;
+                atomicAdd(&sh.m, 1);
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- a5 (order): fill rank of every miss = (count desc, id asc)
+    for (int e = tid; e < E; e += CTL_THREADS) {
+        if (s_cls[e] == 3) {
+            const int ne = s_cnt[e];
+            int r = 0;
+            for (int e2 = 0; e2 < E; ++e2) {
+                if (s_cls[e2] == 3) {
+                    const int n2 = s_cnt[e2];
+                    r += (n2 > ne) || (n2 == ne && e2 < e);
+                }
+            }
+            s_order[r] = e;
+        }
+    }
+    // ---- a4: q, and the clock of this pass
+    if (tid == 0) {
+        const int m = sh.m, h = sh.h;
+        int q0 = 0, q1 = 0, q = 0;
+        if (m > 0) {
+            const double x = __ddiv_rn(__dmul_rn((double)m, p.B_P), p.B_H);
+            const double r = round(x);  // halves away from zero
+            q0 = r > 1.0e9 ? 1000000000 : (int)r;
+            q1 = min(max(q0, 1), m);
+            q = max(min(q1, S - h), 0);
+        }
+        sh.q0 = q0;
+        sh.q1 = q1;
+        sh.q = q;
+        sh.clk = *p.clock + 1u;
+        *p.clock = sh.clk;
+    }
+    __syncthreads();
+    const int q = sh.q, m = sh.m;
+    const unsigned clk = sh.clk;
+
+    // ---- a5: F = first q misses, C = the rest; a7 (part): refresh hit stamps
+    for (int r = tid; r < m; r += CTL_THREADS) {
+        const int e = s_order[r];
+        if (r < q) {
+            s_cls[e] = 2;
+            p.out_F[r] = e;
+        } else {
+            p.out_C[r - q] = e;
+        }
+    }
+    for (int e = tid; e < E; e += CTL_THREADS)
+        if (s_cls[e] == 1) p.stamps[s_slot[e]] = clk;
+    __syncthreads();
+
+    // ---- a6: victims = q smallest (stamp, slot)
+    if (q > 0) {
+        unsigned prefix = 0u, pmask = 0u;
+        int need = q;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int i = tid; i < 256; i += CTL_THREADS) sh.hist[i] = 0;
+            __syncthreads();
+            for (int s = tid; s < S; s += CTL_THREADS) {
+                const unsigned st = p.stamps[s];
+                if ((st & pmask) == prefix) atomicAdd(&sh.hist[(st >> shift) & 255u], 1);
+            }
+            __syncthreads();
+            if (wid == 0) {
+                int c[8];
+                int sum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    c[i] = sh.hist[lane * 8 + i];
+                    sum += c[i];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int excl = incl - sum;
+                const unsigned ball = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+                if (lane == __ffs(ball) - 1) {
+                    int run = excl, b = lane * 8 + 7;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (run + c[i] >= need) {
+                            b = lane * 8 + i;
+                            break;
+                        }
+                        run += c[i];
+                    }
+                    sh.sel_bin = b;
+                    sh.sel_before = run;
+                }
+            }
+            __syncthreads();
+            prefix |= (unsigned)sh.sel_bin << shift;
+            pmask |= 255u << shift;
+            need -= sh.sel_before;
+        }
+        const unsigned tau = prefix;
+        const int c_lt = q - need;  // slots with stamp < tau (all victims); `need` of stamp == tau
+        int base_lt = 0, base_eq = 0;
+        for (int s0 = 0; s0 < S; s0 += CTL_THREADS) {
+            const int s = s0 + tid;
+            const unsigned st = s < S ? p.stamps[s] : 0xffffffffu;
+            const int flt = (s < S && st < tau) ? 1 : 0;
+            const int feq = (s < S && st == tau) ? 1 : 0;
+            int tot;
+            const int ex = block_excl_scan(flt | (feq << 16), sh.warp_tot, &tot);
+            const int ex_lt = (ex & 0xffff) + base_lt;
+            const int ex_eq = (ex >> 16) + base_eq;
+            if (flt) {
+                s_cslot[ex_lt] = s;
+                s_cst[ex_lt] = st;
+            }
+            if (feq && ex_eq < need) s_vict[c_lt + ex_eq] = s;
+            base_lt += tot & 0xffff;
+            base_eq += tot >> 16;
+        }
+        __syncthreads();
+        for (int i = tid; i < c_lt; i += CTL_THREADS) {
+            const unsigned si = s_cst[i];
+            const int li = s_cslot[i];
+            int r = 0;
+            for (int j = 0; j < c_lt; ++j) {
+                const unsigned sj = s_cst[j];
+                r += (sj < si) || (sj == si && s_cslot[j] < li);
+            }
+            s_vict[r] = li;
+        }
+        __syncthreads();
+
+        // ---- a7: evict the victims' owners, install F, stamp the fills
+        for (int i = tid; i < q; i += CTL_THREADS) {
+            const int f = s_order[i];
+            const int v = s_vict[i];
+            const int o = p.id_for_slot[v];
+            if (o >= 0) p.slot_for_id[o] = -1;
+            const int fid = fbase + f;
+            p.id_for_slot[v] = fid;
+            p.slot_for_id[fid] = v;
+            p.stamps[v] = clk;
+            s_slot[f] = v;
+            p.fill_slot[i] = v;
+            p.fill_fid[i] = fid;
+            p.out_victims[i] = v;
+        }
+        __syncthreads();
+    }
+
+    // ---- a7: GPU worklist (entries ascending expert id) and the slot rewrite
+    {
+        const int e = tid;
+        const int isg = (e < E && (s_cls[e] == 1 || s_cls[e] == 2)) ? 1 : 0;
+        const int cnt = isg ? s_cnt[e] : 0;
+        int tot;
+        const int ex = block_excl_scan(isg | (cnt << 12), sh.warp_tot, &tot);
+        if (isg) {
+            const int ent = ex & 0xfff;
+            p.wl_slot[ent] = s_slot[e];
+            p.wl_off[ent] = ex >> 12;
+            s_eoff[e] = ex >> 12;
+        }
+        if (tid == 0) {
+            sh.ugpu = tot & 0xfff;
+            sh.nassign = tot >> 12;
+            p.wl_off[tot & 0xfff] = tot >> 12;
+        }
+    }
+    __syncthreads();
+    for (int a = tid; a < TK; a += CTL_THREADS) {
+        const int e = s_ids[a];
+        const int t = a / k;
+        const int c = s_cls[e];
+        if (c == 1 || c == 2) {
+            const unsigned long long* mk = s_tmask + (size_t)e * TW;
+            int rank = 0;
+            for (int w = 0; w < (t >> 6); ++w) rank += __popcll(mk[w]);
+            rank += __popcll(mk[t >> 6] & ((1ull << (t & 63)) - 1ull));
+            const int pos = s_eoff[e] + rank;
+            p.as_tok[pos] = t;
+            p.as_gate[pos] = s_g[a];
+            p.out_pos[a] = pos;
+            p.out_slots[a] = s_slot[e];
+        } else {
+            p.out_pos[a] = -1;
+            p.out_slots[a] = -1;
+        }
+    }
+    if (tid == 0) {
+        int* I = p.info;
+        I[INFO_LAYER] = p.layer;
+        I[INFO_T] = T;
+        I[INFO_U] = sh.u;
+        I[INFO_H] = sh.h;
+        I[INFO_M] = sh.m;
+        I[INFO_Q0] = sh.q0;
+        I[INFO_Q1] = sh.q1;
+        I[INFO_Q] = q;
+        I[INFO_NC] = sh.m - q;
+        I[INFO_UGPU] = sh.ugpu;
+        I[INFO_NASSIGN] = sh.nassign;
+        I[INFO_CLOCK] = (int)clk;
+        I[INFO_VALID] = 1;
+        unsigned long long* c = p.counters;
+        c[CNT_CALLS] += 1;
+        c[CNT_UNIQUE] += sh.u;
+        c[CNT_HITS] += sh.h;
+        c[CNT_MISSES] += sh.m;
+        c[CNT_FILLS] += q;
+        c[CNT_CPU] += sh.m - q;
+    }
+}
+
+}  // namespace
+
+size_t route_ctl_smem_bytes(int T, int k, int E) {
+    const size_t TW = (T + 63) / 64;
+    return (size_t)E * TW * 8 + (size_t)T * k * 8 + (size_t)E * 9 * 4;
+}
+
+cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s) {
+    const size_t smem = route_ctl_smem_bytes(p.T, p.k, p.E);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(route_ctl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    route_ctl_kernel<<<1, CTL_THREADS, smem, s>>>(p);
+    return cudaGetLastError();
+}
