@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark of the expert-cache MoE decode step on one GB300 (or N replicas).
+
+Workload (default): decode at T=1 through 48 MoE layers of E=128 experts,
+top-8, hidden 2048, expert ffn 768, BF16 records in a 58 GB page-locked host
+pool, 1536 cache slots shared by all layers, AR(1) router logits
+(rho 0.8, sigma 0.6), B_P = 52.7, B_H = 120.  One step = one decode token
+through all 48 layers: for every layer the control pass (routing, dedup,
+hit/miss, q, fill set, LRU victims, map update), the fills, the expert
+gate/up + SwiGLU and down + gated merge with the CPU-set partial sum.
+
+Timed region: K steps after W warm-up steps, bracketed by a barrier and a
+device synchronisation, CUDA events on the library's compute stream, max over
+ranks.  Every step streams about 3.6 GB of expert weights, far more than the
+129 MB L2, so no explicit L2 flush is used.  Per-kernel device times come
+from the library's own event records in the same timed region.
+
+--impl reference times the CPU oracle (exact-integer control + float64
+expert numerics) on this machine's host cores on bounded samples of the same
+workload; it never touches the GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = synth.DECODE_T1
+METRIC = "decode MoE-layer tokens/s"
+UNIT = "tokens/s"
+
+
+# --------------------------------------------------------------- utilities
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (one all-reduce; only timing plumbing)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sm.append(float(c[1]))
+                mx.append(float(c[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, c[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- host pool
+
+def host_pool(shape: synth.Shape, seed: int, world: int, rank: int):
+    """Page-locked host pool with every record.  One process: a pinned torch
+    tensor.  N replicas on one node: rank 0 writes the pool once into a shared
+    file (FT_POOL_DIR, default /dev/shm) and every rank maps and registers it,
+    so the node holds one copy."""
+    import torch
+    nbytes = shape.L * shape.E * shape.record_bytes
+    if world == 1:
+        pool = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        synth.fill_host_pool(pool.numpy(), shape, seed)
+        return pool, None
+    path = os.path.join(os.environ.get("FT_POOL_DIR", "/dev/shm"), f"ft_pool_{shape.L}x{shape.E}_{seed}.bin")
+    if rank == 0:
+        mm = np.memmap(path, dtype=np.uint8, mode="w+", shape=(nbytes,))
+        synth.fill_host_pool(mm, shape, seed)
+        mm.flush()
+        del mm
+    barrier(world)
+    mm = np.memmap(path, dtype=np.uint8, mode="r+", shape=(nbytes,))
+    t = torch.from_numpy(mm)
+    rc = torch.cuda.cudart().cudaHostRegister(t.data_ptr(), nbytes, 0)
+    if int(rc) != 0:
+        raise RuntimeError(f"cudaHostRegister of the shared host pool failed ({rc})")
+    return t, (mm, path)
+
+
+# ------------------------------------------------------------ our arm
+
+def kernel_bytes(shape: synth.Shape, T: int, dcnt: dict) -> dict:
+    """Algorithmic bytes moved by each decode kernel over the timed region.
+
+    fill: every fill copies one record (read over the host link, written to HBM).
+    gateup: W_gu of every GPU expert (2F*H*2 B) + x + h written (fp32).
+    down: W_d of every GPU expert (H*F*2 B) + h read + partial_C read + y written.
+    route_ctl: logits + maps touched (small; reported for completeness).
+    """
+    H, F, E, L, k = shape.H, shape.F, shape.E, shape.L, shape.k
+    ugpu = dcnt["hits"] + dcnt["fills"]
+    calls = dcnt["calls"]
+    rb = shape.record_bytes
+    return {
+        "fill": dcnt["fills"] * rb,
+        "gateup_swiglu": ugpu * 2 * F * H * 2 + calls * T * H * 2 + dcnt["assign"] * F * 4,
+        "down_combine": ugpu * H * F * 2 + dcnt["assign"] * F * 4 + calls * T * H * 4 * 2,
+        "route_ctl": calls * (T * E * 4 + 2 * T * k * 4),
+    }
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import moe_expert_cache_gb300 as ft
+
+    ft.load()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    wl = WORKLOAD
+    sh = wl.shape
+    T, L, E, H = wl.T, sh.L, sh.E, sh.H
+    W, K = args.warmup, args.steps
+    n_steps = W + K
+
+    t0 = time.time()
+    pool, shared = host_pool(sh, wl.seed, world, rank)
+    t_pool = time.time() - t0
+
+    logits = synth.ar1_logits(wl.seed, n_steps, L, T, E, wl.rho, wl.sigma)          # [steps, L, T, E]
+    xs = np.stack([np.stack([synth.tokens_bf16(wl.seed, s, l, T, H) for l in range(L)]) for s in range(n_steps)])
+    pc = np.stack([synth.random_f32(wl.seed, (l,), (T, H), 0.1) for l in range(L)])   # [L, T, H]
+    logits_d = torch.from_numpy(logits).to(device)
+    xs_d = torch.from_numpy(xs.view(np.int16)).to(device).view(torch.bfloat16)
+    pc_d = torch.from_numpy(pc).to(device)
+    y_d = torch.empty(L, T, H, dtype=torch.float32, device=device)
+
+    s = torch.cuda.Stream(device)
+    ts = torch.cuda.Stream(device)
+
+    def make_ctx():
+        return ft.Context(L, E, sh.k, H, sh.F, wl.S, pool, T_max=T, compute_stream=s.cuda_stream,
+                          transfer_stream=ts.cuda_stream)
+
+    def step(ctx, si, lg, x, p, y):
+        for l in range(L):
+            ctx.route_ctl(l, T, logits=lg[si, l], B_P=wl.B_P, B_H=wl.B_H)
+            ctx.moe_forward(x[si, l], p[l], y[l])
+
+    # ---- device-resident run
+    ctx = make_ctx()
+    with torch.cuda.stream(s):
+        for i in range(W):
+            step(ctx, i, logits_d, xs_d, pc_d, y_d)
+    torch.cuda.synchronize(device)
+    c0 = ctx.counters()
+    ctx.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(local_rank)
+    with torch.cuda.stream(s):
+        ev0.record(s)
+        for i in range(W, W + K):
+            step(ctx, i, logits_d, xs_d, pc_d, y_d)
+        ev1.record(s)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    clk = clocks.stop()
+    t_ms = ev0.elapsed_time(ev1)
+    prof = ctx.profile_read()
+    ctx.profile_enable(False)
+    c1 = ctx.counters()
+    assert ctx.status() == ft.FT_OK
+    dcnt = {k_: c1[k_] - c0[k_] for k_ in c1}
+    ctx.close()
+    t_max_ms = max_over_ranks(t_ms, world, device)
+
+    # ---- end to end: inputs copied from pinned host memory and y read back every step
+    lg_h = torch.from_numpy(logits).pin_memory()
+    xs_h = torch.from_numpy(xs.view(np.int16)).pin_memory()
+    pc_h = torch.from_numpy(pc).pin_memory()
+    y_h = torch.empty(L, T, H, dtype=torch.float32).pin_memory()
+    lg_step = torch.empty(1, L, T, E, dtype=torch.float32, device=device)
+    x_step = torch.empty(1, L, T, H, dtype=torch.int16, device=device)
+    pc_step = torch.empty(L, T, H, dtype=torch.float32, device=device)
+    ctx2 = make_ctx()
+    with torch.cuda.stream(s):
+        for i in range(W):
+            step(ctx2, i, logits_d, xs_d, pc_d, y_d)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for i in range(W, W + K):
+            lg_step.copy_(lg_h[i:i + 1], non_blocking=True)
+            x_step.copy_(xs_h[i:i + 1], non_blocking=True)
+            pc_step.copy_(pc_h, non_blocking=True)
+            step(ctx2, 0, lg_step, x_step.view(torch.bfloat16), pc_step, y_d)
+            y_h.copy_(y_d, non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    assert ctx2.status() == ft.FT_OK
+    ctx2.close()
+    h2d_bytes = (L * T * E * 4) + (L * T * H * 2) + (L * T * H * 4)
+    d2h_bytes = L * T * H * 4
+
+    # ---- roofline of the dominant kernel and per-kernel table
+    peaks = read_peaks()
+    kb = kernel_bytes(sh, T, dcnt)
+    total_ms = sum(v["ms"] for v in prof.values())
+    h2d_peak = measure_h2d_peak(device) if rank == 0 else None
+    kernels = {}
+    for name, v in prof.items():
+        ent = {"launches": v["launches"], "ms_total": round(v["ms"], 3),
+               "us_per_launch": round(1e3 * v["ms"] / v["launches"], 3),
+               "share": round(v["ms"] / total_ms, 4)}
+        if name in kb and v["ms"] > 0:
+            gbs = kb[name] / (v["ms"] * 1e-3) / 1e9
+            ent["achieved_GBps"] = round(gbs, 1)
+            if name == "fill":
+                ent["peak_GBps"] = round(h2d_peak, 1) if h2d_peak else None
+                ent["bound"] = "host link"
+            else:
+                ent["peak_GBps"] = peaks["hbm_gbs"]
+                ent["bound"] = "hbm"
+            if ent.get("peak_GBps"):
+                ent["frac"] = round(gbs / ent["peak_GBps"], 4)
+        kernels[name] = ent
+    dom = max(prof, key=lambda n: prof[n]["ms"])
+    hbm_kernels = [n for n in ("gateup_swiglu", "down_combine") if n in prof]
+    exp_ms = sum(prof[n]["ms"] for n in hbm_kernels)
+    exp_bytes = sum(kb[n] for n in hbm_kernels)
+    exp_gbs = exp_bytes / (exp_ms * 1e-3) / 1e9 if exp_ms else 0.0
+    roofline = roofline_entry(dom, kernels, kb, prof, peaks, h2d_peak, K)
+    expert_roofline = {"kernels": hbm_kernels, "bound": "hbm", "achieved": round(exp_gbs, 1),
+                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(exp_gbs / peaks["hbm_gbs"], 4),
+                       "peak_source": peaks["source"],
+                       "traffic": traffic_from_profiles("gateup_swiglu")}
+
+    value = world * T * K / (t_max_ms * 1e-3)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(t_max_ms / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; AR(1) router logits, N(0,0.02) bf16 weights)",
+        "config": {"workload": "decode T=1: 48 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, "
+                               "1536 slots, AR(1) rho=0.8, B_P=52.7, B_H=120",
+                   "L": L, "E": E, "k": sh.k, "H": H, "F": sh.F, "S": wl.S, "T": T,
+                   "l2": "no flush: each step streams ~3.6 GB of expert weights (> 129 MB L2)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "token_layers_per_s": round(value * L, 1),
+        "hit_rate": round(dcnt["hits"] / max(1, dcnt["unique"]), 4),
+        "fills_per_layer_step": round(dcnt["fills"] / max(1, dcnt["calls"]), 4),
+        "cpu_set_per_layer_step": round(dcnt["cpu"] / max(1, dcnt["calls"]), 4),
+        "roofline": roofline,
+        "roofline_expert_kernels": expert_roofline,
+        "kernels": kernels,
+        "gpu_launches": int(sum(v["launches"] for v in prof.values())),
+        "clocks": clk,
+        "e2e": {"value": round(world * T * K / (e2e_ms * 1e-3), 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes},
+        "setup_s": {"host_pool": round(t_pool, 1)},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(pool.numpy() if world == 1 else shared[0], args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if shared is not None:
+        torch.cuda.cudart().cudaHostUnregister(pool.data_ptr())
+    return out
+
+
+def roofline_entry(dom, kernels, kb, prof, peaks, h2d_peak, K):
+    ent = kernels[dom]
+    launches = prof[dom]["launches"]
+    per_launch = kb.get(dom, 0) / max(1, launches)
+    if dom == "fill":
+        bound, peak, src = "h2d", h2d_peak, "measured live: pinned host->device cudaMemcpyAsync, 1 GiB, best of 3"
+    else:
+        bound, peak, src = "hbm", peaks["hbm_gbs"], peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
+    ach = ent.get("achieved_GBps", 0.0)
+    return {"kernel": dom, "bound": bound, "achieved": ach, "peak": round(peak, 1) if peak else None,
+            "unit": "GB/s", "frac": round(ach / peak, 4) if peak else None, "peak_source": src,
+            "bytes_per_launch": int(per_launch), "us_per_launch": ent["us_per_launch"],
+            "traffic": traffic_from_profiles(dom)}
+
+
+def traffic_from_profiles(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if one matches the
+    current kernel source (profiles/traffic.json keyed by kernel and source
+    hash); else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p)).get(kernel)
+        if not d:
+            return None
+        import hashlib
+        src = os.path.join(ROOT, d["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return d["dram_bytes_per_launch"] if h == d["source_sha"] else None
+    except Exception:
+        return None
+
+
+def measure_h2d_peak(device) -> float:
+    import torch
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(n, dtype=torch.uint8, device=device)
+    best = 0.0
+    for _ in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize(device)
+        best = max(best, n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del h, d
+    return best
+
+
+# ---------------------------------------------------------- oracle timing
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else os.cpu_count()
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def oracle_samples(pool_np, n_samples: int, seconds: float | None = None):
+    """Run the oracle on decode samples of the workload: control for every
+    layer of a step (exact integers), fp64 numerics for sampled layers, with
+    the expert weights read from the host pool.  A sample = one MoE layer of
+    one decode step (control + FFN of its T=1 token over its 8 routed experts).
+    Returns (samples done, seconds)."""
+    from oracle import control as ctl
+    from oracle import numerics as nm
+    wl = WORKLOAD
+    sh = wl.shape
+    rb = sh.record_bytes
+    steps = max(1, (n_samples + sh.L - 1) // sh.L)
+    logits = synth.ar1_logits(wl.seed, steps, sh.L, wl.T, sh.E, wl.rho, wl.sigma)
+    st = ctl.CacheState.empty(sh.L, sh.E, wl.S)
+    done = 0
+    t0 = time.perf_counter()
+    for s in range(steps):
+        for l in range(sh.L):
+            ids, gates = zip(*[ctl.topk_route(r, sh.k) for r in logits[s, l]])
+            ctl.route_ctl(st, l, ids, wl.B_P, wl.B_H)
+            x = nm.bf16_to_f64(synth.tokens_bf16(wl.seed, s, l, wl.T, sh.H))
+
+            def weights(e, l=l):
+                fid = l * sh.E + e
+                return nm.record_weights_bf16(pool_np[fid * rb:(fid + 1) * rb], sh.H, sh.F)
+            nm.gated_sum(x, ids, gates, lambda t, j: True, weights)
+            done += 1
+            if done >= n_samples or (seconds is not None and time.perf_counter() - t0 > seconds):
+                return done, time.perf_counter() - t0
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(pool_np, seconds: float) -> dict:
+    done, dt = oracle_samples(pool_np, 10 ** 9, seconds)
+    L = WORKLOAD.shape.L
+    tok_s = WORKLOAD.T * done / L / dt
+    return {"value": round(tok_s, 5), "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{done} layer-steps of the workload (control + fp64 FFN of all 8 routed experts, "
+                      f"weights read from the host pool) in {dt:.1f} s; tokens/s = layer-steps/{L}/s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm, on this machine's host cores."""
+    if rank != 0:
+        return None
+    import torch
+    sh = WORKLOAD.shape
+    pool = np.empty(sh.L * sh.E * sh.record_bytes, dtype=np.uint8)
+    synth.fill_host_pool(pool, sh, WORKLOAD.seed)
+    W, K = args.warmup, args.steps
+    # a step of this arm is one sampled layer-step, bounded in total time
+    oracle_samples(pool, min(W, 2))
+    done, dt = oracle_samples(pool, K, args.cpu_seconds * 4)
+    L = sh.L
+    v = WORKLOAD.T * done / L / dt
+    cores = _blas_threads()
+    del torch
+    return {"metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": world, "steps": done, "warmup": min(W, 2),
+            "ms_per_step": round(1e3 * dt / max(1, done), 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": "decode T=1: 48 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, "
+                                   "1536 slots, AR(1) rho=0.8, B_P=52.7, B_H=120"},
+            "cpu_baseline": {"value": round(v, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{done} layer-steps (one step = one MoE layer of one decode token)"},
+            "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=240)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    rank, world, local_rank = dist_env()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

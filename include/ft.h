@@ -63,10 +63,29 @@ typedef struct {
     uint32_t clock;    /* LRU clock value of the pass                                */
 } ft_ctl_info;
 
-/* Cumulative counters since init (ft_get_counters). */
+/* Cumulative counters since init (ft_get_counters).  calls: control passes;
+ * unique/hits/misses/fills/cpu: sums of u, h, m, q, m-q; assign: routed pairs
+ * computed on the GPU (sum of n_assign). */
 typedef struct {
-    uint64_t calls, unique, hits, misses, fills, cpu;
+    uint64_t calls, unique, hits, misses, fills, cpu, assign;
 } ft_counters;
+
+/* Kernel ids of the profile (ft_profile_read). */
+#define FT_K_ROUTE_CTL    0   /* control pass                                   */
+#define FT_K_FILL         1   /* cache fills (host pool -> slots)               */
+#define FT_K_GATEUP       2   /* decode gate/up + SwiGLU                        */
+#define FT_K_DOWN         3   /* decode down + gated merge + partial_C          */
+#define FT_K_PF_ROUTE     4   /* prefill routing + counting sort                */
+#define FT_K_PF_PERMUTE   5   /* prefill token gather into expert order         */
+#define FT_K_PF_GEMM1     6   /* prefill gate/up grouped GEMM + SwiGLU          */
+#define FT_K_PF_GEMM2     7   /* prefill down grouped GEMM                      */
+#define FT_K_PF_COMBINE   8   /* prefill gated combine                          */
+#define FT_K_PF_H2D       9   /* prefill layer copy (transfer stream)           */
+#define FT_K_COUNT       16
+typedef struct {
+    double ms[FT_K_COUNT];          /* summed device time of the launches       */
+    uint64_t launches[FT_K_COUNT];  /* launches recorded                        */
+} ft_profile;
 
 /* ABI version of this header; ft_abi_version() returns the library's. */
 #define FT_ABI_VERSION 1
@@ -82,8 +101,8 @@ const char* ft_status_str(ft_status s);
  * id layer*E+expert; a GPU slot holds one complete record; one cache is shared
  * by all layers.
  *
- *   L, E, k, H, F  sizes; need E <= 1024, k <= 16, k <= E, H % 256 == 0,
- *                  F % 32 == 0.
+ *   L, E, k, H, F  sizes; need E <= 1024, k <= 16, k <= E, H % 64 == 0,
+ *                  F % 64 == 0 (H, F >= 64).
  *   S              number of slots (>= 1).  Prefill needs S >= 2E.
  *   fmt            FT_FMT_BF16 or FT_FMT_NVFP4 (record layout in ft_record_bytes).
  *   T_max          largest T of a decode call (ft_route_ctl), 1..256, and
@@ -236,6 +255,15 @@ ft_status ft_read_slot(ft_ctx* ctx, int32_t slot, void* host_dst);
 
 /* Cumulative counters into a HOST struct. */
 ft_status ft_get_counters(ft_ctx* ctx, ft_counters* out);
+
+/* Per-kernel device timing.  While enabled, the library records a CUDA event
+ * pair around each of its own launches on the stream the launch uses;
+ * ft_profile_read (syncs) sums the elapsed times per kernel id and clears the
+ * records.  Enabling resets the sums.  Not for use inside stream capture.
+ * ft_kernel_name returns a static name for an id (NULL if unknown). */
+ft_status ft_profile_enable(ft_ctx* ctx, int32_t enable);
+ft_status ft_profile_read(ft_ctx* ctx, ft_profile* out);
+const char* ft_kernel_name(int32_t id);
 
 /* Current number of slots. */
 int32_t ft_num_slots(const ft_ctx* ctx);

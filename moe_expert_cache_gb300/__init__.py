@@ -39,7 +39,14 @@ class CtlInfo(ctypes.Structure):
 
 
 class Counters(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_uint64) for n in ("calls", "unique", "hits", "misses", "fills", "cpu")]
+    _fields_ = [(n, ctypes.c_uint64) for n in ("calls", "unique", "hits", "misses", "fills", "cpu", "assign")]
+
+
+FT_K_COUNT = 16
+
+
+class Profile(ctypes.Structure):
+    _fields_ = [("ms", ctypes.c_double * FT_K_COUNT), ("launches", ctypes.c_uint64 * FT_K_COUNT)]
 
 
 # name -> (restype, argtypes)
@@ -59,6 +66,9 @@ _SIGS = {
     "ft_get_last_ctl": (_c_int, [_c_p, ctypes.POINTER(CtlInfo), _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "ft_read_slot": (_c_int, [_c_p, _c_int, _c_p]),
     "ft_get_counters": (_c_int, [_c_p, ctypes.POINTER(Counters)]),
+    "ft_profile_enable": (_c_int, [_c_p, _c_int]),
+    "ft_profile_read": (_c_int, [_c_p, ctypes.POINTER(Profile)]),
+    "ft_kernel_name": (ctypes.c_char_p, [_c_int]),
     "ft_num_slots": (_c_int, [_c_p]),
     "ft_get_status": (_c_int, [_c_p]),
     "ft_destroy": (None, [_c_p]),
@@ -153,6 +163,19 @@ def read_slot(ctx, slot, host_dst) -> int:
 
 def get_counters(ctx, out) -> int:
     return load().ft_get_counters(ctx, out)
+
+
+def profile_enable(ctx, enable) -> int:
+    return load().ft_profile_enable(ctx, enable)
+
+
+def profile_read(ctx, out) -> int:
+    return load().ft_profile_read(ctx, out)
+
+
+def kernel_name(kid: int):
+    n = load().ft_kernel_name(kid)
+    return n.decode() if n else None
 
 
 def num_slots(ctx) -> int:
@@ -270,3 +293,15 @@ class Context:
 
     def status(self) -> int:
         return get_status(self.h)
+
+    def profile_enable(self, on: bool = True):
+        _check(profile_enable(self.h, 1 if on else 0), "ft_profile_enable")
+
+    def profile_read(self) -> dict:
+        pr = Profile()
+        _check(profile_read(self.h, ctypes.byref(pr)), "ft_profile_read")
+        out = {}
+        for i in range(FT_K_COUNT):
+            if pr.launches[i]:
+                out[kernel_name(i)] = {"ms": pr.ms[i], "launches": int(pr.launches[i])}
+        return out

@@ -15,6 +15,19 @@
 #include <new>
 #include <vector>
 
+// Per-kernel event records of the optional profile.
+struct ProfRec {
+    int kid;
+    cudaEvent_t a, b;
+};
+struct Profiler {
+    bool on = false;
+    std::vector<cudaEvent_t> pool;
+    std::vector<ProfRec> pending;
+    double ms[FT_K_COUNT] = {};
+    uint64_t n[FT_K_COUNT] = {};
+};
+
 struct ft_ctx {
     int L, E, k, H, F, S, fmt, T_max, T_prefill_max;
     size_t rb;
@@ -38,6 +51,7 @@ struct ft_ctx {
     int last_T;
     bool have_ctl;
     PrefillState pf;
+    Profiler prof;
 };
 
 namespace {
@@ -53,8 +67,49 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
         }                                                                                      \
     } while (0)
 
+cudaEvent_t prof_event(Profiler& pr) {
+    if (!pr.pool.empty()) {
+        cudaEvent_t e = pr.pool.back();
+        pr.pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Records an event pair around the launches made in its scope (profile on).
+struct ProfScope {
+    Profiler& pr;
+    cudaStream_t s;
+    ProfRec r{};
+    ProfScope(Profiler& p, int kid, cudaStream_t st) : pr(p), s(st) {
+        if (!pr.on) return;
+        r.kid = kid;
+        r.a = prof_event(pr);
+        r.b = prof_event(pr);
+        if (r.a) cudaEventRecord(r.a, s);
+    }
+    ~ProfScope() {
+        if (!pr.on || !r.a || !r.b) return;
+        cudaEventRecord(r.b, s);
+        pr.pending.push_back(r);
+    }
+};
+
+void prof_release(Profiler& pr) {
+    for (auto& r : pr.pending) {
+        pr.pool.push_back(r.a);
+        pr.pool.push_back(r.b);
+    }
+    pr.pending.clear();
+    for (auto e : pr.pool) cudaEventDestroy(e);
+    pr.pool.clear();
+}
+
 void free_ctx(ft_ctx* c) {
     if (!c) return;
+    prof_release(c->prof);
     prefill_free(c->pf);
     cudaFree(c->slot_pool);
     cudaFree(c->slot_for_id);
@@ -204,13 +259,19 @@ ft_status ft_route_ctl(ft_ctx* c, int32_t layer, int32_t T, const float* logits,
     p.fill_slot = c->fill_slot; p.fill_fid = c->fill_fid;
     p.out_F = c->Fl; p.out_C = c->Cl; p.out_victims = c->victims;
     p.info = c->info; p.counters = c->counters; p.err = c->err;
-    FT_CUDA(launch_route_ctl(p, c->cs));
+    {
+        ProfScope ps(c->prof, FT_K_ROUTE_CTL, c->cs);
+        FT_CUDA(launch_route_ctl(p, c->cs));
+    }
     FillParams fp{};
     fp.host_pool = (const uint4*)c->host_pool_dev;
     fp.slot_pool = (uint4*)c->slot_pool;
     fp.rec16 = c->rb / 16;
     fp.info = c->info; fp.fill_slot = c->fill_slot; fp.fill_fid = c->fill_fid;
-    FT_CUDA(launch_fill(fp, 2 * c->num_sms, c->cs));
+    {
+        ProfScope ps(c->prof, FT_K_FILL, c->cs);
+        FT_CUDA(launch_fill(fp, 2 * c->num_sms, c->cs));
+    }
     c->last_T = T;
     c->have_ctl = true;
     return FT_OK;
@@ -225,8 +286,14 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.x = (const __nv_bfloat16*)x; p.partial_C = partial_C; p.y = y;
     p.info = c->info; p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok;
     p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err;
-    FT_CUDA(launch_gateup(p, c->num_sms, c->cs));
-    FT_CUDA(launch_down(p, c->num_sms, c->cs));
+    {
+        ProfScope ps(c->prof, FT_K_GATEUP, c->cs);
+        FT_CUDA(launch_gateup(p, c->num_sms, c->cs));
+    }
+    {
+        ProfScope ps(c->prof, FT_K_DOWN, c->cs);
+        FT_CUDA(launch_down(p, c->num_sms, c->cs));
+    }
     return FT_OK;
 }
 
@@ -386,7 +453,51 @@ ft_status ft_get_counters(ft_ctx* c, ft_counters* out) {
     FT_CUDA(cudaMemcpy(v, c->counters, sizeof(v), cudaMemcpyDeviceToHost));
     out->calls = v[CNT_CALLS]; out->unique = v[CNT_UNIQUE]; out->hits = v[CNT_HITS];
     out->misses = v[CNT_MISSES]; out->fills = v[CNT_FILLS]; out->cpu = v[CNT_CPU];
+    out->assign = v[CNT_ASSIGN];
     return FT_OK;
+}
+
+ft_status ft_profile_enable(ft_ctx* c, int32_t enable) {
+    if (!c) return FT_ERR_ARG;
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    if (c->ts) FT_CUDA(cudaStreamSynchronize(c->ts));
+    for (auto& r : c->prof.pending) {
+        c->prof.pool.push_back(r.a);
+        c->prof.pool.push_back(r.b);
+    }
+    c->prof.pending.clear();
+    for (int i = 0; i < FT_K_COUNT; ++i) {
+        c->prof.ms[i] = 0.0;
+        c->prof.n[i] = 0;
+    }
+    c->prof.on = enable != 0;
+    return FT_OK;
+}
+
+ft_status ft_profile_read(ft_ctx* c, ft_profile* out) {
+    if (!c || !out) return FT_ERR_ARG;
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    if (c->ts) FT_CUDA(cudaStreamSynchronize(c->ts));
+    for (auto& r : c->prof.pending) {
+        float ms = 0.f;
+        FT_CUDA(cudaEventElapsedTime(&ms, r.a, r.b));
+        c->prof.ms[r.kid] += ms;
+        c->prof.n[r.kid] += 1;
+        c->prof.pool.push_back(r.a);
+        c->prof.pool.push_back(r.b);
+    }
+    c->prof.pending.clear();
+    for (int i = 0; i < FT_K_COUNT; ++i) {
+        out->ms[i] = c->prof.ms[i];
+        out->launches[i] = c->prof.n[i];
+    }
+    return FT_OK;
+}
+
+const char* ft_kernel_name(int32_t id) {
+    static const char* names[FT_K_COUNT] = {"route_ctl", "fill", "gateup_swiglu", "down_combine", "pf_route",
+                                            "pf_permute", "pf_gemm1_swiglu", "pf_gemm2", "pf_combine", "pf_h2d"};
+    return (id >= 0 && id < FT_K_COUNT) ? names[id] : nullptr;
 }
 
 int32_t ft_num_slots(const ft_ctx* c) { return c ? c->S : 0; }

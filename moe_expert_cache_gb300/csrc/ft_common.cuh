@@ -20,8 +20,8 @@ enum {
     INFO_LAYER = 0, INFO_T, INFO_U, INFO_H, INFO_M, INFO_Q0, INFO_Q1, INFO_Q, INFO_NC,
     INFO_UGPU, INFO_NASSIGN, INFO_CLOCK, INFO_VALID, INFO_WORDS
 };
-// Cumulative counters (uint64): calls, unique, hits, misses, fills, cpu.
-enum { CNT_CALLS = 0, CNT_UNIQUE, CNT_HITS, CNT_MISSES, CNT_FILLS, CNT_CPU, CNT_WORDS };
+// Cumulative counters (uint64): calls, unique, hits, misses, fills, cpu, assign.
+enum { CNT_CALLS = 0, CNT_UNIQUE, CNT_HITS, CNT_MISSES, CNT_FILLS, CNT_CPU, CNT_ASSIGN, CNT_WORDS };
 
 namespace ft {
 

@@ -428,6 +428,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         c[CNT_MISSES] += sh.m;
         c[CNT_FILLS] += q;
         c[CNT_CPU] += sh.m - q;
+        c[CNT_ASSIGN] += sh.nassign;
     }
 }
 

@@ -127,3 +127,19 @@ def rel_l2(a, b) -> float:
 
 def max_abs(a, b) -> float:
     return float(np.max(np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64))))
+
+
+def record_weights_bf16(record, H: int, F: int):
+    """(Wg [F,H], Wu [F,H], Wd [H,F]) float64 read from one BF16 record's bytes.
+
+    Layout (the library's record definition): bank W_gu [2F, H] row-major with
+    gate and up rows interleaved in groups of 16 (16 gate rows, then the 16
+    matching up rows), then bank W_d [H, F] row-major.
+    """
+    r16 = np.asarray(record, dtype=np.uint8).view(np.uint16)
+    assert r16.size == 3 * H * F
+    gu = bf16_to_f64(r16[:2 * F * H]).reshape(F // 16, 2, 16, H)
+    Wg = gu[:, 0].reshape(F, H)
+    Wu = gu[:, 1].reshape(F, H)
+    Wd = bf16_to_f64(r16[2 * F * H:]).reshape(H, F)
+    return Wg, Wu, Wd

@@ -125,3 +125,23 @@ def test_bf16_rounding_of_generator():
     assert back[2] == 1.0 + 4 * 2 ** -8        # tie -> even (1 + 2^-6)
     assert back[3] == -2.5
     assert abs(back[4] - 3.14159) <= 2 ** -7 * 2
+
+
+def test_oracle_record_reader_matches_generator():
+    H, F = 64, 128
+    for e in (0, 5):
+        rec = synth.record_bf16(0, 0, e, H, F)
+        got = nm.record_weights_bf16(rec, H, F)
+        want = [nm.bf16_to_f64(a) for a in synth.expert_weights_bf16(0, 0, e, H, F)]
+        for g, w in zip(got, want):
+            assert np.array_equal(g, w)
+    # a record whose gate/up groups were swapped reads back differently
+    rec = synth.record_bf16(0, 0, 1, H, F)
+    sw = rec.copy().view(np.uint16)
+    blk = 16 * H
+    a = sw[:blk].copy()
+    sw[:blk] = sw[blk:2 * blk]
+    sw[blk:2 * blk] = a
+    Wg2, Wu2, _ = nm.record_weights_bf16(sw.view(np.uint8), H, F)
+    Wg, Wu, _ = nm.record_weights_bf16(rec, H, F)
+    assert not np.array_equal(Wg2, Wg) and np.array_equal(Wg2[:16], Wu[:16])
