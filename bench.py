@@ -417,7 +417,7 @@ def oracle_samples(pool_np, n_samples: int, seconds: float | None = None):
     wl = WORKLOAD
     sh = wl.shape
     rb = sh.record_bytes
-    steps = max(1, (n_samples + sh.L - 1) // sh.L)
+    steps = max(1, min(wl.steps, (n_samples + sh.L - 1) // sh.L))
     logits = synth.ar1_logits(wl.seed, steps, sh.L, wl.T, sh.E, wl.rho, wl.sigma)
     st = ctl.CacheState.empty(sh.L, sh.E, wl.S)
     done = 0
