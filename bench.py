@@ -160,9 +160,9 @@ def kernel_bytes(shape: synth.Shape, T: int, dcnt: dict) -> dict:
     """Algorithmic bytes moved by each decode kernel over the timed region.
 
     fill: every fill copies one record (read over the host link, written to HBM).
-    gateup: W_gu of every GPU expert (2F*H*2 B) + x + h written (fp32).
-    down: W_d of every GPU expert (H*F*2 B) + h read + partial_C read + y written.
-    route_ctl: logits + maps touched (small; reported for completeness).
+    expert_ffn: the whole record of every GPU expert (3*F*H*2 B: W_gu and W_d)
+        + x read + h written and read once (fp32) + partial_C read + y written.
+    route_ctl: logits + ids/gates written (small; reported for completeness).
     """
     H, F, E, L, k = shape.H, shape.F, shape.E, shape.L, shape.k
     ugpu = dcnt["hits"] + dcnt["fills"]
@@ -170,8 +170,7 @@ def kernel_bytes(shape: synth.Shape, T: int, dcnt: dict) -> dict:
     rb = shape.record_bytes
     return {
         "fill": dcnt["fills"] * rb,
-        "gateup_swiglu": ugpu * 2 * F * H * 2 + calls * T * H * 2 + dcnt["assign"] * F * 4,
-        "down_combine": ugpu * H * F * 2 + dcnt["assign"] * F * 4 + calls * T * H * 4 * 2,
+        "expert_ffn": ugpu * 3 * F * H * 2 + calls * T * H * 2 + 2 * dcnt["assign"] * F * 4 + calls * T * H * 4 * 2,
         "route_ctl": calls * (T * E * 4 + 2 * T * k * 4),
     }
 
@@ -301,7 +300,7 @@ def run_ours(args, rank, world, local_rank):
                 ent["frac"] = round(gbs / ent["peak_GBps"], 4)
         kernels[name] = ent
     dom = max(prof, key=lambda n: prof[n]["ms"])
-    hbm_kernels = [n for n in ("gateup_swiglu", "down_combine") if n in prof]
+    hbm_kernels = [n for n in ("expert_ffn",) if n in prof]
     exp_ms = sum(prof[n]["ms"] for n in hbm_kernels)
     exp_bytes = sum(kb[n] for n in hbm_kernels)
     exp_gbs = exp_bytes / (exp_ms * 1e-3) / 1e9 if exp_ms else 0.0
@@ -309,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
     expert_roofline = {"kernels": hbm_kernels, "bound": "hbm", "achieved": round(exp_gbs, 1),
                        "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(exp_gbs / peaks["hbm_gbs"], 4),
                        "peak_source": peaks["source"],
-                       "traffic": traffic_from_profiles("gateup_swiglu")}
+                       "traffic": traffic_from_profiles("expert_ffn")}
 
     value = world * T * K / (t_max_ms * 1e-3)
     out = {

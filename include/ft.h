@@ -73,8 +73,8 @@ typedef struct {
 /* Kernel ids of the profile (ft_profile_read). */
 #define FT_K_ROUTE_CTL    0   /* control pass                                   */
 #define FT_K_FILL         1   /* cache fills (host pool -> slots)               */
-#define FT_K_GATEUP       2   /* decode gate/up + SwiGLU                        */
-#define FT_K_DOWN         3   /* decode down + gated merge + partial_C          */
+#define FT_K_EXPERT       2   /* decode expert FFN: gate/up + SwiGLU, down,     */
+                              /* gated merge + partial_C (one fused kernel)     */
 #define FT_K_PF_ROUTE     4   /* prefill routing + counting sort                */
 #define FT_K_PF_PERMUTE   5   /* prefill token gather into expert order         */
 #define FT_K_PF_GEMM1     6   /* prefill gate/up grouped GEMM + SwiGLU          */

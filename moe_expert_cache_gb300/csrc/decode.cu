@@ -12,18 +12,21 @@
 // FFN(x) = W_d (SiLU(W_g x) * (W_u x)); y_t = sum_j g_tj FFN_{e_tj}(x_t) over
 // the routes that run on the GPU, plus the supplied partial sum of the CPU set.
 // Decode is bandwidth-bound (about one flop per weight byte at T = 1), so the
-// kernels are streaming GEMVs: a persistent grid of one CTA per SM, weights
-// staged through a ring of shared-memory buffers by 1-D bulk (TMA) copies
-// completing on mbarriers, consumed by 8 warps with fp32 accumulation.
-//   gate/up: the work is the flat list of (GPU expert, feature pair); CTA c
-//            takes a contiguous 1/G share; one stage = gate rows f, f+1 and
-//            up rows f, f+1 (contiguous in the record thanks to the 16-row
-//            gate/up interleave); h is written in fp32.
-//   down:    CTA c owns output rows [c*H/G, (c+1)*H/G) for every GPU expert:
-//            one stage = those W_d rows of one expert plus the h rows of its
-//            tokens; the gated merge over j (ascending) and partial_C is then
-//            done in the same CTA, so the sum order is fixed and no atomics
-//            are needed.
+// layer is one persistent, cooperatively launched streaming kernel with one
+// CTA per SM:
+//   * a producer warp streams weights into a ring of shared-memory slots with
+//     1-D bulk (TMA) copies completing on mbarriers;
+//   * phase A (gate/up + SwiGLU): the work is the flat list of (GPU expert,
+//     group of 8 features); CTA c takes a contiguous 1/G share; one slot holds
+//     8 gate rows and the 8 matching up rows (contiguous in the record thanks
+//     to the 16-row gate/up interleave); consumer warp w computes feature w of
+//     the slot alone (both dot products, SiLU, product) and writes h in fp32;
+//   * a grid barrier makes every h visible; the producer does not wait for it
+//     and keeps streaming the W_d rows of phase B meanwhile;
+//   * phase B (down + merge): CTA c owns output rows [c*H/G, (c+1)*H/G) of
+//     every GPU expert; then it sums the gated expert outputs over j ascending
+//     and adds partial_C, so the order of the sum is fixed and no atomics are
+//     needed.
 #include "ft_common.cuh"
 
 namespace {
@@ -31,7 +34,9 @@ namespace {
 constexpr int CONSUMER_WARPS = 8;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;
 constexpr int EXPERT_THREADS = CONSUMERS + 32;  // + one producer warp
+constexpr int FPC = CONSUMER_WARPS;             // features per phase-A chunk
 constexpr int MAXTOK = 16;                      // tokens per register block
+constexpr size_t HEAD = 256;                    // barrier area
 
 // ------------------------------------------------------------------- fill
 
@@ -60,48 +65,82 @@ __global__ void __launch_bounds__(512) fill_kernel(FillParams p) {
     }
 }
 
-// ---------------------------------------------------------- gate/up + SwiGLU
+// ------------------------------------------------------------- expert FFN
 
 __device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
 
-struct RingBars {
-    uint64_t* full;
-    uint64_t* empty;
-};
+__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
-// Producer-side drain: wait (bounded) for the last phase of every stage that
-// received a copy, so no bulk copy is in flight into shared memory at exit.
-__device__ void drain_ring(RingBars rb, int issued, int nst, unsigned* err) {
-    for (int it = issued - nst; it < issued; ++it) {
-        if (it < 0) continue;
-        ft::mbar_wait(&rb.full[it % nst], (it / nst) & 1, err);
-    }
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
-__global__ void __launch_bounds__(EXPERT_THREADS, 1) gateup_swiglu_kernel(ExpertParams p) {
+// Sense-reversing grid barrier over all CTAs of a cooperative launch:
+// bar[0] counts arrivals, bar[1] is the generation.  Bounded: gives up after
+// FT_WAIT_LIMIT_NS and latches the timeout bit.  Called by one thread per CTA
+// between CTA-wide barriers.
+__device__ void grid_barrier(unsigned* bar, unsigned G, unsigned* err) {
+    const unsigned gen0 = ld_acquire_gpu(&bar[1]);
+    __threadfence();
+    const unsigned c = atomicAdd(&bar[0], 1u);
+    if (c == G - 1) {
+        atomicExch(&bar[0], 0u);
+        __threadfence();
+        atomicAdd(&bar[1], 1u);
+    } else {
+        const uint64_t t0 = ft::globaltimer();
+        for (unsigned it = 0; ld_acquire_gpu(&bar[1]) == gen0; ++it) {
+            if ((it & 63u) == 63u && ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                atomicOr(err, FT_DEVERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __threadfence();
+}
+
+// Producer-side drain: wait (bounded) for the last phase of every slot that
+// received a copy, so no bulk copy is in flight into shared memory at exit.
+__device__ void drain_ring(uint64_t* full, int issued, int nst, unsigned* err) {
+    for (int it = issued - nst; it < issued; ++it)
+        if (it >= 0) ft::mbar_wait(&full[it % nst], (it / nst) & 1, err);
+}
+
+__global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int H = p.H, F = p.F, T = p.T;
+    const int H = p.H, F = p.F, T = p.T, k = p.k;
     const int nst = p.nstage;
+    const unsigned slot_bytes = p.stage_bytes;
     const int ugpu = p.info[INFO_UGPU];
-    const int upe = F / 2;  // feature pairs per expert
-    const int N = ugpu * upe;
     const int G = gridDim.x, c = blockIdx.x;
-    const int u0 = (int)((long long)N * c / G), u1 = (int)((long long)N * (c + 1) / G);
-    if (u0 >= u1) return;
+    const int cpe = F / FPC;  // phase-A chunks per expert
+    const int NA = ugpu * cpe;
+    const int a0 = (int)((long long)NA * c / G), a1 = (int)((long long)NA * (c + 1) / G);
+    const int r0 = (int)((long long)H * c / G), r1 = (int)((long long)H * (c + 1) / G);
+    const int R = r1 - r0;
+    const int RMAX = (H + G - 1) / G;
+    const int nB = R > 0 ? ugpu : 0;
 
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
-    RingBars bars{reinterpret_cast<uint64_t*>(smem), reinterpret_cast<uint64_t*>(smem) + nst};
-    float* red = reinterpret_cast<float*>(smem + 256);                       // [2][8][MAXTOK]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + nst;
     const size_t xbytes = (size_t)T * H * 2;
     const bool x_in_smem = xbytes <= 65536;
-    __nv_bfloat16* x_s = reinterpret_cast<__nv_bfloat16*>(smem + 256 + 2 * 8 * MAXTOK * 4);
-    unsigned char* stages = smem + 256 + 2 * 8 * MAXTOK * 4 + (x_in_smem ? ((xbytes + 127) & ~(size_t)127) : 0);
+    size_t o = HEAD;
+    __nv_bfloat16* x_s = reinterpret_cast<__nv_bfloat16*>(smem + o);
+    if (x_in_smem) o += (xbytes + 127) & ~(size_t)127;
+    float* o_s = reinterpret_cast<float*>(smem + o);  // [T*k][RMAX] expert outputs of my rows
+    o += ((size_t)T * k * RMAX * 4 + 127) & ~(size_t)127;
+    unsigned char* ring = smem + o;
     const __nv_bfloat16* xsrc = x_in_smem ? x_s : p.x;
+    const unsigned rowbytes = (unsigned)H * 2u;
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
-            ft::mbar_init(&bars.full[s], 1);
-            ft::mbar_init(&bars.empty[s], CONSUMER_WARPS);
+            ft::mbar_init(&full[s], 1);
+            ft::mbar_init(&empty[s], CONSUMER_WARPS);
         }
         ft::mbar_fence_init();
     }
@@ -110,207 +149,150 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) gateup_swiglu_kernel(Expert
             reinterpret_cast<uint4*>(x_s)[i] = reinterpret_cast<const uint4*>(p.x)[i];
     __syncthreads();
 
-    const unsigned rowbytes = (unsigned)H * 2u;
+    // ------------------------------------------------------------ producer
     if (wid == CONSUMER_WARPS) {
         if (lane == 0) {
             const uint64_t pol = ft::l2_policy_evict_first();
             int it = 0;
-            for (int u = u0; u < u1; ++u, ++it) {
+            bool ok = true;
+            for (int a = a0; a < a1 && ok; ++a, ++it) {
                 const int st = it % nst;
-                if (it >= nst && !ft::mbar_wait(&bars.empty[st], ((it / nst) - 1) & 1, p.err)) break;
-                const int ent = u / upe;
-                const int f0 = (u - ent * upe) * 2;
+                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
+                const int ent = a / cpe;
+                const int f0 = (a - ent * cpe) * FPC;
                 const uint8_t* rec = p.slot_pool + (size_t)p.wl_slot[ent] * p.rb;
                 const int grp = f0 >> 4, i = f0 & 15;
-                const uint8_t* gsrc = rec + (size_t)(grp * 32 + i) * rowbytes;
-                const uint8_t* usrc = rec + (size_t)(grp * 32 + 16 + i) * rowbytes;
-                unsigned char* dst = stages + (size_t)st * p.stage_bytes;
-                ft::mbar_arrive_expect_tx(&bars.full[st], 4u * rowbytes);
-                ft::bulk_g2s_hint(dst, gsrc, 2u * rowbytes, &bars.full[st], pol);
-                ft::bulk_g2s_hint(dst + 2u * rowbytes, usrc, 2u * rowbytes, &bars.full[st], pol);
+                unsigned char* dst = ring + (size_t)st * slot_bytes;
+                ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * rowbytes);
+                ft::bulk_g2s_hint(dst, rec + (size_t)(grp * 32 + i) * rowbytes, FPC * rowbytes, &full[st], pol);
+                ft::bulk_g2s_hint(dst + (size_t)FPC * rowbytes, rec + (size_t)(grp * 32 + 16 + i) * rowbytes,
+                                  FPC * rowbytes, &full[st], pol);
             }
-            drain_ring(bars, it, nst, p.err);
+            const unsigned wb = (unsigned)R * F * 2u;
+            for (int e = 0; e < nB && ok; ++e, ++it) {
+                const int st = it % nst;
+                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
+                const uint8_t* wd = p.slot_pool + (size_t)p.wl_slot[e] * p.rb + (size_t)2 * F * H * 2 +
+                                    (size_t)r0 * F * 2;
+                ft::mbar_arrive_expect_tx(&full[st], wb);
+                ft::bulk_g2s_hint(ring + (size_t)st * slot_bytes, wd, wb, &full[st], pol);
+            }
+            drain_ring(full, it, nst, p.err);
         }
         return;
     }
 
-    // consumers: warp w handles row (w >> 1) of the stage (g0, g1, u0, u1) and K half (w & 1).
-    // After a failed (timed-out) wait a warp stops waiting and computing but
-    // keeps the same named-barrier sequence as the others; it no longer
-    // releases stages, so the producer's own bounded wait ends the ring.
-    const int r = wid >> 1, kh = wid & 1;
-    const int nv = H / 16;  // 16-byte vectors per K half
-    int buf = 0;
+    // ------------------------------------------------- phase A: gate/up + SwiGLU
+    // After a failed (timed-out) wait a warp stops waiting, computing and
+    // releasing slots, but keeps the same barrier sequence as the others.
     int it = 0;
     bool failed = false;
-    for (int u = u0; u < u1; ++u, ++it) {
+    for (int a = a0; a < a1; ++a, ++it) {
         const int st = it % nst;
-        const bool ok = !failed && ft::mbar_wait(&bars.full[st], (it / nst) & 1, p.err);
+        const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
         failed = !ok;
-        const int ent = u / upe;
-        const int f0 = (u - ent * upe) * 2;
+        const int ent = a / cpe;
+        const int f = (a - ent * cpe) * FPC + wid;
         const int off = p.wl_off[ent];
         const int ntok = p.wl_off[ent + 1] - off;
-        const uint4* wrow = reinterpret_cast<const uint4*>(stages + (size_t)st * p.stage_bytes +
-                                                           (size_t)r * rowbytes + (size_t)kh * (rowbytes / 2));
-        for (int g0 = 0; g0 < ntok; g0 += MAXTOK) {
+        const uint4* wg = reinterpret_cast<const uint4*>(ring + (size_t)st * slot_bytes + (size_t)wid * rowbytes);
+        const uint4* wu = reinterpret_cast<const uint4*>(ring + (size_t)st * slot_bytes +
+                                                         (size_t)(FPC + wid) * rowbytes);
+        for (int g0 = 0; g0 < ntok && ok; g0 += MAXTOK) {
             const int ng = min(MAXTOK, ntok - g0);
             int tk[MAXTOK];
 #pragma unroll
             for (int n = 0; n < MAXTOK; ++n) tk[n] = n < ng ? p.as_tok[off + g0 + n] : 0;
-            float acc[MAXTOK];
+            float ag[MAXTOK], au[MAXTOK];
 #pragma unroll
-            for (int n = 0; n < MAXTOK; ++n) acc[n] = 0.f;
-            if (ok) {
-                for (int v = lane; v < nv; v += 32) {
+            for (int n = 0; n < MAXTOK; ++n) ag[n] = au[n] = 0.f;
+            for (int v = lane; v < H / 8; v += 32) {
+                float g8[8], u8[8];
+                ft::bf16x8_to_f32(wg[v], g8);
+                ft::bf16x8_to_f32(wu[v], u8);
+#pragma unroll
+                for (int n = 0; n < MAXTOK; ++n) {
+                    if (n < ng) {
+                        float x8[8];
+                        ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(xsrc + (size_t)tk[n] * H)[v], x8);
+                        float sg = ag[n], su = au[n];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            sg = fmaf(g8[q], x8[q], sg);
+                            su = fmaf(u8[q], x8[q], su);
+                        }
+                        ag[n] = sg;
+                        au[n] = su;
+                    }
+                }
+            }
+            float mine = 0.f;
+#pragma unroll
+            for (int n = 0; n < MAXTOK; ++n) {
+                if (n < ng) {
+                    const float sg = ft::warp_sum(ag[n]);
+                    const float su = ft::warp_sum(au[n]);
+                    if (lane == n) mine = silu_mul(sg, su);
+                }
+            }
+            if (lane < ng) p.hbuf[(size_t)(off + g0 + lane) * F + f] = mine;
+        }
+        __syncwarp();
+        if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+    }
+
+    // every h of this layer is written before any CTA starts phase B
+    ft::named_bar_sync(1, CONSUMERS);
+    if (tid == 0) grid_barrier(p.gbar, (unsigned)G, p.err);
+    ft::named_bar_sync(1, CONSUMERS);
+
+    // ---------------------------------------------------- phase B: down rows
+    for (int e = 0; e < nB; ++e, ++it) {
+        const int st = it % nst;
+        const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
+        failed = !ok;
+        const int off = p.wl_off[e];
+        const int ntok = p.wl_off[e + 1] - off;
+        const unsigned char* sb = ring + (size_t)st * slot_bytes;
+        for (int rl = wid; rl < R && ok; rl += CONSUMER_WARPS) {
+            const uint4* wrow = reinterpret_cast<const uint4*>(sb + (size_t)rl * F * 2);
+            for (int g0 = 0; g0 < ntok; g0 += MAXTOK) {
+                const int ng = min(MAXTOK, ntok - g0);
+                float acc[MAXTOK];
+#pragma unroll
+                for (int n = 0; n < MAXTOK; ++n) acc[n] = 0.f;
+                for (int v = lane; v < F / 8; v += 32) {
                     float w8[8];
                     ft::bf16x8_to_f32(wrow[v], w8);
 #pragma unroll
                     for (int n = 0; n < MAXTOK; ++n) {
                         if (n < ng) {
-                            const uint4 xv = reinterpret_cast<const uint4*>(xsrc + (size_t)tk[n] * H +
-                                                                            (size_t)kh * (H / 2))[v];
-                            float x8[8];
-                            ft::bf16x8_to_f32(xv, x8);
+                            const float* hp = p.hbuf + (size_t)(off + g0 + n) * F + v * 8;
+                            const float4 x0 = ldcg4(hp), x1 = ldcg4(hp + 4);
                             float s = acc[n];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) s = fmaf(w8[q], x8[q], s);
+                            s = fmaf(w8[0], x0.x, s);
+                            s = fmaf(w8[1], x0.y, s);
+                            s = fmaf(w8[2], x0.z, s);
+                            s = fmaf(w8[3], x0.w, s);
+                            s = fmaf(w8[4], x1.x, s);
+                            s = fmaf(w8[5], x1.y, s);
+                            s = fmaf(w8[6], x1.z, s);
+                            s = fmaf(w8[7], x1.w, s);
                             acc[n] = s;
                         }
                     }
                 }
-            }
 #pragma unroll
-            for (int n = 0; n < MAXTOK; ++n) {
-                if (n < ng) {
-                    const float sum = ft::warp_sum(acc[n]);
-                    if (lane == 0) red[(buf * 8 + wid) * MAXTOK + n] = sum;
-                }
-            }
-            if (ok && g0 + MAXTOK >= ntok) {
-                __syncwarp();
-                if (lane == 0) ft::mbar_arrive(&bars.empty[st]);
-            }
-            ft::named_bar_sync(1, CONSUMERS);
-            if (tid < 2 * ng) {
-                const int fi = tid / ng, n = tid - fi * ng;
-                const float* R = red + buf * 8 * MAXTOK;
-                const float a = R[(2 * fi) * MAXTOK + n] + R[(2 * fi + 1) * MAXTOK + n];
-                const float b = R[(4 + 2 * fi) * MAXTOK + n] + R[(5 + 2 * fi) * MAXTOK + n];
-                p.hbuf[(size_t)(off + g0 + n) * F + f0 + fi] = silu_mul(a, b);
-            }
-            buf ^= 1;
-        }
-        if (ntok == 0) {
-            __syncwarp();
-            if (ok && lane == 0) ft::mbar_arrive(&bars.empty[st]);
-            ft::named_bar_sync(1, CONSUMERS);
-        }
-    }
-}
-
-// ------------------------------------------------ down + gated merge + partial_C
-
-__global__ void __launch_bounds__(EXPERT_THREADS, 1) down_combine_kernel(ExpertParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int H = p.H, F = p.F, T = p.T, k = p.k;
-    const int nst = p.nstage;
-    const int ugpu = p.info[INFO_UGPU];
-    const int G = gridDim.x, c = blockIdx.x;
-    const int r0 = (int)((long long)H * c / G), r1 = (int)((long long)H * (c + 1) / G);
-    const int R = r1 - r0;
-    if (R <= 0) return;
-    const int RMAX = (H + G - 1) / G;
-    const int nasg_max = T * k;
-
-    const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
-    RingBars bars{reinterpret_cast<uint64_t*>(smem), reinterpret_cast<uint64_t*>(smem) + nst};
-    float* o_s = reinterpret_cast<float*>(smem + 256);  // [T*k][RMAX]
-    unsigned char* stages = smem + 256 + (((size_t)nasg_max * RMAX * 4 + 127) & ~(size_t)127);
-    const unsigned wbytes_max = (unsigned)(((size_t)RMAX * F * 2 + 127) & ~(size_t)127);
-
-    if (tid == 0) {
-        for (int s = 0; s < nst; ++s) {
-            ft::mbar_init(&bars.full[s], 1);
-            ft::mbar_init(&bars.empty[s], CONSUMER_WARPS);
-        }
-        ft::mbar_fence_init();
-    }
-    __syncthreads();
-
-    if (wid == CONSUMER_WARPS) {
-        if (lane == 0) {
-            const uint64_t pol = ft::l2_policy_evict_first();
-            int it = 0;
-            for (int ent = 0; ent < ugpu; ++ent, ++it) {
-                const int st = it % nst;
-                if (it >= nst && !ft::mbar_wait(&bars.empty[st], ((it / nst) - 1) & 1, p.err)) break;
-                const int off = p.wl_off[ent];
-                const int ntok = p.wl_off[ent + 1] - off;
-                const uint8_t* wd = p.slot_pool + (size_t)p.wl_slot[ent] * p.rb + (size_t)2 * F * H * 2 +
-                                    (size_t)r0 * F * 2;
-                unsigned char* dst = stages + (size_t)st * p.stage_bytes;
-                const unsigned wb = (unsigned)R * F * 2, hb = (unsigned)ntok * F * 4;
-                ft::mbar_arrive_expect_tx(&bars.full[st], wb + hb);
-                ft::bulk_g2s_hint(dst, wd, wb, &bars.full[st], pol);
-                if (hb) ft::bulk_g2s(dst + wbytes_max, p.hbuf + (size_t)off * F, hb, &bars.full[st]);
-            }
-            drain_ring(bars, it, nst, p.err);
-        }
-        return;
-    }
-
-    const int nv = F / 8;  // 16-byte weight vectors per row
-    int it = 0;
-    for (int ent = 0; ent < ugpu; ++ent, ++it) {
-        const int st = it % nst;
-        const bool ok = ft::mbar_wait(&bars.full[st], (it / nst) & 1, p.err);
-        const int off = p.wl_off[ent];
-        const int ntok = p.wl_off[ent + 1] - off;
-        const unsigned char* sb = stages + (size_t)st * p.stage_bytes;
-        const float* hs = reinterpret_cast<const float*>(sb + wbytes_max);
-        if (ok) {
-            for (int rl = wid; rl < R; rl += CONSUMER_WARPS) {
-                const uint4* wrow = reinterpret_cast<const uint4*>(sb + (size_t)rl * F * 2);
-                for (int g0 = 0; g0 < ntok; g0 += MAXTOK) {
-                    const int ng = min(MAXTOK, ntok - g0);
-                    float acc[MAXTOK];
-#pragma unroll
-                    for (int n = 0; n < MAXTOK; ++n) acc[n] = 0.f;
-                    for (int v = lane; v < nv; v += 32) {
-                        float w8[8];
-                        ft::bf16x8_to_f32(wrow[v], w8);
-#pragma unroll
-                        for (int n = 0; n < MAXTOK; ++n) {
-                            if (n < ng) {
-                                const float4* h4 = reinterpret_cast<const float4*>(hs + (size_t)(g0 + n) * F + v * 8);
-                                const float4 a = h4[0], b = h4[1];
-                                float s = acc[n];
-                                s = fmaf(w8[0], a.x, s);
-                                s = fmaf(w8[1], a.y, s);
-                                s = fmaf(w8[2], a.z, s);
-                                s = fmaf(w8[3], a.w, s);
-                                s = fmaf(w8[4], b.x, s);
-                                s = fmaf(w8[5], b.y, s);
-                                s = fmaf(w8[6], b.z, s);
-                                s = fmaf(w8[7], b.w, s);
-                                acc[n] = s;
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int n = 0; n < MAXTOK; ++n) {
-                        if (n < ng) {
-                            const float sum = ft::warp_sum(acc[n]);
-                            if (lane == 0) o_s[(size_t)(off + g0 + n) * RMAX + rl] = sum;
-                        }
+                for (int n = 0; n < MAXTOK; ++n) {
+                    if (n < ng) {
+                        const float s = ft::warp_sum(acc[n]);
+                        if (lane == 0) o_s[(size_t)(off + g0 + n) * RMAX + rl] = s;
                     }
                 }
             }
         }
-        if (!ok) break;  // stop releasing stages: the producer's bounded wait ends the ring
         __syncwarp();
-        if (lane == 0) ft::mbar_arrive(&bars.empty[st]);
+        if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
     }
     ft::named_bar_sync(1, CONSUMERS);
     // gated merge in fixed order: j ascending, then the CPU-set partial sum
@@ -321,9 +303,9 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) down_combine_kernel(ExpertP
             const int pos = p.out_pos[t * k + j];
             if (pos >= 0) acc = fmaf(p.as_gate[pos], o_s[(size_t)pos * RMAX + rl], acc);
         }
-        const size_t o = (size_t)t * H + r0 + rl;
-        if (p.partial_C) acc += p.partial_C[o];
-        p.y[o] = acc;
+        const size_t oi = (size_t)t * H + r0 + rl;
+        if (p.partial_C) acc += p.partial_C[oi];
+        p.y[oi] = acc;
     }
 }
 
@@ -334,44 +316,43 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-static cudaError_t set_smem(const void* fn, size_t bytes) {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
 static constexpr size_t kSmemLimit = 227 * 1024;
 
-// Shared-memory plan of the gate/up kernel: fixed header, x (if it fits in
-// 64 KiB), then as many 4-row stages as fit (at most 8).
-cudaError_t launch_gateup(ExpertParams p, int num_sms, cudaStream_t s) {
-    const size_t xbytes = (size_t)p.T * p.H * 2;
-    const size_t head = 256 + 2 * 8 * MAXTOK * 4 + (xbytes <= 65536 ? ((xbytes + 127) & ~(size_t)127) : 0);
-    const size_t stage = (size_t)4 * p.H * 2;
-    int nst = (int)((kSmemLimit - head) / stage);
-    if (nst > 8) nst = 8;
-    if (nst < 2) return cudaErrorInvalidValue;
-    p.nstage = nst;
-    p.stage_bytes = (unsigned)stage;
-    const size_t smem = head + stage * nst;
-    cudaError_t e = set_smem((const void*)gateup_swiglu_kernel, smem);
-    if (e != cudaSuccess) return e;
-    gateup_swiglu_kernel<<<num_sms, EXPERT_THREADS, smem, s>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_down(ExpertParams p, int num_sms, cudaStream_t s) {
+// Shared-memory plan: barriers, x (if it fits in 64 KiB), the per-CTA output
+// block, then as many ring slots as fit (at most 4).  A slot holds one phase-A
+// chunk (16 rows of H) or one phase-B stage (R rows of F).
+cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     const int G = num_sms;
     const int RMAX = (p.H + G - 1) / G;
-    const size_t head = 256 + (((size_t)p.T * p.k * RMAX * 4 + 127) & ~(size_t)127);
-    const size_t wpart = ((size_t)RMAX * p.F * 2 + 127) & ~(size_t)127;
-    const size_t stage = wpart + (size_t)p.T * p.F * 4;
-    int nst = (int)((kSmemLimit - head) / stage);
-    if (nst > 8) nst = 8;
+    const size_t xbytes = (size_t)p.T * p.H * 2;
+    const size_t head = HEAD + (xbytes <= 65536 ? ((xbytes + 127) & ~(size_t)127) : 0) +
+                        (((size_t)p.T * p.k * RMAX * 4 + 127) & ~(size_t)127);
+    size_t slot = (size_t)2 * FPC * p.H * 2;
+    const size_t down = (size_t)RMAX * p.F * 2;
+    if (down > slot) slot = down;
+    slot = (slot + 127) & ~(size_t)127;
+    if (head >= kSmemLimit) return cudaErrorInvalidValue;
+    int nst = (int)((kSmemLimit - head) / slot);
+    if (nst > 4) nst = 4;
     if (nst < 2) return cudaErrorInvalidValue;
     p.nstage = nst;
-    p.stage_bytes = (unsigned)stage;
-    const size_t smem = head + stage * nst;
-    cudaError_t e = set_smem((const void*)down_combine_kernel, smem);
-    if (e != cudaSuccess) return e;
-    down_combine_kernel<<<G, EXPERT_THREADS, smem, s>>>(p);
-    return cudaGetLastError();
+    p.stage_bytes = (unsigned)slot;
+    const size_t smem = head + slot * nst;
+    static size_t smem_set = 0;
+    if (smem != smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(expert_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(EXPERT_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, expert_ffn_kernel, p);
 }

@@ -47,6 +47,7 @@ struct ft_ctx {
     float *gates, *as_gate;
     unsigned long long* counters;
     unsigned* err;
+    unsigned* gbar;
     float* hbuf;
     int last_T;
     bool have_ctl;
@@ -157,6 +158,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
         T_max < 1 || T_max > 256 || T_max * k > 4096 || T_prefill_max < 0 || !host_pool)
         return FT_ERR_ARG;
     if (fmt != FT_FMT_BF16) return FT_ERR_ARG;  // NVFP4 banks are accepted by a later version
+    if (route_ctl_smem_bytes(T_max, k, E, S) > kCtlSmemMax) return FT_ERR_ARG;
     ft_ctx* c = new (std::nothrow) ft_ctx();
     if (!c) return FT_ERR_OOM;
     c->L = L; c->E = E; c->k = k; c->H = H; c->F = F; c->S = S; c->fmt = fmt;
@@ -206,7 +208,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
                  o_wls = carve((size_t)E * 4), o_wlo = carve((size_t)(E + 1) * 4), o_fs = carve((size_t)E * 4),
                  o_ff = carve((size_t)E * 4), o_F = carve((size_t)E * 4), o_C = carve((size_t)E * 4),
                  o_v = carve((size_t)E * 4), o_info = carve(INFO_WORDS * 4), o_cnt = carve(CNT_WORDS * 8),
-                 o_err = carve(4);
+                 o_err = carve(4), o_gbar = carve(8);
     INIT_CUDA(cudaMalloc(&c->arena, off));
     INIT_CUDA(cudaMemset(c->arena, 0, off));
     uint8_t* a = (uint8_t*)c->arena;
@@ -227,6 +229,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     c->info = (int*)(a + o_info);
     c->counters = (unsigned long long*)(a + o_cnt);
     c->err = (unsigned*)(a + o_err);
+    c->gbar = (unsigned*)(a + o_gbar);
     INIT_CUDA(cudaMalloc(&c->hbuf, TK * F * 4));
     if (nvfp4_global) {
         INIT_CUDA(cudaMalloc(&c->nvfp4_global, (size_t)L * E * 4));
@@ -285,14 +288,10 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.slot_pool = c->slot_pool; p.rb = c->rb; p.H = c->H; p.F = c->F; p.T = c->last_T; p.k = c->k;
     p.x = (const __nv_bfloat16*)x; p.partial_C = partial_C; p.y = y;
     p.info = c->info; p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok;
-    p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err;
+    p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err; p.gbar = c->gbar;
     {
-        ProfScope ps(c->prof, FT_K_GATEUP, c->cs);
-        FT_CUDA(launch_gateup(p, c->num_sms, c->cs));
-    }
-    {
-        ProfScope ps(c->prof, FT_K_DOWN, c->cs);
-        FT_CUDA(launch_down(p, c->num_sms, c->cs));
+        ProfScope ps(c->prof, FT_K_EXPERT, c->cs);
+        FT_CUDA(launch_expert_ffn(p, c->num_sms, c->cs));
     }
     return FT_OK;
 }
@@ -301,6 +300,7 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
 
 ft_status ft_cache_resize(ft_ctx* c, int32_t S_new) {
     if (!c || S_new < 1) return FT_ERR_ARG;
+    if (route_ctl_smem_bytes(c->T_max, c->k, c->E, S_new) > kCtlSmemMax) return FT_ERR_ARG;
     if (c->pf.open) return FT_ERR_STATE;
     FT_CUDA(cudaStreamSynchronize(c->cs));
     if (c->ts) FT_CUDA(cudaStreamSynchronize(c->ts));
@@ -495,7 +495,7 @@ ft_status ft_profile_read(ft_ctx* c, ft_profile* out) {
 }
 
 const char* ft_kernel_name(int32_t id) {
-    static const char* names[FT_K_COUNT] = {"route_ctl", "fill", "gateup_swiglu", "down_combine", "pf_route",
+    static const char* names[FT_K_COUNT] = {"route_ctl", "fill", "expert_ffn", nullptr, "pf_route",
                                             "pf_permute", "pf_gemm1_swiglu", "pf_gemm2", "pf_combine", "pf_h2d"};
     return (id >= 0 && id < FT_K_COUNT) ? names[id] : nullptr;
 }

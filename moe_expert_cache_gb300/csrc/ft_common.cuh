@@ -183,6 +183,7 @@ struct ExpertParams {
     const int* out_pos;
     float* hbuf;              // [T*k, F] fp32
     unsigned* err;
+    unsigned* gbar;           // [2] grid barrier (arrivals, generation), zero at init
     int nstage;               // pipeline depth (stages in shared memory)
     unsigned stage_bytes;     // bytes of one stage
 };
@@ -190,6 +191,6 @@ struct ExpertParams {
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s);
 cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);
-cudaError_t launch_gateup(ExpertParams p, int num_sms, cudaStream_t s);
-cudaError_t launch_down(ExpertParams p, int num_sms, cudaStream_t s);
-size_t route_ctl_smem_bytes(int T, int k, int E);
+cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s);
+size_t route_ctl_smem_bytes(int T, int k, int E, int S);
+constexpr size_t kCtlSmemMax = 200 * 1024;

@@ -18,19 +18,24 @@
 //   fills; victims = the q smallest (stamp, slot) among slots not holding a
 //   hit; the i-th fill expert takes the i-th victim.
 //
-// Victim discovery is one radix select over the slot stamps (4 passes of 8
-// bits) -- the txtmix write-up's "one scan yields K LRU candidates" -- done
-// after the hits' stamps were refreshed to the current clock: every non-hit
-// slot then has a smaller stamp than every hit slot, so the q smallest keys
-// over all slots are exactly the q smallest non-hit keys (q <= S - h).
+// Latency design: every global read the pass needs (logits, the layer's row
+// of slot_for_id, the stamps and owners of all slots, the clock) is issued at
+// entry and lands in shared memory; the rest runs on shared memory.  Victim
+// discovery works on (stamp, slot) keys after the hits' stamps were refreshed
+// to the current clock -- every non-hit slot then has a smaller stamp than
+// every hit slot, so the q smallest keys over all slots are exactly the q
+// smallest non-hit keys (q <= S - h).  Small q: q block-wide arg-min rounds;
+// larger q: one radix select over the stamps (the txtmix write-up's "one scan
+// yields K LRU candidates") then a rank sort of the candidates.
 #include "ft_common.cuh"
 
 #include <math.h>
 
 namespace {
 
-constexpr int CTL_THREADS = 1024;
+constexpr int CTL_THREADS = 512;
 constexpr int CTL_WARPS = CTL_THREADS / 32;
+constexpr int SMALL_Q = 8;
 
 struct CtlShared {
     int bad;
@@ -39,11 +44,13 @@ struct CtlShared {
     unsigned clk;
     int sel_bin, sel_before;
     int ugpu, nassign;
+    int carry0, carry1;
     int warp_tot[CTL_WARPS];
+    unsigned long long warp_key[CTL_WARPS];
     int hist[256];
 };
 
-// Block-wide exclusive scan of one int per thread (blockDim == CTL_THREADS).
+// Block-wide exclusive scan of one int per thread.
 __device__ int block_excl_scan(int v, int* warp_tot, int* total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int x = v;
@@ -55,13 +62,13 @@ __device__ int block_excl_scan(int v, int* warp_tot, int* total) {
     if (lane == 31) warp_tot[wid] = x;
     __syncthreads();
     if (wid == 0) {
-        int w = warp_tot[lane];
+        int w = lane < CTL_WARPS ? warp_tot[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        warp_tot[lane] = w;
+        if (lane < CTL_WARPS) warp_tot[lane] = w;
     }
     __syncthreads();
     const int base = wid ? warp_tot[wid - 1] : 0;
@@ -71,51 +78,83 @@ __device__ int block_excl_scan(int v, int* warp_tot, int* total) {
     return base + x - v;
 }
 
+__device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) {
+    return a < b ? a : b;
+}
+
 __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ CtlShared sh;
     const int T = p.T, k = p.k, E = p.E, S = p.S, TK = T * k;
     const int TW = (T + 63) >> 6;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int fbase = p.layer * E;
 
     unsigned long long* s_tmask = reinterpret_cast<unsigned long long*>(smem_raw);  // [E*TW]
-    int* s_ids = reinterpret_cast<int*>(s_tmask + (size_t)E * TW);               // [TK]
-    float* s_g = reinterpret_cast<float*>(s_ids + TK);                            // [TK]
-    int* s_cnt = reinterpret_cast<int*>(s_g + TK);                                // [E]
-    int* s_cls = s_cnt + E;     // [E] 0 not routed, 1 hit, 2 fill, 3 CPU (miss)
+    unsigned* s_stamp = reinterpret_cast<unsigned*>(s_tmask + (size_t)E * TW);     // [S]
+    int* s_owner = reinterpret_cast<int*>(s_stamp + S);                             // [S]
+    int* s_ids = s_owner + S;                                                        // [TK]
+    float* s_g = reinterpret_cast<float*>(s_ids + TK);                               // [TK]
+    int* s_cnt = reinterpret_cast<int*>(s_g + TK);                                   // [E]
+    int* s_row = s_cnt + E;     // [E] slot_for_id row of this layer (before the pass)
+    int* s_cls = s_row + E;     // [E] 0 not routed, 1 hit, 2 fill, 3 CPU (miss)
     int* s_slot = s_cls + E;    // [E] slot of a GPU expert
     int* s_order = s_slot + E;  // [E] misses by fill rank
     int* s_eoff = s_order + E;  // [E] first assignment of GPU expert e
     int* s_vict = s_eoff + E;   // [E] victims by rank
-    int* s_cslot = s_vict + E;  // [E] candidate victims with stamp < tau
+    int* s_cslot = s_vict + E;  // [E] radix path: candidates with stamp < tau
     unsigned* s_cst = reinterpret_cast<unsigned*>(s_cslot + E);  // [E]
 
-    if (tid == 0) {
-        sh.bad = 0;
-        sh.u = sh.h = sh.m = 0;
+    // ---- issue every global read of the pass
+    for (int s = tid; s < S; s += CTL_THREADS) {
+        s_stamp[s] = p.stamps[s];
+        s_owner[s] = p.id_for_slot[s];
     }
     for (int e = tid; e < E; e += CTL_THREADS) {
+        s_row[e] = p.slot_for_id[fbase + e];
         s_cnt[e] = 0;
         s_cls[e] = 0;
         s_slot[e] = -1;
     }
     for (int i = tid; i < E * TW; i += CTL_THREADS) s_tmask[i] = 0ull;
-    __syncthreads();
+    if (tid == 0) {
+        sh.bad = 0;
+        sh.u = sh.h = sh.m = 0;
+        sh.clk = *p.clock;
+    }
 
-    // ---- a1: routing (top-k + softmax gates), or validate the given top-k
+    // ---- a1: routing (top-k + softmax gates), or the given top-k
     if (p.logits) {
         for (int t = wid; t < T; t += CTL_WARPS) {
             const float* row = p.logits + (size_t)t * E;
+            constexpr int RV = 8;  // values per lane held in registers (E <= 256)
+            float vals[RV];
+            bool bad = false;
+#pragma unroll
+            for (int i = 0; i < RV; ++i) {
+                const int e = lane + 32 * i;
+                vals[i] = e < E ? row[e] : -INFINITY;
+                if (e < E && !isfinite(vals[i])) bad = true;
+            }
+            bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the shuffle loop
             unsigned used = 0;
             float sel_v = 0.f;
             int sel_e = 0;
-            bool bad = false;
-            for (int i = 0; lane + 32 * i < E; ++i)
-                if (!isfinite(row[lane + 32 * i])) bad = true;
-            for (int j = 0; j < k; ++j) {
+            for (int j = 0; j < k && !bad; ++j) {
                 float bv = -INFINITY;
                 int be = 0x7fffffff;
-                for (int i = 0; lane + 32 * i < E; ++i) {
+#pragma unroll
+                for (int i = 0; i < RV; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < E && !((used >> i) & 1u)) {
+                        const float v = vals[i];
+                        if (v > bv || (v == bv && e < be)) {
+                            bv = v;
+                            be = e;
+                        }
+                    }
+                }
+                for (int i = RV; lane + 32 * i < E; ++i) {
                     if ((used >> i) & 1u) continue;
                     const int e = lane + 32 * i;
                     const float v = row[e];
@@ -187,7 +226,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             for (int i = 0; i < INFO_WORDS; ++i) p.info[i] = 0;
             p.info[INFO_LAYER] = p.layer;
             p.info[INFO_T] = T;
-            p.info[INFO_CLOCK] = (int)*p.clock;
+            p.info[INFO_CLOCK] = (int)sh.clk;
             p.wl_off[0] = 0;
         }
         return;
@@ -203,10 +242,9 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     __syncthreads();
 
     // ---- a3: classify against the residency row of this layer
-    const int fbase = p.layer * E;
     for (int e = tid; e < E; e += CTL_THREADS) {
         if (s_cnt[e] > 0) {
-            const int sl = p.slot_for_id[fbase + e];
+            const int sl = s_row[e];
             atomicAdd(&sh.u, 1);
             if (sl >= 0) {
                 s_cls[e] = 1;
@@ -220,7 +258,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     }
     __syncthreads();
 
-    // ---- a5 (order): fill rank of every miss = (count desc, id asc)
+    // ---- a5 (order): fill rank of every miss = (count desc, id asc); a4: q
     for (int e = tid; e < E; e += CTL_THREADS) {
         if (s_cls[e] == 3) {
             const int ne = s_cnt[e];
@@ -234,7 +272,6 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             s_order[r] = e;
         }
     }
-    // ---- a4: q, and the clock of this pass
     if (tid == 0) {
         const int m = sh.m, h = sh.h;
         int q0 = 0, q1 = 0, q = 0;
@@ -248,8 +285,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         sh.q0 = q0;
         sh.q1 = q1;
         sh.q = q;
-        sh.clk = *p.clock + 1u;
-        *p.clock = sh.clk;
+        sh.clk = sh.clk + 1u;
     }
     __syncthreads();
     const int q = sh.q, m = sh.m;
@@ -265,19 +301,44 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             p.out_C[r - q] = e;
         }
     }
-    for (int e = tid; e < E; e += CTL_THREADS)
-        if (s_cls[e] == 1) p.stamps[s_slot[e]] = clk;
+    for (int e = tid; e < E; e += CTL_THREADS) {
+        if (s_cls[e] == 1) {
+            s_stamp[s_slot[e]] = clk;
+            p.stamps[s_slot[e]] = clk;
+        }
+    }
     __syncthreads();
 
     // ---- a6: victims = q smallest (stamp, slot)
-    if (q > 0) {
+    if (q > 0 && q <= SMALL_Q) {
+        for (int r = 0; r < q; ++r) {
+            unsigned long long best = ~0ull;
+            for (int s = tid; s < S; s += CTL_THREADS)
+                best = umin64(best, ((unsigned long long)s_stamp[s] << 32) | (unsigned)s);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) best = umin64(best, __shfl_xor_sync(0xffffffffu, best, o));
+            if (lane == 0) sh.warp_key[wid] = best;
+            __syncthreads();
+            if (wid == 0) {
+                unsigned long long b = lane < CTL_WARPS ? sh.warp_key[lane] : ~0ull;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) b = umin64(b, __shfl_xor_sync(0xffffffffu, b, o));
+                if (lane == 0) {
+                    const int v = (int)(b & 0xffffffffu);
+                    s_vict[r] = v;
+                    s_stamp[v] = clk;  // taken: never the minimum again
+                }
+            }
+            __syncthreads();
+        }
+    } else if (q > SMALL_Q) {
         unsigned prefix = 0u, pmask = 0u;
         int need = q;
         for (int shift = 24; shift >= 0; shift -= 8) {
             for (int i = tid; i < 256; i += CTL_THREADS) sh.hist[i] = 0;
             __syncthreads();
             for (int s = tid; s < S; s += CTL_THREADS) {
-                const unsigned st = p.stamps[s];
+                const unsigned st = s_stamp[s];
                 if ((st & pmask) == prefix) atomicAdd(&sh.hist[(st >> shift) & 255u], 1);
             }
             __syncthreads();
@@ -317,26 +378,33 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             need -= sh.sel_before;
         }
         const unsigned tau = prefix;
-        const int c_lt = q - need;  // slots with stamp < tau (all victims); `need` of stamp == tau
-        int base_lt = 0, base_eq = 0;
+        const int c_lt = q - need;  // slots with stamp < tau are all victims; `need` of stamp == tau
+        if (tid == 0) {
+            sh.carry0 = 0;
+            sh.carry1 = 0;
+        }
+        __syncthreads();
         for (int s0 = 0; s0 < S; s0 += CTL_THREADS) {
             const int s = s0 + tid;
-            const unsigned st = s < S ? p.stamps[s] : 0xffffffffu;
+            const unsigned st = s < S ? s_stamp[s] : 0xffffffffu;
             const int flt = (s < S && st < tau) ? 1 : 0;
             const int feq = (s < S && st == tau) ? 1 : 0;
             int tot;
             const int ex = block_excl_scan(flt | (feq << 16), sh.warp_tot, &tot);
-            const int ex_lt = (ex & 0xffff) + base_lt;
-            const int ex_eq = (ex >> 16) + base_eq;
+            const int ex_lt = (ex & 0xffff) + sh.carry0;
+            const int ex_eq = (ex >> 16) + sh.carry1;
             if (flt) {
                 s_cslot[ex_lt] = s;
                 s_cst[ex_lt] = st;
             }
             if (feq && ex_eq < need) s_vict[c_lt + ex_eq] = s;
-            base_lt += tot & 0xffff;
-            base_eq += tot >> 16;
+            __syncthreads();
+            if (tid == 0) {
+                sh.carry0 += tot & 0xffff;
+                sh.carry1 += tot >> 16;
+            }
+            __syncthreads();
         }
-        __syncthreads();
         for (int i = tid; i < c_lt; i += CTL_THREADS) {
             const unsigned si = s_cst[i];
             const int li = s_cslot[i];
@@ -348,45 +416,57 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             s_vict[r] = li;
         }
         __syncthreads();
-
-        // ---- a7: evict the victims' owners, install F, stamp the fills
-        for (int i = tid; i < q; i += CTL_THREADS) {
-            const int f = s_order[i];
-            const int v = s_vict[i];
-            const int o = p.id_for_slot[v];
-            if (o >= 0) p.slot_for_id[o] = -1;
-            const int fid = fbase + f;
-            p.id_for_slot[v] = fid;
-            p.slot_for_id[fid] = v;
-            p.stamps[v] = clk;
-            s_slot[f] = v;
-            p.fill_slot[i] = v;
-            p.fill_fid[i] = fid;
-            p.out_victims[i] = v;
-        }
-        __syncthreads();
     }
 
+    // ---- a7: evict the victims' owners, install F, stamp the fills
+    for (int i = tid; i < q; i += CTL_THREADS) {
+        const int f = s_order[i];
+        const int v = s_vict[i];
+        const int o = s_owner[v];
+        if (o >= 0) p.slot_for_id[o] = -1;
+        const int fid = fbase + f;
+        p.id_for_slot[v] = fid;
+        p.slot_for_id[fid] = v;
+        p.stamps[v] = clk;
+        s_slot[f] = v;
+        p.fill_slot[i] = v;
+        p.fill_fid[i] = fid;
+        p.out_victims[i] = v;
+    }
+    __syncthreads();
+
     // ---- a7: GPU worklist (entries ascending expert id) and the slot rewrite
-    {
-        const int e = tid;
+    if (tid == 0) {
+        sh.carry0 = 0;
+        sh.carry1 = 0;
+    }
+    __syncthreads();
+    for (int e0 = 0; e0 < E; e0 += CTL_THREADS) {
+        const int e = e0 + tid;
         const int isg = (e < E && (s_cls[e] == 1 || s_cls[e] == 2)) ? 1 : 0;
         const int cnt = isg ? s_cnt[e] : 0;
         int tot;
         const int ex = block_excl_scan(isg | (cnt << 12), sh.warp_tot, &tot);
         if (isg) {
-            const int ent = ex & 0xfff;
+            const int ent = (ex & 0xfff) + sh.carry0;
+            const int off = (ex >> 12) + sh.carry1;
             p.wl_slot[ent] = s_slot[e];
-            p.wl_off[ent] = ex >> 12;
-            s_eoff[e] = ex >> 12;
+            p.wl_off[ent] = off;
+            s_eoff[e] = off;
         }
+        __syncthreads();
         if (tid == 0) {
-            sh.ugpu = tot & 0xfff;
-            sh.nassign = tot >> 12;
-            p.wl_off[tot & 0xfff] = tot >> 12;
+            sh.carry0 += tot & 0xfff;
+            sh.carry1 += tot >> 12;
         }
+        __syncthreads();
     }
-    __syncthreads();
+    if (tid == 0) {
+        sh.ugpu = sh.carry0;
+        sh.nassign = sh.carry1;
+        p.wl_off[sh.carry0] = sh.carry1;
+        *p.clock = clk;
+    }
     for (int a = tid; a < TK; a += CTL_THREADS) {
         const int e = s_ids[a];
         const int t = a / k;
@@ -406,6 +486,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             p.out_slots[a] = -1;
         }
     }
+    __syncthreads();
     if (tid == 0) {
         int* I = p.info;
         I[INFO_LAYER] = p.layer;
@@ -434,19 +515,18 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
 
 }  // namespace
 
-size_t route_ctl_smem_bytes(int T, int k, int E) {
+size_t route_ctl_smem_bytes(int T, int k, int E, int S) {
     const size_t TW = (T + 63) / 64;
-    return (size_t)E * TW * 8 + (size_t)T * k * 8 + (size_t)E * 9 * 4;
+    return (size_t)E * TW * 8 + (size_t)S * 8 + (size_t)T * k * 8 + (size_t)E * 10 * 4;
 }
 
 cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s) {
-    const size_t smem = route_ctl_smem_bytes(p.T, p.k, p.E);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(route_ctl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
+    const size_t smem = route_ctl_smem_bytes(p.T, p.k, p.E, p.S);
+    static size_t smem_set = 0;
+    if (smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(route_ctl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        smem_set = smem;
     }
     route_ctl_kernel<<<1, CTL_THREADS, smem, s>>>(p);
     return cudaGetLastError();
