@@ -105,6 +105,11 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     int* s_cslot = s_vict + E;  // [E] radix path: candidates with stamp < tau
     unsigned* s_cst = reinterpret_cast<unsigned*>(s_cslot + E);  // [E]
 
+    if (tid == 0) {
+        sh.bad = 0;
+        sh.u = sh.h = sh.m = 0;
+    }
+    __syncthreads();
     // ---- issue every global read of the pass
     for (int s = tid; s < S; s += CTL_THREADS) {
         s_stamp[s] = p.stamps[s];
@@ -117,11 +122,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         s_slot[e] = -1;
     }
     for (int i = tid; i < E * TW; i += CTL_THREADS) s_tmask[i] = 0ull;
-    if (tid == 0) {
-        sh.bad = 0;
-        sh.u = sh.h = sh.m = 0;
-        sh.clk = *p.clock;
-    }
+    if (tid == 0) sh.clk = *p.clock;
 
     // ---- a1: routing (top-k + softmax gates), or the given top-k
     if (p.logits) {
