@@ -259,8 +259,10 @@ ft_status ft_get_counters(ft_ctx* ctx, ft_counters* out);
 /* Per-kernel device timing.  While enabled, the library records a CUDA event
  * pair around each of its own launches on the stream the launch uses;
  * ft_profile_read (syncs) sums the elapsed times per kernel id and clears the
- * records.  Enabling resets the sums.  Not for use inside stream capture.
- * ft_kernel_name returns a static name for an id (NULL if unknown). */
+ * records.  Enabling resets the sums.  Inside a stream capture the records
+ * become external event-record nodes of the graph: read the profile after the
+ * graph ran once.  ft_kernel_name returns a static name for an id (NULL if
+ * unknown). */
 ft_status ft_profile_enable(ft_ctx* ctx, int32_t enable);
 ft_status ft_profile_read(ft_ctx* ctx, ft_profile* out);
 const char* ft_kernel_name(int32_t id);

@@ -69,7 +69,6 @@ __global__ void __launch_bounds__(512) fill_kernel(FillParams p) {
 
 __device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
 
-__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
@@ -108,12 +107,23 @@ __device__ void drain_ring(uint64_t* full, int issued, int nst, unsigned* err) {
         if (it >= 0) ft::mbar_wait(&full[it % nst], (it / nst) & 1, err);
 }
 
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(ft::smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(ft::smem_addr(p)) : "memory");
+    return v;
+}
+
 __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_gdone;
     const int H = p.H, F = p.F, T = p.T, k = p.k;
     const int nst = p.nstage;
     const unsigned slot_bytes = p.stage_bytes;
     const int ugpu = p.info[INFO_UGPU];
+    const int nasg = p.info[INFO_NASSIGN];
     const int G = gridDim.x, c = blockIdx.x;
     const int cpe = F / FPC;  // phase-A chunks per expert
     const int NA = ugpu * cpe;
@@ -122,6 +132,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     const int R = r1 - r0;
     const int RMAX = (H + G - 1) / G;
     const int nB = R > 0 ? ugpu : 0;
+    const int TK = T * k;
 
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -132,10 +143,18 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     __nv_bfloat16* x_s = reinterpret_cast<__nv_bfloat16*>(smem + o);
     if (x_in_smem) o += (xbytes + 127) & ~(size_t)127;
     float* o_s = reinterpret_cast<float*>(smem + o);  // [T*k][RMAX] expert outputs of my rows
-    o += ((size_t)T * k * RMAX * 4 + 127) & ~(size_t)127;
+    o += ((size_t)TK * RMAX * 4 + 127) & ~(size_t)127;
+    // worklist metadata, staged once
+    int* m_off = reinterpret_cast<int*>(smem + o);    // [TK+1] entry offsets (ugpu+1 used)
+    int* m_slot = m_off + TK + 1;                      // [TK]   entry slots (ugpu used)
+    int* m_tok = m_slot + TK;                          // [TK]   token of each assignment
+    float* m_gate = reinterpret_cast<float*>(m_tok + TK);  // [TK]
+    int* m_pos = reinterpret_cast<int*>(m_gate + TK);      // [TK]   assignment of (t, j)
+    o += ((size_t)(5 * TK + 1) * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
     const __nv_bfloat16* xsrc = x_in_smem ? x_s : p.x;
     const unsigned rowbytes = (unsigned)H * 2u;
+    const unsigned wpart = ((unsigned)RMAX * F * 2u + 127u) & ~127u;  // h rows follow the W_d rows
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -143,7 +162,15 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             ft::mbar_init(&empty[s], CONSUMER_WARPS);
         }
         ft::mbar_fence_init();
+        s_gdone = 0;
     }
+    for (int i = tid; i <= ugpu; i += EXPERT_THREADS) m_off[i] = p.wl_off[i];
+    for (int i = tid; i < ugpu; i += EXPERT_THREADS) m_slot[i] = p.wl_slot[i];
+    for (int i = tid; i < nasg; i += EXPERT_THREADS) {
+        m_tok[i] = p.as_tok[i];
+        m_gate[i] = p.as_gate[i];
+    }
+    for (int i = tid; i < TK; i += EXPERT_THREADS) m_pos[i] = p.out_pos[i];
     if (x_in_smem)
         for (int i = tid; i < (int)(xbytes / 16); i += EXPERT_THREADS)
             reinterpret_cast<uint4*>(x_s)[i] = reinterpret_cast<const uint4*>(p.x)[i];
@@ -160,7 +187,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
                 const int ent = a / cpe;
                 const int f0 = (a - ent * cpe) * FPC;
-                const uint8_t* rec = p.slot_pool + (size_t)p.wl_slot[ent] * p.rb;
+                const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
                 const int grp = f0 >> 4, i = f0 & 15;
                 unsigned char* dst = ring + (size_t)st * slot_bytes;
                 ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * rowbytes);
@@ -168,14 +195,45 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 ft::bulk_g2s_hint(dst + (size_t)FPC * rowbytes, rec + (size_t)(grp * 32 + 16 + i) * rowbytes,
                                   FPC * rowbytes, &full[st], pol);
             }
+            // phase B: W_d rows stream ahead of the grid barrier; the h rows of
+            // an entry are copied once every CTA has written its h.
             const unsigned wb = (unsigned)R * F * 2u;
+            const int pre = nB < nst ? nB : nst;
+            const int itB = it;
+            bool gdone = false;
             for (int e = 0; e < nB && ok; ++e, ++it) {
                 const int st = it % nst;
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
-                const uint8_t* wd = p.slot_pool + (size_t)p.wl_slot[e] * p.rb + (size_t)2 * F * H * 2 +
-                                    (size_t)r0 * F * 2;
-                ft::mbar_arrive_expect_tx(&full[st], wb);
-                ft::bulk_g2s_hint(ring + (size_t)st * slot_bytes, wd, wb, &full[st], pol);
+                const int off = m_off[e];
+                const unsigned hb = (unsigned)(m_off[e + 1] - off) * F * 4u;
+                unsigned char* dst = ring + (size_t)st * slot_bytes;
+                const uint8_t* wd = p.slot_pool + (size_t)m_slot[e] * p.rb + (size_t)2 * F * H * 2 + (size_t)r0 * F * 2;
+                ft::mbar_arrive_expect_tx(&full[st], wb + hb);
+                ft::bulk_g2s_hint(dst, wd, wb, &full[st], pol);
+                if (e == pre - 1 || e >= pre) {
+                    if (!gdone) {
+                        const uint64_t t0 = ft::globaltimer();
+                        while (!ld_acquire_cta(&s_gdone)) {
+                            if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                                atomicOr(p.err, FT_DEVERR_TIMEOUT);
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        gdone = true;
+                        for (int e2 = 0; e2 < pre; ++e2) {  // deferred h rows of the prefetched entries
+                            const int st2 = (itB + e2) % nst;
+                            const int off2 = m_off[e2];
+                            const unsigned hb2 = (unsigned)(m_off[e2 + 1] - off2) * F * 4u;
+                            ft::bulk_g2s(ring + (size_t)st2 * slot_bytes + wpart, p.hbuf + (size_t)off2 * F, hb2,
+                                         &full[st2]);
+                        }
+                    } else {
+                        ft::bulk_g2s(dst + wpart, p.hbuf + (size_t)off * F, hb, &full[st]);
+                    }
+                }
             }
             drain_ring(full, it, nst, p.err);
         }
@@ -193,8 +251,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         failed = !ok;
         const int ent = a / cpe;
         const int f = (a - ent * cpe) * FPC + wid;
-        const int off = p.wl_off[ent];
-        const int ntok = p.wl_off[ent + 1] - off;
+        const int off = m_off[ent];
+        const int ntok = m_off[ent + 1] - off;
         const uint4* wg = reinterpret_cast<const uint4*>(ring + (size_t)st * slot_bytes + (size_t)wid * rowbytes);
         const uint4* wu = reinterpret_cast<const uint4*>(ring + (size_t)st * slot_bytes +
                                                          (size_t)(FPC + wid) * rowbytes);
@@ -202,7 +260,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             const int ng = min(MAXTOK, ntok - g0);
             int tk[MAXTOK];
 #pragma unroll
-            for (int n = 0; n < MAXTOK; ++n) tk[n] = n < ng ? p.as_tok[off + g0 + n] : 0;
+            for (int n = 0; n < MAXTOK; ++n) tk[n] = n < ng ? m_tok[off + g0 + n] : 0;
             float ag[MAXTOK], au[MAXTOK];
 #pragma unroll
             for (int n = 0; n < MAXTOK; ++n) ag[n] = au[n] = 0.f;
@@ -243,7 +301,10 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
 
     // every h of this layer is written before any CTA starts phase B
     ft::named_bar_sync(1, CONSUMERS);
-    if (tid == 0) grid_barrier(p.gbar, (unsigned)G, p.err);
+    if (tid == 0) {
+        grid_barrier(p.gbar, (unsigned)G, p.err);
+        st_release_cta(&s_gdone, 1);
+    }
     ft::named_bar_sync(1, CONSUMERS);
 
     // ---------------------------------------------------- phase B: down rows
@@ -251,9 +312,10 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         const int st = it % nst;
         const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
         failed = !ok;
-        const int off = p.wl_off[e];
-        const int ntok = p.wl_off[e + 1] - off;
+        const int off = m_off[e];
+        const int ntok = m_off[e + 1] - off;
         const unsigned char* sb = ring + (size_t)st * slot_bytes;
+        const float* hs = reinterpret_cast<const float*>(sb + wpart);
         for (int rl = wid; rl < R && ok; rl += CONSUMER_WARPS) {
             const uint4* wrow = reinterpret_cast<const uint4*>(sb + (size_t)rl * F * 2);
             for (int g0 = 0; g0 < ntok; g0 += MAXTOK) {
@@ -267,8 +329,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
 #pragma unroll
                     for (int n = 0; n < MAXTOK; ++n) {
                         if (n < ng) {
-                            const float* hp = p.hbuf + (size_t)(off + g0 + n) * F + v * 8;
-                            const float4 x0 = ldcg4(hp), x1 = ldcg4(hp + 4);
+                            const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)(g0 + n) * F + v * 8);
+                            const float4 x0 = hp[0], x1 = hp[1];
                             float s = acc[n];
                             s = fmaf(w8[0], x0.x, s);
                             s = fmaf(w8[1], x0.y, s);
@@ -300,8 +362,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         const int t = idx / R, rl = idx - t * R;
         float acc = 0.f;
         for (int j = 0; j < k; ++j) {
-            const int pos = p.out_pos[t * k + j];
-            if (pos >= 0) acc = fmaf(p.as_gate[pos], o_s[(size_t)pos * RMAX + rl], acc);
+            const int pos = m_pos[t * k + j];
+            if (pos >= 0) acc = fmaf(m_gate[pos], o_s[(size_t)pos * RMAX + rl], acc);
         }
         const size_t oi = (size_t)t * H + r0 + rl;
         if (p.partial_C) acc += p.partial_C[oi];
@@ -319,16 +381,18 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
 static constexpr size_t kSmemLimit = 227 * 1024;
 
 // Shared-memory plan: barriers, x (if it fits in 64 KiB), the per-CTA output
-// block, then as many ring slots as fit (at most 4).  A slot holds one phase-A
-// chunk (16 rows of H) or one phase-B stage (R rows of F).
+// block, the worklist metadata, then as many ring slots as fit (at most 4).  A
+// slot holds one phase-A chunk (16 rows of H) or one phase-B stage (R rows of
+// W_d followed by the h rows of the entry's tokens).
 cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     const int G = num_sms;
     const int RMAX = (p.H + G - 1) / G;
     const size_t xbytes = (size_t)p.T * p.H * 2;
+    const size_t TK = (size_t)p.T * p.k;
     const size_t head = HEAD + (xbytes <= 65536 ? ((xbytes + 127) & ~(size_t)127) : 0) +
-                        (((size_t)p.T * p.k * RMAX * 4 + 127) & ~(size_t)127);
+                        ((TK * RMAX * 4 + 127) & ~(size_t)127) + (((5 * TK + 1) * 4 + 127) & ~(size_t)127);
     size_t slot = (size_t)2 * FPC * p.H * 2;
-    const size_t down = (size_t)RMAX * p.F * 2;
+    const size_t down = (((size_t)RMAX * p.F * 2 + 127) & ~(size_t)127) + (size_t)p.T * p.F * 4;
     if (down > slot) slot = down;
     slot = (slot + 127) & ~(size_t)127;
     if (head >= kSmemLimit) return cudaErrorInvalidValue;

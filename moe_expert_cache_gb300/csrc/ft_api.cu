@@ -80,6 +80,17 @@ cudaEvent_t prof_event(Profiler& pr) {
 }
 
 // Records an event pair around the launches made in its scope (profile on).
+// Inside a stream capture the records become external event-record nodes of
+// the graph, so they time every replay of the captured launch.
+inline void prof_record(cudaEvent_t e, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, s);
+}
+
 struct ProfScope {
     Profiler& pr;
     cudaStream_t s;
@@ -89,11 +100,11 @@ struct ProfScope {
         r.kid = kid;
         r.a = prof_event(pr);
         r.b = prof_event(pr);
-        if (r.a) cudaEventRecord(r.a, s);
+        if (r.a) prof_record(r.a, s);
     }
     ~ProfScope() {
         if (!pr.on || !r.a || !r.b) return;
-        cudaEventRecord(r.b, s);
+        prof_record(r.b, s);
         pr.pending.push_back(r);
     }
 };
