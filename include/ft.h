@@ -105,8 +105,9 @@ const char* ft_status_str(ft_status s);
  *                  F % 64 == 0 (H, F >= 64).
  *   S              number of slots (>= 1).  Prefill needs S >= 2E.
  *   fmt            FT_FMT_BF16 or FT_FMT_NVFP4 (record layout in ft_record_bytes).
- *   T_max          largest T of a decode call (ft_route_ctl), 1..256, and
- *                  T_max*k <= 4096.
+ *   T_max          largest T of a decode call (ft_route_ctl), 1..256, with
+ *                  T_max*k <= 4096 and T_max*H <= 32768 (the tokens of a
+ *                  decode call are staged in shared memory).
  *   T_prefill_max  largest T of a prefill layer call; 0 disables prefill (no
  *                  prefill scratch is allocated).
  *   host_pool      HOST address of the caller's expert pool: L*E records of
@@ -264,6 +265,10 @@ ft_status ft_get_counters(ft_ctx* ctx, ft_counters* out);
  * graph ran once.  ft_kernel_name returns a static name for an id (NULL if
  * unknown). */
 ft_status ft_profile_enable(ft_ctx* ctx, int32_t enable);
+/* Suspend (paused != 0) or resume recording without synchronising or
+ * resetting: usable between the calls of a stream capture to time a sample
+ * of the captured launches. */
+ft_status ft_profile_pause(ft_ctx* ctx, int32_t paused);
 ft_status ft_profile_read(ft_ctx* ctx, ft_profile* out);
 const char* ft_kernel_name(int32_t id);
 

@@ -68,6 +68,7 @@ _SIGS = {
     "ft_get_counters": (_c_int, [_c_p, ctypes.POINTER(Counters)]),
     "ft_profile_enable": (_c_int, [_c_p, _c_int]),
     "ft_profile_read": (_c_int, [_c_p, ctypes.POINTER(Profile)]),
+    "ft_profile_pause": (_c_int, [_c_p, _c_int]),
     "ft_kernel_name": (ctypes.c_char_p, [_c_int]),
     "ft_num_slots": (_c_int, [_c_p]),
     "ft_get_status": (_c_int, [_c_p]),
@@ -167,6 +168,10 @@ def get_counters(ctx, out) -> int:
 
 def profile_enable(ctx, enable) -> int:
     return load().ft_profile_enable(ctx, enable)
+
+
+def profile_pause(ctx, paused) -> int:
+    return load().ft_profile_pause(ctx, paused)
 
 
 def profile_read(ctx, out) -> int:
@@ -296,6 +301,9 @@ class Context:
 
     def profile_enable(self, on: bool = True):
         _check(profile_enable(self.h, 1 if on else 0), "ft_profile_enable")
+
+    def profile_pause(self, paused: bool):
+        _check(profile_pause(self.h, 1 if paused else 0), "ft_profile_pause")
 
     def profile_read(self) -> dict:
         pr = Profile()

@@ -35,7 +35,6 @@ constexpr int CONSUMER_WARPS = 8;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;
 constexpr int EXPERT_THREADS = CONSUMERS + 32;  // + one producer warp
 constexpr int FPC = CONSUMER_WARPS;             // features per phase-A chunk
-constexpr int MAXTOK = 16;                      // tokens per register block
 constexpr size_t HEAD = 256;                    // barrier area
 
 // ------------------------------------------------------------------- fill
@@ -107,6 +106,140 @@ __device__ void drain_ring(uint64_t* full, int issued, int nst, unsigned* err) {
         if (it >= 0) ft::mbar_wait(&full[it % nst], (it / nst) & 1, err);
 }
 
+// ---- phase A inner loop: gate and up dot products of one feature (full K)
+// for NT tokens.  x is read from shared memory as fp32 (XF) or bf16.
+template <int NT, bool XF>
+__device__ __forceinline__ void gu_dots(const uint4* __restrict__ wg, const uint4* __restrict__ wu,
+                                        const void* xs, const int* tk, int H, int lane, float* ag, float* au) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
+    const int nv = H >> 3;
+#pragma unroll 4
+    for (int v = lane; v < nv; v += 32) {
+        float g8[8], u8[8];
+        ft::bf16x8_to_f32(wg[v], g8);
+        ft::bf16x8_to_f32(wu[v], u8);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            float x8[8];
+            if (XF) {
+                const float4* xp = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) +
+                                                                   (size_t)tk[n] * H + v * 8);
+                const float4 x0 = xp[0], x1 = xp[1];
+                x8[0] = x0.x; x8[1] = x0.y; x8[2] = x0.z; x8[3] = x0.w;
+                x8[4] = x1.x; x8[5] = x1.y; x8[6] = x1.z; x8[7] = x1.w;
+            } else {
+                ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(xs) +
+                                                                 (size_t)tk[n] * H)[v], x8);
+            }
+            float sg = ag[n], su = au[n];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                sg = fmaf(g8[q], x8[q], sg);
+                su = fmaf(u8[q], x8[q], su);
+            }
+            ag[n] = sg;
+            au[n] = su;
+        }
+    }
+}
+
+template <int NT, bool XF>
+__device__ __forceinline__ void gu_group(const uint4* wg, const uint4* wu, const void* xs, const int* m_tok, int off,
+                                         int g0, int H, int F, int f, int lane, float* hbuf) {
+    int tk[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) tk[n] = m_tok[off + g0 + n];
+    float ag[NT], au[NT];
+    gu_dots<NT, XF>(wg, wu, xs, tk, H, lane, ag, au);
+    float mine = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const float sg = ft::warp_sum(ag[n]);
+        const float su = ft::warp_sum(au[n]);
+        if (lane == n) mine = silu_mul(sg, su);
+    }
+    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + f] = mine;
+}
+
+template <bool XF>
+__device__ __forceinline__ void gu_feature(const uint4* wg, const uint4* wu, const void* xs, const int* m_tok,
+                                           int off, int ntok, int H, int F, int f, int lane, float* hbuf) {
+    int g0 = 0;
+    while (g0 < ntok) {
+        const int rem = ntok - g0;
+        if (rem >= 8) {
+            gu_group<8, XF>(wg, wu, xs, m_tok, off, g0, H, F, f, lane, hbuf);
+            g0 += 8;
+        } else if (rem >= 4) {
+            gu_group<4, XF>(wg, wu, xs, m_tok, off, g0, H, F, f, lane, hbuf);
+            g0 += 4;
+        } else if (rem >= 2) {
+            gu_group<2, XF>(wg, wu, xs, m_tok, off, g0, H, F, f, lane, hbuf);
+            g0 += 2;
+        } else {
+            gu_group<1, XF>(wg, wu, xs, m_tok, off, g0, H, F, f, lane, hbuf);
+            g0 += 1;
+        }
+    }
+}
+
+// ---- phase B inner loop: one W_d row against NT token rows of h (fp32, smem)
+template <int NT>
+__device__ __forceinline__ void down_group(const uint4* __restrict__ wrow, const float* hs, int g0, int F, int lane,
+                                           float* o_s, int obase, int RMAX, int rl) {
+    float acc[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n] = 0.f;
+    const int nv = F >> 3;
+#pragma unroll 3
+    for (int v = lane; v < nv; v += 32) {
+        float w8[8];
+        ft::bf16x8_to_f32(wrow[v], w8);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)(g0 + n) * F + v * 8);
+            const float4 x0 = hp[0], x1 = hp[1];
+            float s = acc[n];
+            s = fmaf(w8[0], x0.x, s);
+            s = fmaf(w8[1], x0.y, s);
+            s = fmaf(w8[2], x0.z, s);
+            s = fmaf(w8[3], x0.w, s);
+            s = fmaf(w8[4], x1.x, s);
+            s = fmaf(w8[5], x1.y, s);
+            s = fmaf(w8[6], x1.z, s);
+            s = fmaf(w8[7], x1.w, s);
+            acc[n] = s;
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const float sv = ft::warp_sum(acc[n]);
+        if (lane == 0) o_s[(size_t)(obase + g0 + n) * RMAX + rl] = sv;
+    }
+}
+
+__device__ __forceinline__ void down_row(const uint4* wrow, const float* hs, int ntok, int F, int lane, float* o_s,
+                                         int off, int RMAX, int rl) {
+    int g0 = 0;
+    while (g0 < ntok) {
+        const int rem = ntok - g0;
+        if (rem >= 8) {
+            down_group<8>(wrow, hs, g0, F, lane, o_s, off, RMAX, rl);
+            g0 += 8;
+        } else if (rem >= 4) {
+            down_group<4>(wrow, hs, g0, F, lane, o_s, off, RMAX, rl);
+            g0 += 4;
+        } else if (rem >= 2) {
+            down_group<2>(wrow, hs, g0, F, lane, o_s, off, RMAX, rl);
+            g0 += 2;
+        } else {
+            down_group<1>(wrow, hs, g0, F, lane, o_s, off, RMAX, rl);
+            g0 += 1;
+        }
+    }
+}
+
 __device__ __forceinline__ void st_release_cta(int* p, int v) {
     asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(ft::smem_addr(p)), "r"(v) : "memory");
 }
@@ -137,11 +270,11 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + nst;
-    const size_t xbytes = (size_t)T * H * 2;
-    const bool x_in_smem = xbytes <= 65536;
+    const bool xf32 = (size_t)T * H * 4 <= 65536;  // x kept as fp32 in shared memory
+    const size_t xbytes = (size_t)T * H * (xf32 ? 4 : 2);
     size_t o = HEAD;
-    __nv_bfloat16* x_s = reinterpret_cast<__nv_bfloat16*>(smem + o);
-    if (x_in_smem) o += (xbytes + 127) & ~(size_t)127;
+    void* x_s = smem + o;
+    o += (xbytes + 127) & ~(size_t)127;
     float* o_s = reinterpret_cast<float*>(smem + o);  // [T*k][RMAX] expert outputs of my rows
     o += ((size_t)TK * RMAX * 4 + 127) & ~(size_t)127;
     // worklist metadata, staged once
@@ -152,7 +285,6 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     int* m_pos = reinterpret_cast<int*>(m_gate + TK);      // [TK]   assignment of (t, j)
     o += ((size_t)(5 * TK + 1) * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
-    const __nv_bfloat16* xsrc = x_in_smem ? x_s : p.x;
     const unsigned rowbytes = (unsigned)H * 2u;
     const unsigned wpart = ((unsigned)RMAX * F * 2u + 127u) & ~127u;  // h rows follow the W_d rows
 
@@ -171,9 +303,17 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         m_gate[i] = p.as_gate[i];
     }
     for (int i = tid; i < TK; i += EXPERT_THREADS) m_pos[i] = p.out_pos[i];
-    if (x_in_smem)
+    if (xf32) {
+        for (int i = tid; i < T * H / 8; i += EXPERT_THREADS) {
+            float f8[8];
+            ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
+            reinterpret_cast<float4*>(x_s)[2 * i] = make_float4(f8[0], f8[1], f8[2], f8[3]);
+            reinterpret_cast<float4*>(x_s)[2 * i + 1] = make_float4(f8[4], f8[5], f8[6], f8[7]);
+        }
+    } else {
         for (int i = tid; i < (int)(xbytes / 16); i += EXPERT_THREADS)
             reinterpret_cast<uint4*>(x_s)[i] = reinterpret_cast<const uint4*>(p.x)[i];
+    }
     __syncthreads();
 
     // ------------------------------------------------------------ producer
@@ -256,44 +396,11 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         const uint4* wg = reinterpret_cast<const uint4*>(ring + (size_t)st * slot_bytes + (size_t)wid * rowbytes);
         const uint4* wu = reinterpret_cast<const uint4*>(ring + (size_t)st * slot_bytes +
                                                          (size_t)(FPC + wid) * rowbytes);
-        for (int g0 = 0; g0 < ntok && ok; g0 += MAXTOK) {
-            const int ng = min(MAXTOK, ntok - g0);
-            int tk[MAXTOK];
-#pragma unroll
-            for (int n = 0; n < MAXTOK; ++n) tk[n] = n < ng ? m_tok[off + g0 + n] : 0;
-            float ag[MAXTOK], au[MAXTOK];
-#pragma unroll
-            for (int n = 0; n < MAXTOK; ++n) ag[n] = au[n] = 0.f;
-            for (int v = lane; v < H / 8; v += 32) {
-                float g8[8], u8[8];
-                ft::bf16x8_to_f32(wg[v], g8);
-                ft::bf16x8_to_f32(wu[v], u8);
-#pragma unroll
-                for (int n = 0; n < MAXTOK; ++n) {
-                    if (n < ng) {
-                        float x8[8];
-                        ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(xsrc + (size_t)tk[n] * H)[v], x8);
-                        float sg = ag[n], su = au[n];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            sg = fmaf(g8[q], x8[q], sg);
-                            su = fmaf(u8[q], x8[q], su);
-                        }
-                        ag[n] = sg;
-                        au[n] = su;
-                    }
-                }
-            }
-            float mine = 0.f;
-#pragma unroll
-            for (int n = 0; n < MAXTOK; ++n) {
-                if (n < ng) {
-                    const float sg = ft::warp_sum(ag[n]);
-                    const float su = ft::warp_sum(au[n]);
-                    if (lane == n) mine = silu_mul(sg, su);
-                }
-            }
-            if (lane < ng) p.hbuf[(size_t)(off + g0 + lane) * F + f] = mine;
+        if (ok) {
+            if (xf32)
+                gu_feature<true>(wg, wu, x_s, m_tok, off, ntok, H, F, f, lane, p.hbuf);
+            else
+                gu_feature<false>(wg, wu, x_s, m_tok, off, ntok, H, F, f, lane, p.hbuf);
         }
         __syncwarp();
         if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
@@ -316,43 +423,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         const int ntok = m_off[e + 1] - off;
         const unsigned char* sb = ring + (size_t)st * slot_bytes;
         const float* hs = reinterpret_cast<const float*>(sb + wpart);
-        for (int rl = wid; rl < R && ok; rl += CONSUMER_WARPS) {
-            const uint4* wrow = reinterpret_cast<const uint4*>(sb + (size_t)rl * F * 2);
-            for (int g0 = 0; g0 < ntok; g0 += MAXTOK) {
-                const int ng = min(MAXTOK, ntok - g0);
-                float acc[MAXTOK];
-#pragma unroll
-                for (int n = 0; n < MAXTOK; ++n) acc[n] = 0.f;
-                for (int v = lane; v < F / 8; v += 32) {
-                    float w8[8];
-                    ft::bf16x8_to_f32(wrow[v], w8);
-#pragma unroll
-                    for (int n = 0; n < MAXTOK; ++n) {
-                        if (n < ng) {
-                            const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)(g0 + n) * F + v * 8);
-                            const float4 x0 = hp[0], x1 = hp[1];
-                            float s = acc[n];
-                            s = fmaf(w8[0], x0.x, s);
-                            s = fmaf(w8[1], x0.y, s);
-                            s = fmaf(w8[2], x0.z, s);
-                            s = fmaf(w8[3], x0.w, s);
-                            s = fmaf(w8[4], x1.x, s);
-                            s = fmaf(w8[5], x1.y, s);
-                            s = fmaf(w8[6], x1.z, s);
-                            s = fmaf(w8[7], x1.w, s);
-                            acc[n] = s;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int n = 0; n < MAXTOK; ++n) {
-                    if (n < ng) {
-                        const float s = ft::warp_sum(acc[n]);
-                        if (lane == 0) o_s[(size_t)(off + g0 + n) * RMAX + rl] = s;
-                    }
-                }
-            }
-        }
+        for (int rl = wid; rl < R && ok; rl += CONSUMER_WARPS)
+            down_row(reinterpret_cast<const uint4*>(sb + (size_t)rl * F * 2), hs, ntok, F, lane, o_s, off, RMAX, rl);
         __syncwarp();
         if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
     }
@@ -387,9 +459,10 @@ static constexpr size_t kSmemLimit = 227 * 1024;
 cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     const int G = num_sms;
     const int RMAX = (p.H + G - 1) / G;
-    const size_t xbytes = (size_t)p.T * p.H * 2;
+    const bool xf32 = (size_t)p.T * p.H * 4 <= 65536;
+    const size_t xbytes = (size_t)p.T * p.H * (xf32 ? 4 : 2);
     const size_t TK = (size_t)p.T * p.k;
-    const size_t head = HEAD + (xbytes <= 65536 ? ((xbytes + 127) & ~(size_t)127) : 0) +
+    const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) +
                         ((TK * RMAX * 4 + 127) & ~(size_t)127) + (((5 * TK + 1) * 4 + 127) & ~(size_t)127);
     size_t slot = (size_t)2 * FPC * p.H * 2;
     const size_t down = (((size_t)RMAX * p.F * 2 + 127) & ~(size_t)127) + (size_t)p.T * p.F * 4;

@@ -22,6 +22,7 @@ struct ProfRec {
 };
 struct Profiler {
     bool on = false;
+    bool paused = false;
     std::vector<cudaEvent_t> pool;
     std::vector<ProfRec> pending;
     double ms[FT_K_COUNT] = {};
@@ -95,15 +96,17 @@ struct ProfScope {
     Profiler& pr;
     cudaStream_t s;
     ProfRec r{};
+    bool rec = false;
     ProfScope(Profiler& p, int kid, cudaStream_t st) : pr(p), s(st) {
-        if (!pr.on) return;
+        if (!pr.on || pr.paused) return;
+        rec = true;
         r.kid = kid;
         r.a = prof_event(pr);
         r.b = prof_event(pr);
         if (r.a) prof_record(r.a, s);
     }
     ~ProfScope() {
-        if (!pr.on || !r.a || !r.b) return;
+        if (!rec || !r.a || !r.b) return;
         prof_record(r.b, s);
         pr.pending.push_back(r);
     }
@@ -170,6 +173,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
         return FT_ERR_ARG;
     if (fmt != FT_FMT_BF16) return FT_ERR_ARG;  // NVFP4 banks are accepted by a later version
     if (route_ctl_smem_bytes(T_max, k, E, S) > kCtlSmemMax) return FT_ERR_ARG;
+    if ((size_t)T_max * H * 2 > 65536) return FT_ERR_ARG;  // decode tokens are staged in shared memory
     ft_ctx* c = new (std::nothrow) ft_ctx();
     if (!c) return FT_ERR_OOM;
     c->L = L; c->E = E; c->k = k; c->H = H; c->F = F; c->S = S; c->fmt = fmt;
@@ -482,6 +486,13 @@ ft_status ft_profile_enable(ft_ctx* c, int32_t enable) {
         c->prof.n[i] = 0;
     }
     c->prof.on = enable != 0;
+    c->prof.paused = false;
+    return FT_OK;
+}
+
+ft_status ft_profile_pause(ft_ctx* c, int32_t paused) {
+    if (!c) return FT_ERR_ARG;
+    c->prof.paused = paused != 0;
     return FT_OK;
 }
 
