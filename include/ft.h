@@ -230,6 +230,46 @@ ft_status ft_prefill_layer(ft_ctx* ctx, int32_t buffer, int32_t layer, int32_t n
  */
 ft_status ft_cache_resize(ft_ctx* ctx, int32_t S_new);
 
+/*
+ * ft_expert_ffn_noalloc -- the decode expert FFN without a context and
+ * without allocating anything.  The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory once they
+ * run: code inside a CUDA graph capture, where allocation calls are illegal;
+ * engines that carve all device memory into their own pools at start-up; and
+ * latency-critical paths that cannot afford the synchronisation of
+ * cudaMalloc / cudaFree.  ft_layer_init allocates, so such callers use this.
+ *
+ * For every route (t, j) with route_records[t*k+j] >= 0 it computes
+ * FFN(x_t) = W_d (SiLU(W_g x_t) * (W_u x_t)) over that BF16 record and writes
+ * y_t = sum_j gates[t*k+j] FFN_{route_records[t*k+j]}(x_t) (j ascending) +
+ * partial_C_t -- the same kernel and arithmetic as ft_moe_forward.
+ *
+ *   records        DEVICE array of n_records BF16 records (ft_record_bytes
+ *                  layout), 16-byte aligned; read only.
+ *   route_records  DEVICE int32 [T, k]: record index of each route, or -1 for a
+ *                  route computed elsewhere (the CPU set).  An index outside
+ *                  [-1, n_records) is treated as -1.
+ *   gates          DEVICE fp32 [T, k].
+ *   x              DEVICE bf16 [T, H];  partial_C DEVICE fp32 [T, H] or NULL;
+ *   y              DEVICE fp32 [T, H], not aliasing x or partial_C.
+ *   T, k, H, F     T*k <= 1024, k <= 16, H and F multiples of 64, T*H <= 32768,
+ *                  and 65536 + T*k*F*4 <= FT_NOALLOC_SCRATCH_BYTES (else
+ *                  FT_ERR_ARG).
+ *   stream         cudaStream_t to run on (NULL = legacy default stream).
+ * Scratch: one file-scope device array of FT_NOALLOC_SCRATCH_BYTES per device
+ * that loads the library, held until the process exits; no cudaMalloc,
+ * cudaFree or allocating library call is made.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call shares
+ * the array and leaves its contents behind; each call rewrites what it reads.
+ * Calls that overlap on the GPU (several streams or host threads) race on the
+ * array: serialise them.  Async; returns FT_ERR_ARG or FT_ERR_CUDA on failure.
+ */
+#define FT_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u + 65536u)
+ft_status ft_expert_ffn_noalloc(const void* records, int32_t n_records, const int32_t* route_records,
+                                const float* gates, const void* x, const float* partial_C, float* y,
+                                int32_t T, int32_t k, int32_t H, int32_t F, void* stream);
+
 /* ---- observability and test surface (all sync) ------------------------- */
 
 /* Copy the control state to HOST buffers: slot_for_id [L*E], id_for_slot [S],

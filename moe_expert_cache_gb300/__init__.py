@@ -71,6 +71,8 @@ _SIGS = {
     "ft_profile_pause": (_c_int, [_c_p, _c_int]),
     "ft_kernel_name": (ctypes.c_char_p, [_c_int]),
     "ft_num_slots": (_c_int, [_c_p]),
+    "ft_expert_ffn_noalloc": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
+                                       _c_p]),
     "ft_get_status": (_c_int, [_c_p]),
     "ft_destroy": (None, [_c_p]),
 }
@@ -181,6 +183,12 @@ def profile_read(ctx, out) -> int:
 def kernel_name(kid: int):
     n = load().ft_kernel_name(kid)
     return n.decode() if n else None
+
+
+def expert_ffn_noalloc(records, n_records, route_records, gates, x, partial_C, y, T, k, H, F, stream=None) -> int:
+    """Context-free decode expert FFN that allocates nothing (see include/ft.h)."""
+    return load().ft_expert_ffn_noalloc(records, n_records, route_records, gates, x, partial_C, y, T, k, H, F,
+                                        stream)
 
 
 def num_slots(ctx) -> int:
