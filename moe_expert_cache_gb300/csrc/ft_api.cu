@@ -174,6 +174,9 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     if (fmt != FT_FMT_BF16) return FT_ERR_ARG;  // NVFP4 banks are accepted by a later version
     if (route_ctl_smem_bytes(T_max, k, E, S) > kCtlSmemMax) return FT_ERR_ARG;
     if ((size_t)T_max * H * 2 > 65536) return FT_ERR_ARG;  // decode tokens are staged in shared memory
+    // prefill: 256-column GEMM tiles over 2F and H, top-k of at most 256 logits
+    if (T_prefill_max > 0 && (H % 256 || (2 * F) % 256 || E > 256 || (size_t)T_prefill_max * k > (1u << 30)))
+        return FT_ERR_ARG;
     ft_ctx* c = new (std::nothrow) ft_ctx();
     if (!c) return FT_ERR_OOM;
     c->L = L; c->E = E; c->k = k; c->H = H; c->F = F; c->S = S; c->fmt = fmt;
@@ -254,6 +257,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
         st = prefill_alloc(c->pf, T_prefill_max, k, H, F, E);
         if (st != FT_OK) return fail(st);
     }
+    c->pf.E = E;
     INIT_CUDA(cudaDeviceSynchronize());
 #undef INIT_CUDA
     *out = c;
@@ -518,7 +522,7 @@ ft_status ft_profile_read(ft_ctx* c, ft_profile* out) {
 
 const char* ft_kernel_name(int32_t id) {
     static const char* names[FT_K_COUNT] = {"route_ctl", "fill", "expert_ffn", nullptr, "pf_route",
-                                            "pf_permute", "pf_gemm1_swiglu", "pf_gemm2", "pf_combine", "pf_h2d"};
+                                            "pf_permute_gather", "pf_gemm1_swiglu", "pf_gemm2", "pf_combine", "pf_h2d"};
     return (id >= 0 && id < FT_K_COUNT) ? names[id] : nullptr;
 }
 
@@ -553,14 +557,87 @@ ft_status ft_prefill_begin(ft_ctx* c, int32_t layer) {
     if (!c || layer < 0 || layer >= c->L) return FT_ERR_ARG;
     if (c->T_prefill_max <= 0 || c->pf.open) return FT_ERR_STATE;
     if (c->S < 2 * c->E) return FT_ERR_CAPACITY;
-    return FT_ERR_STATE;  // prefill kernels are added by the prefill translation unit
+    if (c->pf.maps_pool != c->slot_pool) {
+        const ft_status st = prefill_set_pool(c->pf, c->slot_pool, c->rb);
+        if (st != FT_OK) return st;
+    }
+    PrefillState& pf = c->pf;
+    cudaStream_t ts = c->ts ? c->ts : c->cs;
+    const size_t layer_bytes = (size_t)c->E * c->rb;
+    // buffer 0: clear its owners after earlier decode work, then the begin
+    // fence orders the copy after everything enqueued so far on compute
+    FT_CUDA(launch_pf_invalidate(0, c->E, c->slot_for_id, c->id_for_slot, c->stamps, c->cs));
+    FT_CUDA(cudaEventRecord(pf.fence, c->cs));
+    FT_CUDA(cudaStreamWaitEvent(ts, pf.fence, 0));
+    {
+        ProfScope ps(c->prof, FT_K_PF_H2D, ts);
+        FT_CUDA(cudaMemcpyAsync(c->slot_pool, static_cast<const uint8_t*>(c->host_pool) + (size_t)layer * layer_bytes,
+                                layer_bytes, cudaMemcpyHostToDevice, ts));
+    }
+    FT_CUDA(cudaEventRecord(pf.loaded[0], ts));
+    pf.open = true;
+    pf.cur = 0;
+    pf.buf_layer[0] = layer;
+    pf.buf_layer[1] = -1;
+    c->have_ctl = false;
+    return FT_OK;
 }
 
-ft_status ft_prefill_layer(ft_ctx* c, int32_t buffer, int32_t layer, int32_t next_layer, int32_t T,
-                           const void* x, const float* logits, float* y) {
-    (void)buffer; (void)layer; (void)next_layer; (void)T; (void)x; (void)logits; (void)y;
-    if (!c) return FT_ERR_ARG;
-    return FT_ERR_STATE;
+ft_status ft_prefill_layer(ft_ctx* c, int32_t buffer, int32_t layer, int32_t next_layer, int32_t T, const void* x,
+                           const float* logits, float* y) {
+    if (!c || !x || !logits || !y) return FT_ERR_ARG;
+    PrefillState& pf = c->pf;
+    if (!pf.open) return FT_ERR_STATE;
+    if (buffer != pf.cur || layer != pf.buf_layer[buffer]) return FT_ERR_STATE;
+    if (T < 1 || T > c->T_prefill_max || next_layer < -1 || next_layer >= c->L) return FT_ERR_ARG;
+    cudaStream_t cs = c->cs, ts = c->ts ? c->ts : c->cs;
+    const int nb = buffer ^ 1;
+    const size_t layer_bytes = (size_t)c->E * c->rb;
+    if (next_layer >= 0) {
+        // the other buffer is released once the previous layer's GEMMs (earlier
+        // on compute) are done; its owners are cleared before it is overwritten
+        FT_CUDA(launch_pf_invalidate(nb * c->E, c->E, c->slot_for_id, c->id_for_slot, c->stamps, cs));
+        FT_CUDA(cudaEventRecord(pf.released[nb], cs));
+        FT_CUDA(cudaStreamWaitEvent(ts, pf.released[nb], 0));
+        {
+            ProfScope ps(c->prof, FT_K_PF_H2D, ts);
+            FT_CUDA(cudaMemcpyAsync(c->slot_pool + (size_t)nb * layer_bytes,
+                                    static_cast<const uint8_t*>(c->host_pool) + (size_t)next_layer * layer_bytes,
+                                    layer_bytes, cudaMemcpyHostToDevice, ts));
+        }
+        FT_CUDA(cudaEventRecord(pf.loaded[nb], ts));
+        pf.buf_layer[nb] = next_layer;
+    }
+    FT_CUDA(cudaStreamWaitEvent(cs, pf.loaded[buffer], 0));
+    {
+        ProfScope ps(c->prof, FT_K_PF_ROUTE, cs);
+        FT_CUDA(launch_pf_route(pf, logits, T, c->err, cs));
+    }
+    {
+        ProfScope ps(c->prof, FT_K_PF_PERMUTE, cs);
+        FT_CUDA(launch_pf_permute(pf, T, cs));
+        FT_CUDA(launch_pf_gather(pf, x, T, cs));
+    }
+    {
+        ProfScope ps(c->prof, FT_K_PF_GEMM1, cs);
+        FT_CUDA(launch_pf_gemm1(pf, buffer, c->num_sms, c->err, cs));
+    }
+    {
+        ProfScope ps(c->prof, FT_K_PF_GEMM2, cs);
+        FT_CUDA(launch_pf_gemm2(pf, buffer, c->num_sms, c->err, cs));
+    }
+    {
+        ProfScope ps(c->prof, FT_K_PF_COMBINE, cs);
+        FT_CUDA(launch_pf_combine(pf, T, y, cs));
+    }
+    if (next_layer < 0) {
+        pf.open = false;
+        pf.buf_layer[0] = pf.buf_layer[1] = -1;
+        pf.cur = 0;
+    } else {
+        pf.cur = nb;
+    }
+    return FT_OK;
 }
 
 }  // extern "C"
