@@ -16,6 +16,10 @@ stream, max over ranks.  Every step streams about 3.6 GB of expert weights, far 
 129 MB L2, so no explicit L2 flush is used.  Per-kernel device times come
 from the library's own event records in the same timed region.
 
+The JSON line also carries a "prefill" object: the Prefill workload (4
+layers, T=8192, full-layer double buffer) timed per chunk, with overlap and
+tensor-core utilisation of the grouped GEMMs.
+
 --impl reference times the CPU oracle (exact-integer control + float64
 expert numerics) on this machine's host cores on bounded samples of the same
 workload; it never touches the GPU.
@@ -405,6 +409,8 @@ def run_ours(args, rank, world, local_rank):
         "setup_s": {"host_pool": round(t_pool, 1), "graph_capture": round(t_capture, 1)},
         "execution": "the K timed steps run as one CUDA graph (captured from the library calls, uploaded before timing)",
     }
+    if not args.no_prefill:
+        out["prefill"] = run_prefill_bench(device, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(pool.numpy() if world == 1 else shared[0], args.cpu_seconds)
     if world > 1:
@@ -413,6 +419,89 @@ def run_ours(args, rank, world, local_rank):
     if shared is not None:
         torch.cuda.cudart().cudaHostUnregister(pool.data_ptr())
     return out
+
+
+def run_prefill_bench(device, peaks, reps: int = 3) -> dict:
+    """Prefill workload: 4 layers, E=128, top-8, H=2048, F=768, T=8192, 256
+    slots, full-layer double buffer.  Times whole chunks (prefill_begin + 4
+    prefill_layer calls) with CUDA events on the compute stream; per-kernel
+    device times from the library's event records; the same chunk with the
+    copies on the compute stream (one buffer in flight, no overlap) as the
+    single-buffer A/B."""
+    import torch
+    import moe_expert_cache_gb300 as ft
+    wl = synth.PREFILL
+    sh = wl.shape
+    T, L = wl.T, sh.L
+    pool = torch.empty(L * sh.E * sh.record_bytes, dtype=torch.uint8, pin_memory=True)
+    synth.fill_host_pool(pool.numpy(), sh, wl.seed)
+    xs = [torch.from_numpy(synth.tokens_bf16(wl.seed, 900, l, T, sh.H).view(np.int16)).to(device).view(torch.bfloat16)
+          for l in range(L)]
+    lg = [torch.from_numpy(synth.iid_logits(wl.seed, (900, l), T, sh.E)).to(device) for l in range(L)]
+    ys = [torch.empty(T, sh.H, dtype=torch.float32, device=device) for _ in range(L)]
+    cs, ts = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def measure(two_streams: bool):
+        ctx = ft.Context(L, sh.E, sh.k, sh.H, sh.F, wl.S, pool, T_max=4, T_prefill_max=T,
+                         compute_stream=cs.cuda_stream, transfer_stream=ts.cuda_stream if two_streams else 0)
+
+        def chunk():
+            ctx.prefill_begin(0)
+            for l in range(L):
+                ctx.prefill_layer(l & 1, l, l + 1 if l + 1 < L else -1, T, xs[l], lg[l], ys[l])
+
+        with torch.cuda.stream(cs):
+            chunk()
+        torch.cuda.synchronize(device)
+        ctx.profile_enable(True)
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(cs):
+                e0.record(cs)
+                chunk()
+                e1.record(cs)
+            torch.cuda.synchronize(device)
+            times.append(e0.elapsed_time(e1))
+        prof = ctx.profile_read()
+        assert ctx.status() == ft.FT_OK
+        ctx.close()
+        return statistics.median(times), prof
+
+    t_db, prof = measure(True)
+    t_sb, _ = measure(False)
+    n = reps
+    h2d = prof["pf_h2d"]["ms"] / n
+    comp = sum(v["ms"] for k_, v in prof.items() if k_ != "pf_h2d") / n
+    g1 = prof["pf_gemm1_swiglu"]["ms"] / (n * L)
+    g2 = prof["pf_gemm2"]["ms"] / (n * L)
+    fl1 = 2.0 * T * sh.k * 2 * sh.F * sh.H
+    fl2 = 2.0 * T * sh.k * sh.F * sh.H
+    tf = (fl1 + fl2) / ((g1 + g2) * 1e-3) / 1e12
+    tot = sum(v["ms"] for v in prof.values())
+    return {
+        "workload": "prefill: 4 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, T=8192, 256 slots, "
+                    "full-layer double buffer",
+        "expert_tokens_per_s": round(T * L / (t_db * 1e-3), 1),
+        "routed_assignments_per_s": round(T * sh.k * L / (t_db * 1e-3), 1),
+        "ms_per_chunk": round(t_db, 3),
+        "h2d_GBps": round(L * sh.E * sh.record_bytes / (h2d * 1e-3) / 1e9, 1),
+        "ms_h2d": round(h2d, 3), "ms_compute": round(comp, 3),
+        "overlap_eta": round(max(h2d, comp) / t_db, 4),
+        "hidden_fraction": round((h2d + comp - t_db) / min(h2d, comp), 4),
+        "single_buffer_ms_per_chunk": round(t_sb, 3),
+        "double_buffer_speedup": round(t_sb / t_db, 4),
+        "roofline_gemm": {"kernels": ["pf_gemm1_swiglu", "pf_gemm2"], "bound": "tensor",
+                          "achieved": round(tf, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                          "frac": round(tf / peaks["bf16_tflops"], 4),
+                          "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+                          "gemm1_TFLOPs": round(fl1 / (g1 * 1e-3) / 1e12, 1),
+                          "gemm2_TFLOPs": round(fl2 / (g2 * 1e-3) / 1e12, 1),
+                          "flops_per_layer": fl1 + fl2, "peak_source": peaks["source"],
+                          "traffic": traffic_from_profiles("pf_gemm1_swiglu")},
+        "kernels": {k_: {"launches": v["launches"], "ms_total": round(v["ms"], 3),
+                         "share": round(v["ms"] / tot, 4)} for k_, v in prof.items()},
+    }
 
 
 def roofline_entry(dom, kernels, peaks, h2d_peak):
@@ -550,6 +639,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     rank, world, local_rank = dist_env()
