@@ -227,7 +227,7 @@ class Context:
                            compute_stream or None, transfer_stream or None)
         _check(st, "ft_layer_init")
         self.h = h
-        self.L, self.E, self.k, self.H, self.F = L, E, k, H, F
+        self.L, self.E, self.k, self.H, self.F, self.fmt = L, E, k, H, F, fmt
         self._keep = (host_pool, nvfp4_global)
 
     def close(self):
@@ -295,7 +295,7 @@ class Context:
 
     def read_slot(self, slot):
         import numpy as np
-        out = np.empty(record_bytes(self.H, self.F), dtype=np.uint8)
+        out = np.empty(record_bytes(self.H, self.F, self.fmt), dtype=np.uint8)
         _check(read_slot(self.h, slot, _ptr(out)), "ft_read_slot")
         return out
 

@@ -66,46 +66,6 @@ __global__ void __launch_bounds__(512) fill_kernel(FillParams p) {
 
 // ------------------------------------------------------------- expert FFN
 
-__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
-
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Sense-reversing grid barrier over all CTAs of a cooperative launch:
-// bar[0] counts arrivals, bar[1] is the generation.  Bounded: gives up after
-// FT_WAIT_LIMIT_NS and latches the timeout bit.  Called by one thread per CTA
-// between CTA-wide barriers.
-__device__ void grid_barrier(unsigned* bar, unsigned G, unsigned* err) {
-    const unsigned gen0 = ld_acquire_gpu(&bar[1]);
-    __threadfence();
-    const unsigned c = atomicAdd(&bar[0], 1u);
-    if (c == G - 1) {
-        atomicExch(&bar[0], 0u);
-        __threadfence();
-        atomicAdd(&bar[1], 1u);
-    } else {
-        const uint64_t t0 = ft::globaltimer();
-        for (unsigned it = 0; ld_acquire_gpu(&bar[1]) == gen0; ++it) {
-            if ((it & 63u) == 63u && ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
-                atomicOr(err, FT_DEVERR_TIMEOUT);
-                break;
-            }
-        }
-    }
-    __threadfence();
-}
-
-// Producer-side drain: wait (bounded) for the last phase of every slot that
-// received a copy, so no bulk copy is in flight into shared memory at exit.
-__device__ void drain_ring(uint64_t* full, int issued, int nst, unsigned* err) {
-    for (int it = issued - nst; it < issued; ++it)
-        if (it >= 0) ft::mbar_wait(&full[it % nst], (it / nst) & 1, err);
-}
-
 // ---- phase A inner loop: gate and up dot products of one feature (full K)
 // for NT tokens.  x is read from shared memory as fp32 (XF) or bf16.
 template <int NT, bool XF>
@@ -157,7 +117,7 @@ __device__ __forceinline__ void gu_group(const uint4* wg, const uint4* wu, const
     for (int n = 0; n < NT; ++n) {
         const float sg = ft::warp_sum(ag[n]);
         const float su = ft::warp_sum(au[n]);
-        if (lane == n) mine = silu_mul(sg, su);
+        if (lane == n) mine = ft::silu_mul(sg, su);
     }
     if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + f] = mine;
 }
@@ -238,15 +198,6 @@ __device__ __forceinline__ void down_row(const uint4* wrow, const float* hs, int
             g0 += 1;
         }
     }
-}
-
-__device__ __forceinline__ void st_release_cta(int* p, int v) {
-    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(ft::smem_addr(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire_cta(const int* p) {
-    int v;
-    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(ft::smem_addr(p)) : "memory");
-    return v;
 }
 
 __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertParams p) {
@@ -353,7 +304,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 if (e == pre - 1 || e >= pre) {
                     if (!gdone) {
                         const uint64_t t0 = ft::globaltimer();
-                        while (!ld_acquire_cta(&s_gdone)) {
+                        while (!ft::ld_acquire_cta(&s_gdone)) {
                             if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
                                 atomicOr(p.err, FT_DEVERR_TIMEOUT);
                                 ok = false;
@@ -375,7 +326,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                     }
                 }
             }
-            drain_ring(full, it, nst, p.err);
+            ft::drain_ring(full, it, nst, p.err);
         }
         return;
     }
@@ -409,8 +360,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     // every h of this layer is written before any CTA starts phase B
     ft::named_bar_sync(1, CONSUMERS);
     if (tid == 0) {
-        grid_barrier(p.gbar, (unsigned)G, p.err);
-        st_release_cta(&s_gdone, 1);
+        ft::grid_barrier(p.gbar, (unsigned)G, p.err);
+        ft::st_release_cta(&s_gdone, 1);
     }
     ft::named_bar_sync(1, CONSUMERS);
 

@@ -1,0 +1,485 @@
+// Decode expert FFN over NVFP4 records (W4A16): the same persistent,
+// cooperatively launched streaming design as the BF16 kernel, reading packed
+// e2m1 values and e4m3 block-16 scales.
+//
+// deepmox "One logical expert, two physical levels of memory": an NVFP4 bank
+// stores packed four-bit values plus scale information; small per-expert
+// globals stay GPU-resident.  Weight w = e2m1 * e4m3(block of 16 along K) *
+// global(expert).  Each 16-value block is summed in fp32 against the fp32
+// activations, scaled by its e4m3 scale, and the row total is multiplied by
+// the expert's global once.  Activations are not quantised (W4A16).
+//
+// Record (per layer-expert): [W_gu values 2F x H/2 bytes, low nibble first,
+// gate/up rows interleaved in groups of 16][W_d values H x F/2]
+// [W_gu scales 2F x H/16][W_d scales H x F/16].
+//
+// Differences from the BF16 kernel: a phase-A slot holds 8 gate rows, the 8
+// matching up rows and their scale rows (four bulk copies); a phase-B item is
+// (expert, group of at most TG tokens) so that the staged h rows stay within
+// a slot for any T; x is read from shared memory (fp32 or bf16) when it fits
+// and from global memory otherwise.
+#include "ft_common.cuh"
+
+namespace {
+
+constexpr int CW = 8;                 // consumer warps
+constexpr int CONS = CW * 32;
+constexpr int THREADS = CONS + 32;    // + producer warp
+constexpr int FPC = CW;               // features per phase-A chunk
+constexpr size_t HEAD = 256;
+enum { X_F32_SMEM = 0, X_BF16_SMEM = 1, X_BF16_GLOBAL = 2 };
+
+struct Luts {
+    float2 pair[256];   // byte -> (e2m1 of low nibble, e2m1 of high nibble)
+    float e4m3[256];    // scale byte -> value
+};
+
+__device__ __forceinline__ float e2m1_value(int c) {
+    const int m = c & 7;
+    const float mag = m < 2 ? 0.5f * (float)m : (1.f + 0.5f * (float)(m & 1)) * (float)(1 << ((m >> 1) - 1));
+    return (c & 8) ? -mag : mag;
+}
+
+__device__ __forceinline__ float e4m3_value(int c) {
+    const int e = (c >> 3) & 15, m = c & 7;
+    float v = e == 0 ? ldexpf((float)m / 8.f, -6) : ldexpf(1.f + (float)m / 8.f, e - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+__device__ __forceinline__ void init_luts(Luts* L, int tid, int nthreads) {
+    for (int i = tid; i < 256; i += nthreads) {
+        L->pair[i] = make_float2(e2m1_value(i & 15), e2m1_value(i >> 4));
+        L->e4m3[i] = e4m3_value(i);
+    }
+}
+
+// 32 activations of token row `xr` starting at element 32*v.
+template <int XM>
+__device__ __forceinline__ void load_x32(const void* xr, int v, float* x) {
+    if (XM == X_F32_SMEM) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(xr) + (size_t)v * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 q = p[i];
+            x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
+        }
+    } else {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xr) + (size_t)v * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 q = XM == X_BF16_GLOBAL ? __ldg(p + i) : p[i];
+            ft::bf16x8_to_f32(q, x + 8 * i);
+        }
+    }
+}
+
+// sum over 32 values of one uint4 (two scale blocks): sc0 * block0 + sc1 * block1
+__device__ __forceinline__ float fp4_dot32(const uint4& w, const float* x, const float2* pair, float sc0, float sc1) {
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float2 v = pair[(wd[q] >> (8 * b)) & 255u];
+            s0 = fmaf(v.x, x[8 * q + 2 * b], s0);
+            s0 = fmaf(v.y, x[8 * q + 2 * b + 1], s0);
+        }
+    }
+#pragma unroll
+    for (int q = 2; q < 4; ++q) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float2 v = pair[(wd[q] >> (8 * b)) & 255u];
+            s1 = fmaf(v.x, x[8 * q + 2 * b], s1);
+            s1 = fmaf(v.y, x[8 * q + 2 * b + 1], s1);
+        }
+    }
+    return fmaf(sc0, s0, sc1 * s1);
+}
+
+// Phase A: gate and up rows of one feature against NT tokens; returns the
+// un-globalled row sums in ag / au.
+template <int NT, int XM>
+__device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
+                                         const void* xs, size_t xrow_elems, const int* tk, int H, int lane,
+                                         const Luts* L, float* ag, float* au) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
+    const int nv = H >> 5;  // uint4 (32 values) per row
+    for (int v = lane; v < nv; v += 32) {
+        const uint4 wg = gv[v], wu = uv[v];
+        const float g0 = L->e4m3[gs[2 * v]], g1 = L->e4m3[gs[2 * v + 1]];
+        const float u0 = L->e4m3[us[2 * v]], u1 = L->e4m3[us[2 * v + 1]];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            float x[32];
+            const void* xr = XM == X_F32_SMEM
+                                 ? (const void*)(static_cast<const float*>(xs) + (size_t)tk[n] * xrow_elems)
+                                 : (const void*)(static_cast<const __nv_bfloat16*>(xs) + (size_t)tk[n] * xrow_elems);
+            load_x32<XM>(xr, v, x);
+            ag[n] += fp4_dot32(wg, x, L->pair, g0, g1);
+            au[n] += fp4_dot32(wu, x, L->pair, u0, u1);
+        }
+    }
+}
+
+template <int NT, int XM>
+__device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
+                                          const void* xs, int H, const int* m_tok, int off, int g0, int F, int f,
+                                          int lane, const Luts* L, float gsc, float* hbuf) {
+    int tk[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) tk[n] = m_tok[off + g0 + n];
+    float ag[NT], au[NT];
+    gu_dots4<NT, XM>(gv, uv, gs, us, xs, (size_t)H, tk, H, lane, L, ag, au);
+    float mine = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const float sg = ft::warp_sum(ag[n]) * gsc;
+        const float su = ft::warp_sum(au[n]) * gsc;
+        if (lane == n) mine = ft::silu_mul(sg, su);
+    }
+    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + f] = mine;
+}
+
+template <int XM>
+__device__ __forceinline__ void gu_feature4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
+                                            const void* xs, int H, const int* m_tok, int off, int ntok, int F, int f,
+                                            int lane, const Luts* L, float gsc, float* hbuf) {
+    int g0 = 0;
+    while (g0 < ntok) {
+        const int rem = ntok - g0;
+        if (rem >= 4) {
+            gu_group4<4, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, L, gsc, hbuf);
+            g0 += 4;
+        } else if (rem >= 2) {
+            gu_group4<2, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, L, gsc, hbuf);
+            g0 += 2;
+        } else {
+            gu_group4<1, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, L, gsc, hbuf);
+            g0 += 1;
+        }
+    }
+}
+
+// Phase B: one W_d row (values + scales) against NT staged h rows (fp32).
+template <int NT>
+__device__ __forceinline__ void down_group4(const uint4* wv, const uint8_t* ws, const float* hs, int g, int F,
+                                            int lane, const Luts* L, float gsc, float* o_s, int obase, int RMAX,
+                                            int rl) {
+    float acc[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n] = 0.f;
+    const int nv = F >> 5;
+    for (int v = lane; v < nv; v += 32) {
+        const uint4 w = wv[v];
+        const float s0 = L->e4m3[ws[2 * v]], s1 = L->e4m3[ws[2 * v + 1]];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            float x[32];
+            load_x32<X_F32_SMEM>(hs + (size_t)(g + n) * F, v, x);
+            acc[n] += fp4_dot32(w, x, L->pair, s0, s1);
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const float sv = ft::warp_sum(acc[n]) * gsc;
+        if (lane == 0) o_s[(size_t)(obase + g + n) * RMAX + rl] = sv;
+    }
+}
+
+__device__ __forceinline__ void down_row4(const uint4* wv, const uint8_t* ws, const float* hs, int ng, int F,
+                                          int lane, const Luts* L, float gsc, float* o_s, int obase, int RMAX,
+                                          int rl) {
+    int g = 0;
+    while (g < ng) {
+        const int rem = ng - g;
+        if (rem >= 4) {
+            down_group4<4>(wv, ws, hs, g, F, lane, L, gsc, o_s, obase, RMAX, rl);
+            g += 4;
+        } else if (rem >= 2) {
+            down_group4<2>(wv, ws, hs, g, F, lane, L, gsc, o_s, obase, RMAX, rl);
+            g += 2;
+        } else {
+            down_group4<1>(wv, ws, hs, g, F, lane, L, gsc, o_s, obase, RMAX, rl);
+            g += 1;
+        }
+    }
+}
+
+}  // namespace
+
+namespace {
+
+template <int XM>
+__global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_gdone;
+    __shared__ Luts L;
+    const int H = p.H, F = p.F, T = p.T, k = p.k, TG = p.tgroup;
+    const int nst = p.nstage;
+    const unsigned slot_bytes = p.stage_bytes;
+    const int ugpu = p.info[INFO_UGPU];
+    const int nasg = p.info[INFO_NASSIGN];
+    const int G = gridDim.x, c = blockIdx.x;
+    const int cpe = F / FPC;
+    const int NA = ugpu * cpe;
+    const int a0 = (int)((long long)NA * c / G), a1 = (int)((long long)NA * (c + 1) / G);
+    const int r0 = (int)((long long)H * c / G), r1 = (int)((long long)H * (c + 1) / G);
+    const int R = r1 - r0;
+    const int RMAX = (H + G - 1) / G;
+    const int TK = T * k;
+    const size_t VGU = (size_t)F * H;                 // W_gu value bytes (2F x H/2)
+    const size_t VD = (size_t)H * F / 2;              // W_d value bytes
+    const size_t SGU = (size_t)2 * F * H / 16;        // W_gu scale bytes
+    const unsigned vrow = (unsigned)H / 2, srow = (unsigned)H / 16;      // W_gu row bytes
+    const unsigned dvrow = (unsigned)F / 2, dsrow = (unsigned)F / 16;    // W_d row bytes
+
+    const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + nst;
+    size_t o = HEAD;
+    void* x_s = smem + o;
+    if (XM != X_BF16_GLOBAL) o += ((size_t)T * H * (XM == X_F32_SMEM ? 4 : 2) + 127) & ~(size_t)127;
+    float* o_s = reinterpret_cast<float*>(smem + o);
+    o += ((size_t)TK * RMAX * 4 + 127) & ~(size_t)127;
+    int* m_off = reinterpret_cast<int*>(smem + o);
+    int* m_slot = m_off + TK + 1;
+    int* m_tok = m_slot + TK;
+    float* m_gate = reinterpret_cast<float*>(m_tok + TK);
+    int* m_pos = reinterpret_cast<int*>(m_gate + TK);
+    float* m_gs = reinterpret_cast<float*>(m_pos + TK);   // global scale of each entry
+    o += ((size_t)(6 * TK + 1) * 4 + 127) & ~(size_t)127;
+    unsigned char* ring = smem + o;
+    const unsigned wpart = ((unsigned)RMAX * (dvrow + dsrow) + 127u) & ~127u;
+    const void* xsrc = XM == X_BF16_GLOBAL ? static_cast<const void*>(p.x) : x_s;
+
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) {
+            ft::mbar_init(&full[s], 1);
+            ft::mbar_init(&empty[s], CW);
+        }
+        ft::mbar_fence_init();
+        s_gdone = 0;
+    }
+    init_luts(&L, tid, THREADS);
+    for (int i = tid; i <= ugpu; i += THREADS) m_off[i] = p.wl_off[i];
+    for (int i = tid; i < ugpu; i += THREADS) {
+        m_slot[i] = p.wl_slot[i];
+        m_gs[i] = p.gscale[p.wl_fid[i]];
+    }
+    for (int i = tid; i < nasg; i += THREADS) {
+        m_tok[i] = p.as_tok[i];
+        m_gate[i] = p.as_gate[i];
+    }
+    for (int i = tid; i < TK; i += THREADS) m_pos[i] = p.out_pos[i];
+    if (XM == X_F32_SMEM) {
+        for (int i = tid; i < T * H / 8; i += THREADS) {
+            float f8[8];
+            ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
+            reinterpret_cast<float4*>(x_s)[2 * i] = make_float4(f8[0], f8[1], f8[2], f8[3]);
+            reinterpret_cast<float4*>(x_s)[2 * i + 1] = make_float4(f8[4], f8[5], f8[6], f8[7]);
+        }
+    } else if (XM == X_BF16_SMEM) {
+        for (int i = tid; i < T * H / 8; i += THREADS)
+            reinterpret_cast<uint4*>(x_s)[i] = reinterpret_cast<const uint4*>(p.x)[i];
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (wid == CW) {
+        if (lane == 0) {
+            const uint64_t pol = ft::l2_policy_evict_first();
+            int it = 0;
+            bool ok = true;
+            for (int a = a0; a < a1 && ok; ++a, ++it) {
+                const int st = it % nst;
+                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
+                const int ent = a / cpe;
+                const int f0 = (a - ent * cpe) * FPC;
+                const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
+                const int grow = (f0 >> 4) * 32 + (f0 & 15);  // first gate row; up rows 16 later
+                unsigned char* dst = ring + (size_t)st * slot_bytes;
+                ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * (vrow + srow));
+                ft::bulk_g2s_hint(dst, rec + (size_t)grow * vrow, FPC * vrow, &full[st], pol);
+                ft::bulk_g2s_hint(dst + FPC * vrow, rec + (size_t)(grow + 16) * vrow, FPC * vrow, &full[st], pol);
+                ft::bulk_g2s_hint(dst + 2 * FPC * vrow, rec + VGU + VD + (size_t)grow * srow, FPC * srow, &full[st], pol);
+                ft::bulk_g2s_hint(dst + 2 * FPC * vrow + FPC * srow, rec + VGU + VD + (size_t)(grow + 16) * srow,
+                                  FPC * srow, &full[st], pol);
+            }
+            // phase B items = (expert, group of <= TG tokens); W_d rows stream
+            // ahead of the grid barrier, h rows after it
+            int nitems = 0;
+            if (R > 0)
+                for (int e = 0; e < ugpu; ++e) nitems += (m_off[e + 1] - m_off[e] + TG - 1) / TG;
+            const int pre = nitems < nst ? nitems : nst;
+            const int itB = it;
+            bool gdone = false;
+            int e = 0, g0 = 0, idx = 0;
+            for (; idx < nitems && ok; ++idx, ++it) {
+                const int st = it % nst;
+                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
+                const int off = m_off[e], ntok = m_off[e + 1] - off;
+                const int ng = min(TG, ntok - g0);
+                const uint8_t* rec = p.slot_pool + (size_t)m_slot[e] * p.rb;
+                unsigned char* dst = ring + (size_t)st * slot_bytes;
+                const unsigned wb = (unsigned)R * dvrow, sb = (unsigned)R * dsrow, hb = (unsigned)ng * F * 4u;
+                ft::mbar_arrive_expect_tx(&full[st], wb + sb + hb);
+                ft::bulk_g2s_hint(dst, rec + VGU + (size_t)r0 * dvrow, wb, &full[st], pol);
+                ft::bulk_g2s_hint(dst + (size_t)RMAX * dvrow, rec + VGU + VD + SGU + (size_t)r0 * dsrow, sb, &full[st], pol);
+                if (idx >= pre - 1) {
+                    if (!gdone) {
+                        const uint64_t t0 = ft::globaltimer();
+                        while (!ft::ld_acquire_cta(&s_gdone)) {
+                            if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                                atomicOr(p.err, FT_DEVERR_TIMEOUT);
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        gdone = true;
+                        // deferred h rows of the items prefetched before the barrier
+                        int e2 = 0, g2 = 0;
+                        for (int i2 = 0; i2 <= idx; ++i2) {
+                            const int off2 = m_off[e2], nt2 = m_off[e2 + 1] - off2;
+                            const int ng2 = min(TG, nt2 - g2);
+                            const int st2 = (itB + i2) % nst;
+                            ft::bulk_g2s(ring + (size_t)st2 * slot_bytes + wpart, p.hbuf + (size_t)(off2 + g2) * F,
+                                         (unsigned)ng2 * F * 4u, &full[st2]);
+                            g2 += TG;
+                            if (g2 >= nt2) { g2 = 0; ++e2; }
+                        }
+                    } else {
+                        ft::bulk_g2s(dst + wpart, p.hbuf + (size_t)(off + g0) * F, hb, &full[st]);
+                    }
+                }
+                g0 += TG;
+                if (g0 >= ntok) { g0 = 0; ++e; }
+            }
+            ft::drain_ring(full, it, nst, p.err);
+        }
+        return;
+    }
+
+    // ------------------------------------------------- phase A: gate/up + SwiGLU
+    int it = 0;
+    bool failed = false;
+    for (int a = a0; a < a1; ++a, ++it) {
+        const int st = it % nst;
+        const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
+        failed = !ok;
+        const int ent = a / cpe;
+        const int f = (a - ent * cpe) * FPC + wid;
+        const int off = m_off[ent];
+        const int ntok = m_off[ent + 1] - off;
+        const unsigned char* sb = ring + (size_t)st * slot_bytes;
+        const uint4* gv = reinterpret_cast<const uint4*>(sb + (size_t)wid * vrow);
+        const uint4* uv = reinterpret_cast<const uint4*>(sb + (size_t)(FPC + wid) * vrow);
+        const uint8_t* gs = sb + 2 * FPC * vrow + (size_t)wid * srow;
+        const uint8_t* us = sb + 2 * FPC * vrow + FPC * srow + (size_t)wid * srow;
+        if (ok) gu_feature4<XM>(gv, uv, gs, us, xsrc, H, m_tok, off, ntok, F, f, lane, &L, m_gs[ent], p.hbuf);
+        __syncwarp();
+        if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+    }
+
+    ft::named_bar_sync(1, CONS);
+    if (tid == 0) {
+        ft::grid_barrier(p.gbar, (unsigned)G, p.err);
+        ft::st_release_cta(&s_gdone, 1);
+    }
+    ft::named_bar_sync(1, CONS);
+
+    // ---------------------------------------------------- phase B: down rows
+    if (R > 0) {
+        for (int e = 0; e < ugpu; ++e) {
+            const int off = m_off[e], ntok = m_off[e + 1] - off;
+            for (int g0 = 0; g0 < ntok; g0 += TG, ++it) {
+                const int ng = min(TG, ntok - g0);
+                const int st = it % nst;
+                const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
+                failed = !ok;
+                const unsigned char* sb = ring + (size_t)st * slot_bytes;
+                const float* hs = reinterpret_cast<const float*>(sb + wpart);
+                for (int rl = wid; rl < R && ok; rl += CW)
+                    down_row4(reinterpret_cast<const uint4*>(sb + (size_t)rl * dvrow),
+                              sb + (size_t)RMAX * dvrow + (size_t)rl * dsrow, hs, ng, F, lane, &L, m_gs[e], o_s,
+                              off + g0, RMAX, rl);
+                __syncwarp();
+                if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+            }
+        }
+    }
+    ft::named_bar_sync(1, CONS);
+    for (int idx = tid; idx < T * R; idx += CONS) {
+        const int t = idx / R, rl = idx - t * R;
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int pos = m_pos[t * k + j];
+            if (pos >= 0) acc = fmaf(m_gate[pos], o_s[(size_t)pos * RMAX + rl], acc);
+        }
+        const size_t oi = (size_t)t * H + r0 + rl;
+        if (p.partial_C) acc += p.partial_C[oi];
+        p.y[oi] = acc;
+    }
+}
+
+}  // namespace
+
+static constexpr size_t kSmemLimit4 = 227 * 1024 - sizeof(Luts) - 64;
+
+cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
+    const int G = num_sms;
+    const int RMAX = (p.H + G - 1) / G;
+    const size_t TK = (size_t)p.T * p.k;
+    int xm = X_F32_SMEM;
+    size_t xbytes = (size_t)p.T * p.H * 4;
+    if (xbytes > 32768) {
+        xm = X_BF16_SMEM;
+        xbytes = (size_t)p.T * p.H * 2;
+        if (xbytes > 32768) {
+            xm = X_BF16_GLOBAL;
+            xbytes = 0;
+        }
+    }
+    const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127) +
+                        (((6 * TK + 1) * 4 + 127) & ~(size_t)127);
+    const size_t chunk = (size_t)2 * FPC * (p.H / 2 + p.H / 16);
+    const size_t wpart = ((size_t)RMAX * (p.F / 2 + p.F / 16) + 127) & ~(size_t)127;
+    if (head + 2 * chunk > kSmemLimit4) return cudaErrorInvalidValue;
+    // token group of phase B: as many h rows as fit next to the W_d rows in a
+    // slot when two slots fill the shared memory
+    int tg = (int)(((kSmemLimit4 - head) / 2 - wpart) / ((size_t)p.F * 4));
+    if (tg > p.T) tg = p.T;
+    if (tg > 16) tg = 16;
+    if (tg < 1) return cudaErrorInvalidValue;
+    size_t slot = wpart + (size_t)tg * p.F * 4;
+    if (slot < chunk) slot = chunk;
+    slot = (slot + 127) & ~(size_t)127;
+    int nst = (int)((kSmemLimit4 - head) / slot);
+    if (nst > 4) nst = 4;
+    if (nst < 2) return cudaErrorInvalidValue;
+    p.nstage = nst;
+    p.stage_bytes = (unsigned)slot;
+    p.tgroup = tg;
+    const size_t smem = head + slot * nst;
+    const void* fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM>
+                     : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM>
+                                         : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&p};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}

@@ -44,7 +44,7 @@ struct ft_ctx {
     // fixed-size control outputs and worklists (one arena)
     void* arena;
     unsigned* clock;
-    int *ids, *slots_topk, *pos, *as_tok, *wl_slot, *wl_off, *fill_slot, *fill_fid, *Fl, *Cl, *victims, *info;
+    int *ids, *slots_topk, *pos, *as_tok, *wl_slot, *wl_off, *wl_fid, *fill_slot, *fill_fid, *Fl, *Cl, *victims, *info;
     float *gates, *as_gate;
     unsigned long long* counters;
     unsigned* err;
@@ -171,9 +171,10 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     if (L < 1 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E || H < 64 || H % 64 || F < 64 || F % 64 || S < 1 ||
         T_max < 1 || T_max > 256 || T_max * k > 4096 || T_prefill_max < 0 || !host_pool)
         return FT_ERR_ARG;
-    if (fmt != FT_FMT_BF16) return FT_ERR_ARG;  // NVFP4 banks are accepted by a later version
+    if (fmt != FT_FMT_BF16 && fmt != FT_FMT_NVFP4) return FT_ERR_ARG;
+    if (fmt == FT_FMT_NVFP4 && (!nvfp4_global || H % 256 || F % 256)) return FT_ERR_ARG;
     if (route_ctl_smem_bytes(T_max, k, E, S) > kCtlSmemMax) return FT_ERR_ARG;
-    if ((size_t)T_max * H * 2 > 65536) return FT_ERR_ARG;  // decode tokens are staged in shared memory
+    if (fmt == FT_FMT_BF16 && (size_t)T_max * H * 2 > 65536) return FT_ERR_ARG;  // BF16 decode stages x in smem
     // prefill: 256-column GEMM tiles over 2F and H, top-k of at most 256 logits
     if (T_prefill_max > 0 && (H % 256 || (2 * F) % 256 || E > 256 || (size_t)T_prefill_max * k > (1u << 30)))
         return FT_ERR_ARG;
@@ -223,7 +224,8 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     auto carve = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     const size_t o_clock = carve(4), o_ids = carve(TK * 4), o_gates = carve(TK * 4), o_slots = carve(TK * 4),
                  o_pos = carve(TK * 4), o_astok = carve(TK * 4), o_asg = carve(TK * 4),
-                 o_wls = carve((size_t)E * 4), o_wlo = carve((size_t)(E + 1) * 4), o_fs = carve((size_t)E * 4),
+                 o_wls = carve((size_t)E * 4), o_wlo = carve((size_t)(E + 1) * 4), o_wlf = carve((size_t)E * 4),
+                 o_fs = carve((size_t)E * 4),
                  o_ff = carve((size_t)E * 4), o_F = carve((size_t)E * 4), o_C = carve((size_t)E * 4),
                  o_v = carve((size_t)E * 4), o_info = carve(INFO_WORDS * 4), o_cnt = carve(CNT_WORDS * 8),
                  o_err = carve(4), o_gbar = carve(8);
@@ -239,6 +241,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     c->as_gate = (float*)(a + o_asg);
     c->wl_slot = (int*)(a + o_wls);
     c->wl_off = (int*)(a + o_wlo);
+    c->wl_fid = (int*)(a + o_wlf);
     c->fill_slot = (int*)(a + o_fs);
     c->fill_fid = (int*)(a + o_ff);
     c->Fl = (int*)(a + o_F);
@@ -277,7 +280,7 @@ ft_status ft_route_ctl(ft_ctx* c, int32_t layer, int32_t T, const float* logits,
     p.B_P = B_P; p.B_H = B_H;
     p.slot_for_id = c->slot_for_id; p.id_for_slot = c->id_for_slot; p.stamps = c->stamps; p.clock = c->clock;
     p.out_ids = c->ids; p.out_gates = c->gates; p.out_slots = c->slots_topk; p.out_pos = c->pos;
-    p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok; p.as_gate = c->as_gate;
+    p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.wl_fid = c->wl_fid; p.as_tok = c->as_tok; p.as_gate = c->as_gate;
     p.fill_slot = c->fill_slot; p.fill_fid = c->fill_fid;
     p.out_F = c->Fl; p.out_C = c->Cl; p.out_victims = c->victims;
     p.info = c->info; p.counters = c->counters; p.err = c->err;
@@ -308,9 +311,13 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.x = (const __nv_bfloat16*)x; p.partial_C = partial_C; p.y = y;
     p.info = c->info; p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok;
     p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err; p.gbar = c->gbar;
+    p.wl_fid = c->wl_fid; p.gscale = c->nvfp4_global;
     {
         ProfScope ps(c->prof, FT_K_EXPERT, c->cs);
-        FT_CUDA(launch_expert_ffn(p, c->num_sms, c->cs));
+        if (c->fmt == FT_FMT_NVFP4)
+            FT_CUDA(launch_expert_ffn_fp4(p, c->num_sms, c->cs));
+        else
+            FT_CUDA(launch_expert_ffn(p, c->num_sms, c->cs));
     }
     return FT_OK;
 }

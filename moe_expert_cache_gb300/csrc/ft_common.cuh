@@ -127,6 +127,55 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
+
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Sense-reversing grid barrier over all CTAs of a cooperative launch:
+// bar[0] counts arrivals, bar[1] is the generation.  Bounded: gives up after
+// FT_WAIT_LIMIT_NS and latches the timeout bit.  Called by one thread per CTA
+// between CTA-wide barriers.
+__device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned G, unsigned* err) {
+    const unsigned gen0 = ld_acquire_gpu(&bar[1]);
+    __threadfence();
+    const unsigned c = atomicAdd(&bar[0], 1u);
+    if (c == G - 1) {
+        atomicExch(&bar[0], 0u);
+        __threadfence();
+        atomicAdd(&bar[1], 1u);
+    } else {
+        const uint64_t t0 = globaltimer();
+        for (unsigned it = 0; ld_acquire_gpu(&bar[1]) == gen0; ++it) {
+            if ((it & 63u) == 63u && globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                atomicOr(err, FT_DEVERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __threadfence();
+}
+
+// Producer-side drain: wait (bounded) for the last phase of every slot that
+// received a copy, so no bulk copy is in flight into shared memory at exit.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int issued, int nst, unsigned* err) {
+    for (int it = issued - nst; it < issued; ++it)
+        if (it >= 0) mbar_wait(&full[it % nst], (it / nst) & 1, err);
+}
+
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
 }  // namespace ft
 
 // ------------------------------------------------------------------ params
@@ -147,6 +196,7 @@ struct CtlParams {
     int* out_pos;             // [T*k]  row of (t,j) in the assignment arrays or -1
     int* wl_slot;             // [E]    slot of GPU entry i (entries ascending expert id)
     int* wl_off;              // [E+1]  first assignment of entry i
+    int* wl_fid;              // [E]    flat id of entry i
     int* as_tok;              // [T*k]  token of each assignment (entry-major, token ascending)
     float* as_gate;           // [T*k]
     int* fill_slot;           // [E]
@@ -184,6 +234,9 @@ struct ExpertParams {
     float* hbuf;              // [T*k, F] fp32
     unsigned* err;
     unsigned* gbar;           // [2] grid barrier (arrivals, generation), zero at init
+    const int* wl_fid;        // [E] flat id of each GPU entry (NVFP4 global lookup)
+    const float* gscale;      // [L*E] NVFP4 per-expert fp32 global, or null
+    int tgroup;               // NVFP4: tokens per phase-B item
     int nstage;               // pipeline depth (stages in shared memory)
     unsigned stage_bytes;     // bytes of one stage
 };
@@ -192,5 +245,6 @@ struct ExpertParams {
 cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s);
 cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);
 cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s);
+cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s);
 size_t route_ctl_smem_bytes(int T, int k, int E, int S);
 constexpr size_t kCtlSmemMax = 200 * 1024;

@@ -453,6 +453,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             const int off = (ex >> 12) + sh.carry1;
             p.wl_slot[ent] = s_slot[e];
             p.wl_off[ent] = off;
+            p.wl_fid[ent] = fbase + e;
             s_eoff[e] = off;
         }
         __syncthreads();

@@ -1,0 +1,114 @@
+"""GPU parity of the NVFP4 decode path (W4A16): control bit-exact, outputs
+within rel-L2 5e-3 of the fp64 oracle on identically dequantised weights."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import control as ctl
+from oracle import numerics as nm
+from oracle import nvfp4 as fp4
+from tests import harness as hz
+
+pytestmark = pytest.mark.gpu
+NVFP4_REL_L2 = 5e-3
+
+
+@pytest.fixture(scope="module")
+def ft():
+    import torch
+    assert torch.cuda.is_available()
+    import moe_expert_cache_gb300 as ft
+    ft.load()
+    return ft
+
+
+def _dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+class FP4Weights:
+    def __init__(self, pool_np, glob, sh, layer):
+        self.pool, self.glob, self.sh, self.layer, self.cache = pool_np, glob, sh, layer, {}
+
+    def __call__(self, e):
+        if e not in self.cache:
+            sh, rb = self.sh, self.sh.record_bytes
+            fid = self.layer * sh.E + e
+            self.cache[e] = fp4.record_weights(self.pool[fid * rb:(fid + 1) * rb], sh.H, sh.F, float(self.glob[fid]))
+        return self.cache[e]
+
+
+def _replay(ft, sh, S, schedule, B_P, B_H, rho, samples, tok_sample=None, seed=0):
+    """schedule: list of (T, steps).  Every call bit-exact; sampled calls numerically."""
+    import torch
+    pool, glob = hz.pinned_pool(sh, seed)
+    pool_np = pool.numpy()
+    T_max = max(t for t, _ in schedule)
+    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, S, pool, fmt=ft.FT_FMT_NVFP4, T_max=T_max, nvfp4_global=glob)
+    st = ctl.CacheState.empty(sh.L, sh.E, S)
+    step = 0
+    done = []
+    for T, steps in schedule:
+        logits = synth.ar1_logits(seed, steps, sh.L, T, sh.E, rho, None) if rho else None
+        for s in range(steps):
+            for layer in range(sh.L):
+                lg = logits[s, layer] if rho else synth.iid_logits(seed, (step, layer), T, sh.E)
+                ids, gates = zip(*[ctl.topk_route(r, sh.k) for r in lg])
+                r = ctl.route_ctl(st, layer, ids, B_P, B_H)
+                ctl.check_invariants(st, r)
+                ctx.route_ctl(layer, T, logits=_dev(lg), B_P=B_P, B_H=B_H)
+                hz.compare_ctl(ctx, st, r, T, f"T={T} step={s} layer={layer}")
+                if (step, layer) in samples:
+                    toks = list(range(T)) if tok_sample is None else sorted(set(min(t, T - 1) for t in tok_sample))
+                    w = FP4Weights(pool_np, glob, sh, layer)
+                    xb = synth.tokens_bf16(seed, step, layer, T, sh.H)
+                    x = nm.bf16_to_f64(xb)
+                    sub_ids = [ids[t] for t in toks]
+                    sub_g = [gates[t] for t in toks]
+                    sub_sl = [r.slots_topk[t] for t in toks]
+                    y_gpu_ref, pc_sub = nm.moe_layer_split(x[toks], sub_ids, sub_g, sub_sl, w)
+                    pc = np.zeros((T, sh.H), dtype=np.float32)
+                    pc[toks] = pc_sub
+                    xd = _dev(xb.view(np.int16)).view(torch.bfloat16)
+                    y = torch.empty(T, sh.H, dtype=torch.float32, device="cuda")
+                    ctx.moe_forward(xd, _dev(pc), y)
+                    torch.cuda.synchronize()
+                    got = y.cpu().numpy()[toks]
+                    ref = nm.merged_output(y_gpu_ref, pc_sub)
+                    rel = nm.rel_l2(got, ref)
+                    assert np.isfinite(y.cpu().numpy()).all()
+                    assert rel <= NVFP4_REL_L2, (T, step, layer, rel)
+                    done.append(rel)
+                    for f, v in zip(r.F, r.victims):
+                        fid = layer * sh.E + f
+                        rb = sh.record_bytes
+                        assert np.array_equal(ctx.read_slot(v), pool_np[fid * rb:(fid + 1) * rb])
+            step += 1
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
+    return done
+
+
+@pytest.mark.parametrize("H,F,E,k,S,T", [
+    (256, 256, 16, 4, 12, 3),       # x fp32 in shared memory
+    (1024, 512, 16, 4, 24, 9),      # x bf16 in shared memory
+    (1024, 512, 16, 4, 24, 20),     # x from global memory
+    (1024, 2048, 8, 4, 8, 40),      # phase-B items of several token groups
+])
+def test_nvfp4_small(ft, H, F, E, k, S, T):
+    sh = synth.Shape(L=2, E=E, k=k, H=H, F=F, fmt=synth.FMT_NVFP4)
+    samples = {(s, l) for s in range(4) for l in range(2)}
+    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples)
+    assert len(done) == len(samples)
+
+
+@pytest.mark.slow
+def test_large_nvfp4_decode(ft):
+    """Large NVFP4 decode: 8 layers, E=256, top-8, H=4096, F=2048, 512 slots,
+    64 steps at T=1 then 64 at T=64, AR(1) rho=0.8, B_P=52.7, B_H=150."""
+    wl = synth.LARGE_NVFP4
+    samples = {(s, l) for s in (0, 1, 63) for l in (0, 7)} | {(s, l) for s in (64, 127) for l in (0, 7)}
+    done = _replay(ft, wl.shape, wl.S, [(1, 64), (64, 64)], wl.B_P, wl.B_H, wl.rho, samples,
+                   tok_sample=[0, 21, 42, 63])
+    assert len(done) == len(samples)
