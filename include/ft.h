@@ -81,6 +81,7 @@ typedef struct {
 #define FT_K_PF_GEMM2     7   /* prefill down grouped GEMM                      */
 #define FT_K_PF_COMBINE   8   /* prefill gated combine                          */
 #define FT_K_PF_H2D       9   /* prefill layer copy (transfer stream)           */
+#define FT_K_PF_DEQUANT  10   /* prefill NVFP4 layer -> bf16 staging            */
 #define FT_K_COUNT       16
 typedef struct {
     double ms[FT_K_COUNT];          /* summed device time of the launches       */

@@ -257,7 +257,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
         INIT_CUDA(cudaMemcpy(c->nvfp4_global, nvfp4_global, (size_t)L * E * 4, cudaMemcpyHostToDevice));
     }
     if (T_prefill_max > 0) {
-        st = prefill_alloc(c->pf, T_prefill_max, k, H, F, E);
+        st = prefill_alloc(c->pf, T_prefill_max, k, H, F, E, fmt);
         if (st != FT_OK) return fail(st);
     }
     c->pf.E = E;
@@ -529,7 +529,7 @@ ft_status ft_profile_read(ft_ctx* c, ft_profile* out) {
 
 const char* ft_kernel_name(int32_t id) {
     static const char* names[FT_K_COUNT] = {"route_ctl", "fill", "expert_ffn", nullptr, "pf_route",
-                                            "pf_permute_gather", "pf_gemm1_swiglu", "pf_gemm2", "pf_combine", "pf_h2d"};
+                                            "pf_permute_gather", "pf_gemm1_swiglu", "pf_gemm2", "pf_combine", "pf_h2d", "pf_dequant"};
     return (id >= 0 && id < FT_K_COUNT) ? names[id] : nullptr;
 }
 
@@ -616,6 +616,12 @@ ft_status ft_prefill_layer(ft_ctx* c, int32_t buffer, int32_t layer, int32_t nex
         pf.buf_layer[nb] = next_layer;
     }
     FT_CUDA(cudaStreamWaitEvent(cs, pf.loaded[buffer], 0));
+    const float* escale = nullptr;
+    if (c->fmt == FT_FMT_NVFP4) {
+        ProfScope ps(c->prof, FT_K_PF_DEQUANT, cs);
+        FT_CUDA(launch_pf_dequant(pf, c->slot_pool + (size_t)buffer * layer_bytes, cs));
+        escale = c->nvfp4_global + (size_t)layer * c->E;
+    }
     {
         ProfScope ps(c->prof, FT_K_PF_ROUTE, cs);
         FT_CUDA(launch_pf_route(pf, logits, T, c->err, cs));
@@ -627,11 +633,11 @@ ft_status ft_prefill_layer(ft_ctx* c, int32_t buffer, int32_t layer, int32_t nex
     }
     {
         ProfScope ps(c->prof, FT_K_PF_GEMM1, cs);
-        FT_CUDA(launch_pf_gemm1(pf, buffer, c->num_sms, c->err, cs));
+        FT_CUDA(launch_pf_gemm1(pf, buffer, escale, c->num_sms, c->err, cs));
     }
     {
         ProfScope ps(c->prof, FT_K_PF_GEMM2, cs);
-        FT_CUDA(launch_pf_gemm2(pf, buffer, c->num_sms, c->err, cs));
+        FT_CUDA(launch_pf_gemm2(pf, buffer, escale, c->num_sms, c->err, cs));
     }
     {
         ProfScope ps(c->prof, FT_K_PF_COMBINE, cs);

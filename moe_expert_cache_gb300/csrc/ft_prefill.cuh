@@ -28,13 +28,16 @@ struct PrefillState {
     float* row_gate = nullptr;// [T*k] gate of each expert-ordered row
     int* counts = nullptr;    // [E]
     int* offsets = nullptr;   // [E+1]
+    int fmt = 0;              // record format of the slot pool
+    size_t rb = 0;            // record bytes in the slot pool
+    void* staging = nullptr;  // NVFP4: the layer's E records expanded to bf16 (e2m1 * e4m3, exact)
     // tensor maps: A operands are fixed scratch; B operands follow the slot pool
     CUtensorMap mapA1, mapA2;       // X_perm [T_max*k, H], h [T_max*k, F]
     CUtensorMap mapB1[2], mapB2[2]; // W_gu, W_d of the E records of buffer b
     const void* maps_pool = nullptr; // slot pool the B maps were encoded for
 };
 
-ft_status prefill_alloc(PrefillState& pf, int T_max, int k, int H, int F, int E);
+ft_status prefill_alloc(PrefillState& pf, int T_max, int k, int H, int F, int E, int fmt);
 void prefill_free(PrefillState& pf);
 // (Re)encode the B tensor maps for a slot pool (after init or a resize).
 ft_status prefill_set_pool(PrefillState& pf, const uint8_t* slot_pool, size_t record_bytes);
@@ -45,6 +48,10 @@ cudaError_t launch_pf_invalidate(int s0, int n, int* slot_for_id, int* id_for_sl
 cudaError_t launch_pf_route(PrefillState& pf, const float* logits, int T, unsigned* err, cudaStream_t s);
 cudaError_t launch_pf_permute(PrefillState& pf, int T, cudaStream_t s);
 cudaError_t launch_pf_gather(PrefillState& pf, const void* x, int T, cudaStream_t s);
-cudaError_t launch_pf_gemm1(PrefillState& pf, int buffer, int num_sms, unsigned* err, cudaStream_t s);
-cudaError_t launch_pf_gemm2(PrefillState& pf, int buffer, int num_sms, unsigned* err, cudaStream_t s);
+cudaError_t launch_pf_dequant(PrefillState& pf, const uint8_t* layer_records, cudaStream_t s);
+// expert_scale: per-expert fp32 factor of this layer's weights (NVFP4 global), or null
+cudaError_t launch_pf_gemm1(PrefillState& pf, int buffer, const float* expert_scale, int num_sms, unsigned* err,
+                            cudaStream_t s);
+cudaError_t launch_pf_gemm2(PrefillState& pf, int buffer, const float* expert_scale, int num_sms, unsigned* err,
+                            cudaStream_t s);
 cudaError_t launch_pf_combine(PrefillState& pf, int T, float* y, cudaStream_t s);

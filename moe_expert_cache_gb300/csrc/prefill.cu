@@ -242,6 +242,7 @@ struct GemmArgs {
     float* fout;           // mode 1: [rows, ldo]
     int ldo;
     const float* row_gate; // mode 1: gate of each expert-ordered row
+    const float* escale;   // per-expert factor of the weights (NVFP4 global) or null
     unsigned* err;
 };
 
@@ -382,7 +383,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) grouped_gemm_kernel(const __g
             const bool valid = r < ti.rows;
             const int row = ti.m0 + r;
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * GN);
-            const float gate = (p.mode == 1 && valid) ? p.row_gate[row] : 0.f;
+            const float es = p.escale ? p.escale[ti.e] : 1.f;
+            const float gate = (p.mode == 1 && valid) ? p.row_gate[row] * es : 0.f;
 #pragma unroll 1
             for (int c = 0; c < GN / 32; ++c) {
                 uint32_t v[32];
@@ -395,8 +397,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) grouped_gemm_kernel(const __g
                     uint32_t packed[8];
 #pragma unroll
                     for (int i2 = 0; i2 < 8; ++i2) {
-                        const float g0 = __uint_as_float(v[2 * i2]), g1 = __uint_as_float(v[2 * i2 + 1]);
-                        const float u0 = __uint_as_float(v[16 + 2 * i2]), u1 = __uint_as_float(v[16 + 2 * i2 + 1]);
+                        const float g0 = es * __uint_as_float(v[2 * i2]), g1 = es * __uint_as_float(v[2 * i2 + 1]);
+                        const float u0 = es * __uint_as_float(v[16 + 2 * i2]);
+                        const float u1 = es * __uint_as_float(v[16 + 2 * i2 + 1]);
                         const float h0 = g0 / (1.f + expf(-g0)) * u0;
                         const float h1 = g1 / (1.f + expf(-g1)) * u1;
                         const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
@@ -481,9 +484,14 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
 
 }  // namespace
 
-ft_status prefill_alloc(PrefillState& pf, int T_max, int k, int H, int F, int E) {
+ft_status prefill_alloc(PrefillState& pf, int T_max, int k, int H, int F, int E, int fmt) {
     pf.T_max = T_max;
     pf.E = E; pf.k = k; pf.H = H; pf.F = F;
+    pf.fmt = fmt;
+    if (fmt == FT_FMT_NVFP4 && cudaMalloc(&pf.staging, (size_t)E * 3 * H * F * 2) != cudaSuccess) {
+        cudaGetLastError();
+        return FT_ERR_OOM;
+    }
     const size_t TK = (size_t)T_max * k;
     if (cudaMalloc(&pf.xperm, TK * H * 2) != cudaSuccess || cudaMalloc(&pf.hperm, TK * F * 2) != cudaSuccess ||
         cudaMalloc(&pf.outp, TK * H * 4) != cudaSuccess || cudaMalloc(&pf.ids, TK * 4) != cudaSuccess ||
@@ -509,10 +517,15 @@ ft_status prefill_alloc(PrefillState& pf, int T_max, int k, int H, int F, int E)
 
 ft_status prefill_set_pool(PrefillState& pf, const uint8_t* pool, size_t rb) {
     const uint64_t E = pf.E, H = pf.H, F = pf.F;
+    pf.rb = rb;
     for (int b = 0; b < 2; ++b) {
-        const uint8_t* base = pool + (size_t)b * E * rb;
-        if (!encode_3d(&pf.mapB1[b], base, 2 * F, H, E, rb, GN) ||
-            !encode_3d(&pf.mapB2[b], base + 2 * F * H * 2, H, F, E, rb, GN))
+        // BF16: the GEMMs read the buffer's records in place; NVFP4: the bf16
+        // staging copy of the layer (one, reused by both buffers in turn)
+        const uint8_t* base = pf.fmt == FT_FMT_NVFP4 ? static_cast<const uint8_t*>(pf.staging)
+                                                     : pool + (size_t)b * E * rb;
+        const uint64_t rbb = pf.fmt == FT_FMT_NVFP4 ? 3 * H * F * 2 : rb;
+        if (!encode_3d(&pf.mapB1[b], base, 2 * F, H, E, rbb, GN) ||
+            !encode_3d(&pf.mapB2[b], base + 2 * F * H * 2, H, F, E, rbb, GN))
             return FT_ERR_CUDA;
     }
     pf.maps_pool = pool;
@@ -530,6 +543,7 @@ void prefill_free(PrefillState& pf) {
     cudaFree(pf.row_gate);
     cudaFree(pf.counts);
     cudaFree(pf.offsets);
+    cudaFree(pf.staging);
     for (int b = 0; b < 2; ++b) {
         if (pf.loaded[b]) cudaEventDestroy(pf.loaded[b]);
         if (pf.released[b]) cudaEventDestroy(pf.released[b]);
@@ -577,8 +591,10 @@ static cudaError_t launch_gemm(const CUtensorMap& A, const CUtensorMap& B, const
     return cudaGetLastError();
 }
 
-cudaError_t launch_pf_gemm1(PrefillState& pf, int buffer, int num_sms, unsigned* err, cudaStream_t s) {
+cudaError_t launch_pf_gemm1(PrefillState& pf, int buffer, const float* escale, int num_sms, unsigned* err,
+                            cudaStream_t s) {
     GemmArgs a{};
+    a.escale = escale;
     a.E = pf.E;
     a.nk = pf.H / GK;
     a.n_tiles = 2 * pf.F / GN;
@@ -590,8 +606,10 @@ cudaError_t launch_pf_gemm1(PrefillState& pf, int buffer, int num_sms, unsigned*
     return launch_gemm(pf.mapA1, pf.mapB1[buffer], a, num_sms, s);
 }
 
-cudaError_t launch_pf_gemm2(PrefillState& pf, int buffer, int num_sms, unsigned* err, cudaStream_t s) {
+cudaError_t launch_pf_gemm2(PrefillState& pf, int buffer, const float* escale, int num_sms, unsigned* err,
+                            cudaStream_t s) {
     GemmArgs a{};
+    a.escale = escale;
     a.E = pf.E;
     a.nk = pf.F / GK;
     a.n_tiles = pf.H / GN;
@@ -606,5 +624,77 @@ cudaError_t launch_pf_gemm2(PrefillState& pf, int buffer, int num_sms, unsigned*
 
 cudaError_t launch_pf_combine(PrefillState& pf, int T, float* y, cudaStream_t s) {
     pf_combine_kernel<<<T, 256, 0, s>>>(pf.outp, pf.pos, pf.k, pf.H, y);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------- NVFP4 -> bf16 staging
+
+namespace {
+
+// Expand E NVFP4 records into the bf16 record layout: every weight becomes
+// e2m1(value) * e4m3(block scale), which bf16 holds exactly (at most 6
+// significant bits); the per-expert fp32 global is applied by the GEMM
+// epilogues.  One thread per 32 values (one 16-byte group of codes).
+__global__ void __launch_bounds__(256) pf_dequant_kernel(const uint8_t* __restrict__ src, size_t rb4, int E, int H,
+                                                         int F, uint8_t* __restrict__ dst) {
+    __shared__ float e2m1[16];
+    __shared__ float e4m3[256];
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        const int e = (i >> 3) & 15, m = i & 7;
+        const float v = e == 0 ? ldexpf((float)m / 8.f, -6) : ldexpf(1.f + (float)m / 8.f, e - 7);
+        e4m3[i] = (i & 0x80) ? -v : v;
+        if (i < 16) {
+            const int c = i & 7;
+            const float mag = c < 2 ? 0.5f * (float)c : (1.f + 0.5f * (float)(c & 1)) * (float)(1 << ((c >> 1) - 1));
+            e2m1[i] = (i & 8) ? -mag : mag;
+        }
+    }
+    __syncthreads();
+    const size_t VGU = (size_t)F * H, VD = (size_t)H * F / 2, SGU = (size_t)2 * F * H / 16;
+    const size_t rb16 = (size_t)3 * H * F * 2;
+    const size_t gu_units = (size_t)2 * F * H / 32, units = (size_t)3 * H * F / 32;
+    const size_t total = units * E;
+    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += (size_t)gridDim.x * blockDim.x) {
+        const size_t e = u / units, w = u - e * units;
+        const uint8_t* rec = src + e * rb4;
+        uint8_t* out = dst + e * rb16;
+        const uint8_t* codes;
+        const uint8_t* sc;
+        uint8_t* o;
+        if (w < gu_units) {  // W_gu: value group w of row w / (H/32)
+            const size_t r = w / (H / 32), c = w - r * (H / 32);
+            codes = rec + r * (H / 2) + c * 16;
+            sc = rec + VGU + VD + r * (H / 16) + c * 2;
+            o = out + (r * H + c * 32) * 2;
+        } else {
+            const size_t w2 = w - gu_units, r = w2 / (F / 32), c = w2 - r * (F / 32);
+            codes = rec + VGU + r * (F / 2) + c * 16;
+            sc = rec + VGU + VD + SGU + r * (F / 16) + c * 2;
+            o = out + (size_t)2 * F * H * 2 + (r * F + c * 32) * 2;
+        }
+        const uint4 q = *reinterpret_cast<const uint4*>(codes);
+        const float s0 = e4m3[sc[0]], s1 = e4m3[sc[1]];
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t b = (wd[i >> 2] >> (8 * (i & 3))) & 255u;
+            const float s = i < 8 ? s0 : s1;
+            const __nv_bfloat162 v = __floats2bfloat162_rn(e2m1[b & 15] * s, e2m1[b >> 4] * s);
+            packed[i] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pf_dequant(PrefillState& pf, const uint8_t* layer_records, cudaStream_t s) {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+    pf_dequant_kernel<<<sms * 8, 256, 0, s>>>(layer_records, pf.rb, pf.E, pf.H, pf.F,
+                                              static_cast<uint8_t*>(pf.staging));
     return cudaGetLastError();
 }

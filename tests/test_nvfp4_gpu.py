@@ -112,3 +112,49 @@ def test_large_nvfp4_decode(ft):
     done = _replay(ft, wl.shape, wl.S, [(1, 64), (64, 64)], wl.B_P, wl.B_H, wl.rho, samples,
                    tok_sample=[0, 21, 42, 63])
     assert len(done) == len(samples)
+
+
+def _run_prefill_fp4(ft, sh, S, T, check_layers, tok_sample=None, seed=0):
+    import torch
+    pool, glob = hz.pinned_pool(sh, seed)
+    pool_np = pool.numpy()
+    cs, ts = torch.cuda.Stream(), torch.cuda.Stream()
+    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, S, pool, fmt=ft.FT_FMT_NVFP4, T_max=1, T_prefill_max=T,
+                     nvfp4_global=glob, compute_stream=cs.cuda_stream, transfer_stream=ts.cuda_stream)
+    xs = [synth.tokens_bf16(seed, 901, l, T, sh.H) for l in range(sh.L)]
+    lgs = [synth.iid_logits(seed, (901, l), T, sh.E) for l in range(sh.L)]
+    xd = [_dev(x.view(np.int16)).view(torch.bfloat16) for x in xs]
+    ld = [_dev(lg) for lg in lgs]
+    ys = [torch.empty(T, sh.H, dtype=torch.float32, device="cuda") for _ in range(sh.L)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(cs):
+        ctx.prefill_begin(0)
+        for l in range(sh.L):
+            ctx.prefill_layer(l & 1, l, l + 1 if l + 1 < sh.L else -1, T, xd[l], ld[l], ys[l])
+    torch.cuda.synchronize()
+    assert ctx.status() == ft.FT_OK
+    rels = []
+    for l in check_layers:
+        toks = list(range(T)) if tok_sample is None else tok_sample
+        ids, gates = zip(*[ctl.topk_route(lgs[l][t], sh.k) for t in toks])
+        ref = nm.gated_sum(nm.bf16_to_f64(xs[l][toks]), ids, gates, lambda t, j: True,
+                           FP4Weights(pool_np, glob, sh, l))
+        y = ys[l].cpu().numpy()
+        assert np.isfinite(y).all()
+        rel = nm.rel_l2(y[toks], ref)
+        assert rel <= NVFP4_REL_L2, (l, rel)
+        rels.append(rel)
+    ctx.close()
+    return rels
+
+
+def test_nvfp4_prefill_small(ft):
+    sh = synth.Shape(L=2, E=8, k=2, H=256, F=256, fmt=synth.FMT_NVFP4)
+    _run_prefill_fp4(ft, sh, 16, 300, [0, 1])
+
+
+@pytest.mark.slow
+def test_large_nvfp4_prefill(ft):
+    """Large NVFP4 prefill: T=4096 through all 8 layers of E=256, H=4096, F=2048."""
+    wl = synth.LARGE_NVFP4
+    _run_prefill_fp4(ft, wl.shape, wl.S, 4096, [0, 7], tok_sample=[0, 1000, 2047, 3001, 4095])
