@@ -105,12 +105,15 @@ const char* ft_status_str(ft_status s);
  *   L, E, k, H, F  sizes; need E <= 1024, k <= 16, k <= E, H % 64 == 0,
  *                  F % 64 == 0 (H, F >= 64).
  *   S              number of slots (>= 1).  Prefill needs S >= 2E.
- *   fmt            FT_FMT_BF16 or FT_FMT_NVFP4 (record layout in ft_record_bytes).
+ *   fmt            FT_FMT_BF16 or FT_FMT_NVFP4 (record layout in ft_record_bytes);
+ *                  NVFP4 needs H % 256 == 0, F % 256 == 0 and nvfp4_global.
  *   T_max          largest T of a decode call (ft_route_ctl), 1..256, with
  *                  T_max*k <= 4096 and T_max*H <= 32768 (the tokens of a
  *                  decode call are staged in shared memory).
  *   T_prefill_max  largest T of a prefill layer call; 0 disables prefill (no
- *                  prefill scratch is allocated).
+ *                  prefill scratch is allocated).  Prefill needs H % 256 == 0,
+ *                  2F % 256 == 0 and E <= 256.  NVFP4 contexts with prefill
+ *                  also hold a bf16 staging copy of one layer (E*6*H*F bytes).
  *   host_pool      HOST address of the caller's expert pool: L*E records of
  *                  ft_record_bytes(H,F,fmt) bytes, record l*E+e at offset
  *                  (l*E+e)*record_bytes.  Must be page-locked (cudaHostAlloc /
@@ -206,8 +209,8 @@ ft_status ft_prefill_begin(ft_ctx* ctx, int32_t layer);
  * writes y_t = sum_j g_tj FFN_{e_tj}(x_t) (j ascending).  next_layer = -1
  * closes the chunk; the buffer slots are left empty afterwards.
  *
- *   buffer      0 or 1; must equal the buffer the layer was streamed into
- *               (layer & 1 counted from the chunk's first layer parity).
+ *   buffer      0 or 1: the i-th layer of a chunk (counting from 0 at
+ *               ft_prefill_begin) is held by buffer i & 1.
  *   layer       layer held by `buffer`.
  *   next_layer  layer to stream next, or -1.
  *   T           tokens, 1..T_prefill_max.

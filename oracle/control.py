@@ -28,9 +28,10 @@ Readings taken where the pages are silent (each is also stated where used):
      (smallest (stamp, slot) first) until min(S', occupied) remain, and packs
      the survivors, in ascending old slot order, into slots 0..n-1; growing
      keeps every slot index; stamps and clock are kept.
-  R7 prefill: before layer l is copied into buffer b = l & 1 (slots
-     [b*E, (b+1)*E)), every owner of those slots is cleared and the slots are
-     left empty with stamp 0 after the prefill.
+  R7 prefill: the i-th layer of a prefill chunk is copied into buffer
+     b = i & 1 (slots [b*E, (b+1)*E)); before the copy every owner of those
+     slots is cleared, and the slots are left empty with stamp 0 after the
+     prefill.
 """
 from __future__ import annotations
 
