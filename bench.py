@@ -209,20 +209,20 @@ def host_pool(shape: synth.Shape, seed: int, world: int, rank: int):
 def kernel_bytes(shape: synth.Shape, T: int, dcnt: dict) -> dict:
     """Algorithmic bytes moved by each decode kernel over the timed region.
 
-    fill: every fill copies one record (read over the host link, written to HBM).
-    expert_ffn: the whole record of every GPU expert (3*F*H*2 B: W_gu and W_d)
-        + x read + h written and read once (fp32) + partial_C read + y written.
+    expert_ffn (with the fused fill):
+        link: every fill copies one record over the host link;
+        hbm:  the fills written to HBM + the whole record of every GPU expert
+              read (3*F*H*2 B) + x read + h written and read once (fp32)
+              + partial_C read + y written.
     route_ctl: logits + ids/gates written (small; reported for completeness).
     """
     H, F, E, L, k = shape.H, shape.F, shape.E, shape.L, shape.k
     ugpu = dcnt["hits"] + dcnt["fills"]
     calls = dcnt["calls"]
     rb = shape.record_bytes
-    return {
-        "fill": dcnt["fills"] * rb,
-        "expert_ffn": ugpu * 3 * F * H * 2 + calls * T * H * 2 + 2 * dcnt["assign"] * F * 4 + calls * T * H * 4 * 2,
-        "route_ctl": calls * (T * E * 4 + 2 * T * k * 4),
-    }
+    link = dcnt["fills"] * rb
+    hbm = link + ugpu * rb + calls * T * H * 2 + 2 * dcnt["assign"] * F * 4 + calls * T * H * 4 * 2
+    return {"expert_ffn": {"link": link, "hbm": hbm}, "route_ctl": {"hbm": calls * (T * E * 4 + 2 * T * k * 4)}}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -357,32 +357,25 @@ def run_ours(args, rank, world, local_rank):
     kernels = {}
     launches_total = dcnt["calls"]  # each decode kernel runs once per control pass
     for name, v in prof.items():
-        ent = {"launches_timed": v["launches"], "ms_total": round(v["ms"], 3),
-               "us_per_launch": round(1e3 * v["ms"] / v["launches"], 3),
+        us = 1e3 * v["ms"] / v["launches"]
+        ent = {"launches_timed": v["launches"], "ms_total": round(v["ms"], 3), "us_per_launch": round(us, 3),
                "share": round(v["ms"] / total_ms, 4)}
-        if name in kb and v["ms"] > 0:
-            # algorithmic bytes per launch (average over all timed-region launches)
-            bpl = kb[name] / max(1, launches_total)
-            ent["bytes_per_launch"] = int(bpl)
-            gbs = bpl / (1e-3 * v["ms"] / v["launches"]) / 1e9
-            ent["achieved_GBps"] = round(gbs, 1)
-            if name == "fill":
-                ent["peak_GBps"] = round(h2d_peak, 1) if h2d_peak else None
-                ent["bound"] = "host link"
-            else:
-                ent["peak_GBps"] = peaks["hbm_gbs"]
-                ent["bound"] = "hbm"
-            if ent.get("peak_GBps"):
-                ent["frac"] = round(gbs / ent["peak_GBps"], 4)
+        if name in kb:
+            for kind, byts in kb[name].items():
+                bpl = byts / max(1, launches_total)
+                gbs = bpl / (us * 1e-6) / 1e9
+                peak = h2d_peak if kind == "link" else peaks["hbm_gbs"]
+                ent[kind] = {"bytes_per_launch": int(bpl), "achieved_GBps": round(gbs, 1),
+                             "peak_GBps": round(peak, 1) if peak else None,
+                             "frac": round(gbs / peak, 4) if peak else None}
         kernels[name] = ent
     dom = max(prof, key=lambda n: prof[n]["ms"])
-    hbm_kernels = [n for n in ("expert_ffn",) if n in prof]
-    exp_gbs = kernels["expert_ffn"].get("achieved_GBps", 0.0) if "expert_ffn" in kernels else 0.0
     roofline = roofline_entry(dom, kernels, peaks, h2d_peak)
-    expert_roofline = {"kernels": hbm_kernels, "bound": "hbm", "achieved": round(exp_gbs, 1),
-                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(exp_gbs / peaks["hbm_gbs"], 4),
-                       "peak_source": peaks["source"],
-                       "traffic": traffic_from_profiles("expert_ffn")}
+    ex = kernels.get("expert_ffn", {})
+    expert_roofline = {"kernel": "expert_ffn", "bound": "hbm",
+                       "achieved": ex.get("hbm", {}).get("achieved_GBps"), "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": ex.get("hbm", {}).get("frac"), "peak_source": peaks["source"],
+                       "note": "HBM side of the fused kernel; its time also covers the fill over the host link"}
 
     value = world * T * K / (t_max_ms * 1e-3)
     out = {
@@ -401,7 +394,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "roofline_expert_kernels": expert_roofline,
         "kernels": kernels,
-        "gpu_launches": int(3 * dcnt["calls"]),
+        "gpu_launches": int(2 * dcnt["calls"]),
         "kernel_timing": f"library CUDA-event records around each launch of 1 timed step in {PROFILE_EVERY}",
         "clocks": clk,
         "e2e": {"value": round(world * T * K / (e2e_ms * 1e-3), 2), "unit": UNIT,
@@ -505,16 +498,19 @@ def run_prefill_bench(device, peaks, reps: int = 3) -> dict:
 
 
 def roofline_entry(dom, kernels, peaks, h2d_peak):
+    """Roofline of the dominant kernel: the side (host link or HBM) whose
+    bytes at peak take longer is the bound."""
     ent = kernels[dom]
-    per_launch = ent.get("bytes_per_launch", 0)
-    if dom == "fill":
-        bound, peak, src = "h2d", h2d_peak, "measured live: pinned host->device cudaMemcpyAsync, 1 GiB, best of 3"
+    link, hbm = ent.get("link"), ent.get("hbm", {})
+    t_link = link["bytes_per_launch"] / (h2d_peak * 1e9) if link and h2d_peak else 0.0
+    t_hbm = hbm.get("bytes_per_launch", 0) / (peaks["hbm_gbs"] * 1e9)
+    if t_link >= t_hbm and link:
+        side, bound, src = link, "h2d", "measured live: pinned host->device cudaMemcpyAsync, 1 GiB, best of 4"
     else:
-        bound, peak, src = "hbm", peaks["hbm_gbs"], peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
-    ach = ent.get("achieved_GBps", 0.0)
-    return {"kernel": dom, "bound": bound, "achieved": ach, "peak": round(peak, 1) if peak else None,
-            "unit": "GB/s", "frac": round(ach / peak, 4) if peak else None, "peak_source": src,
-            "bytes_per_launch": int(per_launch), "us_per_launch": ent["us_per_launch"],
+        side, bound, src = hbm, "hbm", peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
+    return {"kernel": dom, "bound": bound, "achieved": side.get("achieved_GBps"), "peak": side.get("peak_GBps"),
+            "unit": "GB/s", "frac": side.get("frac"), "peak_source": src,
+            "bytes_per_launch": side.get("bytes_per_launch"), "us_per_launch": ent["us_per_launch"],
             "traffic": traffic_from_profiles(dom)}
 
 

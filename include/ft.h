@@ -152,7 +152,12 @@ size_t ft_record_bytes(int32_t H, int32_t F, int32_t fmt);
  * not holding a hit of this call (smallest (stamp, slot)); hits and fills get
  * the pass's clock as stamp; route ids are rewritten to slot ids; then the q
  * complete records are copied from the host pool into their victim slots.
- * All of it runs on the device: no host synchronisation.
+ * All of it runs on the device: no host synchronisation.  The copies are
+ * enqueued with the next ft_moe_forward of the context, fused into its
+ * expert kernel (the fill overlaps the computation on the hits); every other
+ * call of the context that reads or changes the slots (ft_route_ctl,
+ * ft_read_slot, ft_get/set_ctl_state, ft_cache_resize, ft_prefill_begin,
+ * ft_get_status) first completes a pending fill with a standalone copy.
  *
  *   layer     0..L-1.
  *   T         tokens, 1..T_max.

@@ -33,7 +33,8 @@ namespace {
 
 constexpr int CONSUMER_WARPS = 8;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;
-constexpr int EXPERT_THREADS = CONSUMERS + 32;  // + one producer warp
+constexpr int FILL_WARPS = 4;                   // fused cache fill
+constexpr int EXPERT_THREADS = CONSUMERS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
 constexpr int FPC = CONSUMER_WARPS;             // features per phase-A chunk
 constexpr size_t HEAD = 256;                    // barrier area
 
@@ -234,7 +235,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     int* m_tok = m_slot + TK;                          // [TK]   token of each assignment
     float* m_gate = reinterpret_cast<float*>(m_tok + TK);  // [TK]
     int* m_pos = reinterpret_cast<int*>(m_gate + TK);      // [TK]   assignment of (t, j)
-    o += ((size_t)(5 * TK + 1) * 4 + 127) & ~(size_t)127;
+    int* m_fill = m_pos + TK;                              // [TK]   fill index of entry (or -1)
+    o += ((size_t)(6 * TK + 1) * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
     const unsigned rowbytes = (unsigned)H * 2u;
     const unsigned wpart = ((unsigned)RMAX * F * 2u + 127u) & ~127u;  // h rows follow the W_d rows
@@ -248,7 +250,10 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         s_gdone = 0;
     }
     for (int i = tid; i <= ugpu; i += EXPERT_THREADS) m_off[i] = p.wl_off[i];
-    for (int i = tid; i < ugpu; i += EXPERT_THREADS) m_slot[i] = p.wl_slot[i];
+    for (int i = tid; i < ugpu; i += EXPERT_THREADS) {
+        m_slot[i] = p.wl_slot[i];
+        m_fill[i] = p.do_fill ? p.wl_fill[i] : -1;
+    }
     for (int i = tid; i < nasg; i += EXPERT_THREADS) {
         m_tok[i] = p.as_tok[i];
         m_gate[i] = p.as_gate[i];
@@ -267,16 +272,29 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     }
     __syncthreads();
 
+    // --------------------------------------------------------- fused fill
+    if (wid > CONSUMER_WARPS) {
+        if (p.do_fill)
+            ft::fill_share(p.host_pool, reinterpret_cast<uint4*>(const_cast<uint8_t*>(p.slot_pool)), p.rec16,
+                           p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G, tid - (CONSUMERS + 32),
+                           FILL_WARPS * 32, 2);
+        return;
+    }
     // ------------------------------------------------------------ producer
     if (wid == CONSUMER_WARPS) {
         if (lane == 0) {
             const uint64_t pol = ft::l2_policy_evict_first();
             int it = 0;
             bool ok = true;
+            int waited = -1;  // last fill index known complete
             for (int a = a0; a < a1 && ok; ++a, ++it) {
                 const int st = it % nst;
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
                 const int ent = a / cpe;
+                if (m_fill[ent] >= 0 && m_fill[ent] != waited) {
+                    if (!ft::wait_filled(p.ready, m_fill[ent], (unsigned)G, p.err)) { ok = false; break; }
+                    waited = m_fill[ent];
+                }
                 const int f0 = (a - ent * cpe) * FPC;
                 const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
                 const int grp = f0 >> 4, i = f0 & 15;
@@ -298,6 +316,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 const int off = m_off[e];
                 const unsigned hb = (unsigned)(m_off[e + 1] - off) * F * 4u;
                 unsigned char* dst = ring + (size_t)st * slot_bytes;
+                if (m_fill[e] >= 0 && !ft::wait_filled(p.ready, m_fill[e], (unsigned)G, p.err)) { ok = false; break; }
                 const uint8_t* wd = p.slot_pool + (size_t)m_slot[e] * p.rb + (size_t)2 * F * H * 2 + (size_t)r0 * F * 2;
                 ft::mbar_arrive_expect_tx(&full[st], wb + hb);
                 ft::bulk_g2s_hint(dst, wd, wb, &full[st], pol);
@@ -414,7 +433,7 @@ cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     const size_t xbytes = (size_t)p.T * p.H * (xf32 ? 4 : 2);
     const size_t TK = (size_t)p.T * p.k;
     const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) +
-                        ((TK * RMAX * 4 + 127) & ~(size_t)127) + (((5 * TK + 1) * 4 + 127) & ~(size_t)127);
+                        ((TK * RMAX * 4 + 127) & ~(size_t)127) + (((6 * TK + 1) * 4 + 127) & ~(size_t)127);
     size_t slot = (size_t)2 * FPC * p.H * 2;
     const size_t down = (((size_t)RMAX * p.F * 2 + 127) & ~(size_t)127) + (size_t)p.T * p.F * 4;
     if (down > slot) slot = down;

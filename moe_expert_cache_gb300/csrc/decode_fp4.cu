@@ -24,7 +24,8 @@ namespace {
 
 constexpr int CW = 8;                 // consumer warps
 constexpr int CONS = CW * 32;
-constexpr int THREADS = CONS + 32;    // + producer warp
+constexpr int FILL_WARPS = 4;         // fused cache fill
+constexpr int THREADS = CONS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
 constexpr int FPC = CW;               // features per phase-A chunk
 constexpr size_t HEAD = 256;
 enum { X_F32_SMEM = 0, X_BF16_SMEM = 1, X_BF16_GLOBAL = 2 };
@@ -250,7 +251,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     float* m_gate = reinterpret_cast<float*>(m_tok + TK);
     int* m_pos = reinterpret_cast<int*>(m_gate + TK);
     float* m_gs = reinterpret_cast<float*>(m_pos + TK);   // global scale of each entry
-    o += ((size_t)(6 * TK + 1) * 4 + 127) & ~(size_t)127;
+    int* m_fill = reinterpret_cast<int*>(m_gs + TK);      // fill index of each entry (or -1)
+    o += ((size_t)(7 * TK + 1) * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
     const unsigned wpart = ((unsigned)RMAX * (dvrow + dsrow) + 127u) & ~127u;
     const void* xsrc = XM == X_BF16_GLOBAL ? static_cast<const void*>(p.x) : x_s;
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     for (int i = tid; i < ugpu; i += THREADS) {
         m_slot[i] = p.wl_slot[i];
         m_gs[i] = p.gscale[p.wl_fid[i]];
+        m_fill[i] = p.do_fill ? p.wl_fill[i] : -1;
     }
     for (int i = tid; i < nasg; i += THREADS) {
         m_tok[i] = p.as_tok[i];
@@ -287,16 +290,29 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     }
     __syncthreads();
 
+    // --------------------------------------------------------- fused fill
+    if (wid > CW) {
+        if (p.do_fill)
+            ft::fill_share(p.host_pool, reinterpret_cast<uint4*>(const_cast<uint8_t*>(p.slot_pool)), p.rec16,
+                           p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G, tid - (CONS + 32),
+                           FILL_WARPS * 32, 2);
+        return;
+    }
     // ------------------------------------------------------------ producer
     if (wid == CW) {
         if (lane == 0) {
             const uint64_t pol = ft::l2_policy_evict_first();
             int it = 0;
             bool ok = true;
+            int waited = -1;
             for (int a = a0; a < a1 && ok; ++a, ++it) {
                 const int st = it % nst;
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
                 const int ent = a / cpe;
+                if (m_fill[ent] >= 0 && m_fill[ent] != waited) {
+                    if (!ft::wait_filled(p.ready, m_fill[ent], (unsigned)G, p.err)) { ok = false; break; }
+                    waited = m_fill[ent];
+                }
                 const int f0 = (a - ent * cpe) * FPC;
                 const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
                 const int grow = (f0 >> 4) * 32 + (f0 & 15);  // first gate row; up rows 16 later
@@ -323,6 +339,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 const int off = m_off[e], ntok = m_off[e + 1] - off;
                 const int ng = min(TG, ntok - g0);
                 const uint8_t* rec = p.slot_pool + (size_t)m_slot[e] * p.rb;
+                if (g0 == 0 && m_fill[e] >= 0 && !ft::wait_filled(p.ready, m_fill[e], (unsigned)G, p.err)) {
+                    ok = false;
+                    break;
+                }
                 unsigned char* dst = ring + (size_t)st * slot_bytes;
                 const unsigned wb = (unsigned)R * dvrow, sb = (unsigned)R * dsrow, hb = (unsigned)ng * F * 4u;
                 ft::mbar_arrive_expect_tx(&full[st], wb + sb + hb);
@@ -445,7 +465,7 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
         }
     }
     const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127) +
-                        (((6 * TK + 1) * 4 + 127) & ~(size_t)127);
+                        (((7 * TK + 1) * 4 + 127) & ~(size_t)127);
     const size_t chunk = (size_t)2 * FPC * (p.H / 2 + p.H / 16);
     const size_t wpart = ((size_t)RMAX * (p.F / 2 + p.F / 16) + 127) & ~(size_t)127;
     if (head + 2 * chunk > kSmemLimit4) return cudaErrorInvalidValue;

@@ -44,12 +44,14 @@ struct ft_ctx {
     // fixed-size control outputs and worklists (one arena)
     void* arena;
     unsigned* clock;
-    int *ids, *slots_topk, *pos, *as_tok, *wl_slot, *wl_off, *wl_fid, *fill_slot, *fill_fid, *Fl, *Cl, *victims, *info;
+    int *ids, *slots_topk, *pos, *as_tok, *wl_slot, *wl_off, *wl_fid, *wl_fill, *fill_slot, *fill_fid, *Fl, *Cl, *victims, *info;
     float *gates, *as_gate;
     unsigned long long* counters;
     unsigned* err;
     unsigned* gbar;
+    unsigned* ready;
     float* hbuf;
+    bool fill_pending;
     int last_T;
     bool have_ctl;
     PrefillState pf;
@@ -134,6 +136,22 @@ void free_ctx(ft_ctx* c) {
     cudaFree(c->arena);
     cudaFree(c->hbuf);
     delete c;
+}
+
+// Run a pending cache fill with the standalone kernel (the fill of a control
+// pass is normally fused into the following ft_moe_forward).
+cudaError_t flush_fill(ft_ctx* c) {
+    if (!c->fill_pending) return cudaSuccess;
+    c->fill_pending = false;
+    FillParams fp{};
+    fp.host_pool = (const uint4*)c->host_pool_dev;
+    fp.slot_pool = (uint4*)c->slot_pool;
+    fp.rec16 = c->rb / 16;
+    fp.info = c->info;
+    fp.fill_slot = c->fill_slot;
+    fp.fill_fid = c->fill_fid;
+    ProfScope ps(c->prof, FT_K_FILL, c->cs);
+    return launch_fill(fp, 2 * c->num_sms, c->cs);
 }
 
 }  // namespace
@@ -224,7 +242,8 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     auto carve = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     const size_t o_clock = carve(4), o_ids = carve(TK * 4), o_gates = carve(TK * 4), o_slots = carve(TK * 4),
                  o_pos = carve(TK * 4), o_astok = carve(TK * 4), o_asg = carve(TK * 4),
-                 o_wls = carve((size_t)E * 4), o_wlo = carve((size_t)(E + 1) * 4), o_wlf = carve((size_t)E * 4),
+                 o_wls = carve((size_t)E * 4), o_wlo = carve((size_t)(E + 1) * 4), o_wlf = carve((size_t)E * 4), o_wlfill = carve((size_t)E * 4),
+                 o_ready = carve((size_t)E * 4),
                  o_fs = carve((size_t)E * 4),
                  o_ff = carve((size_t)E * 4), o_F = carve((size_t)E * 4), o_C = carve((size_t)E * 4),
                  o_v = carve((size_t)E * 4), o_info = carve(INFO_WORDS * 4), o_cnt = carve(CNT_WORDS * 8),
@@ -242,6 +261,8 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     c->wl_slot = (int*)(a + o_wls);
     c->wl_off = (int*)(a + o_wlo);
     c->wl_fid = (int*)(a + o_wlf);
+    c->wl_fill = (int*)(a + o_wlfill);
+    c->ready = (unsigned*)(a + o_ready);
     c->fill_slot = (int*)(a + o_fs);
     c->fill_fid = (int*)(a + o_ff);
     c->Fl = (int*)(a + o_F);
@@ -274,13 +295,15 @@ ft_status ft_route_ctl(ft_ctx* c, int32_t layer, int32_t T, const float* logits,
     if ((logits != nullptr) == (topk_ids != nullptr || topk_w != nullptr)) return FT_ERR_ARG;
     if (!logits && (!topk_ids || !topk_w)) return FT_ERR_ARG;
     if (c->pf.open) return FT_ERR_STATE;
+    FT_CUDA(flush_fill(c));
     CtlParams p{};
     p.layer = layer; p.T = T; p.E = c->E; p.k = c->k; p.L = c->L; p.S = c->S;
     p.logits = logits; p.topk_ids = topk_ids; p.topk_w = topk_w;
     p.B_P = B_P; p.B_H = B_H;
     p.slot_for_id = c->slot_for_id; p.id_for_slot = c->id_for_slot; p.stamps = c->stamps; p.clock = c->clock;
     p.out_ids = c->ids; p.out_gates = c->gates; p.out_slots = c->slots_topk; p.out_pos = c->pos;
-    p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.wl_fid = c->wl_fid; p.as_tok = c->as_tok; p.as_gate = c->as_gate;
+    p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.wl_fid = c->wl_fid; p.wl_fill = c->wl_fill; p.ready = c->ready;
+    p.as_tok = c->as_tok; p.as_gate = c->as_gate;
     p.fill_slot = c->fill_slot; p.fill_fid = c->fill_fid;
     p.out_F = c->Fl; p.out_C = c->Cl; p.out_victims = c->victims;
     p.info = c->info; p.counters = c->counters; p.err = c->err;
@@ -288,15 +311,7 @@ ft_status ft_route_ctl(ft_ctx* c, int32_t layer, int32_t T, const float* logits,
         ProfScope ps(c->prof, FT_K_ROUTE_CTL, c->cs);
         FT_CUDA(launch_route_ctl(p, c->cs));
     }
-    FillParams fp{};
-    fp.host_pool = (const uint4*)c->host_pool_dev;
-    fp.slot_pool = (uint4*)c->slot_pool;
-    fp.rec16 = c->rb / 16;
-    fp.info = c->info; fp.fill_slot = c->fill_slot; fp.fill_fid = c->fill_fid;
-    {
-        ProfScope ps(c->prof, FT_K_FILL, c->cs);
-        FT_CUDA(launch_fill(fp, 2 * c->num_sms, c->cs));
-    }
+    c->fill_pending = true;  // performed by the next ft_moe_forward, or flushed
     c->last_T = T;
     c->have_ctl = true;
     return FT_OK;
@@ -312,6 +327,14 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.info = c->info; p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok;
     p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err; p.gbar = c->gbar;
     p.wl_fid = c->wl_fid; p.gscale = c->nvfp4_global;
+    p.do_fill = c->fill_pending ? 1 : 0;
+    p.host_pool = (const uint4*)c->host_pool_dev;
+    p.rec16 = c->rb / 16;
+    p.fill_slot = c->fill_slot;
+    p.fill_fid = c->fill_fid;
+    p.wl_fill = c->wl_fill;
+    p.ready = c->ready;
+    c->fill_pending = false;
     {
         ProfScope ps(c->prof, FT_K_EXPERT, c->cs);
         if (c->fmt == FT_FMT_NVFP4)
@@ -328,6 +351,7 @@ ft_status ft_cache_resize(ft_ctx* c, int32_t S_new) {
     if (!c || S_new < 1) return FT_ERR_ARG;
     if (route_ctl_smem_bytes(c->T_max, c->k, c->E, S_new) > kCtlSmemMax) return FT_ERR_ARG;
     if (c->pf.open) return FT_ERR_STATE;
+    FT_CUDA(flush_fill(c));
     FT_CUDA(cudaStreamSynchronize(c->cs));
     if (c->ts) FT_CUDA(cudaStreamSynchronize(c->ts));
     const int S = c->S, LE = c->L * c->E;
@@ -408,6 +432,7 @@ ft_status ft_cache_resize(ft_ctx* c, int32_t S_new) {
 ft_status ft_get_ctl_state(ft_ctx* c, int32_t* slot_for_id, int32_t* id_for_slot, uint32_t* stamps,
                            uint32_t* clock) {
     if (!c) return FT_ERR_ARG;
+    FT_CUDA(flush_fill(c));
     FT_CUDA(cudaStreamSynchronize(c->cs));
     if (slot_for_id) FT_CUDA(cudaMemcpy(slot_for_id, c->slot_for_id, (size_t)c->L * c->E * 4, cudaMemcpyDeviceToHost));
     if (id_for_slot) FT_CUDA(cudaMemcpy(id_for_slot, c->id_for_slot, (size_t)c->S * 4, cudaMemcpyDeviceToHost));
@@ -432,6 +457,7 @@ ft_status ft_set_ctl_state(ft_ctx* c, const int32_t* slot_for_id, const int32_t*
         if (s < -1 || s >= S) return FT_ERR_ARG;
         if (s >= 0 && id_for_slot[s] != f) return FT_ERR_ARG;
     }
+    FT_CUDA(flush_fill(c));
     FT_CUDA(cudaStreamSynchronize(c->cs));
     FT_CUDA(cudaMemcpy(c->slot_for_id, slot_for_id, (size_t)LE * 4, cudaMemcpyHostToDevice));
     FT_CUDA(cudaMemcpy(c->id_for_slot, id_for_slot, (size_t)S * 4, cudaMemcpyHostToDevice));
@@ -466,6 +492,7 @@ ft_status ft_get_last_ctl(ft_ctx* c, ft_ctl_info* info, int32_t* F, int32_t* C, 
 
 ft_status ft_read_slot(ft_ctx* c, int32_t slot, void* host_dst) {
     if (!c || !host_dst || slot < 0 || slot >= c->S) return FT_ERR_ARG;
+    FT_CUDA(flush_fill(c));
     FT_CUDA(cudaStreamSynchronize(c->cs));
     if (c->ts) FT_CUDA(cudaStreamSynchronize(c->ts));
     FT_CUDA(cudaMemcpy(host_dst, c->slot_pool + (size_t)slot * c->rb, c->rb, cudaMemcpyDeviceToHost));
@@ -537,6 +564,7 @@ int32_t ft_num_slots(const ft_ctx* c) { return c ? c->S : 0; }
 
 ft_status ft_get_status(ft_ctx* c) {
     if (!c) return FT_ERR_ARG;
+    if (flush_fill(c) != cudaSuccess) return FT_ERR_CUDA;
     cudaError_t e1 = cudaStreamSynchronize(c->cs);
     cudaError_t e2 = c->ts ? cudaStreamSynchronize(c->ts) : cudaSuccess;
     if (e1 != cudaSuccess || e2 != cudaSuccess) return FT_ERR_CUDA;
@@ -564,6 +592,7 @@ ft_status ft_prefill_begin(ft_ctx* c, int32_t layer) {
     if (!c || layer < 0 || layer >= c->L) return FT_ERR_ARG;
     if (c->T_prefill_max <= 0 || c->pf.open) return FT_ERR_STATE;
     if (c->S < 2 * c->E) return FT_ERR_CAPACITY;
+    FT_CUDA(flush_fill(c));
     if (c->pf.maps_pool != c->slot_pool) {
         const ft_status st = prefill_set_pool(c->pf, c->slot_pool, c->rb);
         if (st != FT_OK) return st;

@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     int* s_vict = s_eoff + E;   // [E] victims by rank
     int* s_cslot = s_vict + E;  // [E] radix path: candidates with stamp < tau
     unsigned* s_cst = reinterpret_cast<unsigned*>(s_cslot + E);  // [E]
+    int* s_fillrank = reinterpret_cast<int*>(s_cst + E);         // [E] fill index of an F expert
 
     if (tid == 0) {
         sh.bad = 0;
@@ -430,6 +431,8 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         p.slot_for_id[fid] = v;
         p.stamps[v] = clk;
         s_slot[f] = v;
+        s_fillrank[f] = i;
+        p.ready[i] = 0u;
         p.fill_slot[i] = v;
         p.fill_fid[i] = fid;
         p.out_victims[i] = v;
@@ -454,6 +457,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             p.wl_slot[ent] = s_slot[e];
             p.wl_off[ent] = off;
             p.wl_fid[ent] = fbase + e;
+            p.wl_fill[ent] = s_cls[e] == 2 ? s_fillrank[e] : -1;
             s_eoff[e] = off;
         }
         __syncthreads();
@@ -519,7 +523,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
 
 size_t route_ctl_smem_bytes(int T, int k, int E, int S) {
     const size_t TW = (T + 63) / 64;
-    return (size_t)E * TW * 8 + (size_t)S * 8 + (size_t)T * k * 8 + (size_t)E * 10 * 4;
+    return (size_t)E * TW * 8 + (size_t)S * 8 + (size_t)T * k * 8 + (size_t)E * 11 * 4;
 }
 
 cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s) {
