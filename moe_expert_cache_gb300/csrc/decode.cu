@@ -33,7 +33,7 @@ namespace {
 
 constexpr int CONSUMER_WARPS = 8;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;
-constexpr int FILL_WARPS = 4;                   // fused cache fill
+constexpr int FILL_WARPS = 1;                   // fused cache fill (one TMA thread)
 constexpr int EXPERT_THREADS = CONSUMERS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
 constexpr int FPC = CONSUMER_WARPS;             // features per phase-A chunk
 constexpr size_t HEAD = 256;                    // barrier area
@@ -274,10 +274,11 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
 
     // --------------------------------------------------------- fused fill
     if (wid > CONSUMER_WARPS) {
-        if (p.do_fill)
-            ft::fill_share(p.host_pool, reinterpret_cast<uint4*>(const_cast<uint8_t*>(p.slot_pool)), p.rec16,
-                           p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G, tid - (CONSUMERS + 32),
-                           FILL_WARPS * 32, 2);
+        if (lane == 0 && p.do_fill)
+            ft::fill_share_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
+                               p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G,
+                               ring + (size_t)nst * slot_bytes, reinterpret_cast<uint64_t*>(smem + 128),
+                               p.fill_chunk, p.err);
         return;
     }
     // ------------------------------------------------------------ producer
@@ -439,12 +440,21 @@ cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     if (down > slot) slot = down;
     slot = (slot + 127) & ~(size_t)127;
     if (head >= kSmemLimit) return cudaErrorInvalidValue;
-    int nst = (int)((kSmemLimit - head) / slot);
+    // two fused-fill ring slots after the main ring: 16 KiB each, smaller if
+    // that would leave fewer than two main slots
+    size_t fch = 16384;
+    int nst = 0;
+    for (; fch >= 4096; fch /= 2) {
+        if (head + 2 * fch >= kSmemLimit) continue;
+        nst = (int)((kSmemLimit - head - 2 * fch) / slot);
+        if (nst >= 2) break;
+    }
     if (nst > 4) nst = 4;
     if (nst < 2) return cudaErrorInvalidValue;
     p.nstage = nst;
     p.stage_bytes = (unsigned)slot;
-    const size_t smem = head + slot * nst;
+    p.fill_chunk = (unsigned)fch;
+    const size_t smem = head + slot * nst + 2 * fch;
     static size_t smem_set = 0;
     if (smem != smem_set) {
         cudaError_t e = cudaFuncSetAttribute(expert_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -24,7 +24,7 @@ namespace {
 
 constexpr int CW = 8;                 // consumer warps
 constexpr int CONS = CW * 32;
-constexpr int FILL_WARPS = 4;         // fused cache fill
+constexpr int FILL_WARPS = 1;         // fused cache fill (one TMA thread)
 constexpr int THREADS = CONS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
 constexpr int FPC = CW;               // features per phase-A chunk
 constexpr size_t HEAD = 256;
@@ -292,10 +292,11 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
 
     // --------------------------------------------------------- fused fill
     if (wid > CW) {
-        if (p.do_fill)
-            ft::fill_share(p.host_pool, reinterpret_cast<uint4*>(const_cast<uint8_t*>(p.slot_pool)), p.rec16,
-                           p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G, tid - (CONS + 32),
-                           FILL_WARPS * 32, 2);
+        if (lane == 0 && p.do_fill)
+            ft::fill_share_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
+                               p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G,
+                               ring + (size_t)nst * slot_bytes, reinterpret_cast<uint64_t*>(smem + 128),
+                               p.fill_chunk, p.err);
         return;
     }
     // ------------------------------------------------------------ producer
@@ -471,20 +472,27 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
     if (head + 2 * chunk > kSmemLimit4) return cudaErrorInvalidValue;
     // token group of phase B: as many h rows as fit next to the W_d rows in a
     // slot when two slots fill the shared memory
-    int tg = (int)(((kSmemLimit4 - head) / 2 - wpart) / ((size_t)p.F * 4));
+    int tg = (int)(((kSmemLimit4 - head - 16384) / 2 - wpart) / ((size_t)p.F * 4));
     if (tg > p.T) tg = p.T;
     if (tg > 16) tg = 16;
     if (tg < 1) return cudaErrorInvalidValue;
     size_t slot = wpart + (size_t)tg * p.F * 4;
     if (slot < chunk) slot = chunk;
     slot = (slot + 127) & ~(size_t)127;
-    int nst = (int)((kSmemLimit4 - head) / slot);
+    size_t fch = 16384;
+    int nst = 0;
+    for (; fch >= 4096; fch /= 2) {
+        if (head + 2 * fch >= kSmemLimit4) continue;
+        nst = (int)((kSmemLimit4 - head - 2 * fch) / slot);
+        if (nst >= 2) break;
+    }
     if (nst > 4) nst = 4;
     if (nst < 2) return cudaErrorInvalidValue;
     p.nstage = nst;
     p.stage_bytes = (unsigned)slot;
     p.tgroup = tg;
-    const size_t smem = head + slot * nst;
+    p.fill_chunk = (unsigned)fch;
+    const size_t smem = head + slot * nst + 2 * fch;
     const void* fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM>
                      : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM>
                                          : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL>;
