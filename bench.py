@@ -44,7 +44,7 @@ import synth  # noqa: E402
 
 WORKLOAD = synth.DECODE_T1
 METRIC = "decode MoE-layer tokens/s"
-PROFILE_EVERY = 8
+PROFILE_EVERY = 16
 UNIT = "tokens/s"
 
 

@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             ft::fill_share_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
                                p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G,
                                ring + (size_t)nst * slot_bytes, reinterpret_cast<uint64_t*>(smem + 128),
-                               p.fill_chunk, p.err);
+                               p.fill_chunk, p.fill_slots, p.err);
         return;
     }
     // ------------------------------------------------------------ producer
@@ -453,8 +453,11 @@ cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     if (nst < 2) return cudaErrorInvalidValue;
     p.nstage = nst;
     p.stage_bytes = (unsigned)slot;
+    int nf = (int)((kSmemLimit - head - slot * nst) / fch);
+    if (nf > 4) nf = 4;
     p.fill_chunk = (unsigned)fch;
-    const size_t smem = head + slot * nst + 2 * fch;
+    p.fill_slots = nf;
+    const size_t smem = head + slot * nst + (size_t)nf * fch;
     static size_t smem_set = 0;
     if (smem != smem_set) {
         cudaError_t e = cudaFuncSetAttribute(expert_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             ft::fill_share_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
                                p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G,
                                ring + (size_t)nst * slot_bytes, reinterpret_cast<uint64_t*>(smem + 128),
-                               p.fill_chunk, p.err);
+                               p.fill_chunk, p.fill_slots, p.err);
         return;
     }
     // ------------------------------------------------------------ producer
@@ -491,8 +491,11 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
     p.nstage = nst;
     p.stage_bytes = (unsigned)slot;
     p.tgroup = tg;
+    int nf = (int)((kSmemLimit4 - head - slot * nst) / fch);
+    if (nf > 4) nf = 4;
     p.fill_chunk = (unsigned)fch;
-    const size_t smem = head + slot * nst + 2 * fch;
+    p.fill_slots = nf;
+    const size_t smem = head + slot * nst + (size_t)nf * fch;
     const void* fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM>
                      : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM>
                                          : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL>;

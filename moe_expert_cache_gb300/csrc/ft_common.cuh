@@ -225,36 +225,35 @@ __device__ __forceinline__ bool wait_filled(unsigned* ready, int i, unsigned G, 
 }
 
 // Fused cache fill by TMA, run by ONE thread of CTA c (of G): part c of every
-// fill record goes host pool -> shared ring (bulk load on an mbarrier) ->
-// victim slot (bulk store); once the part's stores are complete it orders the
-// async-proxy writes before a release and counts the CTA in ready[i].  The
-// ring has two slots of `fch` bytes and barriers fbar[0..1]; waits bounded.
+// fill record goes host pool -> shared ring (bulk loads on mbarriers, up to
+// `nf` in flight) -> victim slot (bulk stores); once the part's stores are
+// complete it orders the async-proxy writes before a release and counts the
+// CTA in ready[i].  Ring: nf (<= 4) slots of `fch` bytes, barriers fbar[nf].
 __device__ __forceinline__ void fill_share_tma(const uint8_t* host, uint8_t* pool, unsigned long long rb, int q,
                                                const int* fslot, const int* ffid, unsigned* ready, int c, int G,
-                                               uint8_t* fring, uint64_t* fbar, unsigned fch, unsigned* err) {
-    mbar_init(&fbar[0], 1);
-    mbar_init(&fbar[1], 1);
+                                               uint8_t* fring, uint64_t* fbar, unsigned fch, int nf, unsigned* err) {
+    for (int s = 0; s < nf; ++s) mbar_init(&fbar[s], 1);
     mbar_fence_init();
     const unsigned long long rec16 = rb / 16;
     const unsigned long long per = ((rec16 + G - 1) / G) * 16;
     const unsigned long long b0 = per * (unsigned long long)c;
     const unsigned long long b1 = b0 + per < rb ? b0 + per : rb;
-    uint32_t waits[2] = {0u, 0u};
+    uint32_t waits[4] = {0u, 0u, 0u, 0u};
     bool ok = true;
     for (int r = 0; r < q && ok; ++r) {
         const uint8_t* src = host + (unsigned long long)ffid[r] * rb;
         uint8_t* dst = pool + (unsigned long long)fslot[r] * rb;
         const int nch = b1 > b0 ? (int)((b1 - b0 + fch - 1) / fch) : 0;
         int issued = 0;
-        int rw[2] = {0, 0};  // waits of this record per slot
-        for (; issued < nch && issued < 2; ++issued) {
+        int rw[4] = {0, 0, 0, 0};  // waits of this record per slot
+        for (; issued < nch && issued < nf; ++issued) {
             const unsigned long long o = b0 + (unsigned long long)issued * fch;
             const unsigned n = (unsigned)((b1 - o) < fch ? (b1 - o) : fch);
-            mbar_arrive_expect_tx(&fbar[issued & 1], n);
-            bulk_g2s(fring + (size_t)(issued & 1) * fch, src + o, n, &fbar[issued & 1]);
+            mbar_arrive_expect_tx(&fbar[issued], n);
+            bulk_g2s(fring + (size_t)issued * fch, src + o, n, &fbar[issued]);
         }
         for (int j = 0; j < nch; ++j) {
-            const int s = j & 1;
+            const int s = j % nf;
             if (!mbar_wait(&fbar[s], waits[s] & 1, err)) { ok = false; break; }
             ++waits[s];
             ++rw[s];
@@ -272,12 +271,11 @@ __device__ __forceinline__ void fill_share_tma(const uint8_t* host, uint8_t* poo
                 ++issued;
             }
         }
-        // the part's stores have landed: publish (async proxy -> generic release)
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         if (!ok) {
             // loads still in flight land before the CTA may exit (bounded)
-            for (int s = 0; s < 2; ++s) {
-                const int iss = (issued - s + 1) / 2;
+            for (int s = 0; s < nf; ++s) {
+                const int iss = issued > s ? (issued - s + nf - 1) / nf : 0;
                 while (rw[s] < iss) {
                     mbar_wait(&fbar[s], waits[s] & 1, err);
                     ++waits[s];
@@ -286,6 +284,7 @@ __device__ __forceinline__ void fill_share_tma(const uint8_t* host, uint8_t* poo
             }
             break;
         }
+        // the part's stores have landed: publish (async proxy -> generic release)
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __threadfence();
         atomicAdd(&ready[r], 1u);
@@ -361,7 +360,8 @@ struct ExpertParams {
     const int* fill_fid;      // [q] flat id of fill i
     const int* wl_fill;       // [E] fill index of entry i, or -1 for a hit
     unsigned* ready;          // [q] CTAs that finished their part of fill i
-    unsigned fill_chunk;      // bytes of one fused-fill ring slot (two slots)
+    unsigned fill_chunk;      // bytes of one fused-fill ring slot
+    int fill_slots;           // fused-fill ring slots (2..4)
     const float* gscale;      // [L*E] NVFP4 per-expert fp32 global, or null
     int tgroup;               // NVFP4: tokens per phase-B item
     int nstage;               // pipeline depth (stages in shared memory)
