@@ -17,7 +17,8 @@
 //   * a producer warp streams weights into a ring of shared-memory slots with
 //     1-D bulk (TMA) copies completing on mbarriers;
 //   * phase A (gate/up + SwiGLU): the work is the flat list of (GPU expert,
-//     group of 8 features); CTA c takes a contiguous 1/G share; one slot holds
+//     group of 8 features), hits first, then the fills in fill order; CTA c
+//     takes items c, c + G, ...; one slot holds
 //     8 gate rows and the 8 matching up rows (contiguous in the record thanks
 //     to the 16-row gate/up interleave); consumer warp w computes feature w of
 //     the slot alone (both dot products, SiLU, product) and writes h in fp32;
@@ -212,7 +213,6 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     const int G = gridDim.x, c = blockIdx.x;
     const int cpe = F / FPC;  // phase-A chunks per expert
     const int NA = ugpu * cpe;
-    const int a0 = (int)((long long)NA * c / G), a1 = (int)((long long)NA * (c + 1) / G);
     const int r0 = (int)((long long)H * c / G), r1 = (int)((long long)H * (c + 1) / G);
     const int R = r1 - r0;
     const int RMAX = (H + G - 1) / G;
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             int it = 0;
             bool ok = true;
             int waited = -1;  // last fill index known complete
-            for (int a = a0; a < a1 && ok; ++a, ++it) {
+            for (int a = c; a < NA && ok; a += G, ++it) {
                 const int st = it % nst;
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
                 const int ent = a / cpe;
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     // releasing slots, but keeps the same barrier sequence as the others.
     int it = 0;
     bool failed = false;
-    for (int a = a0; a < a1; ++a, ++it) {
+    for (int a = c; a < NA; a += G, ++it) {
         const int st = it % nst;
         const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
         failed = !ok;

@@ -226,7 +226,6 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     const int G = gridDim.x, c = blockIdx.x;
     const int cpe = F / FPC;
     const int NA = ugpu * cpe;
-    const int a0 = (int)((long long)NA * c / G), a1 = (int)((long long)NA * (c + 1) / G);
     const int r0 = (int)((long long)H * c / G), r1 = (int)((long long)H * (c + 1) / G);
     const int R = r1 - r0;
     const int RMAX = (H + G - 1) / G;
@@ -306,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             int it = 0;
             bool ok = true;
             int waited = -1;
-            for (int a = a0; a < a1 && ok; ++a, ++it) {
+            for (int a = c; a < NA && ok; a += G, ++it) {
                 const int st = it % nst;
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
                 const int ent = a / cpe;
@@ -388,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     // ------------------------------------------------- phase A: gate/up + SwiGLU
     int it = 0;
     bool failed = false;
-    for (int a = a0; a < a1; ++a, ++it) {
+    for (int a = c; a < NA; a += G, ++it) {
         const int st = it % nst;
         const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
         failed = !ok;

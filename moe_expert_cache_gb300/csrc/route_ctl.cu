@@ -105,6 +105,8 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     int* s_cslot = s_vict + E;  // [E] radix path: candidates with stamp < tau
     unsigned* s_cst = reinterpret_cast<unsigned*>(s_cslot + E);  // [E]
     int* s_fillrank = reinterpret_cast<int*>(s_cst + E);         // [E] fill index of an F expert
+    int* s_ent = s_fillrank + E;                                  // [E] worklist entry of a GPU expert
+    int* s_ecnt = s_ent + E;                                      // [E] routed count, then offset, per entry
 
     if (tid == 0) {
         sh.bad = 0;
@@ -439,7 +441,9 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     }
     __syncthreads();
 
-    // ---- a7: GPU worklist (entries ascending expert id) and the slot rewrite
+    // ---- a7: GPU worklist and the slot rewrite.  Entries: the hits in
+    // ascending expert id, then the fills in fill order (the expert kernel
+    // computes the hits while the fills are still landing).
     if (tid == 0) {
         sh.carry0 = 0;
         sh.carry1 = 0;
@@ -447,26 +451,49 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     __syncthreads();
     for (int e0 = 0; e0 < E; e0 += CTL_THREADS) {
         const int e = e0 + tid;
-        const int isg = (e < E && (s_cls[e] == 1 || s_cls[e] == 2)) ? 1 : 0;
-        const int cnt = isg ? s_cnt[e] : 0;
+        const int ishit = (e < E && s_cls[e] == 1) ? 1 : 0;
         int tot;
-        const int ex = block_excl_scan(isg | (cnt << 12), sh.warp_tot, &tot);
-        if (isg) {
-            const int ent = (ex & 0xfff) + sh.carry0;
-            const int off = (ex >> 12) + sh.carry1;
-            p.wl_slot[ent] = s_slot[e];
-            p.wl_off[ent] = off;
-            p.wl_fid[ent] = fbase + e;
-            p.wl_fill[ent] = s_cls[e] == 2 ? s_fillrank[e] : -1;
-            s_eoff[e] = off;
-        }
+        const int ex = block_excl_scan(ishit, sh.warp_tot, &tot);
+        if (ishit) s_ent[e] = ex + sh.carry0;
         __syncthreads();
-        if (tid == 0) {
-            sh.carry0 += tot & 0xfff;
-            sh.carry1 += tot >> 12;
-        }
+        if (tid == 0) sh.carry0 += tot;
         __syncthreads();
     }
+    const int nh = sh.carry0;
+    for (int e = tid; e < E; e += CTL_THREADS) {
+        const int cl = s_cls[e];
+        if (cl == 1 || cl == 2) {
+            const int ent = cl == 1 ? s_ent[e] : nh + s_fillrank[e];
+            s_ent[e] = ent;
+            s_ecnt[ent] = s_cnt[e];
+            p.wl_slot[ent] = s_slot[e];
+            p.wl_fid[ent] = fbase + e;
+            p.wl_fill[ent] = cl == 2 ? s_fillrank[e] : -1;
+        }
+    }
+    __syncthreads();
+    const int ug = nh + q;
+    if (tid == 0) sh.carry1 = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < ug; i0 += CTL_THREADS) {
+        const int i = i0 + tid;
+        const int cnt = i < ug ? s_ecnt[i] : 0;
+        int tot;
+        const int ex = block_excl_scan(cnt, sh.warp_tot, &tot);
+        if (i < ug) {
+            s_ecnt[i] = ex + sh.carry1;  // now the entry's first assignment
+            p.wl_off[i] = ex + sh.carry1;
+        }
+        __syncthreads();
+        if (tid == 0) sh.carry1 += tot;
+        __syncthreads();
+    }
+    for (int e = tid; e < E; e += CTL_THREADS) {
+        const int cl = s_cls[e];
+        if (cl == 1 || cl == 2) s_eoff[e] = s_ecnt[s_ent[e]];
+    }
+    if (tid == 0) sh.carry0 = ug;
+    __syncthreads();
     if (tid == 0) {
         sh.ugpu = sh.carry0;
         sh.nassign = sh.carry1;
@@ -523,7 +550,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
 
 size_t route_ctl_smem_bytes(int T, int k, int E, int S) {
     const size_t TW = (T + 63) / 64;
-    return (size_t)E * TW * 8 + (size_t)S * 8 + (size_t)T * k * 8 + (size_t)E * 11 * 4;
+    return (size_t)E * TW * 8 + (size_t)S * 8 + (size_t)T * k * 8 + (size_t)E * 13 * 4;
 }
 
 cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s) {
