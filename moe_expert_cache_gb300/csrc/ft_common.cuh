@@ -226,9 +226,11 @@ __device__ __forceinline__ bool wait_filled(unsigned* ready, int i, unsigned G, 
 
 // Fused cache fill by TMA, run by ONE thread of CTA c (of G): part c of every
 // fill record goes host pool -> shared ring (bulk loads on mbarriers, up to
-// `nf` in flight) -> victim slot (bulk stores); once the part's stores are
-// complete it orders the async-proxy writes before a release and counts the
-// CTA in ready[i].  Ring: nf (<= 4) slots of `fch` bytes, barriers fbar[nf].
+// `nf` in flight) -> victim slot (bulk stores).  The chunks of all records
+// form one stream, so the next record's loads are in flight while a record's
+// last stores complete; then the thread orders those async-proxy writes
+// before a release and counts the CTA in ready[r].  Ring: nf (<= 4) slots of
+// `fch` bytes, barriers fbar[nf]; every wait is bounded.
 __device__ __forceinline__ void fill_share_tma(const uint8_t* host, uint8_t* pool, unsigned long long rb, int q,
                                                const int* fslot, const int* ffid, unsigned* ready, int c, int G,
                                                uint8_t* fring, uint64_t* fbar, unsigned fch, int nf, unsigned* err) {
@@ -238,57 +240,50 @@ __device__ __forceinline__ void fill_share_tma(const uint8_t* host, uint8_t* poo
     const unsigned long long per = ((rec16 + G - 1) / G) * 16;
     const unsigned long long b0 = per * (unsigned long long)c;
     const unsigned long long b1 = b0 + per < rb ? b0 + per : rb;
-    uint32_t waits[4] = {0u, 0u, 0u, 0u};
+    const int nch = b1 > b0 ? (int)((b1 - b0 + fch - 1) / fch) : 0;  // chunks per record part
+    const int total = nch * q;
+    auto chunk = [&](int g, const uint8_t*& src, uint8_t*& dst, unsigned& n) {
+        const int r = g / nch, j = g - r * nch;
+        const unsigned long long o = b0 + (unsigned long long)j * fch;
+        n = (unsigned)((b1 - o) < fch ? (b1 - o) : fch);
+        src = host + (unsigned long long)ffid[r] * rb + o;
+        dst = pool + (unsigned long long)fslot[r] * rb + o;
+    };
+    int issued = 0, done = 0;
+    for (; issued < total && issued < nf; ++issued) {
+        const uint8_t* src; uint8_t* dst; unsigned n;
+        chunk(issued, src, dst, n);
+        mbar_arrive_expect_tx(&fbar[issued], n);
+        bulk_g2s(fring + (size_t)issued * fch, src, n, &fbar[issued]);
+    }
     bool ok = true;
-    for (int r = 0; r < q && ok; ++r) {
-        const uint8_t* src = host + (unsigned long long)ffid[r] * rb;
-        uint8_t* dst = pool + (unsigned long long)fslot[r] * rb;
-        const int nch = b1 > b0 ? (int)((b1 - b0 + fch - 1) / fch) : 0;
-        int issued = 0;
-        int rw[4] = {0, 0, 0, 0};  // waits of this record per slot
-        for (; issued < nch && issued < nf; ++issued) {
-            const unsigned long long o = b0 + (unsigned long long)issued * fch;
-            const unsigned n = (unsigned)((b1 - o) < fch ? (b1 - o) : fch);
-            mbar_arrive_expect_tx(&fbar[issued], n);
-            bulk_g2s(fring + (size_t)issued * fch, src + o, n, &fbar[issued]);
-        }
-        for (int j = 0; j < nch; ++j) {
-            const int s = j % nf;
-            if (!mbar_wait(&fbar[s], waits[s] & 1, err)) { ok = false; break; }
-            ++waits[s];
-            ++rw[s];
-            const unsigned long long o = b0 + (unsigned long long)j * fch;
-            const unsigned n = (unsigned)((b1 - o) < fch ? (b1 - o) : fch);
-            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst + o),
+    for (int r = 0; r < q; ++r) {
+        for (int j = 0; j < nch && ok; ++j, ++done) {
+            const int g = done, s = g % nf;
+            if (!mbar_wait(&fbar[s], (uint32_t)(g / nf) & 1u, err)) { ok = false; break; }
+            const uint8_t* src; uint8_t* dst; unsigned n;
+            chunk(g, src, dst, n);
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
                          "r"(smem_addr(fring + (size_t)s * fch)), "r"(n) : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            if (issued < nch) {
-                const unsigned long long o2 = b0 + (unsigned long long)issued * fch;
-                const unsigned n2 = (unsigned)((b1 - o2) < fch ? (b1 - o2) : fch);
-                mbar_arrive_expect_tx(&fbar[s], n2);
-                bulk_g2s(fring + (size_t)s * fch, src + o2, n2, &fbar[s]);
+            if (issued < total) {
+                chunk(issued, src, dst, n);
+                mbar_arrive_expect_tx(&fbar[s], n);
+                bulk_g2s(fring + (size_t)s * fch, src, n, &fbar[s]);
                 ++issued;
             }
         }
+        if (!ok) break;
+        // record r's part has landed: publish (async proxy -> generic release)
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        if (!ok) {
-            // loads still in flight land before the CTA may exit (bounded)
-            for (int s = 0; s < nf; ++s) {
-                const int iss = issued > s ? (issued - s + nf - 1) / nf : 0;
-                while (rw[s] < iss) {
-                    mbar_wait(&fbar[s], waits[s] & 1, err);
-                    ++waits[s];
-                    ++rw[s];
-                }
-            }
-            break;
-        }
-        // the part's stores have landed: publish (async proxy -> generic release)
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __threadfence();
         atomicAdd(&ready[r], 1u);
     }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    // after a failed wait, loads still in flight land before the CTA may exit (bounded)
+    for (int g = done + (ok ? 0 : 1); g < issued; ++g) mbar_wait(&fbar[g % nf], (uint32_t)(g / nf) & 1u, err);
 }
 
 }  // namespace ft
