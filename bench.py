@@ -211,17 +211,17 @@ def kernel_bytes(shape: synth.Shape, T: int, dcnt: dict) -> dict:
 
     expert_ffn (with the fused fill):
         link: every fill copies one record over the host link;
-        hbm:  the fills written to HBM + the whole record of every GPU expert
-              read (3*F*H*2 B) + x read + h written and read once (fp32)
-              + partial_C read + y written.
+        hbm:  the fills written to HBM + the whole record of every resident
+              GPU expert read (3*F*H*2 B; a fill is computed from the bytes in
+              flight) + x read + h written and read once (fp32) + partial_C
+              read + y written.
     route_ctl: logits + ids/gates written (small; reported for completeness).
     """
     H, F, E, L, k = shape.H, shape.F, shape.E, shape.L, shape.k
-    ugpu = dcnt["hits"] + dcnt["fills"]
     calls = dcnt["calls"]
     rb = shape.record_bytes
     link = dcnt["fills"] * rb
-    hbm = link + ugpu * rb + calls * T * H * 2 + 2 * dcnt["assign"] * F * 4 + calls * T * H * 4 * 2
+    hbm = link + dcnt["hits"] * rb + calls * T * H * 2 + 2 * dcnt["assign"] * F * 4 + calls * T * H * 4 * 2
     return {"expert_ffn": {"link": link, "hbm": hbm}, "route_ctl": {"hbm": calls * (T * E * 4 + 2 * T * k * 4)}}
 
 

@@ -34,8 +34,10 @@ namespace {
 
 constexpr int CONSUMER_WARPS = 8;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;
-constexpr int FILL_WARPS = 1;                   // fused cache fill (one TMA thread)
-constexpr int EXPERT_THREADS = CONSUMERS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
+constexpr int PRODUCER_WARP = CONSUMER_WARPS;   // TMA issue of the phase-A/B ring
+constexpr int FILL_ISSUE_WARP = CONSUMER_WARPS + 1;  // fused cache fill: copies
+constexpr int FILL_MATH_WARP = CONSUMER_WARPS + 2;   // fused cache fill: gate/up math
+constexpr int EXPERT_THREADS = CONSUMERS + 3 * 32;
 constexpr int FPC = CONSUMER_WARPS;             // features per phase-A chunk
 constexpr size_t HEAD = 256;                    // barrier area
 
@@ -68,14 +70,16 @@ __global__ void __launch_bounds__(512) fill_kernel(FillParams p) {
 
 // ------------------------------------------------------------- expert FFN
 
-// ---- phase A inner loop: gate and up dot products of one feature (full K)
-// for NT tokens.  x is read from shared memory as fp32 (XF) or bf16.
+// ---- phase A inner loop: gate and up dot products of one feature over the
+// K columns [k0, k0 + K) held in shared memory, for NT tokens.  x is read from
+// shared memory as fp32 (XF) or bf16, row stride ldx.
 template <int NT, bool XF>
 __device__ __forceinline__ void gu_dots(const uint4* __restrict__ wg, const uint4* __restrict__ wu,
-                                        const void* xs, const int* tk, int H, int lane, float* ag, float* au) {
+                                        const void* xs, const int* tk, int K, int ldx, int k0, int lane, float* ag,
+                                        float* au) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
-    const int nv = H >> 3;
+    const int nv = K >> 3;
 #pragma unroll 4
     for (int v = lane; v < nv; v += 32) {
         float g8[8], u8[8];
@@ -84,15 +88,15 @@ __device__ __forceinline__ void gu_dots(const uint4* __restrict__ wg, const uint
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             float x8[8];
+            const size_t xo = (size_t)tk[n] * ldx + k0;
             if (XF) {
-                const float4* xp = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) +
-                                                                   (size_t)tk[n] * H + v * 8);
+                const float4* xp = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) + xo + v * 8);
                 const float4 x0 = xp[0], x1 = xp[1];
                 x8[0] = x0.x; x8[1] = x0.y; x8[2] = x0.z; x8[3] = x0.w;
                 x8[4] = x1.x; x8[5] = x1.y; x8[6] = x1.z; x8[7] = x1.w;
             } else {
-                ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(xs) +
-                                                                 (size_t)tk[n] * H)[v], x8);
+                ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(xs) + xo)[v],
+                                  x8);
             }
             float sg = ag[n], su = au[n];
 #pragma unroll
@@ -106,41 +110,63 @@ __device__ __forceinline__ void gu_dots(const uint4* __restrict__ wg, const uint
     }
 }
 
+// One token group of one feature.  With nseg K segments the two dot products
+// are summed over the segments in order (segment sums kept per token in facc,
+// by the lane that owns the token), and SwiGLU is applied after the last one.
 template <int NT, bool XF>
 __device__ __forceinline__ void gu_group(const uint4* wg, const uint4* wu, const void* xs, const int* m_tok, int off,
-                                         int g0, int H, int F, int f, int lane, float* hbuf) {
+                                         int g0, int K, int H, int k0, int F, int f, int lane, float* hbuf, int seg,
+                                         int nseg, float* facc) {
     int tk[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) tk[n] = m_tok[off + g0 + n];
     float ag[NT], au[NT];
-    gu_dots<NT, XF>(wg, wu, xs, tk, H, lane, ag, au);
-    float mine = 0.f;
+    gu_dots<NT, XF>(wg, wu, xs, tk, K, H, k0, lane, ag, au);
+    float mg = 0.f, mu = 0.f;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
         const float sg = ft::warp_sum(ag[n]);
         const float su = ft::warp_sum(au[n]);
-        if (lane == n) mine = ft::silu_mul(sg, su);
+        if (lane == n) {
+            mg = sg;
+            mu = su;
+        }
     }
-    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + f] = mine;
+    if (lane < NT) {
+        if (nseg > 1) {
+            float* a = facc + 2 * (g0 + lane);
+            if (seg > 0) {
+                mg += a[0];
+                mu += a[1];
+            }
+            if (seg < nseg - 1) {
+                a[0] = mg;
+                a[1] = mu;
+                return;
+            }
+        }
+        hbuf[(size_t)(off + g0 + lane) * F + f] = ft::silu_mul(mg, mu);
+    }
 }
 
 template <bool XF>
 __device__ __forceinline__ void gu_feature(const uint4* wg, const uint4* wu, const void* xs, const int* m_tok,
-                                           int off, int ntok, int H, int F, int f, int lane, float* hbuf) {
+                                           int off, int ntok, int K, int H, int k0, int F, int f, int lane,
+                                           float* hbuf, int seg = 0, int nseg = 1, float* facc = nullptr) {
     int g0 = 0;
     while (g0 < ntok) {
         const int rem = ntok - g0;
         if (rem >= 8) {
-            gu_group<8, XF>(wg, wu, xs, m_tok, off, g0, H, F, f, lane, hbuf);
+            gu_group<8, XF>(wg, wu, xs, m_tok, off, g0, K, H, k0, F, f, lane, hbuf, seg, nseg, facc);
             g0 += 8;
         } else if (rem >= 4) {
-            gu_group<4, XF>(wg, wu, xs, m_tok, off, g0, H, F, f, lane, hbuf);
+            gu_group<4, XF>(wg, wu, xs, m_tok, off, g0, K, H, k0, F, f, lane, hbuf, seg, nseg, facc);
             g0 += 4;
         } else if (rem >= 2) {
-            gu_group<2, XF>(wg, wu, xs, m_tok, off, g0, H, F, f, lane, hbuf);
+            gu_group<2, XF>(wg, wu, xs, m_tok, off, g0, K, H, k0, F, f, lane, hbuf, seg, nseg, facc);
             g0 += 2;
         } else {
-            gu_group<1, XF>(wg, wu, xs, m_tok, off, g0, H, F, f, lane, hbuf);
+            gu_group<1, XF>(wg, wu, xs, m_tok, off, g0, K, H, k0, F, f, lane, hbuf, seg, nseg, facc);
             g0 += 1;
         }
     }
@@ -204,15 +230,17 @@ __device__ __forceinline__ void down_row(const uint4* wrow, const float* hs, int
 
 __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_gdone;
+    __shared__ int s_wd;     // this CTA's W_d rows of every fill are stored (1), or the fill failed (2)
     const int H = p.H, F = p.F, T = p.T, k = p.k;
     const int nst = p.nstage;
     const unsigned slot_bytes = p.stage_bytes;
     const int ugpu = p.info[INFO_UGPU];
     const int nasg = p.info[INFO_NASSIGN];
+    const int q = p.do_fill ? p.info[INFO_Q] : 0;  // fills performed here: the last q entries
+    const int nA = ugpu - q;                        // entries streamed from their slots in phase A
     const int G = gridDim.x, c = blockIdx.x;
     const int cpe = F / FPC;  // phase-A chunks per expert
-    const int NA = ugpu * cpe;
+    const int NA = nA * cpe;
     const int r0 = (int)((long long)H * c / G), r1 = (int)((long long)H * (c + 1) / G);
     const int R = r1 - r0;
     const int RMAX = (H + G - 1) / G;
@@ -222,6 +250,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + nst;
+    uint64_t* ffull = reinterpret_cast<uint64_t*>(smem + 128);  // fill ring: chunk landed
+    uint64_t* fcons = ffull + 4;                                 // fill ring: chunk's features computed
     const bool xf32 = (size_t)T * H * 4 <= 65536;  // x kept as fp32 in shared memory
     const size_t xbytes = (size_t)T * H * (xf32 ? 4 : 2);
     size_t o = HEAD;
@@ -235,25 +265,64 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     int* m_tok = m_slot + TK;                          // [TK]   token of each assignment
     float* m_gate = reinterpret_cast<float*>(m_tok + TK);  // [TK]
     int* m_pos = reinterpret_cast<int*>(m_gate + TK);      // [TK]   assignment of (t, j)
-    int* m_fill = m_pos + TK;                              // [TK]   fill index of entry (or -1)
-    o += ((size_t)(6 * TK + 1) * 4 + 127) & ~(size_t)127;
+    o += ((size_t)(5 * TK + 1) * 4 + 127) & ~(size_t)127;
+    float* facc = reinterpret_cast<float*>(smem + o);      // [T][2] segment sums of the fill math warp
+    o += ((size_t)2 * T * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
+    unsigned char* fring = ring + (size_t)nst * slot_bytes;
     const unsigned rowbytes = (unsigned)H * 2u;
-    const unsigned wpart = ((unsigned)RMAX * F * 2u + 127u) & ~127u;  // h rows follow the W_d rows
+    // phase-B stage: consecutive entries, each its W_d rows [r0, r1) then its
+    // h rows, as many as fit in a slot (a stage never mixes resident entries
+    // and fills, whose W_d rows this CTA stores itself)
+    const unsigned wpad = ((unsigned)R * F * 2u + 127u) & ~127u;
+    auto hbytes = [&](int e) { return (unsigned)(m_off[e + 1] - m_off[e]) * F * 4u; };
+    auto stage_end = [&](int e0) {
+        unsigned used = 0;
+        int e1 = e0;
+        while (e1 < nB) {
+            const unsigned need = wpad + ((hbytes(e1) + 127u) & ~127u);
+            if (e1 > e0 && (used + need > slot_bytes || e1 == nA)) break;
+            used += need;
+            ++e1;
+        }
+        return e1;
+    };
+
+    // fused-fill geometry: unit = (fill r, group of fpf features), split into
+    // nks K segments of KS columns; units go to CTAs round-robin.  Every CTA
+    // also copies its own W_d rows [r0, r1) of each fill, in npc pieces.
+    const int nf = p.fill_slots;
+    const unsigned fch = p.fill_chunk;
+    const int fpf = p.fill_fpf, nks = p.fill_nks;
+    const int KS = H / nks;
+    const int upr = F / fpf;
+    const int U = q * upr;
+    const int n_gu = (c < U ? (U - c + G - 1) / G : 0) * nks;
+    const unsigned long long wdb = (unsigned long long)R * F * 2;
+    const int npc = (int)((wdb + fch - 1) / fch);
+    const int n_fill = n_gu + q * npc;
+    const unsigned partb = (unsigned)fpf * KS * 2u;  // gate (or up) bytes of one unit chunk
+    auto gu_chunk = [&](int g, int& r, int& f0, int& seg) {
+        const int u = c + (g / nks) * G;
+        seg = g - (g / nks) * nks;
+        r = u / upr;
+        f0 = (u - r * upr) * fpf;
+    };
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
             ft::mbar_init(&full[s], 1);
             ft::mbar_init(&empty[s], CONSUMER_WARPS);
         }
+        for (int s = 0; s < nf; ++s) {
+            ft::mbar_init(&ffull[s], 32);  // one cp.async arrival per lane of the copy warp
+            ft::mbar_init(&fcons[s], 1);
+        }
         ft::mbar_fence_init();
-        s_gdone = 0;
+        s_wd = 0;
     }
     for (int i = tid; i <= ugpu; i += EXPERT_THREADS) m_off[i] = p.wl_off[i];
-    for (int i = tid; i < ugpu; i += EXPERT_THREADS) {
-        m_slot[i] = p.wl_slot[i];
-        m_fill[i] = p.do_fill ? p.wl_fill[i] : -1;
-    }
+    for (int i = tid; i < ugpu; i += EXPERT_THREADS) m_slot[i] = p.wl_slot[i];
     for (int i = tid; i < nasg; i += EXPERT_THREADS) {
         m_tok[i] = p.as_tok[i];
         m_gate[i] = p.as_gate[i];
@@ -272,30 +341,139 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     }
     __syncthreads();
 
-    // --------------------------------------------------------- fused fill
-    if (wid > CONSUMER_WARPS) {
-        if (lane == 0 && p.do_fill)
-            ft::fill_share_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
-                               p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G,
-                               ring + (size_t)nst * slot_bytes, reinterpret_cast<uint64_t*>(smem + 128),
-                               p.fill_chunk, p.fill_slots, p.err);
+    // ------------------------------------------------- fused fill: copy warp
+    // host pool -> fill ring by per-lane cp.async (the load/store path, so the
+    // slow host reads do not queue ahead of the ring's bulk copies from HBM),
+    // then fill ring -> victim slot by one bulk store.  A unit chunk is
+    // released for the next load once the math warp has used it and its store
+    // has read it.
+    if (wid == FILL_ISSUE_WARP) {
+        const uint8_t* host = reinterpret_cast<const uint8_t*>(p.host_pool);
+        uint8_t* pool = const_cast<uint8_t*>(p.slot_pool);
+        const unsigned long long wd0 = (unsigned long long)4 * F * H + (unsigned long long)r0 * F * 2;
+        const unsigned long long upoff = (unsigned long long)16 * H * 2;  // up rows follow gate rows by 16 rows
+        // offset within the record, bytes of one part, and fill index of chunk g
+        auto locate = [&](int g, unsigned long long& off, unsigned& n, int& r) {
+            if (g < n_gu) {
+                int f0, seg;
+                gu_chunk(g, r, f0, seg);
+                const unsigned long long row = (unsigned long long)(f0 >> 4) * 32 + (f0 & 15);
+                off = (row * H + (unsigned long long)seg * KS) * 2;
+                n = partb;
+            } else {
+                const int w = g - n_gu;
+                r = w / npc;
+                const unsigned long long po = (unsigned long long)(w - r * npc) * fch;
+                off = wd0 + po;
+                n = (unsigned)(wdb - po < fch ? wdb - po : fch);
+            }
+        };
+        auto load = [&](int g, int s) {  // all lanes
+            unsigned long long off;
+            unsigned n;
+            int r;
+            locate(g, off, n, r);
+            unsigned char* d = fring + (size_t)s * fch;
+            const uint8_t* src = host + (unsigned long long)p.fill_fid[r] * p.rb + off;
+            for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + v, src + v);
+            if (g < n_gu)
+                for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + n + v, src + upoff + v);
+            ft::cp_async_arrive(&ffull[s]);
+        };
+        auto store = [&](int g, int s) {  // lane 0
+            unsigned long long off;
+            unsigned n;
+            int r;
+            locate(g, off, n, r);
+            const unsigned char* d = fring + (size_t)s * fch;
+            uint8_t* dst = pool + (unsigned long long)p.fill_slot[r] * p.rb + off;
+            ft::bulk_s2g(dst, d, n);
+            if (g < n_gu) ft::bulk_s2g(dst + upoff, d + n, n);
+            ft::bulk_commit();
+        };
+        int issued = 0;
+        for (; issued < n_fill && issued < nf; ++issued) load(issued, issued);
+        bool ok = true;
+        for (int g = 0; g < n_fill; ++g) {
+            const int s = g % nf;
+            const uint32_t par = (uint32_t)(g / nf) & 1u;
+            int w = 1;
+            if (lane == 0) {
+                w = ft::mbar_wait(&ffull[s], par, p.err);
+                if (w) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // cp.async data -> bulk store
+                    store(g, s);
+                    if (g < n_gu) w = ft::mbar_wait(&fcons[s], par, p.err);
+                    ft::bulk_wait_read_all();
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, w, 0)) {
+                ok = false;
+                break;
+            }
+            if (issued < n_fill) {
+                load(issued, s);
+                ++issued;
+            }
+        }
+        ft::cp_async_wait_all();  // nothing in flight into shared memory at exit
+        __syncwarp();
+        if (lane == 0) {
+            ft::bulk_wait_all();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            ft::st_release_cta(&s_wd, ok ? 1 : 2);
+        }
         return;
     }
+
+    // ------------------------------------------ fused fill: gate/up math warp
+    // SwiGLU features of the fill units of this CTA, from the fill ring.
+    if (wid == FILL_MATH_WARP) {
+        for (int g = 0; g < n_gu; ++g) {
+            const int s = g % nf;
+            if (!__all_sync(0xffffffffu, ft::mbar_wait(&ffull[s], (uint32_t)(g / nf) & 1u, p.err))) break;
+            int r, f0, seg;
+            gu_chunk(g, r, f0, seg);
+            const int off = m_off[nA + r];
+            const int ntok = m_off[nA + r + 1] - off;
+            const unsigned char* d = fring + (size_t)s * fch;
+            for (int fi = 0; fi < fpf; ++fi) {
+                const uint4* wg = reinterpret_cast<const uint4*>(d + (size_t)fi * KS * 2);
+                const uint4* wu = reinterpret_cast<const uint4*>(d + partb + (size_t)fi * KS * 2);
+                if (xf32)
+                    gu_feature<true>(wg, wu, x_s, m_tok, off, ntok, KS, H, seg * KS, F, f0 + fi, lane, p.hbuf, seg,
+                                     nks, facc);
+                else
+                    gu_feature<false>(wg, wu, x_s, m_tok, off, ntok, KS, H, seg * KS, F, f0 + fi, lane, p.hbuf, seg,
+                                      nks, facc);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                ft::mbar_arrive(&fcons[s]);
+                if (seg == nks - 1) ft::red_release_gpu_add(&p.ready[nA + r], (unsigned)fpf);
+            }
+        }
+        return;
+    }
+
     // ------------------------------------------------------------ producer
-    if (wid == CONSUMER_WARPS) {
+    if (wid == PRODUCER_WARP) {
         if (lane == 0) {
             const uint64_t pol = ft::l2_policy_evict_first();
+            const unsigned wb = (unsigned)R * F * 2u;
+            // W_d rows of the resident entries go to L2 while phase A streams
+            auto prefetch_wd = [&]() {
+                for (int e = 0; e < nA && wb > 0; ++e)
+                    ft::bulk_prefetch_l2(p.slot_pool + (size_t)m_slot[e] * p.rb + (size_t)4 * F * H + (size_t)r0 * F * 2,
+                                         wb);
+            };
             int it = 0;
             bool ok = true;
-            int waited = -1;  // last fill index known complete
             for (int a = c; a < NA && ok; a += G, ++it) {
                 const int st = it % nst;
+                if (it == nst) prefetch_wd();
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
                 const int ent = a / cpe;
-                if (m_fill[ent] >= 0 && m_fill[ent] != waited) {
-                    if (!ft::wait_filled(p.ready, m_fill[ent], (unsigned)G, p.err)) { ok = false; break; }
-                    waited = m_fill[ent];
-                }
                 const int f0 = (a - ent * cpe) * FPC;
                 const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
                 const int grp = f0 >> 4, i = f0 & 15;
@@ -305,46 +483,47 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 ft::bulk_g2s_hint(dst + (size_t)FPC * rowbytes, rec + (size_t)(grp * 32 + 16 + i) * rowbytes,
                                   FPC * rowbytes, &full[st], pol);
             }
-            // phase B: W_d rows stream ahead of the grid barrier; the h rows of
-            // an entry are copied once every CTA has written its h.
-            const unsigned wb = (unsigned)R * F * 2u;
-            const int pre = nB < nst ? nB : nst;
-            const int itB = it;
-            bool gdone = false;
-            for (int e = 0; e < nB && ok; ++e, ++it) {
+            if (it < nst) prefetch_wd();
+            // phase B, stage by stage: the W_d rows of the stage's entries,
+            // then the h rows of each entry once every feature of it is
+            // written, by whichever CTA computed it.
+            bool wd_ready = false;
+            for (int e0 = 0; e0 < nB && ok; ++it) {
                 const int st = it % nst;
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
-                const int off = m_off[e];
-                const unsigned hb = (unsigned)(m_off[e + 1] - off) * F * 4u;
-                unsigned char* dst = ring + (size_t)st * slot_bytes;
-                if (m_fill[e] >= 0 && !ft::wait_filled(p.ready, m_fill[e], (unsigned)G, p.err)) { ok = false; break; }
-                const uint8_t* wd = p.slot_pool + (size_t)m_slot[e] * p.rb + (size_t)2 * F * H * 2 + (size_t)r0 * F * 2;
-                ft::mbar_arrive_expect_tx(&full[st], wb + hb);
-                ft::bulk_g2s_hint(dst, wd, wb, &full[st], pol);
-                if (e == pre - 1 || e >= pre) {
-                    if (!gdone) {
-                        const uint64_t t0 = ft::globaltimer();
-                        while (!ft::ld_acquire_cta(&s_gdone)) {
-                            if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
-                                atomicOr(p.err, FT_DEVERR_TIMEOUT);
-                                ok = false;
-                                break;
-                            }
+                const int e1 = stage_end(e0);
+                if (e0 >= nA && !wd_ready) {
+                    const uint64_t t0 = ft::globaltimer();
+                    int v;
+                    while ((v = ft::ld_acquire_cta(&s_wd)) == 0) {
+                        if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                            atomicOr(p.err, FT_DEVERR_TIMEOUT);
+                            break;
                         }
-                        if (!ok) break;
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        gdone = true;
-                        for (int e2 = 0; e2 < pre; ++e2) {  // deferred h rows of the prefetched entries
-                            const int st2 = (itB + e2) % nst;
-                            const int off2 = m_off[e2];
-                            const unsigned hb2 = (unsigned)(m_off[e2 + 1] - off2) * F * 4u;
-                            ft::bulk_g2s(ring + (size_t)st2 * slot_bytes + wpart, p.hbuf + (size_t)off2 * F, hb2,
-                                         &full[st2]);
-                        }
-                    } else {
-                        ft::bulk_g2s(dst + wpart, p.hbuf + (size_t)off * F, hb, &full[st]);
                     }
+                    if (v != 1) { ok = false; break; }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    wd_ready = true;
                 }
+                unsigned char* dst = ring + (size_t)st * slot_bytes;
+                unsigned tx = 0;
+                for (int e = e0; e < e1; ++e) tx += wb + hbytes(e);
+                ft::mbar_arrive_expect_tx(&full[st], tx);
+                unsigned o = 0;
+                for (int e = e0; e < e1; ++e) {
+                    const uint8_t* wd = p.slot_pool + (size_t)m_slot[e] * p.rb + (size_t)4 * F * H + (size_t)r0 * F * 2;
+                    ft::bulk_g2s_hint(dst + o, wd, wb, &full[st], pol);
+                    o += wpad + ((hbytes(e) + 127u) & ~127u);
+                }
+                o = 0;
+                for (int e = e0; e < e1; ++e) {
+                    // after a timed-out wait the h rows are still copied (whatever
+                    // they hold) so that the stage completes and the ring drains
+                    if (!ft::wait_count(&p.ready[e], (unsigned)F, p.err)) ok = false;
+                    ft::bulk_g2s(dst + o + wpad, p.hbuf + (size_t)m_off[e] * F, hbytes(e), &full[st]);
+                    o += wpad + ((hbytes(e) + 127u) & ~127u);
+                }
+                e0 = e1;
             }
             ft::drain_ring(full, it, nst, p.err);
         }
@@ -358,7 +537,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     bool failed = false;
     for (int a = c; a < NA; a += G, ++it) {
         const int st = it % nst;
-        const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
+        const bool ok = !failed && __all_sync(0xffffffffu, ft::mbar_wait(&full[st], (it / nst) & 1, p.err));
         failed = !ok;
         const int ent = a / cpe;
         const int f = (a - ent * cpe) * FPC + wid;
@@ -369,35 +548,36 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                                                          (size_t)(FPC + wid) * rowbytes);
         if (ok) {
             if (xf32)
-                gu_feature<true>(wg, wu, x_s, m_tok, off, ntok, H, F, f, lane, p.hbuf);
+                gu_feature<true>(wg, wu, x_s, m_tok, off, ntok, H, H, 0, F, f, lane, p.hbuf);
             else
-                gu_feature<false>(wg, wu, x_s, m_tok, off, ntok, H, F, f, lane, p.hbuf);
+                gu_feature<false>(wg, wu, x_s, m_tok, off, ntok, H, H, 0, F, f, lane, p.hbuf);
+        }
+        __syncwarp();
+        if (ok && lane == 0) {
+            ft::mbar_arrive(&empty[st]);
+            ft::red_release_gpu_add(&p.ready[ent], 1u);
+        }
+    }
+
+    // ---------------------------------------------------- phase B: down rows
+    for (int e0 = 0; e0 < nB; ++it) {
+        const int st = it % nst;
+        const int e1 = stage_end(e0);
+        const bool ok = !failed && __all_sync(0xffffffffu, ft::mbar_wait(&full[st], (it / nst) & 1, p.err));
+        failed = !ok;
+        const unsigned char* sb = ring + (size_t)st * slot_bytes;
+        for (int e = e0; e < e1 && ok; ++e) {
+            const int off = m_off[e];
+            const int ntok = m_off[e + 1] - off;
+            const float* hs = reinterpret_cast<const float*>(sb + wpad);
+            for (int rl = wid; rl < R; rl += CONSUMER_WARPS)
+                down_row(reinterpret_cast<const uint4*>(sb + (size_t)rl * F * 2), hs, ntok, F, lane, o_s, off, RMAX,
+                         rl);
+            sb += wpad + ((hbytes(e) + 127u) & ~127u);
         }
         __syncwarp();
         if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
-    }
-
-    // every h of this layer is written before any CTA starts phase B
-    ft::named_bar_sync(1, CONSUMERS);
-    if (tid == 0) {
-        ft::grid_barrier(p.gbar, (unsigned)G, p.err);
-        ft::st_release_cta(&s_gdone, 1);
-    }
-    ft::named_bar_sync(1, CONSUMERS);
-
-    // ---------------------------------------------------- phase B: down rows
-    for (int e = 0; e < nB; ++e, ++it) {
-        const int st = it % nst;
-        const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
-        failed = !ok;
-        const int off = m_off[e];
-        const int ntok = m_off[e + 1] - off;
-        const unsigned char* sb = ring + (size_t)st * slot_bytes;
-        const float* hs = reinterpret_cast<const float*>(sb + wpart);
-        for (int rl = wid; rl < R && ok; rl += CONSUMER_WARPS)
-            down_row(reinterpret_cast<const uint4*>(sb + (size_t)rl * F * 2), hs, ntok, F, lane, o_s, off, RMAX, rl);
-        __syncwarp();
-        if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+        e0 = e1;
     }
     ft::named_bar_sync(1, CONSUMERS);
     // gated merge in fixed order: j ascending, then the CPU-set partial sum
@@ -412,6 +592,17 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         if (p.partial_C) acc += p.partial_C[oi];
         p.y[oi] = acc;
     }
+    // the last CTA out returns the per-entry counters to zero for the next
+    // launch: every CTA's reads of them precede its exit count
+    ft::named_bar_sync(1, CONSUMERS);
+    if (tid == 0) {
+        unsigned n;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.gbar) : "memory");
+        if (n == (unsigned)G - 1) {
+            for (int e = 0; e < ugpu; ++e) p.ready[e] = 0u;
+            p.gbar[0] = 0u;
+        }
+    }
 }
 
 }  // namespace
@@ -421,42 +612,51 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-static constexpr size_t kSmemLimit = 227 * 1024;
+static constexpr size_t kSmemLimit = 227 * 1024 - 256;  // dynamic; the rest is static shared memory
+static constexpr size_t kFillChunk = 4096;               // bytes of one fused-fill ring chunk
+static constexpr int kFillSlots = 2;                     // fused-fill ring chunks per CTA
 
 // Shared-memory plan: barriers, x (if it fits in 64 KiB), the per-CTA output
-// block, the worklist metadata, then as many ring slots as fit (at most 4).  A
-// slot holds one phase-A chunk (16 rows of H) or one phase-B stage (R rows of
-// W_d followed by the h rows of the entry's tokens).
+// block, the worklist metadata and the fill math warp's segment sums, then the
+// ring (as many slots as fit, at most 4) and the fused-fill ring.  A ring slot
+// holds one phase-A chunk (16 rows of H) or one phase-B stage (R rows of W_d
+// followed by the h rows of the entry's tokens).  The fill ring has 2..4
+// chunks of 16 KiB (smaller if that would leave fewer than two ring slots); a
+// fill unit chunk holds the gate and up rows of fpf features, or of one
+// feature over H / nks columns when one feature does not fit.
 cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     const int G = num_sms;
     const int RMAX = (p.H + G - 1) / G;
     const bool xf32 = (size_t)p.T * p.H * 4 <= 65536;
     const size_t xbytes = (size_t)p.T * p.H * (xf32 ? 4 : 2);
     const size_t TK = (size_t)p.T * p.k;
-    const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) +
-                        ((TK * RMAX * 4 + 127) & ~(size_t)127) + (((6 * TK + 1) * 4 + 127) & ~(size_t)127);
+    const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127) +
+                        (((5 * TK + 1) * 4 + 127) & ~(size_t)127) + (((size_t)2 * p.T * 4 + 127) & ~(size_t)127);
     size_t slot = (size_t)2 * FPC * p.H * 2;
     const size_t down = (((size_t)RMAX * p.F * 2 + 127) & ~(size_t)127) + (size_t)p.T * p.F * 4;
     if (down > slot) slot = down;
     slot = (slot + 127) & ~(size_t)127;
     if (head >= kSmemLimit) return cudaErrorInvalidValue;
-    // two fused-fill ring slots after the main ring: 16 KiB each, smaller if
-    // that would leave fewer than two main slots
-    size_t fch = 16384;
-    int nst = 0;
-    for (; fch >= 4096; fch /= 2) {
-        if (head + 2 * fch >= kSmemLimit) continue;
-        nst = (int)((kSmemLimit - head - 2 * fch) / slot);
-        if (nst >= 2) break;
-    }
+    // The fill ring is deliberately small: the host link's bandwidth-delay
+    // product is well under 1 MB, and host reads queued beyond it delay the
+    // HBM reads of every other SM behind them in the memory system.
+    const size_t fch = kFillChunk;
+    const int nf = kFillSlots;
+    if (head + nf * fch + 2 * slot > kSmemLimit) return cudaErrorInvalidValue;
+    int nst = (int)((kSmemLimit - head - nf * fch) / slot);
     if (nst > 4) nst = 4;
-    if (nst < 2) return cudaErrorInvalidValue;
     p.nstage = nst;
     p.stage_bytes = (unsigned)slot;
-    int nf = (int)((kSmemLimit - head - slot * nst) / fch);
-    if (nf > 4) nf = 4;
     p.fill_chunk = (unsigned)fch;
     p.fill_slots = nf;
+    // fill unit: fpf whole features (a power of two up to 16, so a unit stays
+    // inside one 16-row gate/up group), or one feature in nks K segments
+    int fpf = 1, nks = 1;
+    while (4ull * p.H * (2 * fpf) <= fch && 2 * fpf <= 16) fpf *= 2;
+    while (4ull * (p.H / nks) > fch) nks *= 2;
+    if (p.H % nks || (p.H / nks) % 8) return cudaErrorInvalidValue;
+    p.fill_fpf = fpf;
+    p.fill_nks = nks;
     const size_t smem = head + slot * nst + (size_t)nf * fch;
     static size_t smem_set = 0;
     if (smem != smem_set) {

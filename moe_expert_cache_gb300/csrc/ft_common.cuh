@@ -107,6 +107,42 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
         : "memory");
 }
 
+// 1-D bulk copy this CTA's shared memory -> global, in the thread's current
+// bulk async-group (close it with bulk_commit).  Same alignment rules.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed bulk store of this thread has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed bulk store of this thread has completed its writes
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// 16-byte asynchronous copy global -> shared through the load/store path
+// (not the bulk-copy unit), L1 bypassed.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async issued so far by this thread has landed
+// (the arrival is not pre-counted: the barrier's count includes it).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Counter increment that releases this thread's prior writes (and, through
+// a preceding warp or CTA barrier, its peers') at GPU scope.
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Prefetch `bytes` of global memory into L2 (no completion tracking).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -142,12 +178,12 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 // between CTA-wide barriers.
 __device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned G, unsigned* err) {
     const unsigned gen0 = ld_acquire_gpu(&bar[1]);
-    __threadfence();
-    const unsigned c = atomicAdd(&bar[0], 1u);
+    unsigned c;
+    // arrival: releases this CTA's writes; the last arrival also acquires everyone's
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(c) : "l"(bar) : "memory");
     if (c == G - 1) {
-        atomicExch(&bar[0], 0u);
-        __threadfence();
-        atomicAdd(&bar[1], 1u);
+        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(bar) : "memory");
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(bar + 1), "r"(gen0 + 1u) : "memory");
     } else {
         const uint64_t t0 = globaltimer();
         for (unsigned it = 0; ld_acquire_gpu(&bar[1]) == gen0; ++it) {
@@ -157,7 +193,6 @@ __device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned G, unsigned
             }
         }
     }
-    __threadfence();
 }
 
 // Producer-side drain: wait (bounded) for the last phase of every slot that
@@ -209,6 +244,23 @@ __device__ __forceinline__ void fill_share(const uint4* host, uint4* pool, unsig
 
 // Producer side: wait (bounded) until all G CTAs have copied their part of
 // fill i, then order the async proxy after those generic writes.
+// Bounded wait until *c >= target (acquire at GPU scope), then order the
+// async proxy (bulk copies) after the acquired writes.
+__device__ __forceinline__ bool wait_count(const unsigned* c, unsigned target, unsigned* err) {
+    const uint64_t t0 = globaltimer();
+    for (unsigned it = 0;; ++it) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+        if (v >= target) break;
+        if ((it & 63u) == 63u && globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+            atomicOr(err, FT_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
 __device__ __forceinline__ bool wait_filled(unsigned* ready, int i, unsigned G, unsigned* err) {
     const uint64_t t0 = globaltimer();
     for (unsigned it = 0;; ++it) {
@@ -308,7 +360,7 @@ struct CtlParams {
     int* wl_off;              // [E+1]  first assignment of entry i
     int* wl_fid;              // [E]    flat id of entry i
     int* wl_fill;             // [E]    fill index of entry i, or -1 for a hit
-    unsigned* ready;          // [E]    per-fill readiness counters (reset here)
+    unsigned* ready;          // [E]    per-fill / per-entry counters of the expert kernel (reset here)
     int* as_tok;              // [T*k]  token of each assignment (entry-major, token ascending)
     float* as_gate;           // [T*k]
     int* fill_slot;           // [E]
@@ -345,7 +397,7 @@ struct ExpertParams {
     const int* out_pos;
     float* hbuf;              // [T*k, F] fp32
     unsigned* err;
-    unsigned* gbar;           // [2] grid barrier (arrivals, generation), zero at init
+    unsigned* gbar;           // [2] NVFP4: grid barrier (arrivals, generation); BF16: [0] exit count; zero at rest
     const int* wl_fid;        // [E] flat id of each GPU entry (NVFP4 global lookup)
     // fused cache fill (performed by this launch when do_fill != 0)
     int do_fill;
@@ -354,9 +406,12 @@ struct ExpertParams {
     const int* fill_slot;     // [q] victim slot of fill i
     const int* fill_fid;      // [q] flat id of fill i
     const int* wl_fill;       // [E] fill index of entry i, or -1 for a hit
-    unsigned* ready;          // [q] CTAs that finished their part of fill i
+    unsigned* ready;          // NVFP4: [q] CTAs that finished their part of fill i;
+                              // BF16: [ugpu] h features written per entry (zero at rest)
     unsigned fill_chunk;      // bytes of one fused-fill ring slot
     int fill_slots;           // fused-fill ring slots (2..4)
+    int fill_fpf;             // BF16: features per fused-fill unit
+    int fill_nks;             // BF16: K segments per fused-fill unit
     const float* gscale;      // [L*E] NVFP4 per-expert fp32 global, or null
     int tgroup;               // NVFP4: tokens per phase-B item
     int nstage;               // pipeline depth (stages in shared memory)

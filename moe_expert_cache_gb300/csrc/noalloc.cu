@@ -10,14 +10,14 @@
 // its slot pool, maps and scratch, so those callers need a context-free
 // entry point.  This one runs the same expert kernel as ft_moe_forward, on
 // records the caller already holds in device memory, and keeps its scratch
-// (the SwiGLU activations h, the worklist and the grid-barrier words) in one
+// (the SwiGLU activations h, the worklist and the completion counters) in one
 // file-scope device array of fixed size.
 //
 // That array exists once per device that loads the library and stays
 // allocated until the process exits.  Every call shares it and finds the
 // previous call's contents there: the preparation kernel rewrites every
-// field the expert kernel reads, and the grid-barrier words return to their
-// resting value after each call.  Calls that overlap on the GPU (different
+// field the expert kernel reads, and the completion counters return to their
+// resting value (zero) after each call.  Calls that overlap on the GPU (different
 // streams, or concurrent host threads) race on the array and must not be
 // issued.
 #include "ft_common.cuh"
@@ -33,10 +33,13 @@ constexpr int PREP_THREADS = 512;
 constexpr int MAX_ROUTES = 1024;  // T*k
 // Byte offsets inside the scratch array.
 constexpr size_t OFF_INFO = 0;       // int[INFO_WORDS]
-constexpr size_t OFF_GBAR = 128;     // unsigned[2], zero at load, self-resetting
+constexpr size_t OFF_GBAR = 128;     // unsigned[2]: exit count, zero at load, self-resetting
 constexpr size_t OFF_ERR = 192;      // unsigned
 constexpr size_t OFF_META = 256;     // worklist arrays, MAX_ROUTES entries each
+constexpr size_t OFF_DONE = 32768;   // unsigned[MAX_ROUTES]: h features written per entry
 constexpr size_t OFF_H = 65536;      // fp32 h [T*k, F]
+static_assert(OFF_META + (5 * MAX_ROUTES + 1) * 4 <= OFF_DONE, "worklist overlaps the counters");
+static_assert(OFF_DONE + MAX_ROUTES * 4 <= OFF_H, "counters overlap h");
 
 // Worklist of the expert kernel from per-route record indices: entries are
 // the distinct records in ascending index, each with its routes in (t, j)
@@ -55,6 +58,8 @@ __global__ void __launch_bounds__(PREP_THREADS) noalloc_prep_kernel(const int* _
     int* as_tok = wl_off + MAX_ROUTES + 1;
     float* as_gate = reinterpret_cast<float*>(as_tok + MAX_ROUTES);
     int* out_pos = reinterpret_cast<int*>(as_gate + MAX_ROUTES);
+    unsigned* done = reinterpret_cast<unsigned*>(scratch + OFF_DONE);
+    for (int i = tid; i < MAX_ROUTES; i += PREP_THREADS) done[i] = 0u;
     if (tid == 0) {
         s_ug = 0;
         s_na = 0;
@@ -171,5 +176,6 @@ extern "C" ft_status ft_expert_ffn_noalloc(const void* records, int32_t n_record
     p.hbuf = reinterpret_cast<float*>(sc + OFF_H);
     p.err = reinterpret_cast<unsigned*>(sc + OFF_ERR);
     p.gbar = reinterpret_cast<unsigned*>(sc + OFF_GBAR);
+    p.ready = reinterpret_cast<unsigned*>(sc + OFF_DONE);
     return launch_expert_ffn(p, ds.num_sms, s) == cudaSuccess ? FT_OK : FT_ERR_CUDA;
 }
