@@ -37,7 +37,8 @@ constexpr int CONSUMERS = CONSUMER_WARPS * 32;
 constexpr int PRODUCER_WARP = CONSUMER_WARPS;   // TMA issue of the phase-A/B ring
 constexpr int FILL_ISSUE_WARP = CONSUMER_WARPS + 1;  // fused cache fill: copies
 constexpr int FILL_MATH_WARP = CONSUMER_WARPS + 2;   // fused cache fill: gate/up math
-constexpr int EXPERT_THREADS = CONSUMERS + 3 * 32;
+constexpr int H_WARP = CONSUMER_WARPS + 3;          // phase-B stages: h rows once complete
+constexpr int EXPERT_THREADS = CONSUMERS + 4 * 32;
 constexpr int FPC = CONSUMER_WARPS;             // features per phase-A chunk
 constexpr size_t HEAD = 256;                    // barrier area
 
@@ -80,7 +81,8 @@ __device__ __forceinline__ void gu_dots(const uint4* __restrict__ wg, const uint
 #pragma unroll
     for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
     const int nv = K >> 3;
-#pragma unroll 4
+    // several tokens already give independent chains: unroll only for few
+#pragma unroll(NT >= 4 ? 1 : (NT == 2 ? 2 : 4))
     for (int v = lane; v < nv; v += 32) {
         float g8[8], u8[8];
         ft::bf16x8_to_f32(wg[v], g8);
@@ -149,17 +151,16 @@ __device__ __forceinline__ void gu_group(const uint4* wg, const uint4* wu, const
     }
 }
 
+// Out of line: one copy serves the consumer warps and the fill math warp,
+// which keeps the kernel's hot code small enough for the instruction cache.
 template <bool XF>
-__device__ __forceinline__ void gu_feature(const uint4* wg, const uint4* wu, const void* xs, const int* m_tok,
+__device__ __noinline__ void gu_feature(const uint4* wg, const uint4* wu, const void* xs, const int* m_tok,
                                            int off, int ntok, int K, int H, int k0, int F, int f, int lane,
                                            float* hbuf, int seg = 0, int nseg = 1, float* facc = nullptr) {
     int g0 = 0;
     while (g0 < ntok) {
         const int rem = ntok - g0;
-        if (rem >= 8) {
-            gu_group<8, XF>(wg, wu, xs, m_tok, off, g0, K, H, k0, F, f, lane, hbuf, seg, nseg, facc);
-            g0 += 8;
-        } else if (rem >= 4) {
+        if (rem >= 4) {
             gu_group<4, XF>(wg, wu, xs, m_tok, off, g0, K, H, k0, F, f, lane, hbuf, seg, nseg, facc);
             g0 += 4;
         } else if (rem >= 2) {
@@ -172,58 +173,75 @@ __device__ __forceinline__ void gu_feature(const uint4* wg, const uint4* wu, con
     }
 }
 
-// ---- phase B inner loop: one W_d row against NT token rows of h (fp32, smem)
+// ---- phase B inner loop: the rows rb + wid + 8 i (i < 4, row < R) of one
+// entry's W_d block in shared memory against NT token rows of h (fp32, shared
+// memory).  Each column chunk of h is read once and applied to all the rows
+// of the warp, which gives independent accumulation chains.
 template <int NT>
-__device__ __forceinline__ void down_group(const uint4* __restrict__ wrow, const float* hs, int g0, int F, int lane,
-                                           float* o_s, int obase, int RMAX, int rl) {
-    float acc[NT];
+__device__ __forceinline__ void down_group(uint32_t wbase, uint32_t hs, int g0, int F, int R, int rb, int wid,
+                                           int lane, float* o_s, int obase, int RMAX) {
+    float acc[4][NT];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n] = 0.f;
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[r][n] = 0.f;
     const int nv = F >> 3;
-#pragma unroll 3
     for (int v = lane; v < nv; v += 32) {
-        float w8[8];
-        ft::bf16x8_to_f32(wrow[v], w8);
+        float hv[NT][8];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-            const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)(g0 + n) * F + v * 8);
-            const float4 x0 = hp[0], x1 = hp[1];
-            float s = acc[n];
-            s = fmaf(w8[0], x0.x, s);
-            s = fmaf(w8[1], x0.y, s);
-            s = fmaf(w8[2], x0.z, s);
-            s = fmaf(w8[3], x0.w, s);
-            s = fmaf(w8[4], x1.x, s);
-            s = fmaf(w8[5], x1.y, s);
-            s = fmaf(w8[6], x1.z, s);
-            s = fmaf(w8[7], x1.w, s);
-            acc[n] = s;
+            const uint32_t hp = hs + ((uint32_t)(g0 + n) * F + v * 8) * 4u;
+            const float4 x0 = ft::lds128f(hp), x1 = ft::lds128f(hp + 16);
+            hv[n][0] = x0.x; hv[n][1] = x0.y; hv[n][2] = x0.z; hv[n][3] = x0.w;
+            hv[n][4] = x1.x; hv[n][5] = x1.y; hv[n][6] = x1.z; hv[n][7] = x1.w;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int rl = rb + wid + r * CONSUMER_WARPS;
+            if (rl < R) {
+                float w8[8];
+                ft::bf16x8_to_f32(ft::lds128(wbase + (uint32_t)rl * F * 2 + v * 16), w8);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    float s2 = acc[r][n];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) s2 = fmaf(w8[q], hv[n][q], s2);
+                    acc[r][n] = s2;
+                }
+            }
         }
     }
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-        const float sv = ft::warp_sum(acc[n]);
-        if (lane == 0) o_s[(size_t)(obase + g0 + n) * RMAX + rl] = sv;
+    for (int r = 0; r < 4; ++r) {
+        const int rl = rb + wid + r * CONSUMER_WARPS;
+        if (rl < R) {  // warp-uniform
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const float sv = ft::warp_sum(acc[r][n]);
+                if (lane == 0) o_s[(size_t)(obase + g0 + n) * RMAX + rl] = sv;
+            }
+        }
     }
 }
 
-__device__ __forceinline__ void down_row(const uint4* wrow, const float* hs, int ntok, int F, int lane, float* o_s,
-                                         int off, int RMAX, int rl) {
-    int g0 = 0;
-    while (g0 < ntok) {
-        const int rem = ntok - g0;
-        if (rem >= 8) {
-            down_group<8>(wrow, hs, g0, F, lane, o_s, off, RMAX, rl);
-            g0 += 8;
-        } else if (rem >= 4) {
-            down_group<4>(wrow, hs, g0, F, lane, o_s, off, RMAX, rl);
-            g0 += 4;
-        } else if (rem >= 2) {
-            down_group<2>(wrow, hs, g0, F, lane, o_s, off, RMAX, rl);
-            g0 += 2;
-        } else {
-            down_group<1>(wrow, hs, g0, F, lane, o_s, off, RMAX, rl);
-            g0 += 1;
+// All rows [0, R) of one entry, NT tokens at a time.  Out of line, like
+// gu_feature, to keep the hot code small; W_d rows and h by shared address.
+__device__ __noinline__ void down_entry(uint32_t wbase, uint32_t hs, int ntok, int F, int R, int wid, int lane,
+                                        float* o_s, int obase, int RMAX) {
+    for (int rb = 0; rb < R; rb += 4 * CONSUMER_WARPS) {
+        int g0 = 0;
+        while (g0 < ntok) {
+            const int rem = ntok - g0;
+            if (rem >= 4) {
+                down_group<4>(wbase, hs, g0, F, R, rb, wid, lane, o_s, obase, RMAX);
+                g0 += 4;
+            } else if (rem >= 2) {
+                down_group<2>(wbase, hs, g0, F, R, rb, wid, lane, o_s, obase, RMAX);
+                g0 += 2;
+            } else {
+                down_group<1>(wbase, hs, g0, F, R, rb, wid, lane, o_s, obase, RMAX);
+                g0 += 1;
+            }
         }
     }
 }
@@ -231,6 +249,7 @@ __device__ __forceinline__ void down_row(const uint4* wrow, const float* hs, int
 __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_wd;     // this CTA's W_d rows of every fill are stored (1), or the fill failed (2)
+    __shared__ int s_armed;  // ring steps armed by the producer (-1 after a failure)
     const int H = p.H, F = p.F, T = p.T, k = p.k;
     const int nst = p.nstage;
     const unsigned slot_bytes = p.stage_bytes;
@@ -287,6 +306,13 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         }
         return e1;
     };
+    // One ring sequence for the producer, the h warp and the consumers: the
+    // phase-A items c, c + G, ..., then the phase-B stages.
+    auto stage_due = [&](int a, int e0) { return e0 < nB && a >= NA; };
+    // h of the resident entries is complete once every CTA has counted its
+    // phase-A items in hits_done; h of fill r once the math warps have counted
+    // its F features in ready[r]
+    unsigned* hits_done = p.gbar + 1;
 
     // fused-fill geometry: unit = (fill r, group of fpf features), split into
     // nks K segments of KS columns; units go to CTAs round-robin.  Every CTA
@@ -320,6 +346,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         }
         ft::mbar_fence_init();
         s_wd = 0;
+        s_armed = 0;
     }
     for (int i = tid; i <= ugpu; i += EXPERT_THREADS) m_off[i] = p.wl_off[i];
     for (int i = tid; i < ugpu; i += EXPERT_THREADS) m_slot[i] = p.wl_slot[i];
@@ -456,6 +483,49 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         return;
     }
 
+    // -------------------------------------------------------------- h warp
+    // For each phase-B stage armed by the producer: the h rows of each entry,
+    // once every feature of it is written (by whichever CTA computed it).
+    // After a timed-out wait the rows are still copied (whatever they hold)
+    // so that the stage completes and the ring drains.
+    if (wid == H_WARP) {
+        if (lane == 0) {
+            for (int a = c, e0 = 0, it = 0;; ++it) {
+                const bool isB = stage_due(a, e0);
+                if (!isB && a >= NA) break;
+                if (!isB) {
+                    a += G;
+                    continue;
+                }
+                const int e1 = stage_end(e0);
+                const uint64_t t0 = ft::globaltimer();
+                int armed;
+                while ((armed = ft::ld_acquire_cta(&s_armed)) >= 0 && armed <= it) {
+                    __nanosleep(128);  // leave the issue slots to the consumer warps
+                    if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                        atomicOr(p.err, FT_DEVERR_TIMEOUT);
+                        armed = -1;
+                        break;
+                    }
+                }
+                if (armed < 0) break;
+                const int st = it % nst;
+                unsigned char* dst = ring + (size_t)st * slot_bytes;
+                unsigned o = 0;
+                for (int e = e0; e < e1; ++e) {
+                    if (e < nA)
+                        ft::wait_count(hits_done, (unsigned)G, p.err);
+                    else
+                        ft::wait_count(&p.ready[e], (unsigned)F, p.err);
+                    ft::bulk_g2s(dst + o + wpad, p.hbuf + (size_t)m_off[e] * F, hbytes(e), &full[st]);
+                    o += wpad + ((hbytes(e) + 127u) & ~127u);
+                }
+                e0 = e1;
+            }
+        }
+        return;
+    }
+
     // ------------------------------------------------------------ producer
     if (wid == PRODUCER_WARP) {
         if (lane == 0) {
@@ -469,33 +539,35 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             };
             int it = 0;
             bool ok = true;
-            for (int a = c; a < NA && ok; a += G, ++it) {
+            bool wd_ready = false;
+            for (int a = c, e0 = 0; ok; ++it) {
+                const bool isB = stage_due(a, e0);
+                if (!isB && a >= NA) break;
                 const int st = it % nst;
                 if (it == nst) prefetch_wd();
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
-                const int ent = a / cpe;
-                const int f0 = (a - ent * cpe) * FPC;
-                const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
-                const int grp = f0 >> 4, i = f0 & 15;
                 unsigned char* dst = ring + (size_t)st * slot_bytes;
-                ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * rowbytes);
-                ft::bulk_g2s_hint(dst, rec + (size_t)(grp * 32 + i) * rowbytes, FPC * rowbytes, &full[st], pol);
-                ft::bulk_g2s_hint(dst + (size_t)FPC * rowbytes, rec + (size_t)(grp * 32 + 16 + i) * rowbytes,
-                                  FPC * rowbytes, &full[st], pol);
-            }
-            if (it < nst) prefetch_wd();
-            // phase B, stage by stage: the W_d rows of the stage's entries,
-            // then the h rows of each entry once every feature of it is
-            // written, by whichever CTA computed it.
-            bool wd_ready = false;
-            for (int e0 = 0; e0 < nB && ok; ++it) {
-                const int st = it % nst;
-                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
+                if (!isB) {
+                    const int ent = a / cpe;
+                    const int f0 = (a - ent * cpe) * FPC;
+                    const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
+                    const int grp = f0 >> 4, i = f0 & 15;
+                    ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * rowbytes);
+                    ft::bulk_g2s_hint(dst, rec + (size_t)(grp * 32 + i) * rowbytes, FPC * rowbytes, &full[st], pol);
+                    ft::bulk_g2s_hint(dst + (size_t)FPC * rowbytes, rec + (size_t)(grp * 32 + 16 + i) * rowbytes,
+                                      FPC * rowbytes, &full[st], pol);
+                    a += G;
+                    continue;
+                }
+                // phase-B stage: the W_d rows of its entries (those of a fill
+                // were stored by this CTA's fill warp), then the h rows of each
+                // entry once every feature of it is written
                 const int e1 = stage_end(e0);
                 if (e0 >= nA && !wd_ready) {
                     const uint64_t t0 = ft::globaltimer();
                     int v;
                     while ((v = ft::ld_acquire_cta(&s_wd)) == 0) {
+                        __nanosleep(128);
                         if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
                             atomicOr(p.err, FT_DEVERR_TIMEOUT);
                             break;
@@ -505,7 +577,6 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     wd_ready = true;
                 }
-                unsigned char* dst = ring + (size_t)st * slot_bytes;
                 unsigned tx = 0;
                 for (int e = e0; e < e1; ++e) tx += wb + hbytes(e);
                 ft::mbar_arrive_expect_tx(&full[st], tx);
@@ -515,64 +586,58 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                     ft::bulk_g2s_hint(dst + o, wd, wb, &full[st], pol);
                     o += wpad + ((hbytes(e) + 127u) & ~127u);
                 }
-                o = 0;
-                for (int e = e0; e < e1; ++e) {
-                    // after a timed-out wait the h rows are still copied (whatever
-                    // they hold) so that the stage completes and the ring drains
-                    if (!ft::wait_count(&p.ready[e], (unsigned)F, p.err)) ok = false;
-                    ft::bulk_g2s(dst + o + wpad, p.hbuf + (size_t)m_off[e] * F, hbytes(e), &full[st]);
-                    o += wpad + ((hbytes(e) + 127u) & ~127u);
-                }
+                ft::st_release_cta(&s_armed, it + 1);  // the h warp adds the h rows
                 e0 = e1;
             }
+            if (!ok) ft::st_release_cta(&s_armed, -1);
+            if (it <= nst) prefetch_wd();
             ft::drain_ring(full, it, nst, p.err);
         }
         return;
     }
 
-    // ------------------------------------------------- phase A: gate/up + SwiGLU
+    // ------------------------------- consumers: phase-A items and phase-B stages
     // After a failed (timed-out) wait a warp stops waiting, computing and
     // releasing slots, but keeps the same barrier sequence as the others.
     int it = 0;
     bool failed = false;
-    for (int a = c; a < NA; a += G, ++it) {
+    if (c >= NA && tid == 0) ft::red_release_gpu_add(hits_done, 1u);
+    for (int a = c, e0 = 0;; ++it) {
+        const bool isB = stage_due(a, e0);
+        if (!isB && a >= NA) break;
         const int st = it % nst;
-        const bool ok = !failed && __all_sync(0xffffffffu, ft::mbar_wait(&full[st], (it / nst) & 1, p.err));
-        failed = !ok;
-        const int ent = a / cpe;
-        const int f = (a - ent * cpe) * FPC + wid;
-        const int off = m_off[ent];
-        const int ntok = m_off[ent + 1] - off;
-        const uint4* wg = reinterpret_cast<const uint4*>(ring + (size_t)st * slot_bytes + (size_t)wid * rowbytes);
-        const uint4* wu = reinterpret_cast<const uint4*>(ring + (size_t)st * slot_bytes +
-                                                         (size_t)(FPC + wid) * rowbytes);
-        if (ok) {
-            if (xf32)
-                gu_feature<true>(wg, wu, x_s, m_tok, off, ntok, H, H, 0, F, f, lane, p.hbuf);
-            else
-                gu_feature<false>(wg, wu, x_s, m_tok, off, ntok, H, H, 0, F, f, lane, p.hbuf);
-        }
-        __syncwarp();
-        if (ok && lane == 0) {
-            ft::mbar_arrive(&empty[st]);
-            ft::red_release_gpu_add(&p.ready[ent], 1u);
-        }
-    }
-
-    // ---------------------------------------------------- phase B: down rows
-    for (int e0 = 0; e0 < nB; ++it) {
-        const int st = it % nst;
-        const int e1 = stage_end(e0);
         const bool ok = !failed && __all_sync(0xffffffffu, ft::mbar_wait(&full[st], (it / nst) & 1, p.err));
         failed = !ok;
         const unsigned char* sb = ring + (size_t)st * slot_bytes;
+        if (!isB) {
+            // gate/up + SwiGLU: warp w computes feature w of the item
+            const int ent = a / cpe;
+            const int f = (a - ent * cpe) * FPC + wid;
+            const int off = m_off[ent];
+            const int ntok = m_off[ent + 1] - off;
+            const uint4* wg = reinterpret_cast<const uint4*>(sb + (size_t)wid * rowbytes);
+            const uint4* wu = reinterpret_cast<const uint4*>(sb + (size_t)(FPC + wid) * rowbytes);
+            if (ok) {
+                if (xf32)
+                    gu_feature<true>(wg, wu, x_s, m_tok, off, ntok, H, H, 0, F, f, lane, p.hbuf);
+                else
+                    gu_feature<false>(wg, wu, x_s, m_tok, off, ntok, H, H, 0, F, f, lane, p.hbuf);
+            }
+            __syncwarp();
+            if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+            a += G;
+            if (a >= NA) {  // this CTA's h of the resident entries is written
+                ft::named_bar_sync(2, CONSUMERS);
+                if (tid == 0) ft::red_release_gpu_add(hits_done, 1u);
+            }
+            continue;
+        }
+        // down rows [r0, r1) of the stage's entries
+        const int e1 = stage_end(e0);
         for (int e = e0; e < e1 && ok; ++e) {
             const int off = m_off[e];
             const int ntok = m_off[e + 1] - off;
-            const float* hs = reinterpret_cast<const float*>(sb + wpad);
-            for (int rl = wid; rl < R; rl += CONSUMER_WARPS)
-                down_row(reinterpret_cast<const uint4*>(sb + (size_t)rl * F * 2), hs, ntok, F, lane, o_s, off, RMAX,
-                         rl);
+            down_entry(ft::smem_addr(sb), ft::smem_addr(sb + wpad), ntok, F, R, wid, lane, o_s, off, RMAX);
             sb += wpad + ((hbytes(e) + 127u) & ~127u);
         }
         __syncwarp();
@@ -592,14 +657,15 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         if (p.partial_C) acc += p.partial_C[oi];
         p.y[oi] = acc;
     }
-    // the last CTA out returns the per-entry counters to zero for the next
-    // launch: every CTA's reads of them precede its exit count
+    // the last CTA out returns the counters to zero for the next launch:
+    // every CTA's reads of them precede its exit count
     ft::named_bar_sync(1, CONSUMERS);
     if (tid == 0) {
         unsigned n;
         asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.gbar) : "memory");
         if (n == (unsigned)G - 1) {
             for (int e = 0; e < ugpu; ++e) p.ready[e] = 0u;
+            p.gbar[1] = 0u;
             p.gbar[0] = 0u;
         }
     }

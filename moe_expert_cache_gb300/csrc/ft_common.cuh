@@ -147,6 +147,19 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Explicit shared-memory loads by 32-bit shared address (for out-of-line
+// helpers, where a generic pointer would compile to generic loads).
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+
 // 8 bf16 packed in a uint4 -> 8 floats.
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -252,7 +265,8 @@ __device__ __forceinline__ bool wait_count(const unsigned* c, unsigned target, u
         unsigned v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
         if (v >= target) break;
-        if ((it & 63u) == 63u && globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+        __nanosleep(64);  // a poll of L2: leave the issue slots to the math warps
+        if ((it & 15u) == 15u && globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
             atomicOr(err, FT_DEVERR_TIMEOUT);
             return false;
         }
