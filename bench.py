@@ -628,6 +628,43 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_ncu_case(args):
+    """A small single-layer case for profiler captures (not a bench line).
+
+    One layer of the decode T=1 shape (E=128, top-8, H=2048, F=768) in 128
+    slots.  Every call routes the token to experts 0..7-q (resident) plus q
+    experts not yet resident, so each expert-kernel launch runs 8-q hits and
+    q fused fills.  Six calls; capture e.g. the fifth expert launch with
+    `ncu -k regex:expert_ffn -s 4 -c 1`.
+    """
+    import torch
+    import moe_expert_cache_gb300 as ft
+
+    ft.load()
+    q = args.ncu_case
+    sh = synth.Shape(L=1, E=128, k=8, H=2048, F=768)
+    pool = torch.empty(sh.E * sh.record_bytes, dtype=torch.uint8, pin_memory=True)
+    synth.fill_host_pool(pool.numpy(), sh, 0)
+    s = torch.cuda.Stream()
+    x = torch.from_numpy(synth.tokens_bf16(0, 0, 0, 1, sh.H).view(np.int16)).cuda().view(torch.bfloat16)
+    pc = torch.zeros(1, sh.H, device="cuda")
+    y = torch.empty(1, sh.H, device="cuda")
+    w = torch.full((1, sh.k), 1.0 / sh.k, device="cuda")
+    ctx = ft.Context(1, sh.E, sh.k, sh.H, sh.F, 128, pool, T_max=1, compute_stream=s.cuda_stream)
+    with torch.cuda.stream(s):
+        for i in range(6):
+            ids = list(range(sh.k - q)) + [sh.k + q * i + j for j in range(q)]
+            ctx.route_ctl(0, 1, topk_ids=torch.tensor([ids], dtype=torch.int32, device="cuda"), topk_w=w,
+                          B_P=1.0, B_H=1.0)
+            ctx.moe_forward(x, pc, y)
+    torch.cuda.synchronize()
+    st = ctx.status()
+    ctx.close()
+    if st != ft.FT_OK:
+        raise SystemExit(f"device status {st}")
+    return None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -637,7 +674,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ncu-case", type=int, default=None, metavar="Q",
+                    help="run the small single-layer profiling case with Q fills per call (0..8) and exit")
     args = ap.parse_args()
+    if args.ncu_case is not None:
+        if not 0 <= args.ncu_case <= 8:
+            raise SystemExit("--ncu-case takes 0..8")
+        run_ncu_case(args)
+        return
     rank, world, local_rank = dist_env()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
