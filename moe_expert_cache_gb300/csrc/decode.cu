@@ -313,6 +313,18 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     // phase-A items in hits_done; h of fill r once the math warps have counted
     // its F features in ready[r]
     unsigned* hits_done = p.gbar + 1;
+    // Exit count: the consumers, the fill copy warp and the fill math warp of
+    // every CTA each count out once they are done with the counters; whoever
+    // completes the count returns the counters to zero for the next launch.
+    auto count_out = [&]() {
+        unsigned n;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.gbar) : "memory");
+        if (n == 3u * (unsigned)G - 1u) {
+            for (int e = 0; e < ugpu; ++e) p.ready[e] = 0u;
+            p.gbar[1] = 0u;
+            p.gbar[0] = 0u;
+        }
+    };
 
     // fused-fill geometry: unit = (fill r, group of fpf features), split into
     // nks K segments of KS columns; units go to CTAs round-robin.  Every CTA
@@ -335,38 +347,51 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         f0 = (u - r * upr) * fpf;
     };
 
-    if (tid == 0) {
-        for (int s = 0; s < nst; ++s) {
-            ft::mbar_init(&full[s], 1);
-            ft::mbar_init(&empty[s], CONSUMER_WARPS);
+    // The fill copy warp owns its ring barriers and s_wd and starts at once;
+    // the other warps stage the worklist and x meanwhile.  Named barrier 3:
+    // the copy warp arrives once its state is initialised, the rest sync.
+    if (wid == FILL_ISSUE_WARP) {
+        if (lane == 0) {
+            for (int s = 0; s < nf; ++s) {
+                ft::mbar_init(&ffull[s], 32);  // one cp.async arrival per lane of the copy warp
+                ft::mbar_init(&fcons[s], 1);
+            }
+            ft::mbar_fence_init();
+            s_wd = 0;
         }
-        for (int s = 0; s < nf; ++s) {
-            ft::mbar_init(&ffull[s], 32);  // one cp.async arrival per lane of the copy warp
-            ft::mbar_init(&fcons[s], 1);
-        }
-        ft::mbar_fence_init();
-        s_wd = 0;
-        s_armed = 0;
-    }
-    for (int i = tid; i <= ugpu; i += EXPERT_THREADS) m_off[i] = p.wl_off[i];
-    for (int i = tid; i < ugpu; i += EXPERT_THREADS) m_slot[i] = p.wl_slot[i];
-    for (int i = tid; i < nasg; i += EXPERT_THREADS) {
-        m_tok[i] = p.as_tok[i];
-        m_gate[i] = p.as_gate[i];
-    }
-    for (int i = tid; i < TK; i += EXPERT_THREADS) m_pos[i] = p.out_pos[i];
-    if (xf32) {
-        for (int i = tid; i < T * H / 8; i += EXPERT_THREADS) {
-            float f8[8];
-            ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
-            reinterpret_cast<float4*>(x_s)[2 * i] = make_float4(f8[0], f8[1], f8[2], f8[3]);
-            reinterpret_cast<float4*>(x_s)[2 * i + 1] = make_float4(f8[4], f8[5], f8[6], f8[7]);
-        }
+        __syncwarp();
+        asm volatile("bar.arrive 3, %0;" ::"n"(EXPERT_THREADS) : "memory");
     } else {
-        for (int i = tid; i < (int)(xbytes / 16); i += EXPERT_THREADS)
-            reinterpret_cast<uint4*>(x_s)[i] = reinterpret_cast<const uint4*>(p.x)[i];
+        if (tid == 0) {
+            for (int s = 0; s < nst; ++s) {
+                ft::mbar_init(&full[s], 1);
+                ft::mbar_init(&empty[s], CONSUMER_WARPS);
+            }
+            ft::mbar_fence_init();
+            s_armed = 0;
+        }
+        constexpr int NS = EXPERT_THREADS - 32;  // staging threads: every warp but the copy warp
+        const int st0 = wid < FILL_ISSUE_WARP ? tid : tid - 32;
+        for (int i = st0; i <= ugpu; i += NS) m_off[i] = p.wl_off[i];
+        for (int i = st0; i < ugpu; i += NS) m_slot[i] = p.wl_slot[i];
+        for (int i = st0; i < nasg; i += NS) {
+            m_tok[i] = p.as_tok[i];
+            m_gate[i] = p.as_gate[i];
+        }
+        for (int i = st0; i < TK; i += NS) m_pos[i] = p.out_pos[i];
+        if (xf32) {
+            for (int i = st0; i < T * H / 8; i += NS) {
+                float f8[8];
+                ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
+                reinterpret_cast<float4*>(x_s)[2 * i] = make_float4(f8[0], f8[1], f8[2], f8[3]);
+                reinterpret_cast<float4*>(x_s)[2 * i + 1] = make_float4(f8[4], f8[5], f8[6], f8[7]);
+            }
+        } else {
+            for (int i = st0; i < (int)(xbytes / 16); i += NS)
+                reinterpret_cast<uint4*>(x_s)[i] = reinterpret_cast<const uint4*>(p.x)[i];
+        }
+        ft::named_bar_sync(3, EXPERT_THREADS);
     }
-    __syncthreads();
 
     // ------------------------------------------------- fused fill: copy warp
     // host pool -> fill ring by per-lane cp.async (the load/store path, so the
@@ -449,6 +474,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             ft::bulk_wait_all();
             asm volatile("fence.proxy.async.global;" ::: "memory");
             ft::st_release_cta(&s_wd, ok ? 1 : 2);
+            count_out();
         }
         return;
     }
@@ -480,6 +506,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 if (seg == nks - 1) ft::red_release_gpu_add(&p.ready[nA + r], (unsigned)fpf);
             }
         }
+        __syncwarp();
+        if (lane == 0) count_out();  // after the last release
         return;
     }
 
@@ -657,18 +685,10 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         if (p.partial_C) acc += p.partial_C[oi];
         p.y[oi] = acc;
     }
-    // the last CTA out returns the counters to zero for the next launch:
-    // every CTA's reads of them precede its exit count
+    // every read of the counters by this CTA's consumers, producer and h warp
+    // precedes the end of its phase B
     ft::named_bar_sync(1, CONSUMERS);
-    if (tid == 0) {
-        unsigned n;
-        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.gbar) : "memory");
-        if (n == (unsigned)G - 1) {
-            for (int e = 0; e < ugpu; ++e) p.ready[e] = 0u;
-            p.gbar[1] = 0u;
-            p.gbar[0] = 0u;
-        }
-    }
+    if (tid == 0) count_out();
 }
 
 }  // namespace
@@ -680,7 +700,7 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
 
 static constexpr size_t kSmemLimit = 227 * 1024 - 256;  // dynamic; the rest is static shared memory
 static constexpr size_t kFillChunk = 4096;               // bytes of one fused-fill ring chunk
-static constexpr int kFillSlots = 2;                     // fused-fill ring chunks per CTA
+static constexpr int kFillSlots = 3;                     // fused-fill ring chunks per CTA
 
 // Shared-memory plan: barriers, x (if it fits in 64 KiB), the per-CTA output
 // block, the worklist metadata and the fill math warp's segment sums, then the

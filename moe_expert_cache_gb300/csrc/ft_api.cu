@@ -247,7 +247,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
                  o_fs = carve((size_t)E * 4),
                  o_ff = carve((size_t)E * 4), o_F = carve((size_t)E * 4), o_C = carve((size_t)E * 4),
                  o_v = carve((size_t)E * 4), o_info = carve(INFO_WORDS * 4), o_cnt = carve(CNT_WORDS * 8),
-                 o_err = carve(4), o_gbar = carve(8);
+                 o_err = carve(4), o_gbar = carve(16);
     INIT_CUDA(cudaMalloc(&c->arena, off));
     INIT_CUDA(cudaMemset(c->arena, 0, off));
     uint8_t* a = (uint8_t*)c->arena;

@@ -411,7 +411,8 @@ struct ExpertParams {
     const int* out_pos;
     float* hbuf;              // [T*k, F] fp32
     unsigned* err;
-    unsigned* gbar;           // [2] NVFP4: grid barrier (arrivals, generation); BF16: [0] exit count; zero at rest
+    unsigned* gbar;           // [4] NVFP4: grid barrier (arrivals, generation); BF16: exit count, hits done;
+                              // zero at rest
     const int* wl_fid;        // [E] flat id of each GPU entry (NVFP4 global lookup)
     // fused cache fill (performed by this launch when do_fill != 0)
     int do_fill;

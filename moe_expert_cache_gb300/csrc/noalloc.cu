@@ -33,7 +33,7 @@ constexpr int PREP_THREADS = 512;
 constexpr int MAX_ROUTES = 1024;  // T*k
 // Byte offsets inside the scratch array.
 constexpr size_t OFF_INFO = 0;       // int[INFO_WORDS]
-constexpr size_t OFF_GBAR = 128;     // unsigned[2]: exit count, zero at load, self-resetting
+constexpr size_t OFF_GBAR = 128;     // unsigned[4]: completion words, zero at load, self-resetting
 constexpr size_t OFF_ERR = 192;      // unsigned
 constexpr size_t OFF_META = 256;     // worklist arrays, MAX_ROUTES entries each
 constexpr size_t OFF_DONE = 32768;   // unsigned[MAX_ROUTES]: h features written per entry
