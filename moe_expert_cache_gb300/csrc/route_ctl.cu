@@ -104,9 +104,6 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     int* s_vict = s_eoff + E;   // [E] victims by rank
     int* s_cslot = s_vict + E;  // [E] radix path: candidates with stamp < tau
     unsigned* s_cst = reinterpret_cast<unsigned*>(s_cslot + E);  // [E]
-    int* s_fillrank = reinterpret_cast<int*>(s_cst + E);         // [E] fill index of an F expert
-    int* s_ent = s_fillrank + E;                                  // [E] worklist entry of a GPU expert
-    int* s_ecnt = s_ent + E;                                      // [E] routed count, then offset, per entry
 
     if (tid == 0) {
         sh.bad = 0;
@@ -262,19 +259,21 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     }
     __syncthreads();
 
-    // ---- a5 (order): fill rank of every miss = (count desc, id asc); a4: q
-    for (int e = tid; e < E; e += CTL_THREADS) {
-        if (s_cls[e] == 3) {
-            const int ne = s_cnt[e];
-            int r = 0;
-            for (int e2 = 0; e2 < E; ++e2) {
-                if (s_cls[e2] == 3) {
-                    const int n2 = s_cnt[e2];
-                    r += (n2 > ne) || (n2 == ne && e2 < e);
-                }
+    // ---- a5 (order): fill rank of every miss = (count desc, id asc); a4: q.
+    // One warp per miss counts the misses that precede it, 32 ids at a time.
+    for (int e = wid; e < E; e += CTL_WARPS) {
+        if (s_cls[e] != 3) continue;  // warp-uniform
+        const int ne = s_cnt[e];
+        int r = 0;
+        for (int e2 = lane; e2 < E; e2 += 32) {
+            if (s_cls[e2] == 3) {
+                const int n2 = s_cnt[e2];
+                r += (n2 > ne) || (n2 == ne && e2 < e);
             }
-            s_order[r] = e;
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+        if (lane == 0) s_order[r] = e;
     }
     if (tid == 0) {
         const int m = sh.m, h = sh.h;
@@ -433,7 +432,6 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         p.slot_for_id[fid] = v;
         p.stamps[v] = clk;
         s_slot[f] = v;
-        s_fillrank[f] = i;
         p.ready[i] = 0u;
         p.fill_slot[i] = v;
         p.fill_fid[i] = fid;
@@ -443,63 +441,65 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
 
     // ---- a7: GPU worklist and the slot rewrite.  Entries: the hits in
     // ascending expert id, then the fills in fill order (the expert kernel
-    // computes the hits while the fills are still landing).
-    if (tid == 0) {
-        sh.carry0 = 0;
-        sh.carry1 = 0;
-    }
-    __syncthreads();
-    for (int e0 = 0; e0 < E; e0 += CTL_THREADS) {
-        const int e = e0 + tid;
-        const int ishit = (e < E && s_cls[e] == 1) ? 1 : 0;
-        int tot;
-        const int ex = block_excl_scan(ishit, sh.warp_tot, &tot);
-        if (ishit) s_ent[e] = ex + sh.carry0;
-        __syncthreads();
-        if (tid == 0) sh.carry0 += tot;
-        __syncthreads();
-    }
-    const int nh = sh.carry0;
-    for (int e = tid; e < E; e += CTL_THREADS) {
-        const int cl = s_cls[e];
-        if (cl == 1 || cl == 2) {
-            const int ent = cl == 1 ? s_ent[e] : nh + s_fillrank[e];
-            s_ent[e] = ent;
-            s_ecnt[ent] = s_cnt[e];
-            p.wl_slot[ent] = s_slot[e];
-            p.wl_fid[ent] = fbase + e;
-            p.wl_fill[ent] = cl == 2 ? s_fillrank[e] : -1;
+    // computes the hits while the fills are still landing).  One warp scans
+    // the entry numbers and the assignment offsets, 32 experts at a time.
+    if (wid == 0) {
+        int nh = 0, off = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int hit = (e < E && s_cls[e] == 1) ? 1 : 0;
+            const int cnt = hit ? s_cnt[e] : 0;
+            int xh = hit, xc = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int yh = __shfl_up_sync(0xffffffffu, xh, o);
+                const int yc = __shfl_up_sync(0xffffffffu, xc, o);
+                if (lane >= o) {
+                    xh += yh;
+                    xc += yc;
+                }
+            }
+            if (hit) {
+                const int ent = nh + xh - 1;
+                const int eo = off + xc - cnt;
+                s_eoff[e] = eo;
+                p.wl_slot[ent] = s_slot[e];
+                p.wl_fid[ent] = fbase + e;
+                p.wl_fill[ent] = -1;
+                p.wl_off[ent] = eo;
+            }
+            nh += __shfl_sync(0xffffffffu, xh, 31);
+            off += __shfl_sync(0xffffffffu, xc, 31);
+        }
+        for (int i0 = 0; i0 < q; i0 += 32) {
+            const int i = i0 + lane;
+            const int e = i < q ? s_order[i] : -1;
+            const int cnt = e >= 0 ? s_cnt[e] : 0;
+            int xc = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int yc = __shfl_up_sync(0xffffffffu, xc, o);
+                if (lane >= o) xc += yc;
+            }
+            if (e >= 0) {
+                const int ent = nh + i;
+                const int eo = off + xc - cnt;
+                s_eoff[e] = eo;
+                p.wl_slot[ent] = s_slot[e];
+                p.wl_fid[ent] = fbase + e;
+                p.wl_fill[ent] = i;
+                p.wl_off[ent] = eo;
+            }
+            off += __shfl_sync(0xffffffffu, xc, 31);
+        }
+        if (lane == 0) {
+            sh.ugpu = nh + q;
+            sh.nassign = off;
+            p.wl_off[nh + q] = off;
+            *p.clock = clk;
         }
     }
     __syncthreads();
-    const int ug = nh + q;
-    if (tid == 0) sh.carry1 = 0;
-    __syncthreads();
-    for (int i0 = 0; i0 < ug; i0 += CTL_THREADS) {
-        const int i = i0 + tid;
-        const int cnt = i < ug ? s_ecnt[i] : 0;
-        int tot;
-        const int ex = block_excl_scan(cnt, sh.warp_tot, &tot);
-        if (i < ug) {
-            s_ecnt[i] = ex + sh.carry1;  // now the entry's first assignment
-            p.wl_off[i] = ex + sh.carry1;
-        }
-        __syncthreads();
-        if (tid == 0) sh.carry1 += tot;
-        __syncthreads();
-    }
-    for (int e = tid; e < E; e += CTL_THREADS) {
-        const int cl = s_cls[e];
-        if (cl == 1 || cl == 2) s_eoff[e] = s_ecnt[s_ent[e]];
-    }
-    if (tid == 0) sh.carry0 = ug;
-    __syncthreads();
-    if (tid == 0) {
-        sh.ugpu = sh.carry0;
-        sh.nassign = sh.carry1;
-        p.wl_off[sh.carry0] = sh.carry1;
-        *p.clock = clk;
-    }
     for (int a = tid; a < TK; a += CTL_THREADS) {
         const int e = s_ids[a];
         const int t = a / k;
