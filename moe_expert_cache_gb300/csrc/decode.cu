@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     const int n_gu = (c < U ? (U - c + G - 1) / G : 0) * nks;
     const unsigned long long wdb = (unsigned long long)R * F * 2;
     const int npc = (int)((wdb + fch - 1) / fch);
-    const int n_fill = n_gu + q * npc;
+    const int n_wd = q * npc;  // this CTA's W_d pieces, first in its chunk stream
+    const int n_fill = n_wd + n_gu;
     const unsigned partb = (unsigned)fpf * KS * 2u;  // gate (or up) bytes of one unit chunk
     auto gu_chunk = [&](int g, int& r, int& f0, int& seg) {
         const int u = c + (g / nks) * G;
@@ -406,14 +407,14 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         const unsigned long long upoff = (unsigned long long)16 * H * 2;  // up rows follow gate rows by 16 rows
         // offset within the record, bytes of one part, and fill index of chunk g
         auto locate = [&](int g, unsigned long long& off, unsigned& n, int& r) {
-            if (g < n_gu) {
+            if (g >= n_wd) {
                 int f0, seg;
-                gu_chunk(g, r, f0, seg);
+                gu_chunk(g - n_wd, r, f0, seg);
                 const unsigned long long row = (unsigned long long)(f0 >> 4) * 32 + (f0 & 15);
                 off = (row * H + (unsigned long long)seg * KS) * 2;
                 n = partb;
             } else {
-                const int w = g - n_gu;
+                const int w = g;
                 r = w / npc;
                 const unsigned long long po = (unsigned long long)(w - r * npc) * fch;
                 off = wd0 + po;
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             unsigned char* d = fring + (size_t)s * fch;
             const uint8_t* src = host + (unsigned long long)p.fill_fid[r] * p.rb + off;
             for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + v, src + v);
-            if (g < n_gu)
+            if (g >= n_wd)
                 for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + n + v, src + upoff + v);
             ft::cp_async_arrive(&ffull[s]);
         };
@@ -440,9 +441,17 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             const unsigned char* d = fring + (size_t)s * fch;
             uint8_t* dst = pool + (unsigned long long)p.fill_slot[r] * p.rb + off;
             ft::bulk_s2g(dst, d, n);
-            if (g < n_gu) ft::bulk_s2g(dst + upoff, d + n, n);
+            if (g >= n_wd) ft::bulk_s2g(dst + upoff, d + n, n);
             ft::bulk_commit();
         };
+        // s_wd: this CTA's W_d rows of every fill are in their slots (1), or
+        // the fill failed before that (2)
+        auto publish_wd = [&](int v) {  // lane 0
+            ft::bulk_wait_all();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            ft::st_release_cta(&s_wd, v);
+        };
+        if (lane == 0 && n_wd == 0) ft::st_release_cta(&s_wd, 1);
         int issued = 0;
         for (; issued < n_fill && issued < nf; ++issued) load(issued, issued);
         bool ok = true;
@@ -455,7 +464,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 if (w) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // cp.async data -> bulk store
                     store(g, s);
-                    if (g < n_gu) w = ft::mbar_wait(&fcons[s], par, p.err);
+                    if (g == n_wd - 1) publish_wd(1);
+                    w = ft::mbar_wait(&fcons[s], par, p.err);
                     ft::bulk_wait_read_all();
                 }
             }
@@ -472,8 +482,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         __syncwarp();
         if (lane == 0) {
             ft::bulk_wait_all();
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            ft::st_release_cta(&s_wd, ok ? 1 : 2);
+            if (ft::ld_acquire_cta(&s_wd) == 0) publish_wd(2);  // failed before its W_d rows were stored
             count_out();
         }
         return;
@@ -482,11 +491,16 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     // ------------------------------------------ fused fill: gate/up math warp
     // SwiGLU features of the fill units of this CTA, from the fill ring.
     if (wid == FILL_MATH_WARP) {
-        for (int g = 0; g < n_gu; ++g) {
+        for (int g = 0; g < n_fill; ++g) {
             const int s = g % nf;
             if (!__all_sync(0xffffffffu, ft::mbar_wait(&ffull[s], (uint32_t)(g / nf) & 1u, p.err))) break;
+            if (g < n_wd) {  // a W_d piece: acknowledged so the ring cannot lap this warp
+                __syncwarp();
+                if (lane == 0) ft::mbar_arrive(&fcons[s]);
+                continue;
+            }
             int r, f0, seg;
-            gu_chunk(g, r, f0, seg);
+            gu_chunk(g - n_wd, r, f0, seg);
             const int off = m_off[nA + r];
             const int ntok = m_off[nA + r + 1] - off;
             const unsigned char* d = fring + (size_t)s * fch;
