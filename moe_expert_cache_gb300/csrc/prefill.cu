@@ -217,8 +217,11 @@ __global__ void pf_invalidate_kernel(int s0, int n, int* __restrict__ slot_for_i
 //   warp 1      TMEM allocation (512 columns = two 256-column accumulators) and
 //               the MMA issuer (one thread, 4 x K=16 MMAs per stage)
 //   warps 2-5   epilogue: thread = accumulator row, tcgen05.ld 32 columns at a
-//               time; mode 0 = SwiGLU of the interleaved gate/up columns to bf16
-//               h, mode 1 = gate * value to fp32 out.
+//               time (the next load in flight while one is processed); mode 0 =
+//               SwiGLU of the interleaved gate/up columns to bf16 h, mode 1 =
+//               gate * value to fp32 out.  Each warp transposes its 32 rows x
+//               128 bytes through a padded shared-memory block, so every store
+//               instruction writes four whole 128-byte lines.
 // All waits are bounded; after a failed wait every role stops, the MMA thread
 // waits for its issued MMAs, and TMEM is freed before exit.
 namespace {
@@ -229,7 +232,9 @@ constexpr int GEMM_THREADS = 192;
 constexpr uint32_t A_BYTES = GM * GK * 2;   // 16 KiB
 constexpr uint32_t B_BYTES = GN * GK * 2;   // 32 KiB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr size_t GEMM_SMEM = 1024 + (size_t)GSTAGES * STAGE_BYTES + 1024;
+constexpr uint32_t EPI_ROW = 144;                 // 128 bytes of a row + 16 bytes of padding
+constexpr uint32_t EPI_WARP = 32 * EPI_ROW;       // one epilogue warp's staging block
+constexpr size_t GEMM_SMEM = 1024 + (size_t)GSTAGES * STAGE_BYTES + 4 * EPI_WARP + 1024;
 
 struct GemmArgs {
     int E;                 // experts of the layer (tensor-map z extent)
@@ -371,6 +376,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) grouped_gemm_kernel(const __g
         // ----------------------------------------------------------- epilogue
         const int q = wid & 3;  // TMEM lane quarter of this warp
         const int r = q * 32 + lane;
+        unsigned char* eb = gsm + (size_t)GSTAGES * STAGE_BYTES + (size_t)q * EPI_WARP;
+        const int rsub = lane >> 3, cq = (lane & 7) * 16;  // read-back: row within 4, byte offset in the line
         int t = 0;
         for (int i = blockIdx.x; i < ntiles && !s_fail; i += gridDim.x, ++t) {
             const int acc = t & 1;
@@ -380,23 +387,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) grouped_gemm_kernel(const __g
             }
             tc::fence_after_sync();
             const TileInfo ti = decode_tile(i, s_mt, p.offsets, E, p.n_tiles);
-            const bool valid = r < ti.rows;
             const int row = ti.m0 + r;
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * GN);
             const float es = p.escale ? p.escale[ti.e] : 1.f;
-            const float gate = (p.mode == 1 && valid) ? p.row_gate[row] * es : 0.f;
-#pragma unroll 1
-            for (int c = 0; c < GN / 32; ++c) {
-                uint32_t v[32];
-                tc::tmem_ld32(base + (uint32_t)(c * 32), v);
-                tc::tmem_wait_ld();
-                if (!valid) continue;
+            const float gate = (p.mode == 1 && r < ti.rows) ? p.row_gate[row] * es : 0.f;
+            const int wrow0 = ti.m0 + q * 32;  // first row of this warp's block
+            // one 32-column chunk of the accumulator row -> this lane's row of the
+            // staging block; mode 1: 128 bytes per chunk, mode 0: 32 bytes per
+            // chunk (four chunks fill the 128 bytes)
+            auto stage = [&](const uint32_t* v, int c) {
                 if (p.mode == 0) {
-                    // columns: 16 gate rows then the 16 matching up rows of features
-                    // f0 .. f0+15, f0 = nt*128 + c*16
                     uint32_t packed[8];
 #pragma unroll
                     for (int i2 = 0; i2 < 8; ++i2) {
+                        // columns: 16 gate rows then the 16 matching up rows of
+                        // features f0 .. f0+15, f0 = nt*128 + c*16
                         const float g0 = es * __uint_as_float(v[2 * i2]), g1 = es * __uint_as_float(v[2 * i2 + 1]);
                         const float u0 = es * __uint_as_float(v[16 + 2 * i2]);
                         const float u1 = es * __uint_as_float(v[16 + 2 * i2 + 1]);
@@ -405,17 +410,49 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) grouped_gemm_kernel(const __g
                         const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
                         packed[i2] = *reinterpret_cast<const uint32_t*>(&hb);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(p.hout + (size_t)row * p.F + ti.nt * (GN / 2) + c * 16);
-                    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    uint4* d = reinterpret_cast<uint4*>(eb + lane * EPI_ROW + (c & 3) * 32);
+                    d[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    d[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                 } else {
-                    float4* dst = reinterpret_cast<float4*>(p.fout + (size_t)row * p.ldo + ti.nt * GN + c * 32);
+                    float4* d = reinterpret_cast<float4*>(eb + lane * EPI_ROW);
 #pragma unroll
                     for (int i2 = 0; i2 < 8; ++i2)
-                        dst[i2] = make_float4(gate * __uint_as_float(v[4 * i2]), gate * __uint_as_float(v[4 * i2 + 1]),
-                                              gate * __uint_as_float(v[4 * i2 + 2]),
-                                              gate * __uint_as_float(v[4 * i2 + 3]));
+                        d[i2] = make_float4(gate * __uint_as_float(v[4 * i2]), gate * __uint_as_float(v[4 * i2 + 1]),
+                                            gate * __uint_as_float(v[4 * i2 + 2]),
+                                            gate * __uint_as_float(v[4 * i2 + 3]));
                 }
+            };
+            // the staged 32 rows x 128 bytes -> global, four whole lines per store
+            auto flush = [&](int c) {
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int rr = j * 4 + rsub;
+                    const int grow = wrow0 + rr;
+                    const uint4 v4 = *reinterpret_cast<const uint4*>(eb + rr * EPI_ROW + cq);
+                    if (q * 32 + rr < ti.rows) {
+                        unsigned char* g =
+                            p.mode == 0
+                                ? reinterpret_cast<unsigned char*>(p.hout + (size_t)grow * p.F + ti.nt * (GN / 2) +
+                                                                   (c >> 2) * 64)
+                                : reinterpret_cast<unsigned char*>(p.fout + (size_t)grow * p.ldo + ti.nt * GN + c * 32);
+                        *reinterpret_cast<uint4*>(g + cq) = v4;
+                    }
+                }
+                __syncwarp();
+            };
+            uint32_t va[32], vb[32];
+            tc::tmem_ld32(base, va);
+#pragma unroll 1
+            for (int c = 0; c < GN / 32; c += 2) {
+                tc::tmem_wait_ld(va);
+                tc::tmem_ld32(base + (uint32_t)((c + 1) * 32), vb);
+                stage(va, c);
+                if (p.mode == 1) flush(c);
+                tc::tmem_wait_ld(vb);
+                if (c + 2 < GN / 32) tc::tmem_ld32(base + (uint32_t)((c + 2) * 32), va);
+                stage(vb, c + 1);
+                if (p.mode == 1 || ((c + 1) & 3) == 3) flush(c + 1);
             }
             tc::fence_before_sync();
             __syncwarp();
