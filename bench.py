@@ -178,17 +178,17 @@ class RawGraph:
 
 # ------------------------------------------------------------- host pool
 
-def host_pool(shape: synth.Shape, seed: int, world: int, rank: int):
-    """Page-locked host pool with every record.  One process: a pinned torch
-    tensor.  N replicas on one node: rank 0 writes the pool once into a shared
-    file (FT_POOL_DIR, default /dev/shm) and every rank maps and registers it,
-    so the node holds one copy."""
-    import torch
+def whole_job_rate(units_per_rank: float, seconds_per_rank: float, world: int, device=None) -> float:
+    """Whole-job throughput of N replicas: the units all ranks processed over
+    the slowest rank's time (max over ranks)."""
+    return world * units_per_rank / max_over_ranks(seconds_per_rank, world, device)
+
+
+def shared_pool_file(shape: synth.Shape, seed: int, world: int, rank: int) -> tuple:
+    """The host pool of N replicas on one node as one shared file
+    (FT_POOL_DIR, default /dev/shm): rank 0 writes every record once, the
+    others wait at a barrier and map it.  Returns (memmap, path)."""
     nbytes = shape.L * shape.E * shape.record_bytes
-    if world == 1:
-        pool = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-        synth.fill_host_pool(pool.numpy(), shape, seed)
-        return pool, None
     path = os.path.join(os.environ.get("FT_POOL_DIR", "/dev/shm"), f"ft_pool_{shape.L}x{shape.E}_{seed}.bin")
     if rank == 0:
         mm = np.memmap(path, dtype=np.uint8, mode="w+", shape=(nbytes,))
@@ -196,7 +196,20 @@ def host_pool(shape: synth.Shape, seed: int, world: int, rank: int):
         mm.flush()
         del mm
     barrier(world)
-    mm = np.memmap(path, dtype=np.uint8, mode="r+", shape=(nbytes,))
+    return np.memmap(path, dtype=np.uint8, mode="r+", shape=(nbytes,)), path
+
+
+def host_pool(shape: synth.Shape, seed: int, world: int, rank: int):
+    """Page-locked host pool with every record.  One process: a pinned torch
+    tensor.  N replicas on one node: the shared file of `shared_pool_file`,
+    registered page-locked by every rank, so the node holds one copy."""
+    import torch
+    nbytes = shape.L * shape.E * shape.record_bytes
+    if world == 1:
+        pool = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        synth.fill_host_pool(pool.numpy(), shape, seed)
+        return pool, None
+    mm, path = shared_pool_file(shape, seed, world, rank)
     t = torch.from_numpy(mm)
     rc = torch.cuda.cudart().cudaHostRegister(t.data_ptr(), nbytes, 0)
     if int(rc) != 0:
@@ -377,7 +390,7 @@ def run_ours(args, rank, world, local_rank):
                        "unit": "GB/s", "frac": ex.get("hbm", {}).get("frac"), "peak_source": peaks["source"],
                        "note": "HBM side of the fused kernel; its time also covers the fill over the host link"}
 
-    value = world * T * K / (t_max_ms * 1e-3)
+    value = whole_job_rate(T * K, t_ms * 1e-3, world, device)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(t_max_ms / K, 4), "higher_is_better": True, "scaling": "weak",
@@ -674,6 +687,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prefill measurement and print its object (no bench line)")
     ap.add_argument("--ncu-case", type=int, default=None, metavar="Q",
                     help="run the small single-layer profiling case with Q fills per call (0..8) and exit")
     args = ap.parse_args()
@@ -681,6 +696,13 @@ def main():
         if not 0 <= args.ncu_case <= 8:
             raise SystemExit("--ncu-case takes 0..8")
         run_ncu_case(args)
+        return
+    if args.prefill_only:
+        import torch
+        torch.cuda.set_device(0)
+        import moe_expert_cache_gb300 as ft
+        ft.load()
+        print(json.dumps({"prefill": run_prefill_bench(torch.device("cuda", 0), read_peaks())}), flush=True)
         return
     rank, world, local_rank = dist_env()
     if args.warmup < 3:
