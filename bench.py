@@ -319,6 +319,8 @@ def run_ours(args, rank, world, local_rank):
     c1 = ctx.counters()
     assert ctx.status() == ft.FT_OK
     dcnt = {k_: c1[k_] - c0[k_] for k_ in c1}
+    # B_P as the library measures it (its own fill path, 16 records, best of 3)
+    link_fill_gbps = ctx.measure_link(16, 3)
     ctx.close()
     t_max_ms = max_over_ranks(t_ms, world, device)
 
@@ -406,6 +408,8 @@ def run_ours(args, rank, world, local_rank):
         "cpu_set_per_layer_step": round(dcnt["cpu"] / max(1, dcnt["calls"]), 4),
         "roofline": roofline,
         "roofline_expert_kernels": expert_roofline,
+        "link_GBps": {"pinned_memcpy": round(h2d_peak, 1) if h2d_peak else None,
+                      "fill_path_B_P": round(link_fill_gbps, 1)},
         "kernels": kernels,
         "gpu_launches": int(2 * dcnt["calls"]),
         "kernel_timing": f"library CUDA-event records around each launch of 1 timed step in {PROFILE_EVERY}",

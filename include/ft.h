@@ -240,6 +240,23 @@ ft_status ft_prefill_layer(ft_ctx* ctx, int32_t buffer, int32_t layer, int32_t n
 ft_status ft_cache_resize(ft_ctx* ctx, int32_t S_new);
 
 /*
+ * ft_measure_link -- measure B_P, the record-copy bandwidth over the host
+ * link, with the library's own fill path; syncs.
+ * FreeToken explainer section 5 "Deriving q*": B_P is the measured transfer
+ * bandwidth of expert records; the txtmix write-up describes a one-off
+ * on-machine measurement of it ("ft bench bw") whose result drives q.
+ * Copies n_records complete records of the host pool (flat ids spread evenly
+ * over the pool) into a temporary device buffer with the fill kernel, reps
+ * times, and stores the best repetition's rate in *gbps (1e9 bytes per
+ * second).  The cache, its state and the statistics are not touched; a
+ * pending fill is performed first.  The temporary buffer (n_records *
+ * ft_record_bytes bytes) is allocated and freed inside the call.
+ * Errors: FT_ERR_ARG (n_records < 1 or > L*E, reps < 1 or > 1000, gbps
+ * NULL), FT_ERR_STATE (prefill chunk open), FT_ERR_OOM, FT_ERR_CUDA.
+ */
+ft_status ft_measure_link(ft_ctx* ctx, int32_t n_records, int32_t reps, double* gbps);
+
+/*
  * ft_expert_ffn_noalloc -- the decode expert FFN without a context and
  * without allocating anything.  The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory once they

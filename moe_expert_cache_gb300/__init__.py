@@ -61,6 +61,7 @@ _SIGS = {
     "ft_prefill_begin": (_c_int, [_c_p, _c_int]),
     "ft_prefill_layer": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p]),
     "ft_cache_resize": (_c_int, [_c_p, _c_int]),
+    "ft_measure_link": (_c_int, [_c_p, _c_int, _c_int, ctypes.POINTER(ctypes.c_double)]),
     "ft_get_ctl_state": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p]),
     "ft_set_ctl_state": (_c_int, [_c_p, _c_p, _c_p, _c_p, ctypes.c_uint32]),
     "ft_get_last_ctl": (_c_int, [_c_p, ctypes.POINTER(CtlInfo), _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
@@ -146,6 +147,10 @@ def prefill_layer(ctx, buffer, layer, next_layer, T, x, logits, y) -> int:
 
 def cache_resize(ctx, S_new) -> int:
     return load().ft_cache_resize(ctx, S_new)
+
+
+def measure_link(ctx, n_records, reps, gbps) -> int:
+    return load().ft_measure_link(ctx, n_records, reps, gbps)
 
 
 def get_ctl_state(ctx, slot_for_id, id_for_slot, stamps, clock) -> int:
@@ -260,6 +265,12 @@ class Context:
 
     def cache_resize(self, S_new):
         _check(cache_resize(self.h, S_new), "ft_cache_resize")
+
+    def measure_link(self, n_records, reps=3):
+        """B_P: record-copy GB/s over the host link, measured with the fill path."""
+        g = ctypes.c_double(0.0)
+        _check(measure_link(self.h, n_records, reps, ctypes.byref(g)), "ft_measure_link")
+        return g.value
 
     def ctl_state(self):
         import numpy as np

@@ -682,4 +682,56 @@ ft_status ft_prefill_layer(ft_ctx* c, int32_t buffer, int32_t layer, int32_t nex
     return FT_OK;
 }
 
+
+ft_status ft_measure_link(ft_ctx* c, int32_t n_records, int32_t reps, double* gbps) {
+    if (!c || !gbps || n_records < 1 || (long long)n_records > (long long)c->L * c->E || reps < 1 || reps > 1000)
+        return FT_ERR_ARG;
+    if (c->pf.open) return FT_ERR_STATE;
+    FT_CUDA(flush_fill(c));
+    FT_CUDA(cudaStreamSynchronize(c->cs));
+    const size_t rec = c->rb, lists = ((size_t)(INFO_WORDS + 2 * n_records) * 4 + 255) & ~(size_t)255;
+    unsigned char* buf = nullptr;
+    if (cudaMalloc(&buf, lists + (size_t)n_records * rec) != cudaSuccess) {
+        cudaGetLastError();
+        return FT_ERR_OOM;
+    }
+    std::vector<int> h(INFO_WORDS + 2 * (size_t)n_records, 0);
+    h[INFO_Q] = n_records;
+    const long long nid = (long long)c->L * c->E;
+    for (int i = 0; i < n_records; ++i) {
+        h[INFO_WORDS + i] = i;                                                // destination record i
+        h[INFO_WORDS + n_records + i] = (int)((long long)i * nid / n_records);  // flat id, spread over the pool
+    }
+    ft_status st = FT_OK;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    float best = -1.f;
+    if (cudaMemcpy(buf, h.data(), h.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        st = FT_ERR_CUDA;
+    } else {
+        FillParams fp{};
+        fp.host_pool = (const uint4*)c->host_pool_dev;
+        fp.slot_pool = (uint4*)(buf + lists);
+        fp.rec16 = rec / 16;
+        fp.info = reinterpret_cast<const int*>(buf);
+        fp.fill_slot = reinterpret_cast<const int*>(buf) + INFO_WORDS;
+        fp.fill_fid = reinterpret_cast<const int*>(buf) + INFO_WORDS + n_records;
+        for (int r = 0; r < reps && st == FT_OK; ++r) {
+            float ms = 0.f;
+            if (cudaEventRecord(e0, c->cs) != cudaSuccess || launch_fill(fp, 2 * c->num_sms, c->cs) != cudaSuccess ||
+                cudaEventRecord(e1, c->cs) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+                st = FT_ERR_CUDA;
+            else if (best < 0.f || ms < best)
+                best = ms;
+        }
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(buf);
+    if (st != FT_OK) return st;
+    *gbps = best > 0.f ? (double)n_records * (double)rec / (best * 1e-3) / 1e9 : 0.0;
+    return FT_OK;
+}
+
 }  // extern "C"

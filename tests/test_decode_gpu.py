@@ -198,3 +198,31 @@ def test_decode_t16_with_resize(ft, big_pool):
     samples = {(s, l) for s in (0, 31, 32, 63, 64, 127) for l in (0, 47)}
     checked, cnt = _replay(ft, big_pool, wl, samples, resize=synth.DECODE_T16_RESIZE)
     assert len(checked) == len(samples)
+
+
+def test_measure_link_leaves_the_cache_untouched(ft):
+    """B_P measured with the fill path (explainer section 5; the txtmix
+    write-up's one-off bandwidth measurement): a positive rate, and the cache
+    state and statistics are unchanged by the call."""
+    import torch
+    sh = synth.Shape(L=2, E=8, k=2, H=256, F=128)
+    pool, _ = hz.pinned_pool(sh, 0)
+    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, 8, pool, T_max=4)
+    routes = np.array([[1, 2], [3, 4], [1, 5], [6, 2]], dtype=np.int32)
+    ctx.route_ctl(0, 4, topk_ids=_dev(routes), topk_w=_dev(np.full(routes.shape, 0.5, np.float32)),
+                  B_P=1.0, B_H=1.0)
+    x = torch.zeros(4, sh.H, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(4, sh.H, device="cuda")
+    ctx.moe_forward(x, None, y)
+    before, cnt = ctx.ctl_state(), ctx.counters()
+    gbps = ctx.measure_link(16, 2)
+    assert gbps > 1.0
+    after = ctx.ctl_state()
+    assert all(np.array_equal(a, b) for a, b in zip(before[:3], after[:3])) and before[3] == after[3]
+    assert ctx.counters() == cnt
+    with pytest.raises(ft.FtError):
+        ctx.measure_link(0, 1)
+    with pytest.raises(ft.FtError):
+        ctx.measure_link(sh.L * sh.E + 1, 1)
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
