@@ -30,28 +30,40 @@ constexpr int FPC = CW;               // features per phase-A chunk
 constexpr size_t HEAD = 256;
 enum { X_F32_SMEM = 0, X_BF16_SMEM = 1, X_BF16_GLOBAL = 2 };
 
-struct Luts {
-    float2 pair[256];   // byte -> (e2m1 of low nibble, e2m1 of high nibble)
-    float e4m3[256];    // scale byte -> value
-};
+// e2m1 decode by bit placement: code j of word w (nibble j, low nibble
+// first) becomes the fp32 whose exponent field holds the code's two exponent
+// bits, whose top mantissa bit holds its mantissa bit and whose sign is its
+// sign.  That float equals value * 2^-126 exactly, for the subnormal code 1
+// (0.5) as well; activations are held scaled by 2^64 (kActScale) so the
+// products stay normal, and the row sums are rescaled by 2^62 (kSumScale).
+// Four integer operations per value instead of a table lookup or a
+// conversion instruction.
+constexpr float kActScale = 18446744073709551616.0f;  // 2^64
+constexpr float kSumScale = 4611686018427387904.0f;   // 2^62
 
-__device__ __forceinline__ float e2m1_value(int c) {
-    const int m = c & 7;
-    const float mag = m < 2 ? 0.5f * (float)m : (1.f + 0.5f * (float)(m & 1)) * (float)(1 << ((m >> 1) - 1));
-    return (c & 8) ? -mag : mag;
+template <int J>
+__device__ __forceinline__ float e2m1_scaled(uint32_t w) {
+    const uint32_t mag = (J * 4 <= 22 ? (w << (J * 4 <= 22 ? 22 - 4 * J : 0)) : (w >> (J * 4 > 22 ? 4 * J - 22 : 0))) &
+                         0x01C00000u;
+    const uint32_t sgn = (w << (28 - 4 * J)) & 0x80000000u;
+    return __uint_as_float(mag | sgn);
 }
 
-__device__ __forceinline__ float e4m3_value(int c) {
-    const int e = (c >> 3) & 15, m = c & 7;
-    float v = e == 0 ? ldexpf((float)m / 8.f, -6) : ldexpf(1.f + (float)m / 8.f, e - 7);
-    return (c & 0x80) ? -v : v;
+// Scale bytes: two e4m3 codes (low byte first) to a float pair, by the
+// hardware conversion (one per 16 values).
+__device__ __forceinline__ float2 e4m3x2_f32(const uint8_t* p2) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(*reinterpret_cast<const unsigned short*>(p2)));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-__device__ __forceinline__ void init_luts(Luts* L, int tid, int nthreads) {
-    for (int i = tid; i < 256; i += nthreads) {
-        L->pair[i] = make_float2(e2m1_value(i & 15), e2m1_value(i >> 4));
-        L->e4m3[i] = e4m3_value(i);
-    }
+// Activation rows in shared memory (x and the staged h rows) are swizzled so
+// that a warp's loads of its lanes' 32-value groups spread over all banks:
+// within group v (128 bytes of fp32, or 64 bytes of bf16), 16-byte chunk i
+// is stored at chunk (i + v) mod 8 (fp32) or (i + v) mod 4 (bf16).
+__device__ __forceinline__ int swz_f32(int e) {  // element e of a row -> its stored position
+    const int v = e >> 5, i = (e >> 2) & 7;
+    return (v << 5) | (((i + v) & 7) << 2) | (e & 3);
 }
 
 // 32 activations of token row `xr` starting at element 32*v.
@@ -61,42 +73,42 @@ __device__ __forceinline__ void load_x32(const void* xr, int v, float* x) {
         const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(xr) + (size_t)v * 32);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float4 q = p[i];
+            const float4 q = p[(i + v) & 7];
             x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
         }
     } else {
         const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xr) + (size_t)v * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint4 q = XM == X_BF16_GLOBAL ? __ldg(p + i) : p[i];
+            const uint4 q = XM == X_BF16_GLOBAL ? __ldg(p + i) : p[(i + v) & 3];
             ft::bf16x8_to_f32(q, x + 8 * i);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[8 * i + j] *= kActScale;
         }
     }
 }
 
-// sum over 32 values of one uint4 (two scale blocks): sc0 * block0 + sc1 * block1
-__device__ __forceinline__ float fp4_dot32(const uint4& w, const float* x, const float2* pair, float sc0, float sc1) {
-    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const float2 v = pair[(wd[q] >> (8 * b)) & 255u];
-            s0 = fmaf(v.x, x[8 * q + 2 * b], s0);
-            s0 = fmaf(v.y, x[8 * q + 2 * b + 1], s0);
-        }
-    }
-#pragma unroll
-    for (int q = 2; q < 4; ++q) {
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const float2 v = pair[(wd[q] >> (8 * b)) & 255u];
-            s1 = fmaf(v.x, x[8 * q + 2 * b], s1);
-            s1 = fmaf(v.y, x[8 * q + 2 * b + 1], s1);
-        }
-    }
-    return fmaf(sc0, s0, sc1 * s1);
+// eight values of one word against x[0..7] (scaled), added to a / b (even / odd)
+__device__ __forceinline__ void fp4_word(uint32_t w, const float* x, float& a, float& b) {
+    a = fmaf(e2m1_scaled<0>(w), x[0], a);
+    b = fmaf(e2m1_scaled<1>(w), x[1], b);
+    a = fmaf(e2m1_scaled<2>(w), x[2], a);
+    b = fmaf(e2m1_scaled<3>(w), x[3], b);
+    a = fmaf(e2m1_scaled<4>(w), x[4], a);
+    b = fmaf(e2m1_scaled<5>(w), x[5], b);
+    a = fmaf(e2m1_scaled<6>(w), x[6], a);
+    b = fmaf(e2m1_scaled<7>(w), x[7], b);
+}
+
+// sum over 32 values of one uint4 (two scale blocks): sc0 * block0 + sc1 * block1,
+// in units of 2^-62 (activations scaled by 2^64, values by 2^-126)
+__device__ __forceinline__ float fp4_dot32(const uint4& w, const float* x, float sc0, float sc1) {
+    float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+    fp4_word(w.x, x, a0, b0);
+    fp4_word(w.y, x + 8, a0, b0);
+    fp4_word(w.z, x + 16, a1, b1);
+    fp4_word(w.w, x + 24, a1, b1);
+    return fmaf(sc0, a0 + b0, sc1 * (a1 + b1));
 }
 
 // Phase A: gate and up rows of one feature against NT tokens; returns the
@@ -104,14 +116,14 @@ __device__ __forceinline__ float fp4_dot32(const uint4& w, const float* x, const
 template <int NT, int XM>
 __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                          const void* xs, size_t xrow_elems, const int* tk, int H, int lane,
-                                         const Luts* L, float* ag, float* au) {
+                                         float* ag, float* au) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
     const int nv = H >> 5;  // uint4 (32 values) per row
     for (int v = lane; v < nv; v += 32) {
         const uint4 wg = gv[v], wu = uv[v];
-        const float g0 = L->e4m3[gs[2 * v]], g1 = L->e4m3[gs[2 * v + 1]];
-        const float u0 = L->e4m3[us[2 * v]], u1 = L->e4m3[us[2 * v + 1]];
+        const float2 gsc2 = e4m3x2_f32(gs + 2 * v), usc2 = e4m3x2_f32(us + 2 * v);
+        const float g0 = gsc2.x, g1 = gsc2.y, u0 = usc2.x, u1 = usc2.y;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             float x[32];
@@ -119,8 +131,8 @@ __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const
                                  ? (const void*)(static_cast<const float*>(xs) + (size_t)tk[n] * xrow_elems)
                                  : (const void*)(static_cast<const __nv_bfloat16*>(xs) + (size_t)tk[n] * xrow_elems);
             load_x32<XM>(xr, v, x);
-            ag[n] += fp4_dot32(wg, x, L->pair, g0, g1);
-            au[n] += fp4_dot32(wu, x, L->pair, u0, u1);
+            ag[n] += fp4_dot32(wg, x, g0, g1);
+            au[n] += fp4_dot32(wu, x, u0, u1);
         }
     }
 }
@@ -128,37 +140,38 @@ __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const
 template <int NT, int XM>
 __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                           const void* xs, int H, const int* m_tok, int off, int g0, int F, int f,
-                                          int lane, const Luts* L, float gsc, float* hbuf) {
+                                          int lane, float gsc, float* hbuf) {
     int tk[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) tk[n] = m_tok[off + g0 + n];
     float ag[NT], au[NT];
-    gu_dots4<NT, XM>(gv, uv, gs, us, xs, (size_t)H, tk, H, lane, L, ag, au);
+    gu_dots4<NT, XM>(gv, uv, gs, us, xs, (size_t)H, tk, H, lane, ag, au);
     float mine = 0.f;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-        const float sg = ft::warp_sum(ag[n]) * gsc;
-        const float su = ft::warp_sum(au[n]) * gsc;
+        const float sg = ft::warp_sum(ag[n]) * kSumScale * gsc;
+        const float su = ft::warp_sum(au[n]) * kSumScale * gsc;
         if (lane == n) mine = ft::silu_mul(sg, su);
     }
-    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + f] = mine;
+    // read only by phase B, as staged rows: scaled and swizzled like x
+    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + swz_f32(f)] = mine * kActScale;
 }
 
 template <int XM>
 __device__ __forceinline__ void gu_feature4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                             const void* xs, int H, const int* m_tok, int off, int ntok, int F, int f,
-                                            int lane, const Luts* L, float gsc, float* hbuf) {
+                                            int lane, float gsc, float* hbuf) {
     int g0 = 0;
     while (g0 < ntok) {
         const int rem = ntok - g0;
         if (rem >= 4) {
-            gu_group4<4, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, L, gsc, hbuf);
+            gu_group4<4, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 4;
         } else if (rem >= 2) {
-            gu_group4<2, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, L, gsc, hbuf);
+            gu_group4<2, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 2;
         } else {
-            gu_group4<1, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, L, gsc, hbuf);
+            gu_group4<1, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 1;
         }
     }
@@ -167,7 +180,7 @@ __device__ __forceinline__ void gu_feature4(const uint4* gv, const uint4* uv, co
 // Phase B: one W_d row (values + scales) against NT staged h rows (fp32).
 template <int NT>
 __device__ __forceinline__ void down_group4(const uint4* wv, const uint8_t* ws, const float* hs, int g, int F,
-                                            int lane, const Luts* L, float gsc, float* o_s, int obase, int RMAX,
+                                            int lane, float gsc, float* o_s, int obase, int RMAX,
                                             int rl) {
     float acc[NT];
 #pragma unroll
@@ -175,35 +188,36 @@ __device__ __forceinline__ void down_group4(const uint4* wv, const uint8_t* ws, 
     const int nv = F >> 5;
     for (int v = lane; v < nv; v += 32) {
         const uint4 w = wv[v];
-        const float s0 = L->e4m3[ws[2 * v]], s1 = L->e4m3[ws[2 * v + 1]];
+        const float2 sc2 = e4m3x2_f32(ws + 2 * v);
+        const float s0 = sc2.x, s1 = sc2.y;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             float x[32];
             load_x32<X_F32_SMEM>(hs + (size_t)(g + n) * F, v, x);
-            acc[n] += fp4_dot32(w, x, L->pair, s0, s1);
+            acc[n] += fp4_dot32(w, x, s0, s1);
         }
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-        const float sv = ft::warp_sum(acc[n]) * gsc;
+        const float sv = ft::warp_sum(acc[n]) * kSumScale * gsc;
         if (lane == 0) o_s[(size_t)(obase + g + n) * RMAX + rl] = sv;
     }
 }
 
 __device__ __forceinline__ void down_row4(const uint4* wv, const uint8_t* ws, const float* hs, int ng, int F,
-                                          int lane, const Luts* L, float gsc, float* o_s, int obase, int RMAX,
+                                          int lane, float gsc, float* o_s, int obase, int RMAX,
                                           int rl) {
     int g = 0;
     while (g < ng) {
         const int rem = ng - g;
         if (rem >= 4) {
-            down_group4<4>(wv, ws, hs, g, F, lane, L, gsc, o_s, obase, RMAX, rl);
+            down_group4<4>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
             g += 4;
         } else if (rem >= 2) {
-            down_group4<2>(wv, ws, hs, g, F, lane, L, gsc, o_s, obase, RMAX, rl);
+            down_group4<2>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
             g += 2;
         } else {
-            down_group4<1>(wv, ws, hs, g, F, lane, L, gsc, o_s, obase, RMAX, rl);
+            down_group4<1>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
             g += 1;
         }
     }
@@ -217,7 +231,6 @@ template <int XM>
 __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_gdone;
-    __shared__ Luts L;
     const int H = p.H, F = p.F, T = p.T, k = p.k, TG = p.tgroup;
     const int nst = p.nstage;
     const unsigned slot_bytes = p.stage_bytes;
@@ -264,7 +277,6 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         ft::mbar_fence_init();
         s_gdone = 0;
     }
-    init_luts(&L, tid, THREADS);
     for (int i = tid; i <= ugpu; i += THREADS) m_off[i] = p.wl_off[i];
     for (int i = tid; i < ugpu; i += THREADS) {
         m_slot[i] = p.wl_slot[i];
@@ -280,12 +292,19 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         for (int i = tid; i < T * H / 8; i += THREADS) {
             float f8[8];
             ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
-            reinterpret_cast<float4*>(x_s)[2 * i] = make_float4(f8[0], f8[1], f8[2], f8[3]);
-            reinterpret_cast<float4*>(x_s)[2 * i + 1] = make_float4(f8[4], f8[5], f8[6], f8[7]);
+            for (int j = 0; j < 8; ++j) f8[j] *= kActScale;
+            const int t = (8 * i) / H, e = 8 * i - t * H;  // 8 values from element e of token t
+            float* row = static_cast<float*>(x_s) + (size_t)t * H;
+            *reinterpret_cast<float4*>(row + swz_f32(e)) = make_float4(f8[0], f8[1], f8[2], f8[3]);
+            *reinterpret_cast<float4*>(row + swz_f32(e + 4)) = make_float4(f8[4], f8[5], f8[6], f8[7]);
         }
     } else if (XM == X_BF16_SMEM) {
-        for (int i = tid; i < T * H / 8; i += THREADS)
-            reinterpret_cast<uint4*>(x_s)[i] = reinterpret_cast<const uint4*>(p.x)[i];
+        for (int i = tid; i < T * H / 8; i += THREADS) {
+            const int t = (8 * i) / H, e = 8 * i - t * H;  // 8 values from element e of token t
+            const int v = e >> 5, c = (e >> 3) & 3;
+            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(x_s) + (size_t)t * H + 32 * v)[(c + v) & 3] =
+                reinterpret_cast<const uint4*>(p.x)[i];
+        }
     }
     __syncthreads();
 
@@ -400,7 +419,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         const uint4* uv = reinterpret_cast<const uint4*>(sb + (size_t)(FPC + wid) * vrow);
         const uint8_t* gs = sb + 2 * FPC * vrow + (size_t)wid * srow;
         const uint8_t* us = sb + 2 * FPC * vrow + FPC * srow + (size_t)wid * srow;
-        if (ok) gu_feature4<XM>(gv, uv, gs, us, xsrc, H, m_tok, off, ntok, F, f, lane, &L, m_gs[ent], p.hbuf);
+        if (ok) gu_feature4<XM>(gv, uv, gs, us, xsrc, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf);
         __syncwarp();
         if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
     }
@@ -425,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 const float* hs = reinterpret_cast<const float*>(sb + wpart);
                 for (int rl = wid; rl < R && ok; rl += CW)
                     down_row4(reinterpret_cast<const uint4*>(sb + (size_t)rl * dvrow),
-                              sb + (size_t)RMAX * dvrow + (size_t)rl * dsrow, hs, ng, F, lane, &L, m_gs[e], o_s,
+                              sb + (size_t)RMAX * dvrow + (size_t)rl * dsrow, hs, ng, F, lane, m_gs[e], o_s,
                               off + g0, RMAX, rl);
                 __syncwarp();
                 if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
@@ -448,7 +467,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
 
 }  // namespace
 
-static constexpr size_t kSmemLimit4 = 227 * 1024 - sizeof(Luts) - 64;
+static constexpr size_t kSmemLimit4 = 227 * 1024 - 256;  // dynamic; the rest is static shared memory
 
 cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
     const int G = num_sms;
@@ -478,28 +497,29 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
     size_t slot = wpart + (size_t)tg * p.F * 4;
     if (slot < chunk) slot = chunk;
     slot = (slot + 127) & ~(size_t)127;
-    size_t fch = 16384;
-    int nst = 0;
-    for (; fch >= 4096; fch /= 2) {
-        if (head + 2 * fch >= kSmemLimit4) continue;
-        nst = (int)((kSmemLimit4 - head - 2 * fch) / slot);
-        if (nst >= 2) break;
-    }
+    // The fill ring is kept small (3 x 4 KiB per SM): host reads queued beyond
+    // the link's bandwidth-delay product delay every SM's HBM reads.
+    const size_t fch = 4096;
+    if (head + 2 * fch + 2 * slot > kSmemLimit4) return cudaErrorInvalidValue;
+    int nst = (int)((kSmemLimit4 - head - 2 * fch) / slot);
     if (nst > 4) nst = 4;
-    if (nst < 2) return cudaErrorInvalidValue;
     p.nstage = nst;
     p.stage_bytes = (unsigned)slot;
     p.tgroup = tg;
     int nf = (int)((kSmemLimit4 - head - slot * nst) / fch);
-    if (nf > 4) nf = 4;
+    if (nf > 3) nf = 3;
     p.fill_chunk = (unsigned)fch;
     p.fill_slots = nf;
     const size_t smem = head + slot * nst + (size_t)nf * fch;
     const void* fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM>
                      : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM>
                                          : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    static size_t smem_set[3] = {0, 0, 0};  // per kernel variant: set only when it grows
+    if (smem > smem_set[xm]) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set[xm] = smem;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(THREADS);
