@@ -419,6 +419,8 @@ def run_ours(args, rank, world, local_rank):
         "setup_s": {"host_pool": round(t_pool, 1), "graph_capture": round(t_capture, 1)},
         "execution": "the K timed steps run as one CUDA graph (captured from the library calls, uploaded before timing)",
     }
+    if rank == 0 and not args.no_t16:
+        out["decode_t16"] = run_decode_t16_bench(pool, device)
     if not args.no_prefill:
         out["prefill"] = run_prefill_bench(device, peaks)
     if rank == 0 and not args.no_cpu_baseline:
@@ -429,6 +431,57 @@ def run_ours(args, rank, world, local_rank):
     if shared is not None:
         torch.cuda.cudart().cudaHostUnregister(pool.data_ptr())
     return out
+
+
+def run_decode_t16_bench(pool, device) -> dict:
+    """Decode T=16 with resize (same layer shapes and host pool as decode T=1):
+    48 layers, 768 slots shrunk to 384 before step 32 and grown back before
+    step 64, 128 steps from an empty cache, AR(1) rho=0.7, B_P=25, B_H=90.
+    Steps run eagerly (the resizes are host safe points); tokens/s is over the
+    steps' CUDA-event time, resize latency is each call's host time."""
+    import torch
+    import moe_expert_cache_gb300 as ft
+    wl = synth.DECODE_T16
+    sh = wl.shape
+    T, L, E, H = wl.T, sh.L, sh.E, sh.H
+    logits = torch.from_numpy(synth.ar1_logits(wl.seed, wl.steps, L, T, E, wl.rho, wl.sigma)).to(device)
+    xs = torch.from_numpy(np.stack([synth.tokens_bf16(wl.seed, 0, l, T, H) for l in range(L)]).view(np.int16)).to(
+        device).view(torch.bfloat16)
+    pc = torch.zeros(T, H, device=device)
+    y = torch.empty(T, H, device=device)
+    cs = torch.cuda.Stream(device)
+    ctx = ft.Context(L, E, sh.k, H, sh.F, wl.S, pool, T_max=T, compute_stream=cs.cuda_stream)
+    resize_at = dict(synth.DECODE_T16_RESIZE)
+    ms, resize_ms = 0.0, {}
+    c0 = ctx.counters()
+    for s0, s1 in ((0, 32), (32, 64), (64, wl.steps)):
+        if s0 in resize_at:
+            t0 = time.perf_counter()
+            ctx.cache_resize(resize_at[s0])
+            resize_ms[f"to_{resize_at[s0]}_before_step_{s0}"] = round((time.perf_counter() - t0) * 1e3, 2)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):
+            e0.record(cs)
+            for st in range(s0, s1):
+                for l in range(L):
+                    ctx.route_ctl(l, T, logits=logits[st, l], B_P=wl.B_P, B_H=wl.B_H)
+                    ctx.moe_forward(xs[l], pc, y)
+            e1.record(cs)
+        torch.cuda.synchronize(device)
+        ms += e0.elapsed_time(e1)
+    c1 = ctx.counters()
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
+    d = {k_: c1[k_] - c0[k_] for k_ in c1}
+    calls = max(1, d["calls"])
+    return {"workload": "decode T=16: 48 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, 768 slots "
+                        "(384 during steps 32-63), AR(1) rho=0.7, B_P=25, B_H=90, 128 steps from an empty cache",
+            "tokens_per_s": round(T * wl.steps / (ms * 1e-3), 1), "ms_per_step": round(ms / wl.steps, 3),
+            "resize_ms": resize_ms, "execution": "eager library calls, CUDA-event time of the steps",
+            "hit_rate": round(d["hits"] / max(1, d["unique"]), 4),
+            "fills_per_layer_step": round(d["fills"] / calls, 3),
+            "gpu_experts_per_layer_step": round((d["hits"] + d["fills"]) / calls, 2),
+            "link_floor_ms_per_step": round(d["fills"] / wl.steps * sh.record_bytes / 211e9 * 1e3, 3)}
 
 
 def run_prefill_bench(device, peaks, reps: int = 3) -> dict:
@@ -690,6 +743,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
+    ap.add_argument("--no-t16", action="store_true", help="skip the decode T=16 (resize) measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill measurement and print its object (no bench line)")

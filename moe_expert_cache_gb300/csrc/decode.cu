@@ -71,6 +71,14 @@ __global__ void __launch_bounds__(512) fill_kernel(FillParams p) {
 
 // ------------------------------------------------------------- expert FFN
 
+// fp32 activation rows in shared memory (x, and the h rows staged for phase
+// B) swap the two 16-byte halves of every 32-byte group g with bit 2 of g set,
+// so that a warp's lanes, which read consecutive groups, spread their 16-byte
+// loads over all banks (no 2-way conflict).
+__device__ __forceinline__ int swz8(int e) {  // element e of a row -> its stored position
+    return e ^ (((e >> 5) & 1) << 2);
+}
+
 // ---- phase A inner loop: gate and up dot products of one feature over the
 // K columns [k0, k0 + K) held in shared memory, for NT tokens.  x is read from
 // shared memory as fp32 (XF) or bf16, row stride ldx.
@@ -93,7 +101,8 @@ __device__ __forceinline__ void gu_dots(const uint4* __restrict__ wg, const uint
             const size_t xo = (size_t)tk[n] * ldx + k0;
             if (XF) {
                 const float4* xp = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xs) + xo + v * 8);
-                const float4 x0 = xp[0], x1 = xp[1];
+                const int sw = ((k0 >> 3) + v) >> 2 & 1;  // halves swapped (swz8)
+                const float4 x0 = xp[sw], x1 = xp[sw ^ 1];
                 x8[0] = x0.x; x8[1] = x0.y; x8[2] = x0.z; x8[3] = x0.w;
                 x8[4] = x1.x; x8[5] = x1.y; x8[6] = x1.z; x8[7] = x1.w;
             } else {
@@ -147,7 +156,7 @@ __device__ __forceinline__ void gu_group(const uint4* wg, const uint4* wu, const
                 return;
             }
         }
-        hbuf[(size_t)(off + g0 + lane) * F + f] = ft::silu_mul(mg, mu);
+        hbuf[(size_t)(off + g0 + lane) * F + swz8(f)] = ft::silu_mul(mg, mu);
     }
 }
 
@@ -191,7 +200,8 @@ __device__ __forceinline__ void down_group(uint32_t wbase, uint32_t hs, int g0, 
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             const uint32_t hp = hs + ((uint32_t)(g0 + n) * F + v * 8) * 4u;
-            const float4 x0 = ft::lds128f(hp), x1 = ft::lds128f(hp + 16);
+            const uint32_t sw = (uint32_t)(v >> 2 & 1) * 16u;  // halves swapped (swz8)
+            const float4 x0 = ft::lds128f(hp + sw), x1 = ft::lds128f(hp + (16u - sw));
             hv[n][0] = x0.x; hv[n][1] = x0.y; hv[n][2] = x0.z; hv[n][3] = x0.w;
             hv[n][4] = x1.x; hv[n][5] = x1.y; hv[n][6] = x1.z; hv[n][7] = x1.w;
         }
@@ -384,8 +394,9 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             for (int i = st0; i < T * H / 8; i += NS) {
                 float f8[8];
                 ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
-                reinterpret_cast<float4*>(x_s)[2 * i] = make_float4(f8[0], f8[1], f8[2], f8[3]);
-                reinterpret_cast<float4*>(x_s)[2 * i + 1] = make_float4(f8[4], f8[5], f8[6], f8[7]);
+                const int sw = (i >> 2) & 1;  // halves swapped (swz8); rows start at multiples of 8 groups
+                reinterpret_cast<float4*>(x_s)[2 * i + sw] = make_float4(f8[0], f8[1], f8[2], f8[3]);
+                reinterpret_cast<float4*>(x_s)[2 * i + (sw ^ 1)] = make_float4(f8[4], f8[5], f8[6], f8[7]);
             }
         } else {
             for (int i = st0; i < (int)(xbytes / 16); i += NS)
