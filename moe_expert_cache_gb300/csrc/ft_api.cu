@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <cmath>
 #include <vector>
 
 // Per-kernel event records of the optional profile.
@@ -300,6 +301,19 @@ ft_status ft_route_ctl(ft_ctx* c, int32_t layer, int32_t T, const float* logits,
     p.layer = layer; p.T = T; p.E = c->E; p.k = c->k; p.L = c->L; p.S = c->S;
     p.logits = logits; p.topk_ids = topk_ids; p.topk_w = topk_w;
     p.B_P = B_P; p.B_H = B_H;
+    // q0 per miss count, evaluated here with the same fp64 expression the
+    // device uses (a product, then a quotient, both rounded to nearest, then
+    // round half away from zero): the kernel indexes it instead of running a
+    // slow fp64 divide on the critical path
+    p.q0_n = 0;
+    if (c->E < (int)(sizeof(p.q0tab) / sizeof(p.q0tab[0]))) {
+        for (int m = 0; m <= c->E; ++m) {
+            const double x = ((double)m * B_P) / B_H;
+            const double r = std::round(x);
+            p.q0tab[m] = r > 1.0e9 ? 1000000000 : (int)r;
+        }
+        p.q0_n = c->E + 1;
+    }
     p.slot_for_id = c->slot_for_id; p.id_for_slot = c->id_for_slot; p.stamps = c->stamps; p.clock = c->clock;
     p.out_ids = c->ids; p.out_gates = c->gates; p.out_slots = c->slots_topk; p.out_pos = c->pos;
     p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.wl_fid = c->wl_fid; p.wl_fill = c->wl_fill; p.ready = c->ready;

@@ -362,6 +362,8 @@ struct CtlParams {
     const int* topk_ids;      // [T,k] or null
     const float* topk_w;      // [T,k] or null
     double B_P, B_H;
+    int q0_n;                 // q0tab holds q0 for m < q0_n (0: compute on the device)
+    int q0tab[257];           // q0 = round((m * B_P) / B_H) in fp64, per miss count m
     int* slot_for_id;         // [L*E]
     int* id_for_slot;         // [S]
     unsigned* stamps;         // [S]

@@ -279,9 +279,13 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         const int m = sh.m, h = sh.h;
         int q0 = 0, q1 = 0, q = 0;
         if (m > 0) {
-            const double x = __ddiv_rn(__dmul_rn((double)m, p.B_P), p.B_H);
-            const double r = round(x);  // halves away from zero
-            q0 = r > 1.0e9 ? 1000000000 : (int)r;
+            if (m < p.q0_n) {
+                q0 = p.q0tab[m];  // the same fp64 expression, evaluated on the host per m
+            } else {
+                const double x = __ddiv_rn(__dmul_rn((double)m, p.B_P), p.B_H);
+                const double r = round(x);  // halves away from zero
+                q0 = r > 1.0e9 ? 1000000000 : (int)r;
+            }
             q1 = min(max(q0, 1), m);
             q = max(min(q1, S - h), 0);
         }
