@@ -13,21 +13,25 @@
 // the routes that run on the GPU, plus the supplied partial sum of the CPU set.
 // Decode is bandwidth-bound (about one flop per weight byte at T = 1), so the
 // layer is one persistent, cooperatively launched streaming kernel with one
-// CTA per SM:
+// CTA per SM, and the fills the control pass left pending are performed by
+// the same launch, overlapped with the resident experts' work:
 //   * a producer warp streams weights into a ring of shared-memory slots with
 //     1-D bulk (TMA) copies completing on mbarriers;
-//   * phase A (gate/up + SwiGLU): the work is the flat list of (GPU expert,
-//     group of 8 features), hits first, then the fills in fill order; CTA c
-//     takes items c, c + G, ...; one slot holds
-//     8 gate rows and the 8 matching up rows (contiguous in the record thanks
-//     to the 16-row gate/up interleave); consumer warp w computes feature w of
-//     the slot alone (both dot products, SiLU, product) and writes h in fp32;
-//   * a grid barrier makes every h visible; the producer does not wait for it
-//     and keeps streaming the W_d rows of phase B meanwhile;
+//   * phase A of the resident entries (gate/up + SwiGLU): items of (entry,
+//     8 features); CTA c takes items c, c + G, ...; one slot holds 8 gate rows
+//     and the 8 matching up rows (contiguous in the record thanks to the
+//     16-row gate/up interleave); consumer warp w computes feature w of the
+//     slot (both dot products, SiLU, product) and writes h in fp32;
+//   * the fill copy warp copies this CTA's share of every fill record (its
+//     own W_d rows, then its gate/up units) host pool -> small shared ring ->
+//     victim slot, and the fill math warp computes the SwiGLU features of the
+//     units straight from the ring, so a fill is never read back from HBM;
 //   * phase B (down + merge): CTA c owns output rows [c*H/G, (c+1)*H/G) of
-//     every GPU expert; then it sums the gated expert outputs over j ascending
-//     and adds partial_C, so the order of the sum is fixed and no atomics are
-//     needed.
+//     every GPU expert, in stages of whole entries whose h rows the h warp
+//     adds once they are complete (resident entries: every CTA has counted
+//     its phase-A items; fills: the math warps have counted every feature);
+//     then it sums the gated expert outputs over j ascending and adds
+//     partial_C, so the order of the sum is fixed and no atomics are needed.
 #include "ft_common.cuh"
 
 namespace {

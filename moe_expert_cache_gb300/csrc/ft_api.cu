@@ -343,7 +343,6 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.wl_fid = c->wl_fid; p.gscale = c->nvfp4_global;
     p.do_fill = c->fill_pending ? 1 : 0;
     p.host_pool = (const uint4*)c->host_pool_dev;
-    p.rec16 = c->rb / 16;
     p.fill_slot = c->fill_slot;
     p.fill_fid = c->fill_fid;
     p.wl_fill = c->wl_fill;

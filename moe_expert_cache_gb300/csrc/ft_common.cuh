@@ -224,36 +224,6 @@ __device__ __forceinline__ int ld_acquire_cta(const int* p) {
     return v;
 }
 
-// Fused cache fill: CTA c of G copies part c of every fill record (16-byte
-// vectors, 8 loads in flight per thread) from the host pool into its victim
-// slot, then counts itself in ready[i] with release semantics.  Run by the
-// `nthreads` fill threads of the CTA, which synchronise on named barrier
-// `bar_id`.
-__device__ __forceinline__ void fill_share(const uint4* host, uint4* pool, unsigned long long rec16, int q,
-                                           const int* fslot, const int* ffid, unsigned* ready, int c, int G, int tid,
-                                           int nthreads, uint32_t bar_id) {
-    const unsigned long long per = (rec16 + G - 1) / G;
-    const unsigned long long b0 = per * (unsigned long long)c;
-    const unsigned long long b1 = b0 + per < rec16 ? b0 + per : rec16;
-    for (int r = 0; r < q; ++r) {
-        const uint4* src = host + (unsigned long long)ffid[r] * rec16;
-        uint4* dst = pool + (unsigned long long)fslot[r] * rec16;
-        unsigned long long i = b0 + tid;
-        for (; i + 7ull * nthreads < b1; i += 8ull * nthreads) {
-            uint4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = src[i + (unsigned long long)u * nthreads];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) dst[i + (unsigned long long)u * nthreads] = v[u];
-        }
-        for (; i < b1; i += nthreads) dst[i] = src[i];
-        named_bar_sync(bar_id, nthreads);
-        if (tid == 0) {
-            __threadfence();
-            atomicAdd(&ready[r], 1u);
-        }
-    }
-}
 
 // Producer side: wait (bounded) until all G CTAs have copied their part of
 // fill i, then order the async proxy after those generic writes.
@@ -419,7 +389,6 @@ struct ExpertParams {
     // fused cache fill (performed by this launch when do_fill != 0)
     int do_fill;
     const uint4* host_pool;   // device-accessible address of the host pool
-    unsigned long long rec16; // record bytes / 16
     const int* fill_slot;     // [q] victim slot of fill i
     const int* fill_fid;      // [q] flat id of fill i
     const int* wl_fill;       // [E] fill index of entry i, or -1 for a hit
