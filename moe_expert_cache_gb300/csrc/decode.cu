@@ -186,12 +186,12 @@ __device__ __noinline__ void gu_feature(const uint4* wg, const uint4* wu, const 
     }
 }
 
-// ---- phase B inner loop: the rows rb + wid + 8 i (i < 4, row < R) of one
+// ---- phase B inner loop: the rows rb + rs * i (i < 4, row < R) of one
 // entry's W_d block in shared memory against NT token rows of h (fp32, shared
 // memory).  Each column chunk of h is read once and applied to all the rows
 // of the warp, which gives independent accumulation chains.
 template <int NT>
-__device__ __forceinline__ void down_group(uint32_t wbase, uint32_t hs, int g0, int F, int R, int rb, int wid,
+__device__ __forceinline__ void down_group(uint32_t wbase, uint32_t hs, int g0, int F, int R, int rb, int rs,
                                            int lane, float* o_s, int obase, int RMAX) {
     float acc[4][NT];
 #pragma unroll
@@ -211,7 +211,7 @@ __device__ __forceinline__ void down_group(uint32_t wbase, uint32_t hs, int g0, 
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int rl = rb + wid + r * CONSUMER_WARPS;
+            const int rl = rb + r * rs;
             if (rl < R) {
                 float w8[8];
                 ft::bf16x8_to_f32(ft::lds128(wbase + (uint32_t)rl * F * 2 + v * 16), w8);
@@ -227,7 +227,7 @@ __device__ __forceinline__ void down_group(uint32_t wbase, uint32_t hs, int g0, 
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const int rl = rb + wid + r * CONSUMER_WARPS;
+        const int rl = rb + r * rs;
         if (rl < R) {  // warp-uniform
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
@@ -238,22 +238,24 @@ __device__ __forceinline__ void down_group(uint32_t wbase, uint32_t hs, int g0, 
     }
 }
 
-// All rows [0, R) of one entry, NT tokens at a time.  Out of line, like
-// gu_feature, to keep the hot code small; W_d rows and h by shared address.
-__device__ __noinline__ void down_entry(uint32_t wbase, uint32_t hs, int ntok, int F, int R, int wid, int lane,
-                                        float* o_s, int obase, int RMAX) {
-    for (int rb = 0; rb < R; rb += 4 * CONSUMER_WARPS) {
+// The rows wi, wi + nw, wi + 2 nw, ... (< R) of one entry -- this warp is the
+// wi-th of the nw warps serving the entry -- NT tokens at a time.  Out of
+// line, like gu_feature, to keep the hot code small; W_d rows and h by shared
+// address.
+__device__ __noinline__ void down_entry(uint32_t wbase, uint32_t hs, int ntok, int F, int R, int wi, int nw,
+                                        int lane, float* o_s, int obase, int RMAX) {
+    for (int rb = wi; rb < R; rb += 4 * nw) {
         int g0 = 0;
         while (g0 < ntok) {
             const int rem = ntok - g0;
             if (rem >= 4) {
-                down_group<4>(wbase, hs, g0, F, R, rb, wid, lane, o_s, obase, RMAX);
+                down_group<4>(wbase, hs, g0, F, R, rb, nw, lane, o_s, obase, RMAX);
                 g0 += 4;
             } else if (rem >= 2) {
-                down_group<2>(wbase, hs, g0, F, R, rb, wid, lane, o_s, obase, RMAX);
+                down_group<2>(wbase, hs, g0, F, R, rb, nw, lane, o_s, obase, RMAX);
                 g0 += 2;
             } else {
-                down_group<1>(wbase, hs, g0, F, R, rb, wid, lane, o_s, obase, RMAX);
+                down_group<1>(wbase, hs, g0, F, R, rb, nw, lane, o_s, obase, RMAX);
                 g0 += 1;
             }
         }
@@ -689,13 +691,26 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             }
             continue;
         }
-        // down rows [r0, r1) of the stage's entries
+        // down rows [r0, r1) of the stage's entries.  The warps split over the
+        // entries so that they proceed at the same time: with cls = min(ne, 8)
+        // classes, warp w serves the entries e0 + (w mod cls) + j cls, as the
+        // (w / cls)-th of the nw warps of its class.
         const int e1 = stage_end(e0);
-        for (int e = e0; e < e1 && ok; ++e) {
-            const int off = m_off[e];
-            const int ntok = m_off[e + 1] - off;
-            down_entry(ft::smem_addr(sb), ft::smem_addr(sb + wpad), ntok, F, R, wid, lane, o_s, off, RMAX);
-            sb += wpad + ((hbytes(e) + 127u) & ~127u);
+        if (ok) {
+            const int ne = e1 - e0;
+            const int cls = ne < CONSUMER_WARPS ? ne : CONSUMER_WARPS;
+            const int my = wid % cls, wi = wid / cls;
+            const int nw = (CONSUMER_WARPS - my + cls - 1) / cls;
+            unsigned so = 0;
+            int e = e0;
+            for (; e < e0 + my; ++e) so += wpad + ((hbytes(e) + 127u) & ~127u);
+            while (e < e1) {
+                const int off = m_off[e];
+                const unsigned char* eb = sb + so;
+                down_entry(ft::smem_addr(eb), ft::smem_addr(eb + wpad), m_off[e + 1] - off, F, R, wi, nw, lane, o_s,
+                           off, RMAX);
+                for (int n = 0; n < cls && e < e1; ++n, ++e) so += wpad + ((hbytes(e) + 127u) & ~127u);
+            }
         }
         __syncwarp();
         if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
