@@ -16,6 +16,8 @@ Modules:
               dense masked brute force.
   nvfp4    -- e2m1 / e4m3 decoding of NVFP4 records and the block-16
               activation quantiser.
+  mxfp4    -- e2m1 / E8M0 decoding of MXFP4 records and the block-32 MX
+              conversion.
 
 Readings of the pages that these modules take where the pages are silent are
 listed in each function's docstring.  Parity unpinned: none of the functions

@@ -2,7 +2,7 @@
 
 This module is shared by the oracle, the tests and the benchmark.  It holds
 no arithmetic of the method itself (no routing, no cache control, no expert
-FFN): only random draws, the bf16 / NVFP4 encodings of the drawn weights and
+FFN): only random draws, the bf16 / NVFP4 / MXFP4 encodings of the drawn weights and
 the byte layout of one expert record in the host pool.
 
 Random streams: numpy ``PCG64`` seeded by ``SeedSequence([seed, tag, ...])``
@@ -32,12 +32,15 @@ TAG_TOPK = 5
 
 FMT_BF16 = 0
 FMT_NVFP4 = 1
+FMT_MXFP4 = 2
 
 # Record layout: gate and up rows are interleaved in groups of this many rows
 # (16 gate rows, then the 16 matching up rows, ...).
 GU_INTERLEAVE = 16
 # NVFP4: one e4m3 scale per this many consecutive values along K.
 NVFP4_BLOCK = 16
+# MXFP4: one E8M0 (power-of-two) scale per this many consecutive values along K.
+MXFP4_BLOCK = 32
 
 
 @dataclass(frozen=True)
@@ -62,6 +65,8 @@ def record_bytes(H: int, F: int, fmt: int) -> int:
         return 2 * n
     if fmt == FMT_NVFP4:
         return n // 2 + n // NVFP4_BLOCK
+    if fmt == FMT_MXFP4:
+        return n // 2 + n // MXFP4_BLOCK
     raise ValueError(f"unknown format {fmt}")
 
 
@@ -252,12 +257,80 @@ def record_nvfp4(seed: int, layer: int, expert: int, H: int, F: int, out=None):
     return pack_record_nvfp4(q, out=out), q["global"]
 
 
+# ------------------------------------------------------------ MXFP4 experts
+# Encoding of the drawn weights into MXFP4 (OCP Microscaling v1.0 conversion):
+# per block of 32 along K the shared exponent is floor(log2 amax) - 2 (2 being
+# the largest e2m1 exponent), clamped to [-127, 127], stored biased by 127 in
+# one E8M0 byte; values are e2m1(w / 2^exponent), round to nearest even with
+# saturation.  An all-zero block takes exponent -127.
+
+def quantize_mxfp4(W: np.ndarray):
+    """W [rows, K] float -> (codes uint8 [rows, K], E8M0 codes uint8 [rows, K/32])."""
+    rows, K = W.shape
+    Wb = W.reshape(rows, K // MXFP4_BLOCK, MXFP4_BLOCK).astype(np.float64)
+    amax = np.abs(Wb).max(axis=2)
+    _, ex = np.frexp(amax)              # amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    se = np.where(amax > 0, ex - 1 - 2, -127)
+    se = np.clip(se, -127, 127).astype(np.int64)
+    v = Wb / np.ldexp(1.0, se)[..., None]
+    codes = encode_e2m1(v).reshape(rows, K)
+    return codes, (se + 127).astype(np.uint8)
+
+
+def expert_mxfp4(seed: int, layer: int, expert: int, H: int, F: int):
+    """MXFP4 encoding of one layer-expert drawn like the BF16 weights: e2m1
+    codes and E8M0 scale codes of gate [F,H], up [F,H] and down [H,F]."""
+    rng = _rng(seed, TAG_WEIGHTS, layer, expert)
+    w = rng.standard_normal(3 * H * F, dtype=np.float32) * np.float32(0.02)
+    n = H * F
+    out = {}
+    for name, W in (("g", w[:n].reshape(F, H)), ("u", w[n:2 * n].reshape(F, H)), ("d", w[2 * n:].reshape(H, F))):
+        codes, sc = quantize_mxfp4(W)
+        out[name] = codes
+        out[name + "_scale"] = sc
+    return out
+
+
+def pack_record_mxfp4(q: dict, out: np.ndarray | None = None) -> np.ndarray:
+    """Byte image of one MXFP4 record: the NVFP4 layout with E8M0 block-32
+    scales in place of the e4m3 block-16 ones, and no global.
+
+    [W_gu values: 2F x H e2m1, two per byte, low nibble first, rows
+    interleaved in groups of GU_INTERLEAVE] [W_d values: H x F]
+    [W_gu scales: 2F x H/32, same row order] [W_d scales: H x F/32].
+    """
+    F, H = q["g"].shape
+    g = GU_INTERLEAVE
+    gu = np.empty((F // g, 2, g, H), dtype=np.uint8)
+    gu[:, 0] = q["g"].reshape(F // g, g, H)
+    gu[:, 1] = q["u"].reshape(F // g, g, H)
+    gus = np.empty((F // g, 2, g, H // MXFP4_BLOCK), dtype=np.uint8)
+    gus[:, 0] = q["g_scale"].reshape(F // g, g, -1)
+    gus[:, 1] = q["u_scale"].reshape(F // g, g, -1)
+    parts = [_pack_nibbles(gu), _pack_nibbles(q["d"]), gus.reshape(-1), q["d_scale"].reshape(-1)]
+    nb = record_bytes(H, F, FMT_MXFP4)
+    if out is None:
+        out = np.empty(nb, dtype=np.uint8)
+    off = 0
+    for p in parts:
+        out[off:off + p.size] = p
+        off += p.size
+    assert off == nb
+    return out
+
+
+def record_mxfp4(seed: int, layer: int, expert: int, H: int, F: int, out=None) -> np.ndarray:
+    """Record bytes of one MXFP4 layer-expert."""
+    return pack_record_mxfp4(expert_mxfp4(seed, layer, expert, H, F), out=out)
+
+
 # -------------------------------------------------------------- host pool
 
 def fill_host_pool(pool: np.ndarray, shape: Shape, seed: int, threads: int | None = None) -> np.ndarray | None:
     """Write every record [l*E+e] of the host pool (uint8 [L*E*record_bytes]).
 
-    Returns the per-record fp32 globals [L*E] for NVFP4, else None.
+    Returns the per-record fp32 globals [L*E] for NVFP4, else None (BF16 and
+    MXFP4 records carry no global).
     """
     rb = shape.record_bytes
     n = shape.L * shape.E
@@ -269,6 +342,8 @@ def fill_host_pool(pool: np.ndarray, shape: Shape, seed: int, threads: int | Non
         dst = pool[fid * rb:(fid + 1) * rb]
         if shape.fmt == FMT_BF16:
             record_bf16(seed, l, e, shape.H, shape.F, out=dst)
+        elif shape.fmt == FMT_MXFP4:
+            record_mxfp4(seed, l, e, shape.H, shape.F, out=dst)
         else:
             _, gsv = record_nvfp4(seed, l, e, shape.H, shape.F, out=dst)
             glob[fid] = gsv
@@ -345,6 +420,9 @@ DECODE_T16 = Workload("decode_t16", Shape(L=48, E=128, k=8, H=2048, F=768), S=76
 PREFILL = Workload("prefill", Shape(L=4, E=128, k=8, H=2048, F=768), S=256, steps=1, T=8192,
                    rho=None, sigma=None, B_P=0.0, B_H=0.0)
 LARGE_NVFP4 = Workload("large_nvfp4", Shape(L=8, E=256, k=8, H=4096, F=2048, fmt=FMT_NVFP4), S=512,
+                       steps=64, T=1, rho=0.8, sigma=None, B_P=52.7, B_H=150.0)
+# The Large shapes with MXFP4 banks (a further record format; same routing).
+LARGE_MXFP4 = Workload("large_mxfp4", Shape(L=8, E=256, k=8, H=4096, F=2048, fmt=FMT_MXFP4), S=512,
                        steps=64, T=1, rho=0.8, sigma=None, B_P=52.7, B_H=150.0)
 # Decode T=16 resizes its cache: shrink to this many slots before step 32,
 # grow back before step 64.
