@@ -423,6 +423,8 @@ def run_ours(args, rank, world, local_rank):
         out["decode_t16"] = run_decode_t16_bench(pool, device)
     if not args.no_prefill:
         out["prefill"] = run_prefill_bench(device, peaks)
+    if rank == 0 and not args.no_fp4:
+        out["fp4_decode"] = run_fp4_decode_bench(device, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(pool.numpy() if world == 1 else shared[0], args.cpu_seconds)
     if world > 1:
@@ -482,6 +484,89 @@ def run_decode_t16_bench(pool, device) -> dict:
             "fills_per_layer_step": round(d["fills"] / calls, 3),
             "gpu_experts_per_layer_step": round((d["hits"] + d["fills"]) / calls, 2),
             "link_floor_ms_per_step": round(d["fills"] / wl.steps * sh.record_bytes / 211e9 * 1e3, 3)}
+
+
+def _fp4_pool(sh: synth.Shape, seed: int, distinct: int = 16):
+    """Pinned pool of one layer whose E records are the encodings of
+    `distinct` drawn experts, repeated (the FP4 kernel's time does not depend
+    on the values).  Returns (pool, per-record globals or None)."""
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+    rb = sh.record_bytes
+    enc = synth.record_nvfp4 if sh.fmt == synth.FMT_NVFP4 else synth.record_mxfp4
+    with ThreadPoolExecutor(min(distinct, os.cpu_count() or 1)) as ex:
+        got = list(ex.map(lambda e: enc(seed, 0, e, sh.H, sh.F), range(distinct)))
+    recs = [g[0] for g in got] if sh.fmt == synth.FMT_NVFP4 else got
+    pool = torch.empty(sh.E * rb, dtype=torch.uint8, pin_memory=True)
+    pn = pool.numpy()
+    for e in range(sh.E):
+        pn[e * rb:(e + 1) * rb] = recs[e % distinct]
+    glob = (np.array([got[e % distinct][1] for e in range(sh.E)], dtype=np.float32)
+            if sh.fmt == synth.FMT_NVFP4 else None)
+    return pool, glob
+
+
+def run_fp4_decode_bench(device, peaks, calls_t1: int = 96, calls_t64: int = 24) -> dict:
+    """FP4 expert kernel (NVFP4 and MXFP4 records) on the Large shapes, hits
+    only: one MoE layer of E=256 experts, top-8, H=4096, F=2048, every record
+    resident in 512 slots (a warm-up with B_P = B_H fills every miss), AR(1)
+    rho=0.8 logits, T=1 and T=64.  The bound is HBM: each launch reads the
+    records of its routed experts.  Per-launch device time from the library's
+    CUDA-event records around each expert-kernel launch."""
+    import torch
+    import moe_expert_cache_gb300 as ft
+    out = {"workload": "Large shapes, hits only: 1 MoE layer, E=256, top-8, hidden 4096, ffn 2048, 512 slots "
+                       "holding every record, AR(1) rho=0.8 logits; records of 16 drawn experts repeated",
+           "execution": "eager library calls; expert-kernel time from the library's per-launch CUDA events"}
+    H, F, E, k = 4096, 2048, 256, 8
+    cs = torch.cuda.Stream(device)
+    for name, fmt in (("nvfp4", synth.FMT_NVFP4), ("mxfp4", synth.FMT_MXFP4)):
+        sh = synth.Shape(L=1, E=E, k=k, H=H, F=F, fmt=fmt)
+        pool, glob = _fp4_pool(sh, 0)
+        ctx = ft.Context(1, E, k, H, F, 512, pool, fmt=fmt, T_max=64, nvfp4_global=glob,
+                         compute_stream=cs.cuda_stream)
+        res = {"record_bytes": sh.record_bytes}
+        with torch.cuda.stream(cs):
+            pc = torch.zeros(64, H, device=device)
+            y = torch.empty(64, H, device=device)
+            warm = torch.from_numpy(synth.iid_logits(1, (77,), 64, E)).to(device)
+            for i in range(8):  # fill every expert (q = m when B_P = B_H)
+                ctx.route_ctl(0, 64, logits=torch.roll(warm, i * 32, dims=1), B_P=1.0, B_H=1.0)
+                ctx.moe_forward(torch.zeros(64, H, dtype=torch.bfloat16, device=device), pc, y)
+        torch.cuda.synchronize(device)
+        for T, calls in ((1, calls_t1), (64, calls_t64)):
+            lg = torch.from_numpy(synth.ar1_logits(0, calls, 1, T, E, 0.8)[:, 0]).to(device)
+            x = torch.from_numpy(synth.tokens_bf16(0, 0, 0, T, H).view(np.int16)).to(device).view(torch.bfloat16)
+            with torch.cuda.stream(cs):
+                for i in range(4):
+                    ctx.route_ctl(0, T, logits=lg[i], B_P=52.7, B_H=150.0)
+                    ctx.moe_forward(x, pc[:T], y[:T])
+            torch.cuda.synchronize(device)
+            c0 = ctx.counters()
+            ctx.profile_enable(True)
+            with torch.cuda.stream(cs):
+                for i in range(calls):
+                    ctx.route_ctl(0, T, logits=lg[i], B_P=52.7, B_H=150.0)
+                    ctx.moe_forward(x, pc[:T], y[:T])
+            torch.cuda.synchronize(device)
+            prof = ctx.profile_read()
+            ctx.profile_enable(False)
+            c1 = ctx.counters()
+            d = {k_: c1[k_] - c0[k_] for k_ in c1}
+            ms = prof["expert_ffn"]["ms"]
+            n = prof["expert_ffn"]["launches"]
+            hbm = kernel_bytes(sh, T, d)["expert_ffn"]["hbm"]
+            gbs = hbm / (ms * 1e-3) / 1e9
+            res[f"t{T}"] = {"us_per_launch": round(ms * 1e3 / n, 2), "launches": n,
+                            "hits_per_launch": round(d["hits"] / max(1, d["calls"]), 2),
+                            "fills": d["fills"], "hbm_bytes_per_launch": int(hbm / n),
+                            "achieved_GBps": round(gbs, 1), "peak_GBps": peaks["hbm_gbs"],
+                            "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        assert ctx.status() == ft.FT_OK
+        ctx.close()
+        del pool
+        out[name] = res
+    return out
 
 
 def run_prefill_bench(device, peaks, reps: int = 3) -> dict:
@@ -744,6 +829,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-t16", action="store_true", help="skip the decode T=16 (resize) measurement")
+    ap.add_argument("--no-fp4", action="store_true", help="skip the FP4 (NVFP4, MXFP4) decode measurement")
+    ap.add_argument("--fp4-only", action="store_true", help="only the FP4 decode measurement (one JSON object)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill measurement and print its object (no bench line)")
@@ -761,6 +848,13 @@ def main():
         import moe_expert_cache_gb300 as ft
         ft.load()
         print(json.dumps({"prefill": run_prefill_bench(torch.device("cuda", 0), read_peaks())}), flush=True)
+        return
+    if args.fp4_only:
+        import torch
+        torch.cuda.set_device(0)
+        import moe_expert_cache_gb300 as ft
+        ft.load()
+        print(json.dumps({"fp4_decode": run_fp4_decode_bench(torch.device("cuda", 0), read_peaks())}), flush=True)
         return
     rank, world, local_rank = dist_env()
     if args.warmup < 3:

@@ -44,6 +44,7 @@ typedef int32_t ft_status;
 
 #define FT_FMT_BF16   0       /* bf16 banks                                           */
 #define FT_FMT_NVFP4  1       /* e2m1 values + e4m3 block-16 scales + fp32 global     */
+#define FT_FMT_MXFP4  2       /* e2m1 values + E8M0 block-32 scales (OCP MX v1.0)     */
 
 typedef struct ft_ctx ft_ctx; /* opaque; created by ft_layer_init, freed by ft_destroy */
 
@@ -105,8 +106,14 @@ const char* ft_status_str(ft_status s);
  *   L, E, k, H, F  sizes; need E <= 1024, k <= 16, k <= E, H % 64 == 0,
  *                  F % 64 == 0 (H, F >= 64).
  *   S              number of slots (>= 1).  Prefill needs S >= 2E.
- *   fmt            FT_FMT_BF16 or FT_FMT_NVFP4 (record layout in ft_record_bytes);
- *                  NVFP4 needs H % 256 == 0, F % 256 == 0 and nvfp4_global.
+ *   fmt            FT_FMT_BF16, FT_FMT_NVFP4 or FT_FMT_MXFP4 (record layout in
+ *                  ft_record_bytes); NVFP4 needs H % 256 == 0, F % 256 == 0
+ *                  and nvfp4_global; MXFP4 needs H % 256 == 0, F % 512 == 0
+ *                  (the W_d scale rows of a CTA's output rows are copied as
+ *                  16-byte multiples) and nvfp4_global == NULL.  The pages
+ *                  list MXFP4 among the bank layouts (deepmox, "One logical
+ *                  expert, two physical levels of memory").  MXFP4 contexts
+ *                  with prefill hold the same bf16 staging copy as NVFP4.
  *   T_max          largest T of a decode call (ft_route_ctl), 1..256, with
  *                  T_max*k <= 4096 and T_max*H <= 32768 (the tokens of a
  *                  decode call are staged in shared memory).
@@ -120,7 +127,7 @@ const char* ft_status_str(ft_status s);
  *                  cudaHostRegister) or otherwise device-accessible, and stay
  *                  valid and unchanged until ft_destroy.  Not copied.
  *   nvfp4_global   HOST array of L*E fp32 per-record global scales (NVFP4), or
- *                  NULL for BF16.  Copied to device memory at init (the pages:
+ *                  NULL for BF16 and MXFP4.  Copied to device memory at init (the pages:
  *                  small per-expert values stay GPU-resident).
  *   compute_stream, transfer_stream
  *                  cudaStream_t handles owned by the caller (NULL = legacy
@@ -138,7 +145,11 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
  * BF16 : [W_gu 2F x H bf16, row-major, gate/up rows interleaved in groups of 16
  *         (16 gate rows, the 16 matching up rows, ...)] [W_d H x F bf16 row-major].
  * NVFP4: [W_gu values 2F x H e2m1, 2 per byte, low nibble first, same row order]
- *        [W_d values H x F] [W_gu e4m3 scales 2F x H/16] [W_d scales H x F/16]. */
+ *        [W_d values H x F] [W_gu e4m3 scales 2F x H/16] [W_d scales H x F/16].
+ * MXFP4: the NVFP4 layout with one E8M0 scale (value 2^(code-127), 0xFF NaN)
+ *        per 32 values along K: [W_gu values] [W_d values]
+ *        [W_gu scales 2F x H/32] [W_d scales H x F/32]; no global.
+ * Returns 0 for an unknown fmt. */
 size_t ft_record_bytes(int32_t H, int32_t F, int32_t fmt);
 
 /*

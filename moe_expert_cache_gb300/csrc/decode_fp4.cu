@@ -1,17 +1,22 @@
-// Decode expert FFN over NVFP4 records (W4A16): the same persistent,
+// Decode expert FFN over FP4 records (W4A16): the same persistent,
 // cooperatively launched streaming design as the BF16 kernel, reading packed
-// e2m1 values and e4m3 block-16 scales.
-//
-// deepmox "One logical expert, two physical levels of memory": an NVFP4 bank
-// stores packed four-bit values plus scale information; small per-expert
-// globals stay GPU-resident.  Weight w = e2m1 * e4m3(block of 16 along K) *
-// global(expert).  Each 16-value block is summed in fp32 against the fp32
-// activations, scaled by its e4m3 scale, and the row total is multiplied by
-// the expert's global once.  Activations are not quantised (W4A16).
+// e2m1 values and their block scales.  Two record formats share the code,
+// selected by the scale block SB:
+//   * NVFP4 (SB = 16): one e4m3 scale per 16 values, and a per-expert fp32
+//     global.  deepmox "One logical expert, two physical levels of memory":
+//     an NVFP4 bank stores packed four-bit values plus scale information;
+//     small per-expert globals stay GPU-resident.
+//   * MXFP4 (SB = 32, OCP Microscaling v1.0): one E8M0 scale, 2^(code-127),
+//     per 32 values; no global (the kernel reads 1.0).  The same section
+//     lists MXFP4 among the bank layouts.
+// Weight w = e2m1 * scale(block along K) * global(expert).  Each block is
+// summed in fp32 against the fp32 activations, scaled by its scale, and the
+// row total is multiplied by the expert's global once.  Activations are not
+// quantised (W4A16).
 //
 // Record (per layer-expert): [W_gu values 2F x H/2 bytes, low nibble first,
 // gate/up rows interleaved in groups of 16][W_d values H x F/2]
-// [W_gu scales 2F x H/16][W_d scales H x F/16].
+// [W_gu scales 2F x H/SB][W_d scales H x F/SB].
 //
 // Differences from the BF16 kernel: a phase-A slot holds 8 gate rows, the 8
 // matching up rows and their scale rows (four bulk copies); a phase-B item is
@@ -19,6 +24,7 @@
 // a slot for any T; x is read from shared memory (fp32 or bf16) when it fits
 // and from global memory otherwise.
 #include "ft_common.cuh"
+#include "../../include/ft.h"
 
 namespace {
 
@@ -55,6 +61,18 @@ __device__ __forceinline__ float2 e4m3x2_f32(const uint8_t* p2) {
     uint32_t h;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(*reinterpret_cast<const unsigned short*>(p2)));
     return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Scales of the 32 values of 16-byte group v of a row whose scale bytes
+// start at `srow`: two e4m3 codes (NVFP4) or one E8M0 code used for both
+// halves (MXFP4).  E8M0 is placed as an IEEE single bit pattern: code c is
+// the exponent field, code 0 the subnormal 2^-127, code 255 NaN.
+template <int SB>
+__device__ __forceinline__ float2 scales32(const uint8_t* srow, int v) {
+    if (SB == 16) return e4m3x2_f32(srow + 2 * v);
+    const uint32_t c = srow[v];
+    const float s = __uint_as_float(c == 255u ? 0x7FC00000u : c == 0u ? 0x00400000u : c << 23);
+    return make_float2(s, s);
 }
 
 // Activation rows in shared memory (x and the staged h rows) are swizzled so
@@ -113,7 +131,7 @@ __device__ __forceinline__ float fp4_dot32(const uint4& w, const float* x, float
 
 // Phase A: gate and up rows of one feature against NT tokens; returns the
 // un-globalled row sums in ag / au.
-template <int NT, int XM>
+template <int NT, int XM, int SB>
 __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                          const void* xs, size_t xrow_elems, const int* tk, int H, int lane,
                                          float* ag, float* au) {
@@ -122,7 +140,7 @@ __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const
     const int nv = H >> 5;  // uint4 (32 values) per row
     for (int v = lane; v < nv; v += 32) {
         const uint4 wg = gv[v], wu = uv[v];
-        const float2 gsc2 = e4m3x2_f32(gs + 2 * v), usc2 = e4m3x2_f32(us + 2 * v);
+        const float2 gsc2 = scales32<SB>(gs, v), usc2 = scales32<SB>(us, v);
         const float g0 = gsc2.x, g1 = gsc2.y, u0 = usc2.x, u1 = usc2.y;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
@@ -137,7 +155,7 @@ __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const
     }
 }
 
-template <int NT, int XM>
+template <int NT, int XM, int SB>
 __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                           const void* xs, int H, const int* m_tok, int off, int g0, int F, int f,
                                           int lane, float gsc, float* hbuf) {
@@ -145,7 +163,7 @@ __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, cons
 #pragma unroll
     for (int n = 0; n < NT; ++n) tk[n] = m_tok[off + g0 + n];
     float ag[NT], au[NT];
-    gu_dots4<NT, XM>(gv, uv, gs, us, xs, (size_t)H, tk, H, lane, ag, au);
+    gu_dots4<NT, XM, SB>(gv, uv, gs, us, xs, (size_t)H, tk, H, lane, ag, au);
     float mine = 0.f;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
@@ -157,7 +175,7 @@ __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, cons
     if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + swz_f32(f)] = mine * kActScale;
 }
 
-template <int XM>
+template <int XM, int SB>
 __device__ __forceinline__ void gu_feature4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                             const void* xs, int H, const int* m_tok, int off, int ntok, int F, int f,
                                             int lane, float gsc, float* hbuf) {
@@ -165,20 +183,20 @@ __device__ __forceinline__ void gu_feature4(const uint4* gv, const uint4* uv, co
     while (g0 < ntok) {
         const int rem = ntok - g0;
         if (rem >= 4) {
-            gu_group4<4, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
+            gu_group4<4, XM, SB>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 4;
         } else if (rem >= 2) {
-            gu_group4<2, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
+            gu_group4<2, XM, SB>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 2;
         } else {
-            gu_group4<1, XM>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
+            gu_group4<1, XM, SB>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 1;
         }
     }
 }
 
 // Phase B: one W_d row (values + scales) against NT staged h rows (fp32).
-template <int NT>
+template <int NT, int SB>
 __device__ __forceinline__ void down_group4(const uint4* wv, const uint8_t* ws, const float* hs, int g, int F,
                                             int lane, float gsc, float* o_s, int obase, int RMAX,
                                             int rl) {
@@ -188,7 +206,7 @@ __device__ __forceinline__ void down_group4(const uint4* wv, const uint8_t* ws, 
     const int nv = F >> 5;
     for (int v = lane; v < nv; v += 32) {
         const uint4 w = wv[v];
-        const float2 sc2 = e4m3x2_f32(ws + 2 * v);
+        const float2 sc2 = scales32<SB>(ws, v);
         const float s0 = sc2.x, s1 = sc2.y;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
@@ -204,6 +222,7 @@ __device__ __forceinline__ void down_group4(const uint4* wv, const uint8_t* ws, 
     }
 }
 
+template <int SB>
 __device__ __forceinline__ void down_row4(const uint4* wv, const uint8_t* ws, const float* hs, int ng, int F,
                                           int lane, float gsc, float* o_s, int obase, int RMAX,
                                           int rl) {
@@ -211,13 +230,13 @@ __device__ __forceinline__ void down_row4(const uint4* wv, const uint8_t* ws, co
     while (g < ng) {
         const int rem = ng - g;
         if (rem >= 4) {
-            down_group4<4>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
+            down_group4<4, SB>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
             g += 4;
         } else if (rem >= 2) {
-            down_group4<2>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
+            down_group4<2, SB>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
             g += 2;
         } else {
-            down_group4<1>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
+            down_group4<1, SB>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
             g += 1;
         }
     }
@@ -227,7 +246,7 @@ __device__ __forceinline__ void down_row4(const uint4* wv, const uint8_t* ws, co
 
 namespace {
 
-template <int XM>
+template <int XM, int SB>
 __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_gdone;
@@ -245,9 +264,9 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     const int TK = T * k;
     const size_t VGU = (size_t)F * H;                 // W_gu value bytes (2F x H/2)
     const size_t VD = (size_t)H * F / 2;              // W_d value bytes
-    const size_t SGU = (size_t)2 * F * H / 16;        // W_gu scale bytes
-    const unsigned vrow = (unsigned)H / 2, srow = (unsigned)H / 16;      // W_gu row bytes
-    const unsigned dvrow = (unsigned)F / 2, dsrow = (unsigned)F / 16;    // W_d row bytes
+    const size_t SGU = (size_t)2 * F * H / SB;        // W_gu scale bytes
+    const unsigned vrow = (unsigned)H / 2, srow = (unsigned)H / SB;      // W_gu row bytes
+    const unsigned dvrow = (unsigned)F / 2, dsrow = (unsigned)F / SB;    // W_d row bytes
 
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -419,7 +438,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         const uint4* uv = reinterpret_cast<const uint4*>(sb + (size_t)(FPC + wid) * vrow);
         const uint8_t* gs = sb + 2 * FPC * vrow + (size_t)wid * srow;
         const uint8_t* us = sb + 2 * FPC * vrow + FPC * srow + (size_t)wid * srow;
-        if (ok) gu_feature4<XM>(gv, uv, gs, us, xsrc, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf);
+        if (ok) gu_feature4<XM, SB>(gv, uv, gs, us, xsrc, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf);
         __syncwarp();
         if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
     }
@@ -443,7 +462,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 const unsigned char* sb = ring + (size_t)st * slot_bytes;
                 const float* hs = reinterpret_cast<const float*>(sb + wpart);
                 for (int rl = wid; rl < R && ok; rl += CW)
-                    down_row4(reinterpret_cast<const uint4*>(sb + (size_t)rl * dvrow),
+                    down_row4<SB>(reinterpret_cast<const uint4*>(sb + (size_t)rl * dvrow),
                               sb + (size_t)RMAX * dvrow + (size_t)rl * dsrow, hs, ng, F, lane, m_gs[e], o_s,
                               off + g0, RMAX, rl);
                 __syncwarp();
@@ -469,7 +488,9 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
 
 static constexpr size_t kSmemLimit4 = 227 * 1024 - 256;  // dynamic; the rest is static shared memory
 
-cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
+cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStream_t s) {
+    if (fmt != FT_FMT_NVFP4 && fmt != FT_FMT_MXFP4) return cudaErrorInvalidValue;
+    const int SB = fmt == FT_FMT_MXFP4 ? 32 : 16;
     const int G = num_sms;
     const int RMAX = (p.H + G - 1) / G;
     const size_t TK = (size_t)p.T * p.k;
@@ -485,8 +506,8 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
     }
     const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127) +
                         (((7 * TK + 1) * 4 + 127) & ~(size_t)127);
-    const size_t chunk = (size_t)2 * FPC * (p.H / 2 + p.H / 16);
-    const size_t wpart = ((size_t)RMAX * (p.F / 2 + p.F / 16) + 127) & ~(size_t)127;
+    const size_t chunk = (size_t)2 * FPC * (p.H / 2 + p.H / SB);
+    const size_t wpart = ((size_t)RMAX * (p.F / 2 + p.F / SB) + 127) & ~(size_t)127;
     if (head + 2 * chunk > kSmemLimit4) return cudaErrorInvalidValue;
     // token group of phase B: as many h rows as fit next to the W_d rows in a
     // slot when two slots fill the shared memory
@@ -511,14 +532,21 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s) {
     p.fill_chunk = (unsigned)fch;
     p.fill_slots = nf;
     const size_t smem = head + slot * nst + (size_t)nf * fch;
-    const void* fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM>
-                     : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM>
-                                         : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL>;
-    static size_t smem_set[3] = {0, 0, 0};  // per kernel variant: set only when it grows
-    if (smem > smem_set[xm]) {
+    const void* fn;
+    if (SB == 16)
+        fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM, 16>
+             : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM, 16>
+                                 : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL, 16>;
+    else
+        fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM, 32>
+             : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM, 32>
+                                 : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL, 32>;
+    static size_t smem_set[6] = {0, 0, 0, 0, 0, 0};  // per kernel variant: set only when it grows
+    const int var = xm + (SB == 32 ? 3 : 0);
+    if (smem > smem_set[var]) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        smem_set[xm] = smem;
+        smem_set[var] = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);

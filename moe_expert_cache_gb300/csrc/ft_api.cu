@@ -179,6 +179,7 @@ size_t ft_record_bytes(int32_t H, int32_t F, int32_t fmt) {
     const size_t n = (size_t)3 * H * F;
     if (fmt == FT_FMT_BF16) return 2 * n;
     if (fmt == FT_FMT_NVFP4) return n / 2 + n / 16;
+    if (fmt == FT_FMT_MXFP4) return n / 2 + n / 32;
     return 0;
 }
 
@@ -190,8 +191,10 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     if (L < 1 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E || H < 64 || H % 64 || F < 64 || F % 64 || S < 1 ||
         T_max < 1 || T_max > 256 || T_max * k > 4096 || T_prefill_max < 0 || !host_pool)
         return FT_ERR_ARG;
-    if (fmt != FT_FMT_BF16 && fmt != FT_FMT_NVFP4) return FT_ERR_ARG;
+    if (fmt != FT_FMT_BF16 && fmt != FT_FMT_NVFP4 && fmt != FT_FMT_MXFP4) return FT_ERR_ARG;
     if (fmt == FT_FMT_NVFP4 && (!nvfp4_global || H % 256 || F % 256)) return FT_ERR_ARG;
+    if (fmt == FT_FMT_MXFP4 && (nvfp4_global || H % 256 || F % 512)) return FT_ERR_ARG;
+    if (fmt == FT_FMT_BF16 && nvfp4_global) return FT_ERR_ARG;
     if (route_ctl_smem_bytes(T_max, k, E, S) > kCtlSmemMax) return FT_ERR_ARG;
     if (fmt == FT_FMT_BF16 && (size_t)T_max * H * 2 > 65536) return FT_ERR_ARG;  // BF16 decode stages x in smem
     // prefill: 256-column GEMM tiles over 2F and H, top-k of at most 256 logits
@@ -277,6 +280,11 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     if (nvfp4_global) {
         INIT_CUDA(cudaMalloc(&c->nvfp4_global, (size_t)L * E * 4));
         INIT_CUDA(cudaMemcpy(c->nvfp4_global, nvfp4_global, (size_t)L * E * 4, cudaMemcpyHostToDevice));
+    } else if (fmt == FT_FMT_MXFP4) {
+        // MXFP4 records carry no global: the shared FP4 kernels read 1.0
+        std::vector<float> ones((size_t)L * E, 1.0f);
+        INIT_CUDA(cudaMalloc(&c->nvfp4_global, (size_t)L * E * 4));
+        INIT_CUDA(cudaMemcpy(c->nvfp4_global, ones.data(), (size_t)L * E * 4, cudaMemcpyHostToDevice));
     }
     if (T_prefill_max > 0) {
         st = prefill_alloc(c->pf, T_prefill_max, k, H, F, E, fmt);
@@ -350,8 +358,8 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     c->fill_pending = false;
     {
         ProfScope ps(c->prof, FT_K_EXPERT, c->cs);
-        if (c->fmt == FT_FMT_NVFP4)
-            FT_CUDA(launch_expert_ffn_fp4(p, c->num_sms, c->cs));
+        if (c->fmt == FT_FMT_NVFP4 || c->fmt == FT_FMT_MXFP4)
+            FT_CUDA(launch_expert_ffn_fp4(p, c->fmt, c->num_sms, c->cs));
         else
             FT_CUDA(launch_expert_ffn(p, c->num_sms, c->cs));
     }
@@ -659,10 +667,10 @@ ft_status ft_prefill_layer(ft_ctx* c, int32_t buffer, int32_t layer, int32_t nex
     }
     FT_CUDA(cudaStreamWaitEvent(cs, pf.loaded[buffer], 0));
     const float* escale = nullptr;
-    if (c->fmt == FT_FMT_NVFP4) {
+    if (c->fmt == FT_FMT_NVFP4 || c->fmt == FT_FMT_MXFP4) {
         ProfScope ps(c->prof, FT_K_PF_DEQUANT, cs);
         FT_CUDA(launch_pf_dequant(pf, c->slot_pool + (size_t)buffer * layer_bytes, cs));
-        escale = c->nvfp4_global + (size_t)layer * c->E;
+        if (c->fmt == FT_FMT_NVFP4) escale = c->nvfp4_global + (size_t)layer * c->E;
     }
     {
         ProfScope ps(c->prof, FT_K_PF_ROUTE, cs);

@@ -398,7 +398,7 @@ struct ExpertParams {
     int fill_slots;           // fused-fill ring slots (2..4)
     int fill_fpf;             // BF16: features per fused-fill unit
     int fill_nks;             // BF16: K segments per fused-fill unit
-    const float* gscale;      // [L*E] NVFP4 per-expert fp32 global, or null
+    const float* gscale;      // [L*E] FP4 per-expert fp32 global (all 1 for MXFP4), or null
     int tgroup;               // NVFP4: tokens per phase-B item
     int nstage;               // pipeline depth (stages in shared memory)
     unsigned stage_bytes;     // bytes of one stage
@@ -408,6 +408,7 @@ struct ExpertParams {
 cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s);
 cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);
 cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s);
-cudaError_t launch_expert_ffn_fp4(ExpertParams p, int num_sms, cudaStream_t s);
+// fmt: FT_FMT_NVFP4 (e4m3 block-16 scales) or FT_FMT_MXFP4 (E8M0 block-32 scales)
+cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStream_t s);
 size_t route_ctl_smem_bytes(int T, int k, int E, int S);
 constexpr size_t kCtlSmemMax = 200 * 1024;

@@ -525,7 +525,8 @@ ft_status prefill_alloc(PrefillState& pf, int T_max, int k, int H, int F, int E,
     pf.T_max = T_max;
     pf.E = E; pf.k = k; pf.H = H; pf.F = F;
     pf.fmt = fmt;
-    if (fmt == FT_FMT_NVFP4 && cudaMalloc(&pf.staging, (size_t)E * 3 * H * F * 2) != cudaSuccess) {
+    if ((fmt == FT_FMT_NVFP4 || fmt == FT_FMT_MXFP4) &&
+        cudaMalloc(&pf.staging, (size_t)E * 3 * H * F * 2) != cudaSuccess) {
         cudaGetLastError();
         return FT_ERR_OOM;
     }
@@ -556,11 +557,12 @@ ft_status prefill_set_pool(PrefillState& pf, const uint8_t* pool, size_t rb) {
     const uint64_t E = pf.E, H = pf.H, F = pf.F;
     pf.rb = rb;
     for (int b = 0; b < 2; ++b) {
-        // BF16: the GEMMs read the buffer's records in place; NVFP4: the bf16
-        // staging copy of the layer (one, reused by both buffers in turn)
-        const uint8_t* base = pf.fmt == FT_FMT_NVFP4 ? static_cast<const uint8_t*>(pf.staging)
-                                                     : pool + (size_t)b * E * rb;
-        const uint64_t rbb = pf.fmt == FT_FMT_NVFP4 ? 3 * H * F * 2 : rb;
+        // BF16: the GEMMs read the buffer's records in place; NVFP4 and
+        // MXFP4: the bf16 staging copy of the layer (one, reused by both
+        // buffers in turn)
+        const bool staged = pf.fmt == FT_FMT_NVFP4 || pf.fmt == FT_FMT_MXFP4;
+        const uint8_t* base = staged ? static_cast<const uint8_t*>(pf.staging) : pool + (size_t)b * E * rb;
+        const uint64_t rbb = staged ? 3 * H * F * 2 : rb;
         if (!encode_3d(&pf.mapB1[b], base, 2 * F, H, E, rbb, GN) ||
             !encode_3d(&pf.mapB2[b], base + 2 * F * H * 2, H, F, E, rbb, GN))
             return FT_ERR_CUDA;
@@ -664,22 +666,32 @@ cudaError_t launch_pf_combine(PrefillState& pf, int T, float* y, cudaStream_t s)
     return cudaGetLastError();
 }
 
-// ---------------------------------------------------- NVFP4 -> bf16 staging
+// ------------------------------------------- NVFP4 / MXFP4 -> bf16 staging
 
 namespace {
 
-// Expand E NVFP4 records into the bf16 record layout: every weight becomes
-// e2m1(value) * e4m3(block scale), which bf16 holds exactly (at most 6
-// significant bits); the per-expert fp32 global is applied by the GEMM
-// epilogues.  One thread per 32 values (one 16-byte group of codes).
+// Expand E FP4 records into the bf16 record layout: every weight becomes
+// e2m1(value) * block scale, which bf16 holds exactly (at most 6 significant
+// bits for an e4m3 scale, 2 for a power-of-two E8M0 scale, within bf16's
+// exponent range for every scale a finite weight of magnitude < 2^127 takes);
+// the NVFP4 per-expert fp32 global is applied by the GEMM epilogues.  SB is
+// the scale block: 16 (e4m3 scales, NVFP4) or 32 (E8M0 scales, MXFP4).  One
+// thread per 32 values (one 16-byte group of codes).
+template <int SB>
 __global__ void __launch_bounds__(256) pf_dequant_kernel(const uint8_t* __restrict__ src, size_t rb4, int E, int H,
                                                          int F, uint8_t* __restrict__ dst) {
     __shared__ float e2m1[16];
-    __shared__ float e4m3[256];
+    __shared__ float sct[256];  // scale code -> value
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-        const int e = (i >> 3) & 15, m = i & 7;
-        const float v = e == 0 ? ldexpf((float)m / 8.f, -6) : ldexpf(1.f + (float)m / 8.f, e - 7);
-        e4m3[i] = (i & 0x80) ? -v : v;
+        if (SB == 16) {
+            const int e = (i >> 3) & 15, m = i & 7;
+            const float v = e == 0 ? ldexpf((float)m / 8.f, -6) : ldexpf(1.f + (float)m / 8.f, e - 7);
+            sct[i] = (i & 0x7F) == 0x7F ? __int_as_float(0x7FC00000) : ((i & 0x80) ? -v : v);
+        } else {
+            // E8M0: 2^(i-127) as its IEEE single bit pattern (code 0: the
+            // subnormal 2^-127), code 255 NaN
+            sct[i] = __uint_as_float(i == 255 ? 0x7FC00000u : i == 0 ? 0x00400000u : (uint32_t)i << 23);
+        }
         if (i < 16) {
             const int c = i & 7;
             const float mag = c < 2 ? 0.5f * (float)c : (1.f + 0.5f * (float)(c & 1)) * (float)(1 << ((c >> 1) - 1));
@@ -687,10 +699,11 @@ __global__ void __launch_bounds__(256) pf_dequant_kernel(const uint8_t* __restri
         }
     }
     __syncthreads();
-    const size_t VGU = (size_t)F * H, VD = (size_t)H * F / 2, SGU = (size_t)2 * F * H / 16;
+    const size_t VGU = (size_t)F * H, VD = (size_t)H * F / 2, SGU = (size_t)2 * F * H / SB;
     const size_t rb16 = (size_t)3 * H * F * 2;
     const size_t gu_units = (size_t)2 * F * H / 32, units = (size_t)3 * H * F / 32;
     const size_t total = units * E;
+    constexpr int SPU = 32 / SB;  // scales per unit of 32 values
     for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += (size_t)gridDim.x * blockDim.x) {
         const size_t e = u / units, w = u - e * units;
         const uint8_t* rec = src + e * rb4;
@@ -701,16 +714,16 @@ __global__ void __launch_bounds__(256) pf_dequant_kernel(const uint8_t* __restri
         if (w < gu_units) {  // W_gu: value group w of row w / (H/32)
             const size_t r = w / (H / 32), c = w - r * (H / 32);
             codes = rec + r * (H / 2) + c * 16;
-            sc = rec + VGU + VD + r * (H / 16) + c * 2;
+            sc = rec + VGU + VD + r * (H / SB) + c * SPU;
             o = out + (r * H + c * 32) * 2;
         } else {
             const size_t w2 = w - gu_units, r = w2 / (F / 32), c = w2 - r * (F / 32);
             codes = rec + VGU + r * (F / 2) + c * 16;
-            sc = rec + VGU + VD + SGU + r * (F / 16) + c * 2;
+            sc = rec + VGU + VD + SGU + r * (F / SB) + c * SPU;
             o = out + (size_t)2 * F * H * 2 + (r * F + c * 32) * 2;
         }
         const uint4 q = *reinterpret_cast<const uint4*>(codes);
-        const float s0 = e4m3[sc[0]], s1 = e4m3[sc[1]];
+        const float s0 = sct[sc[0]], s1 = SPU == 2 ? sct[sc[SPU - 1]] : s0;
         const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
         uint32_t packed[16];
 #pragma unroll
@@ -731,7 +744,11 @@ __global__ void __launch_bounds__(256) pf_dequant_kernel(const uint8_t* __restri
 cudaError_t launch_pf_dequant(PrefillState& pf, const uint8_t* layer_records, cudaStream_t s) {
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
-    pf_dequant_kernel<<<sms * 8, 256, 0, s>>>(layer_records, pf.rb, pf.E, pf.H, pf.F,
-                                              static_cast<uint8_t*>(pf.staging));
+    if (pf.fmt == FT_FMT_MXFP4)
+        pf_dequant_kernel<32><<<sms * 8, 256, 0, s>>>(layer_records, pf.rb, pf.E, pf.H, pf.F,
+                                                      static_cast<uint8_t*>(pf.staging));
+    else
+        pf_dequant_kernel<16><<<sms * 8, 256, 0, s>>>(layer_records, pf.rb, pf.E, pf.H, pf.F,
+                                                      static_cast<uint8_t*>(pf.staging));
     return cudaGetLastError();
 }

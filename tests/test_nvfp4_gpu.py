@@ -1,11 +1,14 @@
-"""GPU parity of the NVFP4 decode path (W4A16): control bit-exact, outputs
-within rel-L2 5e-3 of the fp64 oracle on identically dequantised weights."""
+"""GPU parity of the FP4 decode and prefill paths (W4A16) for both FP4 record
+formats, NVFP4 (e4m3 block-16 scales, fp32 global) and MXFP4 (E8M0 block-32
+scales): control bit-exact, outputs within rel-L2 5e-3 of the fp64 oracle on
+identically dequantised weights."""
 import numpy as np
 import pytest
 
 import synth
 from oracle import control as ctl
 from oracle import numerics as nm
+from oracle import mxfp4 as mx
 from oracle import nvfp4 as fp4
 from tests import harness as hz
 
@@ -35,7 +38,11 @@ class FP4Weights:
         if e not in self.cache:
             sh, rb = self.sh, self.sh.record_bytes
             fid = self.layer * sh.E + e
-            self.cache[e] = fp4.record_weights(self.pool[fid * rb:(fid + 1) * rb], sh.H, sh.F, float(self.glob[fid]))
+            rec = self.pool[fid * rb:(fid + 1) * rb]
+            if sh.fmt == synth.FMT_MXFP4:
+                self.cache[e] = mx.record_weights(rec, sh.H, sh.F)
+            else:
+                self.cache[e] = fp4.record_weights(rec, sh.H, sh.F, float(self.glob[fid]))
         return self.cache[e]
 
 
@@ -45,7 +52,7 @@ def _replay(ft, sh, S, schedule, B_P, B_H, rho, samples, tok_sample=None, seed=0
     pool, glob = hz.pinned_pool(sh, seed)
     pool_np = pool.numpy()
     T_max = max(t for t, _ in schedule)
-    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, S, pool, fmt=ft.FT_FMT_NVFP4, T_max=T_max, nvfp4_global=glob)
+    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, S, pool, fmt=sh.fmt, T_max=T_max, nvfp4_global=glob)
     st = ctl.CacheState.empty(sh.L, sh.E, S)
     step = 0
     done = []
@@ -119,7 +126,7 @@ def _run_prefill_fp4(ft, sh, S, T, check_layers, tok_sample=None, seed=0):
     pool, glob = hz.pinned_pool(sh, seed)
     pool_np = pool.numpy()
     cs, ts = torch.cuda.Stream(), torch.cuda.Stream()
-    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, S, pool, fmt=ft.FT_FMT_NVFP4, T_max=1, T_prefill_max=T,
+    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, S, pool, fmt=sh.fmt, T_max=1, T_prefill_max=T,
                      nvfp4_global=glob, compute_stream=cs.cuda_stream, transfer_stream=ts.cuda_stream)
     xs = [synth.tokens_bf16(seed, 901, l, T, sh.H) for l in range(sh.L)]
     lgs = [synth.iid_logits(seed, (901, l), T, sh.E) for l in range(sh.L)]
@@ -158,3 +165,34 @@ def test_large_nvfp4_prefill(ft):
     """Large NVFP4 prefill: T=4096 through all 8 layers of E=256, H=4096, F=2048."""
     wl = synth.LARGE_NVFP4
     _run_prefill_fp4(ft, wl.shape, wl.S, 4096, [0, 7], tok_sample=[0, 1000, 2047, 3001, 4095])
+
+
+# ------------------------------------------------------------------ MXFP4
+
+@pytest.mark.parametrize("H,F,E,k,S,T", [
+    (256, 512, 16, 4, 12, 3),       # x fp32 in shared memory, 8-byte W_gu scale rows
+    (1024, 512, 16, 4, 24, 9),      # x bf16 in shared memory
+    (1024, 512, 16, 4, 24, 20),     # x from global memory
+    (1024, 2048, 8, 4, 8, 40),      # phase-B items of several token groups
+])
+def test_mxfp4_small(ft, H, F, E, k, S, T):
+    sh = synth.Shape(L=2, E=E, k=k, H=H, F=F, fmt=synth.FMT_MXFP4)
+    samples = {(s, l) for s in range(4) for l in range(2)}
+    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples)
+    assert len(done) == len(samples)
+
+
+def test_mxfp4_prefill_small(ft):
+    sh = synth.Shape(L=2, E=8, k=2, H=256, F=512, fmt=synth.FMT_MXFP4)
+    _run_prefill_fp4(ft, sh, 16, 300, [0, 1])
+
+
+@pytest.mark.slow
+def test_large_mxfp4_decode(ft):
+    """Large shapes with MXFP4 banks: 8 layers, E=256, top-8, H=4096, F=2048,
+    512 slots, 16 steps at T=1 then 8 at T=64, AR(1) rho=0.8."""
+    wl = synth.LARGE_MXFP4
+    samples = {(s, l) for s in (0, 15) for l in (0, 7)} | {(s, l) for s in (16, 23) for l in (0, 7)}
+    done = _replay(ft, wl.shape, wl.S, [(1, 16), (64, 8)], wl.B_P, wl.B_H, wl.rho, samples,
+                   tok_sample=[0, 21, 42, 63])
+    assert len(done) == len(samples)
