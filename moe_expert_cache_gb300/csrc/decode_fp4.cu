@@ -28,31 +28,35 @@
 
 namespace {
 
-constexpr int CW = 8;                 // consumer warps
+constexpr int CW = 16;                // consumer warps
 constexpr int CONS = CW * 32;
 constexpr int FILL_WARPS = 1;         // fused cache fill (one TMA thread)
 constexpr int THREADS = CONS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
 constexpr int FPC = CW;               // features per phase-A chunk
+constexpr int RW = 2;                 // W_d rows per warp pass in phase B
 constexpr size_t HEAD = 256;
-enum { X_F32_SMEM = 0, X_BF16_SMEM = 1, X_BF16_GLOBAL = 2 };
+// Phase-A activations: f16 pairs in shared memory (X_SMEM, when T*H*2 bytes
+// fit) or in a global scratch row block written at the start of the launch
+// (X_GLOBAL).
+enum { X_SMEM = 0, X_GLOBAL = 1 };
+constexpr int kXTarget = 14;  // token rows are scaled so their largest magnitude is in [2^14, 2^15)
 
-// e2m1 decode by bit placement: code j of word w (nibble j, low nibble
-// first) becomes the fp32 whose exponent field holds the code's two exponent
-// bits, whose top mantissa bit holds its mantissa bit and whose sign is its
-// sign.  That float equals value * 2^-126 exactly, for the subnormal code 1
-// (0.5) as well; activations are held scaled by 2^64 (kActScale) so the
-// products stay normal, and the row sums are rescaled by 2^62 (kSumScale).
-// Four integer operations per value instead of a table lookup or a
-// conversion instruction.
-constexpr float kActScale = 18446744073709551616.0f;  // 2^64
-constexpr float kSumScale = 4611686018427387904.0f;   // 2^62
+// e2m1 decode by bit placement, two values at a time: codes J and J + 4 of
+// word w (nibble J, low nibble first) become the two halves of an f16x2
+// whose exponent field holds the code's two exponent bits, whose top
+// mantissa bit holds its mantissa bit and whose sign is its sign.  Each half
+// equals value * 2^-14 exactly (the subnormal code 1, 0.5, included): both
+// nibbles of a pair move by the same shift, so a pair costs two shifts and
+// two masks.  The halves are widened to fp32 exactly and the row sums are
+// rescaled by 2^14 (kValScale).
+constexpr float kValScale = 16384.0f;  // 2^14
 
 template <int J>
-__device__ __forceinline__ float e2m1_scaled(uint32_t w) {
-    const uint32_t mag = (J * 4 <= 22 ? (w << (J * 4 <= 22 ? 22 - 4 * J : 0)) : (w >> (J * 4 > 22 ? 4 * J - 22 : 0))) &
-                         0x01C00000u;
-    const uint32_t sgn = (w << (28 - 4 * J)) & 0x80000000u;
-    return __uint_as_float(mag | sgn);
+__device__ __forceinline__ float2 e2m1x2_scaled(uint32_t w) {
+    const uint32_t mag = (J < 3 ? (w << (J < 3 ? 9 - 4 * J : 0)) : (w >> 3)) & 0x0E000E00u;
+    const uint32_t sgn = (w << (12 - 4 * J)) & 0x80008000u;
+    const uint32_t h = mag | sgn;
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
 // Scale bytes: two e4m3 codes (low byte first) to a float pair, by the
@@ -66,60 +70,144 @@ __device__ __forceinline__ float2 e4m3x2_f32(const uint8_t* p2) {
 // Scales of the 32 values of 16-byte group v of a row whose scale bytes
 // start at `srow`: two e4m3 codes (NVFP4) or one E8M0 code used for both
 // halves (MXFP4).  E8M0 is placed as an IEEE single bit pattern: code c is
-// the exponent field, code 0 the subnormal 2^-127, code 255 NaN.
+// the exponent field; codes 0 and 255 also set the top mantissa bit, which
+// makes code 0 the subnormal 2^-127 and code 255 a NaN.  (t - 1) >> 9 has
+// that bit set exactly when t = (c + 1) & 0xFE is 0, i.e. c is 0 or 255.
+__device__ __forceinline__ float e8m0_f32(uint32_t c) {
+    const uint32_t t = (c + 1u) & 0xFEu;
+    return __uint_as_float((c << 23) | (((t - 1u) >> 9) & 0x00400000u));
+}
+
 template <int SB>
 __device__ __forceinline__ float2 scales32(const uint8_t* srow, int v) {
     if (SB == 16) return e4m3x2_f32(srow + 2 * v);
-    const uint32_t c = srow[v];
-    const float s = __uint_as_float(c == 255u ? 0x7FC00000u : c == 0u ? 0x00400000u : c << 23);
+    const float s = e8m0_f32(srow[v]);
     return make_float2(s, s);
 }
 
-// Activation rows in shared memory (x and the staged h rows) are swizzled so
-// that a warp's loads of its lanes' 32-value groups spread over all banks:
-// within group v (128 bytes of fp32, or 64 bytes of bf16), 16-byte chunk i
-// is stored at chunk (i + v) mod 8 (fp32) or (i + v) mod 4 (bf16).
+// The h rows phase B stages (fp32, shared memory) are swizzled so that a
+// warp's loads of its lanes' 32-value groups spread over all banks: within
+// group v (128 bytes), 16-byte chunk i is stored at chunk (i + v) mod 8.
 __device__ __forceinline__ int swz_f32(int e) {  // element e of a row -> its stored position
     const int v = e >> 5, i = (e >> 2) & 7;
     return (v << 5) | (((i + v) & 7) << 2) | (e & 3);
 }
 
-// 32 activations of token row `xr` starting at element 32*v.
-template <int XM>
-__device__ __forceinline__ void load_x32(const void* xr, int v, float* x) {
-    if (XM == X_F32_SMEM) {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(xr) + (size_t)v * 32);
+// 32 h values of a staged row starting at element 32*v.
+__device__ __forceinline__ void load_h32(const float* hr, int v, float* x) {
+    const float4* p = reinterpret_cast<const float4*>(hr + (size_t)v * 32);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 q = p[(i + v) & 7];
-            x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
-        }
-    } else {
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xr) + (size_t)v * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 q = XM == X_BF16_GLOBAL ? __ldg(p + i) : p[(i + v) & 3];
-            ft::bf16x8_to_f32(q, x + 8 * i);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[8 * i + j] *= kActScale;
-        }
+    for (int i = 0; i < 8; ++i) {
+        const float4 q = p[(i + v) & 7];
+        x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
     }
 }
 
-// eight values of one word against x[0..7] (scaled), added to a / b (even / odd)
-__device__ __forceinline__ void fp4_word(uint32_t w, const float* x, float& a, float& b) {
-    a = fmaf(e2m1_scaled<0>(w), x[0], a);
-    b = fmaf(e2m1_scaled<1>(w), x[1], b);
-    a = fmaf(e2m1_scaled<2>(w), x[2], a);
-    b = fmaf(e2m1_scaled<3>(w), x[3], b);
-    a = fmaf(e2m1_scaled<4>(w), x[4], a);
-    b = fmaf(e2m1_scaled<5>(w), x[5], b);
-    a = fmaf(e2m1_scaled<6>(w), x[6], a);
-    b = fmaf(e2m1_scaled<7>(w), x[7], b);
+// Phase-A activations as f16 pairs, in the order the weight decode produces:
+// for word q of a row (values 8q..8q+7) one 16-byte chunk holds the pairs
+// (x[8q+J], x[8q+J+4]), J = 0..3.  The four chunks of the 32-value group v
+// are stored rotated by v/2 (chunk c at (c + v/2) mod 4), so that the eight
+// lanes of a quarter warp (groups v = lane + 32i) read eight different bank
+// quads.  Token row t is held multiplied by 2^a_t, with a_t chosen from the
+// row's largest magnitude (kXTarget): every scaled value is an exact f16
+// (a bf16 value below 2^15), the products with the decoded weights
+// (value * 2^-14) are at most 6 and a 16-value partial sum at most 96, and
+// values down to 2^-28 of the row's largest stay normal f16.  Returns the
+// row's factor 2^(14 - a_t) that turns its sums (in units of 2^(a_t - 14))
+// back into dot products.
+__device__ __forceinline__ int xpos(int q) {  // word q of a row -> its stored chunk
+    const int v = q >> 2;
+    return (v << 2) | (((q & 3) + (v >> 1)) & 3);
 }
 
-// sum over 32 values of one uint4 (two scale blocks): sc0 * block0 + sc1 * block1,
-// in units of 2^-62 (activations scaled by 2^64, values by 2^-126)
+// The scale exponent a_t of a token row from its largest magnitude:
+// kXTarget - floor(log2 amax), within [-100, 100] (2^a finite); 0 for a
+// zero row, 100 for a row whose largest magnitude is subnormal.
+__device__ __forceinline__ int x_exponent(float amax) {
+    if (!(amax > 0.f)) return 0;
+    if (amax < 1.17549435e-38f) return 100;
+    const int a = kXTarget - ((int)((__float_as_uint(amax) >> 23) & 255u) - 127);
+    return a < -100 ? -100 : (a > 100 ? 100 : a);
+}
+
+// Eight bf16 values (one word's activations) times `up` as the chunk of
+// four f16 pairs (x[J], x[J+4]).
+__device__ __forceinline__ uint4 x_pairs(const uint4& raw, float up) {
+    float f[8];
+    ft::bf16x8_to_f32(raw, f);
+    uint4 c;
+    uint32_t* cw = reinterpret_cast<uint32_t*>(&c);
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+        const __half2 h = __floats2half2_rn(f[J] * up, f[J + 4] * up);
+        cw[J] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return c;
+}
+
+// One warp converts token row `xr` (H bf16 values) into the paired layout
+// at `dst` (H/8 chunks); returns the row factor 2^(14 - a_t) (all lanes).
+__device__ __forceinline__ float stage_x_row(const uint4* xr, int H, uint4* dst, int lane) {
+    float amax = 0.f;
+    for (int q = lane; q < H / 8; q += 32) {
+        float f[8];
+        ft::bf16x8_to_f32(xr[q], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int a = x_exponent(amax);
+    const float up = ldexpf(1.f, a);
+    for (int q = lane; q < H / 8; q += 32) dst[xpos(q)] = x_pairs(xr[q], up);
+    return ldexpf(1.f, 14 - a);
+}
+
+// The four f16x2 weight pairs of one word (value * 2^-14 each), in J order.
+__device__ __forceinline__ void e2m1_word_h2(uint32_t w, uint32_t* d) {
+    d[0] = ((w << 9) & 0x0E000E00u) | ((w << 12) & 0x80008000u);
+    d[1] = ((w << 5) & 0x0E000E00u) | ((w << 8) & 0x80008000u);
+    d[2] = ((w << 1) & 0x0E000E00u) | ((w << 4) & 0x80008000u);
+    d[3] = ((w >> 3) & 0x0E000E00u) | (w & 0x80008000u);
+}
+
+__device__ __forceinline__ __half2 hfma2_u(uint32_t a, uint32_t b, __half2 c) {
+    return __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b), c);
+}
+
+// 16 values (two words, decoded pairs d[0..7]) against their activation
+// chunks x0, x1: the f16 sum of the 16 products, widened to fp32.  Two
+// partial chains of four products per half.
+__device__ __forceinline__ float dot16_h(const uint32_t* d, const uint4& x0, const uint4& x1) {
+    const __half2 z = __float2half2_rn(0.f);
+    __half2 p = hfma2_u(d[0], x0.x, z), q = hfma2_u(d[4], x1.x, z);
+    p = hfma2_u(d[1], x0.y, p);
+    q = hfma2_u(d[5], x1.y, q);
+    p = hfma2_u(d[2], x0.z, p);
+    q = hfma2_u(d[6], x1.z, q);
+    p = hfma2_u(d[3], x0.w, p);
+    q = hfma2_u(d[7], x1.w, q);
+    const float2 f = __half22float2(__hadd2(p, q));
+    return f.x + f.y;
+}
+
+// eight values of one word against x[0..7], added to a (values 0-3) and b
+// (values 4-7), in units of 2^-14
+__device__ __forceinline__ void fp4_word(uint32_t w, const float* x, float& a, float& b) {
+    const float2 v0 = e2m1x2_scaled<0>(w), v1 = e2m1x2_scaled<1>(w);
+    const float2 v2 = e2m1x2_scaled<2>(w), v3 = e2m1x2_scaled<3>(w);
+    a = fmaf(v0.x, x[0], a);
+    b = fmaf(v0.y, x[4], b);
+    a = fmaf(v1.x, x[1], a);
+    b = fmaf(v1.y, x[5], b);
+    a = fmaf(v2.x, x[2], a);
+    b = fmaf(v2.y, x[6], b);
+    a = fmaf(v3.x, x[3], a);
+    b = fmaf(v3.y, x[7], b);
+}
+
+// sum over 32 values of one uint4 (two 16-value halves): sc0 * half0 +
+// sc1 * half1, in units of 2^-14
 __device__ __forceinline__ float fp4_dot32(const uint4& w, const float* x, float sc0, float sc1) {
     float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
     fp4_word(w.x, x, a0, b0);
@@ -130,113 +218,137 @@ __device__ __forceinline__ float fp4_dot32(const uint4& w, const float* x, float
 }
 
 // Phase A: gate and up rows of one feature against NT tokens; returns the
-// un-globalled row sums in ag / au.
+// row sums, in units of each token row's 2^(a_t - 14) and without the
+// expert's global, in ag / au.  `xs` is the paired activation block (H/8
+// chunks per token row).
 template <int NT, int XM, int SB>
 __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
-                                         const void* xs, size_t xrow_elems, const int* tk, int H, int lane,
-                                         float* ag, float* au) {
+                                         const uint4* xs, const int* tk, int H, int lane, float* ag, float* au) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
     const int nv = H >> 5;  // uint4 (32 values) per row
+    const int rq = H >> 3;  // activation chunks per token row
     for (int v = lane; v < nv; v += 32) {
         const uint4 wg = gv[v], wu = uv[v];
-        const float2 gsc2 = scales32<SB>(gs, v), usc2 = scales32<SB>(us, v);
-        const float g0 = gsc2.x, g1 = gsc2.y, u0 = usc2.x, u1 = usc2.y;
+        const float2 gsc = scales32<SB>(gs, v), usc = scales32<SB>(us, v);
+        uint32_t dg[16], du[16];
+        e2m1_word_h2(wg.x, dg);
+        e2m1_word_h2(wg.y, dg + 4);
+        e2m1_word_h2(wg.z, dg + 8);
+        e2m1_word_h2(wg.w, dg + 12);
+        e2m1_word_h2(wu.x, du);
+        e2m1_word_h2(wu.y, du + 4);
+        e2m1_word_h2(wu.z, du + 8);
+        e2m1_word_h2(wu.w, du + 12);
+        const int rot = (v >> 1) & 3;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-            float x[32];
-            const void* xr = XM == X_F32_SMEM
-                                 ? (const void*)(static_cast<const float*>(xs) + (size_t)tk[n] * xrow_elems)
-                                 : (const void*)(static_cast<const __nv_bfloat16*>(xs) + (size_t)tk[n] * xrow_elems);
-            load_x32<XM>(xr, v, x);
-            ag[n] += fp4_dot32(wg, x, g0, g1);
-            au[n] += fp4_dot32(wu, x, u0, u1);
+            const uint4* xr = xs + (size_t)tk[n] * rq + (size_t)v * 4;
+            uint4 xc[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) xc[c] = xr[(c + rot) & 3];
+            ag[n] = fmaf(gsc.x, dot16_h(dg, xc[0], xc[1]), fmaf(gsc.y, dot16_h(dg + 8, xc[2], xc[3]), ag[n]));
+            au[n] = fmaf(usc.x, dot16_h(du, xc[0], xc[1]), fmaf(usc.y, dot16_h(du + 8, xc[2], xc[3]), au[n]));
         }
     }
 }
 
 template <int NT, int XM, int SB>
 __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
-                                          const void* xs, int H, const int* m_tok, int off, int g0, int F, int f,
-                                          int lane, float gsc, float* hbuf) {
+                                          const uint4* xs, const float* xf, int H, const int* m_tok, int off, int g0,
+                                          int F, int f, int lane, float gsc, float* hbuf) {
     int tk[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) tk[n] = m_tok[off + g0 + n];
     float ag[NT], au[NT];
-    gu_dots4<NT, XM, SB>(gv, uv, gs, us, xs, (size_t)H, tk, H, lane, ag, au);
+    gu_dots4<NT, XM, SB>(gv, uv, gs, us, xs, tk, H, lane, ag, au);
     float mine = 0.f;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-        const float sg = ft::warp_sum(ag[n]) * kSumScale * gsc;
-        const float su = ft::warp_sum(au[n]) * kSumScale * gsc;
+        const float rs = xf[tk[n]] * gsc;
+        const float sg = ft::warp_sum(ag[n]) * rs;
+        const float su = ft::warp_sum(au[n]) * rs;
         if (lane == n) mine = ft::silu_mul(sg, su);
     }
-    // read only by phase B, as staged rows: scaled and swizzled like x
-    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + swz_f32(f)] = mine * kActScale;
+    // read only by phase B, as staged rows: swizzled like x
+    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + swz_f32(f)] = mine;
 }
 
 template <int XM, int SB>
-__device__ __forceinline__ void gu_feature4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
-                                            const void* xs, int H, const int* m_tok, int off, int ntok, int F, int f,
-                                            int lane, float gsc, float* hbuf) {
+__device__ __noinline__ void gu_feature4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
+                                            const uint4* xs, const float* xf, int H, const int* m_tok, int off,
+                                            int ntok, int F, int f, int lane, float gsc, float* hbuf) {
     int g0 = 0;
     while (g0 < ntok) {
         const int rem = ntok - g0;
-        if (rem >= 4) {
-            gu_group4<4, XM, SB>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
-            g0 += 4;
-        } else if (rem >= 2) {
-            gu_group4<2, XM, SB>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
+        if (rem >= 2) {
+            gu_group4<2, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 2;
         } else {
-            gu_group4<1, XM, SB>(gv, uv, gs, us, xs, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
+            gu_group4<1, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 1;
         }
     }
 }
 
-// Phase B: one W_d row (values + scales) against NT staged h rows (fp32).
+// Phase B: the W_d rows rb + CW*r (r < 4, row < R) of a slot (values +
+// scales) against NT staged h rows (fp32).  Each h chunk is loaded once and
+// applied to every row of the warp, which also gives independent
+// accumulation chains.
 template <int NT, int SB>
-__device__ __forceinline__ void down_group4(const uint4* wv, const uint8_t* ws, const float* hs, int g, int F,
-                                            int lane, float gsc, float* o_s, int obase, int RMAX,
-                                            int rl) {
-    float acc[NT];
+__device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
+                                            unsigned dsrow, const float* hs, int g, int F, int lane, float gsc,
+                                            float* o_s, int obase, int RMAX, int rb, int R) {
+    float acc[RW][NT];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n] = 0.f;
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[r][n] = 0.f;
     const int nv = F >> 5;
     for (int v = lane; v < nv; v += 32) {
-        const uint4 w = wv[v];
-        const float2 sc2 = scales32<SB>(ws, v);
-        const float s0 = sc2.x, s1 = sc2.y;
+        uint4 w[RW];
+        float2 sc[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            const int rl = rb + CW * r < R ? rb + CW * r : rb;  // rows past R repeat row rb (not stored)
+            w[r] = reinterpret_cast<const uint4*>(wrows + (size_t)rl * dvrow)[v];
+            sc[r] = scales32<SB>(srows + (size_t)rl * dsrow, v);
+        }
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             float x[32];
-            load_x32<X_F32_SMEM>(hs + (size_t)(g + n) * F, v, x);
-            acc[n] += fp4_dot32(w, x, s0, s1);
+            load_h32(hs + (size_t)(g + n) * F, v, x);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) acc[r][n] += fp4_dot32(w[r], x, sc[r].x, sc[r].y);
         }
     }
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-        const float sv = ft::warp_sum(acc[n]) * kSumScale * gsc;
-        if (lane == 0) o_s[(size_t)(obase + g + n) * RMAX + rl] = sv;
+    for (int r = 0; r < RW; ++r) {
+        const int rl = rb + CW * r;
+        if (rl < R) {  // warp-uniform
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const float sv = ft::warp_sum(acc[r][n]) * kValScale * gsc;
+                if (lane == 0) o_s[(size_t)(obase + g + n) * RMAX + rl] = sv;
+            }
+        }
     }
 }
 
+// The rows rb + CW*r (r < 4) of a slot against its ng staged h rows, two
+// tokens at a time (four rows by four tokens would not fit the registers).
 template <int SB>
-__device__ __forceinline__ void down_row4(const uint4* wv, const uint8_t* ws, const float* hs, int ng, int F,
-                                          int lane, float gsc, float* o_s, int obase, int RMAX,
-                                          int rl) {
+__device__ __noinline__ void down_rows4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
+                                           unsigned dsrow, const float* hs, int ng, int F, int lane, float gsc,
+                                           float* o_s, int obase, int RMAX, int rb, int R) {
     int g = 0;
     while (g < ng) {
         const int rem = ng - g;
-        if (rem >= 4) {
-            down_group4<4, SB>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
-            g += 4;
-        } else if (rem >= 2) {
-            down_group4<2, SB>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
+        if (rem >= 2) {
+            down_group4<2, SB>(wrows, srows, dvrow, dsrow, hs, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
             g += 2;
         } else {
-            down_group4<1, SB>(wv, ws, hs, g, F, lane, gsc, o_s, obase, RMAX, rl);
+            down_group4<1, SB>(wrows, srows, dvrow, dsrow, hs, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
             g += 1;
         }
     }
@@ -272,8 +384,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + nst;
     size_t o = HEAD;
-    void* x_s = smem + o;
-    if (XM != X_BF16_GLOBAL) o += ((size_t)T * H * (XM == X_F32_SMEM ? 4 : 2) + 127) & ~(size_t)127;
+    uint4* x_s = reinterpret_cast<uint4*>(smem + o);  // paired activations (X_SMEM)
+    if (XM == X_SMEM) o += ((size_t)T * H * 2 + 127) & ~(size_t)127;
     float* o_s = reinterpret_cast<float*>(smem + o);
     o += ((size_t)TK * RMAX * 4 + 127) & ~(size_t)127;
     int* m_off = reinterpret_cast<int*>(smem + o);
@@ -283,10 +395,11 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     int* m_pos = reinterpret_cast<int*>(m_gate + TK);
     float* m_gs = reinterpret_cast<float*>(m_pos + TK);   // global scale of each entry
     int* m_fill = reinterpret_cast<int*>(m_gs + TK);      // fill index of each entry (or -1)
-    o += ((size_t)(7 * TK + 1) * 4 + 127) & ~(size_t)127;
+    float* xf = reinterpret_cast<float*>(m_fill + TK);    // row factor 2^(14 - a_t) of each token
+    o += ((size_t)(7 * TK + 1 + T) * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
     const unsigned wpart = ((unsigned)RMAX * (dvrow + dsrow) + 127u) & ~127u;
-    const void* xsrc = XM == X_BF16_GLOBAL ? static_cast<const void*>(p.x) : x_s;
+    const uint4* xsrc = XM == X_GLOBAL ? p.x16 : x_s;
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -307,25 +420,45 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         m_gate[i] = p.as_gate[i];
     }
     for (int i = tid; i < TK; i += THREADS) m_pos[i] = p.out_pos[i];
-    if (XM == X_F32_SMEM) {
-        for (int i = tid; i < T * H / 8; i += THREADS) {
-            float f8[8];
-            ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
-            for (int j = 0; j < 8; ++j) f8[j] *= kActScale;
-            const int t = (8 * i) / H, e = 8 * i - t * H;  // 8 values from element e of token t
-            float* row = static_cast<float*>(x_s) + (size_t)t * H;
-            *reinterpret_cast<float4*>(row + swz_f32(e)) = make_float4(f8[0], f8[1], f8[2], f8[3]);
-            *reinterpret_cast<float4*>(row + swz_f32(e + 4)) = make_float4(f8[4], f8[5], f8[6], f8[7]);
+    // paired, scaled activations: in shared memory by every CTA, or one
+    // token row per warp across the grid into the global block, then a grid
+    // barrier
+    const uint4* xin = reinterpret_cast<const uint4*>(p.x);
+    if (XM == X_SMEM) {
+        // all threads: per-token maxima (shared atomics on the magnitudes'
+        // bits, which order like the values), then the scaled pairs
+        unsigned* amax_bits = reinterpret_cast<unsigned*>(xf);
+        for (int t = tid; t < T; t += THREADS) amax_bits[t] = 0u;
+        __syncthreads();
+        const int qrow = H / 8;
+        for (int i = tid; i < T * qrow; i += THREADS) {
+            float f[8];
+            ft::bf16x8_to_f32(xin[i], f);
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+            atomicMax(&amax_bits[i / qrow], __float_as_uint(m));
         }
-    } else if (XM == X_BF16_SMEM) {
-        for (int i = tid; i < T * H / 8; i += THREADS) {
-            const int t = (8 * i) / H, e = 8 * i - t * H;  // 8 values from element e of token t
-            const int v = e >> 5, c = (e >> 3) & 3;
-            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(x_s) + (size_t)t * H + 32 * v)[(c + v) & 3] =
-                reinterpret_cast<const uint4*>(p.x)[i];
+        __syncthreads();
+        for (int i = tid; i < T * qrow; i += THREADS) {
+            const int t = i / qrow, q = i - t * qrow;
+            const int a = x_exponent(__uint_as_float(amax_bits[t]));
+            x_s[(size_t)t * qrow + xpos(q)] = x_pairs(xin[i], ldexpf(1.f, a));
         }
+        __syncthreads();
+        for (int t = tid; t < T; t += THREADS) xf[t] = ldexpf(1.f, 14 - x_exponent(__uint_as_float(amax_bits[t])));
+        __syncthreads();
+    } else {
+        for (int t = c + G * wid; t < T; t += G * (THREADS / 32)) {
+            const float fct = stage_x_row(xin + (size_t)t * (H / 8), H, p.x16 + (size_t)t * (H / 8), lane);
+            if (lane == 0) p.xsc[t] = fct;
+        }
+        __syncthreads();
+        if (tid == 0) ft::grid_barrier(p.gbar, (unsigned)G, p.err);
+        __syncthreads();
+        for (int t = tid; t < T; t += THREADS) xf[t] = p.xsc[t];
+        __syncthreads();
     }
-    __syncthreads();
 
     // --------------------------------------------------------- fused fill
     if (wid > CW) {
@@ -340,11 +473,23 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     if (wid == CW) {
         if (lane == 0) {
             const uint64_t pol = ft::l2_policy_evict_first();
+            // this CTA's W_d rows (values and scales) of the resident entries
+            // go to L2 once the ring is primed, so phase B reads them from L2
+            auto prefetch_wd = [&]() {
+                if (R == 0) return;
+                for (int e = 0; e < ugpu; ++e) {
+                    if (m_fill[e] >= 0) continue;
+                    const uint8_t* rec = p.slot_pool + (size_t)m_slot[e] * p.rb;
+                    ft::bulk_prefetch_l2(rec + VGU + (size_t)r0 * dvrow, (unsigned)R * dvrow);
+                    ft::bulk_prefetch_l2(rec + VGU + VD + SGU + (size_t)r0 * dsrow, (unsigned)R * dsrow);
+                }
+            };
             int it = 0;
             bool ok = true;
             int waited = -1;
             for (int a = c; a < NA && ok; a += G, ++it) {
                 const int st = it % nst;
+                if (it == nst) prefetch_wd();
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
                 const int ent = a / cpe;
                 if (m_fill[ent] >= 0 && m_fill[ent] != waited) {
@@ -362,6 +507,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 ft::bulk_g2s_hint(dst + 2 * FPC * vrow + FPC * srow, rec + VGU + VD + (size_t)(grow + 16) * srow,
                                   FPC * srow, &full[st], pol);
             }
+            if (it <= nst && ok) prefetch_wd();
             // phase B items = (expert, group of <= TG tokens); W_d rows stream
             // ahead of the grid barrier, h rows after it
             int nitems = 0;
@@ -438,7 +584,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         const uint4* uv = reinterpret_cast<const uint4*>(sb + (size_t)(FPC + wid) * vrow);
         const uint8_t* gs = sb + 2 * FPC * vrow + (size_t)wid * srow;
         const uint8_t* us = sb + 2 * FPC * vrow + FPC * srow + (size_t)wid * srow;
-        if (ok) gu_feature4<XM, SB>(gv, uv, gs, us, xsrc, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf);
+        if (ok) gu_feature4<XM, SB>(gv, uv, gs, us, xsrc, xf, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf);
         __syncwarp();
         if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
     }
@@ -461,10 +607,9 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 failed = !ok;
                 const unsigned char* sb = ring + (size_t)st * slot_bytes;
                 const float* hs = reinterpret_cast<const float*>(sb + wpart);
-                for (int rl = wid; rl < R && ok; rl += CW)
-                    down_row4<SB>(reinterpret_cast<const uint4*>(sb + (size_t)rl * dvrow),
-                              sb + (size_t)RMAX * dvrow + (size_t)rl * dsrow, hs, ng, F, lane, m_gs[e], o_s,
-                              off + g0, RMAX, rl);
+                for (int rb = wid; rb < R && ok; rb += RW * CW)
+                    down_rows4<SB>(sb, sb + (size_t)RMAX * dvrow, dvrow, dsrow, hs, ng, F, lane, m_gs[e], o_s,
+                                   off + g0, RMAX, rb, R);
                 __syncwarp();
                 if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
             }
@@ -494,18 +639,11 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStre
     const int G = num_sms;
     const int RMAX = (p.H + G - 1) / G;
     const size_t TK = (size_t)p.T * p.k;
-    int xm = X_F32_SMEM;
-    size_t xbytes = (size_t)p.T * p.H * 4;
-    if (xbytes > 32768) {
-        xm = X_BF16_SMEM;
-        xbytes = (size_t)p.T * p.H * 2;
-        if (xbytes > 32768) {
-            xm = X_BF16_GLOBAL;
-            xbytes = 0;
-        }
-    }
+    const int xm = (size_t)p.T * p.H * 2 <= 32768 ? X_SMEM : X_GLOBAL;
+    const size_t xbytes = xm == X_SMEM ? (size_t)p.T * p.H * 2 : 0;
+    if (xm == X_GLOBAL && (!p.x16 || !p.xsc)) return cudaErrorInvalidValue;
     const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127) +
-                        (((7 * TK + 1) * 4 + 127) & ~(size_t)127);
+                        (((7 * TK + 1 + p.T) * 4 + 127) & ~(size_t)127);
     const size_t chunk = (size_t)2 * FPC * (p.H / 2 + p.H / SB);
     const size_t wpart = ((size_t)RMAX * (p.F / 2 + p.F / SB) + 127) & ~(size_t)127;
     if (head + 2 * chunk > kSmemLimit4) return cudaErrorInvalidValue;
@@ -532,17 +670,12 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStre
     p.fill_chunk = (unsigned)fch;
     p.fill_slots = nf;
     const size_t smem = head + slot * nst + (size_t)nf * fch;
-    const void* fn;
-    if (SB == 16)
-        fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM, 16>
-             : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM, 16>
-                                 : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL, 16>;
-    else
-        fn = xm == X_F32_SMEM    ? (const void*)expert_ffn_fp4_kernel<X_F32_SMEM, 32>
-             : xm == X_BF16_SMEM ? (const void*)expert_ffn_fp4_kernel<X_BF16_SMEM, 32>
-                                 : (const void*)expert_ffn_fp4_kernel<X_BF16_GLOBAL, 32>;
-    static size_t smem_set[6] = {0, 0, 0, 0, 0, 0};  // per kernel variant: set only when it grows
-    const int var = xm + (SB == 32 ? 3 : 0);
+    const void* fn = SB == 16 ? (xm == X_SMEM ? (const void*)expert_ffn_fp4_kernel<X_SMEM, 16>
+                                              : (const void*)expert_ffn_fp4_kernel<X_GLOBAL, 16>)
+                              : (xm == X_SMEM ? (const void*)expert_ffn_fp4_kernel<X_SMEM, 32>
+                                              : (const void*)expert_ffn_fp4_kernel<X_GLOBAL, 32>);
+    static size_t smem_set[4] = {0, 0, 0, 0};  // per kernel variant: set only when it grows
+    const int var = xm + (SB == 32 ? 2 : 0);
     if (smem > smem_set[var]) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -399,6 +399,8 @@ struct ExpertParams {
     int fill_fpf;             // BF16: features per fused-fill unit
     int fill_nks;             // BF16: K segments per fused-fill unit
     const float* gscale;      // [L*E] FP4 per-expert fp32 global (all 1 for MXFP4), or null
+    uint4* x16;               // FP4 decode scratch: T_max x H activations as scaled f16 pairs
+    float* xsc;               // FP4 decode scratch: T_max row factors
     int tgroup;               // NVFP4: tokens per phase-B item
     int nstage;               // pipeline depth (stages in shared memory)
     unsigned stage_bytes;     // bytes of one stage
