@@ -32,7 +32,7 @@ constexpr int CW = 16;                // consumer warps
 constexpr int CONS = CW * 32;
 constexpr int FILL_WARPS = 1;         // fused cache fill (one TMA thread)
 constexpr int THREADS = CONS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
-constexpr int FPC = CW;               // features per phase-A chunk
+constexpr int FPC = CW;               // features per phase-A chunk: one per consumer warp
 constexpr int RW = 2;                 // W_d rows per warp pass in phase B
 constexpr size_t HEAD = 256;
 // Phase-A activations: f16 pairs in shared memory (X_SMEM, when T*H*2 bytes
@@ -256,7 +256,7 @@ __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const
 template <int NT, int XM, int SB>
 __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                           const uint4* xs, const float* xf, int H, const int* m_tok, int off, int g0,
-                                          int F, int f, int lane, float gsc, float* hbuf) {
+                                          int F, int f, int lane, float gsc, float* hbuf, unsigned* hmx) {
     int tk[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) tk[n] = m_tok[off + g0 + n];
@@ -270,56 +270,71 @@ __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, cons
         const float su = ft::warp_sum(au[n]) * rs;
         if (lane == n) mine = ft::silu_mul(sg, su);
     }
-    // read only by phase B, as staged rows: swizzled like x
-    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + swz_f32(f)] = mine;
+    // read only by phase B, as staged rows: swizzled for its fp32 loads; the
+    // token's largest |h| of this CTA is kept for phase B's scaling
+    if (lane < NT) {
+        hbuf[(size_t)(off + g0 + lane) * F + swz_f32(f)] = mine;
+        atomicMax(&hmx[tk[lane]], __float_as_uint(fabsf(mine)));
+    }
 }
 
 template <int XM, int SB>
 __device__ __noinline__ void gu_feature4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                             const uint4* xs, const float* xf, int H, const int* m_tok, int off,
-                                            int ntok, int F, int f, int lane, float gsc, float* hbuf) {
+                                            int ntok, int F, int f, int lane, float gsc, float* hbuf,
+                                            unsigned* hmx) {
     int g0 = 0;
     while (g0 < ntok) {
         const int rem = ntok - g0;
         if (rem >= 2) {
-            gu_group4<2, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
+            gu_group4<2, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf, hmx);
             g0 += 2;
         } else {
-            gu_group4<1, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
+            gu_group4<1, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf, hmx);
             g0 += 1;
         }
     }
 }
 
-// Phase B: the W_d rows rb + CW*r (r < 4, row < R) of a slot (values +
-// scales) against NT staged h rows (fp32).  Each h chunk is loaded once and
-// applied to every row of the warp, which also gives independent
-// accumulation chains.
+// Phase B: the W_d rows rb + CW*r (r < RW, row < R) of a slot (values +
+// scales) against NT h rows held as scaled f16 pairs (the layout of the
+// phase-A activations, F/8 chunks per row; row factors hf).  Each h chunk is
+// loaded once and applied to every row of the warp.
 template <int NT, int SB>
 __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
-                                            unsigned dsrow, const float* hs, int g, int F, int lane, float gsc,
-                                            float* o_s, int obase, int RMAX, int rb, int R) {
+                                            unsigned dsrow, const uint4* hp, const float* hfr, int g, int F,
+                                            int lane, float gsc, float* o_s, int obase, int RMAX, int rb, int R) {
     float acc[RW][NT];
 #pragma unroll
     for (int r = 0; r < RW; ++r)
 #pragma unroll
         for (int n = 0; n < NT; ++n) acc[r][n] = 0.f;
     const int nv = F >> 5;
+    const int rq = F >> 3;
     for (int v = lane; v < nv; v += 32) {
-        uint4 w[RW];
+        uint32_t d[RW][16];
         float2 sc[RW];
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
             const int rl = rb + CW * r < R ? rb + CW * r : rb;  // rows past R repeat row rb (not stored)
-            w[r] = reinterpret_cast<const uint4*>(wrows + (size_t)rl * dvrow)[v];
+            const uint4 w = reinterpret_cast<const uint4*>(wrows + (size_t)rl * dvrow)[v];
             sc[r] = scales32<SB>(srows + (size_t)rl * dsrow, v);
+            e2m1_word_h2(w.x, d[r]);
+            e2m1_word_h2(w.y, d[r] + 4);
+            e2m1_word_h2(w.z, d[r] + 8);
+            e2m1_word_h2(w.w, d[r] + 12);
         }
+        const int rot = (v >> 1) & 3;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-            float x[32];
-            load_h32(hs + (size_t)(g + n) * F, v, x);
+            const uint4* hr = hp + (size_t)(g + n) * rq + (size_t)v * 4;
+            uint4 hc[4];
 #pragma unroll
-            for (int r = 0; r < RW; ++r) acc[r][n] += fp4_dot32(w[r], x, sc[r].x, sc[r].y);
+            for (int c = 0; c < 4; ++c) hc[c] = hr[(c + rot) & 3];
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+                acc[r][n] = fmaf(sc[r].x, dot16_h(d[r], hc[0], hc[1]),
+                                 fmaf(sc[r].y, dot16_h(d[r] + 8, hc[2], hc[3]), acc[r][n]));
         }
     }
 #pragma unroll
@@ -328,30 +343,43 @@ __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t*
         if (rl < R) {  // warp-uniform
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                const float sv = ft::warp_sum(acc[r][n]) * kValScale * gsc;
+                const float sv = ft::warp_sum(acc[r][n]) * hfr[g + n] * gsc;
                 if (lane == 0) o_s[(size_t)(obase + g + n) * RMAX + rl] = sv;
             }
         }
     }
 }
 
-// The rows rb + CW*r (r < 4) of a slot against its ng staged h rows, two
-// tokens at a time (four rows by four tokens would not fit the registers).
+// The rows rb + CW*r (r < RW) of a slot against its ng h rows, two tokens
+// at a time.
 template <int SB>
 __device__ __noinline__ void down_rows4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
-                                           unsigned dsrow, const float* hs, int ng, int F, int lane, float gsc,
-                                           float* o_s, int obase, int RMAX, int rb, int R) {
+                                        unsigned dsrow, const uint4* hp, const float* hfr, int ng, int F, int lane,
+                                        float gsc, float* o_s, int obase, int RMAX, int rb, int R) {
     int g = 0;
     while (g < ng) {
-        const int rem = ng - g;
-        if (rem >= 2) {
-            down_group4<2, SB>(wrows, srows, dvrow, dsrow, hs, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
+        if (ng - g >= 2) {
+            down_group4<2, SB>(wrows, srows, dvrow, dsrow, hp, hfr, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
             g += 2;
         } else {
-            down_group4<1, SB>(wrows, srows, dvrow, dsrow, hs, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
+            down_group4<1, SB>(wrows, srows, dvrow, dsrow, hp, hfr, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
             g += 1;
         }
     }
+}
+
+// Eight fp32 values (h elements 8q..8q+7 of a staged row, swizzled as
+// swz_f32) times `up` as the chunk of four f16 pairs (h[J], h[J+4]).
+__device__ __forceinline__ uint4 h_pairs(const float* hr, int q, float up) {
+    const float4 lo = *reinterpret_cast<const float4*>(hr + swz_f32(8 * q));
+    const float4 hi = *reinterpret_cast<const float4*>(hr + swz_f32(8 * q + 4));
+    uint4 c;
+    __half2 t;
+    t = __floats2half2_rn(lo.x * up, hi.x * up); c.x = *reinterpret_cast<const uint32_t*>(&t);
+    t = __floats2half2_rn(lo.y * up, hi.y * up); c.y = *reinterpret_cast<const uint32_t*>(&t);
+    t = __floats2half2_rn(lo.z * up, hi.z * up); c.z = *reinterpret_cast<const uint32_t*>(&t);
+    t = __floats2half2_rn(lo.w * up, hi.w * up); c.w = *reinterpret_cast<const uint32_t*>(&t);
+    return c;
 }
 
 }  // namespace
@@ -362,6 +390,7 @@ template <int XM, int SB>
 __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_gdone;
+    __shared__ unsigned s_gen;  // grid barrier generation at the start of phase A
     const int H = p.H, F = p.F, T = p.T, k = p.k, TG = p.tgroup;
     const int nst = p.nstage;
     const unsigned slot_bytes = p.stage_bytes;
@@ -396,7 +425,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     float* m_gs = reinterpret_cast<float*>(m_pos + TK);   // global scale of each entry
     int* m_fill = reinterpret_cast<int*>(m_gs + TK);      // fill index of each entry (or -1)
     float* xf = reinterpret_cast<float*>(m_fill + TK);    // row factor 2^(14 - a_t) of each token
-    o += ((size_t)(7 * TK + 1 + T) * 4 + 127) & ~(size_t)127;
+    unsigned* hmx = reinterpret_cast<unsigned*>(xf + T);  // largest |h| of each token (this CTA, then all)
+    float* hup = reinterpret_cast<float*>(hmx + T);       // h scale 2^b_t of each token
+    float* hfr = hup + T;                                 // h row factor 2^(14 - b_t) of each staged row
+    o += ((size_t)(7 * TK + 1 + 3 * T + 2 * TG) * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
     const unsigned wpart = ((unsigned)RMAX * (dvrow + dsrow) + 127u) & ~127u;
     const uint4* xsrc = XM == X_GLOBAL ? p.x16 : x_s;
@@ -420,6 +452,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         m_gate[i] = p.as_gate[i];
     }
     for (int i = tid; i < TK; i += THREADS) m_pos[i] = p.out_pos[i];
+    for (int i = tid; i < T; i += THREADS) hmx[i] = 0u;
     // paired, scaled activations: in shared memory by every CTA, or one
     // token row per warp across the grid into the global block, then a grid
     // barrier
@@ -459,6 +492,9 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         for (int t = tid; t < T; t += THREADS) xf[t] = p.xsc[t];
         __syncthreads();
     }
+
+    if (tid == 0) s_gen = ft::ld_acquire_gpu(&p.gbar[1]);  // no grid barrier can pass before phase A ends
+    __syncthreads();
 
     // --------------------------------------------------------- fused fill
     if (wid > CW) {
@@ -584,15 +620,29 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         const uint4* uv = reinterpret_cast<const uint4*>(sb + (size_t)(FPC + wid) * vrow);
         const uint8_t* gs = sb + 2 * FPC * vrow + (size_t)wid * srow;
         const uint8_t* us = sb + 2 * FPC * vrow + FPC * srow + (size_t)wid * srow;
-        if (ok) gu_feature4<XM, SB>(gv, uv, gs, us, xsrc, xf, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf);
+        if (ok)
+            gu_feature4<XM, SB>(gv, uv, gs, us, xsrc, xf, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf, hmx);
         __syncwarp();
         if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
     }
 
+    // per-token |h| maxima of the grid, tagged with the barrier generation of
+    // this launch in the high word (older values lose every comparison)
+    ft::named_bar_sync(1, CONS);
+    const unsigned long long gen = (unsigned long long)s_gen << 32;
+    for (int t = tid; t < T; t += CONS)
+        atomicMax(reinterpret_cast<unsigned long long*>(p.hmax) + t, gen | hmx[t]);
     ft::named_bar_sync(1, CONS);
     if (tid == 0) {
         ft::grid_barrier(p.gbar, (unsigned)G, p.err);
         ft::st_release_cta(&s_gdone, 1);
+    }
+    ft::named_bar_sync(1, CONS);
+    for (int t = tid; t < T; t += CONS) {
+        const unsigned long long v = reinterpret_cast<const unsigned long long*>(p.hmax)[t];
+        const int b = x_exponent((v >> 32) == (gen >> 32) ? __uint_as_float((unsigned)v) : 0.f);
+        hup[t] = ldexpf(1.f, b);
+        xf[t] = ldexpf(1.f, 14 - b);  // phase A is done with the x factors
     }
     ft::named_bar_sync(1, CONS);
 
@@ -607,9 +657,24 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 failed = !ok;
                 const unsigned char* sb = ring + (size_t)st * slot_bytes;
                 const float* hs = reinterpret_cast<const float*>(sb + wpart);
+                // the staged h rows as scaled f16 pairs, written by every
+                // consumer thread into the slot's tail (past the W_d rows and
+                // the fp32 rows the copy lands), then one barrier; warps whose
+                // wait failed still take the barrier.  Consecutive items use
+                // different slots, and a slot's tail is rewritten only after
+                // every warp has passed the barrier of the item before.
+                uint4* hp = reinterpret_cast<uint4*>(ring + (size_t)st * slot_bytes + wpart + (size_t)TG * F * 4);
+                if (ok) {
+                    for (int i = tid; i < ng * (F / 8); i += CONS) {
+                        const int n = i / (F / 8), q = i - n * (F / 8);
+                        hp[(size_t)n * (F / 8) + xpos(q)] = h_pairs(hs + (size_t)n * F, q, hup[m_tok[off + g0 + n]]);
+                    }
+                    if (tid < ng) hfr[(it & 1) * TG + tid] = xf[m_tok[off + g0 + tid]];
+                }
+                ft::named_bar_sync(2, CONS);
                 for (int rb = wid; rb < R && ok; rb += RW * CW)
-                    down_rows4<SB>(sb, sb + (size_t)RMAX * dvrow, dvrow, dsrow, hs, ng, F, lane, m_gs[e], o_s,
-                                   off + g0, RMAX, rb, R);
+                    down_rows4<SB>(sb, sb + (size_t)RMAX * dvrow, dvrow, dsrow, hp, hfr + (it & 1) * TG, ng, F,
+                                   lane, m_gs[e], o_s, off + g0, RMAX, rb, R);
                 __syncwarp();
                 if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
             }
@@ -642,24 +707,24 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStre
     const int xm = (size_t)p.T * p.H * 2 <= 32768 ? X_SMEM : X_GLOBAL;
     const size_t xbytes = xm == X_SMEM ? (size_t)p.T * p.H * 2 : 0;
     if (xm == X_GLOBAL && (!p.x16 || !p.xsc)) return cudaErrorInvalidValue;
-    const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127) +
-                        (((7 * TK + 1 + p.T) * 4 + 127) & ~(size_t)127);
+    const size_t head0 = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127);
     const size_t chunk = (size_t)2 * FPC * (p.H / 2 + p.H / SB);
     const size_t wpart = ((size_t)RMAX * (p.F / 2 + p.F / SB) + 127) & ~(size_t)127;
-    if (head + 2 * chunk > kSmemLimit4) return cudaErrorInvalidValue;
-    // token group of phase B: as many h rows as fit next to the W_d rows in a
-    // slot when two slots fill the shared memory
-    int tg = (int)(((kSmemLimit4 - head - 16384) / 2 - wpart) / ((size_t)p.F * 4));
-    if (tg > p.T) tg = p.T;
-    if (tg > 16) tg = 16;
-    if (tg < 1) return cudaErrorInvalidValue;
-    size_t slot = wpart + (size_t)tg * p.F * 4;
-    if (slot < chunk) slot = chunk;
-    slot = (slot + 127) & ~(size_t)127;
     // The fill ring is kept small (3 x 4 KiB per SM): host reads queued beyond
     // the link's bandwidth-delay product delay every SM's HBM reads.
     const size_t fch = 4096;
-    if (head + 2 * fch + 2 * slot > kSmemLimit4) return cudaErrorInvalidValue;
+    // token group of phase B: the most h rows (at most 16) whose staging in a
+    // slot (fp32 as copied, then f16 pairs) leaves room for two slots
+    int tg = p.T < 16 ? p.T : 16;
+    size_t head = 0, slot = 0;
+    for (; tg >= 1; --tg) {
+        head = head0 + (((7 * TK + 1 + 3 * (size_t)p.T + 2 * (size_t)tg) * 4 + 127) & ~(size_t)127);
+        slot = wpart + (size_t)tg * p.F * 6;
+        if (slot < chunk) slot = chunk;
+        slot = (slot + 127) & ~(size_t)127;
+        if (head + 2 * fch + 2 * slot <= kSmemLimit4) break;
+    }
+    if (tg < 1) return cudaErrorInvalidValue;
     int nst = (int)((kSmemLimit4 - head - 2 * fch) / slot);
     if (nst > 4) nst = 4;
     p.nstage = nst;

@@ -401,6 +401,7 @@ struct ExpertParams {
     const float* gscale;      // [L*E] FP4 per-expert fp32 global (all 1 for MXFP4), or null
     uint4* x16;               // FP4 decode scratch: T_max x H activations as scaled f16 pairs
     float* xsc;               // FP4 decode scratch: T_max row factors
+    unsigned long long* hmax; // FP4 decode scratch: T_max per-token |h| maxima, tagged (zeroed at init)
     int tgroup;               // NVFP4: tokens per phase-B item
     int nstage;               // pipeline depth (stages in shared memory)
     unsigned stage_bytes;     // bytes of one stage

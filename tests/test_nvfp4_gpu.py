@@ -46,10 +46,29 @@ class FP4Weights:
         return self.cache[e]
 
 
-def _replay(ft, sh, S, schedule, B_P, B_H, rho, samples, tok_sample=None, seed=0):
+def _repeated_pool(sh, seed, distinct):
+    """Pinned pool whose records are the encodings of `distinct` drawn
+    experts of layer 0, repeated over every (layer, expert) (valid records,
+    generated in a fraction of the time)."""
+    import torch
+    rb = sh.record_bytes
+    pool = torch.empty(sh.L * sh.E * rb, dtype=torch.uint8, pin_memory=True)
+    pn = pool.numpy()
+    enc = synth.record_mxfp4 if sh.fmt == synth.FMT_MXFP4 else (lambda *a: synth.record_nvfp4(*a)[0])
+    recs = [enc(seed, 0, e, sh.H, sh.F) for e in range(distinct)]
+    for fid in range(sh.L * sh.E):
+        pn[fid * rb:(fid + 1) * rb] = recs[fid % distinct]
+    glob = None
+    if sh.fmt == synth.FMT_NVFP4:
+        g = [synth.record_nvfp4(seed, 0, e, sh.H, sh.F)[1] for e in range(distinct)]
+        glob = np.array([g[fid % distinct] for fid in range(sh.L * sh.E)], dtype=np.float32)
+    return pool, glob
+
+
+def _replay(ft, sh, S, schedule, B_P, B_H, rho, samples, tok_sample=None, seed=0, distinct=None):
     """schedule: list of (T, steps).  Every call bit-exact; sampled calls numerically."""
     import torch
-    pool, glob = hz.pinned_pool(sh, seed)
+    pool, glob = _repeated_pool(sh, seed, distinct) if distinct else hz.pinned_pool(sh, seed)
     pool_np = pool.numpy()
     T_max = max(t for t, _ in schedule)
     ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, S, pool, fmt=sh.fmt, T_max=T_max, nvfp4_global=glob)
@@ -190,9 +209,11 @@ def test_mxfp4_prefill_small(ft):
 @pytest.mark.slow
 def test_large_mxfp4_decode(ft):
     """Large shapes with MXFP4 banks: 8 layers, E=256, top-8, H=4096, F=2048,
-    512 slots, 16 steps at T=1 then 8 at T=64, AR(1) rho=0.8."""
+    512 slots, 16 steps at T=1 then 8 at T=64, AR(1) rho=0.8.  The pool
+    repeats the records of 16 drawn experts (routing and parity do not
+    depend on the values being distinct)."""
     wl = synth.LARGE_MXFP4
     samples = {(s, l) for s in (0, 15) for l in (0, 7)} | {(s, l) for s in (16, 23) for l in (0, 7)}
     done = _replay(ft, wl.shape, wl.S, [(1, 16), (64, 8)], wl.B_P, wl.B_H, wl.rho, samples,
-                   tok_sample=[0, 21, 42, 63])
+                   tok_sample=[0, 21, 42, 63], distinct=16)
     assert len(done) == len(samples)
