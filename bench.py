@@ -820,6 +820,41 @@ def run_ncu_case(args):
     return None
 
 
+def run_ncu_fp4(args):
+    """A small FP4 case for profiler captures (not a bench line).
+
+    One layer of the Large shape (E=256, top-8, H=4096, F=2048) with NVFP4
+    (fmt 1) or MXFP4 (fmt 2) records in 16 slots; T=1 calls alternate
+    between experts 0..7 and 8..15, so after the first two (the fills) every
+    launch reads 8 resident records and the 226 MB working set exceeds L2.
+    Twelve calls; capture e.g. the seventh expert launch with
+    `ncu -k regex:expert_ffn_fp4 -s 6 -c 1`.
+    """
+    import torch
+    import moe_expert_cache_gb300 as ft
+
+    ft.load()
+    fmt = args.ncu_fp4
+    H, F, E, k = 4096, 2048, 256, 8
+    sh = synth.Shape(L=1, E=E, k=k, H=H, F=F, fmt=fmt)
+    pool, glob = _fp4_pool(sh, 0, distinct=2)
+    ctx = ft.Context(1, E, k, H, F, 16, pool, fmt=fmt, T_max=1, nvfp4_global=glob)
+    x = torch.from_numpy(synth.tokens_bf16(0, 0, 0, 1, H).view(np.int16)).cuda().view(torch.bfloat16)
+    pc = torch.zeros(1, H, device="cuda")
+    y = torch.empty(1, H, device="cuda")
+    w = torch.full((1, k), 1.0 / k, device="cuda")
+    for i in range(12):
+        ids = torch.arange(8 * (i & 1), 8 * (i & 1) + 8, dtype=torch.int32, device="cuda").view(1, k)
+        ctx.route_ctl(0, 1, topk_ids=ids, topk_w=w, B_P=1.0, B_H=1.0)
+        ctx.moe_forward(x, pc, y)
+    torch.cuda.synchronize()
+    st = ctx.status()
+    ctx.close()
+    if st != ft.FT_OK:
+        raise SystemExit(f"device status {st}")
+    return None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -834,9 +869,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill measurement and print its object (no bench line)")
+    ap.add_argument("--ncu-fp4", type=int, default=None, metavar="FMT",
+                    help="run the small FP4 profiling case (1 = NVFP4, 2 = MXFP4) and exit")
     ap.add_argument("--ncu-case", type=int, default=None, metavar="Q",
                     help="run the small single-layer profiling case with Q fills per call (0..8) and exit")
     args = ap.parse_args()
+    if args.ncu_fp4 is not None:
+        if args.ncu_fp4 not in (1, 2):
+            raise SystemExit("--ncu-fp4 takes 1 (NVFP4) or 2 (MXFP4)")
+        run_ncu_fp4(args)
+        return
     if args.ncu_case is not None:
         if not 0 <= args.ncu_case <= 8:
             raise SystemExit("--ncu-case takes 0..8")

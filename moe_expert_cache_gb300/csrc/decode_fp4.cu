@@ -9,20 +9,33 @@
 //   * MXFP4 (SB = 32, OCP Microscaling v1.0): one E8M0 scale, 2^(code-127),
 //     per 32 values; no global (the kernel reads 1.0).  The same section
 //     lists MXFP4 among the bank layouts.
-// Weight w = e2m1 * scale(block along K) * global(expert).  Each block is
-// summed in fp32 against the fp32 activations, scaled by its scale, and the
-// row total is multiplied by the expert's global once.  Activations are not
-// quantised (W4A16).
+// Weight w = e2m1 * scale(block along K) * global(expert).  Activations are
+// not quantised to FP4 (W4A16); the arithmetic is packed f16:
+//   * e2m1 codes are decoded two at a time into f16 pairs equal to
+//     value * 2^-14 (bit placement, exact);
+//   * activation rows (x for phase A, h for phase B) are held as f16 pairs in
+//     the same order, each token row multiplied by a power of two chosen from
+//     its largest magnitude (exact for x; one f16 rounding for h);
+//   * each 16-value block is summed with packed f16 FMAs (two chains of four
+//     products per half), widened to fp32, multiplied by its block scale and
+//     added in fp32; the row total is rescaled once by the token's power of
+//     two and the expert's global.
+// The per-token maximum of h is formed in phase A (shared-memory maxima,
+// then one 64-bit atomic max per CTA and token, tagged with the grid
+// barrier's generation so that values from earlier launches lose).
 //
 // Record (per layer-expert): [W_gu values 2F x H/2 bytes, low nibble first,
 // gate/up rows interleaved in groups of 16][W_d values H x F/2]
 // [W_gu scales 2F x H/SB][W_d scales H x F/SB].
 //
-// Differences from the BF16 kernel: a phase-A slot holds 8 gate rows, the 8
-// matching up rows and their scale rows (four bulk copies); a phase-B item is
-// (expert, group of at most TG tokens) so that the staged h rows stay within
-// a slot for any T; x is read from shared memory (fp32 or bf16) when it fits
-// and from global memory otherwise.
+// Layout of the work: 16 consumer warps, one producer warp (TMA ring) and one
+// fill warp.  A phase-A item is 16 features (16 gate rows, the 16 up rows and
+// their scale rows, one warp per feature); a phase-B item is (expert, group
+// of at most TG tokens): the CTA's W_d rows, the staged fp32 h rows and, in
+// the slot's tail, those rows converted to f16 pairs, two W_d rows per warp
+// pass.  x is converted into shared memory when T*H*2 bytes fit, else into a
+// global block behind a grid barrier.  A grid barrier separates phase A from
+// phase B.
 #include "ft_common.cuh"
 #include "../../include/ft.h"
 
