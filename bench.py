@@ -385,7 +385,8 @@ def run_ours(args, rank, world, local_rank):
                              "frac": round(gbs / peak, 4) if peak else None}
         kernels[name] = ent
     dom = max(prof, key=lambda n: prof[n]["ms"])
-    roofline = roofline_entry(dom, kernels, peaks, h2d_peak)
+    roofline = roofline_entry(dom, kernels, peaks, h2d_peak,
+                              dcnt["hits"] / max(1, dcnt["calls"]) if dom == "expert_ffn" else None)
     ex = kernels.get("expert_ffn", {})
     expert_roofline = {"kernel": "expert_ffn", "bound": "hbm",
                        "achieved": ex.get("hbm", {}).get("achieved_GBps"), "peak": peaks["hbm_gbs"],
@@ -561,7 +562,9 @@ def run_fp4_decode_bench(device, peaks, calls_t1: int = 96, calls_t64: int = 24)
                             "hits_per_launch": round(d["hits"] / max(1, d["calls"]), 2),
                             "fills": d["fills"], "hbm_bytes_per_launch": int(hbm / n),
                             "achieved_GBps": round(gbs, 1), "peak_GBps": peaks["hbm_gbs"],
-                            "frac": round(gbs / peaks["hbm_gbs"], 4)}
+                            "frac": round(gbs / peaks["hbm_gbs"], 4),
+                            "traffic": traffic_from_profiles("expert_ffn_fp4", d["hits"] / max(1, d["calls"]))
+                            if fmt == synth.FMT_NVFP4 else None}
         assert ctx.status() == ft.FT_OK
         ctx.close()
         del pool
@@ -652,7 +655,7 @@ def run_prefill_bench(device, peaks, reps: int = 3) -> dict:
     }
 
 
-def roofline_entry(dom, kernels, peaks, h2d_peak):
+def roofline_entry(dom, kernels, peaks, h2d_peak, records_per_launch=None):
     """Roofline of the dominant kernel: the side (host link or HBM) whose
     bytes at peak take longer is the bound."""
     ent = kernels[dom]
@@ -666,13 +669,15 @@ def roofline_entry(dom, kernels, peaks, h2d_peak):
     return {"kernel": dom, "bound": bound, "achieved": side.get("achieved_GBps"), "peak": side.get("peak_GBps"),
             "unit": "GB/s", "frac": side.get("frac"), "peak_source": src,
             "bytes_per_launch": side.get("bytes_per_launch"), "us_per_launch": ent["us_per_launch"],
-            "traffic": traffic_from_profiles(dom)}
+            "traffic": traffic_from_profiles(dom, records_per_launch)}
 
 
-def traffic_from_profiles(kernel: str):
+def traffic_from_profiles(kernel: str, records_per_launch: float | None = None):
     """DRAM bytes per launch from a committed ncu capture, if one matches the
     current kernel source (profiles/traffic.json keyed by kernel and source
-    hash); else None."""
+    hash); else None.  A capture that lists the records its launch read is
+    scaled to `records_per_launch` (the traffic of these kernels grows with
+    the records they read)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -683,7 +688,13 @@ def traffic_from_profiles(kernel: str):
         import hashlib
         src = os.path.join(ROOT, d["source"])
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return d["dram_bytes_per_launch"] if h == d["source_sha"] else None
+        if h != d["source_sha"]:
+            return None
+        if "records_read" in d:
+            if records_per_launch is None:
+                return None
+            return int(d["dram_bytes"] / d["records_read"] * records_per_launch)
+        return d.get("dram_bytes_per_launch")
     except Exception:
         return None
 
