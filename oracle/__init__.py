@@ -18,6 +18,8 @@ Modules:
               activation quantiser.
   mxfp4    -- e2m1 / E8M0 decoding of MXFP4 records and the block-32 MX
               conversion.
+  fp8      -- E4M3 decoding of block-FP8 records (fp32 scale per 128 x 128
+              block) and the block quantiser.
 
 Readings of the pages that these modules take where the pages are silent are
 listed in each function's docstring.  Parity unpinned: none of the functions

@@ -2,7 +2,7 @@
 
 This module is shared by the oracle, the tests and the benchmark.  It holds
 no arithmetic of the method itself (no routing, no cache control, no expert
-FFN): only random draws, the bf16 / NVFP4 / MXFP4 encodings of the drawn weights and
+FFN): only random draws, the bf16 / NVFP4 / MXFP4 / block-FP8 encodings of the drawn weights and
 the byte layout of one expert record in the host pool.
 
 Random streams: numpy ``PCG64`` seeded by ``SeedSequence([seed, tag, ...])``
@@ -33,6 +33,7 @@ TAG_TOPK = 5
 FMT_BF16 = 0
 FMT_NVFP4 = 1
 FMT_MXFP4 = 2
+FMT_FP8 = 3
 
 # Record layout: gate and up rows are interleaved in groups of this many rows
 # (16 gate rows, then the 16 matching up rows, ...).
@@ -41,6 +42,8 @@ GU_INTERLEAVE = 16
 NVFP4_BLOCK = 16
 # MXFP4: one E8M0 (power-of-two) scale per this many consecutive values along K.
 MXFP4_BLOCK = 32
+# Block-FP8: one fp32 scale per FP8_BLOCK x FP8_BLOCK block (rows x K) of each matrix.
+FP8_BLOCK = 128
 
 
 @dataclass(frozen=True)
@@ -67,6 +70,8 @@ def record_bytes(H: int, F: int, fmt: int) -> int:
         return n // 2 + n // NVFP4_BLOCK
     if fmt == FMT_MXFP4:
         return n // 2 + n // MXFP4_BLOCK
+    if fmt == FMT_FP8:
+        return n + 4 * 3 * (H // FP8_BLOCK) * (F // FP8_BLOCK)
     raise ValueError(f"unknown format {fmt}")
 
 
@@ -324,13 +329,81 @@ def record_mxfp4(seed: int, layer: int, expert: int, H: int, F: int, out=None) -
     return pack_record_mxfp4(expert_mxfp4(seed, layer, expert, H, F), out=out)
 
 
+# --------------------------------------------------------- block-FP8 experts
+# Encoding of the drawn weights into block-FP8: per 128 x 128 block the fp32
+# scale amax / 448 (1 for an all-zero block), values e4m3(w / scale) rounded
+# to nearest even with saturation at 448.
+
+def encode_e4m3(x: np.ndarray) -> np.ndarray:
+    """float -> signed e4m3 code (sign in bit 7), RNE, saturating at 448."""
+    idx = encode_e4m3_pos(x)
+    sign = (np.signbit(x) & (idx != 0)).astype(np.uint8) << 7
+    return idx | sign
+
+
+def quantize_fp8(W: np.ndarray):
+    """W [rows, K] float32 -> (codes uint8 [rows, K], scales float32 [rows/128, K/128])."""
+    rows, K = W.shape
+    b = FP8_BLOCK
+    Wb = np.asarray(W, dtype=np.float32).reshape(rows // b, b, K // b, b)
+    amax = np.abs(Wb).max(axis=(1, 3))
+    sc = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0)).astype(np.float32)
+    v = Wb.astype(np.float64) / sc.astype(np.float64)[:, None, :, None]
+    return encode_e4m3(v).reshape(rows, K), sc
+
+
+def expert_fp8(seed: int, layer: int, expert: int, H: int, F: int):
+    """Block-FP8 encoding of one layer-expert drawn like the BF16 weights: e4m3
+    codes and fp32 block scales of gate [F,H], up [F,H] and down [H,F]."""
+    rng = _rng(seed, TAG_WEIGHTS, layer, expert)
+    w = rng.standard_normal(3 * H * F, dtype=np.float32) * np.float32(0.02)
+    n = H * F
+    out = {}
+    for name, W in (("g", w[:n].reshape(F, H)), ("u", w[n:2 * n].reshape(F, H)), ("d", w[2 * n:].reshape(H, F))):
+        codes, sc = quantize_fp8(W)
+        out[name] = codes
+        out[name + "_scale"] = sc
+    return out
+
+
+def pack_record_fp8(q: dict, out: np.ndarray | None = None) -> np.ndarray:
+    """Byte image of one block-FP8 record.
+
+    [W_gu values: 2F x H e4m3, rows interleaved in groups of GU_INTERLEAVE]
+    [W_d values: H x F] [W_g scales: F/128 x H/128 fp32] [W_u scales]
+    [W_d scales: H/128 x F/128].
+    """
+    F, H = q["g"].shape
+    g = GU_INTERLEAVE
+    gu = np.empty((F // g, 2, g, H), dtype=np.uint8)
+    gu[:, 0] = q["g"].reshape(F // g, g, H)
+    gu[:, 1] = q["u"].reshape(F // g, g, H)
+    parts = [gu.reshape(-1), q["d"].reshape(-1)] + [
+        np.ascontiguousarray(q[k], dtype=np.float32).reshape(-1).view(np.uint8)
+        for k in ("g_scale", "u_scale", "d_scale")]
+    nb = record_bytes(H, F, FMT_FP8)
+    if out is None:
+        out = np.empty(nb, dtype=np.uint8)
+    off = 0
+    for p in parts:
+        out[off:off + p.size] = p
+        off += p.size
+    assert off == nb
+    return out
+
+
+def record_fp8(seed: int, layer: int, expert: int, H: int, F: int, out=None) -> np.ndarray:
+    """Record bytes of one block-FP8 layer-expert."""
+    return pack_record_fp8(expert_fp8(seed, layer, expert, H, F), out=out)
+
+
 # -------------------------------------------------------------- host pool
 
 def fill_host_pool(pool: np.ndarray, shape: Shape, seed: int, threads: int | None = None) -> np.ndarray | None:
     """Write every record [l*E+e] of the host pool (uint8 [L*E*record_bytes]).
 
-    Returns the per-record fp32 globals [L*E] for NVFP4, else None (BF16 and
-    MXFP4 records carry no global).
+    Returns the per-record fp32 globals [L*E] for NVFP4, else None (BF16,
+    MXFP4 and block-FP8 records carry no global).
     """
     rb = shape.record_bytes
     n = shape.L * shape.E
@@ -344,6 +417,8 @@ def fill_host_pool(pool: np.ndarray, shape: Shape, seed: int, threads: int | Non
             record_bf16(seed, l, e, shape.H, shape.F, out=dst)
         elif shape.fmt == FMT_MXFP4:
             record_mxfp4(seed, l, e, shape.H, shape.F, out=dst)
+        elif shape.fmt == FMT_FP8:
+            record_fp8(seed, l, e, shape.H, shape.F, out=dst)
         else:
             _, gsv = record_nvfp4(seed, l, e, shape.H, shape.F, out=dst)
             glob[fid] = gsv
