@@ -425,7 +425,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_prefill:
         out["prefill"] = run_prefill_bench(device, peaks)
     if rank == 0 and not args.no_fp4:
-        out["fp4_decode"] = run_fp4_decode_bench(device, peaks)
+        out["quant_decode"] = run_quant_decode_bench(device, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(pool.numpy() if world == 1 else shared[0], args.cpu_seconds)
     if world > 1:
@@ -494,7 +494,8 @@ def _fp4_pool(sh: synth.Shape, seed: int, distinct: int = 16):
     import torch
     from concurrent.futures import ThreadPoolExecutor
     rb = sh.record_bytes
-    enc = synth.record_nvfp4 if sh.fmt == synth.FMT_NVFP4 else synth.record_mxfp4
+    enc = {synth.FMT_NVFP4: synth.record_nvfp4, synth.FMT_MXFP4: synth.record_mxfp4,
+           synth.FMT_FP8: synth.record_fp8}[sh.fmt]
     with ThreadPoolExecutor(min(distinct, os.cpu_count() or 1)) as ex:
         got = list(ex.map(lambda e: enc(seed, 0, e, sh.H, sh.F), range(distinct)))
     recs = [g[0] for g in got] if sh.fmt == synth.FMT_NVFP4 else got
@@ -507,13 +508,14 @@ def _fp4_pool(sh: synth.Shape, seed: int, distinct: int = 16):
     return pool, glob
 
 
-def run_fp4_decode_bench(device, peaks, calls_t1: int = 96, calls_t64: int = 24) -> dict:
-    """FP4 expert kernel (NVFP4 and MXFP4 records) on the Large shapes, hits
-    only: one MoE layer of E=256 experts, top-8, H=4096, F=2048, every record
-    resident in 512 slots (a warm-up with B_P = B_H fills every miss), AR(1)
-    rho=0.8 logits, T=1 and T=64.  The bound is HBM: each launch reads the
-    records of its routed experts.  Per-launch device time from the library's
-    CUDA-event records around each expert-kernel launch."""
+def run_quant_decode_bench(device, peaks, calls_t1: int = 96, calls_t64: int = 24) -> dict:
+    """Quantised expert kernels (NVFP4, MXFP4 and block-FP8 records) on the
+    Large shapes, hits only: one MoE layer of E=256 experts, top-8, H=4096,
+    F=2048, every record resident in 512 slots (a warm-up with B_P = B_H
+    fills every miss), AR(1) rho=0.8 logits, T=1 and T=64.  The bound is
+    HBM: each launch reads the records of its routed experts.  Per-launch
+    device time from the library's CUDA-event records around each launch of
+    the expert kernel (both FP8 kernels under one record)."""
     import torch
     import moe_expert_cache_gb300 as ft
     out = {"workload": "Large shapes, hits only: 1 MoE layer, E=256, top-8, hidden 4096, ffn 2048, 512 slots "
@@ -521,7 +523,7 @@ def run_fp4_decode_bench(device, peaks, calls_t1: int = 96, calls_t64: int = 24)
            "execution": "eager library calls; expert-kernel time from the library's per-launch CUDA events"}
     H, F, E, k = 4096, 2048, 256, 8
     cs = torch.cuda.Stream(device)
-    for name, fmt in (("nvfp4", synth.FMT_NVFP4), ("mxfp4", synth.FMT_MXFP4)):
+    for name, fmt in (("nvfp4", synth.FMT_NVFP4), ("mxfp4", synth.FMT_MXFP4), ("fp8", synth.FMT_FP8)):
         sh = synth.Shape(L=1, E=E, k=k, H=H, F=F, fmt=fmt)
         pool, glob = _fp4_pool(sh, 0)
         ctx = ft.Context(1, E, k, H, F, 512, pool, fmt=fmt, T_max=64, nvfp4_global=glob,
@@ -875,8 +877,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-t16", action="store_true", help="skip the decode T=16 (resize) measurement")
-    ap.add_argument("--no-fp4", action="store_true", help="skip the FP4 (NVFP4, MXFP4) decode measurement")
-    ap.add_argument("--fp4-only", action="store_true", help="only the FP4 decode measurement (one JSON object)")
+    ap.add_argument("--no-fp4", action="store_true",
+                    help="skip the quantised (NVFP4, MXFP4, block-FP8) decode measurement")
+    ap.add_argument("--fp4-only", action="store_true",
+                    help="only the quantised decode measurement (one JSON object)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill measurement and print its object (no bench line)")
@@ -907,7 +911,7 @@ def main():
         torch.cuda.set_device(0)
         import moe_expert_cache_gb300 as ft
         ft.load()
-        print(json.dumps({"fp4_decode": run_fp4_decode_bench(torch.device("cuda", 0), read_peaks())}), flush=True)
+        print(json.dumps({"quant_decode": run_quant_decode_bench(torch.device("cuda", 0), read_peaks())}), flush=True)
         return
     rank, world, local_rank = dist_env()
     if args.warmup < 3:

@@ -45,6 +45,7 @@ typedef int32_t ft_status;
 #define FT_FMT_BF16   0       /* bf16 banks                                           */
 #define FT_FMT_NVFP4  1       /* e2m1 values + e4m3 block-16 scales + fp32 global     */
 #define FT_FMT_MXFP4  2       /* e2m1 values + E8M0 block-32 scales (OCP MX v1.0)     */
+#define FT_FMT_FP8    3       /* E4M3 values + fp32 scale per 128 x 128 block         */
 
 typedef struct ft_ctx ft_ctx; /* opaque; created by ft_layer_init, freed by ft_destroy */
 
@@ -114,6 +115,13 @@ const char* ft_status_str(ft_status s);
  *                  list MXFP4 among the bank layouts (deepmox, "One logical
  *                  expert, two physical levels of memory").  MXFP4 contexts
  *                  with prefill hold the same bf16 staging copy as NVFP4.
+ *                  FP8 (block-FP8, the same section's "FP8 weights and
+ *                  block-scale data") needs H % 128 == 0, F % 128 == 0,
+ *                  nvfp4_global == NULL and T_max*k*ceil(H/SMs)*4 bytes of
+ *                  shared memory (at most 227 KiB); its decode runs the
+ *                  pending fill as a standalone copy before the expert
+ *                  kernels, and its prefill stages the layer in bf16 (one
+ *                  rounding of e4m3 * scale).
  *   T_max          largest T of a decode call (ft_route_ctl), 1..256, with
  *                  T_max*k <= 4096 and T_max*H <= 32768 (the tokens of a
  *                  decode call are staged in shared memory).
@@ -127,7 +135,7 @@ const char* ft_status_str(ft_status s);
  *                  cudaHostRegister) or otherwise device-accessible, and stay
  *                  valid and unchanged until ft_destroy.  Not copied.
  *   nvfp4_global   HOST array of L*E fp32 per-record global scales (NVFP4), or
- *                  NULL for BF16 and MXFP4.  Copied to device memory at init (the pages:
+ *                  NULL for BF16, MXFP4 and FP8.  Copied to device memory at init (the pages:
  *                  small per-expert values stay GPU-resident).
  *   compute_stream, transfer_stream
  *                  cudaStream_t handles owned by the caller (NULL = legacy
@@ -149,6 +157,10 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
  * MXFP4: the NVFP4 layout with one E8M0 scale (value 2^(code-127), 0xFF NaN)
  *        per 32 values along K: [W_gu values] [W_d values]
  *        [W_gu scales 2F x H/32] [W_d scales H x F/32]; no global.
+ * FP8  : [W_gu values 2F x H E4M3, one byte each, same row order]
+ *        [W_d values H x F] [W_g scales F/128 x H/128 fp32]
+ *        [W_u scales F/128 x H/128] [W_d scales H/128 x F/128], row-major;
+ *        w = e4m3 * scale(row / 128, k / 128).
  * Returns 0 for an unknown fmt. */
 size_t ft_record_bytes(int32_t H, int32_t F, int32_t fmt);
 

@@ -28,6 +28,7 @@ FT_ERR_DEVICE = -7
 FT_FMT_BF16 = 0
 FT_FMT_NVFP4 = 1
 FT_FMT_MXFP4 = 2
+FT_FMT_FP8 = 3
 
 _c_int = ctypes.c_int32
 _c_p = ctypes.c_void_p

@@ -1,0 +1,292 @@
+// Decode expert FFN over block-FP8 records (W8A16).
+//
+// deepmox "One logical expert, two physical levels of memory": a block-FP8
+// bank keeps FP8 weights and block-scale data.  Here the values are OCP FP8
+// E4M3 codes and every 128 x 128 block (rows x K) of each weight matrix has
+// one fp32 scale: w = e4m3(code) * scale(row / 128, k / 128).
+//
+// Record (per layer-expert): [W_gu values 2F x H bytes, gate/up rows
+// interleaved in groups of 16] [W_d values H x F] [W_g scales F/128 x H/128
+// fp32] [W_u scales F/128 x H/128] [W_d scales H/128 x F/128].
+//
+// Two plain kernels, without the fused fill of the FP4 and BF16 kernels (a
+// pending fill is completed by the standalone fill kernel before them):
+//   * fp8_gateup_kernel: every warp takes (entry, feature) units; a unit
+//     streams the feature's gate and up rows with 16-byte loads that skip L1,
+//     against every token of the entry, and writes SwiGLU(h) to the fp32
+//     scratch [assignment, F];
+//   * fp8_down_kernel: CTA c owns output rows [c*H/G, (c+1)*H/G); its warps
+//     take (entry, row) units against the h rows, then the CTA merges the
+//     gated sum with the CPU-set partial sum in fixed order.
+// E4M3 pairs are converted by the hardware (cvt.rn.f16x2.e4m3x2, exact),
+// widened to fp32 and accumulated in fp32 per 16-value chunk, then scaled
+// by the chunk's block scale (16 divides 128).
+#include "ft_common.cuh"
+#include "../../include/ft.h"
+
+#include <cuda_fp16.h>
+
+namespace {
+
+constexpr int A_THREADS = 256;
+constexpr int B_THREADS = 512;
+constexpr int FP8_BLK = 128;
+
+// 16-byte load of streamed weights, bypassing L1.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Two e4m3 codes (the low and high byte of `b`) to fp32, exactly.
+__device__ __forceinline__ float2 e4m3x2(uint32_t b) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)b));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Dot of 16 e4m3 values (one uint4, in K order) with 16 fp32 activations.
+__device__ __forceinline__ float dot16(const uint4& w, const float* x) {
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 lo = e4m3x2(ww[i]), hi = e4m3x2(ww[i] >> 16);
+        a = fmaf(lo.x, x[4 * i], a);
+        b = fmaf(lo.y, x[4 * i + 1], b);
+        a = fmaf(hi.x, x[4 * i + 2], a);
+        b = fmaf(hi.y, x[4 * i + 3], b);
+    }
+    return a + b;
+}
+
+// Activations staged in shared memory as fp32, each 16-value chunk's four
+// float4 rotated by (chunk / 2) mod 4 so that the eight lanes of a quarter
+// warp (consecutive chunks) read eight different bank quads.
+__device__ __forceinline__ int xrot(int e) {  // element e of a row -> its stored position
+    const int q = e >> 4, i = (e >> 2) & 3;
+    return (q << 4) | (((i + (q >> 1)) & 3) << 2) | (e & 3);
+}
+
+// The 16 activations of chunk c of a token row: from the rotated fp32 copy
+// in shared memory (XS), or from the bf16 input in global memory.
+template <bool XS>
+__device__ __forceinline__ void load_x16(const float* xs, const __nv_bfloat16* xg, int t, int H, int c, float* x) {
+    if (XS) {
+        const float4* p = reinterpret_cast<const float4*>(xs + (size_t)t * H + (size_t)c * 16);
+        const int r = (c >> 1) & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 q = p[(i + r) & 3];
+            x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
+        }
+    } else {
+        const uint4* p = reinterpret_cast<const uint4*>(xg + (size_t)t * H + (size_t)c * 16);
+        ft::bf16x8_to_f32(__ldg(p), x);
+        ft::bf16x8_to_f32(__ldg(p + 1), x + 8);
+    }
+}
+
+// Gate and up rows of one feature against NT tokens (token rows tk).
+template <int NT, bool XS>
+__device__ __forceinline__ void gu_rows(const uint8_t* wg, const uint8_t* wu, const float* sg, const float* su,
+                                        const float* xs, const __nv_bfloat16* xg, const int* tk, int H, int lane,
+                                        float* ag, float* au) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
+    const int nc = H >> 4;
+#pragma unroll 2
+    for (int c = lane; c < nc; c += 32) {
+        const uint4 a = ld_stream(wg + (size_t)c * 16), b = ld_stream(wu + (size_t)c * 16);
+        const float s1 = sg[c >> 3], s2 = su[c >> 3];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            float x[16];
+            load_x16<XS>(xs, xg, tk[n], H, c, x);
+            ag[n] = fmaf(s1, dot16(a, x), ag[n]);
+            au[n] = fmaf(s2, dot16(b, x), au[n]);
+        }
+    }
+}
+
+template <int NT, bool XS>
+__device__ __forceinline__ void gu_group(const uint8_t* wg, const uint8_t* wu, const float* sg, const float* su,
+                                         const float* xs, const __nv_bfloat16* xg, const int* as_tok, int H, int F,
+                                         int f, int pos0, int lane, float* hbuf) {
+    int tk[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) tk[n] = as_tok[pos0 + n];
+    float ag[NT], au[NT];
+    gu_rows<NT, XS>(wg, wu, sg, su, xs, xg, tk, H, lane, ag, au);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const float g = ft::warp_sum(ag[n]), u = ft::warp_sum(au[n]);
+        if (lane == 0) hbuf[(size_t)(pos0 + n) * F + f] = ft::silu_mul(g, u);
+    }
+}
+
+template <bool XS>
+__global__ void __launch_bounds__(A_THREADS, 2) fp8_gateup_kernel(ExpertParams p) {
+    extern __shared__ __align__(16) float xs_dyn[];
+    const int H = p.H, F = p.F, T = p.T;
+    const int ugpu = p.info[INFO_UGPU];
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (XS) {
+        for (int i = tid; i < T * H / 8; i += A_THREADS) {
+            float f8[8];
+            ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
+            const int t = (8 * i) / H, e = 8 * i - t * H;
+            float* row = xs_dyn + (size_t)t * H;
+            *reinterpret_cast<float4*>(row + xrot(e)) = make_float4(f8[0], f8[1], f8[2], f8[3]);
+            *reinterpret_cast<float4*>(row + xrot(e + 4)) = make_float4(f8[4], f8[5], f8[6], f8[7]);
+        }
+        __syncthreads();
+    }
+    const size_t nbg = (size_t)(F / FP8_BLK) * (H / FP8_BLK);  // scale blocks of W_g (and of W_u)
+    const int warps = gridDim.x * (A_THREADS / 32);
+    for (int u = blockIdx.x * (A_THREADS / 32) + (tid >> 5); u < ugpu * F; u += warps) {
+        const int e = u / F, f = u - e * F;
+        const int off = p.wl_off[e], ntok = p.wl_off[e + 1] - off;
+        const uint8_t* rec = p.slot_pool + (size_t)p.wl_slot[e] * p.rb;
+        const int grow = (f >> 4) * 32 + (f & 15);  // gate row; the up row is 16 later
+        const uint8_t* wg = rec + (size_t)grow * H;
+        const uint8_t* wu = wg + (size_t)16 * H;
+        const float* sc = reinterpret_cast<const float*>(rec + (size_t)3 * H * F);
+        const float* sg = sc + (size_t)(f / FP8_BLK) * (H / FP8_BLK);
+        const float* su = sg + nbg;
+        int g0 = 0;
+        while (g0 < ntok) {
+            const int rem = ntok - g0;
+            if (rem >= 4) {
+                gu_group<4, XS>(wg, wu, sg, su, xs_dyn, p.x, p.as_tok, H, F, f, off + g0, lane, p.hbuf);
+                g0 += 4;
+            } else if (rem >= 2) {
+                gu_group<2, XS>(wg, wu, sg, su, xs_dyn, p.x, p.as_tok, H, F, f, off + g0, lane, p.hbuf);
+                g0 += 2;
+            } else {
+                gu_group<1, XS>(wg, wu, sg, su, xs_dyn, p.x, p.as_tok, H, F, f, off + g0, lane, p.hbuf);
+                g0 += 1;
+            }
+        }
+    }
+}
+
+// One W_d row against NT h rows (fp32, plain [assignment, F] in global memory).
+template <int NT>
+__device__ __forceinline__ void down_row(const uint8_t* wd, const float* sd, const float* hbuf, int pos0, int F,
+                                         int lane, float* acc) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n] = 0.f;
+    const int nc = F >> 4;
+#pragma unroll 2
+    for (int c = lane; c < nc; c += 32) {
+        const uint4 w = ld_stream(wd + (size_t)c * 16);
+        const float s = sd[c >> 3];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const float4* hp = reinterpret_cast<const float4*>(hbuf + (size_t)(pos0 + n) * F + (size_t)c * 16);
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 q = hp[i];
+                x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
+            }
+            acc[n] = fmaf(s, dot16(w, x), acc[n]);
+        }
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ void down_group(const uint8_t* wd, const float* sd, const float* hbuf, int pos0, int F,
+                                           int lane, float* o_s, int RMAX, int rl) {
+    float acc[NT];
+    down_row<NT>(wd, sd, hbuf, pos0, F, lane, acc);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const float v = ft::warp_sum(acc[n]);
+        if (lane == 0) o_s[(size_t)(pos0 + n) * RMAX + rl] = v;
+    }
+}
+
+__global__ void __launch_bounds__(B_THREADS, 1) fp8_down_kernel(ExpertParams p) {
+    extern __shared__ __align__(16) float o_s[];  // [assignment, RMAX]
+    const int H = p.H, F = p.F, T = p.T, k = p.k;
+    const int ugpu = p.info[INFO_UGPU];
+    const int G = gridDim.x, c = blockIdx.x;
+    const int r0 = (int)((long long)H * c / G), r1 = (int)((long long)H * (c + 1) / G);
+    const int R = r1 - r0;
+    const int RMAX = (H + G - 1) / G;
+    const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+    const size_t nbg = (size_t)(F / FP8_BLK) * (H / FP8_BLK);
+    for (int u = wid; u < ugpu * R; u += B_THREADS / 32) {
+        const int e = u / R, rl = u - e * R;
+        const int off = p.wl_off[e], ntok = p.wl_off[e + 1] - off;
+        const uint8_t* rec = p.slot_pool + (size_t)p.wl_slot[e] * p.rb;
+        const int r = r0 + rl;
+        const uint8_t* wd = rec + (size_t)2 * F * H + (size_t)r * F;
+        const float* sd = reinterpret_cast<const float*>(rec + (size_t)3 * H * F) + 2 * nbg +
+                          (size_t)(r / FP8_BLK) * (F / FP8_BLK);
+        int g0 = 0;
+        while (g0 < ntok) {
+            const int rem = ntok - g0;
+            if (rem >= 4) {
+                down_group<4>(wd, sd, p.hbuf, off + g0, F, lane, o_s, RMAX, rl);
+                g0 += 4;
+            } else if (rem >= 2) {
+                down_group<2>(wd, sd, p.hbuf, off + g0, F, lane, o_s, RMAX, rl);
+                g0 += 2;
+            } else {
+                down_group<1>(wd, sd, p.hbuf, off + g0, F, lane, o_s, RMAX, rl);
+                g0 += 1;
+            }
+        }
+    }
+    __syncthreads();
+    // gated merge in fixed order: j ascending, then the CPU-set partial sum
+    for (int idx = tid; idx < T * R; idx += B_THREADS) {
+        const int t = idx / R, rl = idx - t * R;
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int pos = p.out_pos[t * k + j];
+            if (pos >= 0) acc = fmaf(p.as_gate[pos], o_s[(size_t)pos * RMAX + rl], acc);
+        }
+        const size_t oi = (size_t)t * H + r0 + rl;
+        if (p.partial_C) acc += p.partial_C[oi];
+        p.y[oi] = acc;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_expert_ffn_fp8(ExpertParams p, int num_sms, cudaStream_t s) {
+    const size_t xbytes = (size_t)p.T * p.H * 4;
+    const bool xs = xbytes <= 96 * 1024;
+    const size_t smem_a = xs ? xbytes : 0;
+    static size_t set_a[2] = {0, 0};
+    const void* fa = xs ? (const void*)fp8_gateup_kernel<true> : (const void*)fp8_gateup_kernel<false>;
+    if (smem_a > set_a[xs ? 1 : 0]) {
+        cudaError_t e = cudaFuncSetAttribute(fa, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a);
+        if (e != cudaSuccess) return e;
+        set_a[xs ? 1 : 0] = smem_a;
+    }
+    if (xs)
+        fp8_gateup_kernel<true><<<2 * num_sms, A_THREADS, smem_a, s>>>(p);
+    else
+        fp8_gateup_kernel<false><<<2 * num_sms, A_THREADS, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int RMAX = (p.H + num_sms - 1) / num_sms;
+    const size_t smem_b = (size_t)p.T * p.k * RMAX * 4;
+    if (smem_b > 227 * 1024) return cudaErrorInvalidValue;
+    static size_t set_b = 0;
+    if (smem_b > set_b) {
+        e = cudaFuncSetAttribute(fp8_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_b);
+        if (e != cudaSuccess) return e;
+        set_b = smem_b;
+    }
+    fp8_down_kernel<<<num_sms, B_THREADS, smem_b, s>>>(p);
+    return cudaGetLastError();
+}

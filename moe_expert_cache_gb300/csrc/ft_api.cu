@@ -186,6 +186,7 @@ size_t ft_record_bytes(int32_t H, int32_t F, int32_t fmt) {
     if (fmt == FT_FMT_BF16) return 2 * n;
     if (fmt == FT_FMT_NVFP4) return n / 2 + n / 16;
     if (fmt == FT_FMT_MXFP4) return n / 2 + n / 32;
+    if (fmt == FT_FMT_FP8) return n + (size_t)12 * (H / 128) * (F / 128);
     return 0;
 }
 
@@ -197,7 +198,8 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     if (L < 1 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E || H < 64 || H % 64 || F < 64 || F % 64 || S < 1 ||
         T_max < 1 || T_max > 256 || T_max * k > 4096 || T_prefill_max < 0 || !host_pool)
         return FT_ERR_ARG;
-    if (fmt != FT_FMT_BF16 && fmt != FT_FMT_NVFP4 && fmt != FT_FMT_MXFP4) return FT_ERR_ARG;
+    if (fmt != FT_FMT_BF16 && fmt != FT_FMT_NVFP4 && fmt != FT_FMT_MXFP4 && fmt != FT_FMT_FP8) return FT_ERR_ARG;
+    if (fmt == FT_FMT_FP8 && (nvfp4_global || H % 128 || F % 128)) return FT_ERR_ARG;
     if (fmt == FT_FMT_NVFP4 && (!nvfp4_global || H % 256 || F % 256)) return FT_ERR_ARG;
     if (fmt == FT_FMT_MXFP4 && (nvfp4_global || H % 256 || F % 512)) return FT_ERR_ARG;
     if (fmt == FT_FMT_BF16 && nvfp4_global) return FT_ERR_ARG;
@@ -226,6 +228,8 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     } while (0)
     INIT_CUDA(cudaGetDevice(&c->device));
     INIT_CUDA(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
+    if (fmt == FT_FMT_FP8 && (size_t)T_max * k * ((H + c->num_sms - 1) / c->num_sms) * 4 > 227 * 1024)
+        return fail(FT_ERR_ARG);  // the down kernel keeps [assignment, rows] in shared memory
     // Device address of the host pool: the mapping of page-locked memory, or
     // the host address itself where the GPU reads pageable memory directly.
     void* dptr = nullptr;
@@ -361,6 +365,7 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.info = c->info; p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok;
     p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err; p.gbar = c->gbar;
     p.wl_fid = c->wl_fid; p.gscale = c->nvfp4_global; p.x16 = c->x16; p.xsc = c->xsc; p.hmax = c->hmax;
+    if (c->fmt == FT_FMT_FP8) FT_CUDA(flush_fill(c));  // no fused fill in the FP8 kernels
     p.do_fill = c->fill_pending ? 1 : 0;
     p.host_pool = (const uint4*)c->host_pool_dev;
     p.fill_slot = c->fill_slot;
@@ -372,6 +377,8 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
         ProfScope ps(c->prof, FT_K_EXPERT, c->cs);
         if (c->fmt == FT_FMT_NVFP4 || c->fmt == FT_FMT_MXFP4)
             FT_CUDA(launch_expert_ffn_fp4(p, c->fmt, c->num_sms, c->cs));
+        else if (c->fmt == FT_FMT_FP8)
+            FT_CUDA(launch_expert_ffn_fp8(p, c->num_sms, c->cs));
         else
             FT_CUDA(launch_expert_ffn(p, c->num_sms, c->cs));
     }
@@ -679,7 +686,7 @@ ft_status ft_prefill_layer(ft_ctx* c, int32_t buffer, int32_t layer, int32_t nex
     }
     FT_CUDA(cudaStreamWaitEvent(cs, pf.loaded[buffer], 0));
     const float* escale = nullptr;
-    if (c->fmt == FT_FMT_NVFP4 || c->fmt == FT_FMT_MXFP4) {
+    if (c->fmt == FT_FMT_NVFP4 || c->fmt == FT_FMT_MXFP4 || c->fmt == FT_FMT_FP8) {
         ProfScope ps(c->prof, FT_K_PF_DEQUANT, cs);
         FT_CUDA(launch_pf_dequant(pf, c->slot_pool + (size_t)buffer * layer_bytes, cs));
         if (c->fmt == FT_FMT_NVFP4) escale = c->nvfp4_global + (size_t)layer * c->E;

@@ -525,7 +525,7 @@ ft_status prefill_alloc(PrefillState& pf, int T_max, int k, int H, int F, int E,
     pf.T_max = T_max;
     pf.E = E; pf.k = k; pf.H = H; pf.F = F;
     pf.fmt = fmt;
-    if ((fmt == FT_FMT_NVFP4 || fmt == FT_FMT_MXFP4) &&
+    if ((fmt == FT_FMT_NVFP4 || fmt == FT_FMT_MXFP4 || fmt == FT_FMT_FP8) &&
         cudaMalloc(&pf.staging, (size_t)E * 3 * H * F * 2) != cudaSuccess) {
         cudaGetLastError();
         return FT_ERR_OOM;
@@ -560,7 +560,7 @@ ft_status prefill_set_pool(PrefillState& pf, const uint8_t* pool, size_t rb) {
         // BF16: the GEMMs read the buffer's records in place; NVFP4 and
         // MXFP4: the bf16 staging copy of the layer (one, reused by both
         // buffers in turn)
-        const bool staged = pf.fmt == FT_FMT_NVFP4 || pf.fmt == FT_FMT_MXFP4;
+        const bool staged = pf.fmt == FT_FMT_NVFP4 || pf.fmt == FT_FMT_MXFP4 || pf.fmt == FT_FMT_FP8;
         const uint8_t* base = staged ? static_cast<const uint8_t*>(pf.staging) : pool + (size_t)b * E * rb;
         const uint64_t rbb = staged ? 3 * H * F * 2 : rb;
         if (!encode_3d(&pf.mapB1[b], base, 2 * F, H, E, rbb, GN) ||
@@ -739,12 +739,57 @@ __global__ void __launch_bounds__(256) pf_dequant_kernel(const uint8_t* __restri
     }
 }
 
+// Expand E block-FP8 records into the bf16 record layout: every weight
+// becomes bf16(e4m3(code) * scale(row / 128, k / 128)), one rounding (the
+// product of a 4-bit significand and an fp32 scale is not a bf16 in general).
+// One thread per 16 values (one 16-byte group of codes).
+__global__ void __launch_bounds__(256) pf_dequant_fp8_kernel(const uint8_t* __restrict__ src, size_t rb8, int E,
+                                                             int H, int F, uint8_t* __restrict__ dst) {
+    const size_t rb16 = (size_t)3 * H * F * 2;
+    const size_t units = (size_t)3 * H * F / 16;  // W_gu then W_d, 16 values per unit
+    const size_t gu_units = (size_t)2 * F * H / 16;
+    const size_t nbg = (size_t)(F / 128) * (H / 128);
+    const size_t total = units * E;
+    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += (size_t)gridDim.x * blockDim.x) {
+        const size_t e = u / units, w = u - e * units;
+        const uint8_t* rec = src + e * rb8;
+        const float* sc = reinterpret_cast<const float*>(rec + (size_t)3 * H * F);
+        float s;
+        if (w < gu_units) {  // W_gu row r (interleaved gate/up groups of 16), columns c*16..
+            const size_t r = w / (H / 16), c = w - r * (H / 16);
+            const size_t grp = r / 32, i = r - grp * 32;  // i < 16: gate row grp*16+i, else up row grp*16+i-16
+            const size_t frow = grp * 16 + (i & 15);
+            s = sc[(i < 16 ? 0 : nbg) + (frow / 128) * (H / 128) + (c * 16) / 128];
+        } else {
+            const size_t w2 = w - gu_units, r = w2 / (F / 16), c = w2 - r * (F / 16);
+            s = sc[2 * nbg + (r / 128) * (F / 128) + (c * 16) / 128];
+        }
+        const uint4 q = *reinterpret_cast<const uint4*>(rec + w * 16);
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+        uint32_t packed[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t h;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)(wd[i >> 1] >> (16 * (i & 1)))));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+            const __nv_bfloat162 v = __floats2bfloat162_rn(f.x * s, f.y * s);
+            packed[i] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        uint4* o4 = reinterpret_cast<uint4*>(dst + e * rb16 + w * 32);
+        o4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        o4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_pf_dequant(PrefillState& pf, const uint8_t* layer_records, cudaStream_t s) {
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
-    if (pf.fmt == FT_FMT_MXFP4)
+    if (pf.fmt == FT_FMT_FP8)
+        pf_dequant_fp8_kernel<<<sms * 8, 256, 0, s>>>(layer_records, pf.rb, pf.E, pf.H, pf.F,
+                                                      static_cast<uint8_t*>(pf.staging));
+    else if (pf.fmt == FT_FMT_MXFP4)
         pf_dequant_kernel<32><<<sms * 8, 256, 0, s>>>(layer_records, pf.rb, pf.E, pf.H, pf.F,
                                                       static_cast<uint8_t*>(pf.staging));
     else

@@ -59,7 +59,9 @@ def test_host_only_calls(lib):
     assert lib.record_bytes(4096, 2048, 1) == synth.record_bytes(4096, 2048, synth.FMT_NVFP4)
     assert lib.record_bytes(4096, 2048, lib.FT_FMT_MXFP4) == 13369344
     assert lib.record_bytes(4096, 2048, 2) == synth.record_bytes(4096, 2048, synth.FMT_MXFP4)
-    assert lib.record_bytes(4096, 2048, 3) == 0
+    assert lib.record_bytes(4096, 2048, lib.FT_FMT_FP8) == 3 * 4096 * 2048 + 12 * 32 * 16
+    assert lib.record_bytes(4096, 2048, 3) == synth.record_bytes(4096, 2048, synth.FMT_FP8)
+    assert lib.record_bytes(4096, 2048, 4) == 0
 
 
 def test_argument_checks_need_no_gpu(lib):
@@ -70,7 +72,9 @@ def test_argument_checks_need_no_gpu(lib):
     assert lib.layer_init(1, 8, 2, 64, 128, 4, 0, 4, 0, None, None, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 64, 128, 0, 0, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
     # record formats: unknown; MXFP4 with F % 512 != 0 or with a global; NVFP4 without one
-    assert lib.layer_init(1, 8, 2, 256, 512, 4, 3, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
+    assert lib.layer_init(1, 8, 2, 256, 512, 4, 4, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
+    assert lib.layer_init(1, 8, 2, 192, 256, 4, lib.FT_FMT_FP8, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
+    assert lib.layer_init(1, 8, 2, 256, 256, 4, lib.FT_FMT_FP8, 4, 0, 1024, 4096, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 256, 256, 4, lib.FT_FMT_MXFP4, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 256, 512, 4, lib.FT_FMT_MXFP4, 4, 0, 1024, 4096, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 256, 512, 4, lib.FT_FMT_NVFP4, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG

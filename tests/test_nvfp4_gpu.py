@@ -1,6 +1,7 @@
-"""GPU parity of the FP4 decode and prefill paths (W4A16) for both FP4 record
+"""GPU parity of the quantised decode and prefill paths for the FP4 record
 formats, NVFP4 (e4m3 block-16 scales, fp32 global) and MXFP4 (E8M0 block-32
-scales): control bit-exact, outputs within rel-L2 5e-3 of the fp64 oracle on
+scales), and for block-FP8 (E4M3 values, fp32 scale per 128 x 128 block):
+control bit-exact, outputs within rel-L2 5e-3 of the fp64 oracle on
 identically dequantised weights."""
 import numpy as np
 import pytest
@@ -8,6 +9,7 @@ import pytest
 import synth
 from oracle import control as ctl
 from oracle import numerics as nm
+from oracle import fp8 as f8
 from oracle import mxfp4 as mx
 from oracle import nvfp4 as fp4
 from tests import harness as hz
@@ -41,6 +43,8 @@ class FP4Weights:
             rec = self.pool[fid * rb:(fid + 1) * rb]
             if sh.fmt == synth.FMT_MXFP4:
                 self.cache[e] = mx.record_weights(rec, sh.H, sh.F)
+            elif sh.fmt == synth.FMT_FP8:
+                self.cache[e] = f8.record_weights(rec, sh.H, sh.F)
             else:
                 self.cache[e] = fp4.record_weights(rec, sh.H, sh.F, float(self.glob[fid]))
         return self.cache[e]
@@ -54,7 +58,8 @@ def _repeated_pool(sh, seed, distinct):
     rb = sh.record_bytes
     pool = torch.empty(sh.L * sh.E * rb, dtype=torch.uint8, pin_memory=True)
     pn = pool.numpy()
-    enc = synth.record_mxfp4 if sh.fmt == synth.FMT_MXFP4 else (lambda *a: synth.record_nvfp4(*a)[0])
+    enc = {synth.FMT_MXFP4: synth.record_mxfp4, synth.FMT_FP8: synth.record_fp8}.get(
+        sh.fmt, lambda *a: synth.record_nvfp4(*a)[0])
     recs = [enc(seed, 0, e, sh.H, sh.F) for e in range(distinct)]
     for fid in range(sh.L * sh.E):
         pn[fid * rb:(fid + 1) * rb] = recs[fid % distinct]
@@ -215,5 +220,36 @@ def test_large_mxfp4_decode(ft):
     wl = synth.LARGE_MXFP4
     samples = {(s, l) for s in (0, 15) for l in (0, 7)} | {(s, l) for s in (16, 23) for l in (0, 7)}
     done = _replay(ft, wl.shape, wl.S, [(1, 16), (64, 8)], wl.B_P, wl.B_H, wl.rho, samples,
+                   tok_sample=[0, 21, 42, 63], distinct=16)
+    assert len(done) == len(samples)
+
+
+# ------------------------------------------------------------ block-FP8
+
+@pytest.mark.parametrize("H,F,E,k,S,T", [
+    (256, 256, 16, 4, 12, 3),       # x fp32 in shared memory
+    (1024, 512, 16, 4, 24, 9),      # several scale blocks along K and rows
+    (1024, 512, 16, 4, 24, 40),     # x read from global memory
+])
+def test_fp8_small(ft, H, F, E, k, S, T):
+    sh = synth.Shape(L=2, E=E, k=k, H=H, F=F, fmt=synth.FMT_FP8)
+    samples = {(s, l) for s in range(4) for l in range(2)}
+    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples)
+    assert len(done) == len(samples)
+
+
+def test_fp8_prefill_small(ft):
+    sh = synth.Shape(L=2, E=8, k=2, H=256, F=256, fmt=synth.FMT_FP8)
+    _run_prefill_fp4(ft, sh, 16, 300, [0, 1])
+
+
+@pytest.mark.slow
+def test_large_fp8_decode(ft):
+    """The Large layer shape with block-FP8 banks on 2 layers: E=256, top-8,
+    H=4096, F=2048, 512 slots, 8 steps at T=1 then 4 at T=64, AR(1) rho=0.8.
+    The pool repeats the records of 16 drawn experts."""
+    sh = synth.Shape(L=2, E=256, k=8, H=4096, F=2048, fmt=synth.FMT_FP8)
+    samples = {(s, l) for s in (0, 7) for l in (0, 1)} | {(s, l) for s in (8, 11) for l in (0, 1)}
+    done = _replay(ft, sh, 512, [(1, 8), (64, 4)], 52.7, 150.0, 0.8, samples,
                    tok_sample=[0, 21, 42, 63], distinct=16)
     assert len(done) == len(samples)
