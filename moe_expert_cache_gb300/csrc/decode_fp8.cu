@@ -98,16 +98,33 @@ __device__ __forceinline__ void gu_rows(const uint8_t* wg, const uint8_t* wu, co
 #pragma unroll
     for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
     const int nc = H >> 4;
-#pragma unroll 2
-    for (int c = lane; c < nc; c += 32) {
-        const uint4 a = ld_stream(wg + (size_t)c * 16), b = ld_stream(wu + (size_t)c * 16);
-        const float s1 = sg[c >> 3], s2 = su[c >> 3];
+    // BT chunks of both rows are loaded before any is used (2 BT 16-byte
+    // loads in flight per lane; fewer when more tokens share them, for the
+    // registers)
+    constexpr int BT = NT >= 4 ? 1 : (XS ? 4 : 2);
+    for (int c0 = lane; c0 < nc; c0 += 32 * BT) {
+        uint4 a[BT], b[BT];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            float x[16];
-            load_x16<XS>(xs, xg, tk[n], H, c, x);
-            ag[n] = fmaf(s1, dot16(a, x), ag[n]);
-            au[n] = fmaf(s2, dot16(b, x), au[n]);
+        for (int j = 0; j < BT; ++j) {
+            const int c = c0 + 32 * j;
+            if (c < nc) {
+                a[j] = ld_stream(wg + (size_t)c * 16);
+                b[j] = ld_stream(wu + (size_t)c * 16);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < BT; ++j) {
+            const int c = c0 + 32 * j;
+            if (c < nc) {
+                const float s1 = sg[c >> 3], s2 = su[c >> 3];
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    float x[16];
+                    load_x16<XS>(xs, xg, tk[n], H, c, x);
+                    ag[n] = fmaf(s1, dot16(a[j], x), ag[n]);
+                    au[n] = fmaf(s2, dot16(b[j], x), au[n]);
+                }
+            }
         }
     }
 }
@@ -160,7 +177,7 @@ __global__ void __launch_bounds__(A_THREADS, 2) fp8_gateup_kernel(ExpertParams p
         int g0 = 0;
         while (g0 < ntok) {
             const int rem = ntok - g0;
-            if (rem >= 4) {
+            if (!XS && rem >= 4) {  // four-token groups where x comes from global memory (large T)
                 gu_group<4, XS>(wg, wu, sg, su, xs_dyn, p.x, p.as_tok, H, F, f, off + g0, lane, p.hbuf);
                 g0 += 4;
             } else if (rem >= 2) {
@@ -174,36 +191,52 @@ __global__ void __launch_bounds__(A_THREADS, 2) fp8_gateup_kernel(ExpertParams p
     }
 }
 
-// One W_d row against NT h rows (fp32, plain [assignment, F] in global memory).
-template <int NT>
-__device__ __forceinline__ void down_row(const uint8_t* wd, const float* sd, const float* hbuf, int pos0, int F,
+// One W_d row against NT h rows (fp32 rows of F values: the rotated copy in
+// shared memory when HS, else the plain [assignment, F] scratch in global
+// memory).
+template <int NT, bool HS>
+__device__ __forceinline__ void down_row(const uint8_t* wd, const float* sd, const float* hsrc, int pos0, int F,
                                          int lane, float* acc) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n] = 0.f;
     const int nc = F >> 4;
-#pragma unroll 2
-    for (int c = lane; c < nc; c += 32) {
-        const uint4 w = ld_stream(wd + (size_t)c * 16);
-        const float s = sd[c >> 3];
+    constexpr int BT = NT >= 4 ? 1 : 2;  // chunks loaded ahead (fewer with four tokens)
+    for (int c0 = lane; c0 < nc; c0 += 32 * BT) {
+        uint4 w[BT];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            const float4* hp = reinterpret_cast<const float4*>(hbuf + (size_t)(pos0 + n) * F + (size_t)c * 16);
-            float x[16];
+        for (int j = 0; j < BT; ++j)
+            if (c0 + 32 * j < nc) w[j] = ld_stream(wd + (size_t)(c0 + 32 * j) * 16);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 q = hp[i];
-                x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
+        for (int j = 0; j < BT; ++j) {
+            const int c = c0 + 32 * j;
+            if (c < nc) {
+                const float s = sd[c >> 3];
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    float x[16];
+                    if (HS) {
+                        load_x16<true>(hsrc, nullptr, pos0 + n, F, c, x);
+                    } else {
+                        const float4* hp =
+                            reinterpret_cast<const float4*>(hsrc + (size_t)(pos0 + n) * F + (size_t)c * 16);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 q = hp[i];
+                            x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
+                        }
+                    }
+                    acc[n] = fmaf(s, dot16(w[j], x), acc[n]);
+                }
             }
-            acc[n] = fmaf(s, dot16(w, x), acc[n]);
         }
     }
 }
 
-template <int NT>
-__device__ __forceinline__ void down_group(const uint8_t* wd, const float* sd, const float* hbuf, int pos0, int F,
+template <int NT, bool HS>
+__device__ __forceinline__ void down_group(const uint8_t* wd, const float* sd, const float* hsrc, int pos0, int F,
                                            int lane, float* o_s, int RMAX, int rl) {
     float acc[NT];
-    down_row<NT>(wd, sd, hbuf, pos0, F, lane, acc);
+    down_row<NT, HS>(wd, sd, hsrc, pos0, F, lane, acc);
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
         const float v = ft::warp_sum(acc[n]);
@@ -211,8 +244,12 @@ __device__ __forceinline__ void down_group(const uint8_t* wd, const float* sd, c
     }
 }
 
+// HS: the h rows of every assignment (T*k rows of F fp32) are staged once per
+// CTA in shared memory, rotated like x, so that the CTA's (entry, row) units
+// read them from there instead of L2.
+template <bool HS>
 __global__ void __launch_bounds__(B_THREADS, 1) fp8_down_kernel(ExpertParams p) {
-    extern __shared__ __align__(16) float o_s[];  // [assignment, RMAX]
+    extern __shared__ __align__(16) float o_s[];  // [assignment, RMAX], then the h rows (HS)
     const int H = p.H, F = p.F, T = p.T, k = p.k;
     const int ugpu = p.info[INFO_UGPU];
     const int G = gridDim.x, c = blockIdx.x;
@@ -220,6 +257,17 @@ __global__ void __launch_bounds__(B_THREADS, 1) fp8_down_kernel(ExpertParams p) 
     const int R = r1 - r0;
     const int RMAX = (H + G - 1) / G;
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+    float* hs = o_s + (((size_t)T * k * RMAX + 3) & ~(size_t)3);
+    if (HS) {
+        const int nasg = p.info[INFO_NASSIGN];
+        for (int i = tid; i < nasg * F / 4; i += B_THREADS) {
+            const int a = (4 * i) / F, e = 4 * i - a * F;
+            *reinterpret_cast<float4*>(hs + (size_t)a * F + xrot(e)) =
+                reinterpret_cast<const float4*>(p.hbuf)[i];
+        }
+        __syncthreads();
+    }
+    const float* hsrc = HS ? hs : p.hbuf;
     const size_t nbg = (size_t)(F / FP8_BLK) * (H / FP8_BLK);
     for (int u = wid; u < ugpu * R; u += B_THREADS / 32) {
         const int e = u / R, rl = u - e * R;
@@ -233,13 +281,13 @@ __global__ void __launch_bounds__(B_THREADS, 1) fp8_down_kernel(ExpertParams p) 
         while (g0 < ntok) {
             const int rem = ntok - g0;
             if (rem >= 4) {
-                down_group<4>(wd, sd, p.hbuf, off + g0, F, lane, o_s, RMAX, rl);
+                down_group<4, HS>(wd, sd, hsrc, off + g0, F, lane, o_s, RMAX, rl);
                 g0 += 4;
             } else if (rem >= 2) {
-                down_group<2>(wd, sd, p.hbuf, off + g0, F, lane, o_s, RMAX, rl);
+                down_group<2, HS>(wd, sd, hsrc, off + g0, F, lane, o_s, RMAX, rl);
                 g0 += 2;
             } else {
-                down_group<1>(wd, sd, p.hbuf, off + g0, F, lane, o_s, RMAX, rl);
+                down_group<1, HS>(wd, sd, hsrc, off + g0, F, lane, o_s, RMAX, rl);
                 g0 += 1;
             }
         }
@@ -279,14 +327,21 @@ cudaError_t launch_expert_ffn_fp8(ExpertParams p, int num_sms, cudaStream_t s) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int RMAX = (p.H + num_sms - 1) / num_sms;
-    const size_t smem_b = (size_t)p.T * p.k * RMAX * 4;
+    const size_t o_bytes = (((size_t)p.T * p.k * RMAX + 3) & ~(size_t)3) * 4;
+    const size_t h_bytes = (size_t)p.T * p.k * p.F * 4;
+    const bool hs = o_bytes + h_bytes <= 200 * 1024;
+    const size_t smem_b = o_bytes + (hs ? h_bytes : 0);
     if (smem_b > 227 * 1024) return cudaErrorInvalidValue;
-    static size_t set_b = 0;
-    if (smem_b > set_b) {
-        e = cudaFuncSetAttribute(fp8_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_b);
+    static size_t set_b[2] = {0, 0};
+    const void* fb = hs ? (const void*)fp8_down_kernel<true> : (const void*)fp8_down_kernel<false>;
+    if (smem_b > set_b[hs ? 1 : 0]) {
+        e = cudaFuncSetAttribute(fb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_b);
         if (e != cudaSuccess) return e;
-        set_b = smem_b;
+        set_b[hs ? 1 : 0] = smem_b;
     }
-    fp8_down_kernel<<<num_sms, B_THREADS, smem_b, s>>>(p);
+    if (hs)
+        fp8_down_kernel<true><<<num_sms, B_THREADS, smem_b, s>>>(p);
+    else
+        fp8_down_kernel<false><<<num_sms, B_THREADS, smem_b, s>>>(p);
     return cudaGetLastError();
 }
