@@ -711,40 +711,63 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
 
 static constexpr size_t kSmemLimit4 = 227 * 1024 - 256;  // dynamic; the rest is static shared memory
 
+namespace {
+
+// Shared-memory plan of one FP4 launch (T tokens), or false when no plan fits.
+struct Fp4Plan {
+    int xm, tg, nst, nf;
+    size_t head, slot, fch;
+};
+
+bool fp4_plan(int H, int F, int T, int k, int SB, int G, Fp4Plan& pl) {
+    const int RMAX = (H + G - 1) / G;
+    const size_t TK = (size_t)T * k;
+    pl.xm = (size_t)T * H * 2 <= 32768 ? X_SMEM : X_GLOBAL;
+    const size_t xbytes = pl.xm == X_SMEM ? (size_t)T * H * 2 : 0;
+    const size_t head0 = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127);
+    const size_t chunk = (size_t)2 * FPC * (H / 2 + H / SB);
+    const size_t wpart = ((size_t)RMAX * (F / 2 + F / SB) + 127) & ~(size_t)127;
+    // The fill ring is kept small (3 x 4 KiB per SM): host reads queued beyond
+    // the link's bandwidth-delay product delay every SM's HBM reads.
+    pl.fch = 4096;
+    // token group of phase B: the most h rows (at most 16) whose staging in a
+    // slot (fp32 as copied, then f16 pairs) leaves room for two slots
+    int tg = T < 16 ? T : 16;
+    for (; tg >= 1; --tg) {
+        pl.head = head0 + (((7 * TK + 1 + 3 * (size_t)T + 2 * (size_t)tg) * 4 + 127) & ~(size_t)127);
+        pl.slot = wpart + (size_t)tg * F * 6;
+        if (pl.slot < chunk) pl.slot = chunk;
+        pl.slot = (pl.slot + 127) & ~(size_t)127;
+        if (pl.head + 2 * pl.fch + 2 * pl.slot <= kSmemLimit4) break;
+    }
+    if (tg < 1) return false;
+    pl.tg = tg;
+    pl.nst = (int)((kSmemLimit4 - pl.head - 2 * pl.fch) / pl.slot);
+    if (pl.nst > 4) pl.nst = 4;
+    pl.nf = (int)((kSmemLimit4 - pl.head - pl.slot * pl.nst) / pl.fch);
+    if (pl.nf > 3) pl.nf = 3;
+    return true;
+}
+
+}  // namespace
+
+bool expert_ffn_fp4_fits(int H, int F, int T, int k, int fmt, int num_sms) {
+    Fp4Plan pl;
+    return fp4_plan(H, F, T, k, fmt == FT_FMT_MXFP4 ? 32 : 16, num_sms, pl);
+}
+
 cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStream_t s) {
     if (fmt != FT_FMT_NVFP4 && fmt != FT_FMT_MXFP4) return cudaErrorInvalidValue;
     const int SB = fmt == FT_FMT_MXFP4 ? 32 : 16;
-    const int G = num_sms;
-    const int RMAX = (p.H + G - 1) / G;
-    const size_t TK = (size_t)p.T * p.k;
-    const int xm = (size_t)p.T * p.H * 2 <= 32768 ? X_SMEM : X_GLOBAL;
-    const size_t xbytes = xm == X_SMEM ? (size_t)p.T * p.H * 2 : 0;
+    Fp4Plan pl;
+    if (!fp4_plan(p.H, p.F, p.T, p.k, SB, num_sms, pl)) return cudaErrorInvalidValue;
+    const int xm = pl.xm;
     if (xm == X_GLOBAL && (!p.x16 || !p.xsc)) return cudaErrorInvalidValue;
-    const size_t head0 = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127);
-    const size_t chunk = (size_t)2 * FPC * (p.H / 2 + p.H / SB);
-    const size_t wpart = ((size_t)RMAX * (p.F / 2 + p.F / SB) + 127) & ~(size_t)127;
-    // The fill ring is kept small (3 x 4 KiB per SM): host reads queued beyond
-    // the link's bandwidth-delay product delay every SM's HBM reads.
-    const size_t fch = 4096;
-    // token group of phase B: the most h rows (at most 16) whose staging in a
-    // slot (fp32 as copied, then f16 pairs) leaves room for two slots
-    int tg = p.T < 16 ? p.T : 16;
-    size_t head = 0, slot = 0;
-    for (; tg >= 1; --tg) {
-        head = head0 + (((7 * TK + 1 + 3 * (size_t)p.T + 2 * (size_t)tg) * 4 + 127) & ~(size_t)127);
-        slot = wpart + (size_t)tg * p.F * 6;
-        if (slot < chunk) slot = chunk;
-        slot = (slot + 127) & ~(size_t)127;
-        if (head + 2 * fch + 2 * slot <= kSmemLimit4) break;
-    }
-    if (tg < 1) return cudaErrorInvalidValue;
-    int nst = (int)((kSmemLimit4 - head - 2 * fch) / slot);
-    if (nst > 4) nst = 4;
+    const size_t head = pl.head, slot = pl.slot, fch = pl.fch;
+    const int nst = pl.nst, nf = pl.nf;
     p.nstage = nst;
     p.stage_bytes = (unsigned)slot;
-    p.tgroup = tg;
-    int nf = (int)((kSmemLimit4 - head - slot * nst) / fch);
-    if (nf > 3) nf = 3;
+    p.tgroup = pl.tg;
     p.fill_chunk = (unsigned)fch;
     p.fill_slots = nf;
     const size_t smem = head + slot * nst + (size_t)nf * fch;
@@ -760,7 +783,7 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStre
         smem_set[var] = smem;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(G);
+    cfg.gridDim = dim3(num_sms);
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -413,6 +413,8 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);
 cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s);
 // fmt: FT_FMT_NVFP4 (e4m3 block-16 scales) or FT_FMT_MXFP4 (E8M0 block-32 scales)
 cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStream_t s);
+// whether the FP4 kernel has a shared-memory plan for T tokens (checked at init for T_max)
+bool expert_ffn_fp4_fits(int H, int F, int T, int k, int fmt, int num_sms);
 // block-FP8 records: gate/up + SwiGLU kernel, then down + merge kernel (no fused fill)
 cudaError_t launch_expert_ffn_fp8(ExpertParams p, int num_sms, cudaStream_t s);
 size_t route_ctl_smem_bytes(int T, int k, int E, int S);

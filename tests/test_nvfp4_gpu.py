@@ -253,3 +253,19 @@ def test_large_fp8_decode(ft):
     done = _replay(ft, sh, 512, [(1, 8), (64, 4)], 52.7, 150.0, 0.8, samples,
                    tok_sample=[0, 21, 42, 63], distinct=16)
     assert len(done) == len(samples)
+
+
+def test_fp4_init_rejects_a_t_max_without_a_kernel_plan(ft):
+    """T_max = 128 at the Large layer shape leaves the FP4 decode kernel no
+    shared-memory plan (its per-CTA output rows alone take 110 KB): init
+    refuses it instead of the first forward failing.  The control kernel's
+    own limit (26 KB here) is not what rejects it."""
+    import torch
+    pool = torch.empty(4096, dtype=torch.uint8, pin_memory=True)
+    with pytest.raises(ft.FtError):
+        ft.Context(1, 256, 8, 4096, 2048, 16, pool, fmt=ft.FT_FMT_NVFP4, T_max=128,
+                   nvfp4_global=np.ones(256, dtype=np.float32))
+    with pytest.raises(ft.FtError):
+        ft.Context(1, 256, 8, 4096, 2048, 16, pool, fmt=ft.FT_FMT_MXFP4, T_max=128)
+    ctx = ft.Context(1, 256, 8, 4096, 2048, 16, pool, fmt=ft.FT_FMT_MXFP4, T_max=64)
+    ctx.close()
