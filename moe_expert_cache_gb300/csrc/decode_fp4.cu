@@ -54,24 +54,6 @@ constexpr size_t HEAD = 256;
 enum { X_SMEM = 0, X_GLOBAL = 1 };
 constexpr int kXTarget = 14;  // token rows are scaled so their largest magnitude is in [2^14, 2^15)
 
-// e2m1 decode by bit placement, two values at a time: codes J and J + 4 of
-// word w (nibble J, low nibble first) become the two halves of an f16x2
-// whose exponent field holds the code's two exponent bits, whose top
-// mantissa bit holds its mantissa bit and whose sign is its sign.  Each half
-// equals value * 2^-14 exactly (the subnormal code 1, 0.5, included): both
-// nibbles of a pair move by the same shift, so a pair costs two shifts and
-// two masks.  The halves are widened to fp32 exactly and the row sums are
-// rescaled by 2^14 (kValScale).
-constexpr float kValScale = 16384.0f;  // 2^14
-
-template <int J>
-__device__ __forceinline__ float2 e2m1x2_scaled(uint32_t w) {
-    const uint32_t mag = (J < 3 ? (w << (J < 3 ? 9 - 4 * J : 0)) : (w >> 3)) & 0x0E000E00u;
-    const uint32_t sgn = (w << (12 - 4 * J)) & 0x80008000u;
-    const uint32_t h = mag | sgn;
-    return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
-
 // Scale bytes: two e4m3 codes (low byte first) to a float pair, by the
 // hardware conversion (one per 16 values).
 __device__ __forceinline__ float2 e4m3x2_f32(const uint8_t* p2) {
@@ -104,16 +86,6 @@ __device__ __forceinline__ float2 scales32(const uint8_t* srow, int v) {
 __device__ __forceinline__ int swz_f32(int e) {  // element e of a row -> its stored position
     const int v = e >> 5, i = (e >> 2) & 7;
     return (v << 5) | (((i + v) & 7) << 2) | (e & 3);
-}
-
-// 32 h values of a staged row starting at element 32*v.
-__device__ __forceinline__ void load_h32(const float* hr, int v, float* x) {
-    const float4* p = reinterpret_cast<const float4*>(hr + (size_t)v * 32);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float4 q = p[(i + v) & 7];
-        x[4 * i] = q.x; x[4 * i + 1] = q.y; x[4 * i + 2] = q.z; x[4 * i + 3] = q.w;
-    }
 }
 
 // Phase-A activations as f16 pairs, in the order the weight decode produces:
@@ -176,7 +148,13 @@ __device__ __forceinline__ float stage_x_row(const uint4* xr, int H, uint4* dst,
     return ldexpf(1.f, 14 - a);
 }
 
-// The four f16x2 weight pairs of one word (value * 2^-14 each), in J order.
+// e2m1 decode by bit placement, two values at a time: codes J and J + 4 of
+// word w (nibble J, low nibble first) become the two halves of an f16x2
+// whose exponent field holds the code's two exponent bits, whose top
+// mantissa bit holds its mantissa bit and whose sign is its sign.  Each half
+// equals value * 2^-14 exactly (the subnormal code 1, 0.5, included); both
+// nibbles of a pair move by the same shift, so a pair costs two shifts and
+// two masks.  The four pairs of one word, in J order:
 __device__ __forceinline__ void e2m1_word_h2(uint32_t w, uint32_t* d) {
     d[0] = ((w << 9) & 0x0E000E00u) | ((w << 12) & 0x80008000u);
     d[1] = ((w << 5) & 0x0E000E00u) | ((w << 8) & 0x80008000u);
@@ -202,32 +180,6 @@ __device__ __forceinline__ float dot16_h(const uint32_t* d, const uint4& x0, con
     q = hfma2_u(d[7], x1.w, q);
     const float2 f = __half22float2(__hadd2(p, q));
     return f.x + f.y;
-}
-
-// eight values of one word against x[0..7], added to a (values 0-3) and b
-// (values 4-7), in units of 2^-14
-__device__ __forceinline__ void fp4_word(uint32_t w, const float* x, float& a, float& b) {
-    const float2 v0 = e2m1x2_scaled<0>(w), v1 = e2m1x2_scaled<1>(w);
-    const float2 v2 = e2m1x2_scaled<2>(w), v3 = e2m1x2_scaled<3>(w);
-    a = fmaf(v0.x, x[0], a);
-    b = fmaf(v0.y, x[4], b);
-    a = fmaf(v1.x, x[1], a);
-    b = fmaf(v1.y, x[5], b);
-    a = fmaf(v2.x, x[2], a);
-    b = fmaf(v2.y, x[6], b);
-    a = fmaf(v3.x, x[3], a);
-    b = fmaf(v3.y, x[7], b);
-}
-
-// sum over 32 values of one uint4 (two 16-value halves): sc0 * half0 +
-// sc1 * half1, in units of 2^-14
-__device__ __forceinline__ float fp4_dot32(const uint4& w, const float* x, float sc0, float sc1) {
-    float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
-    fp4_word(w.x, x, a0, b0);
-    fp4_word(w.y, x + 8, a0, b0);
-    fp4_word(w.z, x + 16, a1, b1);
-    fp4_word(w.w, x + 24, a1, b1);
-    return fmaf(sc0, a0 + b0, sc1 * (a1 + b1));
 }
 
 // Phase A: gate and up rows of one feature against NT tokens; returns the
