@@ -1,0 +1,89 @@
+"""bench.py's host-side accounting on CPU: the algorithmic bytes of a decode
+launch, the choice of the bounding side of the roofline, and the DRAM
+traffic taken from a committed capture (scaled by records read, dropped once
+the kernel source changes)."""
+import hashlib
+import json
+import os
+import subprocess
+import sys
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import synth  # noqa: E402
+
+
+def test_kernel_bytes_counts_fills_hits_and_activations():
+    sh = synth.Shape(L=1, E=8, k=2, H=64, F=128)
+    rb = sh.record_bytes
+    d = {"calls": 3, "fills": 2, "hits": 4, "assign": 10}
+    T = 2
+    kb = bench.kernel_bytes(sh, T, d)
+    link = 2 * rb
+    assert kb["expert_ffn"]["link"] == link
+    # fills written + hit records read + x (bf16) + h written and read (fp32) + partial_C and y (fp32)
+    assert kb["expert_ffn"]["hbm"] == link + 4 * rb + 3 * T * 64 * 2 + 2 * 10 * 128 * 4 + 3 * T * 64 * 4 * 2
+    assert kb["route_ctl"]["hbm"] == 3 * (T * 8 * 4 + 2 * T * 2 * 4)
+
+
+def _kernels(link_bytes, hbm_bytes, us):
+    gbs = lambda b: b / (us * 1e-6) / 1e9  # noqa: E731
+    return {"expert_ffn": {"us_per_launch": us,
+                           "link": {"bytes_per_launch": link_bytes, "achieved_GBps": gbs(link_bytes),
+                                    "peak_GBps": 200.0, "frac": gbs(link_bytes) / 200.0},
+                           "hbm": {"bytes_per_launch": hbm_bytes, "achieved_GBps": gbs(hbm_bytes),
+                                   "peak_GBps": 6000.0, "frac": gbs(hbm_bytes) / 6000.0}}}
+
+
+def test_roofline_picks_the_side_whose_bytes_take_longer():
+    peaks = {"hbm_gbs": 6000.0, "source": "measured"}
+    # 10 MB over a 200 GB/s link (50 us) outweighs 60 MB of HBM (10 us)
+    r = bench.roofline_entry("expert_ffn", _kernels(10e6, 60e6, 80.0), peaks, 200.0)
+    assert r["bound"] == "h2d" and r["peak"] == 200.0
+    assert abs(r["frac"] - (10e6 / 80e-6 / 1e9) / 200.0) < 1e-12
+    # no link bytes: HBM bound
+    r = bench.roofline_entry("expert_ffn", _kernels(0, 60e6, 20.0), peaks, 200.0)
+    assert r["bound"] == "hbm" and r["peak"] == 6000.0
+
+
+def test_traffic_is_scaled_by_records_and_dropped_when_the_source_changes(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({
+        "per_record": {"source": "k.cu", "source_sha": sha, "dram_bytes": 800, "records_read": 8},
+        "per_launch": {"source": "k.cu", "source_sha": sha, "dram_bytes_per_launch": 1234}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_from_profiles("per_record", 5.5) == 550
+    assert bench.traffic_from_profiles("per_record") is None        # no record count to scale by
+    assert bench.traffic_from_profiles("per_launch") == 1234
+    assert bench.traffic_from_profiles("absent", 3) is None
+    src.write_text("kernel v2")                                      # the kernel changed since
+    assert bench.traffic_from_profiles("per_record", 5.5) is None
+
+
+def test_committed_traffic_entries_name_existing_sources():
+    d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for k, v in d.items():
+        if k.startswith("_"):
+            continue
+        assert os.path.exists(os.path.join(ROOT, v["source"])), k
+        assert v["records_read"] > 0 and v["dram_bytes"] > 0
+
+
+def test_cli_help_needs_no_gpu():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0
+    for flag in ("--gpus", "--steps", "--warmup", "--impl", "--no-fp4", "--fp4-only", "--ncu-fp4", "--ncu-case"):
+        assert flag in r.stdout
+
+
+def test_warmup_below_three_is_refused():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode != 0 and "--warmup must be >= 3" in (r.stderr + r.stdout)
