@@ -92,7 +92,11 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples go to FT_CLOCKS_DIR (default: the system temporary
+        # directory); the JSON line carries their summary
+        import tempfile
+        self.path = os.path.join(os.environ.get("FT_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"ft_clocks_rank{gpu_index}.csv")
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.f = open(self.path, "w")
