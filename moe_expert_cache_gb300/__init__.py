@@ -226,7 +226,15 @@ def _ptr(a) -> int | None:
 
 
 class Context:
-    """Owner of one ft_ctx*; every method raises FtError on a non-zero status."""
+    """Owner of one ft_ctx*; every method raises FtError on a non-zero status.
+
+    ``host_pool`` is a page-locked host tensor (or address) holding L*E
+    records of ``record_bytes(H, F, fmt)`` bytes.  ``fmt`` is FT_FMT_BF16,
+    FT_FMT_NVFP4 (then ``nvfp4_global`` is a fp32 array of L*E per-record
+    globals), FT_FMT_MXFP4 or FT_FMT_FP8 (block-FP8); the record layouts are
+    in include/ft.h.  Streams are ``torch.cuda.Stream.cuda_stream`` handles
+    (0: the legacy default stream).
+    """
 
     def __init__(self, L, E, k, H, F, S, host_pool, *, fmt=FT_FMT_BF16, T_max=16, T_prefill_max=0,
                  nvfp4_global=None, compute_stream=0, transfer_stream=0):
