@@ -87,3 +87,24 @@ def test_warmup_below_three_is_refused():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], capture_output=True,
                        text=True, timeout=120)
     assert r.returncode != 0 and "--warmup must be >= 3" in (r.stderr + r.stdout)
+
+
+def test_clock_sampler_summary_from_a_stand_in_nvidia_smi(tmp_path, monkeypatch):
+    # a stand-in for nvidia-smi on PATH: two samples under load, one with the
+    # power cap active, then it idles until the sampler stops it
+    exe = tmp_path / "bin" / "nvidia-smi"
+    exe.parent.mkdir()
+    exe.write_text("#!/bin/sh\n"
+                   "echo '0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                   "echo '0, 2040, 2070, 1399.0, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                   "exec sleep 30\n")
+    exe.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{exe.parent}:{os.environ['PATH']}")
+    monkeypatch.setenv("FT_CLOCKS_DIR", str(tmp_path / "clocks"))
+    cs = bench.ClockSampler(0)
+    import time
+    time.sleep(0.5)
+    got = cs.stop()
+    assert got["sm_mhz"] == 2055.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"]
+    assert (tmp_path / "clocks" / "ft_clocks_rank0.csv").exists()
