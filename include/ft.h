@@ -282,11 +282,11 @@ ft_status ft_measure_link(ft_ctx* ctx, int32_t n_records, int32_t reps, double* 
 /*
  * ft_expert_ffn_noalloc -- the decode expert FFN without a context and
  * without allocating anything.  The pages have no counterpart to this entry
- * point; it exists for callers that cannot allocate device memory once they
- * run: code inside a CUDA graph capture, where allocation calls are illegal;
- * engines that carve all device memory into their own pools at start-up; and
- * latency-critical paths that cannot afford the synchronisation of
- * cudaMalloc / cudaFree.  ft_layer_init allocates, so such callers use this.
+ * point.  It exists for callers that may not allocate device memory once
+ * they run: serving engines that carve all device memory into their own
+ * pools at start-up and forbid later allocations, and latency-critical paths
+ * that cannot afford the device synchronisation of cudaMalloc / cudaFree.
+ * ft_layer_init allocates, so such callers use this.
  *
  * For every route (t, j) with route_records[t*k+j] >= 0 it computes
  * FFN(x_t) = W_d (SiLU(W_g x_t) * (W_u x_t)) over that BF16 record and writes
@@ -297,7 +297,9 @@ ft_status ft_measure_link(ft_ctx* ctx, int32_t n_records, int32_t reps, double* 
  *                  layout), 16-byte aligned; read only.
  *   route_records  DEVICE int32 [T, k]: record index of each route, or -1 for a
  *                  route computed elsewhere (the CPU set).  An index outside
- *                  [-1, n_records) is treated as -1.
+ *                  [-1, n_records) is an error found on the device: the call
+ *                  then routes nothing (y = partial_C, or 0 without it) and
+ *                  latches FT_ERR_DEVICE for ft_noalloc_status.
  *   gates          DEVICE fp32 [T, k].
  *   x              DEVICE bf16 [T, H];  partial_C DEVICE fp32 [T, H] or NULL;
  *   y              DEVICE fp32 [T, H], not aliasing x or partial_C.
@@ -309,15 +311,26 @@ ft_status ft_measure_link(ft_ctx* ctx, int32_t n_records, int32_t reps, double* 
  * that loads the library, held until the process exits; no cudaMalloc,
  * cudaFree or allocating library call is made.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Every call shares
- * the array and leaves its contents behind; each call rewrites what it reads.
- * Calls that overlap on the GPU (several streams or host threads) race on the
- * array: serialise them.  Async; returns FT_ERR_ARG or FT_ERR_CUDA on failure.
+ * current.  Every call shares the array and leaves its contents behind; each
+ * call rewrites what it reads.  Calls that overlap on the GPU (several streams
+ * or host threads) race on the array: serialise them.  Async; returns
+ * FT_ERR_ARG (host checks) or FT_ERR_CUDA; problems found on the device are
+ * reported by ft_noalloc_status.
  */
 #define FT_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u + 65536u)
 ft_status ft_expert_ffn_noalloc(const void* records, int32_t n_records, const int32_t* route_records,
                                 const float* gates, const void* x, const float* partial_C, float* y,
                                 int32_t T, int32_t k, int32_t H, int32_t F, void* stream);
+
+/*
+ * ft_noalloc_status -- synchronise `stream` (a cudaStream_t, NULL = legacy
+ * default stream) and return, then clear, the error word that the
+ * ft_expert_ffn_noalloc calls on the current device latched since the last
+ * ft_noalloc_status: FT_OK, FT_ERR_DEVICE (an out-of-range record index) or
+ * FT_ERR_TIMEOUT (a bounded wait in the expert kernel gave up; that call's y
+ * is not valid).  Allocates nothing.  FT_ERR_CUDA if a CUDA call fails.
+ */
+ft_status ft_noalloc_status(void* stream);
 
 /* ---- observability and test surface (all sync) ------------------------- */
 
@@ -366,8 +379,23 @@ int32_t ft_num_slots(const ft_ctx* ctx);
 
 /* Synchronise the context's streams and return (and clear) the sticky device
  * error word: FT_OK, FT_ERR_DEVICE or FT_ERR_TIMEOUT; FT_ERR_CUDA if a CUDA
- * error is pending. */
+ * error is pending.  On FT_ERR_TIMEOUT the outputs of the calls since the
+ * last status read are not valid, and, because a wait that gave up may have
+ * left a fill record incomplete, every slot is evicted (maps emptied, stamps
+ * 0, clock kept): later calls refill from the host pool, which stays the
+ * source of truth (deepmox, "How residency follows demand without leaving
+ * the device"). */
 ft_status ft_get_status(ft_ctx* ctx);
+
+/* Limit, in nanoseconds of GPU global time, of the BF16 decode expert
+ * kernel's waits on the progress of its other warps and CTAs (ring slots,
+ * fill chunks, completion counters); each such wait that runs out latches
+ * FT_ERR_TIMEOUT and the kernel winds down.  Waits for a thread's own copies
+ * in flight keep the 2 s default, so a kernel never exits with a copy
+ * landing in its shared memory.  ns = 0 restores the default (2e9); else
+ * 1000 <= ns <= 2e9 (FT_ERR_ARG otherwise).  Host only; applies to the
+ * launches that follow.  The other kernels always use the default. */
+ft_status ft_set_wait_limit(ft_ctx* ctx, uint64_t ns);
 
 /* Free every library-owned resource.  Syncs.  ctx may be NULL. */
 void ft_destroy(ft_ctx* ctx);

@@ -76,6 +76,8 @@ _SIGS = {
     "ft_num_slots": (_c_int, [_c_p]),
     "ft_expert_ffn_noalloc": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
                                        _c_p]),
+    "ft_noalloc_status": (_c_int, [_c_p]),
+    "ft_set_wait_limit": (_c_int, [_c_p, ctypes.c_uint64]),
     "ft_get_status": (_c_int, [_c_p]),
     "ft_destroy": (None, [_c_p]),
 }
@@ -198,8 +200,17 @@ def expert_ffn_noalloc(records, n_records, route_records, gates, x, partial_C, y
                                         stream)
 
 
+def noalloc_status(stream=None) -> int:
+    """Sync `stream`; return and clear the allocation-free path's error word."""
+    return load().ft_noalloc_status(stream)
+
+
 def num_slots(ctx) -> int:
     return load().ft_num_slots(ctx)
+
+
+def set_wait_limit(ctx, ns) -> int:
+    return load().ft_set_wait_limit(ctx, ns)
 
 
 def get_status(ctx) -> int:
@@ -327,6 +338,10 @@ class Context:
 
     def status(self) -> int:
         return get_status(self.h)
+
+    def set_wait_limit(self, ns: int):
+        """Limit of the BF16 decode kernel's progress waits (0: the 2 s default)."""
+        _check(set_wait_limit(self.h, ns), "ft_set_wait_limit")
 
     def profile_enable(self, on: bool = True):
         _check(profile_enable(self.h, 1 if on else 0), "ft_profile_enable")

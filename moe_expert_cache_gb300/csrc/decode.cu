@@ -477,12 +477,12 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             const uint32_t par = (uint32_t)(g / nf) & 1u;
             int w = 1;
             if (lane == 0) {
-                w = ft::mbar_wait(&ffull[s], par, p.err);
+                w = ft::mbar_wait(&ffull[s], par, p.err, p.wait_ns);
                 if (w) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // cp.async data -> bulk store
                     store(g, s);
                     if (g == n_wd - 1) publish_wd(1);
-                    w = ft::mbar_wait(&fcons[s], par, p.err);
+                    w = ft::mbar_wait(&fcons[s], par, p.err, p.wait_ns);
                     ft::bulk_wait_read_all();
                 }
             }
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     if (wid == FILL_MATH_WARP) {
         for (int g = 0; g < n_fill; ++g) {
             const int s = g % nf;
-            if (!__all_sync(0xffffffffu, ft::mbar_wait(&ffull[s], (uint32_t)(g / nf) & 1u, p.err))) break;
+            if (!__all_sync(0xffffffffu, ft::mbar_wait(&ffull[s], (uint32_t)(g / nf) & 1u, p.err, p.wait_ns))) break;
             if (g < n_wd) {  // a W_d piece: acknowledged so the ring cannot lap this warp
                 __syncwarp();
                 if (lane == 0) ft::mbar_arrive(&fcons[s]);
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 int armed;
                 while ((armed = ft::ld_acquire_cta(&s_armed)) >= 0 && armed <= it) {
                     __nanosleep(128);  // leave the issue slots to the consumer warps
-                    if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                    if (ft::globaltimer() - t0 > p.wait_ns) {
                         atomicOr(p.err, FT_DEVERR_TIMEOUT);
                         armed = -1;
                         break;
@@ -573,9 +573,9 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 unsigned o = 0;
                 for (int e = e0; e < e1; ++e) {
                     if (e < nA)
-                        ft::wait_count(hits_done, (unsigned)G, p.err);
+                        ft::wait_count(hits_done, (unsigned)G, p.err, p.wait_ns);
                     else
-                        ft::wait_count(&p.ready[e], (unsigned)F, p.err);
+                        ft::wait_count(&p.ready[e], (unsigned)F, p.err, p.wait_ns);
                     ft::bulk_g2s(dst + o + wpad, p.hbuf + (size_t)m_off[e] * F, hbytes(e), &full[st]);
                     o += wpad + ((hbytes(e) + 127u) & ~127u);
                 }
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                 if (!isB && a >= NA) break;
                 const int st = it % nst;
                 if (it == nst) prefetch_wd();
-                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
+                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err, p.wait_ns)) { ok = false; break; }
                 unsigned char* dst = ring + (size_t)st * slot_bytes;
                 if (!isB) {
                     const int ent = a / cpe;
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                     int v;
                     while ((v = ft::ld_acquire_cta(&s_wd)) == 0) {
                         __nanosleep(128);
-                        if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                        if (ft::globaltimer() - t0 > p.wait_ns) {
                             atomicOr(p.err, FT_DEVERR_TIMEOUT);
                             break;
                         }
@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         const bool isB = stage_due(a, e0);
         if (!isB && a >= NA) break;
         const int st = it % nst;
-        const bool ok = !failed && __all_sync(0xffffffffu, ft::mbar_wait(&full[st], (it / nst) & 1, p.err));
+        const bool ok = !failed && __all_sync(0xffffffffu, ft::mbar_wait(&full[st], (it / nst) & 1, p.err, p.wait_ns));
         failed = !ok;
         const unsigned char* sb = ring + (size_t)st * slot_bytes;
         if (!isB) {
@@ -756,6 +756,7 @@ static constexpr int kFillSlots = 3;                     // fused-fill ring chun
 // feature over H / nks columns when one feature does not fit.
 cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     const int G = num_sms;
+    if (p.wait_ns == 0) p.wait_ns = FT_WAIT_LIMIT_NS;
     const int RMAX = (p.H + G - 1) / G;
     const bool xf32 = (size_t)p.T * p.H * 4 <= 65536;
     const size_t xbytes = (size_t)p.T * p.H * (xf32 ? 4 : 2);
@@ -788,12 +789,8 @@ cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
     p.fill_fpf = fpf;
     p.fill_nks = nks;
     const size_t smem = head + slot * nst + (size_t)nf * fch;
-    static size_t smem_set = 0;
-    if (smem != smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(expert_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+    cudaError_t e = ensure_dynamic_smem((const void*)expert_ffn_kernel, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(EXPERT_THREADS);

@@ -727,13 +727,8 @@ cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStre
                                               : (const void*)expert_ffn_fp4_kernel<X_GLOBAL, 16>)
                               : (xm == X_SMEM ? (const void*)expert_ffn_fp4_kernel<X_SMEM, 32>
                                               : (const void*)expert_ffn_fp4_kernel<X_GLOBAL, 32>);
-    static size_t smem_set[4] = {0, 0, 0, 0};  // per kernel variant: set only when it grows
-    const int var = xm + (SB == 32 ? 2 : 0);
-    if (smem > smem_set[var]) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        smem_set[var] = smem;
-    }
+    cudaError_t e = ensure_dynamic_smem(fn, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
     cfg.blockDim = dim3(THREADS);

@@ -313,12 +313,10 @@ cudaError_t launch_expert_ffn_fp8(ExpertParams p, int num_sms, cudaStream_t s) {
     const size_t xbytes = (size_t)p.T * p.H * 4;
     const bool xs = xbytes <= 96 * 1024;
     const size_t smem_a = xs ? xbytes : 0;
-    static size_t set_a[2] = {0, 0};
     const void* fa = xs ? (const void*)fp8_gateup_kernel<true> : (const void*)fp8_gateup_kernel<false>;
-    if (smem_a > set_a[xs ? 1 : 0]) {
-        cudaError_t e = cudaFuncSetAttribute(fa, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a);
+    if (smem_a > 0) {
+        cudaError_t e = ensure_dynamic_smem(fa, smem_a);
         if (e != cudaSuccess) return e;
-        set_a[xs ? 1 : 0] = smem_a;
     }
     if (xs)
         fp8_gateup_kernel<true><<<2 * num_sms, A_THREADS, smem_a, s>>>(p);
@@ -332,13 +330,9 @@ cudaError_t launch_expert_ffn_fp8(ExpertParams p, int num_sms, cudaStream_t s) {
     const bool hs = o_bytes + h_bytes <= 200 * 1024;
     const size_t smem_b = o_bytes + (hs ? h_bytes : 0);
     if (smem_b > 227 * 1024) return cudaErrorInvalidValue;
-    static size_t set_b[2] = {0, 0};
     const void* fb = hs ? (const void*)fp8_down_kernel<true> : (const void*)fp8_down_kernel<false>;
-    if (smem_b > set_b[hs ? 1 : 0]) {
-        e = cudaFuncSetAttribute(fb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_b);
-        if (e != cudaSuccess) return e;
-        set_b[hs ? 1 : 0] = smem_b;
-    }
+    e = ensure_dynamic_smem(fb, smem_b);
+    if (e != cudaSuccess) return e;
     if (hs)
         fp8_down_kernel<true><<<num_sms, B_THREADS, smem_b, s>>>(p);
     else

@@ -56,6 +56,7 @@ struct ft_ctx {
     unsigned* ready;
     float* hbuf;
     bool fill_pending;
+    unsigned long long wait_ns;  // limit of the BF16 decode kernel's progress waits
     int last_T;
     bool have_ctl;
     PrefillState pf;
@@ -216,6 +217,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     c->cs = (cudaStream_t)compute_stream;
     c->ts = (cudaStream_t)transfer_stream;
     c->host_pool = host_pool;
+    c->wait_ns = FT_WAIT_LIMIT_NS;
     ft_status st = FT_OK;
     auto fail = [&](ft_status s) { free_ctx(c); return s; };
 #define INIT_CUDA(call)                                                                        \
@@ -367,6 +369,7 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.info = c->info; p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok;
     p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err; p.gbar = c->gbar;
     p.wl_fid = c->wl_fid; p.gscale = c->nvfp4_global; p.x16 = c->x16; p.xsc = c->xsc; p.hmax = c->hmax;
+    p.wait_ns = c->wait_ns;
     if (c->fmt == FT_FMT_FP8) FT_CUDA(flush_fill(c));  // no fused fill in the FP8 kernels
     p.do_fill = c->fill_pending ? 1 : 0;
     p.host_pool = (const uint4*)c->host_pool_dev;
@@ -616,8 +619,23 @@ ft_status ft_get_status(ft_ctx* c) {
         const unsigned z = 0;
         if (cudaMemcpy(c->err, &z, 4, cudaMemcpyHostToDevice) != cudaSuccess) return FT_ERR_CUDA;
     }
-    if (e & FT_DEVERR_TIMEOUT) return FT_ERR_TIMEOUT;
+    if (e & FT_DEVERR_TIMEOUT) {
+        // A wait that gave up may have left a fill record incomplete: every
+        // slot is evicted, and the host pool refills the cache on demand.
+        if (cudaMemset(c->slot_for_id, 0xff, (size_t)c->L * c->E * 4) != cudaSuccess ||
+            cudaMemset(c->id_for_slot, 0xff, (size_t)c->S * 4) != cudaSuccess ||
+            cudaMemset(c->stamps, 0, (size_t)c->S * 4) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            return FT_ERR_CUDA;
+        c->have_ctl = false;
+        return FT_ERR_TIMEOUT;
+    }
     if (e & FT_DEVERR_ARG) return FT_ERR_DEVICE;
+    return FT_OK;
+}
+
+ft_status ft_set_wait_limit(ft_ctx* c, uint64_t ns) {
+    if (!c || (ns != 0 && (ns < 1000 || ns > FT_WAIT_LIMIT_NS))) return FT_ERR_ARG;
+    c->wait_ns = ns ? ns : FT_WAIT_LIMIT_NS;
     return FT_OK;
 }
 

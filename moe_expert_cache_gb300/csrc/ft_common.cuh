@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 // Device error bits (latched in ctx->err, read by ft_get_status).
 #define FT_DEVERR_ARG      1u   // invalid ids / non-finite logits
 #define FT_DEVERR_TIMEOUT  2u   // a bounded wait gave up
@@ -66,15 +68,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; bounded by
-// FT_WAIT_LIMIT_NS.  Returns false (and latches the timeout bit) on give-up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+// Wait for the phase with the given parity to complete; bounded by limit_ns
+// of global time.  Returns false (and latches the timeout bit) on give-up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
+                                          uint64_t limit_ns = FT_WAIT_LIMIT_NS) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 63u) == 0 && globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+        if ((it & 63u) == 0 && globaltimer() - t0 > limit_ns) {
             atomicOr(err, FT_DEVERR_TIMEOUT);
             return false;
         }
@@ -210,6 +213,8 @@ __device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned G, unsigned
 
 // Producer-side drain: wait (bounded) for the last phase of every slot that
 // received a copy, so no bulk copy is in flight into shared memory at exit.
+// Always the full FT_WAIT_LIMIT_NS, whatever limit the kernel's other waits
+// use: a copy still in flight must land before the CTA may exit.
 __device__ __forceinline__ void drain_ring(uint64_t* full, int issued, int nst, unsigned* err) {
     for (int it = issued - nst; it < issued; ++it)
         if (it >= 0) mbar_wait(&full[it % nst], (it / nst) & 1, err);
@@ -229,14 +234,15 @@ __device__ __forceinline__ int ld_acquire_cta(const int* p) {
 // fill i, then order the async proxy after those generic writes.
 // Bounded wait until *c >= target (acquire at GPU scope), then order the
 // async proxy (bulk copies) after the acquired writes.
-__device__ __forceinline__ bool wait_count(const unsigned* c, unsigned target, unsigned* err) {
+__device__ __forceinline__ bool wait_count(const unsigned* c, unsigned target, unsigned* err,
+                                           uint64_t limit_ns = FT_WAIT_LIMIT_NS) {
     const uint64_t t0 = globaltimer();
     for (unsigned it = 0;; ++it) {
         unsigned v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
         if (v >= target) break;
         __nanosleep(64);  // a poll of L2: leave the issue slots to the math warps
-        if ((it & 15u) == 15u && globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+        if ((it & 15u) == 15u && globaltimer() - t0 > limit_ns) {
             atomicOr(err, FT_DEVERR_TIMEOUT);
             return false;
         }
@@ -324,6 +330,40 @@ __device__ __forceinline__ void fill_share_tma(const uint8_t* host, uint8_t* poo
 
 }  // namespace ft
 
+// ------------------------------------------------------------- host side
+
+// Raise `kernel`'s dynamic shared-memory limit on the current device to at
+// least `bytes`.  The attribute belongs to one (kernel, device) pair, so the
+// largest size set so far is remembered per pair; the lock makes concurrent
+// host threads safe.  A pair that finds the table full is set on every call.
+inline cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+    struct Set {
+        const void* fn;
+        int dev;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static Set tab[256];
+    static int n = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    Set* hit = nullptr;
+    for (int i = 0; i < n && !hit; ++i)
+        if (tab[i].fn == kernel && tab[i].dev == dev) hit = &tab[i];
+    if (hit && hit->bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    if (!hit && n < (int)(sizeof(tab) / sizeof(tab[0]))) {
+        hit = &tab[n++];
+        hit->fn = kernel;
+        hit->dev = dev;
+    }
+    if (hit) hit->bytes = bytes;
+    return cudaSuccess;
+}
+
 // ------------------------------------------------------------------ params
 
 struct CtlParams {
@@ -402,6 +442,8 @@ struct ExpertParams {
     uint4* x16;               // FP4 decode scratch: T_max x H activations as scaled f16 pairs
     float* xsc;               // FP4 decode scratch: T_max row factors
     unsigned long long* hmax; // FP4 decode scratch: T_max per-token |h| maxima, tagged (zeroed at init)
+    unsigned long long wait_ns;  // BF16: limit of the waits on other warps' or CTAs' progress
+                                 // (waits for a thread's own copies keep FT_WAIT_LIMIT_NS)
     int tgroup;               // NVFP4: tokens per phase-B item
     int nstage;               // pipeline depth (stages in shared memory)
     unsigned stage_bytes;     // bytes of one stage

@@ -1,25 +1,26 @@
 // ft_expert_ffn_noalloc: the decode expert FFN for callers that cannot
 // allocate device memory.
 //
-// Some callers of this library are not allowed to call cudaMalloc once they
-// are running.  Examples: code that runs while a CUDA graph is being
-// captured, where allocation calls are illegal; serving engines that carve
-// all device memory into their own pools at start-up and forbid later
-// allocations; latency-critical paths where the implicit synchronisation of
-// cudaMalloc/cudaFree is not acceptable.  A context (ft_layer_init) allocates
-// its slot pool, maps and scratch, so those callers need a context-free
-// entry point.  This one runs the same expert kernel as ft_moe_forward, on
-// records the caller already holds in device memory, and keeps its scratch
-// (the SwiGLU activations h, the worklist and the completion counters) in one
-// file-scope device array of fixed size.
+// Some callers of this library may not call cudaMalloc once they are
+// running: serving engines that carve all device memory into their own pools
+// at start-up and forbid later allocations, and latency-critical paths where
+// the implicit device synchronisation of cudaMalloc / cudaFree is not
+// acceptable.  A context (ft_layer_init) allocates its slot pool, maps and
+// scratch, so those callers need a context-free entry point.  This one runs
+// the same expert kernel as ft_moe_forward, on records the caller already
+// holds in device memory, and keeps its scratch (the SwiGLU activations h,
+// the worklist, the completion counters and an error word) in one file-scope
+// device array of fixed size.
 //
 // That array exists once per device that loads the library and stays
 // allocated until the process exits.  Every call shares it and finds the
 // previous call's contents there: the preparation kernel rewrites every
 // field the expert kernel reads, and the completion counters return to their
-// resting value (zero) after each call.  Calls that overlap on the GPU (different
-// streams, or concurrent host threads) race on the array and must not be
-// issued.
+// resting value (zero) after each call.  The error word is sticky: problems
+// found by any call (an out-of-range record index, a bounded wait that gave
+// up) stay latched until ft_noalloc_status reads and clears them.  Calls
+// that overlap on the GPU (different streams, or concurrent host threads)
+// race on the array and must not be issued.
 #include "ft_common.cuh"
 #include "../../include/ft.h"
 
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(PREP_THREADS) noalloc_prep_kernel(const int* _
     __shared__ int s_rec[MAX_ROUTES];
     __shared__ float s_g[MAX_ROUTES];
     __shared__ unsigned char s_lead[MAX_ROUTES];
-    __shared__ int s_ug, s_na;
+    __shared__ int s_ug, s_na, s_bad;
     const int TK = T * k, tid = threadIdx.x;
     int* info = reinterpret_cast<int*>(scratch + OFF_INFO);
     int* wl_slot = reinterpret_cast<int*>(scratch + OFF_META);
@@ -63,11 +64,21 @@ __global__ void __launch_bounds__(PREP_THREADS) noalloc_prep_kernel(const int* _
     if (tid == 0) {
         s_ug = 0;
         s_na = 0;
+        s_bad = 0;
     }
+    __syncthreads();
     for (int a = tid; a < TK; a += PREP_THREADS) {
         const int r = route_records[a];
-        s_rec[a] = (r >= 0 && r < n_records) ? r : -1;
+        if (r < -1 || r >= n_records) s_bad = 1;
+        s_rec[a] = r;
         s_g[a] = gates[a];
+    }
+    __syncthreads();
+    // an index outside [-1, n_records) latches the error and the call routes
+    // nothing to the GPU: y = partial_C
+    if (s_bad) {
+        for (int a = tid; a < TK; a += PREP_THREADS) s_rec[a] = -1;
+        if (tid == 0) atomicOr(reinterpret_cast<unsigned*>(scratch + OFF_ERR), FT_DEVERR_ARG);
     }
     __syncthreads();
     for (int a = tid; a < TK; a += PREP_THREADS) {
@@ -119,6 +130,28 @@ struct DeviceSetup {
     int num_sms = 0;
 };
 
+std::mutex g_setup_mu;
+DeviceSetup g_setup[64];
+
+// Set-up, once per device, with that device current: the device address of
+// the scratch array (in host code the array's name is only a stand-in) and
+// the SM count.  Returns false on a CUDA error.
+bool device_setup(DeviceSetup& out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!g_setup[dev].scratch) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return false;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        g_setup[dev].scratch = static_cast<unsigned char*>(ptr);
+        g_setup[dev].num_sms = sms;
+    }
+    out = g_setup[dev];
+    return true;
+}
+
 }  // namespace
 
 extern "C" ft_status ft_expert_ffn_noalloc(const void* records, int32_t n_records, const int32_t* route_records,
@@ -131,25 +164,8 @@ extern "C" ft_status ft_expert_ffn_noalloc(const void* records, int32_t n_record
         return FT_ERR_ARG;
     if (OFF_H + (size_t)T * k * F * 4 > FT_NOALLOC_SCRATCH_BYTES) return FT_ERR_ARG;
 
-    // Set-up, once per device, with that device current: the device address
-    // of the scratch array (the host-side symbol is only a stand-in).
-    static std::mutex mu;
-    static DeviceSetup setup[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FT_ERR_CUDA;
     DeviceSetup ds;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!setup[dev].scratch) {
-            void* ptr = nullptr;
-            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return FT_ERR_CUDA;
-            int sms = 0;
-            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FT_ERR_CUDA;
-            setup[dev].scratch = static_cast<unsigned char*>(ptr);
-            setup[dev].num_sms = sms;
-        }
-        ds = setup[dev];
-    }
+    if (!device_setup(ds)) return FT_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     noalloc_prep_kernel<<<1, PREP_THREADS, 0, s>>>(route_records, gates, T, k, n_records, ds.scratch);
     if (cudaGetLastError() != cudaSuccess) return FT_ERR_CUDA;
@@ -178,4 +194,20 @@ extern "C" ft_status ft_expert_ffn_noalloc(const void* records, int32_t n_record
     p.gbar = reinterpret_cast<unsigned*>(sc + OFF_GBAR);
     p.ready = reinterpret_cast<unsigned*>(sc + OFF_DONE);
     return launch_expert_ffn(p, ds.num_sms, s) == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+extern "C" ft_status ft_noalloc_status(void* stream) {
+    DeviceSetup ds;
+    if (!device_setup(ds)) return FT_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FT_ERR_CUDA;
+    unsigned* err = reinterpret_cast<unsigned*>(ds.scratch + OFF_ERR);
+    unsigned e = 0;
+    if (cudaMemcpy(&e, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return FT_ERR_CUDA;
+    if (e) {
+        const unsigned z = 0;
+        if (cudaMemcpy(err, &z, 4, cudaMemcpyHostToDevice) != cudaSuccess) return FT_ERR_CUDA;
+    }
+    if (e & FT_DEVERR_TIMEOUT) return FT_ERR_TIMEOUT;
+    if (e & FT_DEVERR_ARG) return FT_ERR_DEVICE;
+    return FT_OK;
 }

@@ -619,13 +619,8 @@ cudaError_t launch_pf_gather(PrefillState& pf, const void* x, int T, cudaStream_
 
 static cudaError_t launch_gemm(const CUtensorMap& A, const CUtensorMap& B, const GemmArgs& a, int num_sms,
                                cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)GEMM_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    cudaError_t e = ensure_dynamic_smem((const void*)grouped_gemm_kernel, GEMM_SMEM);
+    if (e != cudaSuccess) return e;
     grouped_gemm_kernel<<<num_sms, GEMM_THREADS, GEMM_SMEM, s>>>(A, B, a);
     return cudaGetLastError();
 }

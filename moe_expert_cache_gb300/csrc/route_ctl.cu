@@ -559,12 +559,8 @@ size_t route_ctl_smem_bytes(int T, int k, int E, int S) {
 
 cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s) {
     const size_t smem = route_ctl_smem_bytes(p.T, p.k, p.E, p.S);
-    static size_t smem_set = 0;
-    if (smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(route_ctl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+    cudaError_t e = ensure_dynamic_smem((const void*)route_ctl_kernel, smem);
+    if (e != cudaSuccess) return e;
     route_ctl_kernel<<<1, CTL_THREADS, smem, s>>>(p);
     return cudaGetLastError();
 }
