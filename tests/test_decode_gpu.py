@@ -226,3 +226,140 @@ def test_measure_link_leaves_the_cache_untouched(ft):
         ctx.measure_link(sh.L * sh.E + 1, 1)
     assert ctx.status() == ft.FT_OK
     ctx.close()
+
+
+# ------------------------------------------------------- failure handling
+
+def _tiny_oracle_step(ctx, st, wl, step, weights, T=None):
+    import torch
+    sh = wl.shape
+    T = T or wl.T
+    logits = synth.iid_logits(wl.seed, (step,), T, sh.E)
+    xb = synth.tokens_bf16(wl.seed, step, 0, T, sh.H)
+    ids, gates = zip(*[ctl.topk_route(r, sh.k) for r in logits])
+    r = ctl.route_ctl(st, 0, ids, wl.B_P, wl.B_H)
+    ctx.route_ctl(0, T, logits=_dev(logits), B_P=wl.B_P, B_H=wl.B_H)
+    hz.compare_ctl(ctx, st, r, T, f"step={step}")
+    _, pc = nm.moe_layer_split(nm.bf16_to_f64(xb), ids, gates, r.slots_topk, weights)
+    x = _dev(xb.view(np.int16)).view(torch.bfloat16)
+    y = torch.empty(T, sh.H, dtype=torch.float32, device="cuda")
+    ctx.moe_forward(x, _dev(pc), y)
+    torch.cuda.synchronize()
+    hz.check_output(y, xb, ids, gates, r.slots_topk, weights, pc, f"step={step}")
+    return r
+
+
+def test_wait_that_runs_out_is_reported_and_the_cache_recovers(ft):
+    """A bounded wait in the decode kernel gives up: with its progress waits
+    limited to 1 microsecond, a forward whose fills stream over the host link
+    (the first chunks land after several microseconds) latches the timeout
+    and winds down without a fault.  ft_get_status reports FT_ERR_TIMEOUT and
+    empties the cache (a fill may be incomplete); the next calls refill from
+    the host pool and match the oracle started from an empty cache with the
+    same clock."""
+    import torch
+    wl = synth.Workload("fail", synth.Shape(L=1, E=16, k=4, H=1024, F=512), S=8, steps=6, T=4, rho=None, sigma=None,
+                        B_P=1.0, B_H=1.0)
+    sh = wl.shape
+    pool, _ = hz.pinned_pool(sh, 0)
+    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, wl.S, pool, T_max=wl.T)
+    st = ctl.CacheState.empty(sh.L, sh.E, wl.S)
+    w = hz.Weights(wl.seed, sh, 0)
+    _tiny_oracle_step(ctx, st, wl, 0, w)
+    assert ctx.status() == ft.FT_OK
+    with pytest.raises(ft.FtError):
+        ctx.set_wait_limit(999)  # below the 1 us floor
+    ctx.set_wait_limit(1000)
+    logits = synth.iid_logits(wl.seed, (1,), wl.T, sh.E)
+    ids, _ = zip(*[ctl.topk_route(r, sh.k) for r in logits])
+    r = ctl.route_ctl(st.copy(), 0, ids, wl.B_P, wl.B_H)
+    assert r.q >= 2  # real fills stream during the forward
+    ctx.route_ctl(0, wl.T, logits=_dev(logits), B_P=wl.B_P, B_H=wl.B_H)
+    y = torch.empty(wl.T, sh.H, dtype=torch.float32, device="cuda")
+    ctx.moe_forward(_dev(synth.tokens_bf16(wl.seed, 1, 0, wl.T, sh.H).view(np.int16)).view(torch.bfloat16), None, y)
+    assert ctx.status() == ft.FT_ERR_TIMEOUT
+    sfi, ifs, stp, clk = ctx.ctl_state()
+    assert (sfi == -1).all() and (ifs == -1).all() and (stp == 0).all() and clk == st.clock + 1
+    ctx.set_wait_limit(0)  # back to the default
+    st = ctl.CacheState.empty(sh.L, sh.E, wl.S)
+    st.clock = clk
+    for step in range(2, wl.steps):
+        _tiny_oracle_step(ctx, st, wl, step, w)
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
+
+
+def test_resize_that_cannot_allocate_leaves_the_cache_intact(ft):
+    """ft_cache_resize "on any failure the old cache is left unchanged": a
+    resize to more slots than device memory holds fails in cudaMalloc (a
+    genuine out-of-memory answer, no fault); the maps, stamps and slot bytes
+    are unchanged and decoding continues against the oracle."""
+    wl = synth.Workload("oom", synth.Shape(L=1, E=16, k=4, H=4096, F=2048), S=6, steps=5, T=2, rho=None,
+                        sigma=None, B_P=1.0, B_H=2.0)
+    sh = wl.shape
+    pool, _ = hz.pinned_pool(sh, 0)
+    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, wl.S, pool, T_max=wl.T)
+    st = ctl.CacheState.empty(sh.L, sh.E, wl.S)
+    w = hz.Weights(wl.seed, sh, 0)
+    for step in range(2):
+        _tiny_oracle_step(ctx, st, wl, step, w)
+    before = ctx.ctl_state()
+    slots = [ctx.read_slot(s) for s in range(wl.S)]
+    # 6000 records of 50 MB: about 302 GB, more than the GPU's memory
+    with pytest.raises(ft.FtError) as ei:
+        ctx.cache_resize(6000)
+    assert ei.value.status == ft.FT_ERR_OOM
+    assert ctx.S == wl.S
+    after = ctx.ctl_state()
+    assert all(np.array_equal(a, b) for a, b in zip(before[:3], after[:3])) and before[3] == after[3]
+    assert all(np.array_equal(ctx.read_slot(s), slots[s]) for s in range(wl.S))
+    for step in range(2, wl.steps):
+        _tiny_oracle_step(ctx, st, wl, step, w)
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
+
+
+def test_set_ctl_state_round_trip(ft, tiny_pool):
+    """ft_set_ctl_state: putting back the state just read changes nothing
+    (later calls still match the oracle, outputs included); a fresh context
+    given an empty cache at clock 1000 follows the oracle from that clock; and
+    states that break the map bijection, name an id or slot out of range or
+    carry a stamp past the clock are refused with the state unchanged."""
+    wl = synth.TINY
+    sh = wl.shape
+    w = hz.Weights(wl.seed, sh, 0)
+    ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, wl.S, tiny_pool, T_max=wl.T)
+    st = ctl.CacheState.empty(sh.L, sh.E, wl.S)
+    for step in range(6):
+        _tiny_oracle_step(ctx, st, wl, step, w)
+    sfi, ifs, stp, clk = ctx.ctl_state()
+    ctx.set_ctl_state(sfi, ifs, stp, clk)
+    for step in range(6, 10):
+        _tiny_oracle_step(ctx, st, wl, step, w)
+    good = ctx.ctl_state()
+    bad_states = []
+    b = [a.copy() for a in good[:3]]
+    occ = int(np.flatnonzero(b[1] >= 0)[0])
+    b[0][b[1][occ]] = (occ + 1) % wl.S          # slot_for_id disagrees with id_for_slot
+    bad_states.append((b, good[3]))
+    b = [a.copy() for a in good[:3]]
+    b[1][occ] = sh.L * sh.E                     # id out of range
+    bad_states.append((b, good[3]))
+    b = [a.copy() for a in good[:3]]
+    b[2][occ] = good[3] + 1                     # stamp past the clock
+    bad_states.append((b, good[3]))
+    for (a0, a1, a2), c in bad_states:
+        with pytest.raises(ft.FtError) as ei:
+            ctx.set_ctl_state(a0, a1, a2, c)
+        assert ei.value.status == ft.FT_ERR_ARG
+        now = ctx.ctl_state()
+        assert all(np.array_equal(x, y) for x, y in zip(good[:3], now[:3])) and good[3] == now[3]
+    ctx.close()
+    ctx2 = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, wl.S, tiny_pool, T_max=wl.T)
+    empty = ctl.CacheState.empty(sh.L, sh.E, wl.S)
+    ctx2.set_ctl_state(empty.slot_for_id, empty.id_for_slot, empty.stamp, 1000)
+    empty.clock = 1000
+    for step in range(4):
+        _tiny_oracle_step(ctx2, empty, wl, step, w)
+    assert ctx2.status() == ft.FT_OK
+    ctx2.close()
