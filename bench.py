@@ -9,16 +9,21 @@ through all 48 layers: for every layer the control pass (routing, dedup,
 hit/miss, q, fill set, LRU victims, map update), the fills, the expert
 gate/up + SwiGLU and down + gated merge with the CPU-set partial sum.
 
-Timed region: K steps after W eager warm-up steps, captured from the library
-calls into one CUDA graph (instantiated and uploaded beforehand), bracketed by
-a barrier and a device synchronisation, CUDA events on the library's compute
-stream, max over ranks.  Every step streams about 3.6 GB of expert weights, far more than the
-129 MB L2, so no explicit L2 flush is used.  Per-kernel device times come
-from the library's own event records in the same timed region.
+Timing: W eager warm-up steps, then R consecutive windows of exactly K steps
+of the same AR(1) sequence.  The K steps are captured from the library calls
+into one CUDA graph (no profiling nodes in it), instantiated and uploaded
+before timing; before each window the window's inputs are copied into the
+graph's input buffers (untimed).  Each window is bracketed by a barrier and a
+device synchronisation and timed with CUDA events on the library's compute
+stream; `value` comes from the median window (max over ranks), and the line
+reports the spread.  Every step streams about 3.6 GB of expert weights, far
+more than the 129 MB L2, so no L2 flush is needed.  Per-kernel device times
+come from one further window of the same K-step graph captured with the
+library's per-launch event records.  Clocks are sampled by the GPU's UUID
+and summarised over the windows' time span.
 
-The JSON line also carries a "prefill" object: the Prefill workload (4
-layers, T=8192, full-layer double buffer) timed per chunk, with overlap and
-tensor-core utilisation of the grouped GEMMs.
+The JSON line carries compact objects for the other workloads ("legs"); with
+FT_BENCH_DETAIL=<path> the full per-leg detail is also written there as JSON.
 
 --impl reference times the CPU oracle (exact-integer control + float64
 expert numerics) on this machine's host cores on bounded samples of the same
@@ -28,6 +33,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -44,8 +50,16 @@ import synth  # noqa: E402
 
 WORKLOAD = synth.DECODE_T1
 METRIC = "decode MoE-layer tokens/s"
-PROFILE_EVERY = 16
 UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def headline_config(world: int = 1) -> dict:
+    """The workload of the bench line (identical in both arms)."""
+    return {"workload": "decode T=1: 48 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, 1536 slots, "
+                        "AR(1) rho=0.8, B_P=52.7, B_H=120",
+            "l2": "no flush: each step streams ~3.6 GB of expert weights (> 129 MB L2)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 # --------------------------------------------------------------- utilities
@@ -84,29 +98,60 @@ def read_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def gpu_query_id(device) -> str:
+    """nvidia-smi's -i argument for a torch device: the GPU's UUID (the CUDA
+    ordinal is not nvidia-smi's index once CUDA_VISIBLE_DEVICES remaps it)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        if u and u != "None":
+            return u if u.startswith(("GPU-", "MIG-")) else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    idx = device.index if hasattr(device, "index") and device.index is not None else 0
+    if vis:
+        ent = [v.strip() for v in vis.split(",") if v.strip()]
+        if idx < len(ent):
+            return ent[idx]
+    return str(idx)
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle-reason samples (every 200 ms) while the
+    timed windows run; stop() summarises the samples that fall inside the
+    given host-time span."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_id: str, tag: str = "0"):
         self.proc = None
         # raw samples go to FT_CLOCKS_DIR (default: the system temporary
         # directory); the JSON line carries their summary
         import tempfile
-        self.path = os.path.join(os.environ.get("FT_CLOCKS_DIR", tempfile.gettempdir()),
-                                 f"ft_clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(os.environ.get("FT_CLOCKS_DIR", tempfile.gettempdir()), f"ft_clocks_rank{tag}.csv")
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self) -> dict:
+    @staticmethod
+    def _epoch(ts: str):
+        ts = ts.strip()
+        try:
+            main, _, frac = ts.partition(".")
+            base = time.mktime(time.strptime(main, "%Y/%m/%d %H:%M:%S"))
+            return base + (float("0." + frac) if frac else 0.0)
+        except ValueError:
+            return None
+
+    def stop(self, t0: float | None = None, t1: float | None = None) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         time.sleep(0.25)
@@ -116,24 +161,28 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, pw, reasons, n_all = [], [], [], set(), 0
         for line in open(self.path):
             c = [x.strip() for x in line.split(",")]
             if len(c) < 9:
                 continue
+            n_all += 1
+            t = self._epoch(c[0])
+            if t0 is not None and t is not None and not (t0 - 0.1 <= t <= t1 + 0.1):
+                continue
             try:
                 sm.append(float(c[1]))
                 mx.append(float(c[2]))
+                pw.append(float(c[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, c[5:9]):
+            for n, v in zip(self.REASONS, c[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(pw) if pw else None}
 
 
 # ------------------------------------------------------------ CUDA graphs
@@ -221,20 +270,43 @@ def host_pool(shape: synth.Shape, seed: int, world: int, rank: int):
     return t, (mm, path)
 
 
-# ------------------------------------------------------------ our arm
+def repeated_pool(sh: synth.Shape, seed: int, distinct: int = 16):
+    """Pinned pool of L*E records that repeats the encodings of `distinct`
+    drawn experts of layer 0 (the kernels' time and the routing do not depend
+    on the values).  Returns (pool, per-record NVFP4 globals or None)."""
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+    rb = sh.record_bytes
+    enc = {synth.FMT_BF16: lambda s, l, e, H, F: synth.record_bf16(s, l, e, H, F),
+           synth.FMT_NVFP4: synth.record_nvfp4, synth.FMT_MXFP4: synth.record_mxfp4,
+           synth.FMT_FP8: synth.record_fp8}[sh.fmt]
+    with ThreadPoolExecutor(min(distinct, os.cpu_count() or 1)) as ex:
+        got = list(ex.map(lambda e: enc(seed, 0, e, sh.H, sh.F), range(distinct)))
+    recs = [g[0] for g in got] if sh.fmt == synth.FMT_NVFP4 else got
+    n = sh.L * sh.E
+    pool = torch.empty(n * rb, dtype=torch.uint8, pin_memory=True)
+    pn = pool.numpy().reshape(n, rb)
+    for i in range(n):
+        pn[i] = recs[i % distinct]
+    glob = (np.array([got[i % distinct][1] for i in range(n)], dtype=np.float32)
+            if sh.fmt == synth.FMT_NVFP4 else None)
+    return pool, glob
+
+
+# ------------------------------------------------------------ accounting
 
 def kernel_bytes(shape: synth.Shape, T: int, dcnt: dict) -> dict:
-    """Algorithmic bytes moved by each decode kernel over the timed region.
+    """Algorithmic bytes moved by each decode kernel over a run.
 
     expert_ffn (with the fused fill):
         link: every fill copies one record over the host link;
         hbm:  the fills written to HBM + the whole record of every resident
-              GPU expert read (3*F*H*2 B; a fill is computed from the bytes in
-              flight) + x read + h written and read once (fp32) + partial_C
-              read + y written.
+              GPU expert read (a fill is computed from the bytes in flight) +
+              x read + h written and read once (fp32) + partial_C read + y
+              written.
     route_ctl: logits + ids/gates written (small; reported for completeness).
     """
-    H, F, E, L, k = shape.H, shape.F, shape.E, shape.L, shape.k
+    H, F, E, k = shape.H, shape.F, shape.E, shape.k
     calls = dcnt["calls"]
     rb = shape.record_bytes
     link = dcnt["fills"] * rb
@@ -242,448 +314,51 @@ def kernel_bytes(shape: synth.Shape, T: int, dcnt: dict) -> dict:
     return {"expert_ffn": {"link": link, "hbm": hbm}, "route_ctl": {"hbm": calls * (T * E * 4 + 2 * T * k * 4)}}
 
 
-def run_ours(args, rank, world, local_rank):
-    import torch
-    import moe_expert_cache_gb300 as ft
-
-    ft.load()
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-    wl = WORKLOAD
-    sh = wl.shape
-    T, L, E, H = wl.T, sh.L, sh.E, sh.H
-    W, K = args.warmup, args.steps
-    n_steps = W + K
-
-    t0 = time.time()
-    pool, shared = host_pool(sh, wl.seed, world, rank)
-    t_pool = time.time() - t0
-
-    logits = synth.ar1_logits(wl.seed, n_steps, L, T, E, wl.rho, wl.sigma)          # [steps, L, T, E]
-    xs = np.stack([np.stack([synth.tokens_bf16(wl.seed, s, l, T, H) for l in range(L)]) for s in range(n_steps)])
-    pc = np.stack([synth.random_f32(wl.seed, (l,), (T, H), 0.1) for l in range(L)])   # [L, T, H]
-    logits_d = torch.from_numpy(logits).to(device)
-    xs_d = torch.from_numpy(xs.view(np.int16)).to(device).view(torch.bfloat16)
-    pc_d = torch.from_numpy(pc).to(device)
-    y_d = torch.empty(L, T, H, dtype=torch.float32, device=device)
-
-    s = torch.cuda.Stream(device)
-    ts = torch.cuda.Stream(device)
-
-    def make_ctx():
-        return ft.Context(L, E, sh.k, H, sh.F, wl.S, pool, T_max=T, compute_stream=s.cuda_stream,
-                          transfer_stream=ts.cuda_stream)
-
-    def step(ctx, si, lg, x, p, y):
-        for l in range(L):
-            ctx.route_ctl(l, T, logits=lg[si, l], B_P=wl.B_P, B_H=wl.B_H)
-            ctx.moe_forward(x[si, l], p[l], y[l])
-
-    # ---- device-resident run: W eager warm-up steps, then the K timed steps
-    # captured (with the library's per-kernel event nodes) into one CUDA graph
-    # that is instantiated and uploaded before the timed region.
-    ctx = make_ctx()
-    with torch.cuda.stream(s):
-        for i in range(W):
-            step(ctx, i, logits_d, xs_d, pc_d, y_d)
-    torch.cuda.synchronize(device)
-    c0 = ctx.counters()
-    ctx.profile_enable(True)
-    t0 = time.time()
-    g = RawGraph(s.cuda_stream)
-    def timed_steps():
-        for i in range(W, W + K):
-            # per-kernel event records on one timed step in PROFILE_EVERY
-            # (an event node costs a few microseconds of GPU time)
-            ctx.profile_pause((i - W) % PROFILE_EVERY != 0)
-            step(ctx, i, logits_d, xs_d, pc_d, y_d)
-        ctx.profile_pause(False)
-
-    with torch.cuda.stream(s):
-        g.capture(timed_steps)
-    t_capture = time.time() - t0
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world, device)
-    torch.cuda.synchronize(device)
-    clocks = ClockSampler(local_rank)
-    with torch.cuda.stream(s):
-        ev0.record(s)
-        g.launch()
-        ev1.record(s)
-    torch.cuda.synchronize(device)
-    barrier(world, device)
-    clk = clocks.stop()
-    t_ms = ev0.elapsed_time(ev1)
-    prof = ctx.profile_read()
-    ctx.profile_enable(False)
-    g.close()
-    c1 = ctx.counters()
-    assert ctx.status() == ft.FT_OK
-    dcnt = {k_: c1[k_] - c0[k_] for k_ in c1}
-    # B_P as the library measures it (its own fill path, 16 records, best of 3)
-    link_fill_gbps = ctx.measure_link(16, 3)
-    ctx.close()
-    t_max_ms = max_over_ranks(t_ms, world, device)
-
-    # ---- end to end: inputs copied from pinned host memory and y read back every step
-    lg_h = torch.from_numpy(logits).pin_memory()
-    xs_h = torch.from_numpy(xs.view(np.int16)).pin_memory()
-    pc_h = torch.from_numpy(pc).pin_memory()
-    y_h = torch.empty(L, T, H, dtype=torch.float32).pin_memory()
-    lg_step = torch.empty(1, L, T, E, dtype=torch.float32, device=device)
-    x_step = torch.empty(1, L, T, H, dtype=torch.int16, device=device)
-    pc_step = torch.empty(L, T, H, dtype=torch.float32, device=device)
-    ctx2 = make_ctx()
-    with torch.cuda.stream(s):
-        for i in range(W):
-            step(ctx2, i, logits_d, xs_d, pc_d, y_d)
-    torch.cuda.synchronize(device)
-    def e2e_steps():
-        for i in range(W, W + K):
-            lg_step.copy_(lg_h[i:i + 1], non_blocking=True)
-            x_step.copy_(xs_h[i:i + 1], non_blocking=True)
-            pc_step.copy_(pc_h, non_blocking=True)
-            step(ctx2, 0, lg_step, x_step.view(torch.bfloat16), pc_step, y_d)
-            y_h.copy_(y_d, non_blocking=True)
-
-    g2 = RawGraph(s.cuda_stream)
-    with torch.cuda.stream(s):
-        g2.capture(e2e_steps)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world, device)
-    torch.cuda.synchronize(device)
-    with torch.cuda.stream(s):
-        e0.record(s)
-        g2.launch()
-        e1.record(s)
-    torch.cuda.synchronize(device)
-    g2.close()
-    barrier(world, device)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
-    assert ctx2.status() == ft.FT_OK
-    ctx2.close()
-    h2d_bytes = (L * T * E * 4) + (L * T * H * 2) + (L * T * H * 4)
-    d2h_bytes = L * T * H * 4
-
-    # ---- roofline of the dominant kernel and per-kernel table
-    peaks = read_peaks()
-    kb = kernel_bytes(sh, T, dcnt)
-    total_ms = sum(v["ms"] for v in prof.values())
-    h2d_peak = measure_h2d_peak(device) if rank == 0 else None
-    kernels = {}
-    launches_total = dcnt["calls"]  # each decode kernel runs once per control pass
+def kernel_table(prof: dict, kb: dict, launches: int, peaks: dict, link_peak: float | None) -> dict:
+    """Per-kernel launches, time, share, and achieved GB/s against the HBM
+    peak (and the host link for the fills)."""
+    total_ms = sum(v["ms"] for v in prof.values()) or 1.0
+    out = {}
     for name, v in prof.items():
-        us = 1e3 * v["ms"] / v["launches"]
-        ent = {"launches_timed": v["launches"], "ms_total": round(v["ms"], 3), "us_per_launch": round(us, 3),
+        us = 1e3 * v["ms"] / max(1, v["launches"])
+        ent = {"launches": v["launches"], "ms_total": round(v["ms"], 3), "us_per_launch": round(us, 3),
                "share": round(v["ms"] / total_ms, 4)}
-        if name in kb:
-            for kind, byts in kb[name].items():
-                bpl = byts / max(1, launches_total)
-                gbs = bpl / (us * 1e-6) / 1e9
-                peak = h2d_peak if kind == "link" else peaks["hbm_gbs"]
-                ent[kind] = {"bytes_per_launch": int(bpl), "achieved_GBps": round(gbs, 1),
-                             "peak_GBps": round(peak, 1) if peak else None,
-                             "frac": round(gbs / peak, 4) if peak else None}
-        kernels[name] = ent
-    dom = max(prof, key=lambda n: prof[n]["ms"])
-    roofline = roofline_entry(dom, kernels, peaks, h2d_peak,
-                              dcnt["hits"] / max(1, dcnt["calls"]) if dom == "expert_ffn" else None)
-    ex = kernels.get("expert_ffn", {})
-    expert_roofline = {"kernel": "expert_ffn", "bound": "hbm",
-                       "achieved": ex.get("hbm", {}).get("achieved_GBps"), "peak": peaks["hbm_gbs"],
-                       "unit": "GB/s", "frac": ex.get("hbm", {}).get("frac"), "peak_source": peaks["source"],
-                       "note": "HBM side of the fused kernel; its time also covers the fill over the host link"}
-
-    value = whole_job_rate(T * K, t_ms * 1e-3, world, device)
-    out = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": round(t_max_ms / K, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; AR(1) router logits, N(0,0.02) bf16 weights)",
-        "config": {"workload": "decode T=1: 48 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, "
-                               "1536 slots, AR(1) rho=0.8, B_P=52.7, B_H=120",
-                   "L": L, "E": E, "k": sh.k, "H": H, "F": sh.F, "S": wl.S, "T": T,
-                   "l2": "no flush: each step streams ~3.6 GB of expert weights (> 129 MB L2)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "token_layers_per_s": round(value * L, 1),
-        "hit_rate": round(dcnt["hits"] / max(1, dcnt["unique"]), 4),
-        "fills_per_layer_step": round(dcnt["fills"] / max(1, dcnt["calls"]), 4),
-        "cpu_set_per_layer_step": round(dcnt["cpu"] / max(1, dcnt["calls"]), 4),
-        "roofline": roofline,
-        "roofline_expert_kernels": expert_roofline,
-        "link_GBps": {"pinned_memcpy": round(h2d_peak, 1) if h2d_peak else None,
-                      "fill_path_B_P": round(link_fill_gbps, 1)},
-        "kernels": kernels,
-        "gpu_launches": int(2 * dcnt["calls"]),
-        "kernel_timing": f"library CUDA-event records around each launch of 1 timed step in {PROFILE_EVERY}",
-        "clocks": clk,
-        "e2e": {"value": round(world * T * K / (e2e_ms * 1e-3), 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes},
-        "setup_s": {"host_pool": round(t_pool, 1), "graph_capture": round(t_capture, 1)},
-        "execution": "the K timed steps run as one CUDA graph (captured from the library calls, uploaded before timing)",
-    }
-    if rank == 0 and not args.no_t16:
-        out["decode_t16"] = run_decode_t16_bench(pool, device)
-    if not args.no_prefill:
-        out["prefill"] = run_prefill_bench(device, peaks)
-    if rank == 0 and not args.no_fp4:
-        out["quant_decode"] = run_quant_decode_bench(device, peaks)
-    if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(pool.numpy() if world == 1 else shared[0], args.cpu_seconds)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    if shared is not None:
-        torch.cuda.cudart().cudaHostUnregister(pool.data_ptr())
+        for kind, byts in kb.get(name, {}).items():
+            bpl = byts / max(1, launches)
+            gbs = bpl / (us * 1e-6) / 1e9 if us > 0 else 0.0
+            peak = link_peak if kind == "link" else peaks["hbm_gbs"]
+            ent[kind] = {"bytes_per_launch": int(bpl), "achieved_GBps": round(gbs, 1),
+                         "peak_GBps": round(peak, 1) if peak else None,
+                         "frac": round(gbs / peak, 4) if peak else None}
+        out[name] = ent
     return out
 
 
-def run_decode_t16_bench(pool, device) -> dict:
-    """Decode T=16 with resize (same layer shapes and host pool as decode T=1):
-    48 layers, 768 slots shrunk to 384 before step 32 and grown back before
-    step 64, 128 steps from an empty cache, AR(1) rho=0.7, B_P=25, B_H=90.
-    Steps run eagerly (the resizes are host safe points); tokens/s is over the
-    steps' CUDA-event time, resize latency is each call's host time."""
-    import torch
-    import moe_expert_cache_gb300 as ft
-    wl = synth.DECODE_T16
-    sh = wl.shape
-    T, L, E, H = wl.T, sh.L, sh.E, sh.H
-    logits = torch.from_numpy(synth.ar1_logits(wl.seed, wl.steps, L, T, E, wl.rho, wl.sigma)).to(device)
-    xs = torch.from_numpy(np.stack([synth.tokens_bf16(wl.seed, 0, l, T, H) for l in range(L)]).view(np.int16)).to(
-        device).view(torch.bfloat16)
-    pc = torch.zeros(T, H, device=device)
-    y = torch.empty(T, H, device=device)
-    cs = torch.cuda.Stream(device)
-    ctx = ft.Context(L, E, sh.k, H, sh.F, wl.S, pool, T_max=T, compute_stream=cs.cuda_stream)
-    resize_at = dict(synth.DECODE_T16_RESIZE)
-    ms, resize_ms = 0.0, {}
-    c0 = ctx.counters()
-    for s0, s1 in ((0, 32), (32, 64), (64, wl.steps)):
-        if s0 in resize_at:
-            t0 = time.perf_counter()
-            ctx.cache_resize(resize_at[s0])
-            resize_ms[f"to_{resize_at[s0]}_before_step_{s0}"] = round((time.perf_counter() - t0) * 1e3, 2)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(cs):
-            e0.record(cs)
-            for st in range(s0, s1):
-                for l in range(L):
-                    ctx.route_ctl(l, T, logits=logits[st, l], B_P=wl.B_P, B_H=wl.B_H)
-                    ctx.moe_forward(xs[l], pc, y)
-            e1.record(cs)
-        torch.cuda.synchronize(device)
-        ms += e0.elapsed_time(e1)
-    c1 = ctx.counters()
-    assert ctx.status() == ft.FT_OK
-    ctx.close()
-    d = {k_: c1[k_] - c0[k_] for k_ in c1}
-    calls = max(1, d["calls"])
-    return {"workload": "decode T=16: 48 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, 768 slots "
-                        "(384 during steps 32-63), AR(1) rho=0.7, B_P=25, B_H=90, 128 steps from an empty cache",
-            "tokens_per_s": round(T * wl.steps / (ms * 1e-3), 1), "ms_per_step": round(ms / wl.steps, 3),
-            "resize_ms": resize_ms, "execution": "eager library calls, CUDA-event time of the steps",
-            "hit_rate": round(d["hits"] / max(1, d["unique"]), 4),
-            "fills_per_layer_step": round(d["fills"] / calls, 3),
-            "gpu_experts_per_layer_step": round((d["hits"] + d["fills"]) / calls, 2),
-            "link_floor_ms_per_step": round(d["fills"] / wl.steps * sh.record_bytes / 211e9 * 1e3, 3)}
-
-
-def _fp4_pool(sh: synth.Shape, seed: int, distinct: int = 16):
-    """Pinned pool of one layer whose E records are the encodings of
-    `distinct` drawn experts, repeated (the FP4 kernel's time does not depend
-    on the values).  Returns (pool, per-record globals or None)."""
-    import torch
-    from concurrent.futures import ThreadPoolExecutor
-    rb = sh.record_bytes
-    enc = {synth.FMT_NVFP4: synth.record_nvfp4, synth.FMT_MXFP4: synth.record_mxfp4,
-           synth.FMT_FP8: synth.record_fp8}[sh.fmt]
-    with ThreadPoolExecutor(min(distinct, os.cpu_count() or 1)) as ex:
-        got = list(ex.map(lambda e: enc(seed, 0, e, sh.H, sh.F), range(distinct)))
-    recs = [g[0] for g in got] if sh.fmt == synth.FMT_NVFP4 else got
-    pool = torch.empty(sh.E * rb, dtype=torch.uint8, pin_memory=True)
-    pn = pool.numpy()
-    for e in range(sh.E):
-        pn[e * rb:(e + 1) * rb] = recs[e % distinct]
-    glob = (np.array([got[e % distinct][1] for e in range(sh.E)], dtype=np.float32)
-            if sh.fmt == synth.FMT_NVFP4 else None)
-    return pool, glob
-
-
-def run_quant_decode_bench(device, peaks, calls_t1: int = 96, calls_t64: int = 24) -> dict:
-    """Quantised expert kernels (NVFP4, MXFP4 and block-FP8 records) on the
-    Large shapes, hits only: one MoE layer of E=256 experts, top-8, H=4096,
-    F=2048, every record resident in 512 slots (a warm-up with B_P = B_H
-    fills every miss), AR(1) rho=0.8 logits, T=1 and T=64.  The bound is
-    HBM: each launch reads the records of its routed experts.  Per-launch
-    device time from the library's CUDA-event records around each launch of
-    the expert kernel (both FP8 kernels under one record)."""
-    import torch
-    import moe_expert_cache_gb300 as ft
-    out = {"workload": "Large shapes, hits only: 1 MoE layer, E=256, top-8, hidden 4096, ffn 2048, 512 slots "
-                       "holding every record, AR(1) rho=0.8 logits; records of 16 drawn experts repeated",
-           "execution": "eager library calls; expert-kernel time from the library's per-launch CUDA events"}
-    H, F, E, k = 4096, 2048, 256, 8
-    cs = torch.cuda.Stream(device)
-    for name, fmt in (("nvfp4", synth.FMT_NVFP4), ("mxfp4", synth.FMT_MXFP4), ("fp8", synth.FMT_FP8)):
-        sh = synth.Shape(L=1, E=E, k=k, H=H, F=F, fmt=fmt)
-        pool, glob = _fp4_pool(sh, 0)
-        ctx = ft.Context(1, E, k, H, F, 512, pool, fmt=fmt, T_max=64, nvfp4_global=glob,
-                         compute_stream=cs.cuda_stream)
-        res = {"record_bytes": sh.record_bytes}
-        with torch.cuda.stream(cs):
-            pc = torch.zeros(64, H, device=device)
-            y = torch.empty(64, H, device=device)
-            warm = torch.from_numpy(synth.iid_logits(1, (77,), 64, E)).to(device)
-            for i in range(8):  # fill every expert (q = m when B_P = B_H)
-                ctx.route_ctl(0, 64, logits=torch.roll(warm, i * 32, dims=1), B_P=1.0, B_H=1.0)
-                ctx.moe_forward(torch.zeros(64, H, dtype=torch.bfloat16, device=device), pc, y)
-        torch.cuda.synchronize(device)
-        for T, calls in ((1, calls_t1), (64, calls_t64)):
-            lg = torch.from_numpy(synth.ar1_logits(0, calls, 1, T, E, 0.8)[:, 0]).to(device)
-            x = torch.from_numpy(synth.tokens_bf16(0, 0, 0, T, H).view(np.int16)).to(device).view(torch.bfloat16)
-            with torch.cuda.stream(cs):
-                for i in range(4):
-                    ctx.route_ctl(0, T, logits=lg[i], B_P=52.7, B_H=150.0)
-                    ctx.moe_forward(x, pc[:T], y[:T])
-            torch.cuda.synchronize(device)
-            c0 = ctx.counters()
-            ctx.profile_enable(True)
-            with torch.cuda.stream(cs):
-                for i in range(calls):
-                    ctx.route_ctl(0, T, logits=lg[i], B_P=52.7, B_H=150.0)
-                    ctx.moe_forward(x, pc[:T], y[:T])
-            torch.cuda.synchronize(device)
-            prof = ctx.profile_read()
-            ctx.profile_enable(False)
-            c1 = ctx.counters()
-            d = {k_: c1[k_] - c0[k_] for k_ in c1}
-            ms = prof["expert_ffn"]["ms"]
-            n = prof["expert_ffn"]["launches"]
-            hbm = kernel_bytes(sh, T, d)["expert_ffn"]["hbm"]
-            gbs = hbm / (ms * 1e-3) / 1e9
-            res[f"t{T}"] = {"us_per_launch": round(ms * 1e3 / n, 2), "launches": n,
-                            "hits_per_launch": round(d["hits"] / max(1, d["calls"]), 2),
-                            "fills": d["fills"], "hbm_bytes_per_launch": int(hbm / n),
-                            "achieved_GBps": round(gbs, 1), "peak_GBps": peaks["hbm_gbs"],
-                            "frac": round(gbs / peaks["hbm_gbs"], 4),
-                            "traffic": traffic_from_profiles("expert_ffn_fp4", d["hits"] / max(1, d["calls"]))
-                            if fmt == synth.FMT_NVFP4 else None}
-        assert ctx.status() == ft.FT_OK
-        ctx.close()
-        del pool
-        out[name] = res
-    return out
-
-
-def run_prefill_bench(device, peaks, reps: int = 3) -> dict:
-    """Prefill workload: 4 layers, E=128, top-8, H=2048, F=768, T=8192, 256
-    slots, full-layer double buffer.  Times whole chunks (prefill_begin + 4
-    prefill_layer calls) with CUDA events on the compute stream; per-kernel
-    device times from the library's event records; the same chunk with the
-    copies on the compute stream (one buffer in flight, no overlap) as the
-    single-buffer A/B."""
-    import torch
-    import moe_expert_cache_gb300 as ft
-    wl = synth.PREFILL
-    sh = wl.shape
-    T, L = wl.T, sh.L
-    pool = torch.empty(L * sh.E * sh.record_bytes, dtype=torch.uint8, pin_memory=True)
-    synth.fill_host_pool(pool.numpy(), sh, wl.seed)
-    xs = [torch.from_numpy(synth.tokens_bf16(wl.seed, 900, l, T, sh.H).view(np.int16)).to(device).view(torch.bfloat16)
-          for l in range(L)]
-    lg = [torch.from_numpy(synth.iid_logits(wl.seed, (900, l), T, sh.E)).to(device) for l in range(L)]
-    ys = [torch.empty(T, sh.H, dtype=torch.float32, device=device) for _ in range(L)]
-    cs, ts = torch.cuda.Stream(device), torch.cuda.Stream(device)
-
-    def measure(two_streams: bool):
-        ctx = ft.Context(L, sh.E, sh.k, sh.H, sh.F, wl.S, pool, T_max=4, T_prefill_max=T,
-                         compute_stream=cs.cuda_stream, transfer_stream=ts.cuda_stream if two_streams else 0)
-
-        def chunk():
-            ctx.prefill_begin(0)
-            for l in range(L):
-                ctx.prefill_layer(l & 1, l, l + 1 if l + 1 < L else -1, T, xs[l], lg[l], ys[l])
-
-        with torch.cuda.stream(cs):
-            chunk()
-        torch.cuda.synchronize(device)
-        ctx.profile_enable(True)
-        times = []
-        for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(cs):
-                e0.record(cs)
-                chunk()
-                e1.record(cs)
-            torch.cuda.synchronize(device)
-            times.append(e0.elapsed_time(e1))
-        prof = ctx.profile_read()
-        assert ctx.status() == ft.FT_OK
-        ctx.close()
-        return statistics.median(times), prof
-
-    t_db, prof = measure(True)
-    t_sb, _ = measure(False)
-    n = reps
-    h2d = prof["pf_h2d"]["ms"] / n
-    comp = sum(v["ms"] for k_, v in prof.items() if k_ != "pf_h2d") / n
-    g1 = prof["pf_gemm1_swiglu"]["ms"] / (n * L)
-    g2 = prof["pf_gemm2"]["ms"] / (n * L)
-    fl1 = 2.0 * T * sh.k * 2 * sh.F * sh.H
-    fl2 = 2.0 * T * sh.k * sh.F * sh.H
-    tf = (fl1 + fl2) / ((g1 + g2) * 1e-3) / 1e12
-    tot = sum(v["ms"] for v in prof.values())
-    return {
-        "workload": "prefill: 4 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, T=8192, 256 slots, "
-                    "full-layer double buffer",
-        "expert_tokens_per_s": round(T * L / (t_db * 1e-3), 1),
-        "routed_assignments_per_s": round(T * sh.k * L / (t_db * 1e-3), 1),
-        "ms_per_chunk": round(t_db, 3),
-        "h2d_GBps": round(L * sh.E * sh.record_bytes / (h2d * 1e-3) / 1e9, 1),
-        "ms_h2d": round(h2d, 3), "ms_compute": round(comp, 3),
-        "overlap_eta": round(max(h2d, comp) / t_db, 4),
-        "hidden_fraction": round((h2d + comp - t_db) / min(h2d, comp), 4),
-        "single_buffer_ms_per_chunk": round(t_sb, 3),
-        "double_buffer_speedup": round(t_sb / t_db, 4),
-        "roofline_gemm": {"kernels": ["pf_gemm1_swiglu", "pf_gemm2"], "bound": "tensor",
-                          "achieved": round(tf, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                          "frac": round(tf / peaks["bf16_tflops"], 4),
-                          "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
-                          "gemm1_TFLOPs": round(fl1 / (g1 * 1e-3) / 1e12, 1),
-                          "gemm2_TFLOPs": round(fl2 / (g2 * 1e-3) / 1e12, 1),
-                          "flops_per_layer": fl1 + fl2, "peak_source": peaks["source"],
-                          "traffic": traffic_from_profiles("pf_gemm1_swiglu")},
-        "kernels": {k_: {"launches": v["launches"], "ms_total": round(v["ms"], 3),
-                         "share": round(v["ms"] / tot, 4)} for k_, v in prof.items()},
-    }
-
-
-def roofline_entry(dom, kernels, peaks, h2d_peak, records_per_launch=None):
-    """Roofline of the dominant kernel: the side (host link or HBM) whose
-    bytes at peak take longer is the bound."""
+def roofline_entry(dom: str, kernels: dict, peaks: dict, link_peak: float | None, traffic=None) -> dict:
+    """Roofline of the dominant kernel against the measured HBM peak.  When
+    the kernel also copies fills over the host link, `link` gives that side
+    and `binding` names whichever side's bytes at its peak take longer."""
     ent = kernels[dom]
-    link, hbm = ent.get("link"), ent.get("hbm", {})
-    t_link = link["bytes_per_launch"] / (h2d_peak * 1e9) if link and h2d_peak else 0.0
-    t_hbm = hbm.get("bytes_per_launch", 0) / (peaks["hbm_gbs"] * 1e9)
-    if t_link >= t_hbm and link:
-        side, bound, src = link, "h2d", "measured live: pinned host->device cudaMemcpyAsync, 1 GiB, best of 4"
-    else:
-        side, bound, src = hbm, "hbm", peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
-    return {"kernel": dom, "bound": bound, "achieved": side.get("achieved_GBps"), "peak": side.get("peak_GBps"),
-            "unit": "GB/s", "frac": side.get("frac"), "peak_source": src,
-            "bytes_per_launch": side.get("bytes_per_launch"), "us_per_launch": ent["us_per_launch"],
-            "traffic": traffic_from_profiles(dom, records_per_launch)}
+    hbm = ent["hbm"]
+    out = {"kernel": dom, "bound": "hbm", "achieved": hbm["achieved_GBps"], "peak": peaks["hbm_gbs"],
+           "unit": "GB/s", "frac": hbm["frac"], "traffic": traffic,
+           "bytes_per_launch": hbm["bytes_per_launch"], "us_per_launch": ent["us_per_launch"],
+           "peak_source": peaks["source"]}
+    link = ent.get("link")
+    if link and link["bytes_per_launch"] > 0 and link_peak:
+        t_link = link["bytes_per_launch"] / (link_peak * 1e9)
+        t_hbm = hbm["bytes_per_launch"] / (peaks["hbm_gbs"] * 1e9)
+        out["link"] = {"achieved": link["achieved_GBps"], "peak": round(link_peak, 1), "frac": link["frac"]}
+        out["binding"] = "link" if t_link >= t_hbm else "hbm"
+    return out
 
 
-def traffic_from_profiles(kernel: str, records_per_launch: float | None = None):
+def traffic_from_profiles(kernel: str, scale_to: float | None = None):
     """DRAM bytes per launch from a committed ncu capture, if one matches the
     current kernel source (profiles/traffic.json keyed by kernel and source
-    hash); else None.  A capture that lists the records its launch read is
-    scaled to `records_per_launch` (the traffic of these kernels grows with
-    the records they read)."""
+    hash); else None.  A capture that records the algorithmic HBM bytes of
+    its launch (`alg_bytes`) is scaled to `scale_to` algorithmic bytes: the
+    traffic of these kernels grows in proportion to the bytes they move."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -692,14 +367,15 @@ def traffic_from_profiles(kernel: str, records_per_launch: float | None = None):
         if not d:
             return None
         import hashlib
-        src = os.path.join(ROOT, d["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if h != d["source_sha"]:
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        if h.hexdigest()[:16] != d["source_sha"]:
             return None
-        if "records_read" in d:
-            if records_per_launch is None:
+        if "alg_bytes" in d:
+            if scale_to is None:
                 return None
-            return int(d["dram_bytes"] / d["records_read"] * records_per_launch)
+            return int(d["dram_bytes"] / d["alg_bytes"] * scale_to)
         return d.get("dram_bytes_per_launch")
     except Exception:
         return None
@@ -720,6 +396,619 @@ def measure_h2d_peak(device) -> float:
         best = max(best, n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
     del h, d
     return best
+
+
+def spread(ms: list) -> dict:
+    return {"n": len(ms), "median_ms": round(statistics.median(ms), 3), "min_ms": round(min(ms), 3),
+            "max_ms": round(max(ms), 3)}
+
+
+# ------------------------------------------------------------ our arm
+
+class Decoder:
+    """One decode context of the headline workload and the K-step graph that
+    reads its inputs from fixed window buffers."""
+
+    def __init__(self, ft, pool, device, K: int, s, ts):
+        import torch
+        wl = WORKLOAD
+        sh = wl.shape
+        self.ft, self.sh, self.wl, self.K, self.s, self.device = ft, sh, wl, K, s, device
+        self.T, self.L = wl.T, sh.L
+        self.ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, wl.S, pool, T_max=wl.T, compute_stream=s.cuda_stream,
+                              transfer_stream=ts.cuda_stream)
+        T, L, E, H = self.T, self.L, sh.E, sh.H
+        self.lg = torch.empty(K, L, T, E, dtype=torch.float32, device=device)
+        self.x = torch.empty(K, L, T, H, dtype=torch.int16, device=device)
+        self.pc = torch.from_numpy(np.stack([synth.random_f32(wl.seed, (l,), (T, H), 0.1) for l in range(L)])).to(
+            device)
+        self.y = torch.empty(L, T, H, dtype=torch.float32, device=device)
+
+    def graph(self):
+        import torch
+        g = RawGraph(self.s.cuda_stream)
+        xb = self.x.view(torch.bfloat16)
+
+        def steps():
+            for i in range(self.K):
+                for l in range(self.L):
+                    self.ctx.route_ctl(l, self.T, logits=self.lg[i, l], B_P=self.wl.B_P, B_H=self.wl.B_H)
+                    self.ctx.moe_forward(xb[i, l], self.pc[l], self.y[l])
+        with torch.cuda.stream(self.s):
+            g.capture(steps)
+        return g
+
+
+def decode_inputs(n_steps: int):
+    """AR(1) logits [n, L, T, E] and bf16 tokens [n, L, T, H] of the headline
+    workload's first n steps."""
+    wl = WORKLOAD
+    sh = wl.shape
+    lg = synth.ar1_logits(wl.seed, n_steps, sh.L, wl.T, sh.E, wl.rho, wl.sigma)
+    xs = np.stack([np.stack([synth.tokens_bf16(wl.seed, s, l, wl.T, sh.H) for l in range(sh.L)])
+                   for s in range(n_steps)]).view(np.int16)
+    return lg, xs
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import moe_expert_cache_gb300 as ft
+
+    ft.load()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    wl = WORKLOAD
+    sh = wl.shape
+    T, L, E, H = wl.T, sh.L, sh.E, sh.H
+    W, K = args.warmup, args.steps
+    peaks = read_peaks()
+
+    t0 = time.time()
+    pool, shared = host_pool(sh, wl.seed, world, rank)
+    t_pool = time.time() - t0
+
+    s = torch.cuda.Stream(device)
+    ts = torch.cuda.Stream(device)
+    dec = Decoder(ft, pool, device, K, s, ts)
+
+    # ---- warm-up: W eager steps (its time sizes the number of windows)
+    lg_w, x_w = decode_inputs(W)
+    lg_wd = torch.from_numpy(lg_w).to(device)
+    x_wd = torch.from_numpy(x_w).to(device).view(torch.bfloat16)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for i in range(W):
+            for l in range(L):
+                dec.ctx.route_ctl(l, T, logits=lg_wd[i, l], B_P=wl.B_P, B_H=wl.B_H)
+                dec.ctx.moe_forward(x_wd[i, l], dec.pc[l], dec.y[l])
+        e1.record(s)
+    torch.cuda.synchronize(device)
+    ms_step_est = max(0.5, e0.elapsed_time(e1) / max(1, W))
+    R = args.windows or int(min(50, max(3, math.ceil(args.timed_seconds * 1e3 / (K * ms_step_est)))))
+    R = int(max_over_ranks(float(R), world, device))
+    n_steps = W + (R + 1) * K  # R timed windows + one profiled window
+    lg_all, x_all = decode_inputs(n_steps)
+    lg_all_d = torch.from_numpy(lg_all).to(device)
+    x_all_d = torch.from_numpy(x_all).to(device)
+
+    def stage(win: int):
+        a = W + win * K
+        with torch.cuda.stream(s):
+            dec.lg.copy_(lg_all_d[a:a + K])
+            dec.x.copy_(x_all_d[a:a + K])
+
+    t0 = time.time()
+    g = dec.graph()
+    t_capture = time.time() - t0
+    link_before = measure_h2d_peak(device) if rank == 0 else None
+    c0 = dec.ctx.counters()
+    clocks = ClockSampler(gpu_query_id(device), str(local_rank))
+    win_ms = []
+    span0 = time.time()
+    for r in range(R):
+        stage(r)
+        torch.cuda.synchronize(device)
+        barrier(world, device)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            ev0.record(s)
+            g.launch()
+            ev1.record(s)
+        torch.cuda.synchronize(device)
+        barrier(world, device)
+        win_ms.append(ev0.elapsed_time(ev1))
+    span1 = time.time()
+    clk = clocks.stop(span0, span1)
+    c1 = dec.ctx.counters()
+    g.close()
+    assert dec.ctx.status() == ft.FT_OK
+    link_after = measure_h2d_peak(device) if rank == 0 else None
+    dcnt = {k_: c1[k_] - c0[k_] for k_ in c1}
+
+    # ---- per-kernel times: one more window of the same K steps, captured
+    # with the library's event records around every launch
+    stage(R)
+    dec.ctx.profile_enable(True)
+    gp = dec.graph()
+    p0 = dec.ctx.counters()
+    with torch.cuda.stream(s):
+        gp.launch()
+    torch.cuda.synchronize(device)
+    prof = dec.ctx.profile_read()
+    dec.ctx.profile_enable(False)
+    p1 = dec.ctx.counters()
+    gp.close()
+    pcnt = {k_: p1[k_] - p0[k_] for k_ in p1}
+    link_fill_gbps = dec.ctx.measure_link(16, 3)
+    assert dec.ctx.status() == ft.FT_OK
+    dec.ctx.close()
+
+    med = statistics.median(win_ms)
+    t_med_max = max_over_ranks(med, world, device)
+    value = world * T * K / (t_med_max * 1e-3)
+    link_peak = max(x for x in (link_before, link_after) if x) if rank == 0 else None
+    kb = kernel_bytes(sh, T, pcnt)
+    kernels = kernel_table(prof, kb, pcnt["calls"], peaks, link_peak)
+    dom = max(prof, key=lambda n: prof[n]["ms"])
+    traffic = (traffic_from_profiles(dom, kernels[dom]["hbm"]["bytes_per_launch"]) if dom == "expert_ffn" else None)
+    roofline = roofline_entry(dom, kernels, peaks, link_peak, traffic)
+    fills = pcnt["fills"] / max(1, pcnt["calls"])
+    floor_ms = fills * L * sh.record_bytes / (link_peak * 1e9) * 1e3 if link_peak else None
+
+    # ---- end to end: every step's inputs copied from pinned host memory and
+    # its y read back, inside the timed graph
+    e2e_ms = run_e2e(ft, pool, device, W, K, R, lg_all, x_all, world)
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(t_med_max / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded AR(1) logits, N(0,0.02) bf16 weights)",
+        "gpu_launches": int(2 * L * K),
+        "config": headline_config(world),
+        "roofline": roofline,
+        "repeats": {"windows": R, "of_steps": K, "median_ms": round(med, 3), "min_ms": round(min(win_ms), 3),
+                    "max_ms": round(max(win_ms), 3),
+                    "link_GBps": [round(x, 1) if x else None for x in (link_before, link_after)],
+                    "B_P_fill_path": round(link_fill_gbps, 1)},
+        "decode": {"hit_rate": round(dcnt["hits"] / max(1, dcnt["unique"]), 4),
+                   "fills_per_layer_step": round(dcnt["fills"] / max(1, dcnt["calls"]), 3),
+                   "link_floor_ms_step": round(floor_ms, 3) if floor_ms else None,
+                   "route_ctl_us": kernels.get("route_ctl", {}).get("us_per_launch")},
+        "clocks": clk,
+        "e2e": {"value": round(world * T * K / (e2e_ms * 1e-3), 2), "unit": UNIT,
+                "h2d_bytes_per_step": L * T * (E * 4 + H * 2 + H * 4), "d2h_bytes_per_step": L * T * H * 4},
+    }
+    detail = {"kernels": kernels, "windows_ms": [round(x, 3) for x in win_ms], "counters": dcnt,
+              "profile_window_counters": pcnt,
+              "setup_s": {"host_pool": round(t_pool, 1), "graph_capture": round(t_capture, 1)}}
+    legs, leg_detail = {}, {}
+    if rank == 0 and not args.no_t16:
+        legs["decode_t16"], leg_detail["decode_t16"] = run_decode_t16_bench(pool, device, link_peak)
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(pool.numpy() if world == 1 else shared[0], args.cpu_seconds)
+    if rank == 0 and not args.no_hbm:
+        legs["bf16_q0"], leg_detail["bf16_q0"] = run_bf16_hbm_bench(pool, device, peaks)
+    del pool, dec
+    if not args.no_prefill:
+        legs["prefill"], leg_detail["prefill"] = run_prefill_bench(device, peaks)
+    if rank == 0 and not args.no_fp4:
+        legs["quant_q0"], leg_detail["quant_q0"] = run_quant_decode_bench(device, peaks)
+    if rank == 0 and not args.no_large:
+        legs["large_nvfp4"], leg_detail["large_nvfp4"] = run_large_nvfp4_bench(device, peaks, link_peak)
+    out["legs"] = legs
+    detail["legs"] = leg_detail
+    path = os.environ.get("FT_BENCH_DETAIL")
+    if path and rank == 0:
+        with open(path, "w") as f:
+            json.dump({"line": out, "detail": detail}, f, indent=1)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if shared is not None:
+        import torch as _t
+        _t.cuda.cudart().cudaHostUnregister(_t.from_numpy(shared[0]).data_ptr())
+    return out
+
+
+def run_e2e(ft, pool, device, W, K, R, lg_all, x_all, world) -> float:
+    """Median window time of the same K-step windows with every step's
+    logits, x and partial_C copied from pinned host memory and y copied back
+    inside the timed graph."""
+    import torch
+    wl = WORKLOAD
+    sh = wl.shape
+    T, L, E, H = wl.T, sh.L, sh.E, sh.H
+    s, ts = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ctx = ft.Context(L, E, sh.k, H, sh.F, wl.S, pool, T_max=T, compute_stream=s.cuda_stream,
+                     transfer_stream=ts.cuda_stream)
+    lg_h = torch.empty(K, L, T, E, dtype=torch.float32).pin_memory()
+    x_h = torch.empty(K, L, T, H, dtype=torch.int16).pin_memory()
+    pc_h = torch.from_numpy(np.stack([synth.random_f32(wl.seed, (l,), (T, H), 0.1) for l in range(L)])).pin_memory()
+    y_h = torch.empty(K, L, T, H, dtype=torch.float32).pin_memory()
+    lg_d = torch.empty(L, T, E, dtype=torch.float32, device=device)
+    x_d = torch.empty(L, T, H, dtype=torch.int16, device=device)
+    pc_d = torch.empty(L, T, H, dtype=torch.float32, device=device)
+    y_d = torch.empty(L, T, H, dtype=torch.float32, device=device)
+    xb = x_d.view(torch.bfloat16)
+    with torch.cuda.stream(s):
+        lgw = torch.from_numpy(lg_all[:W]).to(device)
+        xw = torch.from_numpy(x_all[:W]).to(device).view(torch.bfloat16)
+        pc_d.copy_(pc_h)
+        for i in range(W):
+            for l in range(L):
+                ctx.route_ctl(l, T, logits=lgw[i, l], B_P=wl.B_P, B_H=wl.B_H)
+                ctx.moe_forward(xw[i, l], pc_d[l], y_d[l])
+    torch.cuda.synchronize(device)
+
+    def steps():
+        for i in range(K):
+            lg_d.copy_(lg_h[i], non_blocking=True)
+            x_d.copy_(x_h[i], non_blocking=True)
+            pc_d.copy_(pc_h, non_blocking=True)
+            for l in range(L):
+                ctx.route_ctl(l, T, logits=lg_d[l], B_P=wl.B_P, B_H=wl.B_H)
+                ctx.moe_forward(xb[l], pc_d[l], y_d[l])
+            y_h[i].copy_(y_d, non_blocking=True)
+
+    g = RawGraph(s.cuda_stream)
+    with torch.cuda.stream(s):
+        g.capture(steps)
+    ms = []
+    for r in range(R):
+        a = W + r * K
+        lg_h.numpy()[:] = lg_all[a:a + K]
+        x_h.numpy()[:] = x_all[a:a + K]
+        torch.cuda.synchronize(device)
+        barrier(world, device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.launch()
+            e1.record(s)
+        torch.cuda.synchronize(device)
+        barrier(world, device)
+        ms.append(e0.elapsed_time(e1))
+    g.close()
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
+    return max_over_ranks(statistics.median(ms), world, device)
+
+
+def run_decode_t16_bench(pool, device, link_peak):
+    """Decode T=16 with resize (same layer shapes and host pool as decode T=1):
+    48 layers, 768 slots shrunk to 384 before step 32 and grown back before
+    step 64, 128 steps from an empty cache, AR(1) rho=0.7, B_P=25, B_H=90.
+    Steps run eagerly (the resizes are host safe points); tokens/s is over the
+    steps' CUDA-event time, resize latency is each call's host time."""
+    import torch
+    import moe_expert_cache_gb300 as ft
+    wl = synth.DECODE_T16
+    sh = wl.shape
+    T, L, E, H = wl.T, sh.L, sh.E, sh.H
+    logits = torch.from_numpy(synth.ar1_logits(wl.seed, wl.steps, L, T, E, wl.rho, wl.sigma)).to(device)
+    xs = torch.from_numpy(np.stack([synth.tokens_bf16(wl.seed, 0, l, T, H) for l in range(L)]).view(np.int16)).to(
+        device).view(torch.bfloat16)
+    pc = torch.zeros(T, H, device=device)
+    y = torch.empty(T, H, device=device)
+    cs = torch.cuda.Stream(device)
+    ctx = ft.Context(L, E, sh.k, H, sh.F, wl.S, pool, T_max=T, compute_stream=cs.cuda_stream)
+    resize_at = dict(synth.DECODE_T16_RESIZE)
+    ms, resize_ms = 0.0, []
+    c0 = ctx.counters()
+    for s0, s1 in ((0, 32), (32, 64), (64, wl.steps)):
+        if s0 in resize_at:
+            t0 = time.perf_counter()
+            ctx.cache_resize(resize_at[s0])
+            resize_ms.append(round((time.perf_counter() - t0) * 1e3, 2))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):
+            e0.record(cs)
+            for st in range(s0, s1):
+                for l in range(L):
+                    ctx.route_ctl(l, T, logits=logits[st, l], B_P=wl.B_P, B_H=wl.B_H)
+                    ctx.moe_forward(xs[l], pc, y)
+            e1.record(cs)
+        torch.cuda.synchronize(device)
+        ms += e0.elapsed_time(e1)
+    c1 = ctx.counters()
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
+    d = {k_: c1[k_] - c0[k_] for k_ in c1}
+    calls = max(1, d["calls"])
+    floor = d["fills"] / wl.steps * sh.record_bytes / ((link_peak or 211.0) * 1e9) * 1e3
+    leg = {"tok_s": round(T * wl.steps / (ms * 1e-3), 1), "ms_step": round(ms / wl.steps, 3),
+           "floor_ms": round(floor, 3), "resize_ms": resize_ms}
+    detail = dict(leg, workload="decode T=16: 48 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, 768 slots "
+                                "(384 during steps 32-63), AR(1) rho=0.7, B_P=25, B_H=90, 128 steps from an empty "
+                                "cache; eager library calls, CUDA-event time of the steps",
+                  hit_rate=round(d["hits"] / max(1, d["unique"]), 4),
+                  fills_per_layer_step=round(d["fills"] / calls, 3),
+                  gpu_experts_per_layer_step=round((d["hits"] + d["fills"]) / calls, 2))
+    return leg, detail
+
+
+class L2Flusher:
+    """Writes a buffer twice the size of L2 so the next launch reads HBM."""
+
+    def __init__(self, device):
+        import torch
+        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def hits_only_times(ctx, T, routes, x, pc, y, flush, stream, device):
+    """Expert-kernel device time of each call of `routes` (a list of
+    (topk_ids, topk_w) device tensors or (logits,) tuples), every record
+    resident (q = 0), L2 flushed before each call.  Returns (median us,
+    counters of the calls)."""
+    import torch
+    c0 = ctx.counters()
+    us = []
+    for r in routes:
+        with torch.cuda.stream(stream):
+            flush()
+            if len(r) == 1:
+                ctx.route_ctl(0, T, logits=r[0], B_P=1.0, B_H=1.0)
+            else:
+                ctx.route_ctl(0, T, topk_ids=r[0], topk_w=r[1], B_P=1.0, B_H=1.0)
+            ctx.profile_enable(True)
+            ctx.moe_forward(x, pc, y)
+        pr = ctx.profile_read()
+        ctx.profile_enable(False)
+        us.append(1e3 * pr["expert_ffn"]["ms"] / pr["expert_ffn"]["launches"])
+    c1 = ctx.counters()
+    d = {k_: c1[k_] - c0[k_] for k_ in c1}
+    assert d["fills"] == 0, "a hits-only leg filled"
+    return statistics.median(us), d
+
+
+def run_bf16_hbm_bench(pool, device, peaks, calls: int = 24):
+    """BF16 expert kernel with every record resident (q = 0), the HBM-bound
+    case: one layer of the decode shapes (E=128, top-8, H=2048, F=768) in 128
+    slots, T=1 (disjoint sets of 8 experts in turn) and T=16 (AR(1) rho=0.7
+    routing), L2 flushed before every call; achieved GB/s = the call's
+    algorithmic bytes / its device time."""
+    import torch
+    import moe_expert_cache_gb300 as ft
+    sh1 = synth.Shape(L=1, E=128, k=8, H=2048, F=768)
+    cs = torch.cuda.Stream(device)
+    ctx = ft.Context(1, sh1.E, sh1.k, sh1.H, sh1.F, sh1.E, pool, T_max=16, compute_stream=cs.cuda_stream)
+    flush = L2Flusher(device)
+    x = torch.from_numpy(synth.tokens_bf16(0, 0, 0, 16, sh1.H).view(np.int16)).to(device).view(torch.bfloat16)
+    pc = torch.zeros(16, sh1.H, device=device)
+    y = torch.empty(16, sh1.H, device=device)
+    w8 = torch.full((1, 8), 1.0 / 8, device=device)
+    with torch.cuda.stream(cs):  # make every record of layer 0 resident
+        for i in range(16):
+            ids = torch.arange(8 * i, 8 * i + 8, dtype=torch.int32, device=device).view(1, 8)
+            ctx.route_ctl(0, 1, topk_ids=ids, topk_w=w8, B_P=1.0, B_H=1.0)
+            ctx.moe_forward(x[:1], pc[:1], y[:1])
+    torch.cuda.synchronize(device)
+    leg, detail = {}, {}
+    r1 = [(torch.arange(8 * (i % 16), 8 * (i % 16) + 8, dtype=torch.int32, device=device).view(1, 8), w8)
+          for i in range(calls)]
+    lg16 = torch.from_numpy(synth.ar1_logits(3, calls, 1, 16, sh1.E, 0.7)[:, 0]).to(device)
+    r16 = [(lg16[i],) for i in range(calls)]
+    for T, routes in ((1, r1), (16, r16)):
+        us, d = hits_only_times(ctx, T, routes, x[:T], pc[:T], y[:T], flush, cs, device)
+        hbm = kernel_bytes(sh1, T, d)["expert_ffn"]["hbm"] / max(1, d["calls"])
+        gbs = hbm / (us * 1e-6) / 1e9
+        leg[f"t{T}"] = {"us": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                        "traffic": traffic_from_profiles("expert_ffn", hbm)}
+        detail[f"t{T}"] = dict(leg[f"t{T}"], hits_per_launch=round(d["hits"] / max(1, d["calls"]), 2),
+                               bytes_per_launch=int(hbm), calls=d["calls"])
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
+    detail["workload"] = ("BF16 decode kernel, hits only: 1 layer, E=128, top-8, hidden 2048, ffn 768, 128 slots "
+                          "all resident; T=1 over disjoint 8-expert sets, T=16 AR(1) rho=0.7; L2 flushed per call")
+    return leg, detail
+
+
+def run_quant_decode_bench(device, peaks, calls_t1: int = 48, calls_t64: int = 16):
+    """Quantised expert kernels (NVFP4, MXFP4 and block-FP8 records) on the
+    Large shapes, hits only: one MoE layer of E=256 experts, top-8, H=4096,
+    F=2048, every record resident in 256 slots, AR(1) rho=0.8 logits, T=1
+    and T=64, L2 flushed before every call.  The bound is HBM: each launch
+    reads the records of its routed experts."""
+    import torch
+    import moe_expert_cache_gb300 as ft
+    H, F, E, k = 4096, 2048, 256, 8
+    cs = torch.cuda.Stream(device)
+    flush = L2Flusher(device)
+    leg, detail = {}, {"workload": "Large shapes, hits only: 1 MoE layer, E=256, top-8, hidden 4096, ffn 2048, "
+                                   "every record resident, AR(1) rho=0.8 logits, L2 flushed per call; records of "
+                                   "16 drawn experts repeated"}
+    for name, fmt in (("nvfp4", synth.FMT_NVFP4), ("mxfp4", synth.FMT_MXFP4), ("fp8", synth.FMT_FP8)):
+        sh = synth.Shape(L=1, E=E, k=k, H=H, F=F, fmt=fmt)
+        pool, glob = repeated_pool(sh, 0)
+        ctx = ft.Context(1, E, k, H, F, E, pool, fmt=fmt, T_max=64, nvfp4_global=glob,
+                         compute_stream=cs.cuda_stream)
+        x = torch.from_numpy(synth.tokens_bf16(0, 0, 0, 64, H).view(np.int16)).to(device).view(torch.bfloat16)
+        pc = torch.zeros(64, H, device=device)
+        y = torch.empty(64, H, device=device)
+        w8 = torch.full((1, 8), 1.0 / 8, device=device)
+        with torch.cuda.stream(cs):  # every record resident
+            for i in range(E // 8):
+                ids = torch.arange(8 * i, 8 * i + 8, dtype=torch.int32, device=device).view(1, 8)
+                ctx.route_ctl(0, 1, topk_ids=ids, topk_w=w8, B_P=1.0, B_H=1.0)
+                ctx.moe_forward(x[:1], pc[:1], y[:1])
+        torch.cuda.synchronize(device)
+        res, det = {}, {"record_bytes": sh.record_bytes}
+        for T, calls in ((1, calls_t1), (64, calls_t64)):
+            lg = torch.from_numpy(synth.ar1_logits(0, calls, 1, T, E, 0.8)[:, 0]).to(device)
+            us, d = hits_only_times(ctx, T, [(lg[i],) for i in range(calls)], x[:T], pc[:T], y[:T], flush, cs,
+                                    device)
+            hbm = kernel_bytes(sh, T, d)["expert_ffn"]["hbm"] / max(1, d["calls"])
+            gbs = hbm / (us * 1e-6) / 1e9
+            kname = {synth.FMT_NVFP4: "expert_ffn_fp4", synth.FMT_MXFP4: "expert_ffn_mxfp4",
+                     synth.FMT_FP8: "expert_ffn_fp8"}[fmt]
+            res[f"t{T}"] = [round(us, 1), round(gbs / peaks["hbm_gbs"], 4)]
+            det[f"t{T}"] = {"us_per_launch": round(us, 2), "hits_per_launch": round(d["hits"] / max(1, d["calls"]), 2),
+                            "hbm_bytes_per_launch": int(hbm), "achieved_GBps": round(gbs, 1),
+                            "frac": round(gbs / peaks["hbm_gbs"], 4),
+                            "traffic": traffic_from_profiles(kname, hbm)}
+        assert ctx.status() == ft.FT_OK
+        ctx.close()
+        del pool
+        leg[name] = res
+        detail[name] = det
+    leg["cols"] = "t: [us per launch, frac of HBM]"
+    return leg, detail
+
+
+def prefill_chunk_times(ft, sh, S, T, pool, glob, device, reps: int):
+    """Chunk time (prefill_begin + one prefill_layer per layer) with the
+    double buffer, the per-kernel profile, and the same chunk with the copies
+    on the compute stream (single buffer in flight)."""
+    import torch
+    L = sh.L
+    xs = [torch.from_numpy(synth.tokens_bf16(0, 900, l, T, sh.H).view(np.int16)).to(device).view(torch.bfloat16)
+          for l in range(L)]
+    lg = [torch.from_numpy(synth.iid_logits(0, (900, l), T, sh.E)).to(device) for l in range(L)]
+    ys = [torch.empty(T, sh.H, dtype=torch.float32, device=device) for _ in range(L)]
+    cs, ts = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def measure(two_streams: bool):
+        ctx = ft.Context(L, sh.E, sh.k, sh.H, sh.F, S, pool, fmt=sh.fmt, T_max=4, T_prefill_max=T,
+                         nvfp4_global=glob, compute_stream=cs.cuda_stream,
+                         transfer_stream=ts.cuda_stream if two_streams else 0)
+
+        def chunk():
+            ctx.prefill_begin(0)
+            for l in range(L):
+                ctx.prefill_layer(l & 1, l, l + 1 if l + 1 < L else -1, T, xs[l], lg[l], ys[l])
+
+        with torch.cuda.stream(cs):
+            chunk()
+        torch.cuda.synchronize(device)
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(cs):
+                e0.record(cs)
+                chunk()
+                e1.record(cs)
+            torch.cuda.synchronize(device)
+            times.append(e0.elapsed_time(e1))
+        ctx.profile_enable(True)
+        with torch.cuda.stream(cs):
+            chunk()
+        prof = ctx.profile_read()
+        assert ctx.status() == ft.FT_OK
+        ctx.close()
+        return statistics.median(times), prof
+
+    t_db, prof = measure(True)
+    t_sb, _ = measure(False)
+    return t_db, t_sb, prof
+
+
+def prefill_summary(sh, T, t_db, t_sb, prof, peaks):
+    L = sh.L
+    h2d = prof["pf_h2d"]["ms"]
+    comp = sum(v["ms"] for k_, v in prof.items() if k_ != "pf_h2d")
+    g1 = prof["pf_gemm1_swiglu"]["ms"] / L
+    g2 = prof["pf_gemm2"]["ms"] / L
+    fl1 = 2.0 * T * sh.k * 2 * sh.F * sh.H
+    fl2 = 2.0 * T * sh.k * sh.F * sh.H
+    tf = (fl1 + fl2) / ((g1 + g2) * 1e-3) / 1e12
+    tot = sum(v["ms"] for v in prof.values())
+    leg = {"tok_s": round(T * L / (t_db * 1e-3), 1), "ms_chunk": round(t_db, 2),
+           "eta": round(max(h2d, comp) / t_db, 4), "h2d_GBps": round(L * sh.E * sh.record_bytes / (h2d * 1e-3) / 1e9, 1),
+           "sb_ms": round(t_sb, 2), "gemm_frac": round(tf / peaks["bf16_tflops"], 4),
+           "gemm_TFs": [round(fl1 / (g1 * 1e-3) / 1e12, 1), round(fl2 / (g2 * 1e-3) / 1e12, 1)]}
+    detail = dict(leg, ms_h2d=round(h2d, 3), ms_compute=round(comp, 3),
+                  hidden_fraction=round((h2d + comp - t_db) / min(h2d, comp), 4),
+                  double_buffer_speedup=round(t_sb / t_db, 4),
+                  roofline_gemm={"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                                 "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+                                 "flops_per_layer": fl1 + fl2, "peak_source": peaks["source"],
+                                 "traffic": traffic_from_profiles("pf_gemm")},
+                  kernels={k_: {"launches": v["launches"], "ms_total": round(v["ms"], 3),
+                                "share": round(v["ms"] / tot, 4)} for k_, v in prof.items()})
+    return leg, detail
+
+
+def run_prefill_bench(device, peaks, reps: int = 3):
+    """Prefill workload: 4 layers, E=128, top-8, H=2048, F=768, T=8192, 256
+    slots, full-layer double buffer.  Chunk = prefill_begin + 4 prefill_layer
+    calls, timed with CUDA events on the compute stream; per-kernel device
+    times from the library's event records in one further chunk; the same
+    chunk with the copies on the compute stream as the single-buffer A/B."""
+    import torch
+    import moe_expert_cache_gb300 as ft
+    wl = synth.PREFILL
+    sh = wl.shape
+    pool = torch.empty(sh.L * sh.E * sh.record_bytes, dtype=torch.uint8, pin_memory=True)
+    synth.fill_host_pool(pool.numpy(), sh, wl.seed)
+    t_db, t_sb, prof = prefill_chunk_times(ft, sh, wl.S, wl.T, pool, None, device, reps)
+    leg, detail = prefill_summary(sh, wl.T, t_db, t_sb, prof, peaks)
+    detail["workload"] = ("prefill: 4 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, T=8192, 256 slots, "
+                          "full-layer double buffer")
+    return leg, detail
+
+
+def run_large_nvfp4_bench(device, peaks, link_peak):
+    """Large NVFP4 workload: 8 MoE layers, E=256, top-8, H=4096, F=2048,
+    NVFP4 records (16 drawn experts repeated over the 2048 records), 512
+    slots, AR(1) rho=0.8 logits, B_P=52.7, B_H=150: 64 decode steps at T=1
+    then 64 at T=64 from an empty cache (eager library calls, CUDA-event time
+    of the steps, fills included), then one T=4096 prefill chunk of all 8
+    layers through the full-layer double buffer.  The link floor of a decode
+    phase is its fills' bytes over the measured host link."""
+    import torch
+    import moe_expert_cache_gb300 as ft
+    wl = synth.LARGE_NVFP4
+    sh = wl.shape
+    L, E, H = sh.L, sh.E, sh.H
+    pool, glob = repeated_pool(sh, 0)
+    cs = torch.cuda.Stream(device)
+    ctx = ft.Context(L, E, sh.k, H, sh.F, wl.S, pool, fmt=sh.fmt, T_max=64, nvfp4_global=glob,
+                     compute_stream=cs.cuda_stream)
+    leg, detail = {}, {}
+    lp = link_peak or 211.0
+    for T, steps in ((1, 64), (64, 64)):
+        lg = torch.from_numpy(synth.ar1_logits(wl.seed, steps, L, T, E, wl.rho)).to(device)
+        x = torch.from_numpy(np.stack([synth.tokens_bf16(wl.seed, 0, l, T, H) for l in range(L)]).view(np.int16)).to(
+            device).view(torch.bfloat16)
+        pc = torch.zeros(T, H, device=device)
+        y = torch.empty(T, H, device=device)
+        c0 = ctx.counters()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):
+            e0.record(cs)
+            for st in range(steps):
+                for l in range(L):
+                    ctx.route_ctl(l, T, logits=lg[st, l], B_P=wl.B_P, B_H=wl.B_H)
+                    ctx.moe_forward(x[l], pc, y)
+            e1.record(cs)
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1)
+        c1 = ctx.counters()
+        d = {k_: c1[k_] - c0[k_] for k_ in c1}
+        floor = d["fills"] * sh.record_bytes / (lp * 1e9) * 1e3
+        leg[f"t{T}"] = {"tok_s": round(T * steps / (ms * 1e-3), 1), "ms_step": round(ms / steps, 3),
+                        "floor_ms_step": round(floor / steps, 3)}
+        detail[f"t{T}"] = dict(leg[f"t{T}"], fills_per_layer_step=round(d["fills"] / max(1, d["calls"]), 3),
+                               hit_rate=round(d["hits"] / max(1, d["unique"]), 4))
+    assert ctx.status() == ft.FT_OK
+    ctx.close()
+    t_db, t_sb, prof = prefill_chunk_times(ft, sh, wl.S, 4096, pool, glob, device, reps=2)
+    pl, pd = prefill_summary(sh, 4096, t_db, t_sb, prof, peaks)
+    leg["prefill"] = {k_: pl[k_] for k_ in ("tok_s", "ms_chunk", "eta", "h2d_GBps")}
+    detail["prefill"] = pd
+    detail["workload"] = ("Large NVFP4: 8 MoE layers, E=256, top-8, hidden 4096, ffn 2048, 512 slots, AR(1) rho=0.8, "
+                          "B_P=52.7, B_H=150; 64 steps T=1 then 64 steps T=64 from an empty cache; T=4096 prefill "
+                          "chunk of 8 layers (double buffer)")
+    del pool
+    return leg, detail
 
 
 # ---------------------------------------------------------- oracle timing
@@ -770,38 +1059,37 @@ def cpu_baseline(pool_np, seconds: float) -> dict:
     L = WORKLOAD.shape.L
     tok_s = WORKLOAD.T * done / L / dt
     return {"value": round(tok_s, 5), "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"{done} layer-steps of the workload (control + fp64 FFN of all 8 routed experts, "
-                      f"weights read from the host pool) in {dt:.1f} s; tokens/s = layer-steps/{L}/s"}
+            "sample": f"{done} layer-steps (control + fp64 FFN of 8 experts) in {dt:.1f} s; tok/s = layer-steps/{L}/s"}
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm, on this machine's host cores."""
+    """The oracle as the reference arm, on this machine's host cores: W
+    warm-up and K timed samples, one sample = one MoE layer of one decode
+    token of the headline workload."""
     if rank != 0:
         return None
-    import torch
     sh = WORKLOAD.shape
     pool = np.empty(sh.L * sh.E * sh.record_bytes, dtype=np.uint8)
     synth.fill_host_pool(pool, sh, WORKLOAD.seed)
     W, K = args.warmup, args.steps
-    # a step of this arm is one sampled layer-step, bounded in total time
-    oracle_samples(pool, min(W, 2))
-    done, dt = oracle_samples(pool, K, args.cpu_seconds * 4)
+    oracle_samples(pool, W)
+    done, dt = oracle_samples(pool, K)
     L = sh.L
     v = WORKLOAD.T * done / L / dt
     cores = _blas_threads()
-    del torch
-    return {"metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": world, "steps": done, "warmup": min(W, 2),
+    return {"metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(1e3 * dt / max(1, done), 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "impl": "reference",
-            "config": {"workload": "decode T=1: 48 MoE layers, E=128, top-8, hidden 2048, ffn 768, BF16, "
-                                   "1536 slots, AR(1) rho=0.8, B_P=52.7, B_H=120"},
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded AR(1) logits, N(0,0.02) bf16 weights)",
+            "impl": "reference", "config": headline_config(world),
             "cpu_baseline": {"value": round(v, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"{done} layer-steps (one step = one MoE layer of one decode token)"},
             "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------- profiler cases
+
 def run_ncu_case(args):
-    """A small single-layer case for profiler captures (not a bench line).
+    """A small single-layer BF16 case for profiler captures (not a bench line).
 
     One layer of the decode T=1 shape (E=128, top-8, H=2048, F=768) in 128
     slots.  Every call routes the token to experts 0..7-q (resident) plus q
@@ -834,27 +1122,26 @@ def run_ncu_case(args):
     ctx.close()
     if st != ft.FT_OK:
         raise SystemExit(f"device status {st}")
-    return None
 
 
-def run_ncu_fp4(args):
-    """A small FP4 case for profiler captures (not a bench line).
+def run_ncu_quant(args):
+    """A small quantised case for profiler captures (not a bench line).
 
     One layer of the Large shape (E=256, top-8, H=4096, F=2048) with NVFP4
-    (fmt 1) or MXFP4 (fmt 2) records in 16 slots; T=1 calls alternate
-    between experts 0..7 and 8..15, so after the first two (the fills) every
-    launch reads 8 resident records and the 226 MB working set exceeds L2.
-    Twelve calls; capture e.g. the seventh expert launch with
-    `ncu -k regex:expert_ffn_fp4 -s 6 -c 1`.
+    (fmt 1), MXFP4 (fmt 2) or block-FP8 (fmt 3) records in 16 slots; T=1
+    calls alternate between experts 0..7 and 8..15, so after the first two
+    (the fills) every launch reads 8 resident records and the working set
+    (two sets of 8 records) exceeds L2.  Twelve calls; capture e.g. the
+    seventh expert launch with `ncu -k regex:expert_ffn_fp4 -s 6 -c 1`.
     """
     import torch
     import moe_expert_cache_gb300 as ft
 
     ft.load()
-    fmt = args.ncu_fp4
+    fmt = args.ncu_quant
     H, F, E, k = 4096, 2048, 256, 8
     sh = synth.Shape(L=1, E=E, k=k, H=H, F=F, fmt=fmt)
-    pool, glob = _fp4_pool(sh, 0, distinct=2)
+    pool, glob = repeated_pool(sh, 0, distinct=2)
     ctx = ft.Context(1, E, k, H, F, 16, pool, fmt=fmt, T_max=1, nvfp4_global=glob)
     x = torch.from_numpy(synth.tokens_bf16(0, 0, 0, 1, H).view(np.int16)).cuda().view(torch.bfloat16)
     pc = torch.zeros(1, H, device="cuda")
@@ -869,53 +1156,60 @@ def run_ncu_fp4(args):
     ctx.close()
     if st != ft.FT_OK:
         raise SystemExit(f"device status {st}")
-    return None
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=240)
-    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--windows", type=int, default=0,
+                    help="timed windows of K steps (0: as many as fill --timed-seconds, 3..50)")
+    ap.add_argument("--timed-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-t16", action="store_true", help="skip the decode T=16 (resize) measurement")
+    ap.add_argument("--no-hbm", action="store_true", help="skip the BF16 hits-only (HBM) measurement")
     ap.add_argument("--no-fp4", action="store_true",
-                    help="skip the quantised (NVFP4, MXFP4, block-FP8) decode measurement")
-    ap.add_argument("--fp4-only", action="store_true",
-                    help="only the quantised decode measurement (one JSON object)")
+                    help="skip the quantised (NVFP4, MXFP4, block-FP8) hits-only decode measurement")
+    ap.add_argument("--no-large", action="store_true", help="skip the Large NVFP4 workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--prefill-only", action="store_true",
-                    help="run only the prefill measurement and print its object (no bench line)")
-    ap.add_argument("--ncu-fp4", type=int, default=None, metavar="FMT",
-                    help="run the small FP4 profiling case (1 = NVFP4, 2 = MXFP4) and exit")
+    ap.add_argument("--leg", default=None, choices=["prefill", "quant", "hbm", "large"],
+                    help="run one leg alone and print its detail object (no bench line)")
+    ap.add_argument("--ncu-quant", type=int, default=None, metavar="FMT",
+                    help="run the small quantised profiling case (1 NVFP4, 2 MXFP4, 3 block-FP8) and exit")
     ap.add_argument("--ncu-case", type=int, default=None, metavar="Q",
-                    help="run the small single-layer profiling case with Q fills per call (0..8) and exit")
+                    help="run the small single-layer BF16 profiling case with Q fills per call (0..8) and exit")
     args = ap.parse_args()
-    if args.ncu_fp4 is not None:
-        if args.ncu_fp4 not in (1, 2):
-            raise SystemExit("--ncu-fp4 takes 1 (NVFP4) or 2 (MXFP4)")
-        run_ncu_fp4(args)
+    if args.ncu_quant is not None:
+        if args.ncu_quant not in (1, 2, 3):
+            raise SystemExit("--ncu-quant takes 1 (NVFP4), 2 (MXFP4) or 3 (block-FP8)")
+        run_ncu_quant(args)
         return
     if args.ncu_case is not None:
         if not 0 <= args.ncu_case <= 8:
             raise SystemExit("--ncu-case takes 0..8")
         run_ncu_case(args)
         return
-    if args.prefill_only:
+    if args.leg:
         import torch
         torch.cuda.set_device(0)
         import moe_expert_cache_gb300 as ft
         ft.load()
-        print(json.dumps({"prefill": run_prefill_bench(torch.device("cuda", 0), read_peaks())}), flush=True)
-        return
-    if args.fp4_only:
-        import torch
-        torch.cuda.set_device(0)
-        import moe_expert_cache_gb300 as ft
-        ft.load()
-        print(json.dumps({"quant_decode": run_quant_decode_bench(torch.device("cuda", 0), read_peaks())}), flush=True)
+        dev, peaks = torch.device("cuda", 0), read_peaks()
+        if args.leg == "prefill":
+            r = run_prefill_bench(dev, peaks)
+        elif args.leg == "quant":
+            r = run_quant_decode_bench(dev, peaks)
+        elif args.leg == "large":
+            r = run_large_nvfp4_bench(dev, peaks, measure_h2d_peak(dev))
+        else:
+            sh = WORKLOAD.shape
+            pool = torch.empty(sh.E * sh.record_bytes, dtype=torch.uint8, pin_memory=True)
+            synth.fill_host_pool(pool.numpy(), synth.Shape(L=1, E=sh.E, k=sh.k, H=sh.H, F=sh.F), WORKLOAD.seed)
+            r = run_bf16_hbm_bench(pool, dev, peaks)
+        print(json.dumps({args.leg: r[1]}), flush=True)
         return
     rank, world, local_rank = dist_env()
     if args.warmup < 3:
@@ -925,7 +1219,7 @@ def main():
     else:
         out = run_ours(args, rank, world, local_rank)
     if rank == 0 and out is not None:
-        print(json.dumps(out), flush=True)
+        print(json.dumps(out, separators=(",", ":")), flush=True)
 
 
 if __name__ == "__main__":
