@@ -10,7 +10,8 @@ hit/miss, q, fill set, LRU victims, map update), the fills, the expert
 gate/up + SwiGLU and down + gated merge with the CPU-set partial sum.
 
 Timing: W eager warm-up steps, then R consecutive windows of exactly K steps
-of the same AR(1) sequence.  The K steps are captured from the library calls
+of the same AR(1) sequence (R = ceil(256 / K), at least 3: the windows cover
+the workload's 256 steps from a cache that started empty).  The K steps are captured from the library calls
 into one CUDA graph (no profiling nodes in it), instantiated and uploaded
 before timing; before each window the window's inputs are copied into the
 graph's input buffers (untimed).  Each window is bracketed by a barrier and a
@@ -398,11 +399,6 @@ def measure_h2d_peak(device) -> float:
     return best
 
 
-def spread(ms: list) -> dict:
-    return {"n": len(ms), "median_ms": round(statistics.median(ms), 3), "min_ms": round(min(ms), 3),
-            "max_ms": round(max(ms), 3)}
-
-
 # ------------------------------------------------------------ our arm
 
 class Decoder:
@@ -474,21 +470,19 @@ def run_ours(args, rank, world, local_rank):
     ts = torch.cuda.Stream(device)
     dec = Decoder(ft, pool, device, K, s, ts)
 
-    # ---- warm-up: W eager steps (its time sizes the number of windows)
+    # ---- warm-up: W eager steps
     lg_w, x_w = decode_inputs(W)
     lg_wd = torch.from_numpy(lg_w).to(device)
     x_wd = torch.from_numpy(x_w).to(device).view(torch.bfloat16)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):
-        e0.record(s)
         for i in range(W):
             for l in range(L):
                 dec.ctx.route_ctl(l, T, logits=lg_wd[i, l], B_P=wl.B_P, B_H=wl.B_H)
                 dec.ctx.moe_forward(x_wd[i, l], dec.pc[l], dec.y[l])
-        e1.record(s)
     torch.cuda.synchronize(device)
-    ms_step_est = max(0.5, e0.elapsed_time(e1) / max(1, W))
-    R = args.windows or int(min(50, max(3, math.ceil(args.timed_seconds * 1e3 / (K * ms_step_est)))))
+    # windows: enough to cover the workload's configured steps (256 decode
+    # steps at T=1), at least 3
+    R = args.windows or int(min(50, max(3, math.ceil(wl.steps / K))))
     R = int(max_over_ranks(float(R), world, device))
     n_steps = W + (R + 1) * K  # R timed windows + one profiled window
     lg_all, x_all = decode_inputs(n_steps)
@@ -732,14 +726,18 @@ def run_decode_t16_bench(pool, device, link_peak):
 
 
 class L2Flusher:
-    """Writes a buffer twice the size of L2 so the next launch reads HBM."""
+    """Reads a buffer twice the size of L2 so the next launch reads HBM.  A
+    read leaves only clean lines behind: a write would leave L2 full of dirty
+    lines whose write-back would steal bandwidth from the timed launch."""
 
     def __init__(self, device):
         import torch
-        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+        self.buf = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+        self.out = torch.empty((), dtype=torch.float32, device=device)
 
     def __call__(self):
-        self.buf.zero_()
+        import torch
+        torch.amax(self.buf, dim=0, out=self.out)
 
 
 def hits_only_times(ctx, T, routes, x, pc, y, flush, stream, device):
@@ -800,7 +798,7 @@ def run_bf16_hbm_bench(pool, device, peaks, calls: int = 24):
         hbm = kernel_bytes(sh1, T, d)["expert_ffn"]["hbm"] / max(1, d["calls"])
         gbs = hbm / (us * 1e-6) / 1e9
         leg[f"t{T}"] = {"us": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
-                        "traffic": traffic_from_profiles("expert_ffn", hbm)}
+                        "traffic": traffic_from_profiles("expert_ffn_q0", hbm)}
         detail[f"t{T}"] = dict(leg[f"t{T}"], hits_per_launch=round(d["hits"] / max(1, d["calls"]), 2),
                                bytes_per_launch=int(hbm), calls=d["calls"])
     assert ctx.status() == ft.FT_OK
@@ -1165,8 +1163,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--windows", type=int, default=0,
-                    help="timed windows of K steps (0: as many as fill --timed-seconds, 3..50)")
-    ap.add_argument("--timed-seconds", type=float, default=3.0)
+                    help="timed windows of K steps (0: enough to cover the workload's 256 steps, 3..50)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-t16", action="store_true", help="skip the decode T=16 (resize) measurement")

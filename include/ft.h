@@ -124,7 +124,10 @@ const char* ft_status_str(ft_status s);
  *                  rounding of e4m3 * scale).
  *   T_max          largest T of a decode call (ft_route_ctl), 1..256, with
  *                  T_max*k <= 4096 and T_max*H <= 32768 (the tokens of a
- *                  decode call are staged in shared memory).
+ *                  decode call are staged in shared memory); the decode
+ *                  kernel of the format must have a shared-memory plan for
+ *                  every T <= T_max (BF16: two ring slots of 16 rows of H,
+ *                  so H up to about 3400), else FT_ERR_ARG.
  *   T_prefill_max  largest T of a prefill layer call; 0 disables prefill (no
  *                  prefill scratch is allocated).  Prefill needs H % 256 == 0,
  *                  2F % 256 == 0 and E <= 256.  NVFP4 contexts with prefill
@@ -304,8 +307,9 @@ ft_status ft_measure_link(ft_ctx* ctx, int32_t n_records, int32_t reps, double* 
  *   x              DEVICE bf16 [T, H];  partial_C DEVICE fp32 [T, H] or NULL;
  *   y              DEVICE fp32 [T, H], not aliasing x or partial_C.
  *   T, k, H, F     T*k <= 1024, k <= 16, H and F multiples of 64, T*H <= 32768,
- *                  and 65536 + T*k*F*4 <= FT_NOALLOC_SCRATCH_BYTES (else
- *                  FT_ERR_ARG).
+ *                  65536 + T*k*F*4 <= FT_NOALLOC_SCRATCH_BYTES, and a
+ *                  shared-memory plan of the expert kernel for these sizes
+ *                  (as ft_layer_init's BF16 check; else FT_ERR_ARG).
  *   stream         cudaStream_t to run on (NULL = legacy default stream).
  * Scratch: one file-scope device array of FT_NOALLOC_SCRATCH_BYTES per device
  * that loads the library, held until the process exits; no cudaMalloc,

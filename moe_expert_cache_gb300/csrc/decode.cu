@@ -750,45 +750,64 @@ static constexpr int kFillSlots = 3;                     // fused-fill ring chun
 // block, the worklist metadata and the fill math warp's segment sums, then the
 // ring (as many slots as fit, at most 4) and the fused-fill ring.  A ring slot
 // holds one phase-A chunk (16 rows of H) or one phase-B stage (R rows of W_d
-// followed by the h rows of the entry's tokens).  The fill ring has 2..4
-// chunks of 16 KiB (smaller if that would leave fewer than two ring slots); a
-// fill unit chunk holds the gate and up rows of fpf features, or of one
-// feature over H / nks columns when one feature does not fit.
-cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
-    const int G = num_sms;
-    if (p.wait_ns == 0) p.wait_ns = FT_WAIT_LIMIT_NS;
-    const int RMAX = (p.H + G - 1) / G;
-    const bool xf32 = (size_t)p.T * p.H * 4 <= 65536;
-    const size_t xbytes = (size_t)p.T * p.H * (xf32 ? 4 : 2);
-    const size_t TK = (size_t)p.T * p.k;
+// followed by the h rows of the entry's tokens).  The fill ring has 3 chunks
+// of 4 KiB; a fill unit chunk holds the gate and up rows of fpf features, or
+// of one feature over H / nks columns when one feature does not fit.
+struct Bf16Plan {
+    size_t smem, slot;
+    int nstage, fpf, nks;
+};
+
+static bool bf16_plan(int H, int F, int T, int k, int G, Bf16Plan& pl) {
+    const int RMAX = (H + G - 1) / G;
+    const bool xf32 = (size_t)T * H * 4 <= 65536;
+    const size_t xbytes = (size_t)T * H * (xf32 ? 4 : 2);
+    const size_t TK = (size_t)T * k;
     const size_t head = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127) +
-                        (((5 * TK + 1) * 4 + 127) & ~(size_t)127) + (((size_t)2 * p.T * 4 + 127) & ~(size_t)127);
-    size_t slot = (size_t)2 * FPC * p.H * 2;
-    const size_t down = (((size_t)RMAX * p.F * 2 + 127) & ~(size_t)127) + (size_t)p.T * p.F * 4;
+                        (((5 * TK + 1) * 4 + 127) & ~(size_t)127) + (((size_t)2 * T * 4 + 127) & ~(size_t)127);
+    size_t slot = (size_t)2 * FPC * H * 2;
+    const size_t down = (((size_t)RMAX * F * 2 + 127) & ~(size_t)127) + (size_t)T * F * 4;
     if (down > slot) slot = down;
     slot = (slot + 127) & ~(size_t)127;
-    if (head >= kSmemLimit) return cudaErrorInvalidValue;
     // The fill ring is deliberately small: the host link's bandwidth-delay
     // product is well under 1 MB, and host reads queued beyond it delay the
     // HBM reads of every other SM behind them in the memory system.
     const size_t fch = kFillChunk;
     const int nf = kFillSlots;
-    if (head + nf * fch + 2 * slot > kSmemLimit) return cudaErrorInvalidValue;
+    if (head >= kSmemLimit || head + nf * fch + 2 * slot > kSmemLimit) return false;
     int nst = (int)((kSmemLimit - head - nf * fch) / slot);
     if (nst > 4) nst = 4;
-    p.nstage = nst;
-    p.stage_bytes = (unsigned)slot;
-    p.fill_chunk = (unsigned)fch;
-    p.fill_slots = nf;
     // fill unit: fpf whole features (a power of two up to 16, so a unit stays
     // inside one 16-row gate/up group), or one feature in nks K segments
     int fpf = 1, nks = 1;
-    while (4ull * p.H * (2 * fpf) <= fch && 2 * fpf <= 16) fpf *= 2;
-    while (4ull * (p.H / nks) > fch) nks *= 2;
-    if (p.H % nks || (p.H / nks) % 8) return cudaErrorInvalidValue;
-    p.fill_fpf = fpf;
-    p.fill_nks = nks;
-    const size_t smem = head + slot * nst + (size_t)nf * fch;
+    while (4ull * H * (2 * fpf) <= fch && 2 * fpf <= 16) fpf *= 2;
+    while (4ull * (H / nks) > fch) nks *= 2;
+    if (H % nks || (H / nks) % 8) return false;
+    pl.smem = head + slot * nst + (size_t)nf * fch;
+    pl.slot = slot;
+    pl.nstage = nst;
+    pl.fpf = fpf;
+    pl.nks = nks;
+    return true;
+}
+
+bool expert_ffn_fits(int H, int F, int T, int k, int num_sms) {
+    Bf16Plan pl;
+    return bf16_plan(H, F, T, k, num_sms, pl);
+}
+
+cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s) {
+    const int G = num_sms;
+    if (p.wait_ns == 0) p.wait_ns = FT_WAIT_LIMIT_NS;
+    Bf16Plan pl;
+    if (!bf16_plan(p.H, p.F, p.T, p.k, G, pl)) return cudaErrorInvalidValue;
+    p.nstage = pl.nstage;
+    p.stage_bytes = (unsigned)pl.slot;
+    p.fill_chunk = (unsigned)kFillChunk;
+    p.fill_slots = kFillSlots;
+    p.fill_fpf = pl.fpf;
+    p.fill_nks = pl.nks;
+    const size_t smem = pl.smem;
     cudaError_t e = ensure_dynamic_smem((const void*)expert_ffn_kernel, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -234,6 +234,9 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
         return fail(FT_ERR_ARG);  // the down kernel keeps [assignment, rows] in shared memory
     if ((fmt == FT_FMT_NVFP4 || fmt == FT_FMT_MXFP4) && !expert_ffn_fp4_fits(H, F, T_max, k, fmt, c->num_sms))
         return fail(FT_ERR_ARG);  // the FP4 decode kernel has no shared-memory plan for T_max tokens
+    if (fmt == FT_FMT_BF16)
+        for (int t = 1; t <= T_max; ++t)  // the x staging format switches with T: check every T
+            if (!expert_ffn_fits(H, F, t, k, c->num_sms)) return fail(FT_ERR_ARG);
     // Device address of the host pool: the mapping of page-locked memory, or
     // the host address itself where the GPU reads pageable memory directly.
     void* dptr = nullptr;

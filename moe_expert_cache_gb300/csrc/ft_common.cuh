@@ -453,6 +453,8 @@ struct ExpertParams {
 cudaError_t launch_route_ctl(const CtlParams& p, cudaStream_t s);
 cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);
 cudaError_t launch_expert_ffn(ExpertParams p, int num_sms, cudaStream_t s);
+// whether the BF16 decode kernel has a shared-memory plan for T tokens
+bool expert_ffn_fits(int H, int F, int T, int k, int num_sms);
 // fmt: FT_FMT_NVFP4 (e4m3 block-16 scales) or FT_FMT_MXFP4 (E8M0 block-32 scales)
 cudaError_t launch_expert_ffn_fp4(ExpertParams p, int fmt, int num_sms, cudaStream_t s);
 // whether the FP4 kernel has a shared-memory plan for T tokens (checked at init for T_max)

@@ -166,6 +166,7 @@ extern "C" ft_status ft_expert_ffn_noalloc(const void* records, int32_t n_record
 
     DeviceSetup ds;
     if (!device_setup(ds)) return FT_ERR_CUDA;
+    if (!expert_ffn_fits(H, F, T, k, ds.num_sms)) return FT_ERR_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     noalloc_prep_kernel<<<1, PREP_THREADS, 0, s>>>(route_records, gates, T, k, n_records, ds.scratch);
     if (cudaGetLastError() != cudaSuccess) return FT_ERR_CUDA;

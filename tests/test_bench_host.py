@@ -89,7 +89,10 @@ def test_committed_traffic_entries_name_existing_sources():
             continue
         for src in v["sources"]:
             assert os.path.exists(os.path.join(ROOT, src)), (k, src)
-        assert v["dram_bytes"] > 0 and v["alg_bytes"] > 0
+        if "alg_bytes" in v:
+            assert v["dram_bytes"] > 0 and v["alg_bytes"] > 0
+        else:
+            assert v["dram_bytes_per_launch"] > 0
 
 
 def test_cli_help_needs_no_gpu():

@@ -294,10 +294,14 @@ def test_resize_that_cannot_allocate_leaves_the_cache_intact(ft):
     resize to more slots than device memory holds fails in cudaMalloc (a
     genuine out-of-memory answer, no fault); the maps, stamps and slot bytes
     are unchanged and decoding continues against the oracle."""
-    wl = synth.Workload("oom", synth.Shape(L=1, E=16, k=4, H=4096, F=2048), S=6, steps=5, T=2, rho=None,
+    wl = synth.Workload("oom", synth.Shape(L=1, E=16, k=4, H=2048, F=2048), S=6, steps=5, T=2, rho=None,
                         sigma=None, B_P=1.0, B_H=2.0)
     sh = wl.shape
     pool, _ = hz.pinned_pool(sh, 0)
+    # a BF16 shape whose decode kernel has no shared-memory plan is refused at init
+    with pytest.raises(ft.FtError) as ei:
+        ft.Context(1, 16, 4, 4096, 2048, 6, pool, T_max=2)
+    assert ei.value.status == ft.FT_ERR_ARG
     ctx = ft.Context(sh.L, sh.E, sh.k, sh.H, sh.F, wl.S, pool, T_max=wl.T)
     st = ctl.CacheState.empty(sh.L, sh.E, wl.S)
     w = hz.Weights(wl.seed, sh, 0)
@@ -305,9 +309,9 @@ def test_resize_that_cannot_allocate_leaves_the_cache_intact(ft):
         _tiny_oracle_step(ctx, st, wl, step, w)
     before = ctx.ctl_state()
     slots = [ctx.read_slot(s) for s in range(wl.S)]
-    # 6000 records of 50 MB: about 302 GB, more than the GPU's memory
+    # 13000 records of 25 MB: about 327 GB, more than the GPU's memory
     with pytest.raises(ft.FtError) as ei:
-        ctx.cache_resize(6000)
+        ctx.cache_resize(13000)
     assert ei.value.status == ft.FT_ERR_OOM
     assert ctx.S == wl.S
     after = ctx.ctl_state()
