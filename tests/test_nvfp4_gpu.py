@@ -311,16 +311,16 @@ def test_large_fp8_decode(ft):
 
 
 def test_fp4_init_rejects_a_t_max_without_a_kernel_plan(ft):
-    """T_max = 128 at the Large layer shape leaves the FP4 decode kernel no
-    shared-memory plan (its per-CTA output rows alone take 110 KB): init
-    refuses it instead of the first forward failing.  The control kernel's
-    own limit (26 KB here) is not what rejects it."""
+    """T_max = 256 at the Large layer shape leaves the FP4 decode kernel no
+    shared-memory plan (its per-route output rows and worklist no longer fit
+    beside two ring slots): init refuses it instead of the first forward
+    failing.  T_max = 64 has a plan."""
     import torch
     pool = torch.empty(4096, dtype=torch.uint8, pin_memory=True)
     with pytest.raises(ft.FtError):
-        ft.Context(1, 256, 8, 4096, 2048, 16, pool, fmt=ft.FT_FMT_NVFP4, T_max=128,
+        ft.Context(1, 256, 8, 4096, 2048, 16, pool, fmt=ft.FT_FMT_NVFP4, T_max=256,
                    nvfp4_global=np.ones(256, dtype=np.float32))
     with pytest.raises(ft.FtError):
-        ft.Context(1, 256, 8, 4096, 2048, 16, pool, fmt=ft.FT_FMT_MXFP4, T_max=128)
+        ft.Context(1, 256, 8, 4096, 2048, 16, pool, fmt=ft.FT_FMT_MXFP4, T_max=256)
     ctx = ft.Context(1, 256, 8, 4096, 2048, 16, pool, fmt=ft.FT_FMT_MXFP4, T_max=64)
     ctx.close()
