@@ -766,6 +766,44 @@ def hits_only_times(ctx, T, routes, x, pc, y, flush, stream, device):
     return statistics.median(us), d
 
 
+def one_fill_times(ctx, E, x, pc, y, flush, stream, calls: int = 6):
+    """Expert-kernel device time of T=1 calls that route 7 resident experts
+    and 1 expert evicted just before (ft_set_ctl_state), so each call makes
+    exactly one fill beside 7 hits; L2 flushed before each call.  Returns
+    (median us, the standalone fill time of one record in us)."""
+    import torch
+    k = 8
+    w = torch.full((1, k), 1.0 / k, device=x.device)
+    us = []
+    for i in range(calls):
+        sfi, ifs, stp, clk = ctx.ctl_state()
+        victim = 8 * (i + 1)  # resident, not among the call's 7 hits
+        s_v = int(sfi[victim])
+        sfi[victim] = -1
+        ifs[s_v] = -1
+        stp[s_v] = 0
+        ctx.set_ctl_state(sfi, ifs, stp, clk)
+        ids = torch.tensor([[0, 1, 2, 3, 4, 5, 6, victim]], dtype=torch.int32, device=x.device)
+        c0 = ctx.counters()
+        with torch.cuda.stream(stream):
+            flush()
+            ctx.route_ctl(0, 1, topk_ids=ids, topk_w=w, B_P=1.0, B_H=1.0)
+            ctx.profile_enable(True)
+            ctx.moe_forward(x[:1], pc[:1], y[:1])
+        pr = ctx.profile_read()
+        ctx.profile_enable(False)
+        c1 = ctx.counters()
+        assert c1["fills"] - c0["fills"] == 1 and c1["hits"] - c0["hits"] == 7
+        us.append(1e3 * pr["expert_ffn"]["ms"] / pr["expert_ffn"]["launches"])
+    gbps = ctx.measure_link(1, 3)
+    return statistics.median(us), None if not gbps else 1e6 * ctx_record_bytes(ctx) / (gbps * 1e9)
+
+
+def ctx_record_bytes(ctx) -> int:
+    import moe_expert_cache_gb300 as ft
+    return ft.record_bytes(ctx.H, ctx.F, ctx.fmt)
+
+
 def run_bf16_hbm_bench(pool, device, peaks, calls: int = 24):
     """BF16 expert kernel with every record resident (q = 0), the HBM-bound
     case: one layer of the decode shapes (E=128, top-8, H=2048, F=768) in 128
@@ -851,12 +889,17 @@ def run_quant_decode_bench(device, peaks, calls_t1: int = 48, calls_t64: int = 1
                             "hbm_bytes_per_launch": int(hbm), "achieved_GBps": round(gbs, 1),
                             "frac": round(gbs / peaks["hbm_gbs"], 4),
                             "traffic": traffic_from_profiles(kname, hbm)}
+        # one fill beside 7 hits: the fill streams inside the expert launch
+        us1, fill_us = one_fill_times(ctx, E, x, pc, y, flush, cs)
+        res["fill1"] = [round(us1, 1), round(fill_us, 1) if fill_us else None]
+        det["t1_one_fill"] = {"us_per_launch": round(us1, 2), "standalone_fill_us": round(fill_us, 2) if fill_us else None,
+                              "hits_only_us": det["t1"]["us_per_launch"]}
         assert ctx.status() == ft.FT_OK
         ctx.close()
         del pool
         leg[name] = res
         detail[name] = det
-    leg["cols"] = "t: [us per launch, frac of HBM]"
+    leg["cols"] = "t1, t64: [us per launch, frac of HBM]; fill1: [us per launch with 1 fill + 7 hits, standalone fill us]"
     return leg, detail
 
 

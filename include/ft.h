@@ -118,9 +118,9 @@ const char* ft_status_str(ft_status s);
  *                  FP8 (block-FP8, the same section's "FP8 weights and
  *                  block-scale data") needs H % 128 == 0, F % 128 == 0,
  *                  nvfp4_global == NULL and T_max*k*ceil(H/SMs)*4 bytes of
- *                  shared memory (at most 227 KiB); its decode runs the
- *                  pending fill as a standalone copy before the expert
- *                  kernels, and its prefill stages the layer in bf16 (one
+ *                  shared memory (at most 227 KiB); its decode streams the
+ *                  pending fills inside the gate/up kernel, as the other
+ *                  formats do, and its prefill stages the layer in bf16 (one
  *                  rounding of e4m3 * scale).
  *   T_max          largest T of a decode call (ft_route_ctl), 1..256, with
  *                  T_max*k <= 4096 and T_max*H <= 32768 (the tokens of a

@@ -9,12 +9,19 @@
 // interleaved in groups of 16] [W_d values H x F] [W_g scales F/128 x H/128
 // fp32] [W_u scales F/128 x H/128] [W_d scales H/128 x F/128].
 //
-// Two plain kernels, without the fused fill of the FP4 and BF16 kernels (a
-// pending fill is completed by the standalone fill kernel before them):
-//   * fp8_gateup_kernel: every warp takes (entry, feature) units; a unit
-//     streams the feature's gate and up rows with 16-byte loads that skip L1,
-//     against every token of the entry, and writes SwiGLU(h) to the fp32
-//     scratch [assignment, F];
+// Two kernels:
+//   * fp8_gateup_kernel (cooperative, two CTAs per SM): every warp takes
+//     (entry, feature) units; a unit streams the feature's gate and up rows
+//     with 16-byte loads that skip L1, against every token of the entry, and
+//     writes SwiGLU(h) to the fp32 scratch [assignment, F].  The fills the
+//     control pass left pending stream in the same launch: the first thread
+//     of each CTA's last warp copies the CTA's share of every fill record
+//     from the host pool through a small TMA ring into the victim slot and
+//     counts itself in the fill's counter, then that warp joins the others,
+//     which claim the CTA's units one at a time; the units of a fill entry
+//     wait (bounded) until every CTA has counted, while the resident
+//     entries' units go ahead, so the host-link time overlaps the HBM-bound
+//     work;
 //   * fp8_down_kernel: CTA c owns output rows [c*H/G, (c+1)*H/G); its warps
 //     take (entry, row) units against the h rows, then the CTA merges the
 //     gated sum with the CPU-set partial sum in fixed order.
@@ -28,7 +35,10 @@
 
 namespace {
 
-constexpr int A_THREADS = 256;
+constexpr int A_WARPS = 8;                  // warps of the gate/up kernel (the last one fills first)
+constexpr int A_THREADS = A_WARPS * 32;
+constexpr int A_FILL_SLOTS = 2;             // fused-fill ring chunks per CTA (two CTAs per SM)
+constexpr unsigned A_FILL_CHUNK = 4096;     // bytes of one fused-fill ring chunk
 constexpr int B_THREADS = 512;
 constexpr int FP8_BLK = 128;
 
@@ -145,14 +155,46 @@ __device__ __forceinline__ void gu_group(const uint8_t* wg, const uint8_t* wu, c
     }
 }
 
+// Dynamic shared memory of the gate/up kernel: x as fp32 when XS, then the
+// fused-fill ring.
+__host__ __device__ inline size_t fp8_a_xbytes(int T, int H, bool xs) {
+    return xs ? (((size_t)T * H * 4 + 127) & ~(size_t)127) : 0;
+}
+
 template <bool XS>
 __global__ void __launch_bounds__(A_THREADS, 2) fp8_gateup_kernel(ExpertParams p) {
-    extern __shared__ __align__(16) float xs_dyn[];
+    extern __shared__ __align__(128) unsigned char smem_a[];
+    __shared__ uint64_t fbar[A_FILL_SLOTS];
+    __shared__ int s_xready, s_next;
+    float* xs_dyn = reinterpret_cast<float*>(smem_a);
     const int H = p.H, F = p.F, T = p.T;
     const int ugpu = p.info[INFO_UGPU];
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (XS) {
-        for (int i = tid; i < T * H / 8; i += A_THREADS) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) {
+        s_xready = 0;
+        s_next = 0;
+    }
+    __syncthreads();
+    if (wid == A_WARPS - 1) {
+        // ------------------------------------------- fused fill, then compute
+        // this CTA's share of every fill record (nothing when q = 0), then
+        // this warp's own units once x is staged
+        if (lane == 0 && p.do_fill)
+            ft::fill_share_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
+                               p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, blockIdx.x, gridDim.x,
+                               smem_a + fp8_a_xbytes(T, H, XS), fbar, A_FILL_CHUNK, A_FILL_SLOTS, p.err);
+        if (XS && lane == 0) {
+            const uint64_t t0 = ft::globaltimer();
+            while (!ft::ld_acquire_cta(&s_xready)) {
+                if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+                    atomicOr(p.err, FT_DEVERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (XS) {
+        for (int i = tid; i < T * H / 8; i += (A_WARPS - 1) * 32) {
             float f8[8];
             ft::bf16x8_to_f32(reinterpret_cast<const uint4*>(p.x)[i], f8);
             const int t = (8 * i) / H, e = 8 * i - t * H;
@@ -160,12 +202,29 @@ __global__ void __launch_bounds__(A_THREADS, 2) fp8_gateup_kernel(ExpertParams p
             *reinterpret_cast<float4*>(row + xrot(e)) = make_float4(f8[0], f8[1], f8[2], f8[3]);
             *reinterpret_cast<float4*>(row + xrot(e + 4)) = make_float4(f8[4], f8[5], f8[6], f8[7]);
         }
-        __syncthreads();
+        ft::named_bar_sync(1, (A_WARPS - 1) * 32);  // every warp but the fill warp
+        if (tid == 0) ft::st_release_cta(&s_xready, 1);
     }
     const size_t nbg = (size_t)(F / FP8_BLK) * (H / FP8_BLK);  // scale blocks of W_g (and of W_u)
-    const int warps = gridDim.x * (A_THREADS / 32);
-    for (int u = blockIdx.x * (A_THREADS / 32) + (tid >> 5); u < ugpu * F; u += warps) {
+    int waited = -1;  // the last fill whose record this warp saw complete
+    // this CTA's units c, c + G, ... (resident entries first, fills last),
+    // claimed one at a time by whichever warp is free, so the fill warp
+    // takes what is left once its copies are done
+    for (;;) {
+        int i = 0;
+        if (lane == 0) i = atomicAdd(&s_next, 1);
+        const int u = blockIdx.x + __shfl_sync(0xffffffffu, i, 0) * gridDim.x;
+        if (u >= ugpu * F) break;
         const int e = u / F, f = u - e * F;
+        if (p.do_fill) {
+            const int fi = p.wl_fill[e];
+            if (fi >= 0 && fi != waited) {
+                int ok = 1;
+                if (lane == 0) ok = ft::wait_filled(p.ready, fi, gridDim.x, p.err) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) continue;  // gave up: the status reports it
+                waited = fi;
+            }
+        }
         const int off = p.wl_off[e], ntok = p.wl_off[e + 1] - off;
         const uint8_t* rec = p.slot_pool + (size_t)p.wl_slot[e] * p.rb;
         const int grow = (f >> 4) * 32 + (f & 15);  // gate row; the up row is 16 later
@@ -310,19 +369,29 @@ __global__ void __launch_bounds__(B_THREADS, 1) fp8_down_kernel(ExpertParams p) 
 }  // namespace
 
 cudaError_t launch_expert_ffn_fp8(ExpertParams p, int num_sms, cudaStream_t s) {
-    const size_t xbytes = (size_t)p.T * p.H * 4;
-    const bool xs = xbytes <= 96 * 1024;
-    const size_t smem_a = xs ? xbytes : 0;
+    const bool xs = (size_t)p.T * p.H * 4 <= 96 * 1024;
+    const size_t smem_a = fp8_a_xbytes(p.T, p.H, xs) + (size_t)A_FILL_SLOTS * A_FILL_CHUNK;
     const void* fa = xs ? (const void*)fp8_gateup_kernel<true> : (const void*)fp8_gateup_kernel<false>;
-    if (smem_a > 0) {
-        cudaError_t e = ensure_dynamic_smem(fa, smem_a);
-        if (e != cudaSuccess) return e;
-    }
-    if (xs)
-        fp8_gateup_kernel<true><<<2 * num_sms, A_THREADS, smem_a, s>>>(p);
-    else
-        fp8_gateup_kernel<false><<<2 * num_sms, A_THREADS, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = ensure_dynamic_smem(fa, smem_a);
+    if (e != cudaSuccess) return e;
+    // cooperative: the units of a fill entry wait for every CTA's share of
+    // the record, so all CTAs must be resident together
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fa, A_THREADS, smem_a);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((per_sm < 2 ? per_sm : 2) * num_sms);
+    cfg.blockDim = dim3(A_THREADS);
+    cfg.dynamicSmemBytes = smem_a;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fa, args);
     if (e != cudaSuccess) return e;
     const int RMAX = (p.H + num_sms - 1) / num_sms;
     const size_t o_bytes = (((size_t)p.T * p.k * RMAX + 3) & ~(size_t)3) * 4;

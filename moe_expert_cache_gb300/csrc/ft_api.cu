@@ -373,7 +373,6 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err; p.gbar = c->gbar;
     p.wl_fid = c->wl_fid; p.gscale = c->nvfp4_global; p.x16 = c->x16; p.xsc = c->xsc; p.hmax = c->hmax;
     p.wait_ns = c->wait_ns;
-    if (c->fmt == FT_FMT_FP8) FT_CUDA(flush_fill(c));  // no fused fill in the FP8 kernels
     p.do_fill = c->fill_pending ? 1 : 0;
     p.host_pool = (const uint4*)c->host_pool_dev;
     p.fill_slot = c->fill_slot;
