@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,7 +21,7 @@ struct PrefillState {
     // scratch (sized for T_max)
     void* xperm = nullptr;    // bf16 [T*k, H]  tokens gathered in expert order
     void* hperm = nullptr;    // bf16 [T*k, F]  SwiGLU activations in expert order
-    float* outp = nullptr;    // fp32 [T*k, H]  gate * expert output per row
+    __half* outp = nullptr;   // f16 [T*k, H]  gate * expert output per row (summed in fp32 by the combine)
     int* ids = nullptr;       // [T*k]
     float* gates = nullptr;   // [T*k]
     int* perm_tok = nullptr;  // [T*k] token of each expert-ordered row

@@ -18,8 +18,11 @@
 //   pf_gather   x rows into expert order (bf16)
 //   GEMM1       per expert, X_e [M_e x H] . W_gu^T [H x 2F] on tcgen05, SwiGLU
 //               epilogue -> h [M_e x F] bf16
-//   GEMM2       per expert, h_e . W_d^T [F x H] -> gate * out [M_e x H] fp32
-//   pf_combine  y_t = sum_j (gate * out)[row(t, j)], j ascending
+//   GEMM2       per expert, h_e . W_d^T [F x H] -> gate * out [M_e x H] f16
+//               (fp32 accumulation; the f16 rounding adds about 1e-5 relative
+//               to the bf16 rounding of h, and halves the bytes of the per-route
+//               outputs written here and read back by the combine)
+//   pf_combine  y_t = sum_j (gate * out)[row(t, j)] in fp32, j ascending
 #include "ft_common.cuh"
 #include "ft_prefill.cuh"
 #include "ft_tc.cuh"
@@ -173,9 +176,9 @@ __global__ void __launch_bounds__(256) pf_gather_kernel(const uint4* __restrict_
     for (int v = lane; v < nv; v += 32) dst[v] = src[v];
 }
 
-// One CTA per token: y_t = sum_j out[pos(t, j)] in j order (out already
-// carries the gate).
-__global__ void __launch_bounds__(256) pf_combine_kernel(const float* __restrict__ outp, const int* __restrict__ pos,
+// One CTA per token: y_t = sum_j out[pos(t, j)] in j order, in fp32 (out
+// already carries the gate; f16 values).
+__global__ void __launch_bounds__(256) pf_combine_kernel(const __half* __restrict__ outp, const int* __restrict__ pos,
                                                          int k, int H, float* __restrict__ y) {
     const int t = blockIdx.x;
     int rows[16];
@@ -183,7 +186,10 @@ __global__ void __launch_bounds__(256) pf_combine_kernel(const float* __restrict
     for (int c = threadIdx.x * 4; c < H; c += 256 * 4) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
-            const float4 v = *reinterpret_cast<const float4*>(outp + (size_t)rows[j] * H + c);
+            const uint2 raw = *reinterpret_cast<const uint2*>(outp + (size_t)rows[j] * H + c);
+            const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+            const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+            const float4 v = make_float4(lo.x, lo.y, hi.x, hi.y);
             acc.x += v.x;
             acc.y += v.y;
             acc.z += v.z;
@@ -219,7 +225,7 @@ __global__ void pf_invalidate_kernel(int s0, int n, int* __restrict__ slot_for_i
 //   warps 2-5   epilogue: thread = accumulator row, tcgen05.ld 32 columns at a
 //               time (the next load in flight while one is processed); mode 0 =
 //               SwiGLU of the interleaved gate/up columns to bf16 h, mode 1 =
-//               gate * value to fp32 out.  Each warp transposes its 32 rows x
+//               gate * value to f16 out.  Each warp transposes its 32 rows x
 //               128 bytes through a padded shared-memory block, so every store
 //               instruction writes four whole 128-byte lines.
 // All waits are bounded; after a failed wait every role stops, the MMA thread
@@ -240,11 +246,11 @@ struct GemmArgs {
     int E;                 // experts of the layer (tensor-map z extent)
     int nk;                // K blocks
     int n_tiles;           // 256-column tiles per expert
-    int mode;              // 0: SwiGLU -> bf16 h; 1: gate * out -> fp32
+    int mode;              // 0: SwiGLU -> bf16 h; 1: gate * out -> f16
     const int* offsets;    // [E+1] expert row offsets
     __nv_bfloat16* hout;   // mode 0: [rows, F]
     int F;
-    float* fout;           // mode 1: [rows, ldo]
+    __half* fout;          // mode 1: [rows, ldo] f16
     int ldo;
     const float* row_gate; // mode 1: gate of each expert-ordered row
     const float* escale;   // per-expert factor of the weights (NVFP4 global) or null
@@ -414,12 +420,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) grouped_gemm_kernel(const __g
                     d[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                     d[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                 } else {
-                    float4* d = reinterpret_cast<float4*>(eb + lane * EPI_ROW);
+                    // gate * value as f16: a chunk's 32 columns are 64 bytes,
+                    // half (c & 1) of the staged 128-byte line
+                    uint32_t packed[16];
 #pragma unroll
-                    for (int i2 = 0; i2 < 8; ++i2)
-                        d[i2] = make_float4(gate * __uint_as_float(v[4 * i2]), gate * __uint_as_float(v[4 * i2 + 1]),
-                                            gate * __uint_as_float(v[4 * i2 + 2]),
-                                            gate * __uint_as_float(v[4 * i2 + 3]));
+                    for (int i2 = 0; i2 < 16; ++i2) {
+                        const __half2 hv = __floats2half2_rn(gate * __uint_as_float(v[2 * i2]),
+                                                             gate * __uint_as_float(v[2 * i2 + 1]));
+                        packed[i2] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
+                    uint4* d = reinterpret_cast<uint4*>(eb + lane * EPI_ROW + (c & 1) * 64);
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2)
+                        d[i2] = make_uint4(packed[4 * i2], packed[4 * i2 + 1], packed[4 * i2 + 2], packed[4 * i2 + 3]);
                 }
             };
             // the staged 32 rows x 128 bytes -> global, four whole lines per store
@@ -435,7 +448,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) grouped_gemm_kernel(const __g
                             p.mode == 0
                                 ? reinterpret_cast<unsigned char*>(p.hout + (size_t)grow * p.F + ti.nt * (GN / 2) +
                                                                    (c >> 2) * 64)
-                                : reinterpret_cast<unsigned char*>(p.fout + (size_t)grow * p.ldo + ti.nt * GN + c * 32);
+                                : reinterpret_cast<unsigned char*>(p.fout + (size_t)grow * p.ldo + ti.nt * GN +
+                                                                   (c >> 1) * 64);
                         *reinterpret_cast<uint4*>(g + cq) = v4;
                     }
                 }
@@ -447,12 +461,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) grouped_gemm_kernel(const __g
             for (int c = 0; c < GN / 32; c += 2) {
                 tc::tmem_wait_ld(va);
                 tc::tmem_ld32(base + (uint32_t)((c + 1) * 32), vb);
-                stage(va, c);
-                if (p.mode == 1) flush(c);
+                stage(va, c);  // c is even: the first half of a line in both modes
                 tc::tmem_wait_ld(vb);
                 if (c + 2 < GN / 32) tc::tmem_ld32(base + (uint32_t)((c + 2) * 32), va);
                 stage(vb, c + 1);
-                if (p.mode == 1 || ((c + 1) & 3) == 3) flush(c + 1);
+                if (p.mode == 1 || ((c + 1) & 3) == 3) flush(c + 1);  // mode 1: a line per two chunks
             }
             tc::fence_before_sync();
             __syncwarp();
@@ -532,7 +545,7 @@ ft_status prefill_alloc(PrefillState& pf, int T_max, int k, int H, int F, int E,
     }
     const size_t TK = (size_t)T_max * k;
     if (cudaMalloc(&pf.xperm, TK * H * 2) != cudaSuccess || cudaMalloc(&pf.hperm, TK * F * 2) != cudaSuccess ||
-        cudaMalloc(&pf.outp, TK * H * 4) != cudaSuccess || cudaMalloc(&pf.ids, TK * 4) != cudaSuccess ||
+        cudaMalloc(&pf.outp, TK * H * 2) != cudaSuccess || cudaMalloc(&pf.ids, TK * 4) != cudaSuccess ||
         cudaMalloc(&pf.gates, TK * 4) != cudaSuccess || cudaMalloc(&pf.perm_tok, TK * 4) != cudaSuccess ||
         cudaMalloc(&pf.pos, TK * 4) != cudaSuccess || cudaMalloc(&pf.row_gate, TK * 4) != cudaSuccess ||
         cudaMalloc(&pf.counts, (size_t)E * 4) != cudaSuccess ||
