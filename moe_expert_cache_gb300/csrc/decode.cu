@@ -264,7 +264,7 @@ __device__ __noinline__ void down_entry(uint32_t wbase, uint32_t hs, int ntok, i
 
 __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_wd;     // this CTA's W_d rows of every fill are stored (1), or the fill failed (2)
+    __shared__ int s_fitem[8], s_fsub[8];  // fill ring: item and K segment of the chunk in each slot (-1: end)
     __shared__ int s_armed;  // ring steps armed by the producer (-1 after a failure)
     const int H = p.H, F = p.F, T = p.T, k = p.k;
     const int nst = p.nstage;
@@ -337,44 +337,41 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.gbar) : "memory");
         if (n == 3u * (unsigned)G - 1u) {
             for (int e = 0; e < ugpu; ++e) p.ready[e] = 0u;
+            for (int r = 0; r < q; ++r) p.wdc[r] = 0u;
+            p.gbar[2] = 0u;
             p.gbar[1] = 0u;
             p.gbar[0] = 0u;
         }
     };
 
-    // fused-fill geometry: unit = (fill r, group of fpf features), split into
-    // nks K segments of KS columns; units go to CTAs round-robin.  Every CTA
-    // also copies its own W_d rows [r0, r1) of each fill, in npc pieces.
+    // fused-fill geometry.  Each fill record is cut into items: first its
+    // W_d block in pieces of one ring chunk (NWD items), then its gate/up rows
+    // in units of fpf features (upr items), a unit split into nks chunks of
+    // KS columns.  The CTAs' copy warps draw items from one counter of the
+    // launch (fill 0's items first), so a CTA whose host reads return sooner
+    // copies more, and every CTA finishes its part at about the same time.
     const int nf = p.fill_slots;
     const unsigned fch = p.fill_chunk;
     const int fpf = p.fill_fpf, nks = p.fill_nks;
     const int KS = H / nks;
     const int upr = F / fpf;
-    const int U = q * upr;
-    const int n_gu = (c < U ? (U - c + G - 1) / G : 0) * nks;
-    const unsigned long long wdb = (unsigned long long)R * F * 2;
-    const int npc = (int)((wdb + fch - 1) / fch);
-    const int n_wd = q * npc;  // this CTA's W_d pieces, first in its chunk stream
-    const int n_fill = n_wd + n_gu;
+    const unsigned long long wdt = (unsigned long long)H * F * 2;  // W_d bytes of a record
+    const int NWD = (int)((wdt + fch - 1) / fch);
+    const int ipf = NWD + upr;  // items per fill
+    const int n_items = q * ipf;
     const unsigned partb = (unsigned)fpf * KS * 2u;  // gate (or up) bytes of one unit chunk
-    auto gu_chunk = [&](int g, int& r, int& f0, int& seg) {
-        const int u = c + (g / nks) * G;
-        seg = g - (g / nks) * nks;
-        r = u / upr;
-        f0 = (u - r * upr) * fpf;
-    };
-
-    // The fill copy warp owns its ring barriers and s_wd and starts at once;
+    // The fill copy warp owns its ring barriers and slot tags and starts at once;
     // the other warps stage the worklist and x meanwhile.  Named barrier 3:
     // the copy warp arrives once its state is initialised, the rest sync.
     if (wid == FILL_ISSUE_WARP) {
         if (lane == 0) {
             for (int s = 0; s < nf; ++s) {
-                ft::mbar_init(&ffull[s], 32);  // one cp.async arrival per lane of the copy warp
+                // one cp.async arrival per lane of the copy warp, and lane 0's
+                // arrival that publishes the slot's tag
+                ft::mbar_init(&ffull[s], 33);
                 ft::mbar_init(&fcons[s], 1);
             }
             ft::mbar_fence_init();
-            s_wd = 0;
         }
         __syncwarp();
         asm volatile("bar.arrive 3, %0;" ::"n"(EXPERT_THREADS) : "memory");
@@ -414,84 +411,129 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
     // ------------------------------------------------- fused fill: copy warp
     // host pool -> fill ring by per-lane cp.async (the load/store path, so the
     // slow host reads do not queue ahead of the ring's bulk copies from HBM),
-    // then fill ring -> victim slot by one bulk store.  A unit chunk is
-    // released for the next load once the math warp has used it and its store
-    // has read it.
+    // then fill ring -> victim slot by one bulk store.  A chunk is released
+    // for the next load once the math warp has used it and its store has read
+    // it.  Lane 0 draws the next item one ahead, so the counter's latency
+    // overlaps the chunks in flight.  The W_d pieces a CTA stored are
+    // published in wdc[r] (GPU scope, after their stores complete) when its
+    // sequence moves past them; the producers of every CTA wait for the
+    // count before reading their W_d rows of the fill from its slot.
     if (wid == FILL_ISSUE_WARP) {
         const uint8_t* host = reinterpret_cast<const uint8_t*>(p.host_pool);
         uint8_t* pool = const_cast<uint8_t*>(p.slot_pool);
-        const unsigned long long wd0 = (unsigned long long)4 * F * H + (unsigned long long)r0 * F * 2;
+        const unsigned long long wd0 = (unsigned long long)4 * F * H;
         const unsigned long long upoff = (unsigned long long)16 * H * 2;  // up rows follow gate rows by 16 rows
-        // offset within the record, bytes of one part, and fill index of chunk g
-        auto locate = [&](int g, unsigned long long& off, unsigned& n, int& r) {
-            if (g >= n_wd) {
-                int f0, seg;
-                gu_chunk(g - n_wd, r, f0, seg);
+        // offset within the record and bytes of one part of chunk (item, seg)
+        auto locate = [&](int item, int seg, unsigned long long& off, unsigned& n) {
+            const int li = item % ipf;
+            if (li >= NWD) {
+                const int f0 = (li - NWD) * fpf;
                 const unsigned long long row = (unsigned long long)(f0 >> 4) * 32 + (f0 & 15);
                 off = (row * H + (unsigned long long)seg * KS) * 2;
                 n = partb;
             } else {
-                const int w = g;
-                r = w / npc;
-                const unsigned long long po = (unsigned long long)(w - r * npc) * fch;
+                const unsigned long long po = (unsigned long long)li * fch;
                 off = wd0 + po;
-                n = (unsigned)(wdb - po < fch ? wdb - po : fch);
+                n = (unsigned)(wdt - po < fch ? wdt - po : fch);
             }
         };
-        auto load = [&](int g, int s) {  // all lanes
-            unsigned long long off;
-            unsigned n;
-            int r;
-            locate(g, off, n, r);
-            unsigned char* d = fring + (size_t)s * fch;
-            const uint8_t* src = host + (unsigned long long)p.fill_fid[r] * p.rb + off;
-            for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + v, src + v);
-            if (g >= n_wd)
-                for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + n + v, src + upoff + v);
-            ft::cp_async_arrive(&ffull[s]);
-        };
-        auto store = [&](int g, int s) {  // lane 0
-            unsigned long long off;
-            unsigned n;
-            int r;
-            locate(g, off, n, r);
-            const unsigned char* d = fring + (size_t)s * fch;
-            uint8_t* dst = pool + (unsigned long long)p.fill_slot[r] * p.rb + off;
-            ft::bulk_s2g(dst, d, n);
-            if (g >= n_wd) ft::bulk_s2g(dst + upoff, d + n, n);
-            ft::bulk_commit();
-        };
-        // s_wd: this CTA's W_d rows of every fill are in their slots (1), or
-        // the fill failed before that (2)
-        auto publish_wd = [&](int v) {  // lane 0
-            ft::bulk_wait_all();
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            ft::st_release_cta(&s_wd, v);
-        };
-        if (lane == 0 && n_wd == 0) ft::st_release_cta(&s_wd, 1);
-        int issued = 0;
-        for (; issued < n_fill && issued < nf; ++issued) load(issued, issued);
-        bool ok = true;
-        for (int g = 0; g < n_fill; ++g) {
-            const int s = g % nf;
-            const uint32_t par = (uint32_t)(g / nf) & 1u;
-            int w = 1;
-            if (lane == 0) {
-                w = ft::mbar_wait(&ffull[s], par, p.err, p.wait_ns);
-                if (w) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // cp.async data -> bulk store
-                    store(g, s);
-                    if (g == n_wd - 1) publish_wd(1);
-                    w = ft::mbar_wait(&fcons[s], par, p.err, p.wait_ns);
-                    ft::bulk_wait_read_all();
+        // CTA c takes item c first; every later item is drawn from the
+        // counter (values from G on) right after the current item's first
+        // chunk is issued, and read when that item is exhausted.
+        unsigned* claims = p.gbar + 2;
+        int ahead = 0;  // lane 0: the draw in flight
+        int nxt = c;    // the next item to start, once `known`
+        bool known = true;
+        int cur = -1, sub = 0, nsub = 0;
+        bool more = true;
+        auto load = [&](int s) {  // all lanes: the next chunk into slot s, or the end tag
+            bool started = false;
+            if (more && sub == nsub) {
+                if (!known) nxt = G + __shfl_sync(0xffffffffu, ahead, 0);
+                if (nxt >= n_items) {
+                    more = false;
+                } else {
+                    cur = nxt;
+                    sub = 0;
+                    nsub = cur % ipf < NWD ? 1 : nks;
+                    known = false;
+                    started = true;
                 }
             }
-            if (!__shfl_sync(0xffffffffu, w, 0)) {
-                ok = false;
-                break;
+            if (!more) {
+                if (lane == 0) {
+                    s_fitem[s] = -1;
+                    ft::mbar_arrive(&ffull[s]);
+                }
+                ft::cp_async_arrive(&ffull[s]);
+                return;
             }
-            if (issued < n_fill) {
-                load(issued, s);
+            const int seg = sub++;
+            unsigned long long off;
+            unsigned n;
+            locate(cur, seg, off, n);
+            unsigned char* d = fring + (size_t)s * fch;
+            const uint8_t* src = host + (unsigned long long)p.fill_fid[cur / ipf] * p.rb + off;
+            for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + v, src + v);
+            if (cur % ipf >= NWD)
+                for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + n + v, src + upoff + v);
+            if (lane == 0) {
+                s_fitem[s] = cur;
+                s_fsub[s] = seg;
+                ft::mbar_arrive(&ffull[s]);
+                if (started) ahead = (int)atomicAdd(claims, 1u);
+            }
+            ft::cp_async_arrive(&ffull[s]);
+        };
+        auto store = [&](int item, int seg, int s) {  // lane 0
+            unsigned long long off;
+            unsigned n;
+            locate(item, seg, off, n);
+            const unsigned char* d = fring + (size_t)s * fch;
+            uint8_t* dst = pool + (unsigned long long)p.fill_slot[item / ipf] * p.rb + off;
+            ft::bulk_s2g(dst, d, n);
+            if (item % ipf >= NWD) ft::bulk_s2g(dst + upoff, d + n, n);
+            ft::bulk_commit();
+        };
+        auto publish_wd = [&](int r, int n) {  // lane 0
+            ft::bulk_wait_all();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            ft::red_release_gpu_add(&p.wdc[r], (unsigned)n);
+        };
+        // prime the ring; `more` turns false once the end tag is in it
+        int issued = 0;
+        do load(issued++);
+        while (issued < nf && more);
+        int pend_r = 0, pend_n = 0;  // lane 0: W_d pieces stored, not yet published
+        for (int g = 0; g < issued; ++g) {
+            const int s = g % nf;
+            const uint32_t par = (uint32_t)(g / nf) & 1u;
+            int item = -1, w = 1;
+            if (lane == 0) {
+                item = s_fitem[s];
+                if (item >= 0) {
+                    w = ft::mbar_wait(&ffull[s], par, p.err, p.wait_ns);
+                    if (w) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // cp.async data -> bulk store
+                        store(item, s_fsub[s], s);
+                        if (item % ipf < NWD) {
+                            pend_r = item / ipf;
+                            ++pend_n;
+                            const int nx = s_fitem[(g + 1) % nf];  // the next chunk of this CTA, or the end tag
+                            if (nx < 0 || nx / ipf != pend_r || nx % ipf >= NWD) {
+                                publish_wd(pend_r, pend_n);
+                                pend_n = 0;
+                            }
+                        }
+                        w = ft::mbar_wait(&fcons[s], par, p.err, p.wait_ns);
+                        ft::bulk_wait_read_all();
+                    }
+                }
+            }
+            if (__shfl_sync(0xffffffffu, item, 0) < 0) break;  // the end tag
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            if (more) {
+                load(s);
                 ++issued;
             }
         }
@@ -499,25 +541,28 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         __syncwarp();
         if (lane == 0) {
             ft::bulk_wait_all();
-            if (ft::ld_acquire_cta(&s_wd) == 0) publish_wd(2);  // failed before its W_d rows were stored
             count_out();
         }
         return;
     }
 
     // ------------------------------------------ fused fill: gate/up math warp
-    // SwiGLU features of the fill units of this CTA, from the fill ring.
+    // SwiGLU features of the fill units this CTA copied, from the fill ring,
+    // in the copy warp's order, up to its end tag.
     if (wid == FILL_MATH_WARP) {
-        for (int g = 0; g < n_fill; ++g) {
+        for (int g = 0;; ++g) {
             const int s = g % nf;
             if (!__all_sync(0xffffffffu, ft::mbar_wait(&ffull[s], (uint32_t)(g / nf) & 1u, p.err, p.wait_ns))) break;
-            if (g < n_wd) {  // a W_d piece: acknowledged so the ring cannot lap this warp
+            const int item = s_fitem[s];
+            if (item < 0) break;
+            const int r = item / ipf, li = item - r * ipf;
+            if (li < NWD) {  // a W_d piece: acknowledged so the ring cannot lap this warp
                 __syncwarp();
                 if (lane == 0) ft::mbar_arrive(&fcons[s]);
                 continue;
             }
-            int r, f0, seg;
-            gu_chunk(g - n_wd, r, f0, seg);
+            const int seg = s_fsub[s];
+            const int f0 = (li - NWD) * fpf;
             const int off = m_off[nA + r];
             const int ntok = m_off[nA + r + 1] - off;
             const unsigned char* d = fring + (size_t)s * fch;
@@ -598,7 +643,6 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             };
             int it = 0;
             bool ok = true;
-            bool wd_ready = false;
             for (int a = c, e0 = 0; ok; ++it) {
                 const bool isB = stage_due(a, e0);
                 if (!isB && a >= NA) break;
@@ -619,23 +663,12 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
                     continue;
                 }
                 // phase-B stage: the W_d rows of its entries (those of a fill
-                // were stored by this CTA's fill warp), then the h rows of each
-                // entry once every feature of it is written
+                // once every piece of its W_d block is in the slot), then the
+                // h rows of each entry once every feature of it is written
                 const int e1 = stage_end(e0);
-                if (e0 >= nA && !wd_ready) {
-                    const uint64_t t0 = ft::globaltimer();
-                    int v;
-                    while ((v = ft::ld_acquire_cta(&s_wd)) == 0) {
-                        __nanosleep(128);
-                        if (ft::globaltimer() - t0 > p.wait_ns) {
-                            atomicOr(p.err, FT_DEVERR_TIMEOUT);
-                            break;
-                        }
-                    }
-                    if (v != 1) { ok = false; break; }
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    wd_ready = true;
-                }
+                for (int e = e0 > nA ? e0 : nA; e < e1 && ok; ++e)
+                    ok = ft::wait_count(&p.wdc[e - nA], (unsigned)NWD, p.err, p.wait_ns);
+                if (!ok) break;
                 unsigned tx = 0;
                 for (int e = e0; e < e1; ++e) tx += wb + hbytes(e);
                 ft::mbar_arrive_expect_tx(&full[st], tx);

@@ -54,6 +54,7 @@ struct ft_ctx {
     unsigned* err;
     unsigned* gbar;
     unsigned* ready;
+    unsigned* wdc;
     float* hbuf;
     bool fill_pending;
     unsigned long long wait_ns;  // limit of the BF16 decode kernel's progress waits
@@ -264,7 +265,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     const size_t o_clock = carve(4), o_ids = carve(TK * 4), o_gates = carve(TK * 4), o_slots = carve(TK * 4),
                  o_pos = carve(TK * 4), o_astok = carve(TK * 4), o_asg = carve(TK * 4),
                  o_wls = carve((size_t)E * 4), o_wlo = carve((size_t)(E + 1) * 4), o_wlf = carve((size_t)E * 4), o_wlfill = carve((size_t)E * 4),
-                 o_ready = carve((size_t)E * 4),
+                 o_ready = carve((size_t)E * 4), o_wdc = carve((size_t)E * 4),
                  o_fs = carve((size_t)E * 4),
                  o_ff = carve((size_t)E * 4), o_F = carve((size_t)E * 4), o_C = carve((size_t)E * 4),
                  o_v = carve((size_t)E * 4), o_info = carve(INFO_WORDS * 4), o_cnt = carve(CNT_WORDS * 8),
@@ -284,6 +285,7 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     c->wl_fid = (int*)(a + o_wlf);
     c->wl_fill = (int*)(a + o_wlfill);
     c->ready = (unsigned*)(a + o_ready);
+    c->wdc = (unsigned*)(a + o_wdc);
     c->fill_slot = (int*)(a + o_fs);
     c->fill_fid = (int*)(a + o_ff);
     c->Fl = (int*)(a + o_F);
@@ -379,6 +381,7 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.fill_fid = c->fill_fid;
     p.wl_fill = c->wl_fill;
     p.ready = c->ready;
+    p.wdc = c->wdc;
     c->fill_pending = false;
     {
         ProfScope ps(c->prof, FT_K_EXPERT, c->cs);

@@ -423,8 +423,8 @@ struct ExpertParams {
     const int* out_pos;
     float* hbuf;              // [T*k, F] fp32
     unsigned* err;
-    unsigned* gbar;           // [4] NVFP4: grid barrier (arrivals, generation); BF16: exit count, hits done;
-                              // zero at rest
+    unsigned* gbar;           // [4] NVFP4: grid barrier (arrivals, generation); BF16: exit count, hits done,
+                              // fill items drawn; zero at rest
     const int* wl_fid;        // [E] flat id of each GPU entry (NVFP4 global lookup)
     // fused cache fill (performed by this launch when do_fill != 0)
     int do_fill;
@@ -434,6 +434,7 @@ struct ExpertParams {
     const int* wl_fill;       // [E] fill index of entry i, or -1 for a hit
     unsigned* ready;          // NVFP4: [q] CTAs that finished their part of fill i;
                               // BF16: [ugpu] h features written per entry (zero at rest)
+    unsigned* wdc;            // BF16: [q] W_d pieces of fill i stored in its slot (zero at rest)
     unsigned fill_chunk;      // bytes of one fused-fill ring slot
     int fill_slots;           // fused-fill ring slots (2..4)
     int fill_fpf;             // BF16: features per fused-fill unit
