@@ -82,6 +82,141 @@ __device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsig
     return a < b ? a : b;
 }
 
+// a4: q = min(clamp(q0, 1, m), S - h) with q0 = round(m * B_P / B_H) in fp64
+// (halves away from zero); the host tabulates q0 for m <= E.
+__device__ int fill_count(const CtlParams& p, int m, int h, int S, int& q0, int& q1) {
+    q0 = q1 = 0;
+    if (m <= 0) return 0;
+    if (m < p.q0_n) {
+        q0 = p.q0tab[m];  // the same fp64 expression, evaluated on the host per m
+    } else {
+        const double x = __ddiv_rn(__dmul_rn((double)m, p.B_P), p.B_H);
+        const double r = round(x);  // halves away from zero
+        q0 = r > 1.0e9 ? 1000000000 : (int)r;
+    }
+    q1 = min(max(q0, 1), m);
+    return max(min(q1, S - h), 0);
+}
+
+// a6: victims = the q smallest (stamp, slot) keys, into s_vict[0..q) in
+// ascending key order; called by every thread of the block.  Small q: q
+// block-wide arg-min rounds; larger q: a radix select of the q-th stamp, then
+// a rank sort of the candidates below it.  Each taken slot's staged stamp is
+// set to clk (the hits were refreshed to clk before the call), so no slot is
+// taken twice.
+__device__ void select_victims(CtlShared& sh, unsigned* s_stamp, int* s_vict, int* s_cslot, unsigned* s_cst,
+                               const int S, const int q, const unsigned clk) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (q > 0 && q <= SMALL_Q) {
+        for (int r = 0; r < q; ++r) {
+            unsigned long long best = ~0ull;
+            for (int s = tid; s < S; s += CTL_THREADS)
+                best = umin64(best, ((unsigned long long)s_stamp[s] << 32) | (unsigned)s);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) best = umin64(best, __shfl_xor_sync(0xffffffffu, best, o));
+            if (lane == 0) sh.warp_key[wid] = best;
+            __syncthreads();
+            if (wid == 0) {
+                unsigned long long b = lane < CTL_WARPS ? sh.warp_key[lane] : ~0ull;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) b = umin64(b, __shfl_xor_sync(0xffffffffu, b, o));
+                if (lane == 0) {
+                    const int v = (int)(b & 0xffffffffu);
+                    s_vict[r] = v;
+                    s_stamp[v] = clk;  // taken: never the minimum again
+                }
+            }
+            __syncthreads();
+        }
+    } else if (q > SMALL_Q) {
+        unsigned prefix = 0u, pmask = 0u;
+        int need = q;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int i = tid; i < 256; i += CTL_THREADS) sh.hist[i] = 0;
+            __syncthreads();
+            for (int s = tid; s < S; s += CTL_THREADS) {
+                const unsigned st = s_stamp[s];
+                if ((st & pmask) == prefix) atomicAdd(&sh.hist[(st >> shift) & 255u], 1);
+            }
+            __syncthreads();
+            if (wid == 0) {
+                int c[8];
+                int sum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    c[i] = sh.hist[lane * 8 + i];
+                    sum += c[i];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int excl = incl - sum;
+                const unsigned ball = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+                if (lane == __ffs(ball) - 1) {
+                    int run = excl, b = lane * 8 + 7;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (run + c[i] >= need) {
+                            b = lane * 8 + i;
+                            break;
+                        }
+                        run += c[i];
+                    }
+                    sh.sel_bin = b;
+                    sh.sel_before = run;
+                }
+            }
+            __syncthreads();
+            prefix |= (unsigned)sh.sel_bin << shift;
+            pmask |= 255u << shift;
+            need -= sh.sel_before;
+        }
+        const unsigned tau = prefix;
+        const int c_lt = q - need;  // slots with stamp < tau are all victims; `need` of stamp == tau
+        if (tid == 0) {
+            sh.carry0 = 0;
+            sh.carry1 = 0;
+        }
+        __syncthreads();
+        for (int s0 = 0; s0 < S; s0 += CTL_THREADS) {
+            const int s = s0 + tid;
+            const unsigned st = s < S ? s_stamp[s] : 0xffffffffu;
+            const int flt = (s < S && st < tau) ? 1 : 0;
+            const int feq = (s < S && st == tau) ? 1 : 0;
+            int tot;
+            const int ex = block_excl_scan(flt | (feq << 16), sh.warp_tot, &tot);
+            const int ex_lt = (ex & 0xffff) + sh.carry0;
+            const int ex_eq = (ex >> 16) + sh.carry1;
+            if (flt) {
+                s_cslot[ex_lt] = s;
+                s_cst[ex_lt] = st;
+            }
+            if (feq && ex_eq < need) s_vict[c_lt + ex_eq] = s;
+            __syncthreads();
+            if (tid == 0) {
+                sh.carry0 += tot & 0xffff;
+                sh.carry1 += tot >> 16;
+            }
+            __syncthreads();
+        }
+        for (int i = tid; i < c_lt; i += CTL_THREADS) {
+            const unsigned si = s_cst[i];
+            const int li = s_cslot[i];
+            int r = 0;
+            for (int j = 0; j < c_lt; ++j) {
+                const unsigned sj = s_cst[j];
+                r += (sj < si) || (sj == si && s_cslot[j] < li);
+            }
+            s_vict[r] = li;
+        }
+        __syncthreads();
+    }
+
+}
+
 __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ CtlShared sh;
@@ -233,6 +368,157 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         return;
     }
 
+    // ---- small batches (T*k <= 32): one warp carries the pass, lane a
+    // holding assignment a = t*k + j, with votes and shuffles in place of
+    // the block-wide phases of the general path below; every warp joins for
+    // the victim search only.  Same decisions and outputs as that path.
+    if (TK <= 32) {
+        constexpr unsigned FULL = 0xffffffffu;
+        const bool act = lane < TK;
+        int e = 0, n_e = 0, r = 0, cls = 0, sl = -1, ldr = 0;
+        unsigned peers = 0, hitm = 0, fillm = 0;
+        int q = 0;
+        unsigned clk = 0;
+        if (wid == 0) {
+            // a2: dedup -- the lanes of one expert, its routed-token count, the first as leader
+            e = act ? s_ids[lane] : -1 - lane;  // idle lanes: keys no routed id matches
+            peers = __match_any_sync(FULL, e);
+            ldr = __ffs(peers) - 1;
+            n_e = __popc(peers);
+            const bool leader = act && ldr == lane;
+            // a3: classify against the layer's residency row
+            if (leader) {
+                sl = s_row[e];
+                cls = sl >= 0 ? 1 : 3;
+            }
+            hitm = __ballot_sync(FULL, cls == 1);
+            const unsigned missm = __ballot_sync(FULL, cls == 3);
+            const int u = __popc(__ballot_sync(FULL, leader)), h = __popc(hitm), m = __popc(missm);
+            // a5 order: rank of each miss by (count desc, id asc)
+            for (int i = 0; i < TK; ++i) {
+                const int e2 = __shfl_sync(FULL, e, i), n2 = __shfl_sync(FULL, n_e, i);
+                if ((missm >> i) & 1u) r += (n2 > n_e) || (n2 == n_e && e2 < e);
+            }
+            // a4: q; the clock advances once per pass
+            clk = sh.clk + 1u;
+            int qq = 0;
+            __syncwarp();
+            if (lane == 0) {
+                int q0, q1;
+                qq = fill_count(p, m, h, S, q0, q1);
+                sh.q0 = q0;
+                sh.q1 = q1;
+                sh.q = qq;
+                sh.u = u;
+                sh.h = h;
+                sh.m = m;
+                sh.clk = clk;
+            }
+            q = __shfl_sync(FULL, qq, 0);
+            // a5: F = the first q misses, C = the rest; a7 (part): hit stamps
+            if (cls == 3) {
+                if (r < q) {
+                    cls = 2;
+                    p.out_F[r] = e;
+                    s_order[r] = e;
+                } else {
+                    p.out_C[r - q] = e;
+                }
+            }
+            if (cls == 1) {
+                s_stamp[sl] = clk;
+                p.stamps[sl] = clk;
+            }
+            fillm = __ballot_sync(FULL, cls == 2);
+        }
+        __syncthreads();
+        // ---- a6: victims (every warp)
+        select_victims(sh, s_stamp, s_vict, s_cslot, s_cst, S, sh.q, sh.clk);
+        if (wid != 0) return;
+        // ---- a7: evict the victims' owners, install F, stamp the fills
+        if (lane < q) {
+            const int f = s_order[lane];
+            const int v = s_vict[lane];
+            const int o = s_owner[v];
+            if (o >= 0) p.slot_for_id[o] = -1;
+            const int fid = fbase + f;
+            p.id_for_slot[v] = fid;
+            p.slot_for_id[fid] = v;
+            p.stamps[v] = clk;
+            p.ready[lane] = 0u;
+            p.fill_slot[lane] = v;
+            p.fill_fid[lane] = fid;
+            p.out_victims[lane] = v;
+        }
+        if (cls == 2) sl = s_vict[r];
+        // ---- a7: worklist -- the hits in ascending expert id, then the
+        // fills in fill order; offsets are the routed-token counts before
+        int hidx = 0, hoff = 0, foff = 0;
+        for (int i = 0; i < TK; ++i) {
+            const int e2 = __shfl_sync(FULL, e, i), n2 = __shfl_sync(FULL, n_e, i), r2 = __shfl_sync(FULL, r, i);
+            if (((hitm >> i) & 1u) && e2 < e) {
+                ++hidx;
+                hoff += n2;
+            }
+            if (((fillm >> i) & 1u) && r2 < r) foff += n2;
+        }
+        const int hasg = (int)__reduce_add_sync(FULL, cls == 1 ? (unsigned)n_e : 0u);
+        const int fasg = (int)__reduce_add_sync(FULL, cls == 2 ? (unsigned)n_e : 0u);
+        const int nh = __popc(hitm);
+        int eo = 0;
+        if (cls == 1 || cls == 2) {
+            const int ent = cls == 1 ? hidx : nh + r;
+            eo = cls == 1 ? hoff : hasg + foff;
+            p.wl_slot[ent] = sl;
+            p.wl_fid[ent] = fbase + e;
+            p.wl_fill[ent] = cls == 1 ? -1 : r;
+            p.wl_off[ent] = eo;
+        }
+        // every assignment: its expert's class, slot and offset from the
+        // leader; its rank among the expert's tokens (ascending with the lane)
+        const int c2 = __shfl_sync(FULL, cls, ldr), s2 = __shfl_sync(FULL, sl, ldr), o2 = __shfl_sync(FULL, eo, ldr);
+        if (act) {
+            if (c2 == 1 || c2 == 2) {
+                const int pos = o2 + __popc(peers & ((1u << lane) - 1u));
+                p.as_tok[pos] = lane / k;
+                p.as_gate[pos] = s_g[lane];
+                p.out_pos[lane] = pos;
+                p.out_slots[lane] = s2;
+            } else {
+                p.out_pos[lane] = -1;
+                p.out_slots[lane] = -1;
+            }
+        }
+        if (lane == 0) {
+            const int ugpu = nh + q, nassign = hasg + fasg;
+            p.wl_off[ugpu] = nassign;
+            *p.clock = clk;
+            int* I = p.info;
+            I[INFO_LAYER] = p.layer;
+            I[INFO_T] = T;
+            I[INFO_U] = sh.u;
+            I[INFO_H] = sh.h;
+            I[INFO_M] = sh.m;
+            I[INFO_Q0] = sh.q0;
+            I[INFO_Q1] = sh.q1;
+            I[INFO_Q] = q;
+            I[INFO_NC] = sh.m - q;
+            I[INFO_UGPU] = ugpu;
+            I[INFO_NASSIGN] = nassign;
+            I[INFO_CLOCK] = (int)clk;
+            I[INFO_VALID] = 1;
+            unsigned long long* cn = p.counters;
+            cn[CNT_CALLS] += 1;
+            cn[CNT_UNIQUE] += sh.u;
+            cn[CNT_HITS] += sh.h;
+            cn[CNT_MISSES] += sh.m;
+            cn[CNT_FILLS] += q;
+            cn[CNT_CPU] += sh.m - q;
+            cn[CNT_ASSIGN] += nassign;
+        }
+        return;
+    }
+
     // ---- a2: dedup -- routed-token count n_e and token membership masks
     for (int a = tid; a < TK; a += CTL_THREADS) {
         const int e = s_ids[a];
@@ -276,19 +562,8 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         if (lane == 0) s_order[r] = e;
     }
     if (tid == 0) {
-        const int m = sh.m, h = sh.h;
-        int q0 = 0, q1 = 0, q = 0;
-        if (m > 0) {
-            if (m < p.q0_n) {
-                q0 = p.q0tab[m];  // the same fp64 expression, evaluated on the host per m
-            } else {
-                const double x = __ddiv_rn(__dmul_rn((double)m, p.B_P), p.B_H);
-                const double r = round(x);  // halves away from zero
-                q0 = r > 1.0e9 ? 1000000000 : (int)r;
-            }
-            q1 = min(max(q0, 1), m);
-            q = max(min(q1, S - h), 0);
-        }
+        int q0, q1;
+        const int q = fill_count(p, sh.m, sh.h, S, q0, q1);
         sh.q0 = q0;
         sh.q1 = q1;
         sh.q = q;
@@ -317,113 +592,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
     __syncthreads();
 
     // ---- a6: victims = q smallest (stamp, slot)
-    if (q > 0 && q <= SMALL_Q) {
-        for (int r = 0; r < q; ++r) {
-            unsigned long long best = ~0ull;
-            for (int s = tid; s < S; s += CTL_THREADS)
-                best = umin64(best, ((unsigned long long)s_stamp[s] << 32) | (unsigned)s);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) best = umin64(best, __shfl_xor_sync(0xffffffffu, best, o));
-            if (lane == 0) sh.warp_key[wid] = best;
-            __syncthreads();
-            if (wid == 0) {
-                unsigned long long b = lane < CTL_WARPS ? sh.warp_key[lane] : ~0ull;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) b = umin64(b, __shfl_xor_sync(0xffffffffu, b, o));
-                if (lane == 0) {
-                    const int v = (int)(b & 0xffffffffu);
-                    s_vict[r] = v;
-                    s_stamp[v] = clk;  // taken: never the minimum again
-                }
-            }
-            __syncthreads();
-        }
-    } else if (q > SMALL_Q) {
-        unsigned prefix = 0u, pmask = 0u;
-        int need = q;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = tid; i < 256; i += CTL_THREADS) sh.hist[i] = 0;
-            __syncthreads();
-            for (int s = tid; s < S; s += CTL_THREADS) {
-                const unsigned st = s_stamp[s];
-                if ((st & pmask) == prefix) atomicAdd(&sh.hist[(st >> shift) & 255u], 1);
-            }
-            __syncthreads();
-            if (wid == 0) {
-                int c[8];
-                int sum = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    c[i] = sh.hist[lane * 8 + i];
-                    sum += c[i];
-                }
-                int incl = sum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const int excl = incl - sum;
-                const unsigned ball = __ballot_sync(0xffffffffu, excl < need && need <= incl);
-                if (lane == __ffs(ball) - 1) {
-                    int run = excl, b = lane * 8 + 7;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (run + c[i] >= need) {
-                            b = lane * 8 + i;
-                            break;
-                        }
-                        run += c[i];
-                    }
-                    sh.sel_bin = b;
-                    sh.sel_before = run;
-                }
-            }
-            __syncthreads();
-            prefix |= (unsigned)sh.sel_bin << shift;
-            pmask |= 255u << shift;
-            need -= sh.sel_before;
-        }
-        const unsigned tau = prefix;
-        const int c_lt = q - need;  // slots with stamp < tau are all victims; `need` of stamp == tau
-        if (tid == 0) {
-            sh.carry0 = 0;
-            sh.carry1 = 0;
-        }
-        __syncthreads();
-        for (int s0 = 0; s0 < S; s0 += CTL_THREADS) {
-            const int s = s0 + tid;
-            const unsigned st = s < S ? s_stamp[s] : 0xffffffffu;
-            const int flt = (s < S && st < tau) ? 1 : 0;
-            const int feq = (s < S && st == tau) ? 1 : 0;
-            int tot;
-            const int ex = block_excl_scan(flt | (feq << 16), sh.warp_tot, &tot);
-            const int ex_lt = (ex & 0xffff) + sh.carry0;
-            const int ex_eq = (ex >> 16) + sh.carry1;
-            if (flt) {
-                s_cslot[ex_lt] = s;
-                s_cst[ex_lt] = st;
-            }
-            if (feq && ex_eq < need) s_vict[c_lt + ex_eq] = s;
-            __syncthreads();
-            if (tid == 0) {
-                sh.carry0 += tot & 0xffff;
-                sh.carry1 += tot >> 16;
-            }
-            __syncthreads();
-        }
-        for (int i = tid; i < c_lt; i += CTL_THREADS) {
-            const unsigned si = s_cst[i];
-            const int li = s_cslot[i];
-            int r = 0;
-            for (int j = 0; j < c_lt; ++j) {
-                const unsigned sj = s_cst[j];
-                r += (sj < si) || (sj == si && s_cslot[j] < li);
-            }
-            s_vict[r] = li;
-        }
-        __syncthreads();
-    }
+    select_victims(sh, s_stamp, s_vict, s_cslot, s_cst, S, q, clk);
 
     // ---- a7: evict the victims' owners, install F, stamp the fills
     for (int i = tid; i < q; i += CTL_THREADS) {
