@@ -78,8 +78,27 @@ __device__ int block_excl_scan(int v, int* warp_tot, int* total) {
     return base + x - v;
 }
 
+// Order-preserving unsigned key of a finite float (larger value, larger
+// key); -0 and +0 map to the same key.
+__device__ __forceinline__ unsigned ordered_key(float v) {
+    const unsigned u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) {
     return a < b ? a : b;
+}
+
+// Running totals of the context (read by the host between calls): reductions
+// without a return value, so the pass does not wait on their loads.
+__device__ __forceinline__ void add_counters(unsigned long long* c, int u, int h, int m, int q, int nassign) {
+    atomicAdd(&c[CNT_CALLS], 1ull);
+    atomicAdd(&c[CNT_UNIQUE], (unsigned long long)u);
+    atomicAdd(&c[CNT_HITS], (unsigned long long)h);
+    atomicAdd(&c[CNT_MISSES], (unsigned long long)m);
+    atomicAdd(&c[CNT_FILLS], (unsigned long long)q);
+    atomicAdd(&c[CNT_CPU], (unsigned long long)(m - q));
+    atomicAdd(&c[CNT_ASSIGN], (unsigned long long)nassign);
 }
 
 // a4: q = min(clamp(q0, 1, m), S - h) with q0 = round(m * B_P / B_H) in fp64
@@ -299,15 +318,13 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
                         be = e;
                     }
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                    if (ov > bv || (ov == bv && oe < be)) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
+                // warp arg-max as two reductions: the largest value (as an
+                // order-preserving key, -0 folded into +0 so that equal values
+                // tie), then the lowest id among the lanes holding it
+                const unsigned key = ordered_key(bv);
+                const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
+                be = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (unsigned)be : 0xffffffffu);
+                bv = __shfl_sync(0xffffffffu, bv, be & 31);
                 if (be >= E) {
                     bad = true;
                     break;
@@ -507,14 +524,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
             I[INFO_NASSIGN] = nassign;
             I[INFO_CLOCK] = (int)clk;
             I[INFO_VALID] = 1;
-            unsigned long long* cn = p.counters;
-            cn[CNT_CALLS] += 1;
-            cn[CNT_UNIQUE] += sh.u;
-            cn[CNT_HITS] += sh.h;
-            cn[CNT_MISSES] += sh.m;
-            cn[CNT_FILLS] += q;
-            cn[CNT_CPU] += sh.m - q;
-            cn[CNT_ASSIGN] += nassign;
+            add_counters(p.counters, sh.u, sh.h, sh.m, q, nassign);
         }
         return;
     }
@@ -708,14 +718,7 @@ __global__ void __launch_bounds__(CTL_THREADS, 1) route_ctl_kernel(CtlParams p) 
         I[INFO_NASSIGN] = sh.nassign;
         I[INFO_CLOCK] = (int)clk;
         I[INFO_VALID] = 1;
-        unsigned long long* c = p.counters;
-        c[CNT_CALLS] += 1;
-        c[CNT_UNIQUE] += sh.u;
-        c[CNT_HITS] += sh.h;
-        c[CNT_MISSES] += sh.m;
-        c[CNT_FILLS] += q;
-        c[CNT_CPU] += sh.m - q;
-        c[CNT_ASSIGN] += sh.nassign;
+        add_counters(p.counters, sh.u, sh.h, sh.m, q, sh.nassign);
     }
 }
 
