@@ -11,11 +11,12 @@
 //     lists MXFP4 among the bank layouts.
 // Weight w = e2m1 * scale(block along K) * global(expert).  Activations are
 // not quantised to FP4 (W4A16); the arithmetic is packed f16:
-//   * e2m1 codes are decoded two at a time into f16 pairs equal to
-//     value * 2^-14 (bit placement, exact);
+//   * e2m1 codes are decoded two at a time, adjacent values, into f16 pairs
+//     by the hardware pair conversion (exact);
 //   * activation rows (x for phase A, h for phase B) are held as f16 pairs in
 //     the same order, each token row multiplied by a power of two chosen from
-//     its largest magnitude (exact for x; one f16 rounding for h);
+//     its largest magnitude (exact for x; one f16 rounding for h), so that a
+//     product is below 6 * 2^10 and eight of them below 2^16;
 //   * each 16-value block is summed with packed f16 FMAs (two chains of four
 //     products per half), widened to fp32, multiplied by its block scale and
 //     added in fp32; the row total is rescaled once by the token's power of
@@ -52,7 +53,7 @@ constexpr size_t HEAD = 256;
 // fit) or in a global scratch row block written at the start of the launch
 // (X_GLOBAL).
 enum { X_SMEM = 0, X_GLOBAL = 1 };
-constexpr int kXTarget = 14;  // token rows are scaled so their largest magnitude is in [2^14, 2^15)
+constexpr int kXTarget = 9;  // token rows are scaled so their largest magnitude is in [2^9, 2^10)
 
 // Scale bytes: two e4m3 codes (low byte first) to a float pair, by the
 // hardware conversion (one per 16 values).
@@ -90,16 +91,15 @@ __device__ __forceinline__ int swz_f32(int e) {  // element e of a row -> its st
 
 // Phase-A activations as f16 pairs, in the order the weight decode produces:
 // for word q of a row (values 8q..8q+7) one 16-byte chunk holds the pairs
-// (x[8q+J], x[8q+J+4]), J = 0..3.  The four chunks of the 32-value group v
+// (x[8q+2J], x[8q+2J+1]), J = 0..3.  The four chunks of the 32-value group v
 // are stored rotated by v/2 (chunk c at (c + v/2) mod 4), so that the eight
 // lanes of a quarter warp (groups v = lane + 32i) read eight different bank
 // quads.  Token row t is held multiplied by 2^a_t, with a_t chosen from the
 // row's largest magnitude (kXTarget): every scaled value is an exact f16
-// (a bf16 value below 2^15), the products with the decoded weights
-// (value * 2^-14) are at most 6 and a 16-value partial sum at most 96, and
-// values down to 2^-28 of the row's largest stay normal f16.  Returns the
-// row's factor 2^(14 - a_t) that turns its sums (in units of 2^(a_t - 14))
-// back into dot products.
+// (a bf16 value below 2^10), a product with an e2m1 value (at most 6) is
+// below 6 * 2^10, the eight products one f16 half of a 16-value block sums
+// stay below 2^16, and values down to 2^-23 of the row's largest stay normal
+// f16.  The row's factor 2^-a_t turns its sums back into dot products.
 __device__ __forceinline__ int xpos(int q) {  // word q of a row -> its stored chunk
     const int v = q >> 2;
     return (v << 2) | (((q & 3) + (v >> 1)) & 3);
@@ -116,7 +116,7 @@ __device__ __forceinline__ int x_exponent(float amax) {
 }
 
 // Eight bf16 values (one word's activations) times `up` as the chunk of
-// four f16 pairs (x[J], x[J+4]).
+// four f16 pairs (x[2J], x[2J+1]).
 __device__ __forceinline__ uint4 x_pairs(const uint4& raw, float up) {
     float f[8];
     ft::bf16x8_to_f32(raw, f);
@@ -124,14 +124,14 @@ __device__ __forceinline__ uint4 x_pairs(const uint4& raw, float up) {
     uint32_t* cw = reinterpret_cast<uint32_t*>(&c);
 #pragma unroll
     for (int J = 0; J < 4; ++J) {
-        const __half2 h = __floats2half2_rn(f[J] * up, f[J + 4] * up);
+        const __half2 h = __floats2half2_rn(f[2 * J] * up, f[2 * J + 1] * up);
         cw[J] = *reinterpret_cast<const uint32_t*>(&h);
     }
     return c;
 }
 
 // One warp converts token row `xr` (H bf16 values) into the paired layout
-// at `dst` (H/8 chunks); returns the row factor 2^(14 - a_t) (all lanes).
+// at `dst` (H/8 chunks); returns the row factor 2^-a_t (all lanes).
 __device__ __forceinline__ float stage_x_row(const uint4* xr, int H, uint4* dst, int lane) {
     float amax = 0.f;
     for (int q = lane; q < H / 8; q += 32) {
@@ -145,21 +145,22 @@ __device__ __forceinline__ float stage_x_row(const uint4* xr, int H, uint4* dst,
     const int a = x_exponent(amax);
     const float up = ldexpf(1.f, a);
     for (int q = lane; q < H / 8; q += 32) dst[xpos(q)] = x_pairs(xr[q], up);
-    return ldexpf(1.f, 14 - a);
+    return ldexpf(1.f, -a);
 }
 
-// e2m1 decode by bit placement, two values at a time: codes J and J + 4 of
-// word w (nibble J, low nibble first) become the two halves of an f16x2
-// whose exponent field holds the code's two exponent bits, whose top
-// mantissa bit holds its mantissa bit and whose sign is its sign.  Each half
-// equals value * 2^-14 exactly (the subnormal code 1, 0.5, included); both
-// nibbles of a pair move by the same shift, so a pair costs two shifts and
-// two masks.  The four pairs of one word, in J order:
+// e2m1 decode, two adjacent values at a time: byte J of word w (values 2J
+// in the low nibble, 2J+1 in the high nibble) becomes an f16 pair (low half
+// = low nibble) by the hardware conversion, exact for every code.  The four
+// pairs of one word, in J order:
 __device__ __forceinline__ void e2m1_word_h2(uint32_t w, uint32_t* d) {
-    d[0] = ((w << 9) & 0x0E000E00u) | ((w << 12) & 0x80008000u);
-    d[1] = ((w << 5) & 0x0E000E00u) | ((w << 8) & 0x80008000u);
-    d[2] = ((w << 1) & 0x0E000E00u) | ((w << 4) & 0x80008000u);
-    d[3] = ((w >> 3) & 0x0E000E00u) | (w & 0x80008000u);
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(w));
 }
 
 __device__ __forceinline__ __half2 hfma2_u(uint32_t a, uint32_t b, __half2 c) {
@@ -183,7 +184,7 @@ __device__ __forceinline__ float dot16_h(const uint32_t* d, const uint4& x0, con
 }
 
 // Phase A: gate and up rows of one feature against NT tokens; returns the
-// row sums, in units of each token row's 2^(a_t - 14) and without the
+// row sums, in units of each token row's 2^a_t and without the
 // expert's global, in ag / au.  `xs` is the paired activation block (H/8
 // chunks per token row).
 template <int NT, int XM, int SB>
@@ -334,16 +335,16 @@ __device__ __noinline__ void down_rows4(const uint8_t* wrows, const uint8_t* sro
 }
 
 // Eight fp32 values (h elements 8q..8q+7 of a staged row, swizzled as
-// swz_f32) times `up` as the chunk of four f16 pairs (h[J], h[J+4]).
+// swz_f32) times `up` as the chunk of four f16 pairs (h[2J], h[2J+1]).
 __device__ __forceinline__ uint4 h_pairs(const float* hr, int q, float up) {
     const float4 lo = *reinterpret_cast<const float4*>(hr + swz_f32(8 * q));
     const float4 hi = *reinterpret_cast<const float4*>(hr + swz_f32(8 * q + 4));
     uint4 c;
     __half2 t;
-    t = __floats2half2_rn(lo.x * up, hi.x * up); c.x = *reinterpret_cast<const uint32_t*>(&t);
-    t = __floats2half2_rn(lo.y * up, hi.y * up); c.y = *reinterpret_cast<const uint32_t*>(&t);
-    t = __floats2half2_rn(lo.z * up, hi.z * up); c.z = *reinterpret_cast<const uint32_t*>(&t);
-    t = __floats2half2_rn(lo.w * up, hi.w * up); c.w = *reinterpret_cast<const uint32_t*>(&t);
+    t = __floats2half2_rn(lo.x * up, lo.y * up); c.x = *reinterpret_cast<const uint32_t*>(&t);
+    t = __floats2half2_rn(lo.z * up, lo.w * up); c.y = *reinterpret_cast<const uint32_t*>(&t);
+    t = __floats2half2_rn(hi.x * up, hi.y * up); c.z = *reinterpret_cast<const uint32_t*>(&t);
+    t = __floats2half2_rn(hi.z * up, hi.w * up); c.w = *reinterpret_cast<const uint32_t*>(&t);
     return c;
 }
 
@@ -389,10 +390,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     int* m_pos = reinterpret_cast<int*>(m_gate + TK);
     float* m_gs = reinterpret_cast<float*>(m_pos + TK);   // global scale of each entry
     int* m_fill = reinterpret_cast<int*>(m_gs + TK);      // fill index of each entry (or -1)
-    float* xf = reinterpret_cast<float*>(m_fill + TK);    // row factor 2^(14 - a_t) of each token
+    float* xf = reinterpret_cast<float*>(m_fill + TK);    // row factor 2^-a_t of each token
     unsigned* hmx = reinterpret_cast<unsigned*>(xf + T);  // largest |h| of each token (this CTA, then all)
     float* hup = reinterpret_cast<float*>(hmx + T);       // h scale 2^b_t of each token
-    float* hfr = hup + T;                                 // h row factor 2^(14 - b_t) of each staged row
+    float* hfr = hup + T;                                 // h row factor 2^-b_t of each staged row
     o += ((size_t)(7 * TK + 1 + 3 * T + 2 * TG) * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
     const unsigned wpart = ((unsigned)RMAX * (dvrow + dsrow) + 127u) & ~127u;
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             x_s[(size_t)t * qrow + xpos(q)] = x_pairs(xin[i], ldexpf(1.f, a));
         }
         __syncthreads();
-        for (int t = tid; t < T; t += THREADS) xf[t] = ldexpf(1.f, 14 - x_exponent(__uint_as_float(amax_bits[t])));
+        for (int t = tid; t < T; t += THREADS) xf[t] = ldexpf(1.f, -x_exponent(__uint_as_float(amax_bits[t])));
         __syncthreads();
     } else {
         for (int t = c + G * wid; t < T; t += G * (THREADS / 32)) {
@@ -607,7 +608,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         const unsigned long long v = reinterpret_cast<const unsigned long long*>(p.hmax)[t];
         const int b = x_exponent((v >> 32) == (gen >> 32) ? __uint_as_float((unsigned)v) : 0.f);
         hup[t] = ldexpf(1.f, b);
-        xf[t] = ldexpf(1.f, 14 - b);  // phase A is done with the x factors
+        xf[t] = ldexpf(1.f, -b);  // phase A is done with the x factors
     }
     ft::named_bar_sync(1, CONS);
 
