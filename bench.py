@@ -884,11 +884,12 @@ def run_quant_decode_bench(device, peaks, calls_t1: int = 48, calls_t64: int = 1
             gbs = hbm / (us * 1e-6) / 1e9
             kname = {synth.FMT_NVFP4: "expert_ffn_fp4", synth.FMT_MXFP4: "expert_ffn_mxfp4",
                      synth.FMT_FP8: "expert_ffn_fp8"}[fmt]
-            res[f"t{T}"] = [round(us, 1), round(gbs / peaks["hbm_gbs"], 4)]
+            tr = traffic_from_profiles(kname, hbm)
+            res[f"t{T}"] = [round(us, 1), round(gbs / peaks["hbm_gbs"], 4), round(tr / hbm, 3) if tr else None]
             det[f"t{T}"] = {"us_per_launch": round(us, 2), "hits_per_launch": round(d["hits"] / max(1, d["calls"]), 2),
                             "hbm_bytes_per_launch": int(hbm), "achieved_GBps": round(gbs, 1),
                             "frac": round(gbs / peaks["hbm_gbs"], 4),
-                            "traffic": traffic_from_profiles(kname, hbm)}
+                            "traffic": tr}
         # one fill beside 7 hits: the fill streams inside the expert launch
         us1, fill_us = one_fill_times(ctx, E, x, pc, y, flush, cs)
         res["fill1"] = [round(us1, 1), round(fill_us, 1) if fill_us else None]
@@ -899,7 +900,8 @@ def run_quant_decode_bench(device, peaks, calls_t1: int = 48, calls_t64: int = 1
         del pool
         leg[name] = res
         detail[name] = det
-    leg["cols"] = "t1, t64: [us per launch, frac of HBM]; fill1: [us per launch with 1 fill + 7 hits, standalone fill us]"
+    leg["cols"] = ("t1, t64: [us per launch, frac of HBM, DRAM traffic / algorithmic bytes]; "
+                   "fill1: [us per launch with 1 fill + 7 hits, standalone fill us]")
     return leg, detail
 
 
