@@ -22,14 +22,16 @@
 //     and the 8 matching up rows (contiguous in the record thanks to the
 //     16-row gate/up interleave); consumer warp w computes feature w of the
 //     slot (both dot products, SiLU, product) and writes h in fp32;
-//   * the fill copy warp copies this CTA's share of every fill record (its
-//     own W_d rows, then its gate/up units) host pool -> small shared ring ->
-//     victim slot, and the fill math warp computes the SwiGLU features of the
-//     units straight from the ring, so a fill is never read back from HBM;
+//   * the fill copy warp copies fill items drawn from a counter of the launch
+//     (each record's W_d pieces, then its gate/up units) host pool -> small
+//     shared ring -> victim slot, and the fill math warp computes the SwiGLU
+//     features of the units straight from the ring, so a fill's gate/up rows
+//     are never read back from HBM;
 //   * phase B (down + merge): CTA c owns output rows [c*H/G, (c+1)*H/G) of
 //     every GPU expert, in stages of whole entries whose h rows the h warp
 //     adds once they are complete (resident entries: every CTA has counted
-//     its phase-A items; fills: the math warps have counted every feature);
+//     its phase-A items; fills: the math warps have counted every feature,
+//     and every CTA's W_d pieces of the fill are in its slot);
 //     then it sums the gated expert outputs over j ascending and adds
 //     partial_C, so the order of the sum is fixed and no atomics are needed.
 #include "ft_common.cuh"
