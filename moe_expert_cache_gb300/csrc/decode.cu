@@ -443,6 +443,9 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
         // counter (values from G on) right after the current item's first
         // chunk is issued, and read when that item is exhausted.
         unsigned* claims = p.gbar + 2;
+        // the first fill's record, loaded beside the fill count rather than
+        // after it (launches that perform fills have the array; unused when q = 0)
+        const int fid0 = p.do_fill ? p.fill_fid[0] : 0;
         int ahead = 0;  // lane 0: the draw in flight
         int nxt = c;    // the next item to start, once `known`
         bool known = true;
@@ -475,7 +478,8 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) expert_ffn_kernel(ExpertPar
             unsigned n;
             locate(cur, seg, off, n);
             unsigned char* d = fring + (size_t)s * fch;
-            const uint8_t* src = host + (unsigned long long)p.fill_fid[cur / ipf] * p.rb + off;
+            const int fr = cur / ipf;
+            const uint8_t* src = host + (unsigned long long)(fr == 0 ? fid0 : p.fill_fid[fr]) * p.rb + off;
             for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + v, src + v);
             if (cur % ipf >= NWD)
                 for (unsigned v = lane * 16u; v < n; v += 512u) ft::cp_async16(d + n + v, src + upoff + v);
