@@ -19,24 +19,33 @@
 //     product is below 6 * 2^10 and eight of them below 2^16;
 //   * each 16-value block is summed with packed f16 FMAs (two chains of four
 //     products per half), widened to fp32, multiplied by its block scale and
-//     added in fp32; the row total is rescaled once by the token's power of
-//     two and the expert's global.
-// The per-token maximum of h is formed in phase A (shared-memory maxima,
-// then one 64-bit atomic max per CTA and token, tagged with the grid
-// barrier's generation so that values from earlier launches lose).
+//     added in fp32; the row total is rescaled once by the row's power of two
+//     and the expert's global.
+// x rows are scaled per token; h per 16-value block, when phase B converts
+// the staged rows, so no maximum is shared between CTAs (the block's factor
+// multiplies its sum together with the weight block's scale).
 //
 // Record (per layer-expert): [W_gu values 2F x H/2 bytes, low nibble first,
 // gate/up rows interleaved in groups of 16][W_d values H x F/2]
 // [W_gu scales 2F x H/SB][W_d scales H x F/SB].
 //
 // Layout of the work: 16 consumer warps, one producer warp (TMA ring) and one
-// fill warp.  A phase-A item is 16 features (16 gate rows, the 16 up rows and
-// their scale rows, one warp per feature); a phase-B item is (expert, group
-// of at most TG tokens): the CTA's W_d rows, the staged fp32 h rows and, in
-// the slot's tail, those rows converted to f16 pairs, two W_d rows per warp
-// pass.  x is converted into shared memory when T*H*2 bytes fit, else into a
-// global block behind a grid barrier.  A grid barrier separates phase A from
-// phase B.
+// fill warp (one thread) per CTA, one CTA per SM.  A phase-A item is 16 features (16 gate
+// rows, the 16 up rows and their scale rows, one warp per feature); CTA c
+// takes the items c, c + G, ... of the resident entries.  A phase-B item is
+// (entry, group of at most TG tokens): the CTA's W_d rows [r0, r1), the
+// staged fp32 h rows and, in the slot's tail, those rows converted to f16
+// pairs, two W_d rows per warp pass.  The CTA takes the resident entries'
+// phase-A and phase-B items, then each fill's phase-A and phase-B items; when
+// a group's phase-A items are done the CTA counts itself in the group's
+// counter, and a phase-B item's h rows are copied once all G CTAs have.
+// Fills the control pass left pending are copied by this launch: the fill
+// thread of every CTA copies its equal part of each fill record in turn (one
+// byte range, host pool -> shared ring -> victim slot by bulk copies) and
+// counts itself in ready[r]; a fill's items wait for the whole record (and,
+// in phase B, for every CTA's count of the fill's group), so the resident
+// entries' two phases run while the fills stream.  x is converted into shared memory when T*H*2
+// bytes fit, else into a global block behind a grid barrier at the start.
 #include "ft_common.cuh"
 #include "../../include/ft.h"
 
@@ -114,6 +123,9 @@ __device__ __forceinline__ int x_exponent(float amax) {
     const int a = kXTarget - ((int)((__float_as_uint(amax) >> 23) & 255u) - 127);
     return a < -100 ? -100 : (a > 100 ? 100 : a);
 }
+
+// 2^b for an exponent from x_exponent (|b| <= 100: a normal float).
+__device__ __forceinline__ float pow2i(int b) { return __int_as_float((b + 127) << 23); }
 
 // Eight bf16 values (one word's activations) times `up` as the chunk of
 // four f16 pairs (x[2J], x[2J+1]).
@@ -222,7 +234,7 @@ __device__ __forceinline__ void gu_dots4(const uint4* gv, const uint4* uv, const
 template <int NT, int XM, int SB>
 __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                           const uint4* xs, const float* xf, int H, const int* m_tok, int off, int g0,
-                                          int F, int f, int lane, float gsc, float* hbuf, unsigned* hmx) {
+                                          int F, int f, int lane, float gsc, float* hbuf) {
     int tk[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) tk[n] = m_tok[off + g0 + n];
@@ -236,27 +248,22 @@ __device__ __forceinline__ void gu_group4(const uint4* gv, const uint4* uv, cons
         const float su = ft::warp_sum(au[n]) * rs;
         if (lane == n) mine = ft::silu_mul(sg, su);
     }
-    // read only by phase B, as staged rows: swizzled for its fp32 loads; the
-    // token's largest |h| of this CTA is kept for phase B's scaling
-    if (lane < NT) {
-        hbuf[(size_t)(off + g0 + lane) * F + swz_f32(f)] = mine;
-        atomicMax(&hmx[tk[lane]], __float_as_uint(fabsf(mine)));
-    }
+    // read only by phase B, as staged rows: swizzled for its fp32 loads
+    if (lane < NT) hbuf[(size_t)(off + g0 + lane) * F + swz_f32(f)] = mine;
 }
 
 template <int XM, int SB>
-__device__ __noinline__ void gu_feature4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
+__device__ __forceinline__ void gu_feature4(const uint4* gv, const uint4* uv, const uint8_t* gs, const uint8_t* us,
                                             const uint4* xs, const float* xf, int H, const int* m_tok, int off,
-                                            int ntok, int F, int f, int lane, float gsc, float* hbuf,
-                                            unsigned* hmx) {
+                                            int ntok, int F, int f, int lane, float gsc, float* hbuf) {
     int g0 = 0;
     while (g0 < ntok) {
         const int rem = ntok - g0;
         if (rem >= 2) {
-            gu_group4<2, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf, hmx);
+            gu_group4<2, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 2;
         } else {
-            gu_group4<1, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf, hmx);
+            gu_group4<1, XM, SB>(gv, uv, gs, us, xs, xf, H, m_tok, off, g0, F, f, lane, gsc, hbuf);
             g0 += 1;
         }
     }
@@ -264,11 +271,12 @@ __device__ __noinline__ void gu_feature4(const uint4* gv, const uint4* uv, const
 
 // Phase B: the W_d rows rb + CW*r (r < RW, row < R) of a slot (values +
 // scales) against NT h rows held as scaled f16 pairs (the layout of the
-// phase-A activations, F/8 chunks per row; row factors hf).  Each h chunk is
-// loaded once and applied to every row of the warp.
+// phase-A activations, F/8 chunks per row), each 16-value block of a row
+// with its factor in hfb (F/16 per row).  Each h chunk is loaded once and
+// applied to every row of the warp.
 template <int NT, int SB>
 __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
-                                            unsigned dsrow, const uint4* hp, const float* hfr, int g, int F,
+                                            unsigned dsrow, const uint4* hp, const float* hfb, int g, int F,
                                             int lane, float gsc, float* o_s, int obase, int RMAX, int rb, int R) {
     float acc[RW][NT];
 #pragma unroll
@@ -297,10 +305,11 @@ __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t*
             uint4 hc[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) hc[c] = hr[(c + rot) & 3];
+            const float2 hb = *reinterpret_cast<const float2*>(hfb + (size_t)(g + n) * (F / 16) + 2 * v);
 #pragma unroll
             for (int r = 0; r < RW; ++r)
-                acc[r][n] = fmaf(sc[r].x, dot16_h(d[r], hc[0], hc[1]),
-                                 fmaf(sc[r].y, dot16_h(d[r] + 8, hc[2], hc[3]), acc[r][n]));
+                acc[r][n] = fmaf(sc[r].x * hb.x, dot16_h(d[r], hc[0], hc[1]),
+                                 fmaf(sc[r].y * hb.y, dot16_h(d[r] + 8, hc[2], hc[3]), acc[r][n]));
         }
     }
 #pragma unroll
@@ -309,7 +318,7 @@ __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t*
         if (rl < R) {  // warp-uniform
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                const float sv = ft::warp_sum(acc[r][n]) * hfr[g + n] * gsc;
+                const float sv = ft::warp_sum(acc[r][n]) * gsc;
                 if (lane == 0) o_s[(size_t)(obase + g + n) * RMAX + rl] = sv;
             }
         }
@@ -319,26 +328,35 @@ __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t*
 // The rows rb + CW*r (r < RW) of a slot against its ng h rows, two tokens
 // at a time.
 template <int SB>
-__device__ __noinline__ void down_rows4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
-                                        unsigned dsrow, const uint4* hp, const float* hfr, int ng, int F, int lane,
+__device__ __forceinline__ void down_rows4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
+                                        unsigned dsrow, const uint4* hp, const float* hfb, int ng, int F, int lane,
                                         float gsc, float* o_s, int obase, int RMAX, int rb, int R) {
     int g = 0;
     while (g < ng) {
         if (ng - g >= 2) {
-            down_group4<2, SB>(wrows, srows, dvrow, dsrow, hp, hfr, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
+            down_group4<2, SB>(wrows, srows, dvrow, dsrow, hp, hfb, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
             g += 2;
         } else {
-            down_group4<1, SB>(wrows, srows, dvrow, dsrow, hp, hfr, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
+            down_group4<1, SB>(wrows, srows, dvrow, dsrow, hp, hfb, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
             g += 1;
         }
     }
 }
 
 // Eight fp32 values (h elements 8q..8q+7 of a staged row, swizzled as
-// swz_f32) times `up` as the chunk of four f16 pairs (h[2J], h[2J+1]).
-__device__ __forceinline__ uint4 h_pairs(const float* hr, int q, float up) {
+// swz_f32) as the chunk of four f16 pairs (h[2J], h[2J+1]), scaled by the
+// power of two that puts the largest magnitude of their 16-value block (this
+// chunk and the one of lane ^ 1, which converts chunk q ^ 1 in the same
+// step) in [2^9, 2^10); returns the block's factor 2^-b in *fb.
+__device__ __forceinline__ uint4 h_pairs_block(const float* hr, int q, float* fb) {
     const float4 lo = *reinterpret_cast<const float4*>(hr + swz_f32(8 * q));
     const float4 hi = *reinterpret_cast<const float4*>(hr + swz_f32(8 * q + 4));
+    float m = fmaxf(fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(lo.z), fabsf(lo.w))),
+                    fmaxf(fmaxf(fabsf(hi.x), fabsf(hi.y)), fmaxf(fabsf(hi.z), fabsf(hi.w))));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    const int b = x_exponent(m);
+    const float up = pow2i(b);
+    *fb = pow2i(-b);
     uint4 c;
     __half2 t;
     t = __floats2half2_rn(lo.x * up, lo.y * up); c.x = *reinterpret_cast<const uint32_t*>(&t);
@@ -352,19 +370,79 @@ __device__ __forceinline__ uint4 h_pairs(const float* hr, int q, float up) {
 
 namespace {
 
+// The steps of CTA c, in the order its producer issues them and its
+// consumers take them: the phase-A items of the resident entries (a = c,
+// c + G, ...), a seal, their phase-B items (entry, group of <= TG tokens),
+// then for each fill in turn its phase-A items, a seal and its phase-B items.
+// At a seal the consumers count the CTA in the group's counter (every CTA's
+// h of the group is written once it holds G); a seal takes no ring slot.  A
+// phase-B item waits for its group's count, each group's phase-A items come
+// before its seal on every CTA, and the groups are taken in the same order
+// everywhere: no wait can close a cycle.
+enum { STEP_A = 0, STEP_SEAL = 1, STEP_B = 2 };
+struct Steps {
+    int c, G, cpe, nA, nfill, R, TG;
+    const int* m_off;
+    int grp, eb, ee, a, e, g0;
+    bool inB;
+    __device__ void open(int g) {  // group 0: the resident entries; group 1 + r: fill r
+        grp = g;
+        eb = g == 0 ? 0 : nA + g - 1;
+        ee = g == 0 ? nA : eb + 1;
+        int m = (int)(((long long)c - (long long)eb * cpe) % G);
+        if (m < 0) m += G;
+        a = eb * cpe + m;
+        inB = false;
+    }
+    // The next step (false past the last): its kind, its entry (for a seal:
+    // the group), and the phase-A item index or the first token of the
+    // phase-B group.
+    __device__ bool next(int& kind, int& ent, int& item, int& g) {
+        for (;;) {
+            if (grp > nfill) return false;
+            if (!inB) {
+                if (a < ee * cpe) {
+                    kind = STEP_A;
+                    ent = a / cpe;
+                    item = a;
+                    a += G;
+                    return true;
+                }
+                inB = true;
+                e = eb;
+                g0 = 0;
+                kind = STEP_SEAL;
+                ent = grp;
+                return true;
+            }
+            if (R > 0 && e < ee) {
+                kind = STEP_B;
+                ent = e;
+                g = g0;
+                g0 += TG;
+                if (g0 >= m_off[e + 1] - m_off[e]) {
+                    g0 = 0;
+                    ++e;
+                }
+                return true;
+            }
+            open(grp + 1);
+        }
+    }
+};
+
 template <int XM, int SB>
 __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_gdone;
-    __shared__ unsigned s_gen;  // grid barrier generation at the start of phase A
     const int H = p.H, F = p.F, T = p.T, k = p.k, TG = p.tgroup;
     const int nst = p.nstage;
     const unsigned slot_bytes = p.stage_bytes;
     const int ugpu = p.info[INFO_UGPU];
     const int nasg = p.info[INFO_NASSIGN];
+    const int q = p.do_fill ? p.info[INFO_Q] : 0;  // fills performed by this launch: the last q entries
+    const int nA = ugpu - q;                        // entries resident before the launch
     const int G = gridDim.x, c = blockIdx.x;
     const int cpe = F / FPC;
-    const int NA = ugpu * cpe;
     const int r0 = (int)((long long)H * c / G), r1 = (int)((long long)H * (c + 1) / G);
     const int R = r1 - r0;
     const int RMAX = (H + G - 1) / G;
@@ -389,12 +467,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     float* m_gate = reinterpret_cast<float*>(m_tok + TK);
     int* m_pos = reinterpret_cast<int*>(m_gate + TK);
     float* m_gs = reinterpret_cast<float*>(m_pos + TK);   // global scale of each entry
-    int* m_fill = reinterpret_cast<int*>(m_gs + TK);      // fill index of each entry (or -1)
-    float* xf = reinterpret_cast<float*>(m_fill + TK);    // row factor 2^-a_t of each token
-    unsigned* hmx = reinterpret_cast<unsigned*>(xf + T);  // largest |h| of each token (this CTA, then all)
-    float* hup = reinterpret_cast<float*>(hmx + T);       // h scale 2^b_t of each token
-    float* hfr = hup + T;                                 // h row factor 2^-b_t of each staged row
-    o += ((size_t)(7 * TK + 1 + 3 * T + 2 * TG) * 4 + 127) & ~(size_t)127;
+    float* xf = m_gs + TK;                                // row factor 2^-a_t of each token
+    o += ((size_t)(6 * TK + 1 + T) * 4 + 127) & ~(size_t)127;
     unsigned char* ring = smem + o;
     const unsigned wpart = ((unsigned)RMAX * (dvrow + dsrow) + 127u) & ~127u;
     const uint4* xsrc = XM == X_GLOBAL ? p.x16 : x_s;
@@ -405,20 +479,17 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             ft::mbar_init(&empty[s], CW);
         }
         ft::mbar_fence_init();
-        s_gdone = 0;
     }
     for (int i = tid; i <= ugpu; i += THREADS) m_off[i] = p.wl_off[i];
     for (int i = tid; i < ugpu; i += THREADS) {
         m_slot[i] = p.wl_slot[i];
         m_gs[i] = p.gscale[p.wl_fid[i]];
-        m_fill[i] = p.do_fill ? p.wl_fill[i] : -1;
     }
     for (int i = tid; i < nasg; i += THREADS) {
         m_tok[i] = p.as_tok[i];
         m_gate[i] = p.as_gate[i];
     }
     for (int i = tid; i < TK; i += THREADS) m_pos[i] = p.out_pos[i];
-    for (int i = tid; i < T; i += THREADS) hmx[i] = 0u;
     // paired, scaled activations: in shared memory by every CTA, or one
     // token row per warp across the grid into the global block, then a grid
     // barrier
@@ -440,9 +511,9 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         }
         __syncthreads();
         for (int i = tid; i < T * qrow; i += THREADS) {
-            const int t = i / qrow, q = i - t * qrow;
+            const int t = i / qrow, q8 = i - t * qrow;
             const int a = x_exponent(__uint_as_float(amax_bits[t]));
-            x_s[(size_t)t * qrow + xpos(q)] = x_pairs(xin[i], ldexpf(1.f, a));
+            x_s[(size_t)t * qrow + xpos(q8)] = x_pairs(xin[i], ldexpf(1.f, a));
         }
         __syncthreads();
         for (int t = tid; t < T; t += THREADS) xf[t] = ldexpf(1.f, -x_exponent(__uint_as_float(amax_bits[t])));
@@ -459,16 +530,39 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         __syncthreads();
     }
 
-    if (tid == 0) s_gen = ft::ld_acquire_gpu(&p.gbar[1]);  // no grid barrier can pass before phase A ends
-    __syncthreads();
+    // Group counters: CTAs whose phase-A items of the group are done (the
+    // resident entries in gbar[3], fill r in wdc[r]).  Exit count: the
+    // consumers and the producer of every CTA count out once they are done
+    // with the group counters; whoever completes the count returns them to
+    // zero for the next launch.  (ready[r], the CTAs that have copied their
+    // part of fill r, is zeroed by the control pass that schedules the fill.)
+    auto group_count = [&](int grp) { return grp == 0 ? p.gbar + 3 : p.wdc + grp - 1; };
+    auto count_out = [&]() {
+        unsigned n;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.gbar + 2) : "memory");
+        if (n == 2u * (unsigned)G - 1u) {
+            for (int r = 0; r < q; ++r) p.wdc[r] = 0u;
+            p.gbar[3] = 0u;
+            p.gbar[2] = 0u;
+        }
+    };
+    Steps sq;
+    sq.c = c;
+    sq.G = G;
+    sq.cpe = cpe;
+    sq.nA = nA;
+    sq.nfill = q;
+    sq.R = R;
+    sq.TG = TG;
+    sq.m_off = m_off;
+    sq.open(0);
 
     // --------------------------------------------------------- fused fill
     if (wid > CW) {
-        if (lane == 0 && p.do_fill)
+        if (lane == 0 && q > 0)
             ft::fill_share_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
-                               p.info[INFO_Q], p.fill_slot, p.fill_fid, p.ready, c, G,
-                               ring + (size_t)nst * slot_bytes, reinterpret_cast<uint64_t*>(smem + 128),
-                               p.fill_chunk, p.fill_slots, p.err);
+                               q, p.fill_slot, p.fill_fid, p.ready, c, G, ring + (size_t)nst * slot_bytes,
+                               reinterpret_cast<uint64_t*>(smem + 128), p.fill_chunk, p.fill_slots, p.err);
         return;
     }
     // ------------------------------------------------------------ producer
@@ -479,172 +573,130 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             // go to L2 once the ring is primed, so phase B reads them from L2
             auto prefetch_wd = [&]() {
                 if (R == 0) return;
-                for (int e = 0; e < ugpu; ++e) {
-                    if (m_fill[e] >= 0) continue;
+                for (int e = 0; e < nA; ++e) {
                     const uint8_t* rec = p.slot_pool + (size_t)m_slot[e] * p.rb;
                     ft::bulk_prefetch_l2(rec + VGU + (size_t)r0 * dvrow, (unsigned)R * dvrow);
                     ft::bulk_prefetch_l2(rec + VGU + VD + SGU + (size_t)r0 * dsrow, (unsigned)R * dsrow);
                 }
             };
-            int it = 0;
+            int it = 0, counted = -1;  // the last group whose count this thread has seen complete
+            int filled = 0;            // fills this thread has seen complete in their slots (in order)
             bool ok = true;
-            int waited = -1;
-            for (int a = c; a < NA && ok; a += G, ++it) {
+            int kind, ent, item, g0;
+            while (ok && sq.next(kind, ent, item, g0)) {
+                if (kind == STEP_SEAL) continue;
                 const int st = it % nst;
                 if (it == nst) prefetch_wd();
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
-                const int ent = a / cpe;
-                if (m_fill[ent] >= 0 && m_fill[ent] != waited) {
-                    if (!ft::wait_filled(p.ready, m_fill[ent], (unsigned)G, p.err)) { ok = false; break; }
-                    waited = m_fill[ent];
-                }
-                const int f0 = (a - ent * cpe) * FPC;
                 const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
-                const int grow = (f0 >> 4) * 32 + (f0 & 15);  // first gate row; up rows 16 later
                 unsigned char* dst = ring + (size_t)st * slot_bytes;
-                ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * (vrow + srow));
-                ft::bulk_g2s_hint(dst, rec + (size_t)grow * vrow, FPC * vrow, &full[st], pol);
-                ft::bulk_g2s_hint(dst + FPC * vrow, rec + (size_t)(grow + 16) * vrow, FPC * vrow, &full[st], pol);
-                ft::bulk_g2s_hint(dst + 2 * FPC * vrow, rec + VGU + VD + (size_t)grow * srow, FPC * srow, &full[st], pol);
-                ft::bulk_g2s_hint(dst + 2 * FPC * vrow + FPC * srow, rec + VGU + VD + (size_t)(grow + 16) * srow,
-                                  FPC * srow, &full[st], pol);
-            }
-            if (it <= nst && ok) prefetch_wd();
-            // phase B items = (expert, group of <= TG tokens); W_d rows stream
-            // ahead of the grid barrier, h rows after it
-            int nitems = 0;
-            if (R > 0)
-                for (int e = 0; e < ugpu; ++e) nitems += (m_off[e + 1] - m_off[e] + TG - 1) / TG;
-            const int pre = nitems < nst ? nitems : nst;
-            const int itB = it;
-            bool gdone = false;
-            int e = 0, g0 = 0, idx = 0;
-            for (; idx < nitems && ok; ++idx, ++it) {
-                const int st = it % nst;
-                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
-                const int off = m_off[e], ntok = m_off[e + 1] - off;
-                const int ng = min(TG, ntok - g0);
-                const uint8_t* rec = p.slot_pool + (size_t)m_slot[e] * p.rb;
-                if (g0 == 0 && m_fill[e] >= 0 && !ft::wait_filled(p.ready, m_fill[e], (unsigned)G, p.err)) {
-                    ok = false;
-                    break;
+                // a fill's rows once every CTA has copied its part of the record
+                if (ent - nA + 1 > filled) {
+                    if (!ft::wait_count(p.ready + (ent - nA), (unsigned)G, p.err)) { ok = false; break; }
+                    filled = ent - nA + 1;
                 }
-                unsigned char* dst = ring + (size_t)st * slot_bytes;
+                if (kind == STEP_A) {
+                    const int grow = (item - ent * cpe) * 2 * FPC;  // first gate row; up rows 16 later
+                    ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * (vrow + srow));
+                    ft::bulk_g2s_hint(dst, rec + (size_t)grow * vrow, FPC * vrow, &full[st], pol);
+                    ft::bulk_g2s_hint(dst + FPC * vrow, rec + (size_t)(grow + 16) * vrow, FPC * vrow, &full[st], pol);
+                    ft::bulk_g2s_hint(dst + 2 * FPC * vrow, rec + VGU + VD + (size_t)grow * srow, FPC * srow,
+                                      &full[st], pol);
+                    ft::bulk_g2s_hint(dst + 2 * FPC * vrow + FPC * srow, rec + VGU + VD + (size_t)(grow + 16) * srow,
+                                      FPC * srow, &full[st], pol);
+                    ++it;
+                    continue;
+                }
+                // phase-B item: this CTA's W_d rows of the entry, then the h
+                // rows of the item once every CTA has sealed the entry's group
+                const int off = m_off[ent];
+                const int ng = min(TG, m_off[ent + 1] - off - g0);
                 const unsigned wb = (unsigned)R * dvrow, sb = (unsigned)R * dsrow, hb = (unsigned)ng * F * 4u;
                 ft::mbar_arrive_expect_tx(&full[st], wb + sb + hb);
                 ft::bulk_g2s_hint(dst, rec + VGU + (size_t)r0 * dvrow, wb, &full[st], pol);
-                ft::bulk_g2s_hint(dst + (size_t)RMAX * dvrow, rec + VGU + VD + SGU + (size_t)r0 * dsrow, sb, &full[st], pol);
-                if (idx >= pre - 1) {
-                    if (!gdone) {
-                        const uint64_t t0 = ft::globaltimer();
-                        while (!ft::ld_acquire_cta(&s_gdone)) {
-                            if (ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
-                                atomicOr(p.err, FT_DEVERR_TIMEOUT);
-                                ok = false;
-                                break;
-                            }
-                        }
-                        if (!ok) break;
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        gdone = true;
-                        // deferred h rows of the items prefetched before the barrier
-                        int e2 = 0, g2 = 0;
-                        for (int i2 = 0; i2 <= idx; ++i2) {
-                            const int off2 = m_off[e2], nt2 = m_off[e2 + 1] - off2;
-                            const int ng2 = min(TG, nt2 - g2);
-                            const int st2 = (itB + i2) % nst;
-                            ft::bulk_g2s(ring + (size_t)st2 * slot_bytes + wpart, p.hbuf + (size_t)(off2 + g2) * F,
-                                         (unsigned)ng2 * F * 4u, &full[st2]);
-                            g2 += TG;
-                            if (g2 >= nt2) { g2 = 0; ++e2; }
-                        }
-                    } else {
-                        ft::bulk_g2s(dst + wpart, p.hbuf + (size_t)(off + g0) * F, hb, &full[st]);
-                    }
+                ft::bulk_g2s_hint(dst + (size_t)RMAX * dvrow, rec + VGU + VD + SGU + (size_t)r0 * dsrow, sb,
+                                  &full[st], pol);
+                // (waited for once per group; after a timed-out wait the rows
+                // are still copied, whatever they hold, so that the item
+                // completes and the ring drains)
+                const int gq = ent < nA ? 0 : ent - nA + 1;
+                if (gq != counted) {
+                    ok = ft::wait_count(group_count(gq), (unsigned)G, p.err);
+                    counted = gq;
                 }
-                g0 += TG;
-                if (g0 >= ntok) { g0 = 0; ++e; }
+                ft::bulk_g2s(dst + wpart, p.hbuf + (size_t)(off + g0) * F, hb, &full[st]);
+                ++it;
             }
+            if (it <= nst && ok) prefetch_wd();
             ft::drain_ring(full, it, nst, p.err);
+            count_out();
         }
         return;
     }
 
-    // ------------------------------------------------- phase A: gate/up + SwiGLU
+    // ------------------------------------- consumers: phase-A and phase-B items
+    // After a failed (timed-out) wait a warp stops waiting, computing and
+    // releasing slots, but takes the same barriers and seals as the others.
     int it = 0;
     bool failed = false;
-    for (int a = c; a < NA; a += G, ++it) {
+    int kind, ent, item, g0;
+    while (sq.next(kind, ent, item, g0)) {
+        if (kind == STEP_SEAL) {
+            // every warp's h of the group's items on this CTA is written
+            ft::named_bar_sync(3, CONS);
+            if (tid == 0) ft::red_release_gpu_add(group_count(ent), 1u);
+            continue;
+        }
         const int st = it % nst;
-        const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
+        const bool ok = !failed && __all_sync(0xffffffffu, ft::mbar_wait(&full[st], (it / nst) & 1, p.err));
         failed = !ok;
-        const int ent = a / cpe;
-        const int f = (a - ent * cpe) * FPC + wid;
+        const unsigned char* sb = ring + (size_t)st * slot_bytes;
         const int off = m_off[ent];
         const int ntok = m_off[ent + 1] - off;
-        const unsigned char* sb = ring + (size_t)st * slot_bytes;
-        const uint4* gv = reinterpret_cast<const uint4*>(sb + (size_t)wid * vrow);
-        const uint4* uv = reinterpret_cast<const uint4*>(sb + (size_t)(FPC + wid) * vrow);
-        const uint8_t* gs = sb + 2 * FPC * vrow + (size_t)wid * srow;
-        const uint8_t* us = sb + 2 * FPC * vrow + FPC * srow + (size_t)wid * srow;
-        if (ok)
-            gu_feature4<XM, SB>(gv, uv, gs, us, xsrc, xf, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf, hmx);
-        __syncwarp();
-        if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
-    }
-
-    // per-token |h| maxima of the grid, tagged with the barrier generation of
-    // this launch in the high word (older values lose every comparison)
-    ft::named_bar_sync(1, CONS);
-    const unsigned long long gen = (unsigned long long)s_gen << 32;
-    for (int t = tid; t < T; t += CONS)
-        atomicMax(reinterpret_cast<unsigned long long*>(p.hmax) + t, gen | hmx[t]);
-    ft::named_bar_sync(1, CONS);
-    if (tid == 0) {
-        ft::grid_barrier(p.gbar, (unsigned)G, p.err);
-        ft::st_release_cta(&s_gdone, 1);
-    }
-    ft::named_bar_sync(1, CONS);
-    for (int t = tid; t < T; t += CONS) {
-        const unsigned long long v = reinterpret_cast<const unsigned long long*>(p.hmax)[t];
-        const int b = x_exponent((v >> 32) == (gen >> 32) ? __uint_as_float((unsigned)v) : 0.f);
-        hup[t] = ldexpf(1.f, b);
-        xf[t] = ldexpf(1.f, -b);  // phase A is done with the x factors
-    }
-    ft::named_bar_sync(1, CONS);
-
-    // ---------------------------------------------------- phase B: down rows
-    if (R > 0) {
-        for (int e = 0; e < ugpu; ++e) {
-            const int off = m_off[e], ntok = m_off[e + 1] - off;
-            for (int g0 = 0; g0 < ntok; g0 += TG, ++it) {
-                const int ng = min(TG, ntok - g0);
-                const int st = it % nst;
-                const bool ok = !failed && ft::mbar_wait(&full[st], (it / nst) & 1, p.err);
-                failed = !ok;
-                const unsigned char* sb = ring + (size_t)st * slot_bytes;
-                const float* hs = reinterpret_cast<const float*>(sb + wpart);
-                // the staged h rows as scaled f16 pairs, written by every
-                // consumer thread into the slot's tail (past the W_d rows and
-                // the fp32 rows the copy lands), then one barrier; warps whose
-                // wait failed still take the barrier.  Consecutive items use
-                // different slots, and a slot's tail is rewritten only after
-                // every warp has passed the barrier of the item before.
-                uint4* hp = reinterpret_cast<uint4*>(ring + (size_t)st * slot_bytes + wpart + (size_t)TG * F * 4);
-                if (ok) {
-                    for (int i = tid; i < ng * (F / 8); i += CONS) {
-                        const int n = i / (F / 8), q = i - n * (F / 8);
-                        hp[(size_t)n * (F / 8) + xpos(q)] = h_pairs(hs + (size_t)n * F, q, hup[m_tok[off + g0 + n]]);
-                    }
-                    if (tid < ng) hfr[(it & 1) * TG + tid] = xf[m_tok[off + g0 + tid]];
-                }
-                ft::named_bar_sync(2, CONS);
-                for (int rb = wid; rb < R && ok; rb += RW * CW)
-                    down_rows4<SB>(sb, sb + (size_t)RMAX * dvrow, dvrow, dsrow, hp, hfr + (it & 1) * TG, ng, F,
-                                   lane, m_gs[e], o_s, off + g0, RMAX, rb, R);
-                __syncwarp();
-                if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+        if (kind == STEP_A) {
+            // gate/up + SwiGLU: warp w computes feature w of the item
+            const int f = (item - ent * cpe) * FPC + wid;
+            const uint4* gv = reinterpret_cast<const uint4*>(sb + (size_t)wid * vrow);
+            const uint4* uv = reinterpret_cast<const uint4*>(sb + (size_t)(FPC + wid) * vrow);
+            const uint8_t* gs = sb + 2 * FPC * vrow + (size_t)wid * srow;
+            const uint8_t* us = sb + 2 * FPC * vrow + FPC * srow + (size_t)wid * srow;
+            if (ok) gu_feature4<XM, SB>(gv, uv, gs, us, xsrc, xf, H, m_tok, off, ntok, F, f, lane, m_gs[ent], p.hbuf);
+            __syncwarp();
+            if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+            ++it;
+            continue;
+        }
+        // down rows [r0, r1) of one token group of the entry.  The staged
+        // fp32 h rows are converted to f16 pairs, each 16-value block scaled
+        // by its own power of two, by every consumer thread into the slot's
+        // tail (past the W_d rows and the fp32 rows the copy lands): the
+        // pairs, then the block factors; then one barrier (warps whose wait
+        // failed still take it).  Consecutive items use different slots, and
+        // a slot's tail is rewritten only after every warp has released the
+        // slot.
+        const int ng = min(TG, ntok - g0);
+        const float* hs = reinterpret_cast<const float*>(sb + wpart);
+        unsigned char* tail = ring + (size_t)st * slot_bytes + wpart + (size_t)TG * F * 4;
+        uint4* hp = reinterpret_cast<uint4*>(tail);
+        float* hfb = reinterpret_cast<float*>(tail + (size_t)TG * F * 2);
+        if (ok) {
+            // the two chunks of a block are lanes 2m and 2m + 1 of one step
+            // (F/8 is a multiple of 32, so every lane of a warp takes the same
+            // number of steps)
+            for (int i = tid; i < ng * (F / 8); i += CONS) {
+                const int n = i / (F / 8), q8 = i - n * (F / 8);
+                float fb;
+                hp[(size_t)n * (F / 8) + xpos(q8)] = h_pairs_block(hs + (size_t)n * F, q8, &fb);
+                if ((q8 & 1) == 0) hfb[(size_t)n * (F / 16) + (q8 >> 1)] = fb;
             }
         }
+        ft::named_bar_sync(2, CONS);
+        for (int rb = wid; rb < R && ok; rb += RW * CW)
+            down_rows4<SB>(sb, sb + (size_t)RMAX * dvrow, dvrow, dsrow, hp, hfb, ng, F, lane, m_gs[ent], o_s,
+                           off + g0, RMAX, rb, R);
+        __syncwarp();
+        if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+        ++it;
     }
     ft::named_bar_sync(1, CONS);
     for (int idx = tid; idx < T * R; idx += CONS) {
@@ -658,6 +710,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         if (p.partial_C) acc += p.partial_C[oi];
         p.y[oi] = acc;
     }
+    if (tid == 0) count_out();  // after this CTA's last seal
 }
 
 }  // namespace
@@ -684,11 +737,12 @@ bool fp4_plan(int H, int F, int T, int k, int SB, int G, Fp4Plan& pl) {
     // the link's bandwidth-delay product delay every SM's HBM reads.
     pl.fch = 4096;
     // token group of phase B: the most h rows (at most 16) whose staging in a
-    // slot (fp32 as copied, then f16 pairs) leaves room for two slots
+    // slot (fp32 as copied, then f16 pairs and their block factors) leaves room
+    // for two slots
     int tg = T < 16 ? T : 16;
     for (; tg >= 1; --tg) {
-        pl.head = head0 + (((7 * TK + 1 + 3 * (size_t)T + 2 * (size_t)tg) * 4 + 127) & ~(size_t)127);
-        pl.slot = wpart + (size_t)tg * F * 6;
+        pl.head = head0 + (((6 * TK + 1 + (size_t)T) * 4 + 127) & ~(size_t)127);
+        pl.slot = wpart + (size_t)tg * F * 6 + (size_t)tg * (F / 16) * 4;
         if (pl.slot < chunk) pl.slot = chunk;
         pl.slot = (pl.slot + 127) & ~(size_t)127;
         if (pl.head + 2 * pl.fch + 2 * pl.slot <= kSmemLimit4) break;

@@ -44,7 +44,6 @@ struct ft_ctx {
     float* nvfp4_global;
     uint4* x16;      // FP4 decode: activations as scaled f16 pairs (T_max x H)
     float* xsc;      // FP4 decode: row factors (T_max)
-    unsigned long long* hmax;  // FP4 decode: tagged per-token |h| maxima (T_max)
     // fixed-size control outputs and worklists (one arena)
     void* arena;
     unsigned* clock;
@@ -141,7 +140,6 @@ void free_ctx(ft_ctx* c) {
     cudaFree(c->nvfp4_global);
     cudaFree(c->x16);
     cudaFree(c->xsc);
-    cudaFree(c->hmax);
     cudaFree(c->arena);
     cudaFree(c->hbuf);
     delete c;
@@ -308,8 +306,6 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     if (fmt == FT_FMT_NVFP4 || fmt == FT_FMT_MXFP4) {
         INIT_CUDA(cudaMalloc(&c->x16, (size_t)T_max * H * 2));
         INIT_CUDA(cudaMalloc(&c->xsc, (size_t)T_max * 4));
-        INIT_CUDA(cudaMalloc(&c->hmax, (size_t)T_max * 8));
-        INIT_CUDA(cudaMemset(c->hmax, 0, (size_t)T_max * 8));
     }
     if (T_prefill_max > 0) {
         st = prefill_alloc(c->pf, T_prefill_max, k, H, F, E, fmt);
@@ -373,7 +369,7 @@ ft_status ft_moe_forward(ft_ctx* c, const void* x, const float* partial_C, float
     p.x = (const __nv_bfloat16*)x; p.partial_C = partial_C; p.y = y;
     p.info = c->info; p.wl_slot = c->wl_slot; p.wl_off = c->wl_off; p.as_tok = c->as_tok;
     p.as_gate = c->as_gate; p.out_pos = c->pos; p.hbuf = c->hbuf; p.err = c->err; p.gbar = c->gbar;
-    p.wl_fid = c->wl_fid; p.gscale = c->nvfp4_global; p.x16 = c->x16; p.xsc = c->xsc; p.hmax = c->hmax;
+    p.wl_fid = c->wl_fid; p.gscale = c->nvfp4_global; p.x16 = c->x16; p.xsc = c->xsc;
     p.wait_ns = c->wait_ns;
     p.do_fill = c->fill_pending ? 1 : 0;
     p.host_pool = (const uint4*)c->host_pool_dev;

@@ -423,8 +423,9 @@ struct ExpertParams {
     const int* out_pos;
     float* hbuf;              // [T*k, F] fp32
     unsigned* err;
-    unsigned* gbar;           // [4] NVFP4: grid barrier (arrivals, generation); BF16: exit count, hits done,
-                              // fill items drawn; zero at rest
+    unsigned* gbar;           // [4] FP4: grid barrier of the x staging (arrivals, generation), exit count,
+                              // CTAs done with the resident entries' phase-A items (zero at rest);
+                              // BF16: exit count, hits done, fill items drawn; zero at rest
     const int* wl_fid;        // [E] flat id of each GPU entry (NVFP4 global lookup)
     // fused cache fill (performed by this launch when do_fill != 0)
     int do_fill;
@@ -432,9 +433,10 @@ struct ExpertParams {
     const int* fill_slot;     // [q] victim slot of fill i
     const int* fill_fid;      // [q] flat id of fill i
     const int* wl_fill;       // [E] fill index of entry i, or -1 for a hit
-    unsigned* ready;          // NVFP4: [q] CTAs that finished their part of fill i;
-                              // BF16: [ugpu] h features written per entry (zero at rest)
-    unsigned* wdc;            // BF16: [q] W_d pieces of fill i stored in its slot (zero at rest)
+    unsigned* ready;          // FP4 and block-FP8: [q] CTAs that finished their part of fill i (zeroed by
+                              // the control pass); BF16: [ugpu] h features written per entry (zero at rest)
+    unsigned* wdc;            // BF16: [q] W_d pieces of fill i stored in its slot; FP4: [q] CTAs done with
+                              // the phase-A items of fill i (zero at rest)
     unsigned fill_chunk;      // bytes of one fused-fill ring slot
     int fill_slots;           // fused-fill ring slots (2..4)
     int fill_fpf;             // BF16: features per fused-fill unit
@@ -442,7 +444,6 @@ struct ExpertParams {
     const float* gscale;      // [L*E] FP4 per-expert fp32 global (all 1 for MXFP4), or null
     uint4* x16;               // FP4 decode scratch: T_max x H activations as scaled f16 pairs
     float* xsc;               // FP4 decode scratch: T_max row factors
-    unsigned long long* hmax; // FP4 decode scratch: T_max per-token |h| maxima, tagged (zeroed at init)
     unsigned long long wait_ns;  // BF16: limit of the waits on other warps' or CTAs' progress
                                  // (waits for a thread's own copies keep FT_WAIT_LIMIT_NS)
     int tgroup;               // NVFP4: tokens per phase-B item
