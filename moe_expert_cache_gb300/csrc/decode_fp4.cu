@@ -39,12 +39,14 @@
 // phase-A and phase-B items, then each fill's phase-A and phase-B items; when
 // a group's phase-A items are done the CTA counts itself in the group's
 // counter, and a phase-B item's h rows are copied once all G CTAs have.
-// Fills the control pass left pending are copied by this launch: the fill
-// thread of every CTA copies its equal part of each fill record in turn (one
-// byte range, host pool -> shared ring -> victim slot by bulk copies) and
-// counts itself in ready[r]; a fill's items wait for the whole record (and,
-// in phase B, for every CTA's count of the fill's group), so the resident
-// entries' two phases run while the fills stream.  x is converted into shared memory when T*H*2
+// Fills the control pass left pending are copied by this launch, starting at
+// its entry: the fill thread of every CTA copies its equal share of each fill
+// record in turn, the W_gu values and scales first, then W_d (host pool ->
+// shared ring -> victim slot by bulk copies), counting itself after each
+// part; a fill's phase-A items wait for every CTA's W_gu share, its phase-B
+// items for the whole record and every CTA's count of the fill's group, so
+// the resident entries' two phases run while the fills stream and a fill's
+// phase A runs while its W_d streams.  x is converted into shared memory when T*H*2
 // bytes fit, else into a global block behind a grid barrier at the start.
 #include "ft_common.cuh"
 #include "../../include/ft.h"
@@ -431,6 +433,139 @@ struct Steps {
     }
 };
 
+// Fused fill, run by ONE thread of CTA c (of G): each fill record is copied
+// in two parts, each split into G equal 16-byte-aligned shares (CTA c takes
+// share c) and sent host pool -> shared ring (bulk loads on mbarriers, up to
+// nf in flight) -> victim slot (bulk stores): part 0 = the W_gu values and
+// scales (the bytes the fill's phase-A items read), part 1 = the W_d values
+// and scales.  A part is two byte ranges of the record taken as one run; a
+// chunk never straddles them.  Once a part's share is stored (the stores
+// complete, then the async-proxy writes are ordered before a GPU-scope
+// release) the CTA counts itself: part 0 in the high half-word of cnt0[r],
+// part 1 in ready[r].  Every wait is bounded.
+struct FillParts {
+    unsigned long long off[2][2];  // [part][range] record offsets
+    unsigned long long len[2][2];  // [part][range] bytes (multiples of 16)
+};
+
+__device__ __noinline__ void fill_parts_tma(const uint8_t* host, uint8_t* pool, unsigned long long rb, int q,
+                                            const int* fslot, const int* ffid, unsigned* ready, unsigned* cnt0,
+                                            int c, int G, const FillParts& fp, uint8_t* fring, uint64_t* fbar,
+                                            unsigned fch, int nf, unsigned* err) {
+    for (int s = 0; s < nf; ++s) ft::mbar_init(&fbar[s], 1);
+    ft::mbar_fence_init();
+    // CTA c's share [b0, b1) of part pt (offsets within the part's run)
+    unsigned long long sb0[2], sb1[2];
+    for (int pt = 0; pt < 2; ++pt) {
+        const unsigned long long L = fp.len[pt][0] + fp.len[pt][1];
+        const unsigned long long per = ((L / 16 + G - 1) / G) * 16;
+        const unsigned long long b0 = per * (unsigned long long)c;
+        sb0[pt] = b0 < L ? b0 : L;
+        sb1[pt] = b0 + per < L ? b0 + per : L;
+    }
+    struct Cur { int r, pt; unsigned long long o; };
+    auto settle = [&](Cur& u) {  // onto a chunk, or r == q past the last
+        while (u.r < q && u.o >= sb1[u.pt]) {
+            if (++u.pt == 2) {
+                u.pt = 0;
+                ++u.r;
+            }
+            u.o = sb0[u.pt];
+        }
+    };
+    // the chunk at u: record offset and bytes (not crossing the part's range boundary)
+    auto chunk = [&](const Cur& u, unsigned long long& at, unsigned& n) {
+        const unsigned long long la = fp.len[u.pt][0];
+        unsigned long long end = sb1[u.pt];
+        if (u.o < la && la < end) end = la;
+        n = (unsigned)(end - u.o < fch ? end - u.o : fch);
+        at = u.o < la ? fp.off[u.pt][0] + u.o : fp.off[u.pt][1] + (u.o - la);
+    };
+    auto advance = [&](Cur& u) {
+        unsigned long long at;
+        unsigned n;
+        chunk(u, at, n);
+        u.o += n;
+        settle(u);
+    };
+    // everything before cursor u is stored: count the parts it completes
+    int done_parts = 0;  // parts (2 per fill, in order) counted so far
+    auto publish = [&](const Cur& u) {
+        const int upto = u.r * 2 + u.pt;
+        if (done_parts >= upto) return;
+        ft::bulk_wait_all();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        for (; done_parts < upto; ++done_parts) {
+            const int r = done_parts >> 1;
+            if ((done_parts & 1) == 0)
+                atomicAdd(&cnt0[r], 1u << 16);
+            else
+                atomicAdd(&ready[r], 1u);
+        }
+    };
+    Cur ui{0, 0, sb0[0]}, us{0, 0, sb0[0]};
+    settle(ui);
+    settle(us);
+    publish(us);
+    int issued = 0, done = 0;
+    for (; ui.r < q && issued < nf; ++issued) {
+        unsigned long long at;
+        unsigned n;
+        chunk(ui, at, n);
+        ft::mbar_arrive_expect_tx(&fbar[issued], n);
+        ft::bulk_g2s(fring + (size_t)issued * fch, host + (unsigned long long)ffid[ui.r] * rb + at, n, &fbar[issued]);
+        advance(ui);
+    }
+    bool ok = true;
+    while (us.r < q) {
+        const int s = done % nf;
+        if (!ft::mbar_wait(&fbar[s], (uint32_t)(done / nf) & 1u, err)) {
+            ok = false;
+            break;
+        }
+        unsigned long long at;
+        unsigned n;
+        chunk(us, at, n);
+        ft::bulk_s2g(pool + (unsigned long long)fslot[us.r] * rb + at, fring + (size_t)s * fch, n);
+        ft::bulk_commit();
+        ft::bulk_wait_read_all();
+        ++done;
+        advance(us);
+        if (ui.r < q) {
+            chunk(ui, at, n);
+            ft::mbar_arrive_expect_tx(&fbar[s], n);
+            ft::bulk_g2s(fring + (size_t)s * fch, host + (unsigned long long)ffid[ui.r] * rb + at, n, &fbar[s]);
+            ++issued;
+            advance(ui);
+        }
+        publish(us);
+    }
+    ft::bulk_wait_all();
+    // after a failed wait, loads still in flight land before the CTA may exit (bounded)
+    for (int g = done + (ok ? 0 : 1); g < issued; ++g) ft::mbar_wait(&fbar[g % nf], (uint32_t)(g / nf) & 1u, err);
+}
+
+// Bounded wait until the field (*c >> shift) & 0xFFFF (shift 0 or 16), or the
+// whole word for shift 32, reaches target (acquire at GPU scope), then order
+// the async proxy (bulk copies) after the acquired writes.
+__device__ __forceinline__ bool wait_field(const unsigned* c, unsigned shift, unsigned target, unsigned* err) {
+    const uint64_t t0 = ft::globaltimer();
+    for (unsigned it = 0;; ++it) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+        if (shift < 32) v = (v >> shift) & 0xFFFFu;
+        if (v >= target) break;
+        __nanosleep(64);
+        if ((it & 15u) == 15u && ft::globaltimer() - t0 > FT_WAIT_LIMIT_NS) {
+            atomicOr(err, FT_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
 template <int XM, int SB>
 __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -473,6 +608,28 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     const unsigned wpart = ((unsigned)RMAX * (dvrow + dsrow) + 127u) & ~127u;
     const uint4* xsrc = XM == X_GLOBAL ? p.x16 : x_s;
 
+    // --------------------------------------------------------- fused fill
+    // The fill thread owns its ring and barriers and starts at once; the
+    // other warps stage the worklist and x meanwhile (named barrier 4).
+    if (wid > CW) {
+        if (lane == 0 && q > 0) {
+            FillParts fp;
+            fp.off[0][0] = 0;
+            fp.len[0][0] = VGU;                            // W_gu values
+            fp.off[0][1] = VGU + VD;
+            fp.len[0][1] = SGU;                            // W_gu scales
+            fp.off[1][0] = VGU;
+            fp.len[1][0] = VD;                             // W_d values
+            fp.off[1][1] = VGU + VD + SGU;
+            fp.len[1][1] = p.rb - (VGU + VD + SGU);        // W_d scales
+            fill_parts_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
+                           q, p.fill_slot, p.fill_fid, p.ready, p.wdc, c, G, fp, ring + (size_t)nst * slot_bytes,
+                           reinterpret_cast<uint64_t*>(smem + 128), p.fill_chunk, p.fill_slots, p.err);
+        }
+        return;
+    }
+    constexpr int STAGERS = CONS + 32;  // consumers and producer
+
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
             ft::mbar_init(&full[s], 1);
@@ -480,16 +637,16 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         }
         ft::mbar_fence_init();
     }
-    for (int i = tid; i <= ugpu; i += THREADS) m_off[i] = p.wl_off[i];
-    for (int i = tid; i < ugpu; i += THREADS) {
+    for (int i = tid; i <= ugpu; i += STAGERS) m_off[i] = p.wl_off[i];
+    for (int i = tid; i < ugpu; i += STAGERS) {
         m_slot[i] = p.wl_slot[i];
         m_gs[i] = p.gscale[p.wl_fid[i]];
     }
-    for (int i = tid; i < nasg; i += THREADS) {
+    for (int i = tid; i < nasg; i += STAGERS) {
         m_tok[i] = p.as_tok[i];
         m_gate[i] = p.as_gate[i];
     }
-    for (int i = tid; i < TK; i += THREADS) m_pos[i] = p.out_pos[i];
+    for (int i = tid; i < TK; i += STAGERS) m_pos[i] = p.out_pos[i];
     // paired, scaled activations: in shared memory by every CTA, or one
     // token row per warp across the grid into the global block, then a grid
     // barrier
@@ -498,10 +655,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         // all threads: per-token maxima (shared atomics on the magnitudes'
         // bits, which order like the values), then the scaled pairs
         unsigned* amax_bits = reinterpret_cast<unsigned*>(xf);
-        for (int t = tid; t < T; t += THREADS) amax_bits[t] = 0u;
-        __syncthreads();
+        for (int t = tid; t < T; t += STAGERS) amax_bits[t] = 0u;
+        ft::named_bar_sync(4, STAGERS);
         const int qrow = H / 8;
-        for (int i = tid; i < T * qrow; i += THREADS) {
+        for (int i = tid; i < T * qrow; i += STAGERS) {
             float f[8];
             ft::bf16x8_to_f32(xin[i], f);
             float m = 0.f;
@@ -509,33 +666,35 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
             atomicMax(&amax_bits[i / qrow], __float_as_uint(m));
         }
-        __syncthreads();
-        for (int i = tid; i < T * qrow; i += THREADS) {
+        ft::named_bar_sync(4, STAGERS);
+        for (int i = tid; i < T * qrow; i += STAGERS) {
             const int t = i / qrow, q8 = i - t * qrow;
             const int a = x_exponent(__uint_as_float(amax_bits[t]));
             x_s[(size_t)t * qrow + xpos(q8)] = x_pairs(xin[i], ldexpf(1.f, a));
         }
-        __syncthreads();
-        for (int t = tid; t < T; t += THREADS) xf[t] = ldexpf(1.f, -x_exponent(__uint_as_float(amax_bits[t])));
-        __syncthreads();
+        ft::named_bar_sync(4, STAGERS);
+        for (int t = tid; t < T; t += STAGERS) xf[t] = ldexpf(1.f, -x_exponent(__uint_as_float(amax_bits[t])));
+        ft::named_bar_sync(4, STAGERS);
     } else {
-        for (int t = c + G * wid; t < T; t += G * (THREADS / 32)) {
+        for (int t = c + G * wid; t < T; t += G * (STAGERS / 32)) {
             const float fct = stage_x_row(xin + (size_t)t * (H / 8), H, p.x16 + (size_t)t * (H / 8), lane);
             if (lane == 0) p.xsc[t] = fct;
         }
-        __syncthreads();
+        ft::named_bar_sync(4, STAGERS);
         if (tid == 0) ft::grid_barrier(p.gbar, (unsigned)G, p.err);
-        __syncthreads();
-        for (int t = tid; t < T; t += THREADS) xf[t] = p.xsc[t];
-        __syncthreads();
+        ft::named_bar_sync(4, STAGERS);
+        for (int t = tid; t < T; t += STAGERS) xf[t] = p.xsc[t];
+        ft::named_bar_sync(4, STAGERS);
     }
 
     // Group counters: CTAs whose phase-A items of the group are done (the
-    // resident entries in gbar[3], fill r in wdc[r]).  Exit count: the
-    // consumers and the producer of every CTA count out once they are done
-    // with the group counters; whoever completes the count returns them to
-    // zero for the next launch.  (ready[r], the CTAs that have copied their
-    // part of fill r, is zeroed by the control pass that schedules the fill.)
+    // resident entries in gbar[3], fill r in the low half-word of wdc[r];
+    // its high half-word counts the CTAs whose share of the fill's W_gu is in
+    // the slot).  Exit count: the consumers and the producer of every CTA
+    // count out once they are done with the counters; whoever completes the
+    // count returns them to zero for the next launch.  (ready[r], the CTAs
+    // whose shares of both parts of fill r are stored, is zeroed by the
+    // control pass that schedules the fill.)
     auto group_count = [&](int grp) { return grp == 0 ? p.gbar + 3 : p.wdc + grp - 1; };
     auto count_out = [&]() {
         unsigned n;
@@ -557,14 +716,6 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     sq.m_off = m_off;
     sq.open(0);
 
-    // --------------------------------------------------------- fused fill
-    if (wid > CW) {
-        if (lane == 0 && q > 0)
-            ft::fill_share_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
-                               q, p.fill_slot, p.fill_fid, p.ready, c, G, ring + (size_t)nst * slot_bytes,
-                               reinterpret_cast<uint64_t*>(smem + 128), p.fill_chunk, p.fill_slots, p.err);
-        return;
-    }
     // ------------------------------------------------------------ producer
     if (wid == CW) {
         if (lane == 0) {
@@ -580,7 +731,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 }
             };
             int it = 0, counted = -1;  // the last group whose count this thread has seen complete
-            int filled = 0;            // fills this thread has seen complete in their slots (in order)
+            int filled_a = 0, filled = 0;  // fills seen with W_gu / the whole record in their slots (in order)
             bool ok = true;
             int kind, ent, item, g0;
             while (ok && sq.next(kind, ent, item, g0)) {
@@ -590,9 +741,14 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
                 const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
                 unsigned char* dst = ring + (size_t)st * slot_bytes;
-                // a fill's rows once every CTA has copied its part of the record
-                if (ent - nA + 1 > filled) {
-                    if (!ft::wait_count(p.ready + (ent - nA), (unsigned)G, p.err)) { ok = false; break; }
+                // a fill's W_gu rows (phase A) or its whole record (phase B)
+                // once every CTA has stored its share
+                if (kind == STEP_A && ent - nA + 1 > filled_a) {
+                    if (!wait_field(p.wdc + (ent - nA), 16, (unsigned)G, p.err)) { ok = false; break; }
+                    filled_a = ent - nA + 1;
+                }
+                if (kind == STEP_B && ent - nA + 1 > filled) {
+                    if (!wait_field(p.ready + (ent - nA), 32, (unsigned)G, p.err)) { ok = false; break; }
                     filled = ent - nA + 1;
                 }
                 if (kind == STEP_A) {
@@ -621,7 +777,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
                 // completes and the ring drains)
                 const int gq = ent < nA ? 0 : ent - nA + 1;
                 if (gq != counted) {
-                    ok = ft::wait_count(group_count(gq), (unsigned)G, p.err);
+                    ok = wait_field(group_count(gq), gq == 0 ? 32u : 0u, (unsigned)G, p.err);
                     counted = gq;
                 }
                 ft::bulk_g2s(dst + wpart, p.hbuf + (size_t)(off + g0) * F, hb, &full[st]);
