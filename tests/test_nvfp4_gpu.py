@@ -94,11 +94,14 @@ def _check_tokens(got, ref, where):
     return rel
 
 
-def _replay(ft, sh, S, schedule, B_P, B_H, rho, samples, tok_sample=None, seed=0, distinct=None):
+def _replay(ft, sh, S, schedule, B_P, B_H, rho, samples, tok_sample=None, seed=0, distinct=None, repeat=False):
     """schedule: list of (T, steps).  Every call bit-exact; sampled calls
     numerically: on every token when tok_sample is None, else on every token
     of the sampled calls of each phase's first step and on the tok_sample
-    tokens of the later ones."""
+    tokens of the later ones.  repeat: each sampled forward is run a second
+    time on the same inputs (its fills are then already in their slots, and
+    the launch's counters must have returned to rest); the two outputs must
+    be identical bit for bit."""
     import torch
     pool, glob = _repeated_pool(sh, seed, distinct) if distinct else hz.pinned_pool(sh, seed)
     pool_np = pool.numpy()
@@ -141,6 +144,11 @@ def _replay(ft, sh, S, schedule, B_P, B_H, rho, samples, tok_sample=None, seed=0
                     ref = nm.merged_output(y_gpu_ref, pc_sub)
                     assert np.isfinite(y.cpu().numpy()).all()
                     done.append(_check_tokens(got, ref, (T, step, layer)))
+                    if repeat:
+                        y2 = torch.empty_like(y)
+                        ctx.moe_forward(xd, _dev(pc), y2)
+                        torch.cuda.synchronize()
+                        assert np.array_equal(y2.cpu().numpy(), y.cpu().numpy()), ("repeat", T, step, layer)
                     for f, v in zip(r.F, r.victims):
                         fid = layer * sh.E + f
                         rb = sh.record_bytes
@@ -160,7 +168,7 @@ def _replay(ft, sh, S, schedule, B_P, B_H, rho, samples, tok_sample=None, seed=0
 def test_nvfp4_small(ft, H, F, E, k, S, T):
     sh = synth.Shape(L=2, E=E, k=k, H=H, F=F, fmt=synth.FMT_NVFP4)
     samples = {(s, l) for s in range(4) for l in range(2)}
-    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples)
+    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples, repeat=True)
     assert len(done) == len(samples)
 
 
@@ -257,7 +265,7 @@ def test_large_nvfp4_prefill(ft):
 def test_mxfp4_small(ft, H, F, E, k, S, T):
     sh = synth.Shape(L=2, E=E, k=k, H=H, F=F, fmt=synth.FMT_MXFP4)
     samples = {(s, l) for s in range(4) for l in range(2)}
-    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples)
+    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples, repeat=True)
     assert len(done) == len(samples)
 
 
@@ -289,7 +297,7 @@ def test_large_mxfp4_decode(ft):
 def test_fp8_small(ft, H, F, E, k, S, T):
     sh = synth.Shape(L=2, E=E, k=k, H=H, F=F, fmt=synth.FMT_FP8)
     samples = {(s, l) for s in range(4) for l in range(2)}
-    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples)
+    done = _replay(ft, sh, S, [(T, 4)], 25.0, 75.0, None, samples, repeat=True)
     assert len(done) == len(samples)
 
 
