@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
 
     // --------------------------------------------------------- fused fill
     // The fill thread owns its ring and barriers and starts at once; the
-    // other warps stage the worklist and x meanwhile (named barrier 4).
+    // consumers stage the worklist and x meanwhile (named barrier 4).
     if (wid > CW) {
         if (lane == 0 && q > 0) {
             FillParts fp;
@@ -628,15 +628,122 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         }
         return;
     }
-    constexpr int STAGERS = CONS + 32;  // consumers and producer
-
-    if (tid == 0) {
-        for (int s = 0; s < nst; ++s) {
-            ft::mbar_init(&full[s], 1);
-            ft::mbar_init(&empty[s], CW);
+    // Group counters: CTAs whose phase-A items of the group are done (the
+    // resident entries in gbar[3], fill r in the low half-word of wdc[r];
+    // its high half-word counts the CTAs whose share of the fill's W_gu is in
+    // the slot).  Exit count: the consumers and the producer of every CTA
+    // count out once they are done with the counters; whoever completes the
+    // count returns them to zero for the next launch.  (ready[r], the CTAs
+    // whose shares of both parts of fill r are stored, is zeroed by the
+    // control pass that schedules the fill.)
+    auto group_count = [&](int grp) { return grp == 0 ? p.gbar + 3 : p.wdc + grp - 1; };
+    auto count_out = [&]() {
+        unsigned n;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.gbar + 2) : "memory");
+        if (n == 2u * (unsigned)G - 1u) {
+            for (int r = 0; r < q; ++r) p.wdc[r] = 0u;
+            p.gbar[3] = 0u;
+            p.gbar[2] = 0u;
         }
-        ft::mbar_fence_init();
+    };
+    // ------------------------------------------------------------ producer
+    // The producer starts at once as well: it initialises the ring barriers,
+    // lets the consumers use them (named barrier 5, which they take once x is
+    // staged) and reads the worklist from global memory.
+    if (wid == CW) {
+        if (lane == 0) {
+            for (int s = 0; s < nst; ++s) {
+                ft::mbar_init(&full[s], 1);
+                ft::mbar_init(&empty[s], CW);
+            }
+            ft::mbar_fence_init();
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 5, %0;" ::"n"(CONS + 32) : "memory");
+        if (lane == 0) {
+            Steps sq;
+            sq.c = c;
+            sq.G = G;
+            sq.cpe = cpe;
+            sq.nA = nA;
+            sq.nfill = q;
+            sq.R = R;
+            sq.TG = TG;
+            sq.m_off = p.wl_off;
+            sq.open(0);
+            const uint64_t pol = ft::l2_policy_evict_first();
+            // this CTA's W_d rows (values and scales) of the resident entries
+            // go to L2 once the ring is primed, so phase B reads them from L2
+            auto prefetch_wd = [&]() {
+                if (R == 0) return;
+                for (int e = 0; e < nA; ++e) {
+                    const uint8_t* rec = p.slot_pool + (size_t)p.wl_slot[e] * p.rb;
+                    ft::bulk_prefetch_l2(rec + VGU + (size_t)r0 * dvrow, (unsigned)R * dvrow);
+                    ft::bulk_prefetch_l2(rec + VGU + VD + SGU + (size_t)r0 * dsrow, (unsigned)R * dsrow);
+                }
+            };
+            int it = 0, counted = -1;  // the last group whose count this thread has seen complete
+            int filled_a = 0, filled = 0;  // fills seen with W_gu / the whole record in their slots (in order)
+            bool ok = true;
+            int kind, ent, item, g0;
+            while (ok && sq.next(kind, ent, item, g0)) {
+                if (kind == STEP_SEAL) continue;
+                const int st = it % nst;
+                if (it == nst) prefetch_wd();
+                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
+                const uint8_t* rec = p.slot_pool + (size_t)p.wl_slot[ent] * p.rb;
+                unsigned char* dst = ring + (size_t)st * slot_bytes;
+                // a fill's W_gu rows (phase A) or its whole record (phase B)
+                // once every CTA has stored its share
+                if (kind == STEP_A && ent - nA + 1 > filled_a) {
+                    if (!wait_field(p.wdc + (ent - nA), 16, (unsigned)G, p.err)) { ok = false; break; }
+                    filled_a = ent - nA + 1;
+                }
+                if (kind == STEP_B && ent - nA + 1 > filled) {
+                    if (!wait_field(p.ready + (ent - nA), 32, (unsigned)G, p.err)) { ok = false; break; }
+                    filled = ent - nA + 1;
+                }
+                if (kind == STEP_A) {
+                    const int grow = (item - ent * cpe) * 2 * FPC;  // first gate row; up rows 16 later
+                    ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * (vrow + srow));
+                    ft::bulk_g2s_hint(dst, rec + (size_t)grow * vrow, FPC * vrow, &full[st], pol);
+                    ft::bulk_g2s_hint(dst + FPC * vrow, rec + (size_t)(grow + 16) * vrow, FPC * vrow, &full[st], pol);
+                    ft::bulk_g2s_hint(dst + 2 * FPC * vrow, rec + VGU + VD + (size_t)grow * srow, FPC * srow,
+                                      &full[st], pol);
+                    ft::bulk_g2s_hint(dst + 2 * FPC * vrow + FPC * srow, rec + VGU + VD + (size_t)(grow + 16) * srow,
+                                      FPC * srow, &full[st], pol);
+                    ++it;
+                    continue;
+                }
+                // phase-B item: this CTA's W_d rows of the entry, then the h
+                // rows of the item once every CTA has sealed the entry's group
+                const int off = p.wl_off[ent];
+                const int ng = min(TG, p.wl_off[ent + 1] - off - g0);
+                const unsigned wb = (unsigned)R * dvrow, sb = (unsigned)R * dsrow, hb = (unsigned)ng * F * 4u;
+                ft::mbar_arrive_expect_tx(&full[st], wb + sb + hb);
+                ft::bulk_g2s_hint(dst, rec + VGU + (size_t)r0 * dvrow, wb, &full[st], pol);
+                ft::bulk_g2s_hint(dst + (size_t)RMAX * dvrow, rec + VGU + VD + SGU + (size_t)r0 * dsrow, sb,
+                                  &full[st], pol);
+                // (waited for once per group; after a timed-out wait the rows
+                // are still copied, whatever they hold, so that the item
+                // completes and the ring drains)
+                const int gq = ent < nA ? 0 : ent - nA + 1;
+                if (gq != counted) {
+                    ok = wait_field(group_count(gq), gq == 0 ? 32u : 0u, (unsigned)G, p.err);
+                    counted = gq;
+                }
+                ft::bulk_g2s(dst + wpart, p.hbuf + (size_t)(off + g0) * F, hb, &full[st]);
+                ++it;
+            }
+            if (it <= nst && ok) prefetch_wd();
+            ft::drain_ring(full, it, nst, p.err);
+            count_out();
+        }
+        return;
     }
+
+    // ------------------------------------------------- consumers: staging
+    constexpr int STAGERS = CONS;
     for (int i = tid; i <= ugpu; i += STAGERS) m_off[i] = p.wl_off[i];
     for (int i = tid; i < ugpu; i += STAGERS) {
         m_slot[i] = p.wl_slot[i];
@@ -686,25 +793,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         for (int t = tid; t < T; t += STAGERS) xf[t] = p.xsc[t];
         ft::named_bar_sync(4, STAGERS);
     }
+    ft::named_bar_sync(5, CONS + 32);  // the producer has initialised the ring barriers
 
-    // Group counters: CTAs whose phase-A items of the group are done (the
-    // resident entries in gbar[3], fill r in the low half-word of wdc[r];
-    // its high half-word counts the CTAs whose share of the fill's W_gu is in
-    // the slot).  Exit count: the consumers and the producer of every CTA
-    // count out once they are done with the counters; whoever completes the
-    // count returns them to zero for the next launch.  (ready[r], the CTAs
-    // whose shares of both parts of fill r are stored, is zeroed by the
-    // control pass that schedules the fill.)
-    auto group_count = [&](int grp) { return grp == 0 ? p.gbar + 3 : p.wdc + grp - 1; };
-    auto count_out = [&]() {
-        unsigned n;
-        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.gbar + 2) : "memory");
-        if (n == 2u * (unsigned)G - 1u) {
-            for (int r = 0; r < q; ++r) p.wdc[r] = 0u;
-            p.gbar[3] = 0u;
-            p.gbar[2] = 0u;
-        }
-    };
     Steps sq;
     sq.c = c;
     sq.G = G;
@@ -716,79 +806,6 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     sq.m_off = m_off;
     sq.open(0);
 
-    // ------------------------------------------------------------ producer
-    if (wid == CW) {
-        if (lane == 0) {
-            const uint64_t pol = ft::l2_policy_evict_first();
-            // this CTA's W_d rows (values and scales) of the resident entries
-            // go to L2 once the ring is primed, so phase B reads them from L2
-            auto prefetch_wd = [&]() {
-                if (R == 0) return;
-                for (int e = 0; e < nA; ++e) {
-                    const uint8_t* rec = p.slot_pool + (size_t)m_slot[e] * p.rb;
-                    ft::bulk_prefetch_l2(rec + VGU + (size_t)r0 * dvrow, (unsigned)R * dvrow);
-                    ft::bulk_prefetch_l2(rec + VGU + VD + SGU + (size_t)r0 * dsrow, (unsigned)R * dsrow);
-                }
-            };
-            int it = 0, counted = -1;  // the last group whose count this thread has seen complete
-            int filled_a = 0, filled = 0;  // fills seen with W_gu / the whole record in their slots (in order)
-            bool ok = true;
-            int kind, ent, item, g0;
-            while (ok && sq.next(kind, ent, item, g0)) {
-                if (kind == STEP_SEAL) continue;
-                const int st = it % nst;
-                if (it == nst) prefetch_wd();
-                if (it >= nst && !ft::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err)) { ok = false; break; }
-                const uint8_t* rec = p.slot_pool + (size_t)m_slot[ent] * p.rb;
-                unsigned char* dst = ring + (size_t)st * slot_bytes;
-                // a fill's W_gu rows (phase A) or its whole record (phase B)
-                // once every CTA has stored its share
-                if (kind == STEP_A && ent - nA + 1 > filled_a) {
-                    if (!wait_field(p.wdc + (ent - nA), 16, (unsigned)G, p.err)) { ok = false; break; }
-                    filled_a = ent - nA + 1;
-                }
-                if (kind == STEP_B && ent - nA + 1 > filled) {
-                    if (!wait_field(p.ready + (ent - nA), 32, (unsigned)G, p.err)) { ok = false; break; }
-                    filled = ent - nA + 1;
-                }
-                if (kind == STEP_A) {
-                    const int grow = (item - ent * cpe) * 2 * FPC;  // first gate row; up rows 16 later
-                    ft::mbar_arrive_expect_tx(&full[st], 2u * FPC * (vrow + srow));
-                    ft::bulk_g2s_hint(dst, rec + (size_t)grow * vrow, FPC * vrow, &full[st], pol);
-                    ft::bulk_g2s_hint(dst + FPC * vrow, rec + (size_t)(grow + 16) * vrow, FPC * vrow, &full[st], pol);
-                    ft::bulk_g2s_hint(dst + 2 * FPC * vrow, rec + VGU + VD + (size_t)grow * srow, FPC * srow,
-                                      &full[st], pol);
-                    ft::bulk_g2s_hint(dst + 2 * FPC * vrow + FPC * srow, rec + VGU + VD + (size_t)(grow + 16) * srow,
-                                      FPC * srow, &full[st], pol);
-                    ++it;
-                    continue;
-                }
-                // phase-B item: this CTA's W_d rows of the entry, then the h
-                // rows of the item once every CTA has sealed the entry's group
-                const int off = m_off[ent];
-                const int ng = min(TG, m_off[ent + 1] - off - g0);
-                const unsigned wb = (unsigned)R * dvrow, sb = (unsigned)R * dsrow, hb = (unsigned)ng * F * 4u;
-                ft::mbar_arrive_expect_tx(&full[st], wb + sb + hb);
-                ft::bulk_g2s_hint(dst, rec + VGU + (size_t)r0 * dvrow, wb, &full[st], pol);
-                ft::bulk_g2s_hint(dst + (size_t)RMAX * dvrow, rec + VGU + VD + SGU + (size_t)r0 * dsrow, sb,
-                                  &full[st], pol);
-                // (waited for once per group; after a timed-out wait the rows
-                // are still copied, whatever they hold, so that the item
-                // completes and the ring drains)
-                const int gq = ent < nA ? 0 : ent - nA + 1;
-                if (gq != counted) {
-                    ok = wait_field(group_count(gq), gq == 0 ? 32u : 0u, (unsigned)G, p.err);
-                    counted = gq;
-                }
-                ft::bulk_g2s(dst + wpart, p.hbuf + (size_t)(off + g0) * F, hb, &full[st]);
-                ++it;
-            }
-            if (it <= nst && ok) prefetch_wd();
-            ft::drain_ring(full, it, nst, p.err);
-            count_out();
-        }
-        return;
-    }
 
     // ------------------------------------- consumers: phase-A and phase-B items
     // After a failed (timed-out) wait a warp stops waiting, computing and
