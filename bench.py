@@ -766,16 +766,18 @@ def hits_only_times(ctx, T, routes, x, pc, y, flush, stream, device):
     return statistics.median(us), d
 
 
-def one_fill_times(ctx, E, x, pc, y, flush, stream, calls: int = 6):
+def one_fill_times(ctx, E, x, pc, y, flush, stream, calls: int = 12, warmup: int = 1):
     """Expert-kernel device time of T=1 calls that route 7 resident experts
     and 1 expert evicted just before (ft_set_ctl_state), so each call makes
-    exactly one fill beside 7 hits; L2 flushed before each call.  Returns
-    (median us, the standalone fill time of one record in us)."""
+    exactly one fill beside 7 hits; L2 flushed before each call; `warmup`
+    untimed calls first (the first fill call of a context runs cold).  Returns
+    (median us of the timed calls, the standalone fill time of one record in
+    us)."""
     import torch
     k = 8
     w = torch.full((1, k), 1.0 / k, device=x.device)
     us = []
-    for i in range(calls):
+    for i in range(warmup + calls):
         sfi, ifs, stp, clk = ctx.ctl_state()
         victim = 8 * (i + 1)  # resident, not among the call's 7 hits
         s_v = int(sfi[victim])
@@ -794,7 +796,8 @@ def one_fill_times(ctx, E, x, pc, y, flush, stream, calls: int = 6):
         ctx.profile_enable(False)
         c1 = ctx.counters()
         assert c1["fills"] - c0["fills"] == 1 and c1["hits"] - c0["hits"] == 7
-        us.append(1e3 * pr["expert_ffn"]["ms"] / pr["expert_ffn"]["launches"])
+        if i >= warmup:
+            us.append(1e3 * pr["expert_ffn"]["ms"] / pr["expert_ffn"]["launches"])
     gbps = ctx.measure_link(1, 3)
     return statistics.median(us), None if not gbps else 1e6 * ctx_record_bytes(ctx) / (gbps * 1e9)
 
