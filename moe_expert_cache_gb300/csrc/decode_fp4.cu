@@ -30,24 +30,26 @@
 // [W_gu scales 2F x H/SB][W_d scales H x F/SB].
 //
 // Layout of the work: 16 consumer warps, one producer warp (TMA ring) and one
-// fill warp (one thread) per CTA, one CTA per SM.  A phase-A item is 16 features (16 gate
-// rows, the 16 up rows and their scale rows, one warp per feature); CTA c
-// takes the items c, c + G, ... of the resident entries.  A phase-B item is
-// (entry, group of at most TG tokens): the CTA's W_d rows [r0, r1), the
-// staged fp32 h rows and, in the slot's tail, those rows converted to f16
-// pairs, two W_d rows per warp pass.  The CTA takes the resident entries'
-// phase-A and phase-B items, then each fill's phase-A and phase-B items; when
-// a group's phase-A items are done the CTA counts itself in the group's
-// counter, and a phase-B item's h rows are copied once all G CTAs have.
-// Fills the control pass left pending are copied by this launch, starting at
-// its entry: the fill thread of every CTA copies its equal share of each fill
-// record in turn, the W_gu values and scales first, then W_d (host pool ->
-// shared ring -> victim slot by bulk copies), counting itself after each
-// part; a fill's phase-A items wait for every CTA's W_gu share, its phase-B
-// items for the whole record and every CTA's count of the fill's group, so
-// the resident entries' two phases run while the fills stream and a fill's
-// phase A runs while its W_d streams.  x is converted into shared memory when T*H*2
-// bytes fit, else into a global block behind a grid barrier at the start.
+// fill warp (one thread) per CTA, one CTA per SM.  A phase-A item is 16
+// features (16 gate rows, the 16 up rows and their scale rows, one warp per
+// feature); CTA c takes the items c, c + G, ... of each group of entries.  A
+// phase-B item is (entry, group of at most TG tokens): the CTA's W_d rows
+// [r0, r1), the staged fp32 h rows and, in the slot's tail, those rows
+// converted to f16 pairs, two W_d rows per warp pass.  The CTA takes the
+// resident entries' phase-A and phase-B items, then each fill's phase-A and
+// phase-B items; when a group's phase-A items are done the CTA counts itself
+// in the group's counter, and a phase-B item's h rows are copied once all G
+// CTAs have.  The producer and the fill thread start at the launch's entry,
+// while the consumers stage the worklist and x: x goes into shared memory
+// when T*H*2 bytes fit, else into a global block behind a grid barrier.
+// Fills the control pass left pending are copied by this launch: the fill
+// thread of every CTA copies its equal share of each fill record in turn,
+// the W_gu values and scales first, then W_d (host pool -> shared ring ->
+// victim slot by bulk copies), counting itself after each part; a fill's
+// phase-A items wait for every CTA's W_gu share, its phase-B items for the
+// whole record and every CTA's count of the fill's group, so the resident
+// entries' two phases run while the fills stream and a fill's phase A runs
+// while its W_d streams.
 #include "ft_common.cuh"
 #include "../../include/ft.h"
 
