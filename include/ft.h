@@ -117,7 +117,10 @@ const char* ft_status_str(ft_status s);
  *                  with prefill hold the same bf16 staging copy as NVFP4.
  *                  FP8 (block-FP8, the same section's "FP8 weights and
  *                  block-scale data") needs H % 128 == 0, F % 128 == 0,
- *                  nvfp4_global == NULL and T_max*k*ceil(H/SMs)*4 bytes of
+ *                  (H/128)*(F/128) a multiple of 4 (so that every record and
+ *                  each of its three scale matrices starts on a 16-byte
+ *                  boundary, as the kernels' bulk copies and 16-byte loads
+ *                  require), nvfp4_global == NULL and T_max*k*ceil(H/SMs)*4 bytes of
  *                  shared memory (at most 227 KiB); its decode streams the
  *                  pending fills inside the gate/up kernel, as the other
  *                  formats do, and its prefill stages the layer in bf16 (one

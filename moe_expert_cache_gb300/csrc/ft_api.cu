@@ -199,7 +199,9 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
         T_max < 1 || T_max > 256 || T_max * k > 4096 || T_prefill_max < 0 || !host_pool)
         return FT_ERR_ARG;
     if (fmt != FT_FMT_BF16 && fmt != FT_FMT_NVFP4 && fmt != FT_FMT_MXFP4 && fmt != FT_FMT_FP8) return FT_ERR_ARG;
-    if (fmt == FT_FMT_FP8 && (nvfp4_global || H % 128 || F % 128)) return FT_ERR_ARG;
+    // FP8 records (3HF value bytes + 4 bytes per 128 x 128 block of W_g, W_u and
+    // W_d) and their scale matrices must start on 16-byte boundaries
+    if (fmt == FT_FMT_FP8 && (nvfp4_global || H % 128 || F % 128 || ((H / 128) * (F / 128)) % 4)) return FT_ERR_ARG;
     if (fmt == FT_FMT_NVFP4 && (!nvfp4_global || H % 256 || F % 256)) return FT_ERR_ARG;
     if (fmt == FT_FMT_MXFP4 && (nvfp4_global || H % 256 || F % 512)) return FT_ERR_ARG;
     if (fmt == FT_FMT_BF16 && nvfp4_global) return FT_ERR_ARG;

@@ -75,6 +75,9 @@ def test_argument_checks_need_no_gpu(lib):
     assert lib.layer_init(1, 8, 2, 256, 512, 4, 4, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 192, 256, 4, lib.FT_FMT_FP8, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 256, 256, 4, lib.FT_FMT_FP8, 4, 0, 1024, 4096, None, None)[0] == lib.FT_ERR_ARG
+    # FP8 shapes whose records would not start on 16-byte boundaries: (H/128)*(F/128) = 1, 2, 3, 6
+    for H, F in ((128, 128), (256, 128), (384, 128), (384, 256)):
+        assert lib.layer_init(1, 8, 2, H, F, 4, lib.FT_FMT_FP8, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 256, 256, 4, lib.FT_FMT_MXFP4, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 256, 512, 4, lib.FT_FMT_MXFP4, 4, 0, 1024, 4096, None, None)[0] == lib.FT_ERR_ARG
     assert lib.layer_init(1, 8, 2, 256, 512, 4, lib.FT_FMT_NVFP4, 4, 0, 1024, None, None, None)[0] == lib.FT_ERR_ARG
