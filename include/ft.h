@@ -138,8 +138,10 @@ const char* ft_status_str(ft_status s);
  *   host_pool      HOST address of the caller's expert pool: L*E records of
  *                  ft_record_bytes(H,F,fmt) bytes, record l*E+e at offset
  *                  (l*E+e)*record_bytes.  Must be page-locked (cudaHostAlloc /
- *                  cudaHostRegister) or otherwise device-accessible, and stay
- *                  valid and unchanged until ft_destroy.  Not copied.
+ *                  cudaHostRegister) or otherwise device-accessible, its
+ *                  device address 16-byte aligned (FT_ERR_ARG otherwise: the
+ *                  fills read it with bulk copies), and stay valid and
+ *                  unchanged until ft_destroy.  Not copied.
  *   nvfp4_global   HOST array of L*E fp32 per-record global scales (NVFP4), or
  *                  NULL for BF16, MXFP4 and FP8.  Copied to device memory at init (the pages:
  *                  small per-expert values stay GPU-resident).
