@@ -436,7 +436,8 @@ struct ExpertParams {
     unsigned* ready;          // FP4 and block-FP8: [q] CTAs that finished their part of fill i (zeroed by
                               // the control pass); BF16: [ugpu] h features written per entry (zero at rest)
     unsigned* wdc;            // BF16: [q] W_d pieces of fill i stored in its slot; FP4: [q] CTAs done with
-                              // the phase-A items of fill i (zero at rest)
+                              // the phase-A items of fill i (low half-word) and CTAs whose share of fill
+                              // i's W_gu is stored (high half-word) (zero at rest)
     unsigned fill_chunk;      // bytes of one fused-fill ring slot
     int fill_slots;           // fused-fill ring slots (2..4)
     int fill_fpf;             // BF16: features per fused-fill unit
