@@ -35,7 +35,8 @@
 // feature); CTA c takes the items c, c + G, ... of each group of entries.  A
 // phase-B item is (entry, group of at most TG tokens): the CTA's W_d rows
 // [r0, r1), the staged fp32 h rows and, in the slot's tail, those rows
-// converted to f16 pairs, two W_d rows per warp pass.  The CTA takes the
+// converted to f16 pairs, two W_d rows per warp pass; phase-B items
+// alternate between the two halves of the consumer warps.  The CTA takes the
 // resident entries' phase-A and phase-B items, then each fill's phase-A and
 // phase-B items; when a group's phase-A items are done the CTA counts itself
 // in the group's counter, and a phase-B item's h rows are copied once all G
@@ -130,6 +131,11 @@ __device__ __forceinline__ int x_exponent(float amax) {
 
 // 2^b for an exponent from x_exponent (|b| <= 100: a normal float).
 __device__ __forceinline__ float pow2i(int b) { return __int_as_float((b + 127) << 23); }
+
+// n arrivals on an mbarrier by one thread.
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(ft::smem_addr(bar)), "r"(n) : "memory");
+}
 
 // Eight bf16 values (one word's activations) times `up` as the chunk of
 // four f16 pairs (x[2J], x[2J+1]).
@@ -273,12 +279,12 @@ __device__ __forceinline__ void gu_feature4(const uint4* gv, const uint4* uv, co
     }
 }
 
-// Phase B: the W_d rows rb + CW*r (r < RW, row < R) of a slot (values +
+// Phase B: the W_d rows rb + WS*r (r < RW, row < R) of a slot (values +
 // scales) against NT h rows held as scaled f16 pairs (the layout of the
 // phase-A activations, F/8 chunks per row), each 16-value block of a row
 // with its factor in hfb (F/16 per row).  Each h chunk is loaded once and
 // applied to every row of the warp.
-template <int NT, int SB>
+template <int NT, int SB, int WS>
 __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
                                             unsigned dsrow, const uint4* hp, const float* hfb, int g, int F,
                                             int lane, float gsc, float* o_s, int obase, int RMAX, int rb, int R) {
@@ -294,7 +300,7 @@ __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t*
         float2 sc[RW];
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
-            const int rl = rb + CW * r < R ? rb + CW * r : rb;  // rows past R repeat row rb (not stored)
+            const int rl = rb + WS * r < R ? rb + WS * r : rb;  // rows past R repeat row rb (not stored)
             const uint4 w = reinterpret_cast<const uint4*>(wrows + (size_t)rl * dvrow)[v];
             sc[r] = scales32<SB>(srows + (size_t)rl * dsrow, v);
             e2m1_word_h2(w.x, d[r]);
@@ -318,7 +324,7 @@ __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t*
     }
 #pragma unroll
     for (int r = 0; r < RW; ++r) {
-        const int rl = rb + CW * r;
+        const int rl = rb + WS * r;
         if (rl < R) {  // warp-uniform
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
@@ -329,19 +335,19 @@ __device__ __forceinline__ void down_group4(const uint8_t* wrows, const uint8_t*
     }
 }
 
-// The rows rb + CW*r (r < RW) of a slot against its ng h rows, two tokens
-// at a time.
-template <int SB>
+// The rows rb + WS*r (r < RW) of a slot against its ng h rows, two tokens
+// at a time (WS: the warps sharing the item).
+template <int SB, int WS>
 __device__ __forceinline__ void down_rows4(const uint8_t* wrows, const uint8_t* srows, unsigned dvrow,
                                         unsigned dsrow, const uint4* hp, const float* hfb, int ng, int F, int lane,
                                         float gsc, float* o_s, int obase, int RMAX, int rb, int R) {
     int g = 0;
     while (g < ng) {
         if (ng - g >= 2) {
-            down_group4<2, SB>(wrows, srows, dvrow, dsrow, hp, hfb, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
+            down_group4<2, SB, WS>(wrows, srows, dvrow, dsrow, hp, hfb, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
             g += 2;
         } else {
-            down_group4<1, SB>(wrows, srows, dvrow, dsrow, hp, hfb, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
+            down_group4<1, SB, WS>(wrows, srows, dvrow, dsrow, hp, hfb, g, F, lane, gsc, o_s, obase, RMAX, rb, R);
             g += 1;
         }
     }
@@ -810,9 +816,17 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
 
 
     // ------------------------------------- consumers: phase-A and phase-B items
-    // After a failed (timed-out) wait a warp stops waiting, computing and
-    // releasing slots, but takes the same barriers and seals as the others.
-    int it = 0;
+    // Phase-A items are taken by all 16 warps; phase-B items alternate
+    // between the two halves of 8 warps (half 0 the even ones), so that two
+    // items' conversions, barriers and short row chains overlap; each warp of
+    // the taking half arrives twice on the slot's empty barrier (its count is
+    // 16).  After a failed (timed-out) wait a warp stops waiting, computing
+    // and releasing slots, but takes the same barriers and seals as the
+    // others of its half.
+    constexpr int HW = CW / 2;           // warps per half
+    constexpr int HT = HW * 32;          // threads per half
+    const int half = wid / HW;
+    int it = 0, nb = 0;
     bool failed = false;
     int kind, ent, item, g0;
     while (sq.next(kind, ent, item, g0)) {
@@ -823,6 +837,11 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             continue;
         }
         const int st = it % nst;
+        if (kind == STEP_B && (nb & 1) != half) {  // the other half's item
+            ++it;
+            ++nb;
+            continue;
+        }
         const bool ok = !failed && __all_sync(0xffffffffu, ft::mbar_wait(&full[st], (it / nst) & 1, p.err));
         failed = !ok;
         const unsigned char* sb = ring + (size_t)st * slot_bytes;
@@ -841,14 +860,14 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             ++it;
             continue;
         }
-        // down rows [r0, r1) of one token group of the entry.  The staged
-        // fp32 h rows are converted to f16 pairs, each 16-value block scaled
-        // by its own power of two, by every consumer thread into the slot's
-        // tail (past the W_d rows and the fp32 rows the copy lands): the
-        // pairs, then the block factors; then one barrier (warps whose wait
-        // failed still take it).  Consecutive items use different slots, and
-        // a slot's tail is rewritten only after every warp has released the
-        // slot.
+        // down rows [r0, r1) of one token group of the entry, by this half.
+        // The staged fp32 h rows are converted to f16 pairs, each 16-value
+        // block scaled by its own power of two, by the half's threads into
+        // the slot's tail (past the W_d rows and the fp32 rows the copy
+        // lands): the pairs, then the block factors; then the half's barrier
+        // (warps whose wait failed still take it).  Consecutive items use
+        // different slots, and a slot's tail is rewritten only after every
+        // warp has released the slot.
         const int ng = min(TG, ntok - g0);
         const float* hs = reinterpret_cast<const float*>(sb + wpart);
         unsigned char* tail = ring + (size_t)st * slot_bytes + wpart + (size_t)TG * F * 4;
@@ -858,20 +877,24 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
             // the two chunks of a block are lanes 2m and 2m + 1 of one step
             // (F/8 is a multiple of 32, so every lane of a warp takes the same
             // number of steps)
-            for (int i = tid; i < ng * (F / 8); i += CONS) {
+            for (int i = tid - half * HT; i < ng * (F / 8); i += HT) {
                 const int n = i / (F / 8), q8 = i - n * (F / 8);
                 float fb;
                 hp[(size_t)n * (F / 8) + xpos(q8)] = h_pairs_block(hs + (size_t)n * F, q8, &fb);
                 if ((q8 & 1) == 0) hfb[(size_t)n * (F / 16) + (q8 >> 1)] = fb;
             }
         }
-        ft::named_bar_sync(2, CONS);
-        for (int rb = wid; rb < R && ok; rb += RW * CW)
-            down_rows4<SB>(sb, sb + (size_t)RMAX * dvrow, dvrow, dsrow, hp, hfb, ng, F, lane, m_gs[ent], o_s,
-                           off + g0, RMAX, rb, R);
+        if (half)  // constant barrier ids (a computed id reserves every barrier of the CTA)
+            ft::named_bar_sync(7, HT);
+        else
+            ft::named_bar_sync(6, HT);
+        for (int rb = wid - half * HW; rb < R && ok; rb += RW * HW)
+            down_rows4<SB, HW>(sb, sb + (size_t)RMAX * dvrow, dvrow, dsrow, hp, hfb, ng, F, lane, m_gs[ent], o_s,
+                               off + g0, RMAX, rb, R);
         __syncwarp();
-        if (ok && lane == 0) ft::mbar_arrive(&empty[st]);
+        if (ok && lane == 0) mbar_arrive_n(&empty[st], 2);
         ++it;
+        ++nb;
     }
     ft::named_bar_sync(1, CONS);
     for (int idx = tid; idx < T * R; idx += CONS) {
