@@ -52,7 +52,10 @@
 // entries' two phases run while the fills stream and a fill's phase A runs
 // while its W_d streams.
 #include "ft_common.cuh"
+#include "fp4_steps.cuh"
 #include "../../include/ft.h"
+
+using namespace fp4sched;
 
 namespace {
 
@@ -380,66 +383,6 @@ __device__ __forceinline__ uint4 h_pairs_block(const float* hr, int q, float* fb
 
 namespace {
 
-// The steps of CTA c, in the order its producer issues them and its
-// consumers take them: the phase-A items of the resident entries (a = c,
-// c + G, ...), a seal, their phase-B items (entry, group of <= TG tokens),
-// then for each fill in turn its phase-A items, a seal and its phase-B items.
-// At a seal the consumers count the CTA in the group's counter (every CTA's
-// h of the group is written once it holds G); a seal takes no ring slot.  A
-// phase-B item waits for its group's count, each group's phase-A items come
-// before its seal on every CTA, and the groups are taken in the same order
-// everywhere: no wait can close a cycle.
-enum { STEP_A = 0, STEP_SEAL = 1, STEP_B = 2 };
-struct Steps {
-    int c, G, cpe, nA, nfill, R, TG;
-    const int* m_off;
-    int grp, eb, ee, a, e, g0;
-    bool inB;
-    __device__ void open(int g) {  // group 0: the resident entries; group 1 + r: fill r
-        grp = g;
-        eb = g == 0 ? 0 : nA + g - 1;
-        ee = g == 0 ? nA : eb + 1;
-        int m = (int)(((long long)c - (long long)eb * cpe) % G);
-        if (m < 0) m += G;
-        a = eb * cpe + m;
-        inB = false;
-    }
-    // The next step (false past the last): its kind, its entry (for a seal:
-    // the group), and the phase-A item index or the first token of the
-    // phase-B group.
-    __device__ bool next(int& kind, int& ent, int& item, int& g) {
-        for (;;) {
-            if (grp > nfill) return false;
-            if (!inB) {
-                if (a < ee * cpe) {
-                    kind = STEP_A;
-                    ent = a / cpe;
-                    item = a;
-                    a += G;
-                    return true;
-                }
-                inB = true;
-                e = eb;
-                g0 = 0;
-                kind = STEP_SEAL;
-                ent = grp;
-                return true;
-            }
-            if (R > 0 && e < ee) {
-                kind = STEP_B;
-                ent = e;
-                g = g0;
-                g0 += TG;
-                if (g0 >= m_off[e + 1] - m_off[e]) {
-                    g0 = 0;
-                    ++e;
-                }
-                return true;
-            }
-            open(grp + 1);
-        }
-    }
-};
 
 // Fused fill, run by ONE thread of CTA c (of G): each fill record is copied
 // in two parts, each split into G equal 16-byte-aligned shares (CTA c takes
@@ -451,10 +394,6 @@ struct Steps {
 // complete, then the async-proxy writes are ordered before a GPU-scope
 // release) the CTA counts itself: part 0 in the high half-word of cnt0[r],
 // part 1 in ready[r].  Every wait is bounded.
-struct FillParts {
-    unsigned long long off[2][2];  // [part][range] record offsets
-    unsigned long long len[2][2];  // [part][range] bytes (multiples of 16)
-};
 
 __device__ __noinline__ void fill_parts_tma(const uint8_t* host, uint8_t* pool, unsigned long long rb, int q,
                                             const int* fslot, const int* ffid, unsigned* ready, unsigned* cnt0,
@@ -464,13 +403,7 @@ __device__ __noinline__ void fill_parts_tma(const uint8_t* host, uint8_t* pool, 
     ft::mbar_fence_init();
     // CTA c's share [b0, b1) of part pt (offsets within the part's run)
     unsigned long long sb0[2], sb1[2];
-    for (int pt = 0; pt < 2; ++pt) {
-        const unsigned long long L = fp.len[pt][0] + fp.len[pt][1];
-        const unsigned long long per = ((L / 16 + G - 1) / G) * 16;
-        const unsigned long long b0 = per * (unsigned long long)c;
-        sb0[pt] = b0 < L ? b0 : L;
-        sb1[pt] = b0 + per < L ? b0 + per : L;
-    }
+    for (int pt = 0; pt < 2; ++pt) fill_share(fp.len[pt][0] + fp.len[pt][1], G, c, sb0[pt], sb1[pt]);
     struct Cur { int r, pt; unsigned long long o; };
     auto settle = [&](Cur& u) {  // onto a chunk, or r == q past the last
         while (u.r < q && u.o >= sb1[u.pt]) {
@@ -483,11 +416,7 @@ __device__ __noinline__ void fill_parts_tma(const uint8_t* host, uint8_t* pool, 
     };
     // the chunk at u: record offset and bytes (not crossing the part's range boundary)
     auto chunk = [&](const Cur& u, unsigned long long& at, unsigned& n) {
-        const unsigned long long la = fp.len[u.pt][0];
-        unsigned long long end = sb1[u.pt];
-        if (u.o < la && la < end) end = la;
-        n = (unsigned)(end - u.o < fch ? end - u.o : fch);
-        at = u.o < la ? fp.off[u.pt][0] + u.o : fp.off[u.pt][1] + (u.o - la);
+        n = fill_chunk(fp, u.pt, u.o, sb1[u.pt], fch, at);
     };
     auto advance = [&](Cur& u) {
         unsigned long long at;
@@ -621,15 +550,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
     // consumers stage the worklist and x meanwhile (named barrier 4).
     if (wid > CW) {
         if (lane == 0 && q > 0) {
-            FillParts fp;
-            fp.off[0][0] = 0;
-            fp.len[0][0] = VGU;                            // W_gu values
-            fp.off[0][1] = VGU + VD;
-            fp.len[0][1] = SGU;                            // W_gu scales
-            fp.off[1][0] = VGU;
-            fp.len[1][0] = VD;                             // W_d values
-            fp.off[1][1] = VGU + VD + SGU;
-            fp.len[1][1] = p.rb - (VGU + VD + SGU);        // W_d scales
+            const FillParts fp = fp4_fill_parts(H, F, SB);
             fill_parts_tma(reinterpret_cast<const uint8_t*>(p.host_pool), const_cast<uint8_t*>(p.slot_pool), p.rb,
                            q, p.fill_slot, p.fill_fid, p.ready, p.wdc, c, G, fp, ring + (size_t)nst * slot_bytes,
                            reinterpret_cast<uint64_t*>(smem + 128), p.fill_chunk, p.fill_slots, p.err);
