@@ -59,17 +59,6 @@ using namespace fp4sched;
 
 namespace {
 
-constexpr int CW = 16;                // consumer warps
-constexpr int CONS = CW * 32;
-constexpr int FILL_WARPS = 1;         // fused cache fill (one TMA thread)
-constexpr int THREADS = CONS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
-constexpr int FPC = CW;               // features per phase-A chunk: one per consumer warp
-constexpr int RW = 2;                 // W_d rows per warp pass in phase B
-constexpr size_t HEAD = 256;
-// Phase-A activations: f16 pairs in shared memory (X_SMEM, when T*H*2 bytes
-// fit) or in a global scratch row block written at the start of the launch
-// (X_GLOBAL).
-enum { X_SMEM = 0, X_GLOBAL = 1 };
 constexpr int kXTarget = 9;  // token rows are scaled so their largest magnitude is in [2^9, 2^10)
 
 // Scale bytes: two e4m3 codes (low byte first) to a float pair, by the
@@ -830,49 +819,6 @@ __global__ void __launch_bounds__(THREADS, 1) expert_ffn_fp4_kernel(ExpertParams
         p.y[oi] = acc;
     }
     if (tid == 0) count_out();  // after this CTA's last seal
-}
-
-}  // namespace
-
-static constexpr size_t kSmemLimit4 = 227 * 1024 - 256;  // dynamic; the rest is static shared memory
-
-namespace {
-
-// Shared-memory plan of one FP4 launch (T tokens), or false when no plan fits.
-struct Fp4Plan {
-    int xm, tg, nst, nf;
-    size_t head, slot, fch;
-};
-
-bool fp4_plan(int H, int F, int T, int k, int SB, int G, Fp4Plan& pl) {
-    const int RMAX = (H + G - 1) / G;
-    const size_t TK = (size_t)T * k;
-    pl.xm = (size_t)T * H * 2 <= 32768 ? X_SMEM : X_GLOBAL;
-    const size_t xbytes = pl.xm == X_SMEM ? (size_t)T * H * 2 : 0;
-    const size_t head0 = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127);
-    const size_t chunk = (size_t)2 * FPC * (H / 2 + H / SB);
-    const size_t wpart = ((size_t)RMAX * (F / 2 + F / SB) + 127) & ~(size_t)127;
-    // The fill ring is kept small (3 x 4 KiB per SM): host reads queued beyond
-    // the link's bandwidth-delay product delay every SM's HBM reads.
-    pl.fch = 4096;
-    // token group of phase B: the most h rows (at most 16) whose staging in a
-    // slot (fp32 as copied, then f16 pairs and their block factors) leaves room
-    // for two slots
-    int tg = T < 16 ? T : 16;
-    for (; tg >= 1; --tg) {
-        pl.head = head0 + (((6 * TK + 1 + (size_t)T) * 4 + 127) & ~(size_t)127);
-        pl.slot = wpart + (size_t)tg * F * 6 + (size_t)tg * (F / 16) * 4;
-        if (pl.slot < chunk) pl.slot = chunk;
-        pl.slot = (pl.slot + 127) & ~(size_t)127;
-        if (pl.head + 2 * pl.fch + 2 * pl.slot <= kSmemLimit4) break;
-    }
-    if (tg < 1) return false;
-    pl.tg = tg;
-    pl.nst = (int)((kSmemLimit4 - pl.head - 2 * pl.fch) / pl.slot);
-    if (pl.nst > 4) pl.nst = 4;
-    pl.nf = (int)((kSmemLimit4 - pl.head - pl.slot * pl.nst) / pl.fch);
-    if (pl.nf > 3) pl.nf = 3;
-    return true;
 }
 
 }  // namespace

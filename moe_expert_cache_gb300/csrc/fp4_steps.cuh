@@ -4,12 +4,76 @@
 // intrinsics so that a host compiler can build it for the schedule tests.
 #pragma once
 
+#include <cstddef>
+
 #ifndef __CUDACC__
 #define __host__
 #define __device__
 #endif
 
 namespace fp4sched {
+
+// Launch layout of the kernel.
+constexpr int CW = 16;                // consumer warps
+constexpr int CONS = CW * 32;
+constexpr int FILL_WARPS = 1;         // fused cache fill (one TMA thread)
+constexpr int THREADS = CONS + 32 + FILL_WARPS * 32;  // + producer warp + fill warps
+constexpr int FPC = CW;               // features per phase-A chunk: one per consumer warp
+constexpr int RW = 2;                 // W_d rows per warp pass in phase B
+constexpr size_t HEAD = 256;          // ring barriers (and the fill ring's) at the start of shared memory
+// Phase-A activations: f16 pairs in shared memory (X_SMEM) or in a global
+// scratch row block written at the start of the launch (X_GLOBAL).
+enum { X_SMEM = 0, X_GLOBAL = 1 };
+constexpr size_t kSmemLimit4 = 227 * 1024 - 256;  // dynamic shared memory; the rest is static
+
+// Shared-memory plan of one launch of T tokens: where x lives, the phase-B
+// token group, ring slots and their bytes, fill ring chunks and their bytes,
+// and the bytes ahead of the ring.
+struct Fp4Plan {
+    int xm, tg, nst, nf;
+    size_t head, slot, fch;
+};
+
+// The plan with x placed as xm, or false when two ring slots do not fit.
+inline bool fp4_plan_x(int H, int F, int T, int k, int SB, int G, int xm, Fp4Plan& pl) {
+    const int RMAX = (H + G - 1) / G;
+    const size_t TK = (size_t)T * k;
+    pl.xm = xm;
+    const size_t xbytes = pl.xm == X_SMEM ? (size_t)T * H * 2 : 0;
+    const size_t head0 = HEAD + ((xbytes + 127) & ~(size_t)127) + ((TK * RMAX * 4 + 127) & ~(size_t)127);
+    const size_t chunk = (size_t)2 * FPC * (H / 2 + H / SB);
+    const size_t wpart = ((size_t)RMAX * (F / 2 + F / SB) + 127) & ~(size_t)127;
+    // The fill ring is kept small (3 x 4 KiB per SM): host reads queued beyond
+    // the link's bandwidth-delay product delay every SM's HBM reads.
+    pl.fch = 4096;
+    // token group of phase B: the most h rows (at most 16) whose staging in a
+    // slot (fp32 as copied, then f16 pairs and their block factors) leaves room
+    // for two slots
+    int tg = T < 16 ? T : 16;
+    for (; tg >= 1; --tg) {
+        pl.head = head0 + (((6 * TK + 1 + (size_t)T) * 4 + 127) & ~(size_t)127);
+        pl.slot = wpart + (size_t)tg * F * 6 + (size_t)tg * (F / 16) * 4;
+        if (pl.slot < chunk) pl.slot = chunk;
+        pl.slot = (pl.slot + 127) & ~(size_t)127;
+        if (pl.head + 2 * pl.fch + 2 * pl.slot <= kSmemLimit4) break;
+    }
+    if (tg < 1) return false;
+    pl.tg = tg;
+    pl.nst = (int)((kSmemLimit4 - pl.head - 2 * pl.fch) / pl.slot);
+    if (pl.nst > 4) pl.nst = 4;
+    pl.nf = (int)((kSmemLimit4 - pl.head - pl.slot * pl.nst) / pl.fch);
+    if (pl.nf > 3) pl.nf = 3;
+    return true;
+}
+
+// x in shared memory when T*H*2 bytes fit there (at most 32 KiB) and still
+// leave room for two slots; else x in the global block (always allocated for
+// FP4 contexts), whose plan only shrinks as T falls, so a context whose T_max
+// has a plan has one for every T up to it.
+inline bool fp4_plan(int H, int F, int T, int k, int SB, int G, Fp4Plan& pl) {
+    if ((size_t)T * H * 2 <= 32768 && fp4_plan_x(H, F, T, k, SB, G, X_SMEM, pl)) return true;
+    return fp4_plan_x(H, F, T, k, SB, G, X_GLOBAL, pl);
+}
 
 // The steps of CTA c, in the order its producer issues them and its
 // consumers take them: the phase-A items of the resident entries (a = c,

@@ -233,8 +233,9 @@ ft_status ft_layer_init(ft_ctx** out, int32_t L, int32_t E, int32_t k, int32_t H
     INIT_CUDA(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
     if (fmt == FT_FMT_FP8 && (size_t)T_max * k * ((H + c->num_sms - 1) / c->num_sms) * 4 > 227 * 1024)
         return fail(FT_ERR_ARG);  // the down kernel keeps [assignment, rows] in shared memory
-    if ((fmt == FT_FMT_NVFP4 || fmt == FT_FMT_MXFP4) && !expert_ffn_fp4_fits(H, F, T_max, k, fmt, c->num_sms))
-        return fail(FT_ERR_ARG);  // the FP4 decode kernel has no shared-memory plan for T_max tokens
+    if (fmt == FT_FMT_NVFP4 || fmt == FT_FMT_MXFP4)
+        for (int t = 1; t <= T_max; ++t)  // the FP4 decode kernel needs a shared-memory plan for every T
+            if (!expert_ffn_fp4_fits(H, F, t, k, fmt, c->num_sms)) return fail(FT_ERR_ARG);
     if (fmt == FT_FMT_BF16)
         for (int t = 1; t <= T_max; ++t)  // the x staging format switches with T: check every T
             if (!expert_ffn_fits(H, F, t, k, c->num_sms)) return fail(FT_ERR_ARG);

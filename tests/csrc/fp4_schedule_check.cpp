@@ -8,7 +8,14 @@
 //     waits until every CTA has sealed its group) runs to completion;
 //   * fill shares: the chunks of all CTAs' shares of both parts tile the
 //     record exactly once, each 16-byte aligned, non-empty, at most the
-//     chunk size and inside one range of its part.
+//     chunk size and inside one range of its part;
+//   * shared-memory plans, over every shape the FP4 formats accept (H, F up
+//     to 8192), k up to 16 and T up to 256: each plan fits the dynamic
+//     shared-memory limit with two ring slots and two fill chunks at least,
+//     a slot holds a phase-A item and a phase-B item with its converted tail,
+//     the head holds x (when in shared memory), the per-route outputs and the
+//     worklist, and every T below a T that has a plan has one too (contexts
+//     are accepted by their T_max).
 // Exits 0 and prints "ok", or prints the first failure and exits 1.
 #include "fp4_steps.cuh"
 
@@ -141,9 +148,43 @@ void check_fill(int H, int F, int SB, int G, unsigned fch) {
     if (p != rb) fail("record size", (long long)p, (long long)rb);
 }
 
+void check_plans(int SB, int G) {
+    for (int H = 256; H <= 8192; H += 256)
+        for (int F = SB == 16 ? 256 : 512; F <= 8192; F += SB == 16 ? 256 : 512)
+            for (int k : {1, 2, 4, 8, 16}) {
+                bool gap = false;  // some T has had no plan
+                for (int T = 1; T <= 256 && T * k <= 4096; ++T) {
+                    Fp4Plan pl;
+                    if (!fp4_plan(H, F, T, k, SB, G, pl)) {
+                        gap = true;
+                        continue;
+                    }
+                    if (gap) fail("plan after a T without one", H * 100000 + F, T);
+                    const size_t RMAX = (size_t)(H + G - 1) / G, TK = (size_t)T * k;
+                    auto r128 = [](size_t v) { return (v + 127) & ~(size_t)127; };
+                    const size_t need_head = HEAD + (pl.xm == X_SMEM ? r128((size_t)T * H * 2) : 0) +
+                                             r128(TK * RMAX * 4) + r128((6 * TK + 1 + T) * 4);
+                    const size_t wpart = r128(RMAX * (F / 2 + F / SB));
+                    const size_t need_b = wpart + (size_t)pl.tg * F * 4 + (size_t)pl.tg * F * 2 +
+                                          (size_t)pl.tg * (F / 16) * 4;
+                    const size_t need_a = (size_t)2 * FPC * (H / 2 + H / SB);
+                    if (pl.head + (size_t)pl.nst * pl.slot + (size_t)pl.nf * pl.fch > kSmemLimit4)
+                        fail("plan exceeds shared memory", H * 100000 + F, T);
+                    if (pl.nst < 2 || pl.nf < 2) fail("ring depth", pl.nst, pl.nf);
+                    if (pl.slot < need_a || pl.slot < need_b) fail("slot too small", (long long)pl.slot, T);
+                    if (pl.head < need_head) fail("head too small", (long long)pl.head, T);
+                    if (pl.head % 128 || pl.slot % 128) fail("alignment", (long long)pl.head, (long long)pl.slot);
+                    if (pl.tg < 1 || pl.tg > (T < 16 ? T : 16)) fail("token group", pl.tg, T);
+                    if (pl.xm == X_SMEM && (size_t)T * H * 2 > 32768) fail("x in shared memory", H, T);
+                }
+            }
+}
+
 }  // namespace
 
 int main() {
+    for (int SB : {16, 32})
+        for (int G : {152, 148}) check_plans(SB, G);
     // fill shares: NVFP4 (SB 16) and MXFP4 (SB 32) shapes the kernel accepts
     const int shapes[][3] = {{4096, 2048, 16}, {4096, 2048, 32}, {256, 256, 16}, {256, 512, 32},
                              {1024, 512, 16}, {2048, 768 + 256, 16}};
